@@ -1,0 +1,379 @@
+/*
+ * moe_oracle.c - plain, slow fp64 CPU oracle of the routed mixture-of-experts
+ * feed-forward layer, including the multi-micro-shard variant.
+ *
+ * TEST INFRASTRUCTURE ONLY. This file is loaded by the tests, by the smoke
+ * check and by the benchmark's CPU-baseline leg, and by nothing else. It shares
+ * no code, header, table or helper with the CUDA path; the two meet only in the
+ * seeded input generator, which holds none of the layer's arithmetic.
+ *
+ * What it computes, and where the pages define it:
+ *   - "HunyuanImage3 Hybrid Parallelism" (LightX2V blog), section 5: the
+ *     micro-major MoE pack, W1[micro][expert][2I][H] and W2[micro][expert][H][I];
+ *     section 4.4: each micro's fused gate/up block is [gate_micro; up_micro];
+ *     section 6.1: router ids and scores of shape [num_tokens, top_k], route
+ *     sort by expert giving permuted_to_expanded, bincount+cumsum offsets, one
+ *     gather of the input, per micro grouped GEMM1 -> SwiGLU -> grouped GEMM2,
+ *     inverse permutation, and the finalize
+ *         output[token] = sum over routes of scale[token, route] *
+ *                         (micro0_partial + micro1_partial).
+ *   - CANN/Ascend Hunyuan Image 3.0 guide, section 2.2: the expert is
+ *     down(SiLU(gate(x)) * up(x)) with w13 = concat(gate, up) and the fused
+ *     activation SiLU(x[0]) * x[1]; section 3.1: a shared expert beside the
+ *     routed ones; section 5.2: the gate (router) is computed in fp32.
+ *
+ * Readings taken where the pages are silent (each is listed in the design notes):
+ *   - gate = softmax over all experts, then the top-k, then the k weights are
+ *     renormalised to sum to one;
+ *   - the top-k decision is taken on fp32 logits (the gate's precision in the
+ *     Ascend guide, section 5.2): each logit is formed in fp64 from the exact
+ *     input values and rounded once to fp32; ties go to the lower expert index
+ *     and the k slots are ordered by descending logit, ties by lower index;
+ *   - the route sort is stable in the flattened route index r = t*k + j;
+ *   - offsets has E+1 entries, offsets[E] = T*k;
+ *   - the shared expert's output is added unscaled.
+ *
+ * All floating-point arithmetic is fp64. Inputs are read as fp32 or as bf16 bit
+ * patterns (uint16) and widened exactly to fp64.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_F32 0
+#define ORC_BF16 1
+
+/* Exact widening of one stored element to fp64. */
+static double elem(const void *p, int dtype, int64_t i)
+{
+    if (dtype == ORC_F32)
+        return (double)((const float *)p)[i];
+    uint32_t bits = (uint32_t)((const uint16_t *)p)[i] << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+static size_t elem_size(int dtype) { return dtype == ORC_F32 ? 4u : 2u; }
+
+/* Pointer to element i of a typed buffer (used to address expert blocks). */
+static const void *elem_ptr(const void *p, int dtype, int64_t i)
+{
+    return (const char *)p + (size_t)i * elem_size(dtype);
+}
+
+static double silu(double z) { return z / (1.0 + exp(-z)); }
+
+static int max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+static int thread_id(void)
+{
+#ifdef _OPENMP
+    return omp_get_thread_num();
+#else
+    return 0;
+#endif
+}
+
+/*
+ * Router logits (blog section 6.1, "the router produces ... routing scores";
+ * Ascend guide section 5.2, gate linear):
+ *     logits[t][e] = sum_h x[t][h] * Wr[e][h]  (+ bias[e])
+ * x is [T][H], Wr is [E][H], bias is fp32 [E] or NULL. Output fp64 [T][E].
+ */
+int orc_logits(const void *x, const void *wr, int dtype, const float *bias,
+               int64_t T, int64_t H, int64_t E, double *logits)
+{
+    if (T < 0 || H <= 0 || E <= 0)
+        return -1;
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t e = 0; e < E; ++e) {
+            double s = 0.0;
+            for (int64_t h = 0; h < H; ++h)
+                s += elem(x, dtype, t * H + h) * elem(wr, dtype, e * H + h);
+            if (bias)
+                s += (double)bias[e];
+            logits[t * E + e] = s;
+        }
+    }
+    return 0;
+}
+
+/*
+ * Softmax gate, top-k and renormalisation (blog section 6.1: ids and scores of
+ * shape [num_tokens, top_k]; Ascend guide section 2.3: GatingTopK).
+ *   1. l[e] = fp32 rounding of logits[t][e]   (gate precision)
+ *   2. p = softmax(l) over all E experts     (row max subtracted)
+ *   3. k rounds: take the not-yet-taken expert with the largest l;
+ *      on equal l the lower index wins (strict '>' while scanning upward)
+ *   4. w_j = p[id_j] / sum_j' p[id_j']
+ * ids [T][k] int32, w [T][k] fp64; probs [T][E] (the full softmax) if non-NULL.
+ */
+int orc_route(const double *logits, int64_t T, int64_t E, int64_t k,
+              int32_t *ids, double *w, double *probs)
+{
+    if (T < 0 || E <= 0 || k <= 0 || k > E)
+        return -1;
+    int nt = max_threads();
+    double *lbuf = (double *)malloc(sizeof(double) * (size_t)(E * nt));
+    double *pbuf = (double *)malloc(sizeof(double) * (size_t)(E * nt));
+    char *tbuf = (char *)malloc((size_t)(E * nt));
+    if (!lbuf || !pbuf || !tbuf) {
+        free(lbuf);
+        free(pbuf);
+        free(tbuf);
+        return -2;
+    }
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        double *l = lbuf + (int64_t)thread_id() * E;
+        double *p = pbuf + (int64_t)thread_id() * E;
+        char *taken = tbuf + (int64_t)thread_id() * E;
+        double mx = -INFINITY;
+        for (int64_t e = 0; e < E; ++e) {
+            l[e] = (double)(float)logits[t * E + e];
+            if (l[e] > mx)
+                mx = l[e];
+        }
+        double z = 0.0;
+        for (int64_t e = 0; e < E; ++e) {
+            p[e] = exp(l[e] - mx);
+            z += p[e];
+        }
+        for (int64_t e = 0; e < E; ++e) {
+            p[e] /= z;
+            if (probs)
+                probs[t * E + e] = p[e];
+            taken[e] = 0;
+        }
+        double sel = 0.0;
+        for (int64_t j = 0; j < k; ++j) {
+            int64_t best = -1;
+            for (int64_t e = 0; e < E; ++e)
+                if (!taken[e] && (best < 0 || l[e] > l[best]))
+                    best = e;
+            taken[best] = 1;
+            ids[t * k + j] = (int32_t)best;
+            sel += p[best];
+        }
+        for (int64_t j = 0; j < k; ++j)
+            w[t * k + j] = p[ids[t * k + j]] / sel;
+    }
+    free(lbuf);
+    free(pbuf);
+    free(tbuf);
+    return 0;
+}
+
+/*
+ * Route sort and expert offsets (blog section 6.1: flatten the ids, sort them
+ * by expert -> permuted_to_expanded; bincount(...).cumsum(...) -> offsets;
+ * section 6.2: permutation inverse).
+ *   counts[e]   = number of routes r = t*k+j with ids[r] == e
+ *   offsets[0]  = 0, offsets[e+1] = offsets[e] + counts[e]
+ *   perm        = stable counting sort of r by ids[r] (r ascending inside an expert)
+ *   inv[perm[i]] = i
+ * Returns -1 if an id is out of [0, E).
+ */
+int orc_permute(const int32_t *ids, int64_t T, int64_t k, int64_t E,
+                int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv)
+{
+    int64_t R = T * k;
+    for (int64_t e = 0; e < E; ++e)
+        counts[e] = 0;
+    for (int64_t r = 0; r < R; ++r) {
+        if (ids[r] < 0 || ids[r] >= E)
+            return -1;
+        counts[ids[r]] += 1;
+    }
+    offsets[0] = 0;
+    for (int64_t e = 0; e < E; ++e)
+        offsets[e + 1] = offsets[e] + counts[e];
+    int32_t *fill = (int32_t *)malloc(sizeof(int32_t) * (size_t)(E > 0 ? E : 1));
+    if (!fill)
+        return -2;
+    for (int64_t e = 0; e < E; ++e)
+        fill[e] = offsets[e];
+    for (int64_t r = 0; r < R; ++r)
+        perm[fill[ids[r]]++] = (int32_t)r;
+    for (int64_t i = 0; i < R; ++i)
+        inv[perm[i]] = (int32_t)i;
+    free(fill);
+    return 0;
+}
+
+/*
+ * One SwiGLU expert applied to one row, accumulated with a scale
+ * (Ascend guide section 2.2: down(SiLU(gate(x)) * up(x)); blog section 4.4:
+ * a micro's w13 block is [gate rows (I); up rows (I)]):
+ *     g_i = sum_h w13[i][h]   * x[h]        i in [0, I)
+ *     u_i = sum_h w13[I+i][h] * x[h]
+ *     a_i = silu(g_i) * u_i,   silu(z) = z / (1 + exp(-z))
+ *     acc[h] += scale * sum_i w2[h][i] * a_i
+ * w13 is [2I][H], w2 is [H][I]; a is caller scratch of length I.
+ */
+static void swiglu_expert_acc(const double *xv, int64_t H, int64_t I,
+                              const void *w13, const void *w2, int dtype,
+                              double scale, double *acc, double *a)
+{
+    for (int64_t i = 0; i < I; ++i) {
+        double g = 0.0, u = 0.0;
+        for (int64_t h = 0; h < H; ++h) {
+            g += elem(w13, dtype, i * H + h) * xv[h];
+            u += elem(w13, dtype, (I + i) * H + h) * xv[h];
+        }
+        a[i] = silu(g) * u;
+    }
+    for (int64_t h = 0; h < H; ++h) {
+        double s = 0.0;
+        for (int64_t i = 0; i < I; ++i)
+            s += elem(w2, dtype, h * I + i) * a[i];
+        acc[h] += scale * s;
+    }
+}
+
+/*
+ * The layer's plain per-token definition, evaluated on a list of tokens:
+ *     y[t] = sum_j w[t][j] * sum_m FFN_{m, ids[t][j]}(x[t])  (+ FFN_shared(x[t]))
+ * where FFN_{m,e} is the SwiGLU expert built from micro m's blocks of expert e:
+ * w13[m] + e*2I*H and w2[m] + e*H*I (blog section 5, micro-major pack).
+ * The shared expert (Ascend guide section 3.1) is the same SwiGLU form with
+ * intermediate size Is, sw13 [2Is][H] and sw2 [H][Is]; pass NULL for none.
+ * ids/w are the routing of ALL tokens ([T][k]); tokens[] selects which rows to
+ * evaluate; y is [n_tokens][H].
+ */
+int orc_forward_tokens(const void *x, int dtype, int64_t H, int64_t E, int64_t k,
+                       int64_t I, int64_t n_micro,
+                       const void *const *w13, const void *const *w2,
+                       const void *sw13, const void *sw2, int64_t Is,
+                       const int32_t *ids, const double *w,
+                       const int64_t *tokens, int64_t n_tokens, double *y)
+{
+    if (H <= 0 || E <= 0 || k <= 0 || I <= 0 || n_micro <= 0 || n_tokens < 0)
+        return -1;
+    int nt = max_threads();
+    int64_t scratch = I > Is ? I : Is;
+    double *xbuf = (double *)malloc(sizeof(double) * (size_t)(H * nt));
+    double *abuf = (double *)malloc(sizeof(double) * (size_t)(scratch * nt));
+    if (!xbuf || !abuf) {
+        free(xbuf);
+        free(abuf);
+        return -2;
+    }
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t n = 0; n < n_tokens; ++n) {
+        double *xv = xbuf + (int64_t)thread_id() * H;
+        double *a = abuf + (int64_t)thread_id() * scratch;
+        int64_t t = tokens[n];
+        double *acc = y + n * H;
+        for (int64_t h = 0; h < H; ++h) {
+            xv[h] = elem(x, dtype, t * H + h);
+            acc[h] = 0.0;
+        }
+        for (int64_t j = 0; j < k; ++j) {
+            int64_t e = ids[t * k + j];
+            for (int64_t m = 0; m < n_micro; ++m)
+                swiglu_expert_acc(xv, H, I,
+                                  elem_ptr(w13[m], dtype, e * 2 * I * H),
+                                  elem_ptr(w2[m], dtype, e * H * I),
+                                  dtype, w[t * k + j], acc, a);
+        }
+        if (sw13 && sw2 && Is > 0)
+            swiglu_expert_acc(xv, H, Is, sw13, sw2, dtype, 1.0, acc, a);
+    }
+    free(xbuf);
+    free(abuf);
+    return 0;
+}
+
+/*
+ * The same layer evaluated the way the multi-micro method organises it
+ * (blog section 6.1), for cross-checking the permutation and the finalize:
+ *   xp[i]   = x[perm[i] / k]                    one gather, shared by all micros
+ *   o[i]    = sum_m FFN_{m,e}(xp[i])            e = the expert whose segment
+ *                                               [offsets[e], offsets[e+1]) holds i
+ *   y[t]    = sum_j w[t][j] * o[inv[t*k + j]]   (+ FFN_shared(x[t]))
+ * y is [T][H]. Memory: R*H*2 doubles, so small shapes only.
+ */
+int orc_forward_permuted(const void *x, int dtype, int64_t T, int64_t H, int64_t E,
+                         int64_t k, int64_t I, int64_t n_micro,
+                         const void *const *w13, const void *const *w2,
+                         const void *sw13, const void *sw2, int64_t Is,
+                         const double *w, const int32_t *offsets,
+                         const int32_t *perm, const int32_t *inv, double *y)
+{
+    int64_t R = T * k;
+    if (T < 0 || H <= 0 || E <= 0 || k <= 0 || I <= 0 || n_micro <= 0)
+        return -1;
+    if (offsets[0] != 0 || offsets[E] != R)
+        return -1;
+    int nt = max_threads();
+    int64_t scratch = I > Is ? I : Is;
+    double *xp = (double *)malloc(sizeof(double) * (size_t)(R > 0 ? R * H : 1));
+    double *o = (double *)calloc((size_t)(R > 0 ? R * H : 1), sizeof(double));
+    double *xbuf = (double *)malloc(sizeof(double) * (size_t)(H * nt));
+    double *abuf = (double *)malloc(sizeof(double) * (size_t)(scratch * nt));
+    int rc = 0;
+    if (!xp || !o || !xbuf || !abuf) {
+        rc = -2;
+        goto done;
+    }
+    /* one gather, shared by every micro */
+    for (int64_t i = 0; i < R; ++i) {
+        int64_t t = perm[i] / k;
+        for (int64_t h = 0; h < H; ++h)
+            xp[i * H + h] = elem(x, dtype, t * H + h);
+    }
+    /* grouped GEMM1 -> SwiGLU -> grouped GEMM2, summed over micros, per segment */
+    for (int64_t e = 0; e < E; ++e) {
+#pragma omp parallel for schedule(dynamic, 1)
+        for (int64_t i = offsets[e]; i < offsets[e + 1]; ++i) {
+            double *a = abuf + (int64_t)thread_id() * scratch;
+            for (int64_t m = 0; m < n_micro; ++m)
+                swiglu_expert_acc(xp + i * H, H, I,
+                                  elem_ptr(w13[m], dtype, e * 2 * I * H),
+                                  elem_ptr(w2[m], dtype, e * H * I),
+                                  dtype, 1.0, o + i * H, a);
+        }
+    }
+    /* finalize: routing scale applied once, top-k reduced once */
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        double *xv = xbuf + (int64_t)thread_id() * H;
+        double *a = abuf + (int64_t)thread_id() * scratch;
+        double *acc = y + t * H;
+        for (int64_t h = 0; h < H; ++h)
+            acc[h] = 0.0;
+        for (int64_t j = 0; j < k; ++j) {
+            const double *row = o + (int64_t)inv[t * k + j] * H;
+            for (int64_t h = 0; h < H; ++h)
+                acc[h] += w[t * k + j] * row[h];
+        }
+        if (sw13 && sw2 && Is > 0) {
+            for (int64_t h = 0; h < H; ++h)
+                xv[h] = elem(x, dtype, t * H + h);
+            swiglu_expert_acc(xv, H, Is, sw13, sw2, dtype, 1.0, acc, a);
+        }
+    }
+done:
+    free(xp);
+    free(o);
+    free(xbuf);
+    free(abuf);
+    return rc;
+}
+
+/* Number of OpenMP threads the oracle uses (reported beside its timings). */
+int orc_num_threads(void) { return max_threads(); }

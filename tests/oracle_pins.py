@@ -1,0 +1,282 @@
+"""Checks that pin the fp64 oracle to something other than itself.
+
+Each ``pin_*`` function takes an oracle library handle (``None`` = the real
+oracle; the mutation test passes builds of the oracle with a planted mistake)
+and raises ``AssertionError`` when the oracle disagrees with what the pages or
+the mathematics fix:
+
+* hand-derived worked examples with closed-form values (``tests/golden``);
+* brute force over all k-subsets for the top-k selection;
+* library routines for special cases: ``scipy.special.softmax`` for k = E,
+  ``np.argsort(kind="stable")`` for the route sort, ``np.bincount`` +
+  ``np.cumsum`` for the offsets;
+* identities the pages state: concatenated micro-shards equal the unsharded
+  expert ("HunyuanImage3 Hybrid Parallelism" section 5), two single-micro
+  dispatches summed equal the multi-micro call (section 10.3), the
+  per-token definition equals the gather/segment/finalize organisation
+  (section 6.1);
+* invariants: Sum_j w = 1, distinct ids, bijective permutation.
+"""
+from __future__ import annotations
+
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import scipy.special
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _f32(a):
+    return np.asarray(a, dtype=np.float32)
+
+
+def _rel(a, b):
+    a, b = np.asarray(a, np.float64), np.asarray(b, np.float64)
+    den = max(np.abs(b).max(), 1e-300)
+    return float(np.abs(a - b).max() / den)
+
+
+# ---------------------------------------------------------------- routing pins
+def pin_routing_worked_example(lib=None):
+    g = _golden("routing_worked_example.json")
+    lg = oracle.logits(_f32(g["x"]), _f32(g["router_w"]), _f32(g["router_bias"]), lib=lib)
+    ids, w, probs = oracle.route(lg, g["k"], return_probs=True, lib=lib)
+    assert ids.tolist() == g["expect_ids"], (ids.tolist(), g["expect_ids"])
+    assert np.allclose(w, g["expect_w"], rtol=0, atol=1e-7), w
+    assert np.allclose(probs[2], g["expect_probs_token2"], rtol=0, atol=1e-7), probs[2]
+
+
+def pin_fp32_gate_decision(lib=None):
+    g = _golden("fp32_gate_decision.json")
+    lg = oracle.logits(_f32(g["x"]), _f32(g["router_w"]), lib=lib)
+    ids1, _ = oracle.route(lg, 1, lib=lib)
+    ids2, w2 = oracle.route(lg, 2, lib=lib)
+    assert ids1.tolist() == g["expect_ids_k1"], ids1
+    assert ids2.tolist() == g["expect_ids_k2"], ids2
+    assert np.allclose(w2, g["expect_w_k2"], rtol=0, atol=1e-12), w2
+
+
+def _brute_topk(l, k):
+    """The unique k-subset S with every member ranked above every non-member
+    under (larger logit, then lower index), listed in that rank order."""
+    E = len(l)
+    key = lambda e: (-l[e], e)  # noqa: E731
+    found = []
+    for S in itertools.combinations(range(E), k):
+        rest = [e for e in range(E) if e not in S]
+        if all(key(a) < key(b) for a in S for b in rest):
+            found.append(sorted(S, key=key))
+    assert len(found) == 1
+    return found[0]
+
+
+def pin_topk_brute_force(lib=None):
+    rng = np.random.default_rng(11)
+    for trial in range(60):
+        T = int(rng.integers(1, 7))
+        E = int(rng.integers(1, 7))
+        k = int(rng.integers(1, min(E, 3) + 1))
+        H = int(rng.integers(1, 5))
+        if trial % 2:  # integer grid: exact ties are common
+            x = _f32(rng.integers(-2, 3, (T, H)))
+            wr = _f32(rng.integers(-1, 2, (E, H)))
+        else:
+            x = _f32(rng.standard_normal((T, H)))
+            wr = _f32(rng.standard_normal((E, H)))
+        lg = oracle.logits(x, wr, lib=lib)
+        ids, w = oracle.route(lg, k, lib=lib)
+        lf = lg.astype(np.float32).astype(np.float64)
+        for t in range(T):
+            want = _brute_topk(lf[t], k)
+            assert ids[t].tolist() == want, (t, ids[t], want, lf[t])
+            # renormalised softmax of the chosen subset: k = 1 gives 1; a pair
+            # with logit gap d gives sigma(d) and 1 - sigma(d)
+            if k == 1:
+                assert abs(w[t, 0] - 1.0) < 1e-15
+            if k == 2:
+                d = lf[t, want[0]] - lf[t, want[1]]
+                assert abs(w[t, 0] - scipy.special.expit(d)) < 1e-12
+            assert abs(w[t].sum() - 1.0) < 1e-12
+
+
+def pin_k_equals_E_is_softmax(lib=None):
+    rng = np.random.default_rng(5)
+    x = _f32(rng.standard_normal((9, 7)))
+    wr = _f32(rng.standard_normal((5, 7)))
+    b = _f32(rng.standard_normal(5))
+    lg = oracle.logits(x, wr, b, lib=lib)
+    ids, w = oracle.route(lg, 5, lib=lib)
+    lf = lg.astype(np.float32).astype(np.float64)
+    ref = scipy.special.softmax(lf, axis=1)
+    got = np.zeros_like(ref)
+    for t in range(9):
+        got[t, ids[t]] = w[t]
+    assert _rel(got, ref) < 1e-12
+    # the logits themselves: a library matmul of the widened inputs plus bias
+    assert _rel(lg, x.astype(np.float64) @ wr.astype(np.float64).T + b) < 1e-12
+
+
+# ------------------------------------------------------------ permutation pins
+def pin_permutation_library(lib=None):
+    rng = np.random.default_rng(3)
+    for T, k, E in [(1, 1, 1), (7, 2, 5), (33, 8, 64), (100, 3, 4), (0, 2, 3)]:
+        ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32) \
+            if T else np.zeros((0, k), np.int32)
+        counts, offsets, perm, inv = oracle.permute(ids, E, lib=lib)
+        flat = ids.ravel()
+        assert counts.tolist() == np.bincount(flat, minlength=E).tolist()
+        assert offsets.tolist() == [0] + np.cumsum(np.bincount(flat, minlength=E)).tolist()
+        assert perm.tolist() == np.argsort(flat, kind="stable").tolist()
+        assert np.array_equal(inv[perm], np.arange(T * k))
+        assert sorted(perm.tolist()) == list(range(T * k))
+
+
+# -------------------------------------------------------------------- FFN pins
+def pin_swiglu_worked_example(lib=None):
+    g = _golden("swiglu_expert_worked_example.json")
+    x = _f32(g["x"])
+    ids = np.zeros((1, 1), np.int32)
+    w = np.ones((1, 1))
+    y = oracle.forward_tokens(x, ids, w, [_f32(g["w13"])], [_f32(g["w2"])], lib=lib)
+    assert _rel(y, g["expect_y"]) < 1e-12, y
+    ym = oracle.forward_tokens(x, ids, w, [_f32(a) for a in g["micro_w13"]],
+                               [_f32(a) for a in g["micro_w2"]], lib=lib)
+    assert _rel(ym, g["expect_y"]) < 1e-12, ym
+
+
+def pin_layer_worked_example(lib=None):
+    g = _golden("layer_worked_example.json")
+    out = oracle.layer(_f32(g["x"]), _f32(g["router_w"]), None, [_f32(g["w13"])],
+                       [_f32(g["w2"])], g["k"], lib=lib)
+    assert out["ids"].tolist() == g["expect_ids"], out["ids"]
+    assert _rel(out["y"], g["expect_y"]) < 1e-12, out["y"]
+    yp = oracle.forward_permuted(_f32(g["x"]), out["w"], out["offsets"], out["perm"],
+                                 out["inv"], [_f32(g["w13"])], [_f32(g["w2"])], lib=lib)
+    assert _rel(yp, g["expect_y"]) < 1e-12, yp
+
+
+def _rand_layer(rng, T, H, E, k, I, M, Is=0):
+    x = _f32(rng.standard_normal((T, H)))
+    wr = _f32(rng.standard_normal((E, H)) / math.sqrt(H))
+    w13 = [_f32(rng.standard_normal((E, 2 * I, H)) / math.sqrt(H)) for _ in range(M)]
+    w2 = [_f32(rng.standard_normal((E, H, I)) / math.sqrt(I)) for _ in range(M)]
+    sw13 = _f32(rng.standard_normal((2 * Is, H)) / math.sqrt(H)) if Is else None
+    sw2 = _f32(rng.standard_normal((H, Is)) / math.sqrt(Is)) if Is else None
+    return x, wr, w13, w2, sw13, sw2
+
+
+def pin_per_token_equals_permuted(lib=None):
+    rng = np.random.default_rng(21)
+    x, wr, w13, w2, sw13, sw2 = _rand_layer(rng, 23, 16, 6, 3, 8, 2, Is=12)
+    out = oracle.layer(x, wr, None, w13, w2, 3, sw13, sw2, lib=lib)
+    yp = oracle.forward_permuted(x, out["w"], out["offsets"], out["perm"], out["inv"],
+                                 w13, w2, sw13, sw2, lib=lib)
+    assert _rel(yp, out["y"]) < 1e-12
+
+
+def pin_micro_concat_identity(lib=None):
+    """Two micro-shards equal one unsharded expert with I_full = 2I (blog section 5:
+    the micro-major pack holds the expert's intermediate dimension split in two)."""
+    rng = np.random.default_rng(8)
+    T, H, E, k, I = 11, 12, 4, 2, 5
+    x, wr, w13, w2, _, _ = _rand_layer(rng, T, H, E, k, I, 2)
+    full13 = np.concatenate([w13[0][:, :I], w13[1][:, :I], w13[0][:, I:], w13[1][:, I:]], axis=1)
+    full2 = np.concatenate([w2[0], w2[1]], axis=2)
+    a = oracle.layer(x, wr, None, w13, w2, k, lib=lib)
+    b = oracle.layer(x, wr, None, [full13], [full2], k, lib=lib)
+    assert np.array_equal(a["ids"], b["ids"])
+    assert _rel(a["y"], b["y"]) < 1e-12
+
+
+def pin_two_dispatch_identity(lib=None):
+    """Summing two single-micro layer calls equals one multi-micro call (blog
+    section 10.3, the two-dispatch path adds the two outputs)."""
+    rng = np.random.default_rng(9)
+    x, wr, w13, w2, _, _ = _rand_layer(rng, 13, 10, 5, 2, 6, 2)
+    both = oracle.layer(x, wr, None, w13, w2, 2, lib=lib)["y"]
+    one = oracle.layer(x, wr, None, w13[:1], w2[:1], 2, lib=lib)["y"]
+    two = oracle.layer(x, wr, None, w13[1:], w2[1:], 2, lib=lib)["y"]
+    assert _rel(one + two, both) < 1e-12
+
+
+def pin_degenerate_experts(lib=None):
+    rng = np.random.default_rng(10)
+    T, H, E, k, I = 9, 8, 4, 2, 6
+    x, wr, w13, w2, _, _ = _rand_layer(rng, T, H, E, k, I, 1)
+    # gate rows zero -> silu(0) = 0 -> y = 0; up rows zero -> y = 0
+    for half in (slice(0, I), slice(I, 2 * I)):
+        z = w13[0].copy()
+        z[:, half] = 0
+        y = oracle.layer(x, wr, None, [z], w2, k, lib=lib)["y"]
+        assert np.abs(y).max() == 0.0
+    # every expert identical -> routing weights sum to one -> y = the single expert
+    same13 = np.repeat(w13[0][:1], E, axis=0)
+    same2 = np.repeat(w2[0][:1], E, axis=0)
+    y = oracle.layer(x, wr, None, [same13], [same2], k, lib=lib)["y"]
+    y1 = oracle.forward_tokens(x, np.zeros((T, 1), np.int32), np.ones((T, 1)),
+                               [same13], [same2], lib=lib)
+    assert _rel(y, y1) < 1e-12
+
+
+def pin_textbook_glu(lib=None):
+    """k = 1 and E = 1 reduce the layer to a two-layer GLU MLP, evaluated here
+    with library matmuls and scipy's logistic function."""
+    rng = np.random.default_rng(12)
+    T, H, I = 6, 10, 7
+    x, wr, w13, w2, _, _ = _rand_layer(rng, T, H, 1, 1, I, 1)
+    y = oracle.layer(x, wr, None, w13, w2, 1, lib=lib)["y"]
+    X = x.astype(np.float64)
+    G = w13[0][0, :I].astype(np.float64)
+    U = w13[0][0, I:].astype(np.float64)
+    D = w2[0][0].astype(np.float64)
+    gx = X @ G.T
+    ref = ((gx * scipy.special.expit(gx)) * (X @ U.T)) @ D.T
+    assert _rel(y, ref) < 1e-12
+
+
+def pin_shared_expert_added_unscaled(lib=None):
+    rng = np.random.default_rng(13)
+    T, H, E, k, I, Is = 8, 10, 4, 2, 5, 9
+    x, wr, w13, w2, sw13, sw2 = _rand_layer(rng, T, H, E, k, I, 1, Is)
+    with_s = oracle.layer(x, wr, None, w13, w2, k, sw13, sw2, lib=lib)["y"]
+    without = oracle.layer(x, wr, None, w13, w2, k, lib=lib)["y"]
+    X = x.astype(np.float64)
+    gx = X @ sw13[:Is].astype(np.float64).T
+    s = ((gx * scipy.special.expit(gx)) * (X @ sw13[Is:].astype(np.float64).T)) @ \
+        sw2.astype(np.float64).T
+    assert _rel(with_s - without, s) < 1e-10
+
+
+def pin_bf16_widening(lib=None):
+    """bf16 inputs are widened exactly: the same values given as fp32 and as
+    bf16 bit patterns produce identical results."""
+    rng = np.random.default_rng(14)
+    x, wr, w13, w2, _, _ = _rand_layer(rng, 5, 8, 3, 2, 4, 1)
+
+    def bits(a):
+        u = np.ascontiguousarray(a, np.float32).view(np.uint32)
+        return (u >> 16).astype(np.uint16)
+
+    def back(b):
+        return (b.astype(np.uint32) << 16).view(np.float32)
+
+    xb, wrb = bits(x), bits(wr)
+    w13b, w2b = [bits(w13[0])], [bits(w2[0])]
+    a = oracle.layer(xb, wrb, None, w13b, w2b, 2, lib=lib)
+    b = oracle.layer(back(xb), back(wrb), None, [back(w13b[0])], [back(w2b[0])], 2, lib=lib)
+    assert np.array_equal(a["ids"], b["ids"])
+    assert np.array_equal(a["y"], b["y"])
+
+
+ALL_PINS = [v for k_, v in sorted(globals().items()) if k_.startswith("pin_")]
