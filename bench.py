@@ -1,0 +1,362 @@
+#!/usr/bin/env python
+"""Throughput of the routed MoE layer on one or more GB300s (one replica per GPU).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one call of the whole layer (router, scan, placement, gather,
+GEMM1+SwiGLU, GEMM2, shared expert if any, finalize) on one batch of seeded
+synthetic tokens whose inputs are already in HBM. The default workload is the
+AR-decode-shaped layer (8 tokens, H=4096, 64 experts, top-8, I=768). Between
+steps the token batch rotates through a pool, so each step routes to a
+different expert set; the expert weights (1.2 GB) are larger than L2.
+
+Prints one JSON line on rank 0. ``--impl reference`` times the fp64 CPU oracle
+on the host cores instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from mixture_experts_layer_warp_gb300 import binding  # noqa: E402
+from mixture_experts_layer_warp_gb300 import workloads as W  # noqa: E402
+
+METRIC = "MoE-layer tokens/s on 1 GB300; % of binding roof (bf16 TC peak or HBM)"
+POOL = 8  # distinct token batches rotated through the timed steps
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm=p["hbm_gbs"], bf16=p["bf16_tflops"], bf16_sustained=p["bf16_tflops_sustained"],
+                    source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.path is None:
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]), "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(float(r[3]) for r in rows if r[3] not in ("", "[N/A]"))}
+
+
+# ---------------------------------------------------------------- helpers
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def src_sha(*names) -> str:
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "mixture_experts_layer_warp_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, kernel: str, sha: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if the
+    kernel source has not changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 4 and parts[0] == workload and parts[1] == kernel and parts[2] == sha:
+                return float(parts[3])
+    return None
+
+
+def oracle_tokens_per_s(wl, host_pool, weights, budget_s: float, min_calls: int = 1):
+    """The fp64 oracle on the host cores: whole-layer calls on sample batches."""
+    import oracle
+    n_tok, calls = 0, 0
+    t0 = time.perf_counter()
+    while calls < min_calls or time.perf_counter() - t0 < budget_s:
+        x = host_pool[calls % len(host_pool)]
+        oracle.layer(x, weights["router_w"], weights["router_bias"], weights["w13"], weights["w2"], wl.k,
+                     weights["shared_w13"], weights["shared_w2"])
+        n_tok += x.shape[0]
+        calls += 1
+    dt = time.perf_counter() - t0
+    return n_tok / dt, calls, dt, oracle.num_threads()
+
+
+def host_weights(inp):
+    out = {}
+    for k in ("router_w", "shared_w13", "shared_w2"):
+        out[k] = W.to_numpy(inp[k]) if inp[k] is not None else None
+    out["router_bias"] = None if inp["router_bias"] is None else inp["router_bias"].cpu().numpy()
+    out["w13"] = [W.to_numpy(t) for t in inp["w13"]]
+    out["w2"] = [W.to_numpy(t) for t in inp["w2"]]
+    return out
+
+
+def sample_tokens(wl) -> int:
+    """Tokens per oracle sample call: whole batch when small, else a slice
+    sized to a few seconds of fp64 work."""
+    per_token = 6 * wl.k * wl.H * wl.I * wl.n_micro + 6 * wl.H * wl.shared_inter
+    return int(max(1, min(wl.T, 4e10 // per_token)))
+
+
+# ---------------------------------------------------------------- arms
+def run_reference(args, wl, world, rank):
+    if rank != 0:
+        return
+    torch.cuda.set_device(0) if torch.cuda.is_available() else None
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = W.make_inputs(wl, seed=0, device=dev)
+    weights = host_weights(inp)
+    Ts = sample_tokens(wl)
+    pool = [W.to_numpy(W.make_inputs(wl, seed=100 + i, device=dev, experts=False, T=Ts)["x"])
+            for i in range(max(2, min(POOL, args.steps)))]
+    import oracle
+    for i in range(args.warmup):
+        oracle.layer(pool[i % len(pool)], weights["router_w"], weights["router_bias"], weights["w13"],
+                     weights["w2"], wl.k, weights["shared_w13"], weights["shared_w2"])
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle.layer(pool[i % len(pool)], weights["router_w"], weights["router_bias"], weights["w13"],
+                     weights["w2"], wl.k, weights["shared_w13"], weights["shared_w2"])
+    dt = time.perf_counter() - t0
+    value = Ts * args.steps / dt
+    sample = f"{Ts} of {wl.T} tokens per step (whole layer: routing, permutation, per-token experts)"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(wl),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(wl):
+    return {"workload": wl.name, "T": wl.T, "hidden": wl.H, "experts": wl.E, "top_k": wl.k, "inter": wl.I,
+            "n_micro": wl.n_micro, "shared_inter": wl.shared_inter,
+            "router": wl.router_init + ("+log_zipf_bias" if wl.router_bias else ""),
+            "l2": "inputs larger than L2: expert weights exceed the 129 MB L2; token batches rotate over "
+                  f"{POOL} seeded batches"}
+
+
+def roofline_of(wl, prof, ids_pool, steps, peaks, sha):
+    """Roofline of the kernel with the largest share of the timed region."""
+    dom, (ms, n) = max(prof.items(), key=lambda kv: kv[1][0])
+    per_launch_s = ms / n / 1e3
+    R = wl.T * wl.k
+    esz = 4 if wl.dtype == "f32" else 2
+    # touched experts per step, averaged over the batches the timed steps used
+    touched = statistics.mean(len(np.unique(ids_pool[i % len(ids_pool)])) for i in range(steps))
+    I, H, M = wl.I, wl.H, wl.n_micro
+    if wl.name == "decode":
+        bound, unit, peak = "hbm", "GB/s", peaks["hbm"]
+        algo = {
+            "gemm1_swiglu": touched * 2 * I * H * esz * M + R * H * esz + R * M * I * esz,
+            "gemm2_down": touched * H * I * esz * M + R * M * I * esz + R * H * esz,
+            "gather": 2 * R * H * esz,
+            "finalize": R * H * esz + wl.T * H * esz,
+            "router": wl.T * H * esz + wl.E * H * esz,
+        }.get(dom)
+        achieved = algo / per_launch_s / 1e9 if algo else None
+    else:
+        bound, unit, peak = "tensor", "TFLOP/s", peaks["bf16_sustained"]
+        algo = {"gemm1_swiglu": 4 * R * H * I * M, "gemm2_down": 2 * R * H * I * M,
+                "shared_gemm1": 4 * wl.T * H * wl.shared_inter,
+                "shared_gemm2": 2 * wl.T * H * wl.shared_inter}.get(dom)
+        achieved = algo / per_launch_s / 1e12 if algo else None
+    traffic = recorded_traffic(wl.name, dom, sha)
+    return {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": (achieved / peak) if achieved else None, "traffic": traffic,
+            "algorithmic_per_launch": algo, "launch_ms": per_launch_s * 1e3,
+            "share": ms / sum(v[0] for v in prof.values()), "peak_source": peaks["source"]}
+
+
+def run_ours(args, wl, world, rank, local):
+    peaks = load_peaks()
+    inp = W.make_inputs(wl, seed=0, device="cuda")
+    pool = [W.make_inputs(wl, seed=100 + i, device="cuda", experts=False)["x"] for i in range(POOL)]
+    layer = binding.MoELayer(wl.H, wl.E, wl.k, wl.I, wl.n_micro, max_tokens=wl.T,
+                             shared_inter=wl.shared_inter, dtype=wl.torch_dtype)
+    y = torch.empty((wl.T, wl.H), dtype=wl.torch_dtype, device="cuda")
+    args_w = (inp["router_w"], inp["router_bias"], inp["w13"], inp["w2"], inp["shared_w13"], inp["shared_w2"])
+
+    def step(i):
+        layer.forward(pool[i % POOL], *args_w, out=y)
+
+    ids_pool = [layer.route(x, inp["router_w"], inp["router_bias"])["ids"].cpu().numpy() for x in pool]
+    for i in range(args.warmup):
+        step(i)
+    layer.sync()
+
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    layer.profile_begin(args.steps)
+    l0 = layer.launch_count()
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(args.warmup + i)
+        ev1.record(stream)
+        ev1.synchronize()
+    torch.cuda.synchronize()
+    barrier(world)
+    launches = layer.launch_count() - l0
+    prof = layer.profile_end()
+    layer.sync()
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world)
+    value = world * wl.T * args.steps / (ms / 1e3)
+    shift = args.warmup % POOL
+    ids_timed = ids_pool[shift:] + ids_pool[:shift]
+    roof = roofline_of(wl, prof, ids_timed, args.steps, peaks, src_sha("gemm_tc.cu", "permute.cu", "router.cu",
+                                                                         "finalize.cu"))
+
+    # end to end through the C ABI with host buffers (pinned), copies included
+    host_pool = [x.cpu().pin_memory() for x in pool]
+    y_host = torch.empty((wl.T, wl.H), dtype=wl.torch_dtype).pin_memory()
+    e2e_steps = max(3, min(args.steps, 50))
+    for i in range(2):
+        layer.forward_host(host_pool[i % POOL], *args_w, out_host=y_host)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        layer.forward_host(host_pool[i % POOL], *args_w, out_host=y_host)
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    esz = 4 if wl.dtype == "f32" else 2
+    e2e = {"value": world * wl.T * e2e_steps / e2e_s, "unit": "tokens/s",
+           "h2d_bytes_per_step": wl.T * wl.H * esz, "d2h_bytes_per_step": wl.T * wl.H * esz}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        weights = host_weights(inp)
+        Ts = sample_tokens(wl)
+        hp = [W.to_numpy(x[:Ts]) for x in pool]
+        v, calls, dt, cores = oracle_tokens_per_s(wl, hp, weights, budget_s=args.cpu_seconds)
+        cpu = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"{calls} whole-layer oracle calls of {Ts} tokens ({dt:.1f} s)"}
+
+    layer.close()
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic", "config": config_of(wl),
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+        "kernels_ms_per_step": {k: v[0] / args.steps for k, v in prof.items()},
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(W.WORKLOADS), default="decode")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    wl = W.WORKLOADS[args.workload]
+    world, rank, local = (1, 0, 0)
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        run_reference(args, wl, int(os.environ.get("WORLD_SIZE", "1")), rank)
+        return
+    world, rank, local = dist_setup()
+    run_ours(args, wl, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,197 @@
+/*
+ * moe.h - C ABI of the GB300 (sm_103a) routed mixture-of-experts FFN layer.
+ *
+ * The layer is the denoise/AR MoE feed-forward of "HunyuanImage3 Hybrid
+ * Parallelism" (LightX2V blog), section 6: a router scores every token
+ * against E experts, keeps the top-k, sorts the routes by expert, runs the
+ * selected SwiGLU experts as grouped GEMMs and reduces each token's k expert
+ * outputs with its routing scales. The multi-micro-shard form of section 6.1
+ * is built in: n_micro weight shards of every expert share one routing, one
+ * permutation, one set of offsets and one finalize.
+ *
+ * Conventions for every entry point
+ *   - Tensors are plain device pointers (host pointers only where a name says
+ *     so), row-major, dense, owned by the caller and 16-byte aligned. They
+ *     must stay valid until the work enqueued on the stream has finished.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). Calls enqueue asynchronously and never synchronise, except
+ *     moe_sync and moe_forward_host as documented.
+ *   - After moe_create, no call allocates device memory: the handle owns a
+ *     workspace sized for cfg.max_tokens.
+ *   - Errors are returned, never raised or aborted. A kernel-side failure
+ *     (bounded wait that ran out, failed device check) is recorded in the
+ *     handle's device error word; the next moe_sync reports it and the handle
+ *     turns sticky: every later call returns MOE_ERR_STICKY until
+ *     moe_destroy. moe_last_error gives a one-line description.
+ *   - Calls on one handle must not overlap on the GPU (they share the
+ *     workspace): issue them on one stream, or order the streams.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, size out of range, mismatch with cfg */
+    MOE_ERR_UNSUPPORTED = 2,  /* shape the kernels do not cover (see moe_create) */
+    MOE_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed */
+    MOE_ERR_OOM = 4,          /* workspace allocation failed in moe_create */
+    MOE_ERR_TIMEOUT = 5,      /* a bounded device-side wait ran out */
+    MOE_ERR_DEVICE_CHECK = 6, /* a device-side consistency check failed */
+    MOE_ERR_STICKY = 7        /* an earlier device error poisoned this handle */
+} moe_status;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+/*
+ * Layer configuration. Names follow the pages: hidden H, experts E, top_k k,
+ * inter I (intermediate size of ONE micro-shard; the blog's W2 [2][64][4096][768]
+ * has I = 768 per micro), n_micro micro-shards per expert (section 5), and an
+ * optional dense shared expert of intermediate size shared_inter (Ascend
+ * Hunyuan Image 3.0 guide, section 3.1).
+ *
+ * Supported: 1 <= E <= 64, 1 <= k <= E (k <= 16), 1 <= n_micro <= 4,
+ * max_tokens * k < 2^31.
+ *   bf16 (tcgen05 path): H % 256 == 0, I % 128 == 0, shared_inter % 128 == 0.
+ *   f32  (exact-fp32 SIMT path): H % 64 == 0, I % 64 == 0, shared_inter % 64 == 0.
+ */
+typedef struct {
+    int32_t hidden;       /* H */
+    int32_t num_experts;  /* E */
+    int32_t top_k;        /* k */
+    int32_t inter;        /* I per micro-shard */
+    int32_t n_micro;      /* micro-shards per expert */
+    int32_t max_tokens;   /* workspace capacity (tokens per call) */
+    int32_t shared_inter; /* Is; 0 = no shared expert */
+    int32_t dtype;        /* moe_dtype of x, weights and y */
+} moe_config;
+
+typedef struct moe_handle moe_handle;
+
+/*
+ * Validate cfg, allocate the workspace for cfg.max_tokens on the current
+ * device and return a handle in *out. This is the only call that allocates.
+ * Returns MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED for a bad cfg, MOE_ERR_OOM
+ * if the workspace cannot be allocated, MOE_ERR_CUDA if no device is usable.
+ */
+moe_status moe_create(const moe_config *cfg, moe_handle **out);
+
+/* Free the workspace and the handle (synchronises the device). NULL is a no-op. */
+void moe_destroy(moe_handle *h);
+
+/*
+ * Routing only: router logits, softmax gate, top-k and renormalised scales,
+ * expert offsets and the route permutation.
+ *   blog section 6.1: ids and scores [num_tokens, top_k]; flatten the ids and
+ *   sort them by expert -> permuted_to_expanded; bincount(...).cumsum(...) ->
+ *   offsets; Ascend guide section 5.2: the gate is computed in fp32.
+ * Inputs:  x [T][H] and router_w [E][H] in cfg.dtype; router_bias fp32 [E] or NULL.
+ * Outputs (device, any may be NULL to skip):
+ *   topk_ids [T][k] int32   experts by descending logit, ties -> lower index
+ *   topk_w   [T][k] fp32    softmax over all E, restricted to the k and renormalised
+ *   perm     [T*k]  int32   permuted_to_expanded: route r = t*k + j at its sorted
+ *                           position; stable, so r ascends inside an expert
+ *   offsets  [E+1]  int32   offsets[e] = first sorted position of expert e, offsets[E] = T*k
+ *   logits   [T][E] fp32    the fp32 logits the decision was taken on
+ * 0 <= T <= cfg.max_tokens; T == 0 writes offsets (all zero) and nothing else.
+ */
+moe_status moe_route(moe_handle *h, const void *x, const void *router_w,
+                     const float *router_bias, int32_t T, int32_t *topk_ids,
+                     float *topk_w, int32_t *perm, int32_t *offsets, float *logits,
+                     void *stream);
+
+/*
+ * The whole layer (blog section 6.1 and 6.2):
+ *   y[t] = sum_j topk_w[t][j] * sum_m down_m,e(silu(gate_m,e x_t) * up_m,e x_t)
+ *          (+ shared_down(silu(shared_gate x_t) * shared_up x_t))
+ * with e = topk_ids[t][j]. Steps, all on `stream`: router + histogram, scan
+ * -> offsets, stable placement -> permutation, one gather of x, grouped GEMM1
+ * with the SwiGLU epilogue for every micro, grouped GEMM2 accumulating all
+ * micros of a route in one fp32 accumulator, (shared expert GEMMs), finalize.
+ * Inputs (device):
+ *   x          [T][H]
+ *   router_w   [E][H], router_bias fp32 [E] or NULL
+ *   w13        host array of n_micro device pointers; w13[m] -> [E][2I][H], rows
+ *              0..I-1 of an expert are its gate rows and I..2I-1 its up rows
+ *              (blog section 4.4 [gate_micro, up_micro]; Ascend guide section 2.2).
+ *              A micro-major pack W1[n_micro][E][2I][H] is passed as
+ *              w13[m] = W1 + m*E*2I*H without repacking (blog section 5).
+ *   w2         host array of n_micro device pointers; w2[m] -> [E][H][I]
+ *   n_micro, top_k   must equal cfg.n_micro and cfg.top_k
+ *   shared_w13 [2Is][H] and shared_w2 [H][Is], both NULL iff cfg.shared_inter == 0
+ * Output: y [T][H] in cfg.dtype (fp32 accumulation, one rounding at the end).
+ */
+moe_status moe_forward(moe_handle *h, const void *x, const void *router_w,
+                       const float *router_bias, const void *const *w13,
+                       const void *const *w2, int32_t n_micro, int32_t top_k,
+                       const void *shared_w13, const void *shared_w2, int32_t T,
+                       void *y, void *stream);
+
+/*
+ * moe_forward with x and y in HOST memory (pinned memory gives the fastest
+ * copies): copies x to the handle's device staging buffer, runs the layer and
+ * copies y back, all on `stream`, then synchronises the stream. Weights and
+ * the router are device pointers as in moe_forward.
+ */
+moe_status moe_forward_host(moe_handle *h, const void *x_host, const void *router_w,
+                            const float *router_bias, const void *const *w13,
+                            const void *const *w2, int32_t n_micro, int32_t top_k,
+                            const void *shared_w13, const void *shared_w2, int32_t T,
+                            void *y_host, void *stream);
+
+/*
+ * Synchronise the stream of the handle's last call and read its device error
+ * word. Returns MOE_OK, or MOE_ERR_TIMEOUT / MOE_ERR_DEVICE_CHECK (and makes
+ * the handle sticky), or MOE_ERR_CUDA.
+ */
+moe_status moe_sync(moe_handle *h);
+
+/* One-line description of the handle's last error ("" if none). Never NULL. */
+const char *moe_last_error(const moe_handle *h);
+
+/* Static name of a status code. */
+const char *moe_status_string(moe_status s);
+
+/*
+ * Diagnostics for tests: device address of a workspace buffer of the last
+ * call. which: 0 = gathered input xp [T*k][H], 1 = SwiGLU output h [T*k][n_micro*I],
+ * 2 = expert outputs o [T*k][H], 3 = inverse permutation [T*k] int32,
+ * 4 = device error word (int32). Returns NULL for an unknown `which`.
+ */
+void *moe_workspace_ptr(const moe_handle *h, int32_t which);
+
+/*
+ * Diagnostics: per-kernel timing with CUDA events. Between moe_profile_begin
+ * and moe_profile_end, the first `max_calls` calls of moe_forward /
+ * moe_forward_host / moe_route record an event pair around every kernel they
+ * launch, on the call's stream. moe_profile_end synchronises those events and
+ * writes, per kernel slot, the summed duration in milliseconds and the number
+ * of launches. Slots: 0 router, 1 scan, 2 place, 3 gather, 4 GEMM1 (+SwiGLU),
+ * 5 GEMM2, 6 shared-expert GEMM1, 7 shared-expert GEMM2, 8 finalize.
+ */
+#define MOE_PROFILE_SLOTS 9
+moe_status moe_profile_begin(moe_handle *h, int32_t max_calls);
+moe_status moe_profile_end(moe_handle *h, float *ms /* [MOE_PROFILE_SLOTS] */,
+                           int32_t *launches /* [MOE_PROFILE_SLOTS] */);
+
+/* Number of kernels this handle has launched since moe_create. */
+int64_t moe_launch_count(const moe_handle *h);
+
+/*
+ * Self-test of the bounded device-side wait: launches one block whose thread
+ * waits on an mbarrier that nothing completes, with a limit of `timeout_us`
+ * microseconds, then returns the status the kernel reported (expected:
+ * MOE_ERR_TIMEOUT). Synchronises the stream. Does not touch any handle.
+ */
+moe_status moe_selftest_wait_timeout(int32_t timeout_us, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

@@ -1,0 +1,99 @@
+// finalize.cu - the single unpermute, routing-scale and top-k reduction.
+//
+// "HunyuanImage3 Hybrid Parallelism", section 6.1: the finalize reads the
+// expert outputs by original token and top-k slot and forms
+//     output[token] = sum over routes of routing_scale[token, route] * partial,
+// adding in fp32, applying the scale once and reducing over top-k once. Here
+// the per-micro partials were already summed in the GEMM2 accumulator, so
+// each route contributes one row o[inv[t*k + j]]. The shared expert's output
+// (Ascend Hunyuan Image 3.0 guide, section 3.1) is added unscaled.
+//
+// HBM-bound: one block per token, 16-byte vector loads of the k expert rows.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 128;
+
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&v)[8]) {
+    uint4 u = *reinterpret_cast<const uint4*>(p);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float2 f = __bfloat1622float2(h[i]);
+        v[2 * i] = f.x;
+        v[2 * i + 1] = f.y;
+    }
+}
+
+__device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
+    float4 a = *reinterpret_cast<const float4*>(p);
+    float4 b = *reinterpret_cast<const float4*>(p + 4);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+__device__ __forceinline__ void store8(__nv_bfloat16* p, const float (&v)[8]) {
+    uint4 u;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    *reinterpret_cast<uint4*>(p) = u;
+}
+
+__device__ __forceinline__ void store8(float* p, const float (&v)[8]) {
+    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+    *reinterpret_cast<float4*>(p + 4) = make_float4(v[4], v[5], v[6], v[7]);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) finalize_kernel(FinalizeArgs a) {
+    __shared__ int64_t rows[kMaxTopK];
+    __shared__ float scale[kMaxTopK];
+    const int t = blockIdx.x;
+    const int64_t R = (int64_t)a.T * a.k;
+    if (threadIdx.x < a.k) {
+        int64_t r = a.inv[(int64_t)t * a.k + threadIdx.x];
+        if (r < 0 || r >= R) r = 0;  // unreachable for a valid permutation
+        rows[threadIdx.x] = r;
+        scale[threadIdx.x] = a.w[(int64_t)t * a.k + threadIdx.x];
+    }
+    __syncthreads();
+    const T* o = static_cast<const T*>(a.o);
+    const T* sh = static_cast<const T*>(a.shared);
+    T* y = static_cast<T*>(a.y);
+    const int nv = a.H / 8;
+    for (int v = threadIdx.x; v < nv; v += kThreads) {
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int j = 0; j < a.k; ++j) {
+            float val[8];
+            load8(o + rows[j] * a.H + v * 8, val);
+            const float s = scale[j];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = fmaf(s, val[i], acc[i]);
+        }
+        if (sh != nullptr) {
+            float val[8];
+            load8(sh + (int64_t)t * a.H + v * 8, val);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] += val[i];
+        }
+        store8(y + (int64_t)t * a.H + v * 8, acc);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t s) {
+    if (a.T == 0) return cudaSuccess;
+    if (a.bf16)
+        finalize_kernel<__nv_bfloat16><<<a.T, kThreads, 0, s>>>(a);
+    else
+        finalize_kernel<float><<<a.T, kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,144 @@
+// kernels.h - internal launch interfaces of the layer's kernels (not the ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace moe {
+
+// Bits of the device error word.
+enum DeviceError : int {
+    kErrTimeout = 1,  // a bounded wait ran out
+    kErrCheck = 2,    // a device-side consistency check failed
+};
+
+constexpr int kMaxExperts = 64;
+constexpr int kMaxTopK = 16;
+constexpr int kMaxMicro = 4;
+
+// ---------------------------------------------------------------- router
+// One block routes kRouterTokens tokens; its histogram row is blk_hist[block].
+constexpr int kRouterTokens = 32;
+
+struct RouterArgs {
+    const void* x;         // [T][H]
+    const void* wr;        // [E][H]
+    const float* bias;     // [E] or null
+    int T, H, E, k;
+    bool bf16;
+    int32_t* ids;          // [T][k]
+    float* w;              // [T][k]
+    float* logits;         // [T][E] or null
+    int32_t* blk_hist;     // [NB][E]
+    int* err;
+};
+cudaError_t launch_router(const RouterArgs& a, cudaStream_t s);
+
+// --------------------------------------------------------- scan / place
+struct ScanArgs {
+    const int32_t* blk_hist;  // [NB][E]
+    int NB, E, T, k;
+    int32_t* blk_base;        // [NB][E] first sorted position of block b's expert-e routes
+    int32_t* offsets;         // [E+1]
+    int32_t* tiles_tc;        // [E+1] prefix of ceil(count/kTcBM)
+    int32_t* tiles_simt;      // [E+1] prefix of ceil(count/kSimtBM)
+    int32_t* shared_seg;      // [2] = {0, T}
+    int32_t* shared_tiles_tc;   // [2] = {0, ceil(T/kTcBM)}
+    int32_t* shared_tiles_simt; // [2] = {0, ceil(T/kSimtBM)}
+};
+cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s);
+
+struct PlaceArgs {
+    const int32_t* ids;       // [T][k]
+    const int32_t* blk_base;  // [NB][E]
+    int T, k, E, NB;
+    int32_t* perm;            // [T*k]
+    int32_t* inv;             // [T*k]
+    int* err;
+};
+cudaError_t launch_place(const PlaceArgs& a, cudaStream_t s);
+
+struct GatherArgs {
+    const void* x;            // [T][row_bytes]
+    const int32_t* perm;      // [R]
+    int R, k;
+    uint32_t row_bytes;       // multiple of 16
+    void* xp;                 // [R][row_bytes]
+    int* err;
+    uint64_t limit_ns;
+    int num_sms;
+};
+cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s);
+
+// ------------------------------------------------------- tcgen05 GEMMs
+constexpr int kTcBM = 128;   // rows per tile (MMA M)
+constexpr int kTcBK = 64;    // K per stage: 64 bf16 = one 128-byte swizzled row
+
+// Grouped GEMM over row segments [seg[g], seg[g+1]) of A, one weight block per group.
+//   SwiGLU form (GEMM1): out[r][m*I + n] = silu(A_r . B_m[g][n]) * (A_r . B_m[g][I + n])
+//   Plain form (GEMM2):  out[r][n] = sum_m A_r[m*I:(m+1)*I] . B_m[g][n]
+struct TcGemmArgs {
+    const int32_t* seg;       // [G+1] row offsets
+    const int32_t* tiles;     // [G+1] prefix of ceil(rows/kTcBM)
+    int G;
+    int n_micro;
+    int k_blocks;             // kTcBK-blocks of K per micro
+    int n_tiles;              // output column tiles per (group, micro)
+    int b_rows_per_group;     // rows of B per group (2I for GEMM1, H for GEMM2)
+    int up_offset;            // GEMM1: I (row offset of the up rows)
+    int a_micro_cols;         // GEMM2: A columns per micro (I)
+    void* out;                // bf16
+    int64_t out_ld;           // elements per output row
+    int out_micro_cols;       // GEMM1: I (column offset of micro m in out)
+    int max_tiles;            // upper bound used for the grid
+    int* err;
+    uint64_t limit_ns;
+};
+// tmA: A [rows][K] bf16, box {64, 128}; tmB[m]: B_m [G*b_rows][K] bf16, box {64, 128}.
+cudaError_t launch_tc_gemm_swiglu(const TcGemmArgs& a, const CUtensorMap& tmA, const CUtensorMap* tmB,
+                                  int num_sms, cudaStream_t s);
+cudaError_t launch_tc_gemm_down(const TcGemmArgs& a, const CUtensorMap& tmA, const CUtensorMap* tmB,
+                                int num_sms, cudaStream_t s);
+
+// ---------------------------------------------------- fp32 SIMT GEMMs
+constexpr int kSimtBM = 32;
+
+struct SimtGemmArgs {
+    const float* a;           // [rows][lda]
+    int64_t lda;
+    const int32_t* seg;       // [G+1]
+    const int32_t* tiles;     // [G+1] prefix of ceil(rows/kSimtBM)
+    int G;
+    int n_micro;
+    const float* b[kMaxMicro];  // per micro: [G][b_rows][K]
+    int K;                    // reduction length per micro (H for GEMM1, I for GEMM2)
+    int N;                    // output columns per micro (I for GEMM1, H for GEMM2)
+    int b_rows_per_group;     // 2I (GEMM1) or H (GEMM2)
+    int a_micro_cols;         // GEMM2: A column offset per micro (I); GEMM1: 0
+    float* out;
+    int64_t out_ld;
+    int out_micro_cols;       // GEMM1: I; GEMM2: 0
+    int max_tiles;
+};
+cudaError_t launch_simt_gemm_swiglu(const SimtGemmArgs& a, cudaStream_t s);
+cudaError_t launch_simt_gemm_down(const SimtGemmArgs& a, cudaStream_t s);
+
+// ------------------------------------------------------------ finalize
+struct FinalizeArgs {
+    const void* o;            // [R][H] expert outputs (bf16 or f32)
+    const int32_t* inv;       // [R]
+    const float* w;           // [T][k]
+    const void* shared;       // [T][H] or null
+    int T, k, H;
+    bool bf16;
+    void* y;                  // [T][H]
+};
+cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t s);
+
+// ------------------------------------------------------------ self-test
+cudaError_t launch_wait_selftest(int* err, uint64_t limit_ns, cudaStream_t s);
+
+}  // namespace moe

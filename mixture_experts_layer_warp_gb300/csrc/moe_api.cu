@@ -1,0 +1,590 @@
+// moe_api.cu - the C ABI of include/moe.h: argument checks, the workspace,
+// tensor-map encoding and the launch sequence of one layer call.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/moe.h"
+#include "kernels.h"
+
+using namespace moe;
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (fn == nullptr) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s per bounded wait
+
+}  // namespace
+
+struct moe_handle {
+    moe_config cfg;
+    int device = 0;
+    int num_sms = 0;
+    size_t esz = 2;
+    uint64_t limit_ns = kDefaultWaitLimitNs;
+    cudaStream_t last_stream = nullptr;
+    bool sticky = false;
+    char msg[512] = {0};
+    void* ws = nullptr;
+    size_t ws_bytes = 0;
+    // workspace views
+    int* err = nullptr;
+    int32_t* ids = nullptr;
+    float* topw = nullptr;
+    int32_t* perm = nullptr;
+    int32_t* inv = nullptr;
+    int32_t* offsets = nullptr;
+    int32_t* tiles_tc = nullptr;
+    int32_t* tiles_simt = nullptr;
+    int32_t* shared_seg = nullptr;
+    int32_t* shared_tiles_tc = nullptr;
+    int32_t* shared_tiles_simt = nullptr;
+    int32_t* blk_hist = nullptr;
+    int32_t* blk_base = nullptr;
+    void* xp = nullptr;
+    void* hbuf = nullptr;
+    void* obuf = nullptr;
+    void* hs = nullptr;
+    void* sbuf = nullptr;
+    void* x_stage = nullptr;
+    void* y_stage = nullptr;
+    // diagnostics
+    int64_t launches = 0;
+    bool prof_on = false;
+    int prof_max = 0;
+    int prof_calls = 0;
+    std::vector<cudaEvent_t> prof_ev;   // [max_calls][slots][2]
+    std::vector<unsigned char> prof_used;  // [max_calls][slots]
+};
+
+namespace {
+
+moe_status set_err(moe_handle* h, moe_status st, const char* fmt, ...) {
+    if (h != nullptr) {
+        va_list ap;
+        va_start(ap, fmt);
+        vsnprintf(h->msg, sizeof h->msg, fmt, ap);
+        va_end(ap);
+    }
+    return st;
+}
+
+moe_status cuda_err(moe_handle* h, cudaError_t e, const char* what) {
+    return set_err(h, MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+moe_status check_cfg(const moe_config* c, char* msg, size_t n) {
+    auto bad = [&](moe_status st, const char* why) {
+        snprintf(msg, n, "%s", why);
+        return st;
+    };
+    if (c->hidden <= 0 || c->num_experts <= 0 || c->top_k <= 0 || c->inter <= 0 || c->n_micro <= 0 ||
+        c->max_tokens < 0 || c->shared_inter < 0)
+        return bad(MOE_ERR_INVALID_ARG, "config sizes must be positive");
+    if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return bad(MOE_ERR_INVALID_ARG, "dtype must be MOE_F32 or MOE_BF16");
+    if (c->top_k > c->num_experts) return bad(MOE_ERR_INVALID_ARG, "top_k must not exceed num_experts");
+    if (c->num_experts > kMaxExperts) return bad(MOE_ERR_UNSUPPORTED, "num_experts > 64");
+    if (c->top_k > kMaxTopK) return bad(MOE_ERR_UNSUPPORTED, "top_k > 16");
+    if (c->n_micro > kMaxMicro) return bad(MOE_ERR_UNSUPPORTED, "n_micro > 4");
+    if ((int64_t)c->max_tokens * c->top_k >= (1ll << 31)) return bad(MOE_ERR_UNSUPPORTED, "max_tokens * top_k >= 2^31");
+    if (c->dtype == MOE_BF16) {
+        if (c->hidden % 256) return bad(MOE_ERR_UNSUPPORTED, "bf16 path needs hidden % 256 == 0");
+        if (c->inter % 128) return bad(MOE_ERR_UNSUPPORTED, "bf16 path needs inter % 128 == 0");
+        if (c->shared_inter % 128) return bad(MOE_ERR_UNSUPPORTED, "bf16 path needs shared_inter % 128 == 0");
+    } else {
+        if (c->hidden % 64) return bad(MOE_ERR_UNSUPPORTED, "f32 path needs hidden % 64 == 0");
+        if (c->inter % 64) return bad(MOE_ERR_UNSUPPORTED, "f32 path needs inter % 64 == 0");
+        if (c->shared_inter % 64) return bad(MOE_ERR_UNSUPPORTED, "f32 path needs shared_inter % 64 == 0");
+        if ((int64_t)c->max_tokens * c->top_k / kSimtBM + c->num_experts >= 65535)
+            return bad(MOE_ERR_UNSUPPORTED, "f32 path supports max_tokens * top_k < 2M");
+    }
+    return MOE_OK;
+}
+
+// 2D bf16 tensor map over a row-major [rows][inner] matrix with a 64 x 128 box
+// and 128-byte swizzling (the K-major operand layout of the tcgen05 kernels).
+bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t row_bytes) {
+    EncodeTiledFn enc = get_encode_fn();
+    if (enc == nullptr) return false;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {(cuuint32_t)kTcBK, (cuuint32_t)kTcBM};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+enum Slot { kRouter = 0, kScan, kPlace, kGather, kGemm1, kGemm2, kSharedGemm1, kSharedGemm2, kFinalize };
+
+// Runs one kernel launch, counting it and, while profiling, bracketing it with
+// an event pair on the stream.
+template <typename F>
+cudaError_t timed(moe_handle* h, Slot slot, cudaStream_t s, F&& launch) {
+    const bool rec = h->prof_on && h->prof_calls < h->prof_max;
+    const size_t i = ((size_t)h->prof_calls * MOE_PROFILE_SLOTS + slot);
+    if (rec) cudaEventRecord(h->prof_ev[2 * i], s);
+    cudaError_t e = launch();
+    if (rec) {
+        cudaEventRecord(h->prof_ev[2 * i + 1], s);
+        h->prof_used[i] = 1;
+    }
+    if (e == cudaSuccess) h->launches += 1;
+    return e;
+}
+
+void end_call(moe_handle* h) {
+    if (h->prof_on && h->prof_calls < h->prof_max) h->prof_calls += 1;
+}
+
+moe_status check_call(moe_handle* h, const void* x, const void* router_w, int32_t T) {
+    if (h == nullptr) return MOE_ERR_INVALID_ARG;
+    if (h->sticky) return set_err(h, MOE_ERR_STICKY, "handle is sticky after an earlier device error");
+    if (T < 0 || T > h->cfg.max_tokens)
+        return set_err(h, MOE_ERR_INVALID_ARG, "T=%d outside [0, max_tokens=%d]", T, h->cfg.max_tokens);
+    if (T > 0 && (x == nullptr || router_w == nullptr))
+        return set_err(h, MOE_ERR_INVALID_ARG, "x and router_w must be non-null");
+    if (!aligned16(x) || !aligned16(router_w))
+        return set_err(h, MOE_ERR_INVALID_ARG, "x and router_w must be 16-byte aligned");
+    return MOE_OK;
+}
+
+// Router, scan and placement: leaves ids, topw, offsets, tiles, perm and inv in the workspace.
+moe_status run_routing(moe_handle* h, const void* x, const void* router_w, const float* bias, int32_t T,
+                       float* logits, cudaStream_t s) {
+    const moe_config& c = h->cfg;
+    const int NB = (T + kRouterTokens - 1) / kRouterTokens;
+    cudaError_t e;
+    RouterArgs ra{x, router_w, bias, T, c.hidden, c.num_experts, c.top_k, c.dtype == MOE_BF16,
+                  h->ids, h->topw, logits, h->blk_hist, h->err};
+    if ((e = timed(h, kRouter, s, [&] { return launch_router(ra, s); })) != cudaSuccess) return cuda_err(h, e, "router launch");
+    ScanArgs sa{h->blk_hist, NB, c.num_experts, T, c.top_k, h->blk_base, h->offsets, h->tiles_tc,
+                h->tiles_simt, h->shared_seg, h->shared_tiles_tc, h->shared_tiles_simt};
+    if ((e = timed(h, kScan, s, [&] { return launch_scan(sa, s); })) != cudaSuccess) return cuda_err(h, e, "scan launch");
+    PlaceArgs pa{h->ids, h->blk_base, T, c.top_k, c.num_experts, NB, h->perm, h->inv, h->err};
+    if ((e = timed(h, kPlace, s, [&] { return launch_place(pa, s); })) != cudaSuccess) return cuda_err(h, e, "place launch");
+    return MOE_OK;
+}
+
+moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const float* bias,
+                       const void* const* w13, const void* const* w2, const void* sw13, const void* sw2, int32_t T,
+                       void* y, cudaStream_t s) {
+    const moe_config& c = h->cfg;
+    const int H = c.hidden, E = c.num_experts, k = c.top_k, I = c.inter, M = c.n_micro, Is = c.shared_inter;
+    const int64_t R = (int64_t)T * k;
+    cudaError_t e;
+    moe_status st = run_routing(h, x, router_w, bias, T, nullptr, s);
+    if (st != MOE_OK) return st;
+
+    GatherArgs ga{x, h->perm, (int)R, k, (uint32_t)(H * h->esz), h->xp, h->err, h->limit_ns, h->num_sms};
+    if ((e = timed(h, kGather, s, [&] { return launch_gather(ga, s); })) != cudaSuccess) return cuda_err(h, e, "gather launch");
+
+    const int routed_tiles_tc = (int)(R / kTcBM) + E;  // bound on sum of ceil(count/128)
+    if (c.dtype == MOE_BF16) {
+        CUtensorMap tmA, tmB[kMaxMicro];
+        // GEMM1 + SwiGLU: xp [R][H] x w13[m] [E*2I][H] -> h [R][M*I]
+        if (!encode_2d(&tmA, h->xp, H, R, (uint64_t)H * 2))
+            return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (xp)");
+        for (int m = 0; m < M; ++m)
+            if (!encode_2d(&tmB[m], w13[m], H, (uint64_t)E * 2 * I, (uint64_t)H * 2))
+                return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (w13[%d])", m);
+        TcGemmArgs g1{h->offsets, h->tiles_tc, E, M, H / kTcBK, I / 128, 2 * I, I, 0,
+                      h->hbuf, (int64_t)M * I, I, M * routed_tiles_tc * (I / 128), h->err, h->limit_ns};
+        if ((e = timed(h, kGemm1, s, [&] { return launch_tc_gemm_swiglu(g1, tmA, tmB, h->num_sms, s); })) != cudaSuccess)
+            return cuda_err(h, e, "GEMM1 launch");
+        // GEMM2: h [R][M*I] x w2[m] [E*H][I], summed over m -> o [R][H]
+        if (!encode_2d(&tmA, h->hbuf, (uint64_t)M * I, R, (uint64_t)M * I * 2))
+            return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (h)");
+        for (int m = 0; m < M; ++m)
+            if (!encode_2d(&tmB[m], w2[m], I, (uint64_t)E * H, (uint64_t)I * 2))
+                return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (w2[%d])", m);
+        TcGemmArgs g2{h->offsets, h->tiles_tc, E, M, I / kTcBK, H / 256, H, 0, I,
+                      h->obuf, (int64_t)H, 0, routed_tiles_tc * (H / 256), h->err, h->limit_ns};
+        if ((e = timed(h, kGemm2, s, [&] { return launch_tc_gemm_down(g2, tmA, tmB, h->num_sms, s); })) != cudaSuccess)
+            return cuda_err(h, e, "GEMM2 launch");
+        if (Is > 0) {
+            const int stiles = (T + kTcBM - 1) / kTcBM;
+            if (!encode_2d(&tmA, x, H, T, (uint64_t)H * 2) || !encode_2d(&tmB[0], sw13, H, 2 * (uint64_t)Is, (uint64_t)H * 2))
+                return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (shared GEMM1)");
+            TcGemmArgs s1{h->shared_seg, h->shared_tiles_tc, 1, 1, H / kTcBK, Is / 128, 2 * Is, Is, 0,
+                          h->hs, (int64_t)Is, 0, stiles * (Is / 128), h->err, h->limit_ns};
+            if ((e = timed(h, kSharedGemm1, s, [&] { return launch_tc_gemm_swiglu(s1, tmA, tmB, h->num_sms, s); })) != cudaSuccess)
+                return cuda_err(h, e, "shared GEMM1 launch");
+            if (!encode_2d(&tmA, h->hs, Is, T, (uint64_t)Is * 2) || !encode_2d(&tmB[0], sw2, Is, H, (uint64_t)Is * 2))
+                return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (shared GEMM2)");
+            TcGemmArgs s2{h->shared_seg, h->shared_tiles_tc, 1, 1, Is / kTcBK, H / 256, H, 0, Is,
+                          h->sbuf, (int64_t)H, 0, stiles * (H / 256), h->err, h->limit_ns};
+            if ((e = timed(h, kSharedGemm2, s, [&] { return launch_tc_gemm_down(s2, tmA, tmB, h->num_sms, s); })) != cudaSuccess)
+                return cuda_err(h, e, "shared GEMM2 launch");
+        }
+    } else {
+        const int routed_tiles = (int)(R / kSimtBM) + E;
+        SimtGemmArgs g1{};
+        g1.a = static_cast<const float*>(h->xp);
+        g1.lda = H;
+        g1.seg = h->offsets;
+        g1.tiles = h->tiles_simt;
+        g1.G = E;
+        g1.n_micro = M;
+        for (int m = 0; m < M; ++m) g1.b[m] = static_cast<const float*>(w13[m]);
+        g1.K = H;
+        g1.N = I;
+        g1.b_rows_per_group = 2 * I;
+        g1.a_micro_cols = 0;
+        g1.out = static_cast<float*>(h->hbuf);
+        g1.out_ld = (int64_t)M * I;
+        g1.out_micro_cols = I;
+        g1.max_tiles = routed_tiles;
+        if ((e = timed(h, kGemm1, s, [&] { return launch_simt_gemm_swiglu(g1, s); })) != cudaSuccess) return cuda_err(h, e, "f32 GEMM1 launch");
+        SimtGemmArgs g2 = g1;
+        g2.a = static_cast<const float*>(h->hbuf);
+        g2.lda = (int64_t)M * I;
+        for (int m = 0; m < M; ++m) g2.b[m] = static_cast<const float*>(w2[m]);
+        g2.K = I;
+        g2.N = H;
+        g2.b_rows_per_group = H;
+        g2.a_micro_cols = I;
+        g2.out = static_cast<float*>(h->obuf);
+        g2.out_ld = H;
+        g2.out_micro_cols = 0;
+        if ((e = timed(h, kGemm2, s, [&] { return launch_simt_gemm_down(g2, s); })) != cudaSuccess) return cuda_err(h, e, "f32 GEMM2 launch");
+        if (Is > 0) {
+            SimtGemmArgs s1{};
+            s1.a = static_cast<const float*>(x);
+            s1.lda = H;
+            s1.seg = h->shared_seg;
+            s1.tiles = h->shared_tiles_simt;
+            s1.G = 1;
+            s1.n_micro = 1;
+            s1.b[0] = static_cast<const float*>(sw13);
+            s1.K = H;
+            s1.N = Is;
+            s1.b_rows_per_group = 2 * Is;
+            s1.out = static_cast<float*>(h->hs);
+            s1.out_ld = Is;
+            s1.max_tiles = (T + kSimtBM - 1) / kSimtBM;
+            if ((e = timed(h, kSharedGemm1, s, [&] { return launch_simt_gemm_swiglu(s1, s); })) != cudaSuccess) return cuda_err(h, e, "f32 shared GEMM1");
+            SimtGemmArgs s2 = s1;
+            s2.a = static_cast<const float*>(h->hs);
+            s2.lda = Is;
+            s2.b[0] = static_cast<const float*>(sw2);
+            s2.K = Is;
+            s2.N = H;
+            s2.b_rows_per_group = H;
+            s2.a_micro_cols = Is;
+            s2.out = static_cast<float*>(h->sbuf);
+            s2.out_ld = H;
+            if ((e = timed(h, kSharedGemm2, s, [&] { return launch_simt_gemm_down(s2, s); })) != cudaSuccess) return cuda_err(h, e, "f32 shared GEMM2");
+        }
+    }
+    FinalizeArgs fa{h->obuf, h->inv, h->topw, Is > 0 ? h->sbuf : nullptr, T, k, H, c.dtype == MOE_BF16, y};
+    if ((e = timed(h, kFinalize, s, [&] { return launch_finalize(fa, s); })) != cudaSuccess) return cuda_err(h, e, "finalize launch");
+    return MOE_OK;
+}
+
+moe_status check_weights(moe_handle* h, const void* const* w13, const void* const* w2, int32_t n_micro,
+                         int32_t top_k, const void* sw13, const void* sw2, const void* y) {
+    const moe_config& c = h->cfg;
+    if (n_micro != c.n_micro) return set_err(h, MOE_ERR_INVALID_ARG, "n_micro=%d != config %d", n_micro, c.n_micro);
+    if (top_k != c.top_k) return set_err(h, MOE_ERR_INVALID_ARG, "top_k=%d != config %d", top_k, c.top_k);
+    if (w13 == nullptr || w2 == nullptr) return set_err(h, MOE_ERR_INVALID_ARG, "w13 and w2 arrays must be non-null");
+    for (int m = 0; m < n_micro; ++m)
+        if (w13[m] == nullptr || w2[m] == nullptr || !aligned16(w13[m]) || !aligned16(w2[m]))
+            return set_err(h, MOE_ERR_INVALID_ARG, "micro %d weights null or not 16-byte aligned", m);
+    const bool has_shared = c.shared_inter > 0;
+    if (has_shared != (sw13 != nullptr) || has_shared != (sw2 != nullptr))
+        return set_err(h, MOE_ERR_INVALID_ARG, "shared expert weights must be given iff shared_inter > 0");
+    if (!aligned16(sw13) || !aligned16(sw2)) return set_err(h, MOE_ERR_INVALID_ARG, "shared weights not 16-byte aligned");
+    if (y == nullptr || !aligned16(y)) return set_err(h, MOE_ERR_INVALID_ARG, "y null or not 16-byte aligned");
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_create(const moe_config* cfg, moe_handle** out) {
+    if (cfg == nullptr || out == nullptr) return MOE_ERR_INVALID_ARG;
+    *out = nullptr;
+    char why[256];
+    moe_status st = check_cfg(cfg, why, sizeof why);
+    if (st != MOE_OK) {
+        fprintf(stderr, "moe_create: %s\n", why);
+        return st;
+    }
+    moe_handle* h = new (std::nothrow) moe_handle();
+    if (h == nullptr) return MOE_ERR_OOM;
+    h->cfg = *cfg;
+    h->esz = cfg->dtype == MOE_BF16 ? 2 : 4;
+    if (const char* v = getenv("MOE_WAIT_LIMIT_MS")) {
+        const long long ms = atoll(v);
+        if (ms > 0) h->limit_ns = (uint64_t)ms * 1000000ull;
+    }
+    if (cudaGetDevice(&h->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
+        delete h;
+        return MOE_ERR_CUDA;
+    }
+    if (cfg->dtype == MOE_BF16) {
+        int major = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, h->device);
+        if (major != 10 || get_encode_fn() == nullptr) {
+            delete h;
+            return MOE_ERR_UNSUPPORTED;
+        }
+    }
+    const int64_t T = cfg->max_tokens, k = cfg->top_k, E = cfg->num_experts, H = cfg->hidden;
+    const int64_t R = T * k, NB = (T + kRouterTokens - 1) / kRouterTokens;
+    const int64_t M = cfg->n_micro, I = cfg->inter, Is = cfg->shared_inter;
+    const size_t esz = h->esz;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t o = off;
+        off = round_up(off + (bytes ? bytes : 1), 256);
+        return o;
+    };
+    const size_t o_err = take(sizeof(int));
+    const size_t o_ids = take(R * 4), o_topw = take(R * 4), o_perm = take(R * 4), o_inv = take(R * 4);
+    const size_t o_off = take((E + 1) * 4), o_ttc = take((E + 1) * 4), o_tsi = take((E + 1) * 4);
+    const size_t o_sseg = take(8), o_sttc = take(8), o_stsi = take(8);
+    const size_t o_hist = take(NB * E * 4), o_base = take(NB * E * 4);
+    const size_t o_xp = take(R * H * esz), o_h = take(R * M * I * esz), o_o = take(R * H * esz);
+    const size_t o_hs = take(T * Is * esz), o_s = take(Is ? T * H * esz : 0);
+    const size_t o_xst = take(T * H * esz), o_yst = take(T * H * esz);
+    h->ws_bytes = off;
+    if (cudaMalloc(&h->ws, h->ws_bytes) != cudaSuccess) {
+        cudaGetLastError();
+        delete h;
+        return MOE_ERR_OOM;
+    }
+    char* b = static_cast<char*>(h->ws);
+    h->err = reinterpret_cast<int*>(b + o_err);
+    h->ids = reinterpret_cast<int32_t*>(b + o_ids);
+    h->topw = reinterpret_cast<float*>(b + o_topw);
+    h->perm = reinterpret_cast<int32_t*>(b + o_perm);
+    h->inv = reinterpret_cast<int32_t*>(b + o_inv);
+    h->offsets = reinterpret_cast<int32_t*>(b + o_off);
+    h->tiles_tc = reinterpret_cast<int32_t*>(b + o_ttc);
+    h->tiles_simt = reinterpret_cast<int32_t*>(b + o_tsi);
+    h->shared_seg = reinterpret_cast<int32_t*>(b + o_sseg);
+    h->shared_tiles_tc = reinterpret_cast<int32_t*>(b + o_sttc);
+    h->shared_tiles_simt = reinterpret_cast<int32_t*>(b + o_stsi);
+    h->blk_hist = reinterpret_cast<int32_t*>(b + o_hist);
+    h->blk_base = reinterpret_cast<int32_t*>(b + o_base);
+    h->xp = b + o_xp;
+    h->hbuf = b + o_h;
+    h->obuf = b + o_o;
+    h->hs = b + o_hs;
+    h->sbuf = b + o_s;
+    h->x_stage = b + o_xst;
+    h->y_stage = b + o_yst;
+    if (cudaMemset(h->err, 0, sizeof(int)) != cudaSuccess) {
+        cudaFree(h->ws);
+        delete h;
+        return MOE_ERR_CUDA;
+    }
+    *out = h;
+    return MOE_OK;
+}
+
+void moe_destroy(moe_handle* h) {
+    if (h == nullptr) return;
+    cudaDeviceSynchronize();
+    for (cudaEvent_t ev : h->prof_ev) cudaEventDestroy(ev);
+    cudaFree(h->ws);
+    delete h;
+}
+
+moe_status moe_route(moe_handle* h, const void* x, const void* router_w, const float* router_bias, int32_t T,
+                     int32_t* topk_ids, float* topk_w, int32_t* perm, int32_t* offsets, float* logits,
+                     void* stream) {
+    moe_status st = check_call(h, x, router_w, T);
+    if (st != MOE_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    h->last_stream = s;
+    const moe_config& c = h->cfg;
+    const size_t nE1 = (size_t)(c.num_experts + 1) * 4;
+    if (T == 0) {
+        if (offsets != nullptr && cudaMemsetAsync(offsets, 0, nE1, s) != cudaSuccess)
+            return set_err(h, MOE_ERR_CUDA, "memset offsets failed");
+        return MOE_OK;
+    }
+    st = run_routing(h, x, router_w, router_bias, T, logits, s);
+    end_call(h);
+    if (st != MOE_OK) return st;
+    const size_t R = (size_t)T * c.top_k;
+    cudaError_t e = cudaSuccess;
+    if (topk_ids && e == cudaSuccess) e = cudaMemcpyAsync(topk_ids, h->ids, R * 4, cudaMemcpyDeviceToDevice, s);
+    if (topk_w && e == cudaSuccess) e = cudaMemcpyAsync(topk_w, h->topw, R * 4, cudaMemcpyDeviceToDevice, s);
+    if (perm && e == cudaSuccess) e = cudaMemcpyAsync(perm, h->perm, R * 4, cudaMemcpyDeviceToDevice, s);
+    if (offsets && e == cudaSuccess) e = cudaMemcpyAsync(offsets, h->offsets, nE1, cudaMemcpyDeviceToDevice, s);
+    if (e != cudaSuccess) return cuda_err(h, e, "copy routing outputs");
+    return MOE_OK;
+}
+
+moe_status moe_forward(moe_handle* h, const void* x, const void* router_w, const float* router_bias,
+                       const void* const* w13, const void* const* w2, int32_t n_micro, int32_t top_k,
+                       const void* shared_w13, const void* shared_w2, int32_t T, void* y, void* stream) {
+    moe_status st = check_call(h, x, router_w, T);
+    if (st != MOE_OK) return st;
+    if (T == 0) return MOE_OK;
+    st = check_weights(h, w13, w2, n_micro, top_k, shared_w13, shared_w2, y);
+    if (st != MOE_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    h->last_stream = s;
+    st = run_forward(h, x, router_w, router_bias, w13, w2, shared_w13, shared_w2, T, y, s);
+    end_call(h);
+    return st;
+}
+
+moe_status moe_forward_host(moe_handle* h, const void* x_host, const void* router_w, const float* router_bias,
+                            const void* const* w13, const void* const* w2, int32_t n_micro, int32_t top_k,
+                            const void* shared_w13, const void* shared_w2, int32_t T, void* y_host,
+                            void* stream) {
+    moe_status st = check_call(h, h ? h->x_stage : nullptr, router_w, T);
+    if (st != MOE_OK) return st;
+    if (T == 0) return MOE_OK;
+    if (x_host == nullptr || y_host == nullptr) return set_err(h, MOE_ERR_INVALID_ARG, "host x and y must be non-null");
+    st = check_weights(h, w13, w2, n_micro, top_k, shared_w13, shared_w2, h->y_stage);
+    if (st != MOE_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    h->last_stream = s;
+    const size_t bytes = (size_t)T * h->cfg.hidden * h->esz;
+    cudaError_t e = cudaMemcpyAsync(h->x_stage, x_host, bytes, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_err(h, e, "copy x to device");
+    st = run_forward(h, h->x_stage, router_w, router_bias, w13, w2, shared_w13, shared_w2, T, h->y_stage, s);
+    end_call(h);
+    if (st != MOE_OK) return st;
+    if ((e = cudaMemcpyAsync(y_host, h->y_stage, bytes, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+        return cuda_err(h, e, "copy y to host");
+    if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_err(h, e, "stream synchronize");
+    return MOE_OK;
+}
+
+moe_status moe_sync(moe_handle* h) {
+    if (h == nullptr) return MOE_ERR_INVALID_ARG;
+    if (h->sticky) return set_err(h, MOE_ERR_STICKY, "handle is sticky after an earlier device error");
+    cudaError_t e = cudaStreamSynchronize(h->last_stream);
+    if (e != cudaSuccess) return cuda_err(h, e, "stream synchronize");
+    int word = 0;
+    if ((e = cudaMemcpy(&word, h->err, sizeof word, cudaMemcpyDeviceToHost)) != cudaSuccess)
+        return cuda_err(h, e, "read device error word");
+    if (word & kErrTimeout) {
+        h->sticky = true;
+        return set_err(h, MOE_ERR_TIMEOUT, "a bounded device wait ran out (error word %d)", word);
+    }
+    if (word & kErrCheck) {
+        h->sticky = true;
+        return set_err(h, MOE_ERR_DEVICE_CHECK, "a device-side check failed (error word %d)", word);
+    }
+    return MOE_OK;
+}
+
+const char* moe_last_error(const moe_handle* h) { return h ? h->msg : "null handle"; }
+
+const char* moe_status_string(moe_status s) {
+    switch (s) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+        case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+        case MOE_ERR_OOM: return "MOE_ERR_OOM";
+        case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+        case MOE_ERR_DEVICE_CHECK: return "MOE_ERR_DEVICE_CHECK";
+        case MOE_ERR_STICKY: return "MOE_ERR_STICKY";
+    }
+    return "unknown moe_status";
+}
+
+void* moe_workspace_ptr(const moe_handle* h, int32_t which) {
+    if (h == nullptr) return nullptr;
+    switch (which) {
+        case 0: return h->xp;
+        case 1: return h->hbuf;
+        case 2: return h->obuf;
+        case 3: return h->inv;
+        case 4: return h->err;
+        default: return nullptr;
+    }
+}
+
+moe_status moe_profile_begin(moe_handle* h, int32_t max_calls) {
+    if (h == nullptr || max_calls <= 0) return MOE_ERR_INVALID_ARG;
+    for (cudaEvent_t ev : h->prof_ev) cudaEventDestroy(ev);
+    h->prof_ev.assign((size_t)max_calls * MOE_PROFILE_SLOTS * 2, nullptr);
+    h->prof_used.assign((size_t)max_calls * MOE_PROFILE_SLOTS, 0);
+    for (auto& ev : h->prof_ev) {
+        cudaError_t e = cudaEventCreate(&ev);
+        if (e != cudaSuccess) return cuda_err(h, e, "event create");
+    }
+    h->prof_max = max_calls;
+    h->prof_calls = 0;
+    h->prof_on = true;
+    return MOE_OK;
+}
+
+moe_status moe_profile_end(moe_handle* h, float* ms, int32_t* launches) {
+    if (h == nullptr || !h->prof_on) return MOE_ERR_INVALID_ARG;
+    h->prof_on = false;
+    for (int k = 0; k < MOE_PROFILE_SLOTS; ++k) {
+        if (ms) ms[k] = 0.f;
+        if (launches) launches[k] = 0;
+    }
+    for (int c = 0; c < h->prof_calls; ++c)
+        for (int k = 0; k < MOE_PROFILE_SLOTS; ++k) {
+            const size_t i = (size_t)c * MOE_PROFILE_SLOTS + k;
+            if (!h->prof_used[i]) continue;
+            cudaError_t e = cudaEventSynchronize(h->prof_ev[2 * i + 1]);
+            float t = 0.f;
+            if (e == cudaSuccess) e = cudaEventElapsedTime(&t, h->prof_ev[2 * i], h->prof_ev[2 * i + 1]);
+            if (e != cudaSuccess) return cuda_err(h, e, "event elapsed time");
+            if (ms) ms[k] += t;
+            if (launches) launches[k] += 1;
+        }
+    return MOE_OK;
+}
+
+int64_t moe_launch_count(const moe_handle* h) { return h ? h->launches : 0; }
+
+moe_status moe_selftest_wait_timeout(int32_t timeout_us, void* stream) {
+    if (timeout_us <= 0) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int* d = nullptr;
+    if (cudaMalloc(&d, sizeof(int)) != cudaSuccess) return MOE_ERR_OOM;
+    int word = 0;
+    cudaError_t e = cudaMemsetAsync(d, 0, sizeof(int), s);
+    if (e == cudaSuccess) e = launch_wait_selftest(d, (uint64_t)timeout_us * 1000ull, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&word, d, sizeof(int), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    cudaFree(d);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    return (word & kErrTimeout) ? MOE_ERR_TIMEOUT : MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,142 @@
+"""The whole layer (moe_forward) against the fp64 oracle.
+
+Small shapes are compared on every token; the five workloads at full size on a
+sample of tokens (the oracle evaluates the per-token definition for those).
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import parity
+from mixture_experts_layer_warp_gb300 import binding
+from mixture_experts_layer_warp_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+TAU = 2e-6
+
+
+def _layer(wl: W.Workload, T=None):
+    return binding.MoELayer(wl.H, wl.E, wl.k, wl.I, wl.n_micro, max_tokens=T or wl.T,
+                            shared_inter=wl.shared_inter, dtype=wl.torch_dtype)
+
+
+def _forward(layer, dev):
+    y = layer.forward(dev["x"], dev["router_w"], dev["router_bias"], dev["w13"], dev["w2"],
+                      dev["shared_w13"], dev["shared_w2"])
+    layer.sync()
+    return y
+
+
+def _check(wl, inp, y, rows=None):
+    host = parity.to_host_numpy(inp)
+    orc = parity.oracle_routing(host, wl.k)
+    set_ok, _ = parity.decided(orc["lf"], orc["ids"], TAU if wl.dtype == "bf16" else 0.0)
+    T = host["x"].shape[0]
+    rows = np.arange(T) if rows is None else np.asarray(rows)
+    rows = rows[set_ok[rows]]
+    ref = oracle.forward_tokens(host["x"], orc["ids"], orc["w"], host["w13"], host["w2"], rows,
+                                host["shared_w13"], host["shared_w2"])
+    err = parity.y_error(y, ref, rows)
+    assert err <= parity.Y_TOL[wl.dtype], f"{wl.name}: rel err {err:.3e}"
+    return err
+
+
+SMALL = [
+    W.Workload("bf16_two_micro", 300, 256, 8, 2, 128, 2),
+    W.Workload("bf16_one_token", 1, 256, 8, 2, 128, 1),
+    W.Workload("bf16_e64_k8_ragged", 129, 512, 64, 8, 256, 1),
+    W.Workload("bf16_shared", 257, 256, 16, 4, 128, 2, shared_inter=256),
+    W.Workload("bf16_four_micro", 70, 512, 8, 3, 128, 4),
+    W.Workload("bf16_skew_bias", 600, 256, 64, 8, 128, 1, router_bias="log_zipf"),
+    W.Workload("f32_tiny_multi_shared", 45, 128, 4, 2, 64, 2, shared_inter=64, dtype="f32"),
+    W.WORKLOADS["tiny_fp32"],
+]
+
+
+@pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
+def test_small_layer_matches_oracle_on_every_token(wl):
+    inp = W.make_inputs(wl, seed=1)
+    layer = _layer(wl)
+    y = _forward(layer, parity.to_device(inp))
+    err = _check(wl, inp, y)
+    print(f"{wl.name}: rel err {err:.3e}")
+    layer.close()
+
+
+@pytest.mark.parametrize("name", ["decode", "denoise_multi_micro", "skewed", "cfg_shared"])
+def test_workload_matches_oracle_on_sampled_tokens(name):
+    wl = W.WORKLOADS[name]
+    inp = W.make_inputs(wl, seed=0, device="cuda")
+    layer = _layer(wl)
+    y = _forward(layer, inp)
+    rng = np.random.default_rng(0)
+    rows = np.unique(np.concatenate([[0, wl.T - 1], rng.integers(0, wl.T, 30)]))
+    err = _check(wl, inp, y, rows)
+    print(f"{name}: rel err {err:.3e} on {rows.size} tokens")
+    layer.close()
+
+
+def test_bitwise_deterministic_across_calls():
+    wl = W.Workload("det", 513, 512, 64, 8, 256, 2, shared_inter=128)
+    dev = parity.to_device(W.make_inputs(wl, seed=2))
+    layer = _layer(wl)
+    a = _forward(layer, dev).clone()
+    b = _forward(layer, dev)
+    assert torch.equal(a, b)
+    layer.close()
+
+
+def test_two_dispatches_sum_to_the_multi_micro_call():
+    """Two single-micro calls summed equal one multi-micro call ("HunyuanImage3
+    Hybrid Parallelism", section 10.3), up to the bf16 rounding of y."""
+    wl = W.Workload("mm", 200, 256, 8, 2, 128, 2)
+    dev = parity.to_device(W.make_inputs(wl, seed=3))
+    both = _forward(_layer(wl), dev).float()
+    one = W.Workload("m1", 200, 256, 8, 2, 128, 1)
+    y0 = _forward(_layer(one), dict(dev, w13=dev["w13"][:1], w2=dev["w2"][:1])).float()
+    y1 = _forward(_layer(one), dict(dev, w13=dev["w13"][1:], w2=dev["w2"][1:])).float()
+    err = ((y0 + y1) - both).abs().max().item() / both.abs().max().item()
+    assert err < 1e-2
+
+
+def test_host_entry_point_matches_device_entry_point():
+    wl = W.Workload("host", 100, 256, 8, 2, 128, 1)
+    inp = W.make_inputs(wl, seed=4)
+    dev = parity.to_device(inp)
+    layer = _layer(wl)
+    y_dev = _forward(layer, dev).cpu()
+    y_host = layer.forward_host(inp["x"].pin_memory(), dev["router_w"], None, dev["w13"], dev["w2"])
+    assert torch.equal(y_dev, y_host)
+    layer.close()
+
+
+def test_invalid_arguments_are_rejected_without_poisoning_the_handle():
+    wl = W.Workload("args", 16, 256, 8, 2, 128, 2)
+    dev = parity.to_device(W.make_inputs(wl, seed=5))
+    layer = _layer(wl)
+    lib = binding.load()
+    p13 = (ctypes.c_void_p * 2)(*[t.data_ptr() for t in dev["w13"]])
+    p2 = (ctypes.c_void_p * 2)(*[t.data_ptr() for t in dev["w2"]])
+    y = torch.empty((16, 256), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    args = [layer._h, dev["x"].data_ptr(), dev["router_w"].data_ptr(), None, p13, p2, 2, 2, None, None, 16,
+            y.data_ptr(), s]
+    assert lib.moe_forward(*args) == 0
+    for i, v in [(6, 1), (7, 3), (10, 17), (10, -1), (11, y.data_ptr() + 2), (1, dev["x"].data_ptr() + 8),
+                 (8, dev["w13"][0].data_ptr())]:
+        bad = list(args)
+        bad[i] = v
+        assert lib.moe_forward(*bad) == 1, (i, v)
+    assert lib.moe_forward(*args) == 0
+    layer.sync()
+    layer.close()
+
+
+def test_bounded_wait_reports_timeout_instead_of_hanging():
+    assert binding.selftest_wait_timeout(2000) == "MOE_ERR_TIMEOUT"
+    # the context is still usable afterwards
+    x = torch.ones(4, device="cuda")
+    assert x.sum().item() == 4.0
