@@ -183,6 +183,34 @@ moe_status moe_profile_end(moe_handle *h, float *ms /* [MOE_PROFILE_SLOTS] */,
 int64_t moe_launch_count(const moe_handle *h);
 
 /*
+ * Routing for callers that cannot allocate device memory. The pages have no
+ * counterpart to this entry point: it exists for programs whose device heap
+ * belongs to a pooling allocator with a fixed budget, or whose hot path must
+ * not take the implicit device synchronisation of cudaMalloc. It computes the
+ * same topk_ids, topk_w, perm and offsets as moe_route (same kernels, same
+ * bits) without a handle: its intermediate data lives in one file-scope
+ * device array of the library (about 1.3 MB, held on every GPU that loads the
+ * library until the process exits). It calls no cudaMalloc/cudaFree.
+ *   x [T][hidden], router_w [num_experts][hidden] in `dtype`; router_bias fp32
+ *   [num_experts] or NULL; outputs as in moe_route (all four required; logits
+ *   are not produced).
+ *   0 <= T <= MOE_ROUTE_NOALLOC_MAX_TOKENS, hidden % 32 == 0,
+ *   1 <= num_experts <= 64, 1 <= top_k <= min(num_experts, 16); anything else,
+ *   or a null or misaligned pointer, returns MOE_ERR_INVALID_ARG.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture. Every call shares the array and overwrites what the previous call
+ * left there, so calls that overlap on the GPU race: order them (one stream).
+ * Device-side check failures are recorded only in the array's error word and
+ * are not reported by this entry point.
+ */
+#define MOE_ROUTE_NOALLOC_MAX_TOKENS 16384
+moe_status moe_route_noalloc(const void *x, const void *router_w, const float *router_bias,
+                             int32_t T, int32_t hidden, int32_t num_experts, int32_t top_k,
+                             int32_t dtype, int32_t *topk_ids, float *topk_w, int32_t *perm,
+                             int32_t *offsets, void *stream);
+
+/*
  * Self-test of the bounded device-side wait: launches one block whose thread
  * waits on an mbarrier that nothing completes, with a limit of `timeout_us`
  * microseconds, then returns the status the kernel reported (expected:

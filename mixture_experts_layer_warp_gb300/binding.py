@@ -70,6 +70,7 @@ def load() -> ctypes.CDLL:
         "moe_profile_begin": (st, [p, i32]),
         "moe_profile_end": (st, [p, p, p]),
         "moe_launch_count": (ctypes.c_int64, [p]),
+        "moe_route_noalloc": (st, [p, p, p, i32, i32, i32, i32, i32, p, p, p, p, p]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
