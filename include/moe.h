@@ -194,7 +194,7 @@ int64_t moe_launch_count(const moe_handle *h);
  *   x [T][hidden], router_w [num_experts][hidden] in `dtype`; router_bias fp32
  *   [num_experts] or NULL; outputs as in moe_route (all four required; logits
  *   are not produced).
- *   0 <= T <= MOE_ROUTE_NOALLOC_MAX_TOKENS, hidden % 32 == 0,
+ *   0 <= T <= MOE_ROUTE_NOALLOC_MAX_TOKENS, hidden % 64 == 0 (bf16) or % 32 (fp32),
  *   1 <= num_experts <= 64, 1 <= top_k <= min(num_experts, 16); anything else,
  *   or a null or misaligned pointer, returns MOE_ERR_INVALID_ARG.
  * The first call on a device looks up the array's device address (once per

@@ -8,7 +8,8 @@
 // each route contributes one row o[inv[t*k + j]]. The shared expert's output
 // (Ascend Hunyuan Image 3.0 guide, section 3.1) is added unscaled.
 //
-// HBM-bound: one block per token, 16-byte vector loads of the k expert rows.
+// HBM-bound: one block per (token, 1024-column chunk), 16-byte vector loads
+// of the k expert rows.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -66,7 +67,8 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(FinalizeArgs a) {
     const T* sh = static_cast<const T*>(a.shared);
     T* y = static_cast<T*>(a.y);
     const int nv = a.H / 8;
-    for (int v = threadIdx.x; v < nv; v += kThreads) {
+    const int v = blockIdx.y * kThreads + threadIdx.x;  // one 8-element vector per thread
+    if (v < nv) {
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         for (int j = 0; j < a.k; ++j) {
             float val[8];
@@ -89,10 +91,11 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(FinalizeArgs a) {
 
 cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t s) {
     if (a.T == 0) return cudaSuccess;
+    const dim3 grid(a.T, (a.H / 8 + kThreads - 1) / kThreads);
     if (a.bf16)
-        finalize_kernel<__nv_bfloat16><<<a.T, kThreads, 0, s>>>(a);
+        finalize_kernel<__nv_bfloat16><<<grid, kThreads, 0, s>>>(a);
     else
-        finalize_kernel<float><<<a.T, kThreads, 0, s>>>(a);
+        finalize_kernel<float><<<grid, kThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 

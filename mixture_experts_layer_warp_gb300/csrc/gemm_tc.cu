@@ -18,15 +18,15 @@
 //       per-micro partial outputs of the pages never exist and the fp32 sum
 //       over micros happens inside the tensor core.
 //
-// Structure: persistent CTAs (one per SM), static round-robin over tiles whose
-// order keeps the m-tiles of one (expert, n-tile) adjacent so concurrent CTAs
-// share each weight tile through L2. 8 warps: warp 0 issues TMA loads into a
+// Structure: persistent CTAs (one per SM), static round-robin over tiles (see
+// decode_tile for their order). 8 warps: warp 0 issues TMA loads into a
 // 4-stage ring (128B-swizzled K-major tiles), warp 1 issues tcgen05.mma into
 // one of two TMEM accumulators (2 x 256 fp32 columns), warp 2 owns the TMEM
 // allocation, warps 4-7 drain an accumulator (one TMEM lane quarter each)
 // while the next tile accumulates into the other. All waits are bounded.
 #include <cuda_bf16.h>
 
+#include "gemm_common.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -57,49 +57,10 @@ struct Ctl {
 
 constexpr int kSmemBytes = kStages * kStageBytes + (int)sizeof(Ctl) + 1024;
 
-struct Tile {
-    int m, g, nt, row0, row_end;
-};
-
 template <bool SWIGLU>
 __device__ __forceinline__ Tile decode_tile(int tile, const Ctl& c, const TcGemmArgs& a) {
-    Tile t;
-    const int per_micro = c.tiles[a.G] * a.n_tiles;
-    int rem = tile;
-    t.m = 0;
-    if (SWIGLU) {
-        t.m = tile / per_micro;
-        rem = tile - t.m * per_micro;
-    }
-    int lo = 0, hi = a.G - 1;  // largest g with tiles[g] * n_tiles <= rem
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (c.tiles[mid] * a.n_tiles <= rem)
-            lo = mid;
-        else
-            hi = mid - 1;
-    }
-    t.g = lo;
-    const int local = rem - c.tiles[lo] * a.n_tiles;
-    const int mtiles = c.tiles[lo + 1] - c.tiles[lo];
-    t.nt = local / mtiles;
-    const int mt = local - t.nt * mtiles;
-    t.row0 = c.seg[lo] + mt * kTcBM;
-    t.row_end = c.seg[lo + 1];
-    return t;
+    return decode_group_tile(tile, c.seg, c.tiles, a.G, a.n_tiles, a.n_micro, SWIGLU, kTcBM);
 }
-
-__device__ __forceinline__ const CUtensorMap* pick(int m, const CUtensorMap& b0, const CUtensorMap& b1,
-                                                   const CUtensorMap& b2, const CUtensorMap& b3) {
-    return m == 0 ? &b0 : m == 1 ? &b1 : m == 2 ? &b2 : &b3;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
-}
-
-__device__ __forceinline__ float silu(float z) { return z / (1.f + __expf(-z)); }
 
 __device__ __forceinline__ void fail(Ctl& c, int* err) {
     c.abort = 1;
@@ -161,7 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const Tile t = decode_tile<SWIGLU>(tile, c, a);
             for (int mi = 0; ok && mi < n_micro_k; ++mi) {
                 const int m = SWIGLU ? t.m : mi;
-                const CUtensorMap* tb = pick(m, tmB0, tmB1, tmB2, tmB3);
+                const CUtensorMap* tb = pick_map(m, tmB0, tmB1, tmB2, tmB3);
                 const int brow = t.g * a.b_rows_per_group + t.nt * (SWIGLU ? 128 : kBN);
                 const int brow2 = brow + (SWIGLU ? a.up_offset : 128);
                 for (int kb = 0; kb < a.k_blocks; ++kb) {

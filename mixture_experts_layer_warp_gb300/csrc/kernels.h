@@ -20,8 +20,10 @@ constexpr int kMaxTopK = 16;
 constexpr int kMaxMicro = 4;
 
 // ---------------------------------------------------------------- router
-// One block routes kRouterTokens tokens; its histogram row is blk_hist[block].
+// One block routes kRouterTokens tokens (fp32 SIMT router) or kRouterTokensTc
+// tokens (bf16 tensor-core router); its histogram row is blk_hist[block].
 constexpr int kRouterTokens = 32;
+constexpr int kRouterTokensTc = 128;
 
 struct RouterArgs {
     const void* x;         // [T][H]
@@ -36,6 +38,29 @@ struct RouterArgs {
     int* err;
 };
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t s);
+
+struct RouterTcArgs {
+    const float* bias;      // [E] or null
+    int T, H, E, k;
+    int32_t* ids;           // [T][k]
+    float* w;               // [T][k]
+    float* logits;          // [T][E] or null
+    int32_t* blk_hist;      // [NB][E] (written when more than one CTA)
+    // written only when a single CTA covers all T tokens:
+    int32_t* offsets;       // [E+1]
+    int32_t* tiles_tc;      // [E+1]
+    int32_t* tiles_simt;    // [E+1]
+    int32_t* shared_seg;    // [2]
+    int32_t* shared_tiles_tc;    // [2]
+    int32_t* shared_tiles_simt;  // [2]
+    int32_t* perm;          // [T*k]
+    int32_t* inv;           // [T*k]
+    int* err;
+    uint64_t limit_ns;
+};
+// tmX: x [T][H] bf16, box {64, 128}; tmW: Wr [E][H] bf16, box {64, 64}.
+cudaError_t launch_router_tc(const RouterTcArgs& a, const CUtensorMap& tmX, const CUtensorMap& tmW,
+                             cudaStream_t s);
 
 // --------------------------------------------------------- scan / place
 struct ScanArgs {
@@ -55,6 +80,7 @@ struct PlaceArgs {
     const int32_t* ids;       // [T][k]
     const int32_t* blk_base;  // [NB][E]
     int T, k, E, NB;
+    int tok_per_blk;          // tokens per histogram block (router block size)
     int32_t* perm;            // [T*k]
     int32_t* inv;             // [T*k]
     int* err;
@@ -103,6 +129,17 @@ cudaError_t launch_tc_gemm_swiglu(const TcGemmArgs& a, const CUtensorMap& tmA, c
 cudaError_t launch_tc_gemm_down(const TcGemmArgs& a, const CUtensorMap& tmA, const CUtensorMap* tmB,
                                 int num_sms, cudaStream_t s);
 
+// Swapped-operand variants for batches of at most kSmallTokens tokens (every
+// expert then owns at most kSmallTokens routes): weights on the MMA M side,
+// tokens on N. tmX: activations [rows][K], box {64, 16}; tmW[m]: weights,
+// box {64, 64} (SwiGLU form: gate and up halves) or {64, 128} (down form).
+// n_tiles counts 64 h-columns (SwiGLU) or 128 output columns (down).
+constexpr int kSmallTokens = 16;
+cudaError_t launch_tc_small_swiglu(const TcGemmArgs& a, const CUtensorMap& tmX, const CUtensorMap* tmW,
+                                   int num_sms, cudaStream_t s);
+cudaError_t launch_tc_small_down(const TcGemmArgs& a, const CUtensorMap& tmX, const CUtensorMap* tmW,
+                                 int num_sms, cudaStream_t s);
+
 // ---------------------------------------------------- fp32 SIMT GEMMs
 constexpr int kSimtBM = 32;
 
@@ -137,6 +174,49 @@ struct FinalizeArgs {
     void* y;                  // [T][H]
 };
 cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t s);
+
+// ------------------------------------------------------------- routing
+// The routing sequence shared by moe_route, moe_forward and moe_route_noalloc:
+// bf16 layers use the tensor-core router (one launch when T <= 128, else
+// router + scan + place), fp32 layers the SIMT router + scan + place.
+struct RoutingJob {
+    const void* x;
+    const void* wr;
+    const float* bias;
+    int T, H, E, k;
+    bool bf16;
+    int32_t* ids;
+    float* w;
+    float* logits;            // or null
+    int32_t* perm;
+    int32_t* inv;
+    int32_t* offsets;
+    int32_t* tiles_tc;        // [E+1]
+    int32_t* tiles_simt;      // [E+1]
+    int32_t* shared_meta;     // [6]: shared seg[2], tiles_tc[2], tiles_simt[2]
+    int32_t* blk_hist;        // [ceil(T/kRouterTokens)][E]
+    int32_t* blk_base;        // same
+    int* err;
+    uint64_t limit_ns;
+};
+
+// Optional callbacks around every kernel launch (timing, counting).
+struct LaunchHook {
+    void* ctx;
+    void (*before)(void* ctx, int slot, cudaStream_t s);
+    void (*after)(void* ctx, int slot, cudaStream_t s, cudaError_t e);
+};
+
+enum KernelSlot { kSlotRouter = 0, kSlotScan, kSlotPlace, kSlotGather, kSlotGemm1, kSlotGemm2, kSlotSharedGemm1,
+                  kSlotSharedGemm2, kSlotFinalize, kNumSlots };
+
+// Returns cudaErrorInvalidValue if a tensor map cannot be encoded.
+cudaError_t enqueue_routing(const RoutingJob& j, cudaStream_t s, const LaunchHook* hook);
+
+// 2D bf16 tensor map over a row-major [rows][inner] matrix, box {64, box_rows},
+// 128-byte swizzle: the K-major operand layout of the tcgen05 kernels.
+bool encode_bf16_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
+                    uint32_t box_rows);
 
 // ------------------------------------------------------------ self-test
 cudaError_t launch_wait_selftest(int* err, uint64_t limit_ns, cudaStream_t s);

@@ -17,23 +17,6 @@ using namespace moe;
 
 namespace {
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn get_encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (fn == nullptr) {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    }
-    return fn;
-}
-
 constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s per bounded wait
 
 }  // namespace
@@ -58,9 +41,7 @@ struct moe_handle {
     int32_t* offsets = nullptr;
     int32_t* tiles_tc = nullptr;
     int32_t* tiles_simt = nullptr;
-    int32_t* shared_seg = nullptr;
-    int32_t* shared_tiles_tc = nullptr;
-    int32_t* shared_tiles_simt = nullptr;
+    int32_t* shared_meta = nullptr;  // shared expert: seg[2], tiles_tc[2], tiles_simt[2]
     int32_t* blk_hist = nullptr;
     int32_t* blk_base = nullptr;
     void* xp = nullptr;
@@ -127,35 +108,32 @@ moe_status check_cfg(const moe_config* c, char* msg, size_t n) {
     return MOE_OK;
 }
 
-// 2D bf16 tensor map over a row-major [rows][inner] matrix with a 64 x 128 box
-// and 128-byte swizzling (the K-major operand layout of the tcgen05 kernels).
 bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t row_bytes) {
-    EncodeTiledFn enc = get_encode_fn();
-    if (enc == nullptr) return false;
-    cuuint64_t dims[2] = {inner, rows};
-    cuuint64_t strides[1] = {row_bytes};
-    cuuint32_t box[2] = {(cuuint32_t)kTcBK, (cuuint32_t)kTcBM};
-    cuuint32_t estr[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return encode_bf16_2d(m, base, inner, rows, row_bytes, kTcBM);
 }
 
-enum Slot { kRouter = 0, kScan, kPlace, kGather, kGemm1, kGemm2, kSharedGemm1, kSharedGemm2, kFinalize };
+void hook_before(void* ctx, int slot, cudaStream_t s) {
+    moe_handle* h = static_cast<moe_handle*>(ctx);
+    if (h->prof_on && h->prof_calls < h->prof_max)
+        cudaEventRecord(h->prof_ev[2 * ((size_t)h->prof_calls * MOE_PROFILE_SLOTS + slot)], s);
+}
 
-// Runs one kernel launch, counting it and, while profiling, bracketing it with
-// an event pair on the stream.
-template <typename F>
-cudaError_t timed(moe_handle* h, Slot slot, cudaStream_t s, F&& launch) {
-    const bool rec = h->prof_on && h->prof_calls < h->prof_max;
-    const size_t i = ((size_t)h->prof_calls * MOE_PROFILE_SLOTS + slot);
-    if (rec) cudaEventRecord(h->prof_ev[2 * i], s);
-    cudaError_t e = launch();
-    if (rec) {
+void hook_after(void* ctx, int slot, cudaStream_t s, cudaError_t e) {
+    moe_handle* h = static_cast<moe_handle*>(ctx);
+    if (h->prof_on && h->prof_calls < h->prof_max) {
+        const size_t i = (size_t)h->prof_calls * MOE_PROFILE_SLOTS + slot;
         cudaEventRecord(h->prof_ev[2 * i + 1], s);
         h->prof_used[i] = 1;
     }
     if (e == cudaSuccess) h->launches += 1;
+}
+
+// Runs one kernel launch between the handle's hooks (counting, optional timing).
+template <typename F>
+cudaError_t timed(moe_handle* h, int slot, cudaStream_t s, F&& launch) {
+    hook_before(h, slot, s);
+    cudaError_t e = launch();
+    hook_after(h, slot, s, e);
     return e;
 }
 
@@ -179,16 +157,13 @@ moe_status check_call(moe_handle* h, const void* x, const void* router_w, int32_
 moe_status run_routing(moe_handle* h, const void* x, const void* router_w, const float* bias, int32_t T,
                        float* logits, cudaStream_t s) {
     const moe_config& c = h->cfg;
-    const int NB = (T + kRouterTokens - 1) / kRouterTokens;
-    cudaError_t e;
-    RouterArgs ra{x, router_w, bias, T, c.hidden, c.num_experts, c.top_k, c.dtype == MOE_BF16,
-                  h->ids, h->topw, logits, h->blk_hist, h->err};
-    if ((e = timed(h, kRouter, s, [&] { return launch_router(ra, s); })) != cudaSuccess) return cuda_err(h, e, "router launch");
-    ScanArgs sa{h->blk_hist, NB, c.num_experts, T, c.top_k, h->blk_base, h->offsets, h->tiles_tc,
-                h->tiles_simt, h->shared_seg, h->shared_tiles_tc, h->shared_tiles_simt};
-    if ((e = timed(h, kScan, s, [&] { return launch_scan(sa, s); })) != cudaSuccess) return cuda_err(h, e, "scan launch");
-    PlaceArgs pa{h->ids, h->blk_base, T, c.top_k, c.num_experts, NB, h->perm, h->inv, h->err};
-    if ((e = timed(h, kPlace, s, [&] { return launch_place(pa, s); })) != cudaSuccess) return cuda_err(h, e, "place launch");
+    RoutingJob j{x, router_w, bias, T, c.hidden, c.num_experts, c.top_k, c.dtype == MOE_BF16, h->ids, h->topw,
+                 logits, h->perm, h->inv, h->offsets, h->tiles_tc, h->tiles_simt, h->shared_meta, h->blk_hist,
+                 h->blk_base, h->err, h->limit_ns};
+    LaunchHook hook{h, hook_before, hook_after};
+    cudaError_t e = enqueue_routing(j, s, &hook);
+    if (e == cudaErrorInvalidValue) return set_err(h, MOE_ERR_CUDA, "router tensor map encode failed");
+    if (e != cudaSuccess) return cuda_err(h, e, "routing launch");
     return MOE_OK;
 }
 
@@ -203,10 +178,52 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
     if (st != MOE_OK) return st;
 
     GatherArgs ga{x, h->perm, (int)R, k, (uint32_t)(H * h->esz), h->xp, h->err, h->limit_ns, h->num_sms};
-    if ((e = timed(h, kGather, s, [&] { return launch_gather(ga, s); })) != cudaSuccess) return cuda_err(h, e, "gather launch");
+    if ((e = timed(h, kSlotGather, s, [&] { return launch_gather(ga, s); })) != cudaSuccess) return cuda_err(h, e, "gather launch");
 
     const int routed_tiles_tc = (int)(R / kTcBM) + E;  // bound on sum of ceil(count/128)
-    if (c.dtype == MOE_BF16) {
+    if (c.dtype == MOE_BF16 && T <= kSmallTokens) {
+        // swapped operands: weights on the MMA M side, the <= 16 tokens on N
+        CUtensorMap tmX, tmW[kMaxMicro];
+        const int active = (int)(R < E ? R : E);  // experts that can own routes
+        if (!encode_bf16_2d(&tmX, h->xp, H, R, (uint64_t)H * 2, kSmallTokens))
+            return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (xp)");
+        for (int m = 0; m < M; ++m)
+            if (!encode_bf16_2d(&tmW[m], w13[m], H, (uint64_t)E * 2 * I, (uint64_t)H * 2, 64))
+                return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (w13[%d])", m);
+        TcGemmArgs g1{h->offsets, h->tiles_tc, E, M, H / kTcBK, I / 64, 2 * I, I, 0,
+                      h->hbuf, (int64_t)M * I, I, active * M * (I / 64), h->err, h->limit_ns};
+        if ((e = timed(h, kSlotGemm1, s, [&] { return launch_tc_small_swiglu(g1, tmX, tmW, h->num_sms, s); })) !=
+            cudaSuccess)
+            return cuda_err(h, e, "GEMM1 launch");
+        if (!encode_bf16_2d(&tmX, h->hbuf, (uint64_t)M * I, R, (uint64_t)M * I * 2, kSmallTokens))
+            return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (h)");
+        for (int m = 0; m < M; ++m)
+            if (!encode_bf16_2d(&tmW[m], w2[m], I, (uint64_t)E * H, (uint64_t)I * 2, 128))
+                return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (w2[%d])", m);
+        TcGemmArgs g2{h->offsets, h->tiles_tc, E, M, I / kTcBK, H / 128, H, 0, I,
+                      h->obuf, (int64_t)H, 0, active * (H / 128), h->err, h->limit_ns};
+        if ((e = timed(h, kSlotGemm2, s, [&] { return launch_tc_small_down(g2, tmX, tmW, h->num_sms, s); })) !=
+            cudaSuccess)
+            return cuda_err(h, e, "GEMM2 launch");
+        if (Is > 0) {
+            if (!encode_bf16_2d(&tmX, x, H, T, (uint64_t)H * 2, kSmallTokens) ||
+                !encode_bf16_2d(&tmW[0], sw13, H, 2 * (uint64_t)Is, (uint64_t)H * 2, 64))
+                return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (shared GEMM1)");
+            TcGemmArgs s1{h->shared_meta, h->shared_meta + 2, 1, 1, H / kTcBK, Is / 64, 2 * Is, Is, 0,
+                          h->hs, (int64_t)Is, 0, Is / 64, h->err, h->limit_ns};
+            if ((e = timed(h, kSlotSharedGemm1, s,
+                           [&] { return launch_tc_small_swiglu(s1, tmX, tmW, h->num_sms, s); })) != cudaSuccess)
+                return cuda_err(h, e, "shared GEMM1 launch");
+            if (!encode_bf16_2d(&tmX, h->hs, Is, T, (uint64_t)Is * 2, kSmallTokens) ||
+                !encode_bf16_2d(&tmW[0], sw2, Is, H, (uint64_t)Is * 2, 128))
+                return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (shared GEMM2)");
+            TcGemmArgs s2{h->shared_meta, h->shared_meta + 2, 1, 1, Is / kTcBK, H / 128, H, 0, Is,
+                          h->sbuf, (int64_t)H, 0, H / 128, h->err, h->limit_ns};
+            if ((e = timed(h, kSlotSharedGemm2, s,
+                           [&] { return launch_tc_small_down(s2, tmX, tmW, h->num_sms, s); })) != cudaSuccess)
+                return cuda_err(h, e, "shared GEMM2 launch");
+        }
+    } else if (c.dtype == MOE_BF16) {
         CUtensorMap tmA, tmB[kMaxMicro];
         // GEMM1 + SwiGLU: xp [R][H] x w13[m] [E*2I][H] -> h [R][M*I]
         if (!encode_2d(&tmA, h->xp, H, R, (uint64_t)H * 2))
@@ -216,7 +233,7 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
                 return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (w13[%d])", m);
         TcGemmArgs g1{h->offsets, h->tiles_tc, E, M, H / kTcBK, I / 128, 2 * I, I, 0,
                       h->hbuf, (int64_t)M * I, I, M * routed_tiles_tc * (I / 128), h->err, h->limit_ns};
-        if ((e = timed(h, kGemm1, s, [&] { return launch_tc_gemm_swiglu(g1, tmA, tmB, h->num_sms, s); })) != cudaSuccess)
+        if ((e = timed(h, kSlotGemm1, s, [&] { return launch_tc_gemm_swiglu(g1, tmA, tmB, h->num_sms, s); })) != cudaSuccess)
             return cuda_err(h, e, "GEMM1 launch");
         // GEMM2: h [R][M*I] x w2[m] [E*H][I], summed over m -> o [R][H]
         if (!encode_2d(&tmA, h->hbuf, (uint64_t)M * I, R, (uint64_t)M * I * 2))
@@ -226,21 +243,21 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
                 return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (w2[%d])", m);
         TcGemmArgs g2{h->offsets, h->tiles_tc, E, M, I / kTcBK, H / 256, H, 0, I,
                       h->obuf, (int64_t)H, 0, routed_tiles_tc * (H / 256), h->err, h->limit_ns};
-        if ((e = timed(h, kGemm2, s, [&] { return launch_tc_gemm_down(g2, tmA, tmB, h->num_sms, s); })) != cudaSuccess)
+        if ((e = timed(h, kSlotGemm2, s, [&] { return launch_tc_gemm_down(g2, tmA, tmB, h->num_sms, s); })) != cudaSuccess)
             return cuda_err(h, e, "GEMM2 launch");
         if (Is > 0) {
             const int stiles = (T + kTcBM - 1) / kTcBM;
             if (!encode_2d(&tmA, x, H, T, (uint64_t)H * 2) || !encode_2d(&tmB[0], sw13, H, 2 * (uint64_t)Is, (uint64_t)H * 2))
                 return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (shared GEMM1)");
-            TcGemmArgs s1{h->shared_seg, h->shared_tiles_tc, 1, 1, H / kTcBK, Is / 128, 2 * Is, Is, 0,
+            TcGemmArgs s1{h->shared_meta, h->shared_meta + 2, 1, 1, H / kTcBK, Is / 128, 2 * Is, Is, 0,
                           h->hs, (int64_t)Is, 0, stiles * (Is / 128), h->err, h->limit_ns};
-            if ((e = timed(h, kSharedGemm1, s, [&] { return launch_tc_gemm_swiglu(s1, tmA, tmB, h->num_sms, s); })) != cudaSuccess)
+            if ((e = timed(h, kSlotSharedGemm1, s, [&] { return launch_tc_gemm_swiglu(s1, tmA, tmB, h->num_sms, s); })) != cudaSuccess)
                 return cuda_err(h, e, "shared GEMM1 launch");
             if (!encode_2d(&tmA, h->hs, Is, T, (uint64_t)Is * 2) || !encode_2d(&tmB[0], sw2, Is, H, (uint64_t)Is * 2))
                 return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (shared GEMM2)");
-            TcGemmArgs s2{h->shared_seg, h->shared_tiles_tc, 1, 1, Is / kTcBK, H / 256, H, 0, Is,
+            TcGemmArgs s2{h->shared_meta, h->shared_meta + 2, 1, 1, Is / kTcBK, H / 256, H, 0, Is,
                           h->sbuf, (int64_t)H, 0, stiles * (H / 256), h->err, h->limit_ns};
-            if ((e = timed(h, kSharedGemm2, s, [&] { return launch_tc_gemm_down(s2, tmA, tmB, h->num_sms, s); })) != cudaSuccess)
+            if ((e = timed(h, kSlotSharedGemm2, s, [&] { return launch_tc_gemm_down(s2, tmA, tmB, h->num_sms, s); })) != cudaSuccess)
                 return cuda_err(h, e, "shared GEMM2 launch");
         }
     } else {
@@ -261,7 +278,7 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
         g1.out_ld = (int64_t)M * I;
         g1.out_micro_cols = I;
         g1.max_tiles = routed_tiles;
-        if ((e = timed(h, kGemm1, s, [&] { return launch_simt_gemm_swiglu(g1, s); })) != cudaSuccess) return cuda_err(h, e, "f32 GEMM1 launch");
+        if ((e = timed(h, kSlotGemm1, s, [&] { return launch_simt_gemm_swiglu(g1, s); })) != cudaSuccess) return cuda_err(h, e, "f32 GEMM1 launch");
         SimtGemmArgs g2 = g1;
         g2.a = static_cast<const float*>(h->hbuf);
         g2.lda = (int64_t)M * I;
@@ -273,13 +290,13 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
         g2.out = static_cast<float*>(h->obuf);
         g2.out_ld = H;
         g2.out_micro_cols = 0;
-        if ((e = timed(h, kGemm2, s, [&] { return launch_simt_gemm_down(g2, s); })) != cudaSuccess) return cuda_err(h, e, "f32 GEMM2 launch");
+        if ((e = timed(h, kSlotGemm2, s, [&] { return launch_simt_gemm_down(g2, s); })) != cudaSuccess) return cuda_err(h, e, "f32 GEMM2 launch");
         if (Is > 0) {
             SimtGemmArgs s1{};
             s1.a = static_cast<const float*>(x);
             s1.lda = H;
-            s1.seg = h->shared_seg;
-            s1.tiles = h->shared_tiles_simt;
+            s1.seg = h->shared_meta;
+            s1.tiles = h->shared_meta + 4;
             s1.G = 1;
             s1.n_micro = 1;
             s1.b[0] = static_cast<const float*>(sw13);
@@ -289,7 +306,7 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
             s1.out = static_cast<float*>(h->hs);
             s1.out_ld = Is;
             s1.max_tiles = (T + kSimtBM - 1) / kSimtBM;
-            if ((e = timed(h, kSharedGemm1, s, [&] { return launch_simt_gemm_swiglu(s1, s); })) != cudaSuccess) return cuda_err(h, e, "f32 shared GEMM1");
+            if ((e = timed(h, kSlotSharedGemm1, s, [&] { return launch_simt_gemm_swiglu(s1, s); })) != cudaSuccess) return cuda_err(h, e, "f32 shared GEMM1");
             SimtGemmArgs s2 = s1;
             s2.a = static_cast<const float*>(h->hs);
             s2.lda = Is;
@@ -300,11 +317,11 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
             s2.a_micro_cols = Is;
             s2.out = static_cast<float*>(h->sbuf);
             s2.out_ld = H;
-            if ((e = timed(h, kSharedGemm2, s, [&] { return launch_simt_gemm_down(s2, s); })) != cudaSuccess) return cuda_err(h, e, "f32 shared GEMM2");
+            if ((e = timed(h, kSlotSharedGemm2, s, [&] { return launch_simt_gemm_down(s2, s); })) != cudaSuccess) return cuda_err(h, e, "f32 shared GEMM2");
         }
     }
     FinalizeArgs fa{h->obuf, h->inv, h->topw, Is > 0 ? h->sbuf : nullptr, T, k, H, c.dtype == MOE_BF16, y};
-    if ((e = timed(h, kFinalize, s, [&] { return launch_finalize(fa, s); })) != cudaSuccess) return cuda_err(h, e, "finalize launch");
+    if ((e = timed(h, kSlotFinalize, s, [&] { return launch_finalize(fa, s); })) != cudaSuccess) return cuda_err(h, e, "finalize launch");
     return MOE_OK;
 }
 
@@ -354,7 +371,7 @@ moe_status moe_create(const moe_config* cfg, moe_handle** out) {
     if (cfg->dtype == MOE_BF16) {
         int major = 0;
         cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, h->device);
-        if (major != 10 || get_encode_fn() == nullptr) {
+        if (major != 10) {
             delete h;
             return MOE_ERR_UNSUPPORTED;
         }
@@ -372,7 +389,7 @@ moe_status moe_create(const moe_config* cfg, moe_handle** out) {
     const size_t o_err = take(sizeof(int));
     const size_t o_ids = take(R * 4), o_topw = take(R * 4), o_perm = take(R * 4), o_inv = take(R * 4);
     const size_t o_off = take((E + 1) * 4), o_ttc = take((E + 1) * 4), o_tsi = take((E + 1) * 4);
-    const size_t o_sseg = take(8), o_sttc = take(8), o_stsi = take(8);
+    const size_t o_smeta = take(6 * 4);
     const size_t o_hist = take(NB * E * 4), o_base = take(NB * E * 4);
     const size_t o_xp = take(R * H * esz), o_h = take(R * M * I * esz), o_o = take(R * H * esz);
     const size_t o_hs = take(T * Is * esz), o_s = take(Is ? T * H * esz : 0);
@@ -392,9 +409,7 @@ moe_status moe_create(const moe_config* cfg, moe_handle** out) {
     h->offsets = reinterpret_cast<int32_t*>(b + o_off);
     h->tiles_tc = reinterpret_cast<int32_t*>(b + o_ttc);
     h->tiles_simt = reinterpret_cast<int32_t*>(b + o_tsi);
-    h->shared_seg = reinterpret_cast<int32_t*>(b + o_sseg);
-    h->shared_tiles_tc = reinterpret_cast<int32_t*>(b + o_sttc);
-    h->shared_tiles_simt = reinterpret_cast<int32_t*>(b + o_stsi);
+    h->shared_meta = reinterpret_cast<int32_t*>(b + o_smeta);
     h->blk_hist = reinterpret_cast<int32_t*>(b + o_hist);
     h->blk_base = reinterpret_cast<int32_t*>(b + o_base);
     h->xp = b + o_xp;

@@ -69,7 +69,7 @@ extern "C" moe_status moe_route_noalloc(const void* x, const void* router_w, con
                                         int32_t hidden, int32_t num_experts, int32_t top_k, int32_t dtype,
                                         int32_t* topk_ids, float* topk_w, int32_t* perm, int32_t* offsets,
                                         void* stream) {
-    if (T < 0 || T > kMaxTokens || hidden <= 0 || hidden % 32 != 0 || num_experts <= 0 ||
+    if (T < 0 || T > kMaxTokens || hidden <= 0 || hidden % (dtype == MOE_BF16 ? 64 : 32) != 0 || num_experts <= 0 ||
         num_experts > kMaxExperts || top_k <= 0 || top_k > num_experts || top_k > kMaxTopK ||
         (dtype != MOE_F32 && dtype != MOE_BF16))
         return MOE_ERR_INVALID_ARG;
@@ -93,14 +93,9 @@ extern "C" moe_status moe_route_noalloc(const void* x, const void* router_w, con
     int32_t* tiles_tc = reinterpret_cast<int32_t*>(b + kTilesTcOff);
     int32_t* tiles_simt = reinterpret_cast<int32_t*>(b + kTilesSimtOff);
     int32_t* shared = reinterpret_cast<int32_t*>(b + kSharedOff);
-    const int NB = (T + kRouterTokens - 1) / kRouterTokens;
-    RouterArgs ra{x, router_w, router_bias, T, hidden, num_experts, top_k, dtype == MOE_BF16,
-                  topk_ids, topk_w, nullptr, hist, err};
-    if (launch_router(ra, s) != cudaSuccess) return MOE_ERR_CUDA;
-    ScanArgs sa{hist, NB, num_experts, T, top_k, blk_base, offsets, tiles_tc, tiles_simt, shared, shared + 2,
-                shared + 4};
-    if (launch_scan(sa, s) != cudaSuccess) return MOE_ERR_CUDA;
-    PlaceArgs pa{topk_ids, blk_base, T, top_k, num_experts, NB, perm, inv, err};
-    if (launch_place(pa, s) != cudaSuccess) return MOE_ERR_CUDA;
+    RoutingJob j{x, router_w, router_bias, T, hidden, num_experts, top_k, dtype == MOE_BF16, topk_ids, topk_w,
+                 nullptr, perm, inv, offsets, tiles_tc, tiles_simt, shared, hist, blk_base, err,
+                 2000000000ull};
+    if (enqueue_routing(j, s, nullptr) != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_OK;
 }

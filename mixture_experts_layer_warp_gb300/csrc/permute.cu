@@ -5,15 +5,17 @@
 // gives the expert offsets, and the input is index_select-ed once by the
 // permutation; section 6.2 lists the permutation inverse. Here the sort is a
 // deterministic counting sort without atomics on the output order:
-//   router block b owns routes [b*32k, (b+1)*32k) and wrote its histogram row;
+//   router block b owns routes [b*n*k, (b+1)*n*k) (n tokens per router block)
+//   and wrote its histogram row;
 //   scan:  offsets[e] = sum of all counts of experts < e, and
 //          base[b][e] = offsets[e] + counts of expert e in blocks < b;
-//   place: block b walks its routes in order and gives the n-th route of
-//          expert e the position base[b][e] + n.
+//   place: block b walks its routes in order and gives the i-th route of
+//          expert e the position base[b][e] + i (warp rounds, place.cuh).
 // So within an expert the routes keep ascending r = t*k + j (a stable sort).
 #include <algorithm>
 
 #include "kernels.h"
+#include "place.cuh"
 #include "ptx.cuh"
 
 namespace moe {
@@ -77,27 +79,20 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
     }
 }
 
-__global__ void __launch_bounds__(kMaxExperts) place_kernel(PlaceArgs a) {
-    __shared__ int sid[kRouterTokens * kMaxTopK];
+constexpr int kPlaceWarps = 8;
+
+__global__ void __launch_bounds__(kPlaceWarps * 32) place_kernel(PlaceArgs a) {
+    __shared__ int sid[kRouterTokensTc * kMaxTopK];
+    __shared__ int cnt[kPlaceWarps][kMaxExperts];
+    __shared__ int run[kPlaceWarps][kMaxExperts];
     const int64_t R = (int64_t)a.T * a.k;
-    const int64_t r0 = (int64_t)blockIdx.x * kRouterTokens * a.k;
+    const int64_t r0 = (int64_t)blockIdx.x * a.tok_per_blk * a.k;
     const int64_t left = R - r0;
-    const int n = (int)(left < (int64_t)kRouterTokens * a.k ? left : (int64_t)kRouterTokens * a.k);
+    const int n = (int)(left < (int64_t)a.tok_per_blk * a.k ? left : (int64_t)a.tok_per_blk * a.k);
     for (int i = threadIdx.x; i < n; i += blockDim.x) sid[i] = a.ids[r0 + i];
     __syncthreads();
-    const int e = threadIdx.x;
-    if (e >= a.E) return;
-    int pos = a.blk_base[(int64_t)blockIdx.x * a.E + e];
-    for (int i = 0; i < n; ++i) {
-        if (sid[i] != e) continue;
-        if (pos < 0 || pos >= R) {
-            atomicOr(a.err, kErrCheck);
-            return;
-        }
-        a.perm[pos] = (int32_t)(r0 + i);
-        a.inv[r0 + i] = pos;
-        ++pos;
-    }
+    const int32_t* base = a.blk_base + (int64_t)blockIdx.x * a.E;
+    place_chunk<kPlaceWarps>(sid, n, r0, a.E, R, [&](int e) { return base[e]; }, cnt, run, a.perm, a.inv, a.err);
 }
 
 // Gather xp[i] = x[perm[i] / k]: each single-warp block moves one row chunk
@@ -152,7 +147,7 @@ cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s) {
 
 cudaError_t launch_place(const PlaceArgs& a, cudaStream_t s) {
     if (a.NB == 0) return cudaSuccess;
-    place_kernel<<<a.NB, kMaxExperts, 0, s>>>(a);
+    place_kernel<<<a.NB, kPlaceWarps * 32, 0, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -1,0 +1,77 @@
+// routing.cu - the routing launch sequence and tensor-map encoding shared by
+// every entry point that routes (moe_route, moe_forward, moe_route_noalloc).
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (fn == nullptr) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+template <typename F>
+cudaError_t hooked(const LaunchHook* hook, int slot, cudaStream_t s, F&& launch) {
+    if (hook && hook->before) hook->before(hook->ctx, slot, s);
+    cudaError_t e = launch();
+    if (hook && hook->after) hook->after(hook->ctx, slot, s, e);
+    return e;
+}
+
+}  // namespace
+
+bool encode_bf16_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
+                    uint32_t box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (enc == nullptr) return false;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {(cuuint32_t)kTcBK, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t enqueue_routing(const RoutingJob& j, cudaStream_t s, const LaunchHook* hook) {
+    cudaError_t e;
+    int NB, tpb;
+    if (j.bf16) {
+        CUtensorMap tmX, tmW;
+        if (!encode_bf16_2d(&tmX, j.x, j.H, j.T, (uint64_t)j.H * 2, kRouterTokensTc) ||
+            !encode_bf16_2d(&tmW, j.wr, j.H, j.E, (uint64_t)j.H * 2, 64))
+            return cudaErrorInvalidValue;
+        RouterTcArgs ra{j.bias, j.T, j.H, j.E, j.k, j.ids, j.w, j.logits, j.blk_hist, j.offsets, j.tiles_tc,
+                        j.tiles_simt, j.shared_meta, j.shared_meta + 2, j.shared_meta + 4, j.perm, j.inv, j.err,
+                        j.limit_ns};
+        if ((e = hooked(hook, kSlotRouter, s, [&] { return launch_router_tc(ra, tmX, tmW, s); })) != cudaSuccess)
+            return e;
+        tpb = kRouterTokensTc;
+        NB = (j.T + tpb - 1) / tpb;
+        if (NB <= 1) return cudaSuccess;  // the single CTA also scanned and placed
+    } else {
+        tpb = kRouterTokens;
+        NB = (j.T + tpb - 1) / tpb;
+        RouterArgs ra{j.x, j.wr, j.bias, j.T, j.H, j.E, j.k, false, j.ids, j.w, j.logits, j.blk_hist, j.err};
+        if ((e = hooked(hook, kSlotRouter, s, [&] { return launch_router(ra, s); })) != cudaSuccess) return e;
+    }
+    ScanArgs sa{j.blk_hist, NB, j.E, j.T, j.k, j.blk_base, j.offsets, j.tiles_tc, j.tiles_simt, j.shared_meta,
+                j.shared_meta + 2, j.shared_meta + 4};
+    if ((e = hooked(hook, kSlotScan, s, [&] { return launch_scan(sa, s); })) != cudaSuccess) return e;
+    PlaceArgs pa{j.ids, j.blk_base, j.T, j.k, j.E, NB, tpb, j.perm, j.inv, j.err};
+    return hooked(hook, kSlotPlace, s, [&] { return launch_place(pa, s); });
+}
+
+}  // namespace moe

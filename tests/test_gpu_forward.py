@@ -15,7 +15,7 @@ from mixture_experts_layer_warp_gb300 import binding
 from mixture_experts_layer_warp_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
-TAU = 2e-6
+TAU = 4e-6
 
 
 def _layer(wl: W.Workload, T=None):
@@ -47,6 +47,9 @@ def _check(wl, inp, y, rows=None):
 SMALL = [
     W.Workload("bf16_two_micro", 300, 256, 8, 2, 128, 2),
     W.Workload("bf16_one_token", 1, 256, 8, 2, 128, 1),
+    W.Workload("bf16_small_batch_shared", 13, 512, 16, 4, 128, 2, shared_inter=256),
+    W.Workload("bf16_small_batch_e64", 16, 4096, 64, 8, 768, 1),
+    W.Workload("bf16_17_tokens", 17, 512, 8, 2, 256, 2, shared_inter=128),
     W.Workload("bf16_e64_k8_ragged", 129, 512, 64, 8, 256, 1),
     W.Workload("bf16_shared", 257, 256, 16, 4, 128, 2, shared_inter=256),
     W.Workload("bf16_four_micro", 70, 512, 8, 3, 128, 4),
