@@ -24,6 +24,8 @@ constexpr int kMaxMicro = 4;
 // tokens (bf16 tensor-core router); its histogram row is blk_hist[block].
 constexpr int kRouterTokens = 32;
 constexpr int kRouterTokensTc = 128;
+// Batches of at most kSmallTokens tokens take the small-batch kernels.
+constexpr int kSmallTokens = 16;
 
 struct RouterArgs {
     const void* x;         // [T][H]
@@ -61,6 +63,9 @@ struct RouterTcArgs {
 // tmX: x [T][H] bf16, box {64, 128}; tmW: Wr [E][H] bf16, box {64, 64}.
 cudaError_t launch_router_tc(const RouterTcArgs& a, const CUtensorMap& tmX, const CUtensorMap& tmW,
                              cudaStream_t s);
+// T <= kSmallTokens: one 8-CTA cluster; tmX box {64, 16}. Same logits bit for bit.
+cudaError_t launch_router_tc_small(const RouterTcArgs& a, const CUtensorMap& tmX, const CUtensorMap& tmW,
+                                   cudaStream_t s);
 
 // --------------------------------------------------------- scan / place
 struct ScanArgs {
@@ -134,7 +139,6 @@ cudaError_t launch_tc_gemm_down(const TcGemmArgs& a, const CUtensorMap& tmA, con
 // tokens on N. tmX: activations [rows][K], box {64, 16}; tmW[m]: weights,
 // box {64, 64} (SwiGLU form: gate and up halves) or {64, 128} (down form).
 // n_tiles counts 64 h-columns (SwiGLU) or 128 output columns (down).
-constexpr int kSmallTokens = 16;
 cudaError_t launch_tc_small_swiglu(const TcGemmArgs& a, const CUtensorMap& tmX, const CUtensorMap* tmW,
                                    int num_sms, cudaStream_t s);
 cudaError_t launch_tc_small_down(const TcGemmArgs& a, const CUtensorMap& tmX, const CUtensorMap* tmW,

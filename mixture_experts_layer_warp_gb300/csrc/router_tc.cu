@@ -11,10 +11,11 @@
 // kb % 8, and the epilogue adds the eight partials with compensated (Kahan)
 // addition, so each fp32 logit stays within a few ulps of the exact dot
 // product and near-ties between experts stay rare. Each thread then owns one
-// token (its TMEM lane): softmax top-k over its 64 logits, renormalised
-// weights, and the CTA's expert histogram. When one CTA covers all tokens
+// token (its TMEM lane) and keeps its 64 logits in registers: softmax top-k,
+// renormalised weights, and the CTA's expert histogram. When one CTA covers all tokens
 // (T <= 128: decode-sized batches) it also computes the offsets and places
-// every route itself, so routing is a single launch.
+// every route itself, so routing is a single launch. Batches of at most 16
+// tokens use an 8-CTA cluster that splits K (router_tc_cluster_kernel below).
 #include <cuda_bf16.h>
 
 #include <cfloat>
@@ -49,9 +50,141 @@ struct Ctl {
     int run[4][kMaxExperts];
 };
 
-constexpr int kLgBytes = kTok * (kMaxExperts + 1) * 4;
 constexpr int kIdsBytes = kTok * kMaxTopK * 4;
-constexpr int kSmemBytes = kStages * kStageBytes + kLgBytes + kIdsBytes + (int)sizeof(Ctl) + 1024;
+constexpr int kSmemBytes = kStages * kStageBytes + kIdsBytes + (int)sizeof(Ctl) + 1024;
+
+// Kahan step: adds v into (sum, comp).
+__device__ __forceinline__ void kahan_add(float& sum, float& comp, float v) {
+    const float y = v - comp;
+    const float t = sum + y;
+    comp = (t - sum) - y;
+    sum = t;
+}
+
+// Top-k of one token from its 64 fp32 logits held in registers (experts >= E
+// are -inf): k rounds of a pairwise tournament, larger logit first and the
+// lower index on equal logits; the chosen expert is then masked to -inf. Weights exp(l_j - l_0) / sum_j' exp(l_j' - l_0) are the
+// softmax over all experts restricted to the k and renormalised. Writes the
+// token's ids and weights, keeps the ids in shared memory (sid) and counts them
+// in the CTA histogram.
+__device__ __forceinline__ void select_topk(float (&l)[kN], int k, int64_t t, int row, const RouterTcArgs& a,
+                                            int* sid, int* hist) {
+    float vals[kMaxTopK];
+    int ids[kMaxTopK];
+#pragma unroll 1
+    for (int j = 0; j < k; ++j) {
+        // pairwise tournament: a right (higher-index) entry wins only when strictly
+        // larger, and every left subtree holds lower indices, so ties go to the
+        // lower expert index exactly as a scan with strict '>' would
+        float v[kN / 2];
+        int ix[kN / 2];
+#pragma unroll
+        for (int i = 0; i < kN / 2; ++i) {
+            const bool r = l[2 * i + 1] > l[2 * i];
+            v[i] = r ? l[2 * i + 1] : l[2 * i];
+            ix[i] = r ? 2 * i + 1 : 2 * i;
+        }
+#pragma unroll
+        for (int w = kN / 4; w >= 1; w >>= 1) {
+#pragma unroll
+            for (int i = 0; i < w; ++i) {
+                const bool r = v[2 * i + 1] > v[2 * i];
+                v[i] = r ? v[2 * i + 1] : v[2 * i];
+                ix[i] = r ? ix[2 * i + 1] : ix[2 * i];
+            }
+        }
+        const float bv = v[0];
+        const int be = ix[0];
+        if (bv != bv || be >= a.E) atomicOr(a.err, kErrCheck);  // NaN logits only
+#pragma unroll
+        for (int e = 0; e < kN; ++e) l[e] = (e == be) ? -INFINITY : l[e];
+        ids[j] = be;
+        vals[j] = bv;
+    }
+    const float v0 = vals[0];
+    float den = 0.f;
+    for (int j = 0; j < k; ++j) {
+        vals[j] = expf(vals[j] - v0);
+        den += vals[j];
+    }
+    for (int j = 0; j < k; ++j) {
+        a.ids[t * k + j] = ids[j];
+        a.w[t * k + j] = vals[j] / den;
+        sid[row * k + j] = ids[j];
+        atomicAdd(&hist[ids[j]], 1);
+    }
+}
+
+// Adds the router bias, writes the optional logits output and masks experts >= E.
+__device__ __forceinline__ void finish_logits(float (&l)[kN], int64_t t, const RouterTcArgs& a) {
+#pragma unroll
+    for (int e = 0; e < kN; ++e) {
+        if (e < a.E) {
+            if (a.bias != nullptr) l[e] += a.bias[e];
+            if (a.logits != nullptr) a.logits[t * a.E + e] = l[e];
+        } else {
+            l[e] = -INFINITY;
+        }
+    }
+}
+
+// When one CTA holds every route: offsets, tile prefixes, the shared expert's
+// segment, and the stable placement of all T*k routes.
+template <int NW>
+__device__ __forceinline__ void finish_single(const RouterTcArgs& a, const int* hist, int* off,
+                                              int (*cnt)[kMaxExperts], int (*run)[kMaxExperts], const int* sid) {
+    const int E = a.E;
+    if (threadIdx.x < 32) {
+        // warp-wide exclusive scans over the (up to 64) experts, two per lane
+        const int lane = threadIdx.x;
+        const int e0 = 2 * lane, e1 = 2 * lane + 1;
+        const int c0 = e0 < E ? hist[e0] : 0, c1 = e1 < E ? hist[e1] : 0;
+        int s_cnt = c0 + c1;
+        int s_tc = (c0 + kTcBM - 1) / kTcBM + (c1 + kTcBM - 1) / kTcBM;
+        int s_si = (c0 + kSimtBM - 1) / kSimtBM + (c1 + kSimtBM - 1) / kSimtBM;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int a0 = __shfl_up_sync(0xffffffffu, s_cnt, d);
+            const int a1 = __shfl_up_sync(0xffffffffu, s_tc, d);
+            const int a2 = __shfl_up_sync(0xffffffffu, s_si, d);
+            if (lane >= d) {
+                s_cnt += a0;
+                s_tc += a1;
+                s_si += a2;
+            }
+        }
+        // inclusive sums up to e1; the value before e0 is the exclusive sum
+        const int x_cnt = s_cnt - c0 - c1, x_tc = s_tc - (c0 + kTcBM - 1) / kTcBM - (c1 + kTcBM - 1) / kTcBM;
+        const int x_si = s_si - (c0 + kSimtBM - 1) / kSimtBM - (c1 + kSimtBM - 1) / kSimtBM;
+        if (e0 <= E) {
+            off[e0] = x_cnt;
+            a.tiles_tc[e0] = x_tc;
+            a.tiles_simt[e0] = x_si;
+        }
+        if (e1 <= E) {
+            off[e1] = x_cnt + c0;
+            a.tiles_tc[e1] = x_tc + (c0 + kTcBM - 1) / kTcBM;
+            a.tiles_simt[e1] = x_si + (c0 + kSimtBM - 1) / kSimtBM;
+        }
+        if (E == 64 && lane == 31) {
+            off[64] = s_cnt;
+            a.tiles_tc[64] = s_tc;
+            a.tiles_simt[64] = s_si;
+        }
+        if (lane == 0) {
+            a.shared_seg[0] = 0;
+            a.shared_seg[1] = a.T;
+            a.shared_tiles_tc[0] = 0;
+            a.shared_tiles_tc[1] = (a.T + kTcBM - 1) / kTcBM;
+            a.shared_tiles_simt[0] = 0;
+            a.shared_tiles_simt[1] = (a.T + kSimtBM - 1) / kSimtBM;
+        }
+    }
+    __syncthreads();
+    if ((int)threadIdx.x <= E) a.offsets[threadIdx.x] = off[threadIdx.x];
+    place_chunk<NW>(sid, a.T * a.k, 0, E, (int64_t)a.T * a.k, [&](int e) { return off[e]; }, cnt, run, a.perm,
+                    a.inv, a.err);
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
     router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
@@ -59,9 +192,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    float (*lg)[kMaxExperts + 1] = reinterpret_cast<float (*)[kMaxExperts + 1]>(smem + kStages * kStageBytes);
-    int* sid = reinterpret_cast<int*>(smem + kStages * kStageBytes + kLgBytes);
-    Ctl& c = *reinterpret_cast<Ctl*>(smem + kStages * kStageBytes + kLgBytes + kIdsBytes);
+    int* sid = reinterpret_cast<int*>(smem + kStages * kStageBytes);
+    Ctl& c = *reinterpret_cast<Ctl*>(smem + kStages * kStageBytes + kIdsBytes);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int t0 = blockIdx.x * kTok;
     const int E = a.E, k = a.k;
@@ -156,98 +288,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = warp * 32 + lane;
     const int t = t0 + row;
     if (ready) {
-        // combine the partials: logits of token `row`, experts 0..63
+        // combine the partials of token `row` (its TMEM lane): four partials per
+        // batched load, compensated addition in partial order 0..7
         const int nparts = kb_total < kParts ? kb_total : kParts;
         const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        float l[kN], comp[kN];
+#pragma unroll
+        for (int e = 0; e < kN; ++e) l[e] = comp[e] = 0.f;
 #pragma unroll 1
-        for (int col = 0; col < kN; col += 16) {
-            float sum[16], comp[16];
+        for (int p0 = 0; p0 < nparts; p0 += 4) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) sum[i] = comp[i] = 0.f;
-#pragma unroll 1
-            for (int p = 0; p < nparts; ++p) {
-                uint32_t v[16];
-                ptx::tmem_ld16(lane_base + (uint32_t)(p * kN + col), v);
+            for (int col = 0; col < kN; col += 16) {
+                uint32_t v[64];
+                const uint32_t base = lane_base + (uint32_t)col;
+                ptx::tmem_ld16x4(base + (uint32_t)(p0 * kN), base + (uint32_t)(min(p0 + 1, nparts - 1) * kN),
+                                 base + (uint32_t)(min(p0 + 2, nparts - 1) * kN),
+                                 base + (uint32_t)(min(p0 + 3, nparts - 1) * kN), v);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float y = __uint_as_float(v[i]) - comp[i];
-                    const float s2 = sum[i] + y;
-                    comp[i] = (s2 - sum[i]) - y;
-                    sum[i] = s2;
-                }
-            }
+                for (int q = 0; q < 4; ++q)
+                    if (p0 + q < nparts) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int e = col + i;
-                float l = sum[i];
-                if (a.bias != nullptr && e < E) l += a.bias[e];
-                lg[row][e] = l;
-                if (a.logits != nullptr && t < a.T && e < E) a.logits[(int64_t)t * E + e] = l;
+                        for (int i = 0; i < 16; ++i)
+                            kahan_add(l[col + i], comp[col + i], __uint_as_float(v[q * 16 + i]));
+                    }
             }
         }
-        // top-k over this token's logits: larger logit first, ties to the lower index
         if (t < a.T) {
-            uint64_t taken = 0;
-            float v0 = 0.f, den = 0.f;
-            float vals[kMaxTopK];
-            int ids[kMaxTopK];
-            for (int j = 0; j < k; ++j) {
-                int best = -1;
-                float bv = -INFINITY;
-                for (int e = 0; e < E; ++e) {
-                    if ((taken >> e) & 1ull) continue;
-                    const float v = lg[row][e];
-                    if (best < 0 || v > bv) {
-                        best = e;
-                        bv = v;
-                    }
-                }
-                if (bv != bv) atomicOr(a.err, kErrCheck);  // NaN logit
-                taken |= 1ull << best;
-                ids[j] = best;
-                vals[j] = bv;
-            }
-            v0 = vals[0];
-            for (int j = 0; j < k; ++j) {
-                vals[j] = expf(vals[j] - v0);
-                den += vals[j];
-            }
-            for (int j = 0; j < k; ++j) {
-                a.ids[(int64_t)t * k + j] = ids[j];
-                a.w[(int64_t)t * k + j] = vals[j] / den;
-                sid[row * k + j] = ids[j];
-                atomicAdd(&c.hist[ids[j]], 1);
-            }
+            finish_logits(l, t, a);
+            select_topk(l, k, t, row, a, sid, c.hist);
         }
     }
     __syncthreads();
 
-    const int n_tok = min(kTok, a.T - t0);
     if (gridDim.x == 1) {
-        // single CTA: offsets, tile prefixes and the placement of every route
-        if (threadIdx.x == 0) {
-            int ttc = 0, tsi = 0;
-            c.off[0] = 0;
-            a.tiles_tc[0] = 0;
-            a.tiles_simt[0] = 0;
-            for (int e = 0; e < E; ++e) {
-                c.off[e + 1] = c.off[e] + c.hist[e];
-                ttc += (c.hist[e] + kTcBM - 1) / kTcBM;
-                tsi += (c.hist[e] + kSimtBM - 1) / kSimtBM;
-                a.tiles_tc[e + 1] = ttc;
-                a.tiles_simt[e + 1] = tsi;
-            }
-            a.shared_seg[0] = 0;
-            a.shared_seg[1] = a.T;
-            a.shared_tiles_tc[0] = 0;
-            a.shared_tiles_tc[1] = (a.T + kTcBM - 1) / kTcBM;
-            a.shared_tiles_simt[0] = 0;
-            a.shared_tiles_simt[1] = (a.T + kSimtBM - 1) / kSimtBM;
-        }
-        __syncthreads();
-        if ((int)threadIdx.x <= E) a.offsets[threadIdx.x] = c.off[threadIdx.x];
-        place_chunk<4>(sid, n_tok * k, 0, E, (int64_t)a.T * k, [&](int e) { return c.off[e]; }, c.cnt, c.run,
-                       a.perm, a.inv, a.err);
+        finish_single<4>(a, c.hist, c.off, c.cnt, c.run, sid);
     } else if ((int)threadIdx.x < E) {
         a.blk_hist[(int64_t)blockIdx.x * E + threadIdx.x] = c.hist[threadIdx.x];
     }
@@ -257,6 +331,180 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 2) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+
+// ------------------------------------------------------------------------
+// Batches of at most kSmallTokens tokens: a cluster of 8 CTAs splits K. CTA c
+// accumulates exactly the K-blocks kb = c, c+8, c+16, ... that form partial c
+// of router_tc_kernel, in the same order, sends its partial logits to CTA 0
+// through distributed shared memory, and CTA 0 combines the partials in the
+// same compensated order. The logits are therefore bit-identical to the
+// 128-token kernel's (routing does not depend on the batch size), while eight
+// SMs instead of one stream the router weights.
+constexpr int kCluster = 8;
+constexpr int kCStages = 4;
+constexpr int kCTok = kSmallTokens;
+constexpr int kXBytesSmall = kCTok * kTcBK * 2;                    // 2 KB of x per stage
+constexpr int kPartBytes = kCluster * kCTok * kN * 4;              // 32 KB
+constexpr int kCIdsBytes = kCTok * kMaxTopK * 4;
+constexpr int kCSmemBytes = kCStages * kStageBytes + kPartBytes + kCIdsBytes + (int)sizeof(Ctl) + 1024;
+
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
+    router_tc_cluster_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                             const RouterTcArgs a) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float* part = reinterpret_cast<float*>(smem + kCStages * kStageBytes);   // [kCluster][kCTok][kN] on CTA 0
+    int* sid = reinterpret_cast<int*>(smem + kCStages * kStageBytes + kPartBytes);
+    Ctl& c = *reinterpret_cast<Ctl*>(smem + kCStages * kStageBytes + kPartBytes + kCIdsBytes);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int rank = (int)ptx::cluster_ctarank();
+    const int k = a.k;
+    const int kb_total = a.H / kTcBK;
+    const int my_blocks = kb_total > rank ? (kb_total - rank + kCluster - 1) / kCluster : 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kCStages; ++s) {
+            ptx::mbar_init(ptx::smem_u32(&c.full[s]), 1);
+            ptx::mbar_init(ptx::smem_u32(&c.empty[s]), 1);
+        }
+        ptx::mbar_init(ptx::smem_u32(&c.done), 1);
+        c.abort = 0;
+        ptx::fence_mbar_init();
+    }
+    if (threadIdx.x < kMaxExperts) c.hist[threadIdx.x] = 0;
+    if (warp == 2) {
+        ptx::tmem_alloc(ptx::smem_u32(&c.tmem), kN);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = c.tmem;
+
+    if (warp == 0 && lane == 0) {
+        int stage = 0;
+        uint32_t phase = 0, last_par[kCStages];
+        int issued = 0;
+        bool ok = true;
+        for (int i = 0; i < my_blocks; ++i) {
+            const int kb = rank + i * kCluster;
+            if (!ptx::mbar_wait(ptx::smem_u32(&c.empty[stage]), phase ^ 1u, a.limit_ns, &c.abort)) {
+                ok = false;
+                break;
+            }
+            const uint32_t sa = ptx::smem_u32(smem + stage * kStageBytes);
+            const uint32_t fb = ptx::smem_u32(&c.full[stage]);
+            ptx::mbar_arrive_expect_tx(fb, kXBytesSmall + kBBytes);
+            ptx::tma_load_2d(sa, &tmX, kb * kTcBK, 0, fb);  // 16 token rows; rows 16..127 unused
+            ptx::tma_load_2d(sa + kABytes, &tmW, kb * kTcBK, 0, fb);
+            last_par[stage] = phase;
+            ++issued;
+            if (++stage == kCStages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        if (!ok) {
+            c.abort = 1;
+            atomicOr(a.err, kErrTimeout);
+            const int n = issued < kCStages ? issued : kCStages;
+            for (int s = 0; s < n; ++s) ptx::mbar_wait(ptx::smem_u32(&c.full[s]), last_par[s], a.limit_ns, nullptr);
+        }
+    } else if (warp == 1 && lane == 0) {
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int i = 0; i < my_blocks; ++i) {
+            if (!ptx::mbar_wait(ptx::smem_u32(&c.full[stage]), phase, a.limit_ns, &c.abort)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t sa = ptx::smem_u32(smem + stage * kStageBytes);
+            const uint64_t adesc = ptx::sw128_desc(sa), bdesc = ptx::sw128_desc(sa + kABytes);
+#pragma unroll
+            for (int kk = 0; kk < kTcBK / 16; ++kk)
+                ptx::mma_bf16(tmem, adesc + 2u * kk, bdesc + 2u * kk, kIdesc, (i > 0 || kk > 0) ? 1u : 0u);
+            ptx::mma_commit(ptx::smem_u32(&c.empty[stage]));
+            if (++stage == kCStages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        if (!ok) {
+            c.abort = 1;
+            atomicOr(a.err, kErrTimeout);
+        }
+        ptx::mma_commit(ptx::smem_u32(&c.done));
+    }
+
+    bool ready = false;
+    if (lane == 0)
+        ready = ptx::mbar_wait(ptx::smem_u32(&c.done), 0, a.limit_ns, nullptr) &&
+                *static_cast<volatile int*>(&c.abort) == 0;
+    ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
+    ptx::tc_fence_after();
+    const int row = warp * 32 + lane;
+    if (ready && my_blocks > 0 && warp == 0) {  // rows 0..15 live in warp 0's lanes
+#pragma unroll 1
+        for (int col = 0; col < kN; col += 16) {
+            uint32_t v[16];
+            ptx::tmem_ld16(tmem + (uint32_t)col, v);
+            if (row < a.T) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const uint32_t local = ptx::smem_u32(part + ((size_t)rank * kCTok + row) * kN + col + i);
+                    ptx::st_cluster_f32(ptx::map_to_rank(local, 0), __uint_as_float(v[i]));
+                }
+            }
+        }
+    }
+    ptx::cluster_sync();
+
+    if (rank == 0) {
+        const int nparts = kb_total < kCluster ? kb_total : kCluster;
+        // combine: every thread takes (token, 4 experts) tasks; partials in order 0..7
+        for (int task = threadIdx.x; task < a.T * (kN / 4); task += kThreads) {
+            const int r = task / (kN / 4), e4 = task % (kN / 4);
+            float s4[4] = {0.f, 0.f, 0.f, 0.f}, c4[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int p = 0; p < nparts; ++p) {
+                const float4 v = reinterpret_cast<const float4*>(part + ((size_t)p * kCTok + r) * kN)[e4];
+                kahan_add(s4[0], c4[0], v.x);
+                kahan_add(s4[1], c4[1], v.y);
+                kahan_add(s4[2], c4[2], v.z);
+                kahan_add(s4[3], c4[3], v.w);
+            }
+            // partial 0 is no longer needed: the combined logits overwrite it
+            reinterpret_cast<float4*>(part + (size_t)r * kN)[e4] = make_float4(s4[0], s4[1], s4[2], s4[3]);
+        }
+        __syncthreads();
+        if (row < a.T) {
+            float l[kN];
+            const float4* src = reinterpret_cast<const float4*>(part + (size_t)row * kN);
+#pragma unroll
+            for (int e4 = 0; e4 < kN / 4; ++e4) {
+                const float4 v = src[e4];
+                l[4 * e4] = v.x;
+                l[4 * e4 + 1] = v.y;
+                l[4 * e4 + 2] = v.z;
+                l[4 * e4 + 3] = v.w;
+            }
+            finish_logits(l, row, a);
+            select_topk(l, k, row, row, a, sid, c.hist);
+        }
+        __syncthreads();
+        finish_single<4>(a, c.hist, c.off, c.cnt, c.run, sid);
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, kN);
     }
 }
 
@@ -274,6 +522,21 @@ cudaError_t launch_router_tc(const RouterTcArgs& a, const CUtensorMap& tmX, cons
         configured = true;
     }
     router_tc_kernel<<<nb, kThreads, kSmemBytes, s>>>(tmX, tmW, a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_router_tc_small(const RouterTcArgs& a, const CUtensorMap& tmX, const CUtensorMap& tmW,
+                                   cudaStream_t s) {
+    if (a.T <= 0) return cudaSuccess;
+    if (a.T > kCTok) return cudaErrorInvalidValue;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(router_tc_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kCSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    router_tc_cluster_kernel<<<kCluster, kThreads, kCSmemBytes, s>>>(tmX, tmW, a);
     return cudaGetLastError();
 }
 

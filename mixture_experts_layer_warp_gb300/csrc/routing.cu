@@ -49,15 +49,18 @@ cudaError_t enqueue_routing(const RoutingJob& j, cudaStream_t s, const LaunchHoo
     cudaError_t e;
     int NB, tpb;
     if (j.bf16) {
+        const bool small = j.T <= kSmallTokens;
         CUtensorMap tmX, tmW;
-        if (!encode_bf16_2d(&tmX, j.x, j.H, j.T, (uint64_t)j.H * 2, kRouterTokensTc) ||
+        if (!encode_bf16_2d(&tmX, j.x, j.H, j.T, (uint64_t)j.H * 2, small ? kSmallTokens : kRouterTokensTc) ||
             !encode_bf16_2d(&tmW, j.wr, j.H, j.E, (uint64_t)j.H * 2, 64))
             return cudaErrorInvalidValue;
         RouterTcArgs ra{j.bias, j.T, j.H, j.E, j.k, j.ids, j.w, j.logits, j.blk_hist, j.offsets, j.tiles_tc,
                         j.tiles_simt, j.shared_meta, j.shared_meta + 2, j.shared_meta + 4, j.perm, j.inv, j.err,
                         j.limit_ns};
-        if ((e = hooked(hook, kSlotRouter, s, [&] { return launch_router_tc(ra, tmX, tmW, s); })) != cudaSuccess)
-            return e;
+        e = hooked(hook, kSlotRouter, s, [&] {
+            return small ? launch_router_tc_small(ra, tmX, tmW, s) : launch_router_tc(ra, tmX, tmW, s);
+        });
+        if (e != cudaSuccess) return e;
         tpb = kRouterTokensTc;
         NB = (j.T + tpb - 1) / tpb;
         if (NB <= 1) return cudaSuccess;  // the single CTA also scanned and placed

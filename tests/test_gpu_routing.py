@@ -73,3 +73,19 @@ def test_empty_batch_routes_nothing():
     layer.sync()
     assert out["offsets"].cpu().tolist() == [0] * 9
     layer.close()
+
+
+@pytest.mark.parametrize("H", [4096, 256])
+def test_routing_does_not_depend_on_batch_size(H):
+    """A token's fp32 logits, and so its experts, are bit-identical whether it is
+    routed in a batch of <= 16 tokens (8-CTA cluster router) or inside a large
+    batch (128-token router): both combine the same K partials in the same order."""
+    wl = W.Workload("inv", 300, H, 64, 8, 128, 1, router_bias="log_zipf")
+    inp = W.make_inputs(wl, seed=21, device="cuda", experts=False)
+    big = _route(300, H, 64, 8, inp, torch.bfloat16)
+    for lo, hi in [(0, 8), (133, 149), (299, 300)]:
+        part = dict(inp, x=inp["x"][lo:hi].contiguous())
+        small = _route(hi - lo, H, 64, 8, part, torch.bfloat16)
+        assert torch.equal(small["logits"], big["logits"][lo:hi])
+        assert torch.equal(small["ids"], big["ids"][lo:hi])
+        assert torch.equal(small["w"], big["w"][lo:hi])
