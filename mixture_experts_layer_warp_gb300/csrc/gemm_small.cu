@@ -8,14 +8,24 @@
 // rows its N side (N = 16): each K stage moves 16 KB of weights and 2 KB of
 // activations instead of 16 KB of mostly-padding activation rows. The layer is
 // then a weight stream, bounded by HBM bandwidth.
-//   SwiGLU (GEMM1): a tile is (expert e, micro m, 64 columns of h): the A
-//       tile stacks 64 gate rows of w13[m][e] over the matching 64 up rows,
-//       so TMEM lanes 0-63 hold gate and 64-127 up for the 16 tokens; the
-//       epilogue pairs them through shared memory and writes silu(gate) * up.
-//   down (GEMM2): a tile is (expert e, 128 output columns), K runs over all
-//       micros into one accumulator.
-// Persistent CTAs, 8-stage TMA ring, one MMA issuer, four epilogue warps on a
+//   SwiGLU tile (GEMM1): (expert e, micro m, 64 columns of h): the A tile
+//       stacks 64 gate rows of w13[m][e] over the matching 64 up rows, so TMEM
+//       lanes 0-63 hold gate and 64-127 up for the 16 tokens; the epilogue
+//       pairs them through shared memory and writes silu(gate) * up.
+//   down tile (GEMM2): (expert e, 128 output columns), K runs over all micros
+//       into one accumulator.
+// The routed layer runs both in ONE persistent cooperative launch: the work
+// list is every SwiGLU tile (expert order) followed by every down tile. A
+// down tile of expert e first waits until all SwiGLU tiles of e have stored
+// their h rows (a per-expert counter, bounded wait), so the down projection's
+// weight stream starts on SMs as soon as they run out of SwiGLU tiles instead
+// of after the slowest one, and one kernel boundary disappears. All CTAs are
+// co-resident (cooperative launch, one CTA per SM) and each CTA takes its tiles
+// in increasing order, so every awaited SwiGLU tile is already owned by a
+// running CTA that reaches it first.
+// Structure: 8-stage TMA ring, one MMA issuer, four epilogue warps on a
 // double-buffered 2 x 16-column TMEM accumulator. All waits are bounded.
+#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 
 #include "gemm_common.cuh"
@@ -35,6 +45,8 @@ constexpr int kTmemCols = 32;                  // 2 accumulators x 16 columns
 constexpr int kThreads = 256;
 constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kM, kTok);
 
+enum Mode { kSwiGLUOnly = 0, kDownOnly = 1, kFused = 2 };
+
 struct Ctl {
     uint64_t full[kStages];
     uint64_t empty[kStages];
@@ -51,6 +63,19 @@ struct Ctl {
 
 constexpr int kSmemBytes = kStages * kStageBytes + (int)sizeof(Ctl) + 1024;
 
+struct SmallParams {
+    TcGemmArgs g1;   // SwiGLU tiles (unused in kDownOnly)
+    TcGemmArgs g2;   // down tiles (unused in kSwiGLUOnly)
+    int* done;       // kFused: per-expert count of finished SwiGLU tiles, zero at launch
+};
+
+struct SmallMaps {
+    CUtensorMap x1;      // SwiGLU token rows [R][H], box {64, 16}
+    CUtensorMap x2;      // down token rows (h) [R][M*I], box {64, 16}
+    CUtensorMap w1[kMaxMicro];  // w13[m] [E*2I][H], box {64, 64}
+    CUtensorMap w2[kMaxMicro];  // w2[m] [E*H][I], box {64, 128}
+};
+
 __device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 __device__ __forceinline__ void fail(Ctl& c, int* err) {
@@ -58,16 +83,42 @@ __device__ __forceinline__ void fail(Ctl& c, int* err) {
     atomicOr(err, kErrTimeout);
 }
 
-template <bool SWIGLU>
+__device__ __forceinline__ int ld_acquire(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Tile list position -> (is a SwiGLU tile, tile) for the given mode.
+template <int MODE>
+__device__ __forceinline__ Tile locate(int tile, const Ctl& c, const SmallParams& p, bool& swiglu) {
+    if (MODE == kSwiGLUOnly) {
+        swiglu = true;
+        return decode_group_tile(tile, c.seg, c.tiles, p.g1.G, p.g1.n_tiles, p.g1.n_micro, true, kTcBM);
+    }
+    if (MODE == kDownOnly) {
+        swiglu = false;
+        return decode_group_tile(tile, c.seg, c.tiles, p.g2.G, p.g2.n_tiles, p.g2.n_micro, false, kTcBM);
+    }
+    const int n1 = p.g1.n_micro * c.tiles[p.g1.G] * p.g1.n_tiles;
+    swiglu = tile < n1;
+    return swiglu ? decode_group_tile(tile, c.seg, c.tiles, p.g1.G, p.g1.n_tiles, p.g1.n_micro, true, kTcBM)
+                  : decode_group_tile(tile - n1, c.seg, c.tiles, p.g2.G, p.g2.n_tiles, p.g2.n_micro, false, kTcBM);
+}
+
+template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
-    tc_small_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW0,
-                    const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmW2,
-                    const __grid_constant__ CUtensorMap tmW3, const TcGemmArgs a) {
+    tc_small_kernel(const __grid_constant__ SmallMaps maps, const SmallParams p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Ctl& c = *reinterpret_cast<Ctl*>(smem + kStages * kStageBytes);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const TcGemmArgs& a0 = MODE == kDownOnly ? p.g2 : p.g1;  // seg, tiles, G, err, limit
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -82,13 +133,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         c.abort = 0;
         ptx::fence_mbar_init();
     }
-    for (int i = threadIdx.x; i <= a.G; i += kThreads) {
-        c.seg[i] = a.seg[i];
-        c.tiles[i] = a.tiles[i];
+    for (int i = threadIdx.x; i <= a0.G; i += kThreads) {
+        c.seg[i] = a0.seg[i];
+        c.tiles[i] = a0.tiles[i];
     }
     if (warp == 0 && lane == 0) {
-        ptx::prefetch_tmap(&tmX);
-        ptx::prefetch_tmap(&tmW0);
+        if (MODE != kDownOnly) ptx::prefetch_tmap(&maps.x1);
+        if (MODE != kSwiGLUOnly) ptx::prefetch_tmap(&maps.x2);
     }
     if (warp == 2) {
         ptx::tmem_alloc(ptx::smem_u32(&c.tmem_base), kTmemCols);
@@ -99,8 +150,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
 
     const uint32_t tmem = c.tmem_base;
-    const int total = (SWIGLU ? a.n_micro : 1) * c.tiles[a.G] * a.n_tiles;
-    const int n_micro_k = SWIGLU ? 1 : a.n_micro;
+    const int n1 = MODE == kDownOnly ? 0 : p.g1.n_micro * c.tiles[p.g1.G] * p.g1.n_tiles;
+    const int n2 = MODE == kSwiGLUOnly ? 0 : c.tiles[p.g2.G] * p.g2.n_tiles;
+    const int total = n1 + n2;
+    const int target = p.g1.n_micro * p.g1.n_tiles;  // SwiGLU tiles per expert (kFused)
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer
@@ -109,27 +162,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         int issued = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-            const Tile t = decode_group_tile(tile, c.seg, c.tiles, a.G, a.n_tiles, a.n_micro, SWIGLU, kTcBM);
+            bool sw;
+            const Tile t = locate<MODE>(tile, c, p, sw);
+            const TcGemmArgs& g = sw ? p.g1 : p.g2;
+            if (MODE == kFused && !sw) {
+                // the down tile reads h rows of expert g: wait for all its SwiGLU tiles
+                const int* cnt = p.done + t.g;
+                if (ld_acquire(cnt) < target) {
+                    const uint64_t t0 = ptx::globaltimer();
+                    uint32_t it = 0;
+                    while (ld_acquire(cnt) < target) {
+                        if ((++it & 15u) == 0u &&
+                            (c.abort || ptx::globaltimer() - t0 > g.limit_ns)) {
+                            ok = false;
+                            break;
+                        }
+                        __nanosleep(64);
+                    }
+                    if (!ok) break;
+                }
+                fence_proxy_async_global();
+            }
+            const int n_micro_k = sw ? 1 : g.n_micro;
             for (int mi = 0; ok && mi < n_micro_k; ++mi) {
-                const int m = SWIGLU ? t.m : mi;
-                const CUtensorMap* tw = pick_map(m, tmW0, tmW1, tmW2, tmW3);
-                const int wrow = t.g * a.b_rows_per_group + t.nt * (SWIGLU ? 64 : kM);
-                for (int kb = 0; kb < a.k_blocks; ++kb) {
-                    if (!ptx::mbar_wait(ptx::smem_u32(&c.empty[stage]), phase ^ 1u, a.limit_ns, &c.abort)) {
+                const int m = sw ? t.m : mi;
+                const CUtensorMap* tw = sw ? &maps.w1[m] : &maps.w2[m];
+                const CUtensorMap* tx = sw ? &maps.x1 : &maps.x2;
+                const int wrow = t.g * g.b_rows_per_group + t.nt * (sw ? 64 : kM);
+                for (int kb = 0; kb < g.k_blocks; ++kb) {
+                    if (!ptx::mbar_wait(ptx::smem_u32(&c.empty[stage]), phase ^ 1u, g.limit_ns, &c.abort)) {
                         ok = false;
                         break;
                     }
                     const uint32_t sa = ptx::smem_u32(smem + stage * kStageBytes);
                     const uint32_t fb = ptx::smem_u32(&c.full[stage]);
                     ptx::mbar_arrive_expect_tx(fb, kStageBytes);
-                    if (SWIGLU) {
+                    if (sw) {
                         ptx::tma_load_2d(sa, tw, kb * kTcBK, wrow, fb);                       // 64 gate rows
-                        ptx::tma_load_2d(sa + kABytes / 2, tw, kb * kTcBK, wrow + a.up_offset, fb);  // 64 up rows
+                        ptx::tma_load_2d(sa + kABytes / 2, tw, kb * kTcBK, wrow + g.up_offset, fb);  // 64 up rows
                     } else {
                         ptx::tma_load_2d(sa, tw, kb * kTcBK, wrow, fb);                       // 128 rows
                     }
-                    const int kx = (SWIGLU ? 0 : m * a.a_micro_cols) + kb * kTcBK;
-                    ptx::tma_load_2d(sa + kABytes, &tmX, kx, t.row0, fb);                      // 16 token rows
+                    const int kx = (sw ? 0 : m * g.a_micro_cols) + kb * kTcBK;
+                    ptx::tma_load_2d(sa + kABytes, tx, kx, t.row0, fb);                       // 16 token rows
                     last_par[stage] = phase;
                     ++issued;
                     if (++stage == kStages) {
@@ -140,9 +215,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         if (!ok) {
-            fail(c, a.err);
+            fail(c, a0.err);
             const int n = issued < kStages ? issued : kStages;
-            for (int s = 0; s < n; ++s) ptx::mbar_wait(ptx::smem_u32(&c.full[s]), last_par[s], a.limit_ns, nullptr);
+            for (int s = 0; s < n; ++s) ptx::mbar_wait(ptx::smem_u32(&c.full[s]), last_par[s], a0.limit_ns, nullptr);
         }
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------ MMA issuer
@@ -151,18 +226,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         int local = 0;
         for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++local) {
+            bool sw;
+            locate<MODE>(tile, c, p, sw);
+            const TcGemmArgs& g = sw ? p.g1 : p.g2;
             const int acc = local & 1;
             const uint32_t acc_par = (uint32_t)(local >> 1) & 1u;
-            if (!ptx::mbar_wait(ptx::smem_u32(&c.tempty[acc]), acc_par ^ 1u, a.limit_ns, &c.abort)) {
+            if (!ptx::mbar_wait(ptx::smem_u32(&c.tempty[acc]), acc_par ^ 1u, g.limit_ns, &c.abort)) {
                 ok = false;
                 break;
             }
             ptx::tc_fence_after();
             const uint32_t d = tmem + (uint32_t)(acc * kTok);
             uint32_t accumulate = 0;
+            const int n_micro_k = sw ? 1 : g.n_micro;
             for (int mi = 0; ok && mi < n_micro_k; ++mi) {
-                for (int kb = 0; kb < a.k_blocks; ++kb) {
-                    if (!ptx::mbar_wait(ptx::smem_u32(&c.full[stage]), phase, a.limit_ns, &c.abort)) {
+                for (int kb = 0; kb < g.k_blocks; ++kb) {
+                    if (!ptx::mbar_wait(ptx::smem_u32(&c.full[stage]), phase, g.limit_ns, &c.abort)) {
                         ok = false;
                         break;
                     }
@@ -183,56 +262,61 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (ok) ptx::mma_commit(ptx::smem_u32(&c.tfull[acc]));
         }
-        if (!ok) fail(c, a.err);
+        if (!ok) fail(c, a0.err);
         ptx::mma_commit(ptx::smem_u32(&c.drain));
-        ptx::mbar_wait(ptx::smem_u32(&c.drain), 0, a.limit_ns, nullptr);
+        ptx::mbar_wait(ptx::smem_u32(&c.drain), 0, a0.limit_ns, nullptr);
     } else if (warp >= 4) {
         // ------------------------------------------------ epilogue
         const int q = warp - 4;            // TMEM lanes 32q .. 32q+31 = weight rows
         const int r = q * 32 + lane;
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
         int local = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
+            bool sw;
+            const Tile t = locate<MODE>(tile, c, p, sw);
+            const TcGemmArgs& g = sw ? p.g1 : p.g2;
+            __nv_bfloat16* out = static_cast<__nv_bfloat16*>(g.out);
             const int acc = local & 1;
             const uint32_t acc_par = (uint32_t)(local >> 1) & 1u;
-            const Tile t = decode_group_tile(tile, c.seg, c.tiles, a.G, a.n_tiles, a.n_micro, SWIGLU, kTcBM);
             bool ready = false;
-            if (lane == 0)
-                ready = ptx::mbar_wait(ptx::smem_u32(&c.tfull[acc]), acc_par, a.limit_ns, &c.abort);
+            if (lane == 0) ready = ptx::mbar_wait(ptx::smem_u32(&c.tfull[acc]), acc_par, g.limit_ns, &c.abort);
             ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
-            if (SWIGLU) {
-                // the four epilogue warps meet at named barriers below, so they
-                // take the continue-or-stop decision together
-                if (lane == 0) c.ep_ok[q] = ready ? 1 : 0;
-                epilogue_bar();
-                ready = c.ep_ok[0] && c.ep_ok[1] && c.ep_ok[2] && c.ep_ok[3];
-            }
+            // the four epilogue warps meet at named barriers below, so they take
+            // the continue-or-stop decision together
+            if (lane == 0) c.ep_ok[q] = ready ? 1 : 0;
+            epilogue_bar();
+            ready = c.ep_ok[0] && c.ep_ok[1] && c.ep_ok[2] && c.ep_ok[3];
             if (!ready) {
-                if (lane == 0) fail(c, a.err);
+                if (lane == 0) fail(c, a0.err);
                 break;
             }
             ptx::tc_fence_after();
             uint32_t v[kTok];
             ptx::tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kTok), v);
             const int cnt = min(kTok, t.row_end - t.row0);
-            if (SWIGLU) {
+            if (sw) {
                 if (q >= 2) {
 #pragma unroll
                     for (int j = 0; j < kTok; ++j) c.up[r - 64][j] = __uint_as_float(v[j]);
                 }
                 epilogue_bar();
                 if (q < 2) {
-                    const int64_t col = (int64_t)t.m * a.out_micro_cols + t.nt * 64 + r;
+                    const int64_t col = (int64_t)t.m * g.out_micro_cols + t.nt * 64 + r;
                     for (int j = 0; j < cnt; ++j) {
                         const float h = silu(__uint_as_float(v[j])) * c.up[r][j];
-                        out[(int64_t)(t.row0 + j) * a.out_ld + col] = __float2bfloat16_rn(h);
+                        out[(int64_t)(t.row0 + j) * g.out_ld + col] = __float2bfloat16_rn(h);
                     }
+                    if (MODE == kFused) fence_proxy_async_global();
                 }
                 epilogue_bar();
+                if (MODE == kFused && threadIdx.x == 128) {
+                    // every h store of this tile happened before the barrier above
+                    __threadfence();
+                    atomicAdd(p.done + t.g, 1);
+                }
             } else {
                 const int64_t col = (int64_t)t.nt * kM + r;
                 for (int j = 0; j < cnt; ++j)
-                    out[(int64_t)(t.row0 + j) * a.out_ld + col] = __float2bfloat16_rn(__uint_as_float(v[j]));
+                    out[(int64_t)(t.row0 + j) * g.out_ld + col] = __float2bfloat16_rn(__uint_as_float(v[j]));
             }
             ptx::tc_fence_before();
             __syncwarp();
@@ -248,35 +332,68 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <bool SWIGLU>
-cudaError_t launch_small(const TcGemmArgs& a, const CUtensorMap& tmX, const CUtensorMap* tmW, int num_sms,
-                         cudaStream_t s) {
-    if (a.max_tiles <= 0) return cudaSuccess;
+template <int MODE>
+cudaError_t launch_small(const SmallMaps& maps, const SmallParams& p, int max_tiles, int num_sms, cudaStream_t s) {
+    if (max_tiles <= 0) return cudaSuccess;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(tc_small_kernel<SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kSmemBytes);
+        cudaError_t e =
+            cudaFuncSetAttribute(tc_small_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    const int grid = a.max_tiles < num_sms ? a.max_tiles : num_sms;
-    const CUtensorMap& w1 = a.n_micro > 1 ? tmW[1] : tmW[0];
-    const CUtensorMap& w2 = a.n_micro > 2 ? tmW[2] : tmW[0];
-    const CUtensorMap& w3 = a.n_micro > 3 ? tmW[3] : tmW[0];
-    tc_small_kernel<SWIGLU><<<grid, kThreads, kSmemBytes, s>>>(tmX, tmW[0], w1, w2, w3, a);
+    const int grid = max_tiles < num_sms ? max_tiles : num_sms;
+    if (MODE == kFused) {
+        // all CTAs must be resident at once: down tiles wait on other CTAs' SwiGLU tiles
+        void* args[] = {const_cast<SmallMaps*>(&maps), const_cast<SmallParams*>(&p)};
+        return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(tc_small_kernel<MODE>), dim3(grid),
+                                           dim3(kThreads), args, kSmemBytes, s);
+    }
+    tc_small_kernel<MODE><<<grid, kThreads, kSmemBytes, s>>>(maps, p);
     return cudaGetLastError();
+}
+
+void fill_maps(SmallMaps& m, const CUtensorMap& x, const CUtensorMap* w, int n_micro, bool swiglu) {
+    for (int i = 0; i < kMaxMicro; ++i) {
+        const CUtensorMap& src = w[i < n_micro ? i : 0];
+        if (swiglu) {
+            m.x1 = x;
+            m.w1[i] = src;
+        } else {
+            m.x2 = x;
+            m.w2[i] = src;
+        }
+    }
 }
 
 }  // namespace
 
 cudaError_t launch_tc_small_swiglu(const TcGemmArgs& a, const CUtensorMap& tmX, const CUtensorMap* tmW,
                                    int num_sms, cudaStream_t s) {
-    return launch_small<true>(a, tmX, tmW, num_sms, s);
+    SmallMaps maps;
+    fill_maps(maps, tmX, tmW, a.n_micro, true);
+    fill_maps(maps, tmX, tmW, 1, false);  // unused slots
+    SmallParams p{a, a, nullptr};
+    return launch_small<kSwiGLUOnly>(maps, p, a.max_tiles, num_sms, s);
 }
 
 cudaError_t launch_tc_small_down(const TcGemmArgs& a, const CUtensorMap& tmX, const CUtensorMap* tmW,
                                  int num_sms, cudaStream_t s) {
-    return launch_small<false>(a, tmX, tmW, num_sms, s);
+    SmallMaps maps;
+    fill_maps(maps, tmX, tmW, a.n_micro, false);
+    fill_maps(maps, tmX, tmW, 1, true);  // unused slots
+    SmallParams p{a, a, nullptr};
+    return launch_small<kDownOnly>(maps, p, a.max_tiles, num_sms, s);
+}
+
+cudaError_t launch_tc_small_fused(const TcGemmArgs& g1, const CUtensorMap& tmX1, const CUtensorMap* tmW1,
+                                  const TcGemmArgs& g2, const CUtensorMap& tmX2, const CUtensorMap* tmW2,
+                                  int* done, int num_sms, cudaStream_t s) {
+    SmallMaps maps;
+    fill_maps(maps, tmX1, tmW1, g1.n_micro, true);
+    fill_maps(maps, tmX2, tmW2, g2.n_micro, false);
+    SmallParams p{g1, g2, done};
+    return launch_small<kFused>(maps, p, g1.max_tiles + g2.max_tiles, num_sms, s);
 }
 
 }  // namespace moe

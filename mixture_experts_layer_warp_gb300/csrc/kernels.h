@@ -57,6 +57,7 @@ struct RouterTcArgs {
     int32_t* shared_tiles_simt;  // [2]
     int32_t* perm;          // [T*k]
     int32_t* inv;           // [T*k]
+    int32_t* zero_counters; // [E] set to 0 by the single-CTA paths, or null
     int* err;
     uint64_t limit_ns;
 };
@@ -143,6 +144,12 @@ cudaError_t launch_tc_small_swiglu(const TcGemmArgs& a, const CUtensorMap& tmX, 
                                    int num_sms, cudaStream_t s);
 cudaError_t launch_tc_small_down(const TcGemmArgs& a, const CUtensorMap& tmX, const CUtensorMap* tmW,
                                  int num_sms, cudaStream_t s);
+// Both GEMMs of the routed experts in one persistent cooperative launch: the
+// down tiles of expert e start once the SwiGLU tiles of e have stored h.
+// done[E] must be zero at launch (the small-batch router zeroes it).
+cudaError_t launch_tc_small_fused(const TcGemmArgs& g1, const CUtensorMap& tmX1, const CUtensorMap* tmW1,
+                                  const TcGemmArgs& g2, const CUtensorMap& tmX2, const CUtensorMap* tmW2,
+                                  int* done, int num_sms, cudaStream_t s);
 
 // ---------------------------------------------------- fp32 SIMT GEMMs
 constexpr int kSimtBM = 32;
@@ -202,6 +209,7 @@ struct RoutingJob {
     int32_t* blk_base;        // same
     int* err;
     uint64_t limit_ns;
+    int32_t* zero_counters;   // [E] zeroed when routing runs in one CTA (T <= 128), or null
 };
 
 // Optional callbacks around every kernel launch (timing, counting).

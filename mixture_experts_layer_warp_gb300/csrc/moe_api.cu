@@ -44,6 +44,7 @@ struct moe_handle {
     int32_t* shared_meta = nullptr;  // shared expert: seg[2], tiles_tc[2], tiles_simt[2]
     int32_t* blk_hist = nullptr;
     int32_t* blk_base = nullptr;
+    int* done = nullptr;  // per-expert SwiGLU-tile counters of the fused small-batch GEMMs
     void* xp = nullptr;
     void* hbuf = nullptr;
     void* obuf = nullptr;
@@ -159,7 +160,7 @@ moe_status run_routing(moe_handle* h, const void* x, const void* router_w, const
     const moe_config& c = h->cfg;
     RoutingJob j{x, router_w, bias, T, c.hidden, c.num_experts, c.top_k, c.dtype == MOE_BF16, h->ids, h->topw,
                  logits, h->perm, h->inv, h->offsets, h->tiles_tc, h->tiles_simt, h->shared_meta, h->blk_hist,
-                 h->blk_base, h->err, h->limit_ns};
+                 h->blk_base, h->err, h->limit_ns, h->done};
     LaunchHook hook{h, hook_before, hook_after};
     cudaError_t e = enqueue_routing(j, s, &hook);
     if (e == cudaErrorInvalidValue) return set_err(h, MOE_ERR_CUDA, "router tensor map encode failed");
@@ -192,19 +193,19 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
                 return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (w13[%d])", m);
         TcGemmArgs g1{h->offsets, h->tiles_tc, E, M, H / kTcBK, I / 64, 2 * I, I, 0,
                       h->hbuf, (int64_t)M * I, I, active * M * (I / 64), h->err, h->limit_ns};
-        if ((e = timed(h, kSlotGemm1, s, [&] { return launch_tc_small_swiglu(g1, tmX, tmW, h->num_sms, s); })) !=
-            cudaSuccess)
-            return cuda_err(h, e, "GEMM1 launch");
-        if (!encode_bf16_2d(&tmX, h->hbuf, (uint64_t)M * I, R, (uint64_t)M * I * 2, kSmallTokens))
+        CUtensorMap tmX2, tmW2[kMaxMicro];
+        if (!encode_bf16_2d(&tmX2, h->hbuf, (uint64_t)M * I, R, (uint64_t)M * I * 2, kSmallTokens))
             return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (h)");
         for (int m = 0; m < M; ++m)
-            if (!encode_bf16_2d(&tmW[m], w2[m], I, (uint64_t)E * H, (uint64_t)I * 2, 128))
+            if (!encode_bf16_2d(&tmW2[m], w2[m], I, (uint64_t)E * H, (uint64_t)I * 2, 128))
                 return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (w2[%d])", m);
         TcGemmArgs g2{h->offsets, h->tiles_tc, E, M, I / kTcBK, H / 128, H, 0, I,
                       h->obuf, (int64_t)H, 0, active * (H / 128), h->err, h->limit_ns};
-        if ((e = timed(h, kSlotGemm2, s, [&] { return launch_tc_small_down(g2, tmX, tmW, h->num_sms, s); })) !=
-            cudaSuccess)
-            return cuda_err(h, e, "GEMM2 launch");
+        // both GEMMs in one cooperative launch (the router zeroed h->done)
+        if ((e = timed(h, kSlotGemm1, s, [&] {
+                 return launch_tc_small_fused(g1, tmX, tmW, g2, tmX2, tmW2, h->done, h->num_sms, s);
+             })) != cudaSuccess)
+            return cuda_err(h, e, "fused GEMM launch");
         if (Is > 0) {
             if (!encode_bf16_2d(&tmX, x, H, T, (uint64_t)H * 2, kSmallTokens) ||
                 !encode_bf16_2d(&tmW[0], sw13, H, 2 * (uint64_t)Is, (uint64_t)H * 2, 64))
@@ -390,7 +391,7 @@ moe_status moe_create(const moe_config* cfg, moe_handle** out) {
     const size_t o_ids = take(R * 4), o_topw = take(R * 4), o_perm = take(R * 4), o_inv = take(R * 4);
     const size_t o_off = take((E + 1) * 4), o_ttc = take((E + 1) * 4), o_tsi = take((E + 1) * 4);
     const size_t o_smeta = take(6 * 4);
-    const size_t o_hist = take(NB * E * 4), o_base = take(NB * E * 4);
+    const size_t o_hist = take(NB * E * 4), o_base = take(NB * E * 4), o_done = take(E * 4);
     const size_t o_xp = take(R * H * esz), o_h = take(R * M * I * esz), o_o = take(R * H * esz);
     const size_t o_hs = take(T * Is * esz), o_s = take(Is ? T * H * esz : 0);
     const size_t o_xst = take(T * H * esz), o_yst = take(T * H * esz);
@@ -412,6 +413,7 @@ moe_status moe_create(const moe_config* cfg, moe_handle** out) {
     h->shared_meta = reinterpret_cast<int32_t*>(b + o_smeta);
     h->blk_hist = reinterpret_cast<int32_t*>(b + o_hist);
     h->blk_base = reinterpret_cast<int32_t*>(b + o_base);
+    h->done = reinterpret_cast<int*>(b + o_done);
     h->xp = b + o_xp;
     h->hbuf = b + o_h;
     h->obuf = b + o_o;
