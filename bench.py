@@ -235,7 +235,8 @@ def roofline_of(wl, prof, ids_pool, steps, peaks, sha):
     if wl.name == "decode":
         bound, unit, peak = "hbm", "GB/s", peaks["hbm"]
         algo = {
-            "gemm1_swiglu": (touched * 3 * I * H * esz * M + 2 * R * H * esz + 2 * R * M * I * esz) if fused
+            "gemm1_swiglu": (touched * 3 * I * H * esz * M + 3 * R * H * esz + 2 * R * M * I * esz + wl.T * H * esz)
+            if fused
             else (touched * 2 * I * H * esz * M + R * H * esz + R * M * I * esz),
             "gemm2_down": touched * H * I * esz * M + R * M * I * esz + R * H * esz,
             "gather": 2 * R * H * esz,
@@ -250,7 +251,7 @@ def roofline_of(wl, prof, ids_pool, steps, peaks, sha):
                 "shared_gemm2": 2 * wl.T * H * wl.shared_inter}.get(dom)
         achieved = algo / per_launch_s / 1e12 if algo else None
     traffic = recorded_traffic(wl.name, dom, sha)
-    return {"kernel": dom + ("+gemm2_down (one launch)" if fused and dom == "gemm1_swiglu" else ""),
+    return {"kernel": dom + ("+gemm2_down+finalize (one launch)" if fused and dom == "gemm1_swiglu" else ""),
             "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
             "frac": (achieved / peak) if achieved else None, "traffic": traffic,
             "algorithmic_per_launch": algo, "launch_ms": per_launch_s * 1e3,

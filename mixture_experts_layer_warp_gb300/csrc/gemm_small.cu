@@ -22,7 +22,9 @@
 // of after the slowest one, and one kernel boundary disappears. All CTAs are
 // co-resident (cooperative launch, one CTA per SM) and each CTA takes its tiles
 // in increasing order, so every awaited SwiGLU tile is already owned by a
-// running CTA that reaches it first.
+// running CTA that reaches it first. After its tiles, each CTA's epilogue
+// warps run finalize items, each gated on the down tiles of its token's
+// experts, so the finalize needs no launch of its own.
 // Structure: 8-stage TMA ring, one MMA issuer, four epilogue warps on a
 // double-buffered 2 x 16-column TMEM accumulator. All waits are bounded.
 #include <cooperative_groups.h>
@@ -59,14 +61,16 @@ struct Ctl {
     int tiles[kMaxExperts + 1];
     float up[64][kTok + 1];
     int ep_ok[4];
+    int fin_fail;
 };
 
 constexpr int kSmemBytes = kStages * kStageBytes + (int)sizeof(Ctl) + 1024;
 
 struct SmallParams {
-    TcGemmArgs g1;   // SwiGLU tiles (unused in kDownOnly)
-    TcGemmArgs g2;   // down tiles (unused in kSwiGLUOnly)
-    int* done;       // kFused: per-expert count of finished SwiGLU tiles, zero at launch
+    TcGemmArgs g1;     // SwiGLU tiles (unused in kDownOnly)
+    TcGemmArgs g2;     // down tiles (unused in kSwiGLUOnly)
+    int* done;         // kFused: [E] finished SwiGLU tiles, then [E] finished down tiles; zero at launch
+    FinalizeArgs fin;  // kFused: the finalize run after the tiles (fin.y null = none)
 };
 
 struct SmallMaps {
@@ -91,6 +95,92 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
 
 __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// The finalize ("HunyuanImage3 Hybrid Parallelism", section 6.1: routing scale
+// applied once, top-k reduced once) as the fused kernel's last phase, run by
+// the four epilogue warps: item (token t, 1024 columns) waits until the down
+// tiles of t's k experts have stored their o rows, then
+//     y[t] = sum_j w[t][j] * o[inv[t*k + j]] (+ shared[t]), fp32 accumulate.
+// o rows come from other CTAs, so they are read through L2 (ld.global.cg).
+__device__ __forceinline__ void finalize_items(Ctl& c, const SmallParams& p) {
+    const FinalizeArgs& f = p.fin;
+    const int tid = threadIdx.x - 128;  // 0..127: the epilogue warps
+    const int G = p.g1.G;
+    const int target = p.g2.n_tiles;    // down tiles per expert (one row block each)
+    const int nvec = f.H / 8;
+    const int chunks = (nvec + 127) / 128;
+    const int items = f.T * chunks;
+    const __nv_bfloat16* o = static_cast<const __nv_bfloat16*>(f.o);
+    const __nv_bfloat16* sh = static_cast<const __nv_bfloat16*>(f.shared);
+    __nv_bfloat16* y = static_cast<__nv_bfloat16*>(f.y);
+    for (int item = blockIdx.x; item < items; item += gridDim.x) {
+        const int t = item / chunks, ch = item % chunks;
+        if (tid < f.k) {
+            const int pos = f.inv[(int64_t)t * f.k + tid];
+            int lo = 0, hi = G - 1;  // the expert whose segment holds sorted position pos
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (c.seg[mid] <= pos)
+                    lo = mid;
+                else
+                    hi = mid - 1;
+            }
+            const int* cnt = p.done + G + lo;
+            if (ld_acquire(cnt) < target) {
+                const uint64_t t0 = ptx::globaltimer();
+                uint32_t it = 0;
+                while (ld_acquire(cnt) < target) {
+                    if ((++it & 15u) == 0u && (c.abort || ptx::globaltimer() - t0 > p.g2.limit_ns)) {
+                        c.fin_fail = 1;
+                        fail(c, p.g2.err);
+                        break;
+                    }
+                    __nanosleep(64);
+                }
+            }
+        }
+        epilogue_bar();
+        if (c.fin_fail) break;
+        const int v = ch * 128 + tid;
+        if (v < nvec) {
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            uint4 u[kMaxTopK];  // all k rows in flight before the arithmetic
+#pragma unroll
+            for (int j = 0; j < kMaxTopK; ++j)
+                if (j < f.k)
+                    u[j] = __ldcg(reinterpret_cast<const uint4*>(o + (int64_t)f.inv[(int64_t)t * f.k + j] * f.H) + v);
+#pragma unroll
+            for (int j = 0; j < kMaxTopK; ++j) {
+                if (j < f.k) {
+                    const float wj = f.w[(int64_t)t * f.k + j];
+                    const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&u[j]);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 x2 = __bfloat1622float2(hv[i]);
+                        acc[2 * i] = fmaf(wj, x2.x, acc[2 * i]);
+                        acc[2 * i + 1] = fmaf(wj, x2.y, acc[2 * i + 1]);
+                    }
+                }
+            }
+            if (sh != nullptr) {
+                const uint4 u = *(reinterpret_cast<const uint4*>(sh + (int64_t)t * f.H) + v);
+                const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 x2 = __bfloat1622float2(hv[i]);
+                    acc[2 * i] += x2.x;
+                    acc[2 * i + 1] += x2.y;
+                }
+            }
+            uint4 out;
+            __nv_bfloat162* ov = reinterpret_cast<__nv_bfloat162*>(&out);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) ov[i] = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+            *(reinterpret_cast<uint4*>(y + (int64_t)t * f.H) + v) = out;
+        }
+        epilogue_bar();
+    }
 }
 
 // Tile list position -> (is a SwiGLU tile, tile) for the given mode.
@@ -131,6 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::mbar_init(ptx::smem_u32(&c.drain), 1);
         c.abort = 0;
+        c.fin_fail = 0;
         ptx::fence_mbar_init();
     }
     for (int i = threadIdx.x; i <= a0.G; i += kThreads) {
@@ -317,11 +408,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int64_t col = (int64_t)t.nt * kM + r;
                 for (int j = 0; j < cnt; ++j)
                     out[(int64_t)(t.row0 + j) * g.out_ld + col] = __float2bfloat16_rn(__uint_as_float(v[j]));
+                if (MODE == kFused) {
+                    epilogue_bar();
+                    if (threadIdx.x == 128) {
+                        __threadfence();
+                        atomicAdd(p.done + p.g1.G + t.g, 1);
+                    }
+                }
             }
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&c.tempty[acc]));
         }
+        if (MODE == kFused && p.fin.y != nullptr) finalize_items(c, p);
     }
 
     ptx::tc_fence_before();
@@ -373,7 +472,7 @@ cudaError_t launch_tc_small_swiglu(const TcGemmArgs& a, const CUtensorMap& tmX, 
     SmallMaps maps;
     fill_maps(maps, tmX, tmW, a.n_micro, true);
     fill_maps(maps, tmX, tmW, 1, false);  // unused slots
-    SmallParams p{a, a, nullptr};
+    SmallParams p{a, a, nullptr, FinalizeArgs{}};
     return launch_small<kSwiGLUOnly>(maps, p, a.max_tiles, num_sms, s);
 }
 
@@ -382,18 +481,21 @@ cudaError_t launch_tc_small_down(const TcGemmArgs& a, const CUtensorMap& tmX, co
     SmallMaps maps;
     fill_maps(maps, tmX, tmW, a.n_micro, false);
     fill_maps(maps, tmX, tmW, 1, true);  // unused slots
-    SmallParams p{a, a, nullptr};
+    SmallParams p{a, a, nullptr, FinalizeArgs{}};
     return launch_small<kDownOnly>(maps, p, a.max_tiles, num_sms, s);
 }
 
 cudaError_t launch_tc_small_fused(const TcGemmArgs& g1, const CUtensorMap& tmX1, const CUtensorMap* tmW1,
                                   const TcGemmArgs& g2, const CUtensorMap& tmX2, const CUtensorMap* tmW2,
-                                  int* done, int num_sms, cudaStream_t s) {
+                                  const FinalizeArgs& fin, int* done, int num_sms, cudaStream_t s) {
     SmallMaps maps;
     fill_maps(maps, tmX1, tmW1, g1.n_micro, true);
     fill_maps(maps, tmX2, tmW2, g2.n_micro, false);
-    SmallParams p{g1, g2, done};
-    return launch_small<kFused>(maps, p, g1.max_tiles + g2.max_tiles, num_sms, s);
+    SmallParams p{g1, g2, done, fin};
+    // enough CTAs for the finalize items as well (T tokens x 1024-column chunks)
+    const int fin_items = fin.y ? fin.T * ((fin.H / 8 + 127) / 128) : 0;
+    const int work = g1.max_tiles + g2.max_tiles > fin_items ? g1.max_tiles + g2.max_tiles : fin_items;
+    return launch_small<kFused>(maps, p, work, num_sms, s);
 }
 
 }  // namespace moe

@@ -57,9 +57,13 @@ struct RouterTcArgs {
     int32_t* shared_tiles_simt;  // [2]
     int32_t* perm;          // [T*k]
     int32_t* inv;           // [T*k]
-    int32_t* zero_counters; // [E] set to 0 by the single-CTA paths, or null
+    int32_t* zero_counters; // [2E] set to 0 by the single-CTA paths, or null
     int* err;
     uint64_t limit_ns;
+    // small-batch cluster router only: after placement, copy xp[i] = x[perm[i]/k]
+    const void* gather_x;   // [T][row_bytes] or null
+    void* gather_xp;        // [T*k][row_bytes]
+    int gather_row_bytes;
 };
 // tmX: x [T][H] bf16, box {64, 128}; tmW: Wr [E][H] bf16, box {64, 64}.
 cudaError_t launch_router_tc(const RouterTcArgs& a, const CUtensorMap& tmX, const CUtensorMap& tmW,
@@ -105,6 +109,18 @@ struct GatherArgs {
 };
 cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s);
 
+// ------------------------------------------------------------ finalize
+struct FinalizeArgs {
+    const void* o;            // [R][H] expert outputs (bf16 or f32)
+    const int32_t* inv;       // [R]
+    const float* w;           // [T][k]
+    const void* shared;       // [T][H] or null
+    int T, k, H;
+    bool bf16;
+    void* y;                  // [T][H]
+};
+cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t s);
+
 // ------------------------------------------------------- tcgen05 GEMMs
 constexpr int kTcBM = 128;   // rows per tile (MMA M)
 constexpr int kTcBK = 64;    // K per stage: 64 bf16 = one 128-byte swizzled row
@@ -144,12 +160,14 @@ cudaError_t launch_tc_small_swiglu(const TcGemmArgs& a, const CUtensorMap& tmX, 
                                    int num_sms, cudaStream_t s);
 cudaError_t launch_tc_small_down(const TcGemmArgs& a, const CUtensorMap& tmX, const CUtensorMap* tmW,
                                  int num_sms, cudaStream_t s);
-// Both GEMMs of the routed experts in one persistent cooperative launch: the
-// down tiles of expert e start once the SwiGLU tiles of e have stored h.
-// done[E] must be zero at launch (the small-batch router zeroes it).
+// Both GEMMs of the routed experts and the finalize in one persistent
+// cooperative launch: the down tiles of expert e start once the SwiGLU tiles
+// of e have stored h, and a token's finalize once the down tiles of its k
+// experts have stored o. done[2E] must be zero at launch (the small-batch
+// router zeroes it).
 cudaError_t launch_tc_small_fused(const TcGemmArgs& g1, const CUtensorMap& tmX1, const CUtensorMap* tmW1,
                                   const TcGemmArgs& g2, const CUtensorMap& tmX2, const CUtensorMap* tmW2,
-                                  int* done, int num_sms, cudaStream_t s);
+                                  const FinalizeArgs& fin, int* done, int num_sms, cudaStream_t s);
 
 // ---------------------------------------------------- fp32 SIMT GEMMs
 constexpr int kSimtBM = 32;
@@ -174,17 +192,7 @@ struct SimtGemmArgs {
 cudaError_t launch_simt_gemm_swiglu(const SimtGemmArgs& a, cudaStream_t s);
 cudaError_t launch_simt_gemm_down(const SimtGemmArgs& a, cudaStream_t s);
 
-// ------------------------------------------------------------ finalize
-struct FinalizeArgs {
-    const void* o;            // [R][H] expert outputs (bf16 or f32)
-    const int32_t* inv;       // [R]
-    const float* w;           // [T][k]
-    const void* shared;       // [T][H] or null
-    int T, k, H;
-    bool bf16;
-    void* y;                  // [T][H]
-};
-cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t s);
+
 
 // ------------------------------------------------------------- routing
 // The routing sequence shared by moe_route, moe_forward and moe_route_noalloc:
@@ -209,7 +217,9 @@ struct RoutingJob {
     int32_t* blk_base;        // same
     int* err;
     uint64_t limit_ns;
-    int32_t* zero_counters;   // [E] zeroed when routing runs in one CTA (T <= 128), or null
+    int32_t* zero_counters;   // [2E] zeroed when routing runs in one CTA (T <= 128), or null
+    // T <= kSmallTokens (bf16): the router also gathers xp[i] = x[perm[i]/k]
+    void* gather_xp;          // or null
 };
 
 // Optional callbacks around every kernel launch (timing, counting).

@@ -156,11 +156,12 @@ moe_status check_call(moe_handle* h, const void* x, const void* router_w, int32_
 
 // Router, scan and placement: leaves ids, topw, offsets, tiles, perm and inv in the workspace.
 moe_status run_routing(moe_handle* h, const void* x, const void* router_w, const float* bias, int32_t T,
-                       float* logits, cudaStream_t s) {
+                       float* logits, cudaStream_t s, bool gather_xp = false) {
     const moe_config& c = h->cfg;
     RoutingJob j{x, router_w, bias, T, c.hidden, c.num_experts, c.top_k, c.dtype == MOE_BF16, h->ids, h->topw,
                  logits, h->perm, h->inv, h->offsets, h->tiles_tc, h->tiles_simt, h->shared_meta, h->blk_hist,
-                 h->blk_base, h->err, h->limit_ns, h->done};
+                 h->blk_base, h->err, h->limit_ns, h->done,
+                 (c.dtype == MOE_BF16 && T <= kSmallTokens && gather_xp) ? h->xp : nullptr};
     LaunchHook hook{h, hook_before, hook_after};
     cudaError_t e = enqueue_routing(j, s, &hook);
     if (e == cudaErrorInvalidValue) return set_err(h, MOE_ERR_CUDA, "router tensor map encode failed");
@@ -175,11 +176,15 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
     const int H = c.hidden, E = c.num_experts, k = c.top_k, I = c.inter, M = c.n_micro, Is = c.shared_inter;
     const int64_t R = (int64_t)T * k;
     cudaError_t e;
-    moe_status st = run_routing(h, x, router_w, bias, T, nullptr, s);
+    const bool small_bf16 = c.dtype == MOE_BF16 && T <= kSmallTokens;
+    moe_status st = run_routing(h, x, router_w, bias, T, nullptr, s, small_bf16);
     if (st != MOE_OK) return st;
 
-    GatherArgs ga{x, h->perm, (int)R, k, (uint32_t)(H * h->esz), h->xp, h->err, h->limit_ns, h->num_sms};
-    if ((e = timed(h, kSlotGather, s, [&] { return launch_gather(ga, s); })) != cudaSuccess) return cuda_err(h, e, "gather launch");
+    if (!small_bf16) {  // small bf16 batches were gathered by the router
+        GatherArgs ga{x, h->perm, (int)R, k, (uint32_t)(H * h->esz), h->xp, h->err, h->limit_ns, h->num_sms};
+        if ((e = timed(h, kSlotGather, s, [&] { return launch_gather(ga, s); })) != cudaSuccess)
+            return cuda_err(h, e, "gather launch");
+    }
 
     const int routed_tiles_tc = (int)(R / kTcBM) + E;  // bound on sum of ceil(count/128)
     if (c.dtype == MOE_BF16 && T <= kSmallTokens) {
@@ -201,29 +206,32 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
                 return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (w2[%d])", m);
         TcGemmArgs g2{h->offsets, h->tiles_tc, E, M, I / kTcBK, H / 128, H, 0, I,
                       h->obuf, (int64_t)H, 0, active * (H / 128), h->err, h->limit_ns};
-        // both GEMMs in one cooperative launch (the router zeroed h->done)
-        if ((e = timed(h, kSlotGemm1, s, [&] {
-                 return launch_tc_small_fused(g1, tmX, tmW, g2, tmX2, tmW2, h->done, h->num_sms, s);
-             })) != cudaSuccess)
-            return cuda_err(h, e, "fused GEMM launch");
         if (Is > 0) {
-            if (!encode_bf16_2d(&tmX, x, H, T, (uint64_t)H * 2, kSmallTokens) ||
-                !encode_bf16_2d(&tmW[0], sw13, H, 2 * (uint64_t)Is, (uint64_t)H * 2, 64))
+            CUtensorMap sX, sW[1];
+            if (!encode_bf16_2d(&sX, x, H, T, (uint64_t)H * 2, kSmallTokens) ||
+                !encode_bf16_2d(&sW[0], sw13, H, 2 * (uint64_t)Is, (uint64_t)H * 2, 64))
                 return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (shared GEMM1)");
             TcGemmArgs s1{h->shared_meta, h->shared_meta + 2, 1, 1, H / kTcBK, Is / 64, 2 * Is, Is, 0,
                           h->hs, (int64_t)Is, 0, Is / 64, h->err, h->limit_ns};
             if ((e = timed(h, kSlotSharedGemm1, s,
-                           [&] { return launch_tc_small_swiglu(s1, tmX, tmW, h->num_sms, s); })) != cudaSuccess)
+                           [&] { return launch_tc_small_swiglu(s1, sX, sW, h->num_sms, s); })) != cudaSuccess)
                 return cuda_err(h, e, "shared GEMM1 launch");
-            if (!encode_bf16_2d(&tmX, h->hs, Is, T, (uint64_t)Is * 2, kSmallTokens) ||
-                !encode_bf16_2d(&tmW[0], sw2, Is, H, (uint64_t)Is * 2, 128))
+            if (!encode_bf16_2d(&sX, h->hs, Is, T, (uint64_t)Is * 2, kSmallTokens) ||
+                !encode_bf16_2d(&sW[0], sw2, Is, H, (uint64_t)Is * 2, 128))
                 return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (shared GEMM2)");
             TcGemmArgs s2{h->shared_meta, h->shared_meta + 2, 1, 1, Is / kTcBK, H / 128, H, 0, Is,
                           h->sbuf, (int64_t)H, 0, H / 128, h->err, h->limit_ns};
             if ((e = timed(h, kSlotSharedGemm2, s,
-                           [&] { return launch_tc_small_down(s2, tmX, tmW, h->num_sms, s); })) != cudaSuccess)
+                           [&] { return launch_tc_small_down(s2, sX, sW, h->num_sms, s); })) != cudaSuccess)
                 return cuda_err(h, e, "shared GEMM2 launch");
         }
+        // both GEMMs and the finalize in one cooperative launch (the router
+        // zeroed h->done); the shared expert's GEMMs ran first
+        FinalizeArgs fin{h->obuf, h->inv, h->topw, Is > 0 ? h->sbuf : nullptr, T, k, H, true, y};
+        if ((e = timed(h, kSlotGemm1, s, [&] {
+                 return launch_tc_small_fused(g1, tmX, tmW, g2, tmX2, tmW2, fin, h->done, h->num_sms, s);
+             })) != cudaSuccess)
+            return cuda_err(h, e, "fused GEMM launch");
     } else if (c.dtype == MOE_BF16) {
         CUtensorMap tmA, tmB[kMaxMicro];
         // GEMM1 + SwiGLU: xp [R][H] x w13[m] [E*2I][H] -> h [R][M*I]
@@ -321,8 +329,11 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
             if ((e = timed(h, kSlotSharedGemm2, s, [&] { return launch_simt_gemm_down(s2, s); })) != cudaSuccess) return cuda_err(h, e, "f32 shared GEMM2");
         }
     }
-    FinalizeArgs fa{h->obuf, h->inv, h->topw, Is > 0 ? h->sbuf : nullptr, T, k, H, c.dtype == MOE_BF16, y};
-    if ((e = timed(h, kSlotFinalize, s, [&] { return launch_finalize(fa, s); })) != cudaSuccess) return cuda_err(h, e, "finalize launch");
+    if (!small_bf16) {  // small bf16 batches finalize inside the fused GEMM launch
+        FinalizeArgs fa{h->obuf, h->inv, h->topw, Is > 0 ? h->sbuf : nullptr, T, k, H, c.dtype == MOE_BF16, y};
+        if ((e = timed(h, kSlotFinalize, s, [&] { return launch_finalize(fa, s); })) != cudaSuccess)
+            return cuda_err(h, e, "finalize launch");
+    }
     return MOE_OK;
 }
 
@@ -391,7 +402,7 @@ moe_status moe_create(const moe_config* cfg, moe_handle** out) {
     const size_t o_ids = take(R * 4), o_topw = take(R * 4), o_perm = take(R * 4), o_inv = take(R * 4);
     const size_t o_off = take((E + 1) * 4), o_ttc = take((E + 1) * 4), o_tsi = take((E + 1) * 4);
     const size_t o_smeta = take(6 * 4);
-    const size_t o_hist = take(NB * E * 4), o_base = take(NB * E * 4), o_done = take(E * 4);
+    const size_t o_hist = take(NB * E * 4), o_base = take(NB * E * 4), o_done = take(2 * E * 4);
     const size_t o_xp = take(R * H * esz), o_h = take(R * M * I * esz), o_o = take(R * H * esz);
     const size_t o_hs = take(T * Is * esz), o_s = take(Is ? T * H * esz : 0);
     const size_t o_xst = take(T * H * esz), o_yst = take(T * H * esz);
