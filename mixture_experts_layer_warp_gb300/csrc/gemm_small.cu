@@ -62,6 +62,11 @@ struct Ctl {
     float up[64][kTok + 1];
     int ep_ok[4];
     int fin_fail;
+    // kFused: tiles fetched from a global counter by the producer and handed to
+    // the MMA and epilogue warps through this ring
+    uint64_t tq_full[4];
+    uint64_t tq_empty[4];
+    int tq[4];
 };
 
 constexpr int kSmemBytes = kStages * kStageBytes + (int)sizeof(Ctl) + 1024;
@@ -69,7 +74,8 @@ constexpr int kSmemBytes = kStages * kStageBytes + (int)sizeof(Ctl) + 1024;
 struct SmallParams {
     TcGemmArgs g1;     // SwiGLU tiles (unused in kDownOnly)
     TcGemmArgs g2;     // down tiles (unused in kSwiGLUOnly)
-    int* done;         // kFused: [E] finished SwiGLU tiles, then [E] finished down tiles; zero at launch
+    int* done;         // kFused: [E] finished SwiGLU tiles, [E] finished down tiles, [1] next
+                       // tile to hand out; zero at launch
     FinalizeArgs fin;  // kFused: the finalize run after the tiles (fin.y null = none)
 };
 
@@ -200,6 +206,59 @@ __device__ __forceinline__ Tile locate(int tile, const Ctl& c, const SmallParams
                   : decode_group_tile(tile - n1, c.seg, c.tiles, p.g2.G, p.g2.n_tiles, p.g2.n_micro, false, kTcBM);
 }
 
+// Tile sequence of one CTA. Static modes stride over the list (blockIdx.x,
+// + gridDim.x, ...). The fused mode hands tiles out dynamically: the producer
+// takes the next list position from a global counter (so every position is
+// taken in increasing order and CTAs that drew cheap tiles take more) and
+// passes it through the shared ring to the MMA and epilogue warps; -1 ends.
+struct TileStream {
+    int slot = 0;
+    uint32_t phase = 0;
+    int next_static;
+};
+
+// Producer side (one thread). Returns the tile to process, or -1 when done or failed.
+template <int MODE>
+__device__ __forceinline__ int produce_tile(Ctl& c, const SmallParams& p, TileStream& ts, int total,
+                                            uint64_t limit_ns, bool& ok) {
+    if (MODE != kFused) {
+        const int t = ts.next_static;
+        ts.next_static += gridDim.x;
+        return t < total ? t : -1;
+    }
+    int t = atomicAdd(p.done + 2 * p.g1.G, 1);
+    if (t >= total) t = -1;
+    if (!ptx::mbar_wait(ptx::smem_u32(&c.tq_empty[ts.slot]), ts.phase ^ 1u, limit_ns, &c.abort)) {
+        ok = false;
+        t = -1;
+    }
+    c.tq[ts.slot] = t;
+    ptx::mbar_arrive(ptx::smem_u32(&c.tq_full[ts.slot]));
+    if (++ts.slot == 4) {
+        ts.slot = 0;
+        ts.phase ^= 1u;
+    }
+    return t;
+}
+
+// Consumer side (one thread per consuming warp). Returns -1 when done or failed.
+template <int MODE>
+__device__ __forceinline__ int consume_tile(Ctl& c, TileStream& ts, int total, uint64_t limit_ns) {
+    if (MODE != kFused) {
+        const int t = ts.next_static;
+        ts.next_static += gridDim.x;
+        return t < total ? t : -1;
+    }
+    int t = -1;
+    if (ptx::mbar_wait(ptx::smem_u32(&c.tq_full[ts.slot]), ts.phase, limit_ns, &c.abort)) t = c.tq[ts.slot];
+    ptx::mbar_arrive(ptx::smem_u32(&c.tq_empty[ts.slot]));
+    if (++ts.slot == 4) {
+        ts.slot = 0;
+        ts.phase ^= 1u;
+    }
+    return t;
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_small_kernel(const __grid_constant__ SmallMaps maps, const SmallParams p) {
@@ -220,6 +279,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(ptx::smem_u32(&c.tempty[b]), 4);
         }
         ptx::mbar_init(ptx::smem_u32(&c.drain), 1);
+        for (int q = 0; q < 4; ++q) {
+            ptx::mbar_init(ptx::smem_u32(&c.tq_full[q]), 1);
+            ptx::mbar_init(ptx::smem_u32(&c.tq_empty[q]), 5);  // MMA issuer + four epilogue warps
+        }
         c.abort = 0;
         c.fin_fail = 0;
         ptx::fence_mbar_init();
@@ -252,7 +315,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t phase = 0, last_par[kStages];
         int issued = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        TileStream ts;
+        ts.next_static = blockIdx.x;
+        for (;;) {
+            const int tile = produce_tile<MODE>(c, p, ts, total, a0.limit_ns, ok);
+            if (tile < 0) break;
             bool sw;
             const Tile t = locate<MODE>(tile, c, p, sw);
             const TcGemmArgs& g = sw ? p.g1 : p.g2;
@@ -304,6 +371,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+            if (!ok) {
+                // tell the consumers to stop: a -1 in the ring, or the abort flag
+                c.abort = 1;
+                if (MODE == kFused) produce_tile<MODE>(c, p, ts, 0, a0.limit_ns, ok);
+                break;
+            }
         }
         if (!ok) {
             fail(c, a0.err);
@@ -315,8 +388,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
-        int local = 0;
-        for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++local) {
+        TileStream ts;
+        ts.next_static = blockIdx.x;
+        for (int local = 0; ok; ++local) {
+            const int tile = consume_tile<MODE>(c, ts, total, a0.limit_ns);
+            if (tile < 0) break;
             bool sw;
             locate<MODE>(tile, c, p, sw);
             const TcGemmArgs& g = sw ? p.g1 : p.g2;
@@ -360,8 +436,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------ epilogue
         const int q = warp - 4;            // TMEM lanes 32q .. 32q+31 = weight rows
         const int r = q * 32 + lane;
-        int local = 0;
-        for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
+        TileStream ts;
+        ts.next_static = blockIdx.x;
+        for (int local = 0;; ++local) {
+            int tile = -1;
+            if (lane == 0) tile = consume_tile<MODE>(c, ts, total, a0.limit_ns);
+            tile = __shfl_sync(0xffffffffu, tile, 0);
+            if (tile < 0) break;
             bool sw;
             const Tile t = locate<MODE>(tile, c, p, sw);
             const TcGemmArgs& g = sw ? p.g1 : p.g2;

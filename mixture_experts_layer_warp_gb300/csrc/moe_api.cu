@@ -402,7 +402,7 @@ moe_status moe_create(const moe_config* cfg, moe_handle** out) {
     const size_t o_ids = take(R * 4), o_topw = take(R * 4), o_perm = take(R * 4), o_inv = take(R * 4);
     const size_t o_off = take((E + 1) * 4), o_ttc = take((E + 1) * 4), o_tsi = take((E + 1) * 4);
     const size_t o_smeta = take(6 * 4);
-    const size_t o_hist = take(NB * E * 4), o_base = take(NB * E * 4), o_done = take(2 * E * 4);
+    const size_t o_hist = take(NB * E * 4), o_base = take(NB * E * 4), o_done = take((2 * E + 1) * 4);
     const size_t o_xp = take(R * H * esz), o_h = take(R * M * I * esz), o_o = take(R * H * esz);
     const size_t o_hs = take(T * Is * esz), o_s = take(Is ? T * H * esz : 0);
     const size_t o_xst = take(T * H * esz), o_yst = take(T * H * esz);

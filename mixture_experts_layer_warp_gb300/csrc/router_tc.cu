@@ -182,7 +182,8 @@ __device__ __forceinline__ void finish_single(const RouterTcArgs& a, const int* 
     }
     __syncthreads();
     if ((int)threadIdx.x <= E) a.offsets[threadIdx.x] = off[threadIdx.x];
-    if (a.zero_counters != nullptr && (int)threadIdx.x < 2 * E) a.zero_counters[threadIdx.x] = 0;
+    if (a.zero_counters != nullptr)
+        for (int i = threadIdx.x; i <= 2 * E; i += blockDim.x) a.zero_counters[i] = 0;
     place_chunk<NW>(sid, a.T * a.k, 0, E, (int64_t)a.T * a.k, [&](int e) { return off[e]; }, cnt, run, a.perm,
                     a.inv, a.err);
 }

@@ -143,3 +143,18 @@ def test_bounded_wait_reports_timeout_instead_of_hanging():
     # the context is still usable afterwards
     x = torch.ones(4, device="cuda")
     assert x.sum().item() == 4.0
+
+
+def test_back_to_back_small_batches_reuse_the_workspace():
+    """Consecutive decode-sized calls on one handle (per-call counters must be
+    reset by each call) give the same result as fresh handles."""
+    wl = W.Workload("b2b", 8, 512, 64, 8, 128, 1)
+    inps = [parity.to_device(W.make_inputs(wl, seed=s)) for s in (31, 32, 33)]
+    layer = _layer(wl)
+    ys = [_forward(layer, d).clone() for d in inps + inps]
+    layer.close()
+    for i, d in enumerate(inps):
+        fresh = _layer(wl)
+        ref = _forward(fresh, d)
+        fresh.close()
+        assert torch.equal(ys[i], ref) and torch.equal(ys[i + 3], ref)
