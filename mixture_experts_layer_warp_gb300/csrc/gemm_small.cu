@@ -20,11 +20,13 @@
 // their h rows (a per-expert counter, bounded wait), so the down projection's
 // weight stream starts on SMs as soon as they run out of SwiGLU tiles instead
 // of after the slowest one, and one kernel boundary disappears. All CTAs are
-// co-resident (cooperative launch, one CTA per SM) and each CTA takes its tiles
-// in increasing order, so every awaited SwiGLU tile is already owned by a
-// running CTA that reaches it first. After its tiles, each CTA's epilogue
-// warps run finalize items, each gated on the down tiles of its token's
-// experts, so the finalize needs no launch of its own.
+// co-resident (cooperative launch, one CTA per SM) and tiles are handed out in
+// increasing order, so every awaited SwiGLU tile is already owned by a running
+// CTA. Before its tiles, each CTA's epilogue warps gather a share of the routed
+// token rows (a SwiGLU tile waits only for its expert's rows, and its weight
+// stages are issued meanwhile); after its tiles they run finalize items, each
+// gated on the down tiles of its token's experts. The whole routed layer after
+// routing is therefore one launch.
 // Structure: 8-stage TMA ring, one MMA issuer, four epilogue warps on a
 // double-buffered 2 x 16-column TMEM accumulator. All waits are bounded.
 #include <cooperative_groups.h>
@@ -75,8 +77,14 @@ struct SmallParams {
     TcGemmArgs g1;     // SwiGLU tiles (unused in kDownOnly)
     TcGemmArgs g2;     // down tiles (unused in kSwiGLUOnly)
     int* done;         // kFused: [E] finished SwiGLU tiles, [E] finished down tiles, [1] next
-                       // tile to hand out; zero at launch
+                       // tile to hand out, [E] gathered rows; zero at launch
     FinalizeArgs fin;  // kFused: the finalize run after the tiles (fin.y null = none)
+    // kFused: the gather xp[i] = x[perm[i] / k] run at the start (x null = none)
+    const void* gx;
+    void* gxp;
+    const int32_t* gperm;
+    int gk;
+    int grow_bytes;
 };
 
 struct SmallMaps {
@@ -103,6 +111,50 @@ __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// Expert whose segment [seg[g], seg[g+1]) holds sorted position pos.
+__device__ __forceinline__ int expert_of(const int* seg, int G, int pos) {
+    int lo = 0, hi = G - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (seg[mid] <= pos)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
+// The gather xp[i] = x[perm[i] / k] (blog section 6.1: index_select once), as
+// the fused kernel's first phase, run by the four epilogue warps: CTA b copies
+// rows b, b + gridDim.x, ... and counts each finished row for its expert, so a
+// SwiGLU tile only waits for the rows of its own expert.
+__device__ __forceinline__ void gather_rows(const Ctl& c, const SmallParams& p) {
+    const int tid = threadIdx.x - 128;
+    const int R = c.seg[p.g1.G];
+    const int nvec = p.grow_bytes / 16;
+    const uint4* __restrict__ src = static_cast<const uint4*>(p.gx);
+    uint4* __restrict__ dst = static_cast<uint4*>(p.gxp);
+    for (int i = blockIdx.x; i < R; i += gridDim.x) {
+        const int64_t tok = p.gperm[i] / p.gk;
+        constexpr int kBatch = 8;
+        for (int v0 = tid; v0 < nvec; v0 += 128 * kBatch) {
+            uint4 buf[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u)
+                if (v0 + u * 128 < nvec) buf[u] = src[tok * nvec + v0 + u * 128];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u)
+                if (v0 + u * 128 < nvec) dst[(int64_t)i * nvec + v0 + u * 128] = buf[u];
+        }
+        fence_proxy_async_global();  // the rows are read next by TMA (async proxy)
+        epilogue_bar();
+        if (tid == 0) {
+            __threadfence();
+            atomicAdd(p.done + 2 * p.g1.G + 1 + expert_of(c.seg, p.g1.G, i), 1);
+        }
+    }
+}
+
 // The finalize ("HunyuanImage3 Hybrid Parallelism", section 6.1: routing scale
 // applied once, top-k reduced once) as the fused kernel's last phase, run by
 // the four epilogue warps: item (token t, 1024 columns) waits until the down
@@ -123,16 +175,7 @@ __device__ __forceinline__ void finalize_items(Ctl& c, const SmallParams& p) {
     for (int item = blockIdx.x; item < items; item += gridDim.x) {
         const int t = item / chunks, ch = item % chunks;
         if (tid < f.k) {
-            const int pos = f.inv[(int64_t)t * f.k + tid];
-            int lo = 0, hi = G - 1;  // the expert whose segment holds sorted position pos
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (c.seg[mid] <= pos)
-                    lo = mid;
-                else
-                    hi = mid - 1;
-            }
-            const int* cnt = p.done + G + lo;
+            const int* cnt = p.done + G + expert_of(c.seg, G, f.inv[(int64_t)t * f.k + tid]);
             if (ld_acquire(cnt) < target) {
                 const uint64_t t0 = ptx::globaltimer();
                 uint32_t it = 0;
@@ -341,6 +384,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 fence_proxy_async_global();
             }
+            // kFused: the token rows of a SwiGLU tile exist once the gather phase
+            // counted all rows of its expert; until then only weights are loaded
+            const int* gcnt = (MODE == kFused && sw && p.gx != nullptr) ? p.done + 2 * p.g1.G + 1 + t.g : nullptr;
+            bool rows_ready = gcnt == nullptr || ld_acquire(gcnt) >= t.row_end - t.row0;
+            int pend_stage[kStages], pend_kb[kStages], pending = 0;
             const int n_micro_k = sw ? 1 : g.n_micro;
             for (int mi = 0; ok && mi < n_micro_k; ++mi) {
                 const int m = sw ? t.m : mi;
@@ -362,12 +410,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ptx::tma_load_2d(sa, tw, kb * kTcBK, wrow, fb);                       // 128 rows
                     }
                     const int kx = (sw ? 0 : m * g.a_micro_cols) + kb * kTcBK;
-                    ptx::tma_load_2d(sa + kABytes, tx, kx, t.row0, fb);                       // 16 token rows
+                    if (rows_ready) {
+                        ptx::tma_load_2d(sa + kABytes, tx, kx, t.row0, fb);                   // 16 token rows
+                    } else {
+                        pend_stage[pending] = stage;
+                        pend_kb[pending] = kx;
+                        ++pending;
+                    }
                     last_par[stage] = phase;
                     ++issued;
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
+                    }
+                    if (!rows_ready && (pending == kStages || kb + 1 == g.k_blocks)) {
+                        // every free stage holds weights: wait for the rows, then
+                        // complete the pending stages with their token rows
+                        const uint64_t t0 = ptx::globaltimer();
+                        uint32_t it = 0;
+                        while (ld_acquire(gcnt) < t.row_end - t.row0) {
+                            if ((++it & 15u) == 0u && (c.abort || ptx::globaltimer() - t0 > g.limit_ns)) {
+                                ok = false;
+                                break;
+                            }
+                            __nanosleep(32);
+                        }
+                        fence_proxy_async_global();
+                        for (int q = 0; q < pending; ++q) {  // completes the armed stages even on failure
+                            const uint32_t psa = ptx::smem_u32(smem + pend_stage[q] * kStageBytes);
+                            ptx::tma_load_2d(psa + kABytes, tx, pend_kb[q], t.row0,
+                                             ptx::smem_u32(&c.full[pend_stage[q]]));
+                        }
+                        pending = 0;
+                        rows_ready = true;
+                        if (!ok) break;
                     }
                 }
             }
@@ -436,6 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------ epilogue
         const int q = warp - 4;            // TMEM lanes 32q .. 32q+31 = weight rows
         const int r = q * 32 + lane;
+        if (MODE == kFused && p.gx != nullptr) gather_rows(c, p);
         TileStream ts;
         ts.next_static = blockIdx.x;
         for (int local = 0;; ++local) {
@@ -553,7 +630,7 @@ cudaError_t launch_tc_small_swiglu(const TcGemmArgs& a, const CUtensorMap& tmX, 
     SmallMaps maps;
     fill_maps(maps, tmX, tmW, a.n_micro, true);
     fill_maps(maps, tmX, tmW, 1, false);  // unused slots
-    SmallParams p{a, a, nullptr, FinalizeArgs{}};
+    SmallParams p{a, a, nullptr, FinalizeArgs{}, nullptr, nullptr, nullptr, 0, 0};
     return launch_small<kSwiGLUOnly>(maps, p, a.max_tiles, num_sms, s);
 }
 
@@ -562,17 +639,18 @@ cudaError_t launch_tc_small_down(const TcGemmArgs& a, const CUtensorMap& tmX, co
     SmallMaps maps;
     fill_maps(maps, tmX, tmW, a.n_micro, false);
     fill_maps(maps, tmX, tmW, 1, true);  // unused slots
-    SmallParams p{a, a, nullptr, FinalizeArgs{}};
+    SmallParams p{a, a, nullptr, FinalizeArgs{}, nullptr, nullptr, nullptr, 0, 0};
     return launch_small<kDownOnly>(maps, p, a.max_tiles, num_sms, s);
 }
 
 cudaError_t launch_tc_small_fused(const TcGemmArgs& g1, const CUtensorMap& tmX1, const CUtensorMap* tmW1,
                                   const TcGemmArgs& g2, const CUtensorMap& tmX2, const CUtensorMap* tmW2,
-                                  const FinalizeArgs& fin, int* done, int num_sms, cudaStream_t s) {
+                                  const FinalizeArgs& fin, const GatherArgs& gat, int* done, int num_sms,
+                                  cudaStream_t s) {
     SmallMaps maps;
     fill_maps(maps, tmX1, tmW1, g1.n_micro, true);
     fill_maps(maps, tmX2, tmW2, g2.n_micro, false);
-    SmallParams p{g1, g2, done, fin};
+    SmallParams p{g1, g2, done, fin, gat.x, gat.xp, gat.perm, gat.k, (int)gat.row_bytes};
     // enough CTAs for the finalize items as well (T tokens x 1024-column chunks)
     const int fin_items = fin.y ? fin.T * ((fin.H / 8 + 127) / 128) : 0;
     const int work = g1.max_tiles + g2.max_tiles > fin_items ? g1.max_tiles + g2.max_tiles : fin_items;

@@ -57,13 +57,9 @@ struct RouterTcArgs {
     int32_t* shared_tiles_simt;  // [2]
     int32_t* perm;          // [T*k]
     int32_t* inv;           // [T*k]
-    int32_t* zero_counters; // [2E+1] set to 0 by the single-CTA paths, or null
+    int32_t* zero_counters; // [3E+1] set to 0 by the single-CTA paths, or null
     int* err;
     uint64_t limit_ns;
-    // small-batch cluster router only: after placement, copy xp[i] = x[perm[i]/k]
-    const void* gather_x;   // [T][row_bytes] or null
-    void* gather_xp;        // [T*k][row_bytes]
-    int gather_row_bytes;
 };
 // tmX: x [T][H] bf16, box {64, 128}; tmW: Wr [E][H] bf16, box {64, 64}.
 cudaError_t launch_router_tc(const RouterTcArgs& a, const CUtensorMap& tmX, const CUtensorMap& tmW,
@@ -163,11 +159,12 @@ cudaError_t launch_tc_small_down(const TcGemmArgs& a, const CUtensorMap& tmX, co
 // Both GEMMs of the routed experts and the finalize in one persistent
 // cooperative launch: the down tiles of expert e start once the SwiGLU tiles
 // of e have stored h, and a token's finalize once the down tiles of its k
-// experts have stored o. done[2E+1] must be zero at launch (the small-batch
-// router zeroes it).
+// experts have stored o; its first phase gathers xp from x (gat.x non-null).
+// done[3E+1] must be zero at launch (the small-batch router zeroes it).
 cudaError_t launch_tc_small_fused(const TcGemmArgs& g1, const CUtensorMap& tmX1, const CUtensorMap* tmW1,
                                   const TcGemmArgs& g2, const CUtensorMap& tmX2, const CUtensorMap* tmW2,
-                                  const FinalizeArgs& fin, int* done, int num_sms, cudaStream_t s);
+                                  const FinalizeArgs& fin, const GatherArgs& gat, int* done, int num_sms,
+                                  cudaStream_t s);
 
 // ---------------------------------------------------- fp32 SIMT GEMMs
 constexpr int kSimtBM = 32;
@@ -217,9 +214,7 @@ struct RoutingJob {
     int32_t* blk_base;        // same
     int* err;
     uint64_t limit_ns;
-    int32_t* zero_counters;   // [2E+1] zeroed when routing runs in one CTA (T <= 128), or null
-    // T <= kSmallTokens (bf16): the router also gathers xp[i] = x[perm[i]/k]
-    void* gather_xp;          // or null
+    int32_t* zero_counters;   // [3E+1] zeroed when routing runs in one CTA (T <= 128), or null
 };
 
 // Optional callbacks around every kernel launch (timing, counting).

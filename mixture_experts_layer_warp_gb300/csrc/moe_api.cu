@@ -156,12 +156,11 @@ moe_status check_call(moe_handle* h, const void* x, const void* router_w, int32_
 
 // Router, scan and placement: leaves ids, topw, offsets, tiles, perm and inv in the workspace.
 moe_status run_routing(moe_handle* h, const void* x, const void* router_w, const float* bias, int32_t T,
-                       float* logits, cudaStream_t s, bool gather_xp = false) {
+                       float* logits, cudaStream_t s) {
     const moe_config& c = h->cfg;
     RoutingJob j{x, router_w, bias, T, c.hidden, c.num_experts, c.top_k, c.dtype == MOE_BF16, h->ids, h->topw,
                  logits, h->perm, h->inv, h->offsets, h->tiles_tc, h->tiles_simt, h->shared_meta, h->blk_hist,
-                 h->blk_base, h->err, h->limit_ns, h->done,
-                 (c.dtype == MOE_BF16 && T <= kSmallTokens && gather_xp) ? h->xp : nullptr};
+                 h->blk_base, h->err, h->limit_ns, h->done};
     LaunchHook hook{h, hook_before, hook_after};
     cudaError_t e = enqueue_routing(j, s, &hook);
     if (e == cudaErrorInvalidValue) return set_err(h, MOE_ERR_CUDA, "router tensor map encode failed");
@@ -177,10 +176,10 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
     const int64_t R = (int64_t)T * k;
     cudaError_t e;
     const bool small_bf16 = c.dtype == MOE_BF16 && T <= kSmallTokens;
-    moe_status st = run_routing(h, x, router_w, bias, T, nullptr, s, small_bf16);
+    moe_status st = run_routing(h, x, router_w, bias, T, nullptr, s);
     if (st != MOE_OK) return st;
 
-    if (!small_bf16) {  // small bf16 batches were gathered by the router
+    if (!small_bf16) {  // small bf16 batches gather inside the fused GEMM launch
         GatherArgs ga{x, h->perm, (int)R, k, (uint32_t)(H * h->esz), h->xp, h->err, h->limit_ns, h->num_sms};
         if ((e = timed(h, kSlotGather, s, [&] { return launch_gather(ga, s); })) != cudaSuccess)
             return cuda_err(h, e, "gather launch");
@@ -225,11 +224,12 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
                            [&] { return launch_tc_small_down(s2, sX, sW, h->num_sms, s); })) != cudaSuccess)
                 return cuda_err(h, e, "shared GEMM2 launch");
         }
-        // both GEMMs and the finalize in one cooperative launch (the router
-        // zeroed h->done); the shared expert's GEMMs ran first
+        // gather, both GEMMs and the finalize in one cooperative launch (the
+        // router zeroed h->done); the shared expert's GEMMs ran first
         FinalizeArgs fin{h->obuf, h->inv, h->topw, Is > 0 ? h->sbuf : nullptr, T, k, H, true, y};
         if ((e = timed(h, kSlotGemm1, s, [&] {
-                 return launch_tc_small_fused(g1, tmX, tmW, g2, tmX2, tmW2, fin, h->done, h->num_sms, s);
+                 GatherArgs gat{x, h->perm, (int)R, k, (uint32_t)(H * 2), h->xp, h->err, h->limit_ns, h->num_sms};
+                 return launch_tc_small_fused(g1, tmX, tmW, g2, tmX2, tmW2, fin, gat, h->done, h->num_sms, s);
              })) != cudaSuccess)
             return cuda_err(h, e, "fused GEMM launch");
     } else if (c.dtype == MOE_BF16) {
@@ -402,7 +402,7 @@ moe_status moe_create(const moe_config* cfg, moe_handle** out) {
     const size_t o_ids = take(R * 4), o_topw = take(R * 4), o_perm = take(R * 4), o_inv = take(R * 4);
     const size_t o_off = take((E + 1) * 4), o_ttc = take((E + 1) * 4), o_tsi = take((E + 1) * 4);
     const size_t o_smeta = take(6 * 4);
-    const size_t o_hist = take(NB * E * 4), o_base = take(NB * E * 4), o_done = take((2 * E + 1) * 4);
+    const size_t o_hist = take(NB * E * 4), o_base = take(NB * E * 4), o_done = take((3 * E + 1) * 4);
     const size_t o_xp = take(R * H * esz), o_h = take(R * M * I * esz), o_o = take(R * H * esz);
     const size_t o_hs = take(T * Is * esz), o_s = take(Is ? T * H * esz : 0);
     const size_t o_xst = take(T * H * esz), o_yst = take(T * H * esz);

@@ -183,7 +183,7 @@ __device__ __forceinline__ void finish_single(const RouterTcArgs& a, const int* 
     __syncthreads();
     if ((int)threadIdx.x <= E) a.offsets[threadIdx.x] = off[threadIdx.x];
     if (a.zero_counters != nullptr)
-        for (int i = threadIdx.x; i <= 2 * E; i += blockDim.x) a.zero_counters[i] = 0;
+        for (int i = threadIdx.x; i <= 3 * E; i += blockDim.x) a.zero_counters[i] = 0;
     place_chunk<NW>(sid, a.T * a.k, 0, E, (int64_t)a.T * a.k, [&](int e) { return off[e]; }, cnt, run, a.perm,
                     a.inv, a.err);
 }
@@ -500,34 +500,6 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
         }
         __syncthreads();
         finish_single<4>(a, c.hist, c.off, c.cnt, c.run, sid);
-    }
-
-    if (a.gather_xp != nullptr) {
-        // the gather of the routed rows, shared by the cluster: CTA 0's
-        // permutation is visible cluster-wide after the barrier
-        ptx::cluster_sync();
-        const int R = a.T * k;
-        const int nvec = a.gather_row_bytes / 16;
-        const int my_rows = R > rank ? (R - rank + kCluster - 1) / kCluster : 0;  // rows rank, rank+8, ...
-        for (int r = threadIdx.x; r < my_rows; r += kThreads) sid[r] = __ldcg(a.perm + rank + r * kCluster) / k;
-        __syncthreads();
-        const uint4* __restrict__ src = static_cast<const uint4*>(a.gather_x);
-        uint4* __restrict__ dst = static_cast<uint4*>(a.gather_xp);
-        const int total = my_rows * nvec;
-        constexpr int kBatch = 8;  // loads in flight per thread before the stores
-        for (int base = threadIdx.x; base < total; base += kThreads * kBatch) {
-            uint4 buf[kBatch];
-#pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-                const int q = base + u * kThreads;
-                if (q < total) buf[u] = src[(int64_t)sid[q / nvec] * nvec + q % nvec];
-            }
-#pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-                const int q = base + u * kThreads;
-                if (q < total) dst[(int64_t)(rank + (q / nvec) * kCluster) * nvec + q % nvec] = buf[u];
-            }
-        }
     }
 
     ptx::tc_fence_before();
