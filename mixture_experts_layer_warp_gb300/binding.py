@@ -113,6 +113,8 @@ class MoELayer:
                              MOE_BF16 if dtype == torch.bfloat16 else MOE_F32)
         self._lib = load()
         self._h = ctypes.c_void_p()
+        self._wcache = None
+        self._stream_id = None
         with torch.cuda.device(self.device):
             rc = self._lib.moe_create(ctypes.byref(self.cfg), ctypes.byref(self._h))
         if rc != 0:
@@ -140,6 +142,12 @@ class MoELayer:
         return t
 
     def _weights(self, w13, w2, shared_w13, shared_w2):
+        # the same resident weight tensors are passed on every call: validate once
+        key = (tuple(t.data_ptr() for t in w13), tuple(t.data_ptr() for t in w2),
+               None if shared_w13 is None else shared_w13.data_ptr(),
+               None if shared_w2 is None else shared_w2.data_ptr())
+        if self._wcache is not None and self._wcache[0] == key:
+            return self._wcache[1], self._wcache[2]
         c = self.cfg
         if len(w13) != c.n_micro or len(w2) != c.n_micro:
             raise ValueError(f"expected {c.n_micro} micro-shards of w13 and w2")
@@ -153,6 +161,7 @@ class MoELayer:
             raise ValueError("this layer has no shared expert")
         p13 = (ctypes.c_void_p * c.n_micro)(*[t.data_ptr() for t in w13])
         p2 = (ctypes.c_void_p * c.n_micro)(*[t.data_ptr() for t in w2])
+        self._wcache = (key, p13, p2)
         return p13, p2
 
     def _router(self, router_w, router_bias):

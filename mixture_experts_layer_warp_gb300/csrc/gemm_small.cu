@@ -27,7 +27,7 @@
 // stages are issued meanwhile); after its tiles they run finalize items, each
 // gated on the down tiles of its token's experts. The whole routed layer after
 // routing is therefore one launch.
-// Structure: 8-stage TMA ring, one MMA issuer, four epilogue warps on a
+// Structure: 12-stage TMA ring, one MMA issuer, four epilogue warps on a
 // double-buffered 2 x 16-column TMEM accumulator. All waits are bounded.
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
@@ -41,7 +41,7 @@ namespace {
 
 constexpr int kTok = kSmallTokens;             // 16: MMA N
 constexpr int kM = 128;                        // MMA M: weight rows
-constexpr int kStages = 8;
+constexpr int kStages = 12;
 constexpr int kABytes = kM * kTcBK * 2;        // 16 KB
 constexpr int kBBytes = kTok * kTcBK * 2;      // 2 KB
 constexpr int kStageBytes = kABytes + kBBytes; // 18 KB (a multiple of 1024)

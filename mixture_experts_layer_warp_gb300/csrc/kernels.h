@@ -26,6 +26,7 @@ constexpr int kRouterTokens = 32;
 constexpr int kRouterTokensTc = 128;
 // Batches of at most kSmallTokens tokens take the small-batch kernels.
 constexpr int kSmallTokens = 16;
+constexpr int kRouterClusterCtas = 8;  // CTAs of the small-batch router
 
 struct RouterArgs {
     const void* x;         // [T][H]

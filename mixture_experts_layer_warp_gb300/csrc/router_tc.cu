@@ -345,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // same compensated order. The logits are therefore bit-identical to the
 // 128-token kernel's (routing does not depend on the batch size), while eight
 // SMs instead of one stream the router weights.
-constexpr int kCluster = 8;
+constexpr int kCluster = kRouterClusterCtas;
 constexpr int kCStages = 4;
 constexpr int kCTok = kSmallTokens;
 constexpr int kXBytesSmall = kCTok * kTcBK * 2;                    // 2 KB of x per stage
