@@ -118,12 +118,22 @@ def barrier(world):
 
 
 def max_over_ranks(v: float, world: int) -> float:
+    """Largest value over the replicas (the slowest rank's time)."""
     if world == 1:
         return v
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(world: int, tokens_per_step: int, steps: int, ms_local: float):
+    """Whole-job tokens/s of N independent replicas (weak scaling): every rank
+    runs `steps` steps of `tokens_per_step` tokens; the job takes as long as the
+    slowest rank. Returns (ms_max, tokens_per_s)."""
+    ms = max_over_ranks(ms_local, world)
+    return ms, world * tokens_per_step * steps / (ms / 1e3)
 
 
 def src_sha() -> str:
@@ -264,6 +274,41 @@ def roofline_of(wl, prof, ids_pool, steps, peaks, sha):
             "timing": "per-kernel CUDA events in a profiling pass of the same steps"}
 
 
+def time_two_dispatch(args, wl, inp, pool, multi_ms, world):
+    """The pages' ablation baseline ("HunyuanImage3 Hybrid Parallelism",
+    section 10.3): one full layer call per micro-shard, outputs added (here the
+    later calls accumulate into the first one's y), against the multi-micro
+    layer that shares one routing, permutation and finalize."""
+    layers = [binding.MoELayer(wl.H, wl.E, wl.k, wl.I, 1, max_tokens=wl.T,
+                               shared_inter=wl.shared_inter if m == 0 else 0, dtype=wl.torch_dtype)
+              for m in range(wl.n_micro)]
+    for lay in layers[1:]:
+        lay.set_accumulate(True)
+    y = torch.empty((wl.T, wl.H), dtype=wl.torch_dtype, device="cuda")
+
+    def step(i):
+        x = pool[i % POOL]
+        for m, lay in enumerate(layers):
+            lay.forward(x, inp["router_w"], inp["router_bias"], [inp["w13"][m]], [inp["w2"][m]],
+                        inp["shared_w13"] if m == 0 else None, inp["shared_w2"] if m == 0 else None, out=y)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    ev1.record()
+    ev1.synchronize()
+    for lay in layers:
+        lay.sync()
+        lay.close()
+    two_ms = max_over_ranks(ev0.elapsed_time(ev1), world) / args.steps
+    return {"ms_per_step": two_ms, "multi_micro_ms_per_step": multi_ms, "saving_ms": two_ms - multi_ms,
+            "saving_pct_of_two_dispatch": 100.0 * (two_ms - multi_ms) / two_ms}
+
+
 def run_ours(args, wl, world, rank, local):
     peaks = load_peaks()
     inp = W.make_inputs(wl, seed=0, device="cuda")
@@ -296,7 +341,7 @@ def run_ours(args, wl, world, rank, local):
     barrier(world)
     launches = layer.launch_count() - l0
     layer.sync()
-    ms = max_over_ranks(ev0.elapsed_time(ev1), world)
+    ms, value = job_throughput(world, wl.T, args.steps, ev0.elapsed_time(ev1))
 
     # per-kernel durations: the same steps again with an event pair around every
     # launch (kept out of the timed region above, whose launches run back to back)
@@ -305,7 +350,6 @@ def run_ours(args, wl, world, rank, local):
         step(args.warmup + i)
     prof = layer.profile_end()
     layer.sync()
-    value = world * wl.T * args.steps / (ms / 1e3)
     shift = args.warmup % POOL
     ids_timed = ids_pool[shift:] + ids_pool[:shift]
     roof = roofline_of(wl, prof, ids_timed, args.steps, peaks, src_sha())
@@ -321,10 +365,14 @@ def run_ours(args, wl, world, rank, local):
     t0 = time.perf_counter()
     for i in range(e2e_steps):
         layer.forward_host(host_pool[i % POOL], *args_w, out_host=y_host)
-    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    _, e2e_value = job_throughput(world, wl.T, e2e_steps, (time.perf_counter() - t0) * 1e3)
     esz = 4 if wl.dtype == "f32" else 2
-    e2e = {"value": world * wl.T * e2e_steps / e2e_s, "unit": "tokens/s",
+    e2e = {"value": e2e_value, "unit": "tokens/s",
            "h2d_bytes_per_step": wl.T * wl.H * esz, "d2h_bytes_per_step": wl.T * wl.H * esz}
+
+    two = None
+    if args.two_dispatch and wl.n_micro > 1:
+        two = time_two_dispatch(args, wl, inp, pool, ms / args.steps, world)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -346,6 +394,8 @@ def run_ours(args, wl, world, rank, local):
         "kernels_ms_per_step": {k: v[0] / args.steps for k, v in prof.items()},
         "clocks": clk.summary(),
     }
+    if two is not None:
+        line["two_dispatch"] = two
     print(json.dumps(line), flush=True)
 
 
@@ -358,6 +408,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(W.WORKLOADS), default="decode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--two-dispatch", action="store_true",
+                    help="also time the two-dispatch form of a multi-micro workload")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     wl = W.WORKLOADS[args.workload]

@@ -145,6 +145,16 @@ moe_status moe_forward_host(moe_handle *h, const void *x_host, const void *route
                             void *y_host, void *stream);
 
 /*
+ * Output accumulation. With `on` non-zero, later moe_forward / moe_forward_host
+ * calls on this handle add the layer's output into y (y += layer(x)): the
+ * finalize reads y, adds it in fp32 and rounds once. It serves a residual add,
+ * and the pages' two-dispatch form of a multi-micro layer (blog section 10.3:
+ * one full layer call per micro-shard, outputs added), which is two calls of
+ * single-micro handles, the second with accumulation on. Default off.
+ */
+moe_status moe_set_accumulate(moe_handle *h, int32_t on);
+
+/*
  * Synchronise the stream of the handle's last call and read its device error
  * word. Returns MOE_OK, or MOE_ERR_TIMEOUT / MOE_ERR_DEVICE_CHECK (and makes
  * the handle sticky), or MOE_ERR_CUDA.

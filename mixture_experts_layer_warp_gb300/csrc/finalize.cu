@@ -6,7 +6,8 @@
 // adding in fp32, applying the scale once and reducing over top-k once. Here
 // the per-micro partials were already summed in the GEMM2 accumulator, so
 // each route contributes one row o[inv[t*k + j]]. The shared expert's output
-// (Ascend Hunyuan Image 3.0 guide, section 3.1) is added unscaled.
+// (Ascend Hunyuan Image 3.0 guide, section 3.1) is added unscaled, and with
+// output accumulation on, the previous content of y as well.
 //
 // HBM-bound: one block per (token, 1024-column chunk), 16-byte vector loads
 // of the k expert rows.
@@ -80,6 +81,12 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(FinalizeArgs a) {
         if (sh != nullptr) {
             float val[8];
             load8(sh + (int64_t)t * a.H + v * 8, val);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] += val[i];
+        }
+        if (a.accumulate) {
+            float val[8];
+            load8(y + (int64_t)t * a.H + v * 8, val);
 #pragma unroll
             for (int i = 0; i < 8; ++i) acc[i] += val[i];
         }

@@ -159,7 +159,8 @@ __device__ __forceinline__ void gather_rows(const Ctl& c, const SmallParams& p) 
 // applied once, top-k reduced once) as the fused kernel's last phase, run by
 // the four epilogue warps: item (token t, 1024 columns) waits until the down
 // tiles of t's k experts have stored their o rows, then
-//     y[t] = sum_j w[t][j] * o[inv[t*k + j]] (+ shared[t]), fp32 accumulate.
+//     y[t] = sum_j w[t][j] * o[inv[t*k + j]] (+ shared[t]) (+ y[t] when
+//     accumulating), fp32 accumulate.
 // o rows come from other CTAs, so they are read through L2 (ld.global.cg).
 __device__ __forceinline__ void finalize_items(Ctl& c, const SmallParams& p) {
     const FinalizeArgs& f = p.fin;
@@ -212,8 +213,10 @@ __device__ __forceinline__ void finalize_items(Ctl& c, const SmallParams& p) {
                     }
                 }
             }
-            if (sh != nullptr) {
-                const uint4 u = *(reinterpret_cast<const uint4*>(sh + (int64_t)t * f.H) + v);
+            for (int extra = 0; extra < 2; ++extra) {  // shared expert, then the previous y
+                const __nv_bfloat16* src = extra == 0 ? sh : (f.accumulate ? y : nullptr);
+                if (src == nullptr) continue;
+                const uint4 u = *(reinterpret_cast<const uint4*>(src + (int64_t)t * f.H) + v);
                 const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {

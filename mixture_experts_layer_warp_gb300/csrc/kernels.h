@@ -115,6 +115,7 @@ struct FinalizeArgs {
     int T, k, H;
     bool bf16;
     void* y;                  // [T][H]
+    bool accumulate;          // y += result instead of y = result
 };
 cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t s);
 

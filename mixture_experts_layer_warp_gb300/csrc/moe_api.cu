@@ -54,6 +54,7 @@ struct moe_handle {
     void* y_stage = nullptr;
     // diagnostics
     int64_t launches = 0;
+    bool accumulate = false;
     bool prof_on = false;
     int prof_max = 0;
     int prof_calls = 0;
@@ -226,7 +227,7 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
         }
         // gather, both GEMMs and the finalize in one cooperative launch (the
         // router zeroed h->done); the shared expert's GEMMs ran first
-        FinalizeArgs fin{h->obuf, h->inv, h->topw, Is > 0 ? h->sbuf : nullptr, T, k, H, true, y};
+        FinalizeArgs fin{h->obuf, h->inv, h->topw, Is > 0 ? h->sbuf : nullptr, T, k, H, true, y, h->accumulate};
         if ((e = timed(h, kSlotGemm1, s, [&] {
                  GatherArgs gat{x, h->perm, (int)R, k, (uint32_t)(H * 2), h->xp, h->err, h->limit_ns, h->num_sms};
                  return launch_tc_small_fused(g1, tmX, tmW, g2, tmX2, tmW2, fin, gat, h->done, h->num_sms, s);
@@ -330,7 +331,8 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
         }
     }
     if (!small_bf16) {  // small bf16 batches finalize inside the fused GEMM launch
-        FinalizeArgs fa{h->obuf, h->inv, h->topw, Is > 0 ? h->sbuf : nullptr, T, k, H, c.dtype == MOE_BF16, y};
+        FinalizeArgs fa{h->obuf, h->inv, h->topw, Is > 0 ? h->sbuf : nullptr, T, k, H, c.dtype == MOE_BF16, y,
+                        h->accumulate};
         if ((e = timed(h, kSlotFinalize, s, [&] { return launch_finalize(fa, s); })) != cudaSuccess)
             return cuda_err(h, e, "finalize launch");
     }
@@ -506,6 +508,8 @@ moe_status moe_forward_host(moe_handle* h, const void* x_host, const void* route
     const size_t bytes = (size_t)T * h->cfg.hidden * h->esz;
     cudaError_t e = cudaMemcpyAsync(h->x_stage, x_host, bytes, cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess) return cuda_err(h, e, "copy x to device");
+    if (h->accumulate && (e = cudaMemcpyAsync(h->y_stage, y_host, bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+        return cuda_err(h, e, "copy y to device");
     st = run_forward(h, h->x_stage, router_w, router_bias, w13, w2, shared_w13, shared_w2, T, h->y_stage, s);
     end_call(h);
     if (st != MOE_OK) return st;
@@ -599,6 +603,12 @@ moe_status moe_profile_end(moe_handle* h, float* ms, int32_t* launches) {
 }
 
 int64_t moe_launch_count(const moe_handle* h) { return h ? h->launches : 0; }
+
+moe_status moe_set_accumulate(moe_handle* h, int32_t on) {
+    if (h == nullptr) return MOE_ERR_INVALID_ARG;
+    h->accumulate = on != 0;
+    return MOE_OK;
+}
 
 moe_status moe_selftest_wait_timeout(int32_t timeout_us, void* stream) {
     if (timeout_us <= 0) return MOE_ERR_INVALID_ARG;

@@ -92,17 +92,48 @@ def test_bitwise_deterministic_across_calls():
     layer.close()
 
 
-def test_two_dispatches_sum_to_the_multi_micro_call():
-    """Two single-micro calls summed equal one multi-micro call ("HunyuanImage3
-    Hybrid Parallelism", section 10.3), up to the bf16 rounding of y."""
-    wl = W.Workload("mm", 200, 256, 8, 2, 128, 2)
+@pytest.mark.parametrize("T", [8, 200])
+def test_two_dispatches_sum_to_the_multi_micro_call(T):
+    """Two single-micro layer calls, the second accumulating into the first's
+    output, equal one multi-micro call ("HunyuanImage3 Hybrid Parallelism",
+    section 10.3), up to bf16 rounding of the intermediate y."""
+    wl = W.Workload("mm", T, 256, 8, 2, 128, 2)
     dev = parity.to_device(W.make_inputs(wl, seed=3))
     both = _forward(_layer(wl), dev).float()
-    one = W.Workload("m1", 200, 256, 8, 2, 128, 1)
-    y0 = _forward(_layer(one), dict(dev, w13=dev["w13"][:1], w2=dev["w2"][:1])).float()
-    y1 = _forward(_layer(one), dict(dev, w13=dev["w13"][1:], w2=dev["w2"][1:])).float()
-    err = ((y0 + y1) - both).abs().max().item() / both.abs().max().item()
+    one = W.Workload("m1", T, 256, 8, 2, 128, 1)
+    l0, l1 = _layer(one), _layer(one)
+    l1.set_accumulate(True)
+    y = l0.forward(dev["x"], dev["router_w"], None, dev["w13"][:1], dev["w2"][:1])
+    l1.forward(dev["x"], dev["router_w"], None, dev["w13"][1:], dev["w2"][1:], out=y)
+    l1.sync()
+    err = (y.float() - both).abs().max().item() / both.abs().max().item()
     assert err < 1e-2
+
+
+@pytest.mark.parametrize("wl", [W.Workload("acc_small", 12, 512, 16, 4, 128, 2, shared_inter=128),
+                                W.Workload("acc_large", 300, 512, 16, 4, 128, 2, shared_inter=128),
+                                W.Workload("acc_f32", 40, 128, 4, 2, 64, 1, dtype="f32")],
+                         ids=lambda w: w.name)
+def test_accumulate_adds_the_layer_output_into_y(wl):
+    dev = parity.to_device(W.make_inputs(wl, seed=6))
+    layer = _layer(wl)
+    plain = _forward(layer, dev).float()
+    g = torch.Generator(device="cuda").manual_seed(1)
+    y0 = torch.randn(plain.shape, generator=g, device="cuda").to(wl.torch_dtype)
+    y = y0.clone()
+    layer.set_accumulate(True)
+    layer.forward(dev["x"], dev["router_w"], dev["router_bias"], dev["w13"], dev["w2"], dev["shared_w13"],
+                  dev["shared_w2"], out=y)
+    layer.sync()
+    want = y0.float() + plain
+    err = (y.float() - want).abs().max().item() / want.abs().max().item()
+    assert err <= (1e-2 if wl.dtype == "bf16" else 1e-5)
+    # the host entry point accumulates into the host buffer the same way
+    yh = y0.cpu().pin_memory()
+    layer.forward_host(dev["x"].cpu().pin_memory(), dev["router_w"], dev["router_bias"], dev["w13"], dev["w2"],
+                       dev["shared_w13"], dev["shared_w2"], out_host=yh)
+    assert torch.equal(yh, y.cpu())
+    layer.close()
 
 
 def test_host_entry_point_matches_device_entry_point():
