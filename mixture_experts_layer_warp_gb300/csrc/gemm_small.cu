@@ -28,7 +28,11 @@
 // gated on the down tiles of its token's experts. The whole routed layer after
 // routing is therefore one launch.
 // Structure: 12-stage TMA ring, one MMA issuer, four epilogue warps on a
-// double-buffered 2 x 16-column TMEM accumulator. All waits are bounded.
+// double-buffered 2 x 16-column TMEM accumulator. In the fused mode a fifth
+// role, the scheduler thread, claims the next tile from the global counter and
+// waits for its dependency (the expert's SwiGLU tiles, or its gathered rows)
+// while the producer streams the current one, so neither global round trip
+// sits between two tiles of the weight stream. All waits are bounded.
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
 
@@ -69,6 +73,12 @@ struct Ctl {
     uint64_t tq_full[4];
     uint64_t tq_empty[4];
     int tq[4];
+    // kFused: the scheduler thread's one-deep queue to the producer (a tile
+    // claimed and resolved while the previous one streams)
+    uint64_t sq_full;
+    uint64_t sq_empty;
+    int sq_tile;
+    int sq_rows;
 };
 
 constexpr int kSmemBytes = kStages * kStageBytes + (int)sizeof(Ctl) + 1024;
@@ -253,10 +263,11 @@ __device__ __forceinline__ Tile locate(int tile, const Ctl& c, const SmallParams
 }
 
 // Tile sequence of one CTA. Static modes stride over the list (blockIdx.x,
-// + gridDim.x, ...). The fused mode hands tiles out dynamically: the producer
-// takes the next list position from a global counter (so every position is
-// taken in increasing order and CTAs that drew cheap tiles take more) and
-// passes it through the shared ring to the MMA and epilogue warps; -1 ends.
+// + gridDim.x, ...). The fused mode hands tiles out dynamically: the scheduler
+// thread takes the next list position from a global counter (so every position
+// is taken in increasing order and CTAs that drew cheap tiles take more), the
+// producer takes it from the scheduler and passes it through the shared ring
+// to the MMA and epilogue warps; -1 ends.
 struct TileStream {
     int slot = 0;
     uint32_t phase = 0;
@@ -264,16 +275,15 @@ struct TileStream {
 };
 
 // Producer side (one thread). Returns the tile to process, or -1 when done or failed.
+// In the fused mode `t` is the tile taken from the scheduler (-1 to end).
 template <int MODE>
-__device__ __forceinline__ int produce_tile(Ctl& c, const SmallParams& p, TileStream& ts, int total,
-                                            uint64_t limit_ns, bool& ok) {
+__device__ __forceinline__ int produce_tile(Ctl& c, TileStream& ts, int total, int t, uint64_t limit_ns,
+                                            bool& ok) {
     if (MODE != kFused) {
-        const int t = ts.next_static;
+        const int ts_t = ts.next_static;
         ts.next_static += gridDim.x;
-        return t < total ? t : -1;
+        return ts_t < total ? ts_t : -1;
     }
-    int t = atomicAdd(p.done + 2 * p.g1.G, 1);
-    if (t >= total) t = -1;
     if (!ptx::mbar_wait(ptx::smem_u32(&c.tq_empty[ts.slot]), ts.phase ^ 1u, limit_ns, &c.abort)) {
         ok = false;
         t = -1;
@@ -305,6 +315,73 @@ __device__ __forceinline__ int consume_tile(Ctl& c, TileStream& ts, int total, u
     return t;
 }
 
+// Bounded spin until *cnt >= target (acquire); false on timeout or abort.
+__device__ __forceinline__ bool wait_count(const int* cnt, int target, Ctl& c, uint64_t limit_ns) {
+    if (ld_acquire(cnt) >= target) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    uint32_t it = 0;
+    while (ld_acquire(cnt) < target) {
+        if ((++it & 15u) == 0u && (c.abort || ptx::globaltimer() - t0 > limit_ns)) return false;
+        __nanosleep(64);
+    }
+    return true;
+}
+
+// Fused mode, scheduler thread: claims list positions one at a time, each only
+// once the producer has taken the previous one (so a CTA holds at most one
+// tile beyond the one it streams), waits until a down tile's SwiGLU tiles are
+// all stored, notes whether a SwiGLU tile's gathered rows are complete, and
+// hands the tile to the producer; -1 ends. The acquire loads here and the
+// queue's mbarrier (release on arrive, acquire on wait) make the h and x rows
+// visible to the producer's thread before it issues their loads.
+__device__ __forceinline__ void schedule_tiles(Ctl& c, const SmallParams& p, int total) {
+    const int target = p.g1.n_micro * p.g1.n_tiles;  // SwiGLU tiles per expert
+    uint32_t phase = 0;
+    bool ok = true;
+    for (;;) {
+        if (!ptx::mbar_wait(ptx::smem_u32(&c.sq_empty), phase ^ 1u, p.g1.limit_ns, &c.abort)) ok = false;
+        int t = -1, rows = 0;
+        if (ok) {
+            t = atomicAdd(p.done + 2 * p.g1.G, 1);
+            if (t >= total) t = -1;
+        }
+        if (t >= 0) {
+            bool sw;
+            const Tile tt = locate<kFused>(t, c, p, sw);
+            if (!sw) {
+                if (!wait_count(p.done + tt.g, target, c, p.g2.limit_ns)) {
+                    ok = false;
+                    t = -1;
+                }
+            } else {
+                rows = p.gx == nullptr || ld_acquire(p.done + 2 * p.g1.G + 1 + tt.g) >= tt.row_end - tt.row0;
+            }
+        }
+        c.sq_tile = t;
+        c.sq_rows = rows;
+        ptx::mbar_arrive(ptx::smem_u32(&c.sq_full));
+        phase ^= 1u;
+        if (t < 0) break;
+    }
+    if (!ok) fail(c, p.g1.err);
+}
+
+// Fused mode, producer: the next tile from the scheduler (-1 on end or failure,
+// ok cleared on failure) and whether its gathered rows were already complete.
+__device__ __forceinline__ int pop_scheduled(Ctl& c, uint32_t& phase, uint64_t limit_ns, bool& rows, bool& ok) {
+    int t = -1;
+    rows = false;
+    if (ptx::mbar_wait(ptx::smem_u32(&c.sq_full), phase, limit_ns, &c.abort)) {
+        t = c.sq_tile;
+        rows = c.sq_rows != 0;
+    } else {
+        ok = false;
+    }
+    ptx::mbar_arrive(ptx::smem_u32(&c.sq_empty));
+    phase ^= 1u;
+    return t;
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_small_kernel(const __grid_constant__ SmallMaps maps, const SmallParams p) {
@@ -329,6 +406,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(ptx::smem_u32(&c.tq_full[q]), 1);
             ptx::mbar_init(ptx::smem_u32(&c.tq_empty[q]), 5);  // MMA issuer + four epilogue warps
         }
+        ptx::mbar_init(ptx::smem_u32(&c.sq_full), 1);
+        ptx::mbar_init(ptx::smem_u32(&c.sq_empty), 1);
         c.abort = 0;
         c.fin_fail = 0;
         ptx::fence_mbar_init();
@@ -353,7 +432,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n1 = MODE == kDownOnly ? 0 : p.g1.n_micro * c.tiles[p.g1.G] * p.g1.n_tiles;
     const int n2 = MODE == kSwiGLUOnly ? 0 : c.tiles[p.g2.G] * p.g2.n_tiles;
     const int total = n1 + n2;
-    const int target = p.g1.n_micro * p.g1.n_tiles;  // SwiGLU tiles per expert (kFused)
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer
@@ -363,34 +441,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         TileStream ts;
         ts.next_static = blockIdx.x;
+        uint32_t sq_phase = 0;
         for (;;) {
-            const int tile = produce_tile<MODE>(c, p, ts, total, a0.limit_ns, ok);
+            bool rows_seen = false;
+            const int next = MODE == kFused ? pop_scheduled(c, sq_phase, a0.limit_ns, rows_seen, ok) : -1;
+            const int tile = produce_tile<MODE>(c, ts, total, next, a0.limit_ns, ok);
             if (tile < 0) break;
             bool sw;
             const Tile t = locate<MODE>(tile, c, p, sw);
             const TcGemmArgs& g = sw ? p.g1 : p.g2;
-            if (MODE == kFused && !sw) {
-                // the down tile reads h rows of expert g: wait for all its SwiGLU tiles
-                const int* cnt = p.done + t.g;
-                if (ld_acquire(cnt) < target) {
-                    const uint64_t t0 = ptx::globaltimer();
-                    uint32_t it = 0;
-                    while (ld_acquire(cnt) < target) {
-                        if ((++it & 15u) == 0u &&
-                            (c.abort || ptx::globaltimer() - t0 > g.limit_ns)) {
-                            ok = false;
-                            break;
-                        }
-                        __nanosleep(64);
-                    }
-                    if (!ok) break;
-                }
-                fence_proxy_async_global();
-            }
-            // kFused: the token rows of a SwiGLU tile exist once the gather phase
-            // counted all rows of its expert; until then only weights are loaded
+            // kFused: a down tile comes from the scheduler only once all SwiGLU
+            // tiles of its expert stored their h rows; the token rows of a SwiGLU
+            // tile exist once the gather phase counted all rows of its expert
+            // (until then only weights are loaded)
             const int* gcnt = (MODE == kFused && sw && p.gx != nullptr) ? p.done + 2 * p.g1.G + 1 + t.g : nullptr;
-            bool rows_ready = gcnt == nullptr || ld_acquire(gcnt) >= t.row_end - t.row0;
+            bool rows_ready = gcnt == nullptr || rows_seen || ld_acquire(gcnt) >= t.row_end - t.row0;
+            if (MODE == kFused) fence_proxy_async_global();  // the rows are read by TMA (async proxy)
             int pend_stage[kStages], pend_kb[kStages], pending = 0;
             const int n_micro_k = sw ? 1 : g.n_micro;
             for (int mi = 0; ok && mi < n_micro_k; ++mi) {
@@ -453,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) {
                 // tell the consumers to stop: a -1 in the ring, or the abort flag
                 c.abort = 1;
-                if (MODE == kFused) produce_tile<MODE>(c, p, ts, 0, a0.limit_ns, ok);
+                if (MODE == kFused) produce_tile<MODE>(c, ts, total, -1, a0.limit_ns, ok);
                 break;
             }
         }
@@ -462,6 +528,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int n = issued < kStages ? issued : kStages;
             for (int s = 0; s < n; ++s) ptx::mbar_wait(ptx::smem_u32(&c.full[s]), last_par[s], a0.limit_ns, nullptr);
         }
+    } else if (MODE == kFused && warp == 3 && lane == 0) {
+        // ------------------------------------------------ scheduler
+        schedule_tiles(c, p, total);
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------ MMA issuer
         int stage = 0;

@@ -78,6 +78,29 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
     }
 }
 
+// try_wait with acquire at cluster scope: for phases completed by st.async
+// writes that other CTAs of the cluster made into this CTA's shared memory.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait of mbar_try_wait_cluster; false once `limit_ns` elapsed.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((it & 31u) == 0u && globaltimer() - t0 > limit_ns) return false;
+    }
+}
+
 // ---------------------------------------------------------------------- TMA
 // 2D tiled load of one box into shared memory; completes `bytes` on `bar`.
 // c0 is the innermost (contiguous) coordinate in elements, c1 the row.
@@ -137,6 +160,22 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
 __device__ __forceinline__ void st_cluster_f32(uint32_t caddr, float v) {
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(caddr), "f"(v) : "memory");
 }
+
+// 16 bytes into another CTA's shared memory (shared::cluster address `caddr`);
+// the write completes 16 bytes of transaction count on that CTA's mbarrier
+// `cbar` (also a shared::cluster address), so the receiver waits on its own
+// barrier instead of a cluster-wide one.
+__device__ __forceinline__ void st_async_v4(uint32_t caddr, uint32_t x, uint32_t y, uint32_t z, uint32_t w,
+                                            uint32_t cbar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     caddr),
+                 "r"(x), "r"(y), "r"(z), "r"(w), "r"(cbar)
+                 : "memory");
+}
+
+// The two halves of a cluster barrier, for work placed between them.
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
 
 // Whole-cluster barrier with release/acquire semantics on shared::cluster data.
 __device__ __forceinline__ void cluster_sync() {

@@ -341,17 +341,41 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Batches of at most kSmallTokens tokens: a cluster of 8 CTAs splits K. CTA c
 // accumulates exactly the K-blocks kb = c, c+8, c+16, ... that form partial c
 // of router_tc_kernel, in the same order, sends its partial logits to CTA 0
-// through distributed shared memory, and CTA 0 combines the partials in the
-// same compensated order. The logits are therefore bit-identical to the
-// 128-token kernel's (routing does not depend on the batch size), while eight
-// SMs instead of one stream the router weights.
+// with st.async (completing bytes on CTA 0's exchange barrier), and CTA 0
+// combines the partials in the same compensated order. The logits are
+// therefore bit-identical to the 128-token kernel's (routing does not depend
+// on the batch size), while eight SMs instead of one stream the router weights.
+//
+// Only 16 of the 128 A rows carry tokens, so the stages are packed 10 KB apart
+// (2 KB of x, then 8 KB of Wr): the MMA's rows 16..127 read whatever follows
+// (the next stage or the pad) and land in TMEM lanes nobody reads. With eight
+// stages, every K-block of a 4096-wide hidden state is in flight at once.
 constexpr int kCluster = kRouterClusterCtas;
-constexpr int kCStages = 4;
+constexpr int kCStages = 8;
 constexpr int kCTok = kSmallTokens;
 constexpr int kXBytesSmall = kCTok * kTcBK * 2;                    // 2 KB of x per stage
+constexpr int kCStageBytes = kXBytesSmall + kBBytes;               // 10 KB, a multiple of 1024
+constexpr int kCRingBytes = kCStages * kCStageBytes + (kABytes - kCStageBytes);  // + pad: last stage's rows 16..127
 constexpr int kPartBytes = kCluster * kCTok * kN * 4;              // 32 KB
 constexpr int kCIdsBytes = kCTok * kMaxTopK * 4;
-constexpr int kCSmemBytes = kCStages * kStageBytes + kPartBytes + kCIdsBytes + (int)sizeof(Ctl) + 1024;
+constexpr int kGroup = kThreads / kCTok;                           // 8 threads per token in the top-k
+constexpr int kPerThread = kN / kGroup;                            // 8 experts per thread
+static_assert(kCStageBytes % 1024 == 0, "128B-swizzled tiles need 1024-byte aligned stages");
+static_assert(kGroup == 8 && kPerThread == 8, "top-k layout assumes 16 tokens x 8 threads x 8 experts");
+
+struct CCtl {
+    uint64_t full[kCStages];
+    uint64_t empty[kCStages];
+    uint64_t done;
+    uint64_t xfer;   // CTA 0: completes when every other CTA's partial has arrived
+    uint32_t tmem;
+    int abort;
+    int hist[kMaxExperts];
+    int off[kMaxExperts + 1];
+    int cnt[4][kMaxExperts];
+    int run[4][kMaxExperts];
+};
+constexpr int kCSmemBytes = kCRingBytes + kPartBytes + kCIdsBytes + (int)sizeof(CCtl) + 1024;
 
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     router_tc_cluster_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
@@ -359,14 +383,16 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    float* part = reinterpret_cast<float*>(smem + kCStages * kStageBytes);   // [kCluster][kCTok][kN] on CTA 0
-    int* sid = reinterpret_cast<int*>(smem + kCStages * kStageBytes + kPartBytes);
-    Ctl& c = *reinterpret_cast<Ctl*>(smem + kCStages * kStageBytes + kPartBytes + kCIdsBytes);
+    float* part = reinterpret_cast<float*>(smem + kCRingBytes);   // [kCluster][kCTok][kN] on CTA 0
+    int* sid = reinterpret_cast<int*>(smem + kCRingBytes + kPartBytes);
+    CCtl& c = *reinterpret_cast<CCtl*>(smem + kCRingBytes + kPartBytes + kCIdsBytes);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int rank = (int)ptx::cluster_ctarank();
     const int k = a.k;
     const int kb_total = a.H / kTcBK;
     const int my_blocks = kb_total > rank ? (kb_total - rank + kCluster - 1) / kCluster : 0;
+    const int nparts = kb_total < kCluster ? kb_total : kCluster;
+    const uint32_t xfer = ptx::smem_u32(&c.xfer);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kCStages; ++s) {
@@ -374,6 +400,10 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
             ptx::mbar_init(ptx::smem_u32(&c.empty[s]), 1);
         }
         ptx::mbar_init(ptx::smem_u32(&c.done), 1);
+        ptx::mbar_init(xfer, 1);
+        // CTA 0 announces the bytes the other CTAs will send before any can
+        // start (they first pass the cluster barrier that follows the init)
+        if (rank == 0) ptx::mbar_arrive_expect_tx(xfer, (uint32_t)((nparts - 1) * a.T * kN * 4));
         c.abort = 0;
         ptx::fence_mbar_init();
     }
@@ -385,6 +415,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
+    ptx::cluster_arrive();   // first phase: barrier inits visible cluster-wide
     const uint32_t tmem = c.tmem;
 
     if (warp == 0 && lane == 0) {
@@ -398,11 +429,11 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
                 ok = false;
                 break;
             }
-            const uint32_t sa = ptx::smem_u32(smem + stage * kStageBytes);
+            const uint32_t sa = ptx::smem_u32(smem + stage * kCStageBytes);
             const uint32_t fb = ptx::smem_u32(&c.full[stage]);
             ptx::mbar_arrive_expect_tx(fb, kXBytesSmall + kBBytes);
-            ptx::tma_load_2d(sa, &tmX, kb * kTcBK, 0, fb);  // 16 token rows; rows 16..127 unused
-            ptx::tma_load_2d(sa + kABytes, &tmW, kb * kTcBK, 0, fb);
+            ptx::tma_load_2d(sa, &tmX, kb * kTcBK, 0, fb);  // 16 token rows
+            ptx::tma_load_2d(sa + kXBytesSmall, &tmW, kb * kTcBK, 0, fb);
             last_par[stage] = phase;
             ++issued;
             if (++stage == kCStages) {
@@ -426,8 +457,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
                 break;
             }
             ptx::tc_fence_after();
-            const uint32_t sa = ptx::smem_u32(smem + stage * kStageBytes);
-            const uint64_t adesc = ptx::sw128_desc(sa), bdesc = ptx::sw128_desc(sa + kABytes);
+            const uint32_t sa = ptx::smem_u32(smem + stage * kCStageBytes);
+            const uint64_t adesc = ptx::sw128_desc(sa), bdesc = ptx::sw128_desc(sa + kXBytesSmall);
 #pragma unroll
             for (int kk = 0; kk < kTcBK / 16; ++kk)
                 ptx::mma_bf16(tmem, adesc + 2u * kk, bdesc + 2u * kk, kIdesc, (i > 0 || kk > 0) ? 1u : 0u);
@@ -450,56 +481,133 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
                 *static_cast<volatile int*>(&c.abort) == 0;
     ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
     ptx::tc_fence_after();
+    ptx::cluster_wait();
     const int row = warp * 32 + lane;
     if (ready && my_blocks > 0 && warp == 0) {  // rows 0..15 live in warp 0's lanes
-#pragma unroll 1
-        for (int col = 0; col < kN; col += 16) {
-            uint32_t v[16];
-            ptx::tmem_ld16(tmem + (uint32_t)col, v);
-            if (row < a.T) {
+        uint32_t v[kN];
+        ptx::tmem_ld16x4(tmem, tmem + 16u, tmem + 32u, tmem + 48u, v);
+        if (row < a.T) {
+            float* mine = part + ((size_t)rank * kCTok + row) * kN;
+            if (rank == 0) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const uint32_t local = ptx::smem_u32(part + ((size_t)rank * kCTok + row) * kN + col + i);
-                    ptx::st_cluster_f32(ptx::map_to_rank(local, 0), __uint_as_float(v[i]));
-                }
+                for (int q = 0; q < kN / 4; ++q)
+                    reinterpret_cast<float4*>(mine)[q] = make_float4(
+                        __uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]), __uint_as_float(v[4 * q + 2]),
+                        __uint_as_float(v[4 * q + 3]));
+            } else {
+                const uint32_t dst = ptx::map_to_rank(ptx::smem_u32(mine), 0);
+                const uint32_t bar = ptx::map_to_rank(xfer, 0);
+#pragma unroll
+                for (int q = 0; q < kN / 4; ++q)
+                    ptx::st_async_v4(dst + 16u * q, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3], bar);
             }
         }
     }
-    ptx::cluster_sync();
 
     if (rank == 0) {
-        const int nparts = kb_total < kCluster ? kb_total : kCluster;
-        // combine: every thread takes (token, 4 experts) tasks; partials in order 0..7
-        for (int task = threadIdx.x; task < a.T * (kN / 4); task += kThreads) {
-            const int r = task / (kN / 4), e4 = task % (kN / 4);
-            float s4[4] = {0.f, 0.f, 0.f, 0.f}, c4[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int p = 0; p < nparts; ++p) {
-                const float4 v = reinterpret_cast<const float4*>(part + ((size_t)p * kCTok + r) * kN)[e4];
-                kahan_add(s4[0], c4[0], v.x);
-                kahan_add(s4[1], c4[1], v.y);
-                kahan_add(s4[2], c4[2], v.z);
-                kahan_add(s4[3], c4[3], v.w);
-            }
-            // partial 0 is no longer needed: the combined logits overwrite it
-            reinterpret_cast<float4*>(part + (size_t)r * kN)[e4] = make_float4(s4[0], s4[1], s4[2], s4[3]);
+        // the other partials: bounded wait on the exchange barrier (also when
+        // this CTA failed, so that no write lands after it has exited)
+        bool got = true;
+        if (threadIdx.x == 0) {
+            got = ptx::mbar_wait_cluster(xfer, 0, a.limit_ns);
+            if (!got || !ready) atomicOr(a.err, kErrTimeout);
         }
-        __syncthreads();
-        if (row < a.T) {
-            float l[kN];
-            const float4* src = reinterpret_cast<const float4*>(part + (size_t)row * kN);
+        const bool go = __syncthreads_and(got && ready) != 0;
+        ptx::cluster_arrive();   // second phase: CTA 0 has received everything
+        if (go) {
+            // thread (token r, lane-group position g) owns experts 8g..8g+7
+            const int r = threadIdx.x / kGroup, g = threadIdx.x % kGroup;
+            const unsigned gmask = 0xffu << (lane & ~(kGroup - 1));
+            if (r < a.T) {
+                float l[kPerThread];
+                {
+                    float sum[kPerThread], comp[kPerThread];
 #pragma unroll
-            for (int e4 = 0; e4 < kN / 4; ++e4) {
-                const float4 v = src[e4];
-                l[4 * e4] = v.x;
-                l[4 * e4 + 1] = v.y;
-                l[4 * e4 + 2] = v.z;
-                l[4 * e4 + 3] = v.w;
+                    for (int i = 0; i < kPerThread; ++i) sum[i] = comp[i] = 0.f;
+                    for (int p = 0; p < nparts; ++p) {  // partials in order 0..7, as router_tc_kernel
+                        const float4* src =
+                            reinterpret_cast<const float4*>(part + ((size_t)p * kCTok + r) * kN + g * kPerThread);
+                        const float4 v0 = src[0], v1 = src[1];
+                        kahan_add(sum[0], comp[0], v0.x);
+                        kahan_add(sum[1], comp[1], v0.y);
+                        kahan_add(sum[2], comp[2], v0.z);
+                        kahan_add(sum[3], comp[3], v0.w);
+                        kahan_add(sum[4], comp[4], v1.x);
+                        kahan_add(sum[5], comp[5], v1.y);
+                        kahan_add(sum[6], comp[6], v1.z);
+                        kahan_add(sum[7], comp[7], v1.w);
+                    }
+#pragma unroll
+                    for (int i = 0; i < kPerThread; ++i) {
+                        const int e = g * kPerThread + i;
+                        l[i] = sum[i];
+                        if (e < a.E) {
+                            if (a.bias != nullptr) l[i] += a.bias[e];
+                            if (a.logits != nullptr) a.logits[(int64_t)r * a.E + e] = l[i];
+                        } else {
+                            l[i] = -INFINITY;
+                        }
+                    }
+                }
+                // k rounds: the group's maximum logit, lower expert index on
+                // equal logits (the rule of select_topk), then masked out.
+                // Weights exp(l_j - l_0) / sum_j' exp(l_j' - l_0), summed in
+                // round order exactly as select_topk does.
+                float v0 = 0.f, den = 0.f, w_lo = 0.f, w_hi = 0.f;
+                int id_lo = 0, id_hi = 0;
+#pragma unroll 1
+                for (int j = 0; j < k; ++j) {
+                    float bv = l[0];
+                    int bi = 0;
+#pragma unroll
+                    for (int i = 1; i < kPerThread; ++i)
+                        if (l[i] > bv) {
+                            bv = l[i];
+                            bi = i;
+                        }
+                    bi += g * kPerThread;
+#pragma unroll
+                    for (int d = 1; d < kGroup; d <<= 1) {
+                        const float ov = __shfl_xor_sync(gmask, bv, d);
+                        const int oi = __shfl_xor_sync(gmask, bi, d);
+                        if (ov > bv || (ov == bv && oi < bi)) {
+                            bv = ov;
+                            bi = oi;
+                        }
+                    }
+                    if (g == 0 && (bv != bv || bi >= a.E)) atomicOr(a.err, kErrCheck);  // NaN logits only
+#pragma unroll
+                    for (int i = 0; i < kPerThread; ++i)
+                        if (g * kPerThread + i == bi) l[i] = -INFINITY;
+                    if (j == 0) v0 = bv;
+                    const float ej = expf(bv - v0);
+                    den += ej;
+                    if (j == g) {
+                        w_lo = ej;
+                        id_lo = bi;
+                    } else if (j == g + kGroup) {
+                        w_hi = ej;
+                        id_hi = bi;
+                    }
+                }
+                if (g < k) {
+                    a.ids[(int64_t)r * k + g] = id_lo;
+                    a.w[(int64_t)r * k + g] = w_lo / den;
+                    sid[r * k + g] = id_lo;
+                    atomicAdd(&c.hist[id_lo], 1);
+                }
+                if (g + kGroup < k) {
+                    a.ids[(int64_t)r * k + g + kGroup] = id_hi;
+                    a.w[(int64_t)r * k + g + kGroup] = w_hi / den;
+                    sid[r * k + g + kGroup] = id_hi;
+                    atomicAdd(&c.hist[id_hi], 1);
+                }
             }
-            finish_logits(l, row, a);
-            select_topk(l, k, row, row, a, sid, c.hist);
+            __syncthreads();
+            finish_single<4>(a, c.hist, c.off, c.cnt, c.run, sid);
         }
-        __syncthreads();
-        finish_single<4>(a, c.hist, c.off, c.cnt, c.run, sid);
+    } else {
+        ptx::cluster_arrive();   // second phase: this CTA's partial is on its way
     }
 
     ptx::tc_fence_before();
@@ -508,6 +616,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, kN);
     }
+    ptx::cluster_wait();   // no CTA leaves before CTA 0 holds every partial
 }
 
 }  // namespace
