@@ -14,17 +14,21 @@
 //       pairs them through shared memory and writes silu(gate) * up.
 //   down tile (GEMM2): (expert e, 128 output columns), K runs over all micros
 //       into one accumulator.
-// The routed layer runs both in ONE persistent cooperative launch: the work
+// The routed layer runs both in ONE persistent launch: the work
 // list is every SwiGLU tile (expert order) followed by every down tile. A
 // down tile of expert e first waits until all SwiGLU tiles of e have stored
 // their h rows (a per-expert counter, bounded wait), so the down projection's
 // weight stream starts on SMs as soon as they run out of SwiGLU tiles instead
-// of after the slowest one, and one kernel boundary disappears. All CTAs are
-// co-resident (cooperative launch, one CTA per SM) and tiles are handed out in
-// increasing order, so every awaited SwiGLU tile is already owned by a running
-// CTA. Before its tiles, each CTA's epilogue warps gather a share of the routed
+// of after the slowest one, and one kernel boundary disappears. Tiles (and
+// finalize items) are handed out in increasing order to CTAs that are already
+// running, so every awaited SwiGLU tile is owned by a running CTA and no CTA
+// waits for another to become resident: the launch is an ordinary one with
+// programmatic dependent launch, so the CTAs that find a free SM set up while
+// the router still runs and the rest join when the router's SMs free up; the
+// gathered rows go to the first kGatherCtas CTAs, which start first. Before its tiles, each CTA's epilogue warps gather a share of the routed
 // token rows (a SwiGLU tile waits only for its expert's rows, and its weight
-// stages are issued meanwhile); after its tiles they run finalize items, each
+// stages are issued meanwhile); after its tiles they take finalize items from
+// a global counter (the CTAs that run out of tiles first take them), each
 // gated on the down tiles of its token's experts. The whole routed layer after
 // routing is therefore one launch.
 // Structure: 12-stage TMA ring, one MMA issuer, four epilogue warps on a
@@ -33,7 +37,6 @@
 // waits for its dependency (the expert's SwiGLU tiles, or its gathered rows)
 // while the producer streams the current one, so neither global round trip
 // sits between two tiles of the weight stream. All waits are bounded.
-#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 
 #include "gemm_common.cuh"
@@ -51,6 +54,7 @@ constexpr int kBBytes = kTok * kTcBK * 2;      // 2 KB
 constexpr int kStageBytes = kABytes + kBBytes; // 18 KB (a multiple of 1024)
 constexpr int kTmemCols = 32;                  // 2 accumulators x 16 columns
 constexpr int kThreads = 256;
+constexpr int kGatherCtas = 128;               // kFused: CTAs that gather token rows
 constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kM, kTok);
 
 enum Mode { kSwiGLUOnly = 0, kDownOnly = 1, kFused = 2 };
@@ -68,6 +72,7 @@ struct Ctl {
     float up[64][kTok + 1];
     int ep_ok[4];
     int fin_fail;
+    int fin_item;
     // kFused: tiles fetched from a global counter by the producer and handed to
     // the MMA and epilogue warps through this ring
     uint64_t tq_full[4];
@@ -87,7 +92,8 @@ struct SmallParams {
     TcGemmArgs g1;     // SwiGLU tiles (unused in kDownOnly)
     TcGemmArgs g2;     // down tiles (unused in kSwiGLUOnly)
     int* done;         // kFused: [E] finished SwiGLU tiles, [E] finished down tiles, [1] next
-                       // tile to hand out, [E] gathered rows; zero at launch
+                       // tile to hand out, [E] gathered rows, [1] next finalize item;
+                       // zero at launch
     FinalizeArgs fin;  // kFused: the finalize run after the tiles (fin.y null = none)
     // kFused: the gather xp[i] = x[perm[i] / k] run at the start (x null = none)
     const void* gx;
@@ -135,16 +141,17 @@ __device__ __forceinline__ int expert_of(const int* seg, int G, int pos) {
 }
 
 // The gather xp[i] = x[perm[i] / k] (blog section 6.1: index_select once), as
-// the fused kernel's first phase, run by the four epilogue warps: CTA b copies
-// rows b, b + gridDim.x, ... and counts each finished row for its expert, so a
-// SwiGLU tile only waits for the rows of its own expert.
+// the fused kernel's first phase, run by the four epilogue warps: CTA b <
+// kGatherCtas copies rows b, b + kGatherCtas, ... and counts each finished row
+// for its expert, so a SwiGLU tile only waits for the rows of its own expert.
 __device__ __forceinline__ void gather_rows(const Ctl& c, const SmallParams& p) {
     const int tid = threadIdx.x - 128;
     const int R = c.seg[p.g1.G];
     const int nvec = p.grow_bytes / 16;
     const uint4* __restrict__ src = static_cast<const uint4*>(p.gx);
     uint4* __restrict__ dst = static_cast<uint4*>(p.gxp);
-    for (int i = blockIdx.x; i < R; i += gridDim.x) {
+    const int gctas = (int)gridDim.x < kGatherCtas ? (int)gridDim.x : kGatherCtas;
+    for (int i = blockIdx.x; i < R; i += gctas) {
         const int64_t tok = p.gperm[i] / p.gk;
         constexpr int kBatch = 8;
         for (int v0 = tid; v0 < nvec; v0 += 128 * kBatch) {
@@ -167,7 +174,8 @@ __device__ __forceinline__ void gather_rows(const Ctl& c, const SmallParams& p) 
 
 // The finalize ("HunyuanImage3 Hybrid Parallelism", section 6.1: routing scale
 // applied once, top-k reduced once) as the fused kernel's last phase, run by
-// the four epilogue warps: item (token t, 1024 columns) waits until the down
+// the four epilogue warps once their CTA has no tiles left: items are taken
+// from a global counter, and item (token t, 1024 columns) waits until the down
 // tiles of t's k experts have stored their o rows, then
 //     y[t] = sum_j w[t][j] * o[inv[t*k + j]] (+ shared[t]) (+ y[t] when
 //     accumulating), fp32 accumulate.
@@ -183,7 +191,11 @@ __device__ __forceinline__ void finalize_items(Ctl& c, const SmallParams& p) {
     const __nv_bfloat16* o = static_cast<const __nv_bfloat16*>(f.o);
     const __nv_bfloat16* sh = static_cast<const __nv_bfloat16*>(f.shared);
     __nv_bfloat16* y = static_cast<__nv_bfloat16*>(f.y);
-    for (int item = blockIdx.x; item < items; item += gridDim.x) {
+    for (;;) {
+        if (tid == 0) c.fin_item = atomicAdd(p.done + 3 * G + 1, 1);
+        epilogue_bar();
+        const int item = c.fin_item;
+        if (item >= items) break;
         const int t = item / chunks, ch = item % chunks;
         if (tid < f.k) {
             const int* cnt = p.done + G + expert_of(c.seg, G, f.inv[(int64_t)t * f.k + tid]);
@@ -412,9 +424,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         c.fin_fail = 0;
         ptx::fence_mbar_init();
     }
-    for (int i = threadIdx.x; i <= a0.G; i += kThreads) {
-        c.seg[i] = a0.seg[i];
-        c.tiles[i] = a0.tiles[i];
+    if (MODE != kFused) {
+        for (int i = threadIdx.x; i <= a0.G; i += kThreads) {
+            c.seg[i] = a0.seg[i];
+            c.tiles[i] = a0.tiles[i];
+        }
     }
     if (warp == 0 && lane == 0) {
         if (MODE != kDownOnly) ptx::prefetch_tmap(&maps.x1);
@@ -427,6 +441,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
+    if (MODE == kFused) {
+        // started early (programmatic dependent launch): nothing the router or
+        // the shared expert's GEMMs write is read before this wait
+        ptx::griddep_wait();
+        for (int i = threadIdx.x; i <= a0.G; i += kThreads) {
+            c.seg[i] = a0.seg[i];
+            c.tiles[i] = a0.tiles[i];
+        }
+        __syncthreads();
+    }
 
     const uint32_t tmem = c.tmem_base;
     const int n1 = MODE == kDownOnly ? 0 : p.g1.n_micro * c.tiles[p.g1.G] * p.g1.n_tiles;
@@ -613,6 +637,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tc_fence_after();
             uint32_t v[kTok];
             ptx::tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kTok), v);
+            // the accumulator is in registers: hand it back to the MMA issuer
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&c.tempty[acc]));
             const int cnt = min(kTok, t.row_end - t.row0);
             if (sw) {
                 if (q >= 2) {
@@ -646,9 +674,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&c.tempty[acc]));
         }
         if (MODE == kFused && p.fin.y != nullptr) finalize_items(c, p);
     }
@@ -673,10 +698,19 @@ cudaError_t launch_small(const SmallMaps& maps, const SmallParams& p, int max_ti
     }
     const int grid = max_tiles < num_sms ? max_tiles : num_sms;
     if (MODE == kFused) {
-        // all CTAs must be resident at once: down tiles wait on other CTAs' SwiGLU tiles
-        void* args[] = {const_cast<SmallMaps*>(&maps), const_cast<SmallParams*>(&p)};
-        return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(tc_small_kernel<MODE>), dim3(grid),
-                                           dim3(kThreads), args, kSmemBytes, s);
+        // may start while the previous kernel in the stream still runs; the
+        // kernel waits for its results (griddep_wait) after its own set-up
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = kSmemBytes;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, tc_small_kernel<MODE>, maps, p);
     }
     tc_small_kernel<MODE><<<grid, kThreads, kSmemBytes, s>>>(maps, p);
     return cudaGetLastError();
@@ -723,10 +757,7 @@ cudaError_t launch_tc_small_fused(const TcGemmArgs& g1, const CUtensorMap& tmX1,
     fill_maps(maps, tmX1, tmW1, g1.n_micro, true);
     fill_maps(maps, tmX2, tmW2, g2.n_micro, false);
     SmallParams p{g1, g2, done, fin, gat.x, gat.xp, gat.perm, gat.k, (int)gat.row_bytes};
-    // enough CTAs for the finalize items as well (T tokens x 1024-column chunks)
-    const int fin_items = fin.y ? fin.T * ((fin.H / 8 + 127) / 128) : 0;
-    const int work = g1.max_tiles + g2.max_tiles > fin_items ? g1.max_tiles + g2.max_tiles : fin_items;
-    return launch_small<kFused>(maps, p, work, num_sms, s);
+    return launch_small<kFused>(maps, p, g1.max_tiles + g2.max_tiles, num_sms, s);
 }
 
 }  // namespace moe

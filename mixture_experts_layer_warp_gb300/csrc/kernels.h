@@ -58,7 +58,8 @@ struct RouterTcArgs {
     int32_t* shared_tiles_simt;  // [2]
     int32_t* perm;          // [T*k]
     int32_t* inv;           // [T*k]
-    int32_t* zero_counters; // [3E+1] set to 0 by the single-CTA paths, or null
+    int32_t* zero_counters; // [zero_count] set to 0 by the single-CTA paths, or null
+    int zero_count;
     int* err;
     uint64_t limit_ns;
 };
@@ -158,11 +159,14 @@ cudaError_t launch_tc_small_swiglu(const TcGemmArgs& a, const CUtensorMap& tmX, 
                                    int num_sms, cudaStream_t s);
 cudaError_t launch_tc_small_down(const TcGemmArgs& a, const CUtensorMap& tmX, const CUtensorMap* tmW,
                                  int num_sms, cudaStream_t s);
-// Both GEMMs of the routed experts and the finalize in one persistent
-// cooperative launch: the down tiles of expert e start once the SwiGLU tiles
-// of e have stored h, and a token's finalize once the down tiles of its k
-// experts have stored o; its first phase gathers xp from x (gat.x non-null).
-// done[3E+1] must be zero at launch (the small-batch router zeroes it).
+// Both GEMMs of the routed experts and the finalize in one persistent launch
+// (programmatic dependent launch: it may start while the previous kernel in
+// the stream runs and waits for it after its set-up): the down tiles of
+// expert e start once the SwiGLU tiles of e have stored h, and a token's
+// finalize once the down tiles of its k experts have stored o; its first phase
+// gathers xp from x (gat.x non-null). done[fused_counter_ints(E)] must be zero
+// at launch (the small-batch router zeroes it).
+inline int fused_counter_ints(int E) { return 3 * E + 2; }
 cudaError_t launch_tc_small_fused(const TcGemmArgs& g1, const CUtensorMap& tmX1, const CUtensorMap* tmW1,
                                   const TcGemmArgs& g2, const CUtensorMap& tmX2, const CUtensorMap* tmW2,
                                   const FinalizeArgs& fin, const GatherArgs& gat, int* done, int num_sms,
@@ -216,7 +220,8 @@ struct RoutingJob {
     int32_t* blk_base;        // same
     int* err;
     uint64_t limit_ns;
-    int32_t* zero_counters;   // [3E+1] zeroed when routing runs in one CTA (T <= 128), or null
+    int32_t* zero_counters;   // zeroed when routing runs in one CTA (T <= 128), or null
+    int zero_count;           // ints of zero_counters
 };
 
 // Optional callbacks around every kernel launch (timing, counting).

@@ -44,7 +44,7 @@ struct moe_handle {
     int32_t* shared_meta = nullptr;  // shared expert: seg[2], tiles_tc[2], tiles_simt[2]
     int32_t* blk_hist = nullptr;
     int32_t* blk_base = nullptr;
-    int* done = nullptr;  // per-expert SwiGLU-tile counters of the fused small-batch GEMMs
+    int* done = nullptr;  // counters of the fused small-batch kernel (fused_counter_ints of them)
     void* xp = nullptr;
     void* hbuf = nullptr;
     void* obuf = nullptr;
@@ -161,7 +161,8 @@ moe_status run_routing(moe_handle* h, const void* x, const void* router_w, const
     const moe_config& c = h->cfg;
     RoutingJob j{x, router_w, bias, T, c.hidden, c.num_experts, c.top_k, c.dtype == MOE_BF16, h->ids, h->topw,
                  logits, h->perm, h->inv, h->offsets, h->tiles_tc, h->tiles_simt, h->shared_meta, h->blk_hist,
-                 h->blk_base, h->err, h->limit_ns, h->done};
+                 h->blk_base, h->err, h->limit_ns, h->done,
+                 fused_counter_ints(c.num_experts)};
     LaunchHook hook{h, hook_before, hook_after};
     cudaError_t e = enqueue_routing(j, s, &hook);
     if (e == cudaErrorInvalidValue) return set_err(h, MOE_ERR_CUDA, "router tensor map encode failed");
@@ -225,7 +226,7 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
                            [&] { return launch_tc_small_down(s2, sX, sW, h->num_sms, s); })) != cudaSuccess)
                 return cuda_err(h, e, "shared GEMM2 launch");
         }
-        // gather, both GEMMs and the finalize in one cooperative launch (the
+        // gather, both GEMMs and the finalize in one launch (the
         // router zeroed h->done); the shared expert's GEMMs ran first
         FinalizeArgs fin{h->obuf, h->inv, h->topw, Is > 0 ? h->sbuf : nullptr, T, k, H, true, y, h->accumulate};
         if ((e = timed(h, kSlotGemm1, s, [&] {
@@ -404,7 +405,7 @@ moe_status moe_create(const moe_config* cfg, moe_handle** out) {
     const size_t o_ids = take(R * 4), o_topw = take(R * 4), o_perm = take(R * 4), o_inv = take(R * 4);
     const size_t o_off = take((E + 1) * 4), o_ttc = take((E + 1) * 4), o_tsi = take((E + 1) * 4);
     const size_t o_smeta = take(6 * 4);
-    const size_t o_hist = take(NB * E * 4), o_base = take(NB * E * 4), o_done = take((3 * E + 1) * 4);
+    const size_t o_hist = take(NB * E * 4), o_base = take(NB * E * 4), o_done = take(fused_counter_ints((int)E) * 4);
     const size_t o_xp = take(R * H * esz), o_h = take(R * M * I * esz), o_o = take(R * H * esz);
     const size_t o_hs = take(T * Is * esz), o_s = take(Is ? T * H * esz : 0);
     const size_t o_xst = take(T * H * esz), o_yst = take(T * H * esz);

@@ -95,7 +95,7 @@ extern "C" moe_status moe_route_noalloc(const void* x, const void* router_w, con
     int32_t* shared = reinterpret_cast<int32_t*>(b + kSharedOff);
     RoutingJob j{x, router_w, router_bias, T, hidden, num_experts, top_k, dtype == MOE_BF16, topk_ids, topk_w,
                  nullptr, perm, inv, offsets, tiles_tc, tiles_simt, shared, hist, blk_base, err,
-                 2000000000ull, nullptr};
+                 2000000000ull, nullptr, 0};
     if (enqueue_routing(j, s, nullptr) != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_OK;
 }

@@ -177,6 +177,15 @@ __device__ __forceinline__ void st_async_v4(uint32_t caddr, uint32_t x, uint32_t
 __device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
 
+// Programmatic dependent launch: let the next kernel in the stream start its
+// CTAs now (it waits for this grid's results with griddep_wait) ...
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// ... and, in that kernel, wait until the preceding grid has completed and its
+// memory operations are visible.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Whole-cluster barrier with release/acquire semantics on shared::cluster data.
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");

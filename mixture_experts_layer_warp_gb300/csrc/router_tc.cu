@@ -183,7 +183,7 @@ __device__ __forceinline__ void finish_single(const RouterTcArgs& a, const int* 
     __syncthreads();
     if ((int)threadIdx.x <= E) a.offsets[threadIdx.x] = off[threadIdx.x];
     if (a.zero_counters != nullptr)
-        for (int i = threadIdx.x; i <= 3 * E; i += blockDim.x) a.zero_counters[i] = 0;
+        for (int i = threadIdx.x; i < a.zero_count; i += blockDim.x) a.zero_counters[i] = 0;
     place_chunk<NW>(sid, a.T * a.k, 0, E, (int64_t)a.T * a.k, [&](int e) { return off[e]; }, cnt, run, a.perm,
                     a.inv, a.err);
 }
@@ -191,6 +191,7 @@ __device__ __forceinline__ void finish_single(const RouterTcArgs& a, const int* 
 __global__ void __launch_bounds__(kThreads, 1)
     router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                      const RouterTcArgs a) {
+    ptx::griddep_launch_dependents();  // the fused GEMM kernel may set up meanwhile
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -380,6 +381,7 @@ constexpr int kCSmemBytes = kCRingBytes + kPartBytes + kCIdsBytes + (int)sizeof(
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     router_tc_cluster_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                              const RouterTcArgs a) {
+    ptx::griddep_launch_dependents();  // the fused GEMM kernel may set up meanwhile
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));

@@ -56,7 +56,7 @@ cudaError_t enqueue_routing(const RoutingJob& j, cudaStream_t s, const LaunchHoo
             return cudaErrorInvalidValue;
         RouterTcArgs ra{j.bias, j.T, j.H, j.E, j.k, j.ids, j.w, j.logits, j.blk_hist, j.offsets, j.tiles_tc,
                         j.tiles_simt, j.shared_meta, j.shared_meta + 2, j.shared_meta + 4, j.perm, j.inv,
-                        j.zero_counters, j.err, j.limit_ns};
+                        j.zero_counters, j.zero_count, j.err, j.limit_ns};
         e = hooked(hook, kSlotRouter, s, [&] {
             return small ? launch_router_tc_small(ra, tmX, tmW, s) : launch_router_tc(ra, tmX, tmW, s);
         });
