@@ -14,23 +14,25 @@
 //       pairs them through shared memory and writes silu(gate) * up.
 //   down tile (GEMM2): (expert e, 128 output columns), K runs over all micros
 //       into one accumulator.
-// The routed layer runs both in ONE persistent launch: the work
-// list is every SwiGLU tile (expert order) followed by every down tile. A
-// down tile of expert e first waits until all SwiGLU tiles of e have stored
-// their h rows (a per-expert counter, bounded wait), so the down projection's
-// weight stream starts on SMs as soon as they run out of SwiGLU tiles instead
-// of after the slowest one, and one kernel boundary disappears. Tiles (and
-// finalize items) are handed out in increasing order to CTAs that are already
-// running, so every awaited SwiGLU tile is owned by a running CTA and no CTA
-// waits for another to become resident: the launch is an ordinary one with
-// programmatic dependent launch, so the CTAs that find a free SM set up while
-// the router still runs and the rest join when the router's SMs free up; the
-// gathered rows go to the first kGatherCtas CTAs, which start first. Before its tiles, each CTA's epilogue warps gather a share of the routed
-// token rows (a SwiGLU tile waits only for its expert's rows, and its weight
-// stages are issued meanwhile); after its tiles they take finalize items from
-// a global counter (the CTAs that run out of tiles first take them), each
-// gated on the down tiles of its token's experts. The whole routed layer after
-// routing is therefore one launch.
+// The routed layer runs both in ONE persistent launch: the work list is every
+// SwiGLU tile (expert order) followed by every down tile. A down tile of
+// expert e first waits until all SwiGLU tiles of e have stored their h rows (a
+// per-expert counter, bounded wait), so the down projection's weight stream
+// starts on SMs as soon as they run out of SwiGLU tiles instead of after the
+// slowest one, and one kernel boundary disappears. CTA b starts with tile b;
+// the later tiles (and the finalize items) are handed out in increasing order
+// to CTAs that are running. A down tile therefore only waits for SwiGLU tiles
+// held by CTAs that are running or start as soon as an SM frees up, and no CTA
+// needs all others to be resident: the launch is an ordinary one with
+// programmatic dependent launch, so the CTAs that find a free SM set up (and
+// prefetch weights into L2) while the router still runs and the rest join when
+// the router's SMs free up. Before its tiles, each of the first kGatherCtas
+// CTAs' epilogue warps gather a share of the routed token rows (a SwiGLU tile
+// waits only for its expert's rows, and its weight stages are issued
+// meanwhile); after its tiles they take finalize items from a global counter
+// (the CTAs that run out of tiles first take them), each gated on the down
+// tiles of its token's experts. The whole routed layer after routing is
+// therefore one launch.
 // Structure: 12-stage TMA ring, one MMA issuer, four epilogue warps on a
 // double-buffered 2 x 16-column TMEM accumulator. In the fused mode a fifth
 // role, the scheduler thread, claims the next tile from the global counter and
@@ -101,6 +103,7 @@ struct SmallParams {
     const int32_t* gperm;
     int gk;
     int grow_bytes;
+    WeightPrefetch pf;  // kFused: prefetched into L2 while waiting for the routing
 };
 
 struct SmallMaps {
@@ -327,6 +330,20 @@ __device__ __forceinline__ int consume_tile(Ctl& c, TileStream& ts, int total, u
     return t;
 }
 
+// This CTA's share of the weight prefetch (WeightPrefetch), one warp: boxes
+// {64 columns, 64 rows} of w13 of micro 0, in expert order, gate then up rows
+// of each K-block, spread over all CTAs' prefetching warps.
+__device__ __forceinline__ void prefetch_weights(const CUtensorMap* m, const WeightPrefetch& pf, int lane) {
+    const int boxes = pf.experts * pf.tiles * pf.kblocks * 2;
+    for (int b = blockIdx.x * 32 + lane; b < boxes; b += gridDim.x * 32) {
+        const int half = b & 1;
+        const int kb = (b >> 1) % pf.kblocks;
+        const int tile = (b >> 1) / pf.kblocks;
+        const int e = tile / pf.tiles, nt = tile % pf.tiles;
+        ptx::prefetch_tensor_2d(m, kb * kTcBK, e * pf.rows_per_expert + half * pf.up_offset + nt * 64);
+    }
+}
+
 // Bounded spin until *cnt >= target (acquire); false on timeout or abort.
 __device__ __forceinline__ bool wait_count(const int* cnt, int target, Ctl& c, uint64_t limit_ns) {
     if (ld_acquire(cnt) >= target) return true;
@@ -339,7 +356,8 @@ __device__ __forceinline__ bool wait_count(const int* cnt, int target, Ctl& c, u
     return true;
 }
 
-// Fused mode, scheduler thread: claims list positions one at a time, each only
+// Fused mode, scheduler thread: claims list positions one at a time (the
+// first is the CTA's own index, so no claim delays the start), each only
 // once the producer has taken the previous one (so a CTA holds at most one
 // tile beyond the one it streams), waits until a down tile's SwiGLU tiles are
 // all stored, notes whether a SwiGLU tile's gathered rows are complete, and
@@ -350,11 +368,12 @@ __device__ __forceinline__ void schedule_tiles(Ctl& c, const SmallParams& p, int
     const int target = p.g1.n_micro * p.g1.n_tiles;  // SwiGLU tiles per expert
     uint32_t phase = 0;
     bool ok = true;
-    for (;;) {
+    for (bool first = true;; first = false) {
         if (!ptx::mbar_wait(ptx::smem_u32(&c.sq_empty), phase ^ 1u, p.g1.limit_ns, &c.abort)) ok = false;
         int t = -1, rows = 0;
         if (ok) {
-            t = atomicAdd(p.done + 2 * p.g1.G, 1);
+            // CTA b starts with tile b; the counter hands out the rest in order
+            t = first ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(p.done + 2 * p.g1.G, 1);
             if (t >= total) t = -1;
         }
         if (t >= 0) {
@@ -403,6 +422,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     Ctl& c = *reinterpret_cast<Ctl*>(smem + kStages * kStageBytes);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const TcGemmArgs& a0 = MODE == kDownOnly ? p.g2 : p.g1;  // seg, tiles, G, err, limit
+    // the next routing call's kernels may be placed as SMs free up; they wait
+    // for this grid to complete before touching memory
+    if (MODE == kFused) ptx::griddep_launch_dependents();
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -442,6 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     ptx::tc_fence_after();
     if (MODE == kFused) {
+        if (warp == 3) prefetch_weights(&maps.w1[0], p.pf, lane);
         // started early (programmatic dependent launch): nothing the router or
         // the shared expert's GEMMs write is read before this wait
         ptx::griddep_wait();
@@ -459,6 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer
+        const uint64_t wpol = ptx::policy_evict_first();  // each weight byte is read once per call
         int stage = 0;
         uint32_t phase = 0, last_par[kStages];
         int issued = 0;
@@ -497,10 +521,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t fb = ptx::smem_u32(&c.full[stage]);
                     ptx::mbar_arrive_expect_tx(fb, kStageBytes);
                     if (sw) {
-                        ptx::tma_load_2d(sa, tw, kb * kTcBK, wrow, fb);                       // 64 gate rows
-                        ptx::tma_load_2d(sa + kABytes / 2, tw, kb * kTcBK, wrow + g.up_offset, fb);  // 64 up rows
+                        ptx::tma_load_2d_hint(sa, tw, kb * kTcBK, wrow, fb, wpol);            // 64 gate rows
+                        ptx::tma_load_2d_hint(sa + kABytes / 2, tw, kb * kTcBK, wrow + g.up_offset, fb,
+                                              wpol);                                           // 64 up rows
                     } else {
-                        ptx::tma_load_2d(sa, tw, kb * kTcBK, wrow, fb);                       // 128 rows
+                        ptx::tma_load_2d_hint(sa, tw, kb * kTcBK, wrow, fb, wpol);            // 128 rows
                     }
                     const int kx = (sw ? 0 : m * g.a_micro_cols) + kb * kTcBK;
                     if (rows_ready) {
@@ -751,12 +776,12 @@ cudaError_t launch_tc_small_down(const TcGemmArgs& a, const CUtensorMap& tmX, co
 
 cudaError_t launch_tc_small_fused(const TcGemmArgs& g1, const CUtensorMap& tmX1, const CUtensorMap* tmW1,
                                   const TcGemmArgs& g2, const CUtensorMap& tmX2, const CUtensorMap* tmW2,
-                                  const FinalizeArgs& fin, const GatherArgs& gat, int* done, int num_sms,
-                                  cudaStream_t s) {
+                                  const FinalizeArgs& fin, const GatherArgs& gat, int* done,
+                                  const WeightPrefetch& pf, int num_sms, cudaStream_t s) {
     SmallMaps maps;
     fill_maps(maps, tmX1, tmW1, g1.n_micro, true);
     fill_maps(maps, tmX2, tmW2, g2.n_micro, false);
-    SmallParams p{g1, g2, done, fin, gat.x, gat.xp, gat.perm, gat.k, (int)gat.row_bytes};
+    SmallParams p{g1, g2, done, fin, gat.x, gat.xp, gat.perm, gat.k, (int)gat.row_bytes, pf};
     return launch_small<kFused>(maps, p, g1.max_tiles + g2.max_tiles, num_sms, s);
 }
 

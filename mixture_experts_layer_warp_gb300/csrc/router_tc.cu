@@ -191,7 +191,6 @@ __device__ __forceinline__ void finish_single(const RouterTcArgs& a, const int* 
 __global__ void __launch_bounds__(kThreads, 1)
     router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                      const RouterTcArgs a) {
-    ptx::griddep_launch_dependents();  // the fused GEMM kernel may set up meanwhile
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -219,10 +218,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
+    // launched early (programmatic dependent launch): no global memory is
+    // touched before the previous kernel in the stream has completed
+    ptx::griddep_wait();
     const uint32_t tmem = c.tmem;
 
     if (warp == 0 && lane == 0) {
         // TMA producer
+        const uint64_t wpol = ptx::policy_evict_last();  // the router matrix is read on every call
         int stage = 0;
         uint32_t phase = 0, last_par[kStages];
         int issued = 0;
@@ -236,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t fb = ptx::smem_u32(&c.full[stage]);
             ptx::mbar_arrive_expect_tx(fb, kStageBytes);
             ptx::tma_load_2d(sa, &tmX, kb * kTcBK, t0, fb);
-            ptx::tma_load_2d(sa + kABytes, &tmW, kb * kTcBK, 0, fb);
+            ptx::tma_load_2d_hint(sa + kABytes, &tmW, kb * kTcBK, 0, fb, wpol);
             last_par[stage] = phase;
             ++issued;
             if (++stage == kStages) {
@@ -286,6 +289,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ready = ptx::mbar_wait(ptx::smem_u32(&c.done), 0, a.limit_ns, nullptr) &&
                 *static_cast<volatile int*>(&c.abort) == 0;
     ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
+    // the logits' loads are done: the next kernel (the fused GEMMs) may start
+    // its set-up and weight prefetch now without queueing ahead of them
+    ptx::griddep_launch_dependents();
     ptx::tc_fence_after();
 
     const int row = warp * 32 + lane;
@@ -381,7 +387,6 @@ constexpr int kCSmemBytes = kCRingBytes + kPartBytes + kCIdsBytes + (int)sizeof(
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     router_tc_cluster_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                              const RouterTcArgs a) {
-    ptx::griddep_launch_dependents();  // the fused GEMM kernel may set up meanwhile
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -418,9 +423,13 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     __syncthreads();
     ptx::tc_fence_after();
     ptx::cluster_arrive();   // first phase: barrier inits visible cluster-wide
+    // launched early (programmatic dependent launch): no global memory is
+    // touched before the previous kernel in the stream has completed
+    ptx::griddep_wait();
     const uint32_t tmem = c.tmem;
 
     if (warp == 0 && lane == 0) {
+        const uint64_t wpol = ptx::policy_evict_last();  // the router matrix is read on every call
         int stage = 0;
         uint32_t phase = 0, last_par[kCStages];
         int issued = 0;
@@ -435,7 +444,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
             const uint32_t fb = ptx::smem_u32(&c.full[stage]);
             ptx::mbar_arrive_expect_tx(fb, kXBytesSmall + kBBytes);
             ptx::tma_load_2d(sa, &tmX, kb * kTcBK, 0, fb);  // 16 token rows
-            ptx::tma_load_2d(sa + kXBytesSmall, &tmW, kb * kTcBK, 0, fb);
+            ptx::tma_load_2d_hint(sa + kXBytesSmall, &tmW, kb * kTcBK, 0, fb, wpol);
             last_par[stage] = phase;
             ++issued;
             if (++stage == kCStages) {
@@ -482,6 +491,9 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
         ready = ptx::mbar_wait(ptx::smem_u32(&c.done), 0, a.limit_ns, nullptr) &&
                 *static_cast<volatile int*>(&c.abort) == 0;
     ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
+    // the logits' loads are done: the next kernel (the fused GEMMs) may start
+    // its set-up and weight prefetch now without queueing ahead of them
+    ptx::griddep_launch_dependents();
     ptx::tc_fence_after();
     ptx::cluster_wait();
     const int row = warp * 32 + lane;
@@ -621,6 +633,25 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     ptx::cluster_wait();   // no CTA leaves before CTA 0 holds every partial
 }
 
+// Launch with programmatic stream serialization: the CTAs may be placed while
+// the previous kernel in the stream finishes (its CTAs free SMs); each kernel
+// here waits for it (griddep_wait) after its shared-memory and TMEM set-up.
+template <typename K>
+cudaError_t launch_early(K kernel, dim3 grid, int smem, cudaStream_t s, const CUtensorMap& tmX,
+                         const CUtensorMap& tmW, const RouterTcArgs& a) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, tmX, tmW, a);
+}
+
 }  // namespace
 
 cudaError_t launch_router_tc(const RouterTcArgs& a, const CUtensorMap& tmX, const CUtensorMap& tmW,
@@ -634,8 +665,7 @@ cudaError_t launch_router_tc(const RouterTcArgs& a, const CUtensorMap& tmX, cons
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    router_tc_kernel<<<nb, kThreads, kSmemBytes, s>>>(tmX, tmW, a);
-    return cudaGetLastError();
+    return launch_early(router_tc_kernel, dim3(nb), kSmemBytes, s, tmX, tmW, a);
 }
 
 cudaError_t launch_router_tc_small(const RouterTcArgs& a, const CUtensorMap& tmX, const CUtensorMap& tmW,
@@ -649,8 +679,7 @@ cudaError_t launch_router_tc_small(const RouterTcArgs& a, const CUtensorMap& tmX
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    router_tc_cluster_kernel<<<kCluster, kThreads, kCSmemBytes, s>>>(tmX, tmW, a);
-    return cudaGetLastError();
+    return launch_early(router_tc_cluster_kernel, dim3(kCluster), kCSmemBytes, s, tmX, tmW, a);
 }
 
 }  // namespace moe
