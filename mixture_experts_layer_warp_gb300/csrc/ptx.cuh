@@ -208,6 +208,10 @@ __device__ __forceinline__ void st_async_v4(uint32_t caddr, uint32_t x, uint32_t
 // The two halves of a cluster barrier, for work placed between them.
 __device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
+// Arrive that orders no memory (the barrier only keeps CTAs alive or in step).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
 
 // Programmatic dependent launch: let the next kernel in the stream start its
 // CTAs now (it waits for this grid's results with griddep_wait) ...

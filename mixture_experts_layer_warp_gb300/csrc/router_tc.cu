@@ -191,6 +191,9 @@ __device__ __forceinline__ void finish_single(const RouterTcArgs& a, const int* 
 __global__ void __launch_bounds__(kThreads, 1)
     router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                      const RouterTcArgs a) {
+    // the next kernel (the fused GEMMs) may place its CTAs as SMs free up: it
+    // only sets up and prefetches weights into L2 before waiting for this grid
+    ptx::griddep_launch_dependents();
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -289,9 +292,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         ready = ptx::mbar_wait(ptx::smem_u32(&c.done), 0, a.limit_ns, nullptr) &&
                 *static_cast<volatile int*>(&c.abort) == 0;
     ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
-    // the logits' loads are done: the next kernel (the fused GEMMs) may start
-    // its set-up and weight prefetch now without queueing ahead of them
-    ptx::griddep_launch_dependents();
     ptx::tc_fence_after();
 
     const int row = warp * 32 + lane;
@@ -387,6 +387,9 @@ constexpr int kCSmemBytes = kCRingBytes + kPartBytes + kCIdsBytes + (int)sizeof(
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     router_tc_cluster_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                              const RouterTcArgs a) {
+    // the next kernel (the fused GEMMs) may place its CTAs as SMs free up: it
+    // only sets up and prefetches weights into L2 before waiting for this grid
+    ptx::griddep_launch_dependents();
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -491,9 +494,6 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
         ready = ptx::mbar_wait(ptx::smem_u32(&c.done), 0, a.limit_ns, nullptr) &&
                 *static_cast<volatile int*>(&c.abort) == 0;
     ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
-    // the logits' loads are done: the next kernel (the fused GEMMs) may start
-    // its set-up and weight prefetch now without queueing ahead of them
-    ptx::griddep_launch_dependents();
     ptx::tc_fence_after();
     ptx::cluster_wait();
     const int row = warp * 32 + lane;
@@ -527,7 +527,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
             if (!got || !ready) atomicOr(a.err, kErrTimeout);
         }
         const bool go = __syncthreads_and(got && ready) != 0;
-        ptx::cluster_arrive();   // second phase: CTA 0 has received everything
+        ptx::cluster_arrive_relaxed();   // second phase: CTA 0 has received everything
         if (go) {
             // thread (token r, lane-group position g) owns experts 8g..8g+7
             const int r = threadIdx.x / kGroup, g = threadIdx.x % kGroup;
@@ -621,7 +621,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
             finish_single<4>(a, c.hist, c.off, c.cnt, c.run, sid);
         }
     } else {
-        ptx::cluster_arrive();   // second phase: this CTA's partial is on its way
+        ptx::cluster_arrive_relaxed();   // second phase: this CTA's partial is on its way
     }
 
     ptx::tc_fence_before();
