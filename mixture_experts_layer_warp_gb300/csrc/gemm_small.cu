@@ -24,9 +24,8 @@
 // to CTAs that are running. A down tile therefore only waits for SwiGLU tiles
 // held by CTAs that are running or start as soon as an SM frees up, and no CTA
 // needs all others to be resident: the launch is an ordinary one with
-// programmatic dependent launch, so the CTAs that find a free SM set up (and
-// prefetch weights into L2) while the router still runs and the rest join when
-// the router's SMs free up. Before its tiles, each of the first kGatherCtas
+// programmatic dependent launch, so the CTAs that find a free SM set up while
+// the router still runs and the rest join when the router's SMs free up. Before its tiles, each of the first kGatherCtas
 // CTAs' epilogue warps gather a share of the routed token rows (a SwiGLU tile
 // waits only for its expert's rows, and its weight stages are issued
 // meanwhile); after its tiles they take finalize items from a global counter
@@ -103,7 +102,6 @@ struct SmallParams {
     const int32_t* gperm;
     int gk;
     int grow_bytes;
-    WeightPrefetch pf;  // kFused: prefetched into L2 while waiting for the routing
 };
 
 struct SmallMaps {
@@ -330,20 +328,6 @@ __device__ __forceinline__ int consume_tile(Ctl& c, TileStream& ts, int total, u
     return t;
 }
 
-// This CTA's share of the weight prefetch (WeightPrefetch), one warp: boxes
-// {64 columns, 64 rows} of w13 of micro 0, in expert order, gate then up rows
-// of each K-block, spread over all CTAs' prefetching warps.
-__device__ __forceinline__ void prefetch_weights(const CUtensorMap* m, const WeightPrefetch& pf, int lane) {
-    const int boxes = pf.experts * pf.tiles * pf.kblocks * 2;
-    for (int b = blockIdx.x * 32 + lane; b < boxes; b += gridDim.x * 32) {
-        const int half = b & 1;
-        const int kb = (b >> 1) % pf.kblocks;
-        const int tile = (b >> 1) / pf.kblocks;
-        const int e = tile / pf.tiles, nt = tile % pf.tiles;
-        ptx::prefetch_tensor_2d(m, kb * kTcBK, e * pf.rows_per_expert + half * pf.up_offset + nt * 64);
-    }
-}
-
 // Bounded spin until *cnt >= target (acquire); false on timeout or abort.
 __device__ __forceinline__ bool wait_count(const int* cnt, int target, Ctl& c, uint64_t limit_ns) {
     if (ld_acquire(cnt) >= target) return true;
@@ -464,7 +448,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     ptx::tc_fence_after();
     if (MODE == kFused) {
-        if (warp == 3) prefetch_weights(&maps.w1[0], p.pf, lane);
         // started early (programmatic dependent launch): nothing the router or
         // the shared expert's GEMMs write is read before this wait
         ptx::griddep_wait();
@@ -776,12 +759,12 @@ cudaError_t launch_tc_small_down(const TcGemmArgs& a, const CUtensorMap& tmX, co
 
 cudaError_t launch_tc_small_fused(const TcGemmArgs& g1, const CUtensorMap& tmX1, const CUtensorMap* tmW1,
                                   const TcGemmArgs& g2, const CUtensorMap& tmX2, const CUtensorMap* tmW2,
-                                  const FinalizeArgs& fin, const GatherArgs& gat, int* done,
-                                  const WeightPrefetch& pf, int num_sms, cudaStream_t s) {
+                                  const FinalizeArgs& fin, const GatherArgs& gat, int* done, int num_sms,
+                                  cudaStream_t s) {
     SmallMaps maps;
     fill_maps(maps, tmX1, tmW1, g1.n_micro, true);
     fill_maps(maps, tmX2, tmW2, g2.n_micro, false);
-    SmallParams p{g1, g2, done, fin, gat.x, gat.xp, gat.perm, gat.k, (int)gat.row_bytes, pf};
+    SmallParams p{g1, g2, done, fin, gat.x, gat.xp, gat.perm, gat.k, (int)gat.row_bytes};
     return launch_small<kFused>(maps, p, g1.max_tiles + g2.max_tiles, num_sms, s);
 }
 

@@ -42,21 +42,6 @@ struct RouterArgs {
 };
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t s);
 
-// Expert weights the fused small-batch kernel is likely to stream first: the
-// leading K-blocks of every SwiGLU tile of experts 0 .. experts-1 (tiles are
-// handed out in expert order), prefetched into L2 by the kernel's CTAs while
-// they wait for the routing results, so that HBM works while the routing
-// finishes. experts = 0: no prefetch.
-struct WeightPrefetch {
-    int experts;
-    int rows_per_expert;  // 2I rows of w13 per expert
-    int up_offset;        // I: the up rows follow the gate rows
-    int tiles;            // I/64 SwiGLU tiles per expert
-    int kblocks;          // leading 64-column K-blocks prefetched per tile
-};
-constexpr int kPrefetchKBlocks = 12;               // the fused kernel's ring depth
-constexpr int64_t kPrefetchMaxBytes = 48ll << 20;  // about what lands while routing finishes
-
 struct RouterTcArgs {
     const float* bias;      // [E] or null
     int T, H, E, k;
@@ -184,8 +169,8 @@ cudaError_t launch_tc_small_down(const TcGemmArgs& a, const CUtensorMap& tmX, co
 inline int fused_counter_ints(int E) { return 3 * E + 2; }
 cudaError_t launch_tc_small_fused(const TcGemmArgs& g1, const CUtensorMap& tmX1, const CUtensorMap* tmW1,
                                   const TcGemmArgs& g2, const CUtensorMap& tmX2, const CUtensorMap* tmW2,
-                                  const FinalizeArgs& fin, const GatherArgs& gat, int* done,
-                                  const WeightPrefetch& pf, int num_sms, cudaStream_t s);
+                                  const FinalizeArgs& fin, const GatherArgs& gat, int* done, int num_sms,
+                                  cudaStream_t s);
 
 // ---------------------------------------------------- fp32 SIMT GEMMs
 constexpr int kSimtBM = 32;

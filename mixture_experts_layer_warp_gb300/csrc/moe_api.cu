@@ -3,7 +3,6 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
-#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -156,24 +155,6 @@ moe_status check_call(moe_handle* h, const void* x, const void* router_w, int32_
     return MOE_OK;
 }
 
-// Experts whose leading weight K-blocks the small-batch router prefetches for
-// the fused kernel: enough low-index experts to cover its first wave of tiles
-// (one per SM) when each expert is touched with probability 1 - (1 - k/E)^T
-// (uniform routing), capped by kPrefetchMaxBytes.
-WeightPrefetch plan_prefetch(const moe_handle* h, int32_t T) {
-    const moe_config& c = h->cfg;
-    const int tiles = c.inter / 64, kblocks = c.hidden / kTcBK < kPrefetchKBlocks ? c.hidden / kTcBK
-                                                                                   : kPrefetchKBlocks;
-    const double p_touch = 1.0 - std::pow(1.0 - (double)c.top_k / c.num_experts, (double)T);
-    const double wave = (double)h->num_sms / ((double)c.n_micro * tiles);
-    int experts = (int)std::ceil(wave / (p_touch > 0.01 ? p_touch : 0.01));
-    const int64_t per_expert = (int64_t)tiles * kblocks * 2 * 64 * kTcBK * 2;  // bytes
-    const int cap = (int)(kPrefetchMaxBytes / per_expert);
-    if (experts > cap) experts = cap;
-    if (experts > c.num_experts) experts = c.num_experts;
-    return WeightPrefetch{experts, 2 * c.inter, c.inter, tiles, kblocks};
-}
-
 // Router, scan and placement: leaves ids, topw, offsets, tiles, perm and inv in the workspace.
 moe_status run_routing(moe_handle* h, const void* x, const void* router_w, const float* bias, int32_t T,
                        float* logits, cudaStream_t s) {
@@ -249,8 +230,7 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
         FinalizeArgs fin{h->obuf, h->inv, h->topw, Is > 0 ? h->sbuf : nullptr, T, k, H, true, y, h->accumulate};
         if ((e = timed(h, kSlotGemm1, s, [&] {
                  GatherArgs gat{x, h->perm, (int)R, k, (uint32_t)(H * 2), h->xp, h->err, h->limit_ns, h->num_sms};
-                 return launch_tc_small_fused(g1, tmX, tmW, g2, tmX2, tmW2, fin, gat, h->done,
-                                              plan_prefetch(h, T), h->num_sms, s);
+                 return launch_tc_small_fused(g1, tmX, tmW, g2, tmX2, tmW2, fin, gat, h->done, h->num_sms, s);
              })) != cudaSuccess)
             return cuda_err(h, e, "fused GEMM launch");
     } else if (c.dtype == MOE_BF16) {

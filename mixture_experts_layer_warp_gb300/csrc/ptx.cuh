@@ -126,14 +126,6 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void* tmap,
         : "memory");
 }
 
-// Prefetch of one box of a tensor map into L2 (no completion to wait for).
-__device__ __forceinline__ void prefetch_tensor_2d(const void* tmap, int32_t c0, int32_t c1) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                     reinterpret_cast<uint64_t>(tmap)),
-                 "r"(c0), "r"(c1)
-                 : "memory");
-}
-
 // 2D tiled load of one box into shared memory; completes `bytes` on `bar`.
 // c0 is the innermost (contiguous) coordinate in elements, c1 the row.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int32_t c0, int32_t c1,

@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                      const RouterTcArgs a) {
     // the next kernel (the fused GEMMs) may place its CTAs as SMs free up: it
-    // only sets up and prefetches weights into L2 before waiting for this grid
+    // only sets up its shared memory and TMEM before waiting for this grid
     ptx::griddep_launch_dependents();
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -388,7 +388,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     router_tc_cluster_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                              const RouterTcArgs a) {
     // the next kernel (the fused GEMMs) may place its CTAs as SMs free up: it
-    // only sets up and prefetches weights into L2 before waiting for this grid
+    // only sets up its shared memory and TMEM before waiting for this grid
     ptx::griddep_launch_dependents();
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
