@@ -17,6 +17,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import math
 import json
 import os
 import statistics
@@ -78,6 +79,14 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
+    def wait_first_sample(self, timeout_s: float = 3.0):
+        """Block until nvidia-smi has written its first line (it needs a moment to start)."""
+        t0 = time.time()
+        while self.proc is not None and self.path is not None and time.time() - t0 < timeout_s:
+            if os.path.getsize(self.path) > 0:
+                return
+            time.sleep(0.02)
+
     def summary(self):
         if self.proc is None or self.path is None:
             return None
@@ -94,7 +103,9 @@ class ClockSampler:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]), "reasons": reasons,
-                "samples": len(rows), "power_w_max": max(float(r[3]) for r in rows if r[3] not in ("", "[N/A]"))}
+                "samples": len(rows), "power_w_max": max(float(r[3]) for r in rows if r[3] not in ("", "[N/A]")),
+                "window": f"the timed steps plus {ROLL_S} s of the same steps run back to back before and "
+                          f"after them (nvidia-smi samples every 200 ms)"}
 
 
 # ---------------------------------------------------------------- helpers
@@ -309,6 +320,14 @@ def time_two_dispatch(args, wl, inp, pool, multi_ms, world):
             "saving_pct_of_two_dispatch": 100.0 * (two_ms - multi_ms) / two_ms}
 
 
+ROLL_S = 0.3  # untimed load before and after the timed steps, so that clock samples see it
+
+
+def roll_steps(step_ms: float) -> int:
+    """Steps of about ROLL_S seconds, run untimed around the timed region."""
+    return int(min(20000, max(1, math.ceil(ROLL_S * 1e3 / max(step_ms, 1e-3)))))
+
+
 def run_ours(args, wl, world, rank, local):
     peaks = load_peaks()
     inp = W.make_inputs(wl, seed=0, device="cuda")
@@ -322,24 +341,32 @@ def run_ours(args, wl, world, rank, local):
         layer.forward(pool[i % POOL], *args_w, out=y)
 
     ids_pool = [layer.route(x, inp["router_w"], inp["router_bias"])["ids"].cpu().numpy() for x in pool]
-    for i in range(args.warmup):
-        step(i)
-    layer.sync()
-
     stream = torch.cuda.current_stream()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    l0 = layer.launch_count()
+    ev0.record(stream)
+    for i in range(args.warmup):
+        step(i)
+    ev1.record(stream)
+    layer.sync()
+    roll = roll_steps(ev0.elapsed_time(ev1) / max(args.warmup, 1))
+
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        clk.wait_first_sample()
+        for i in range(roll):  # untimed: the same load, so the clock samples see it
+            step(i)
+        l0 = layer.launch_count()
         ev0.record(stream)
         for i in range(args.steps):
             step(args.warmup + i)
         ev1.record(stream)
+        launches = layer.launch_count() - l0
+        for i in range(roll):
+            step(i)
         ev1.synchronize()
-    torch.cuda.synchronize()
+        torch.cuda.synchronize()
     barrier(world)
-    launches = layer.launch_count() - l0
     layer.sync()
     ms, value = job_throughput(world, wl.T, args.steps, ev0.elapsed_time(ev1))
 
