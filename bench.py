@@ -334,6 +334,8 @@ def run_ours(args, wl, world, rank, local):
     pool = [W.make_inputs(wl, seed=100 + i, device="cuda", experts=False)["x"] for i in range(POOL)]
     layer = binding.MoELayer(wl.H, wl.E, wl.k, wl.I, wl.n_micro, max_tokens=wl.T,
                              shared_inter=wl.shared_inter, dtype=wl.torch_dtype)
+    if args.shared_stream:
+        layer.set_shared_stream(True)
     y = torch.empty((wl.T, wl.H), dtype=wl.torch_dtype, device="cuda")
     args_w = (inp["router_w"], inp["router_bias"], inp["w13"], inp["w2"], inp["shared_w13"], inp["shared_w2"])
 
@@ -416,7 +418,8 @@ def run_ours(args, wl, world, rank, local):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic", "config": config_of(wl),
+        "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "config": dict(config_of(wl), **({"shared_stream": True} if args.shared_stream else {})),
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
         "kernels_ms_per_step": {k: v[0] / args.steps for k, v in prof.items()},
         "clocks": clk.summary(),
@@ -435,6 +438,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(W.WORKLOADS), default="decode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--shared-stream", action="store_true",
+                    help="run the shared expert's GEMMs on a second stream (moe_set_shared_stream)")
     ap.add_argument("--two-dispatch", action="store_true",
                     help="also time the two-dispatch form of a multi-micro workload")
     args = ap.parse_args()

@@ -109,10 +109,12 @@ moe_status moe_route(moe_handle *h, const void *x, const void *router_w,
  * The whole layer (blog section 6.1 and 6.2):
  *   y[t] = sum_j topk_w[t][j] * sum_m down_m,e(silu(gate_m,e x_t) * up_m,e x_t)
  *          (+ shared_down(silu(shared_gate x_t) * shared_up x_t))
- * with e = topk_ids[t][j]. Steps, all on `stream`: router + histogram, scan
- * -> offsets, stable placement -> permutation, one gather of x, grouped GEMM1
- * with the SwiGLU epilogue for every micro, grouped GEMM2 accumulating all
- * micros of a route in one fp32 accumulator, (shared expert GEMMs), finalize.
+ * with e = topk_ids[t][j]. Steps, all ordered on `stream`: router + histogram,
+ * scan -> offsets, stable placement -> permutation, one gather of x, grouped
+ * GEMM1 with the SwiGLU epilogue for every micro, grouped GEMM2 accumulating
+ * all micros of a route in one fp32 accumulator, (shared expert GEMMs),
+ * finalize (see moe_set_shared_stream for running the shared expert's GEMMs
+ * on a second stream).
  * Inputs (device):
  *   x          [T][H]
  *   router_w   [E][H], router_bias fp32 [E] or NULL
@@ -153,6 +155,19 @@ moe_status moe_forward_host(moe_handle *h, const void *x_host, const void *route
  * single-micro handles, the second with accumulation on. Default off.
  */
 moe_status moe_set_accumulate(moe_handle *h, int32_t on);
+
+/*
+ * Shared expert on a second stream (Ascend guide section 3.1, multi-stream
+ * overlap): when on, a bf16 layer with a shared expert runs the shared
+ * expert's two GEMMs, for calls with T > 16, on a stream the handle creates
+ * (on the first call of this function with on != 0), forked from the call's
+ * stream after routing and joined back before the finalize; the call still
+ * completes in `stream` order and its result is bit-identical. Default off:
+ * on one GPU the routed and shared GEMMs both fill every SM, so running them
+ * concurrently does not shorten the layer (it only overlaps the gather).
+ * Returns MOE_ERR_CUDA if the stream or its events cannot be created.
+ */
+moe_status moe_set_shared_stream(moe_handle *h, int32_t on);
 
 /*
  * Synchronise the stream of the handle's last call and read its device error

@@ -72,6 +72,7 @@ def load() -> ctypes.CDLL:
         "moe_launch_count": (ctypes.c_int64, [p]),
         "moe_route_noalloc": (st, [p, p, p, i32, i32, i32, i32, i32, p, p, p, p, p]),
         "moe_set_accumulate": (st, [p, i32]),
+        "moe_set_shared_stream": (st, [p, i32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -228,6 +229,10 @@ class MoELayer:
     def set_accumulate(self, on: bool):
         """``moe_set_accumulate``: later forwards add into ``out`` (y += layer(x))."""
         self._check(self._lib.moe_set_accumulate(self._h, 1 if on else 0))
+
+    def set_shared_stream(self, on: bool):
+        """``moe_set_shared_stream``: the shared expert's GEMMs on a second stream."""
+        self._check(self._lib.moe_set_shared_stream(self._h, 1 if on else 0))
 
     def sync(self):
         """``moe_sync``: wait for the last call and raise on a device-side error."""

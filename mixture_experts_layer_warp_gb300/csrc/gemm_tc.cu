@@ -91,9 +91,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         c.abort = 0;
         ptx::fence_mbar_init();
     }
-    for (int i = threadIdx.x; i <= a.G; i += kThreads) {
-        c.seg[i] = a.seg[i];
-        c.tiles[i] = a.tiles[i];
+    if (a.seg != nullptr) {
+        for (int i = threadIdx.x; i <= a.G; i += kThreads) {
+            c.seg[i] = a.seg[i];
+            c.tiles[i] = a.tiles[i];
+        }
+    } else if (threadIdx.x == 0) {  // one dense segment (the shared expert over all T rows)
+        c.seg[0] = 0;
+        c.seg[1] = a.dense_rows;
+        c.tiles[0] = 0;
+        c.tiles[1] = (a.dense_rows + kTcBM - 1) / kTcBM;
     }
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tmap(&tmA);

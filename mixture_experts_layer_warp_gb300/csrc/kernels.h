@@ -128,8 +128,8 @@ constexpr int kTcBK = 64;    // K per stage: 64 bf16 = one 128-byte swizzled row
 //   SwiGLU form (GEMM1): out[r][m*I + n] = silu(A_r . B_m[g][n]) * (A_r . B_m[g][I + n])
 //   Plain form (GEMM2):  out[r][n] = sum_m A_r[m*I:(m+1)*I] . B_m[g][n]
 struct TcGemmArgs {
-    const int32_t* seg;       // [G+1] row offsets
-    const int32_t* tiles;     // [G+1] prefix of ceil(rows/kTcBM)
+    const int32_t* seg;       // [G+1] row offsets, or null: one dense segment [0, dense_rows) (G = 1)
+    const int32_t* tiles;     // [G+1] prefix of ceil(rows/kTcBM) (unused when seg is null)
     int G;
     int n_micro;
     int k_blocks;             // kTcBK-blocks of K per micro
@@ -143,6 +143,7 @@ struct TcGemmArgs {
     int max_tiles;            // upper bound used for the grid
     int* err;
     uint64_t limit_ns;
+    int dense_rows;           // rows of the dense segment when seg is null
 };
 // tmA: A [rows][K] bf16, box {64, 128}; tmB[m]: B_m [G*b_rows][K] bf16, box {64, 128}.
 cudaError_t launch_tc_gemm_swiglu(const TcGemmArgs& a, const CUtensorMap& tmA, const CUtensorMap* tmB,

@@ -52,6 +52,12 @@ struct moe_handle {
     void* sbuf = nullptr;
     void* x_stage = nullptr;
     void* y_stage = nullptr;
+    // moe_set_shared_stream: bf16 layers with a shared expert and more than
+    // kSmallTokens tokens run the shared expert's GEMMs on this stream
+    bool shared_stream = false;
+    cudaStream_t side = nullptr;
+    cudaEvent_t ev_fork = nullptr;
+    cudaEvent_t ev_join = nullptr;
     // diagnostics
     int64_t launches = 0;
     bool accumulate = false;
@@ -177,8 +183,35 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
     const int64_t R = (int64_t)T * k;
     cudaError_t e;
     const bool small_bf16 = c.dtype == MOE_BF16 && T <= kSmallTokens;
+    // the shared expert depends on x only: fork it onto the side stream once
+    // routing is done (its persistent CTAs would otherwise hold the SMs the
+    // routing kernels need), so it overlaps the gather; join before the finalize
+    const bool fork = h->shared_stream && c.dtype == MOE_BF16 && !small_bf16 && Is > 0 && T > 0;
     moe_status st = run_routing(h, x, router_w, bias, T, nullptr, s);
     if (st != MOE_OK) return st;
+    if (fork && ((e = cudaEventRecord(h->ev_fork, s)) != cudaSuccess ||
+                 (e = cudaStreamWaitEvent(h->side, h->ev_fork, 0)) != cudaSuccess))
+        return cuda_err(h, e, "shared-expert fork");
+    if (fork) {
+        const cudaStream_t ss = h->side;
+        CUtensorMap sA, sB[kMaxMicro];
+        const int stiles = (T + kTcBM - 1) / kTcBM;
+        if (!encode_2d(&sA, x, H, T, (uint64_t)H * 2) || !encode_2d(&sB[0], sw13, H, 2 * (uint64_t)Is, (uint64_t)H * 2))
+            return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (shared GEMM1)");
+        TcGemmArgs s1{nullptr, nullptr, 1, 1, H / kTcBK, Is / 128, 2 * Is, Is, 0,
+                      h->hs, (int64_t)Is, 0, stiles * (Is / 128), h->err, h->limit_ns, T};
+        if ((e = timed(h, kSlotSharedGemm1, ss, [&] { return launch_tc_gemm_swiglu(s1, sA, sB, h->num_sms, ss); })) !=
+            cudaSuccess)
+            return cuda_err(h, e, "shared GEMM1 launch");
+        if (!encode_2d(&sA, h->hs, Is, T, (uint64_t)Is * 2) || !encode_2d(&sB[0], sw2, Is, H, (uint64_t)Is * 2))
+            return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (shared GEMM2)");
+        TcGemmArgs s2{nullptr, nullptr, 1, 1, Is / kTcBK, H / 256, H, 0, Is,
+                      h->sbuf, (int64_t)H, 0, stiles * (H / 256), h->err, h->limit_ns, T};
+        if ((e = timed(h, kSlotSharedGemm2, ss, [&] { return launch_tc_gemm_down(s2, sA, sB, h->num_sms, ss); })) !=
+            cudaSuccess)
+            return cuda_err(h, e, "shared GEMM2 launch");
+        if ((e = cudaEventRecord(h->ev_join, ss)) != cudaSuccess) return cuda_err(h, e, "shared-expert join");
+    }
 
     if (!small_bf16) {  // small bf16 batches gather inside the fused GEMM launch
         GatherArgs ga{x, h->perm, (int)R, k, (uint32_t)(H * h->esz), h->xp, h->err, h->limit_ns, h->num_sms};
@@ -255,7 +288,7 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
                       h->obuf, (int64_t)H, 0, routed_tiles_tc * (H / 256), h->err, h->limit_ns};
         if ((e = timed(h, kSlotGemm2, s, [&] { return launch_tc_gemm_down(g2, tmA, tmB, h->num_sms, s); })) != cudaSuccess)
             return cuda_err(h, e, "GEMM2 launch");
-        if (Is > 0) {
+        if (Is > 0 && !fork) {
             const int stiles = (T + kTcBM - 1) / kTcBM;
             if (!encode_2d(&tmA, x, H, T, (uint64_t)H * 2) || !encode_2d(&tmB[0], sw13, H, 2 * (uint64_t)Is, (uint64_t)H * 2))
                 return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (shared GEMM1)");
@@ -330,6 +363,7 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
             if ((e = timed(h, kSlotSharedGemm2, s, [&] { return launch_simt_gemm_down(s2, s); })) != cudaSuccess) return cuda_err(h, e, "f32 shared GEMM2");
         }
     }
+    if (fork && (e = cudaStreamWaitEvent(s, h->ev_join, 0)) != cudaSuccess) return cuda_err(h, e, "shared-expert join");
     if (!small_bf16) {  // small bf16 batches finalize inside the fused GEMM launch
         FinalizeArgs fa{h->obuf, h->inv, h->topw, Is > 0 ? h->sbuf : nullptr, T, k, H, c.dtype == MOE_BF16, y,
                         h->accumulate};
@@ -447,6 +481,9 @@ void moe_destroy(moe_handle* h) {
     if (h == nullptr) return;
     cudaDeviceSynchronize();
     for (cudaEvent_t ev : h->prof_ev) cudaEventDestroy(ev);
+    if (h->ev_fork != nullptr) cudaEventDestroy(h->ev_fork);
+    if (h->ev_join != nullptr) cudaEventDestroy(h->ev_join);
+    if (h->side != nullptr) cudaStreamDestroy(h->side);
     cudaFree(h->ws);
     delete h;
 }
@@ -607,6 +644,20 @@ int64_t moe_launch_count(const moe_handle* h) { return h ? h->launches : 0; }
 moe_status moe_set_accumulate(moe_handle* h, int32_t on) {
     if (h == nullptr) return MOE_ERR_INVALID_ARG;
     h->accumulate = on != 0;
+    return MOE_OK;
+}
+
+moe_status moe_set_shared_stream(moe_handle* h, int32_t on) {
+    if (h == nullptr) return MOE_ERR_INVALID_ARG;
+    if (on && h->side == nullptr) {
+        if (cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) != cudaSuccess) {
+            cudaGetLastError();
+            return set_err(h, MOE_ERR_CUDA, "could not create the shared-expert stream");
+        }
+    }
+    h->shared_stream = on != 0;
     return MOE_OK;
 }
 

@@ -189,3 +189,23 @@ def test_back_to_back_small_batches_reuse_the_workspace():
         ref = _forward(fresh, d)
         fresh.close()
         assert torch.equal(ys[i], ref) and torch.equal(ys[i + 3], ref)
+
+
+@pytest.mark.parametrize("wl", [W.Workload("side_17", 17, 512, 8, 2, 256, 2, shared_inter=128),
+                                W.Workload("side_257", 257, 256, 16, 4, 128, 2, shared_inter=256)],
+                         ids=lambda w: w.name)
+def test_shared_expert_on_a_second_stream_is_bit_identical(wl):
+    """moe_set_shared_stream: the shared expert's GEMMs forked onto the handle's
+    stream and joined before the finalize give the same bits as the default
+    single-stream order, also for back-to-back calls on one handle."""
+    inps = [parity.to_device(W.make_inputs(wl, seed=s)) for s in (41, 42)]
+    plain = _layer(wl)
+    ref = [_forward(plain, d).clone() for d in inps]
+    plain.close()
+    side = _layer(wl)
+    side.set_shared_stream(True)
+    ys = [_forward(side, d).clone() for d in inps + inps]
+    side.close()
+    for i in range(2):
+        assert torch.equal(ys[i], ref[i]) and torch.equal(ys[i + 2], ref[i])
+    _check(wl, W.make_inputs(wl, seed=41), ys[0])
