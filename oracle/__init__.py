@@ -12,6 +12,8 @@ from .oracle import (  # noqa: F401
     forward_tokens,
     layer,
     logits,
+    mx_dequant,
+    mx_quantize,
     num_threads,
     permute,
     route,

@@ -33,8 +33,15 @@
  *   - offsets has E+1 entries, offsets[E] = T*k;
  *   - the shared expert's output is added unscaled.
  *
- * All floating-point arithmetic is fp64. Inputs are read as fp32 or as bf16 bit
- * patterns (uint16) and widened exactly to fp64.
+ * All floating-point arithmetic is fp64. Inputs are read as fp32, as bf16 bit
+ * patterns (uint16) or as fp64, and widened exactly to fp64.
+ *
+ * Quantised expert weights (the block-scaled FP8 variant of the experts; the
+ * pages name no format, the reading taken is the OCP Microscaling (MX) MXFP8
+ * format): codes are FP8 E4M3 (OCP E4M3FN: 4 exponent bits, bias 7, 3 mantissa
+ * bits, no infinities, largest 448), one shared power-of-two scale (E8M0 code
+ * S, value 2^(S-127)) per block of 32 consecutive elements along K; the
+ * weights the layer computes with are the f16 roundings of code * scale.
  */
 #include <math.h>
 #include <stdint.h>
@@ -46,10 +53,13 @@
 
 #define ORC_F32 0
 #define ORC_BF16 1
+#define ORC_F64 2
 
 /* Exact widening of one stored element to fp64. */
 static double elem(const void *p, int dtype, int64_t i)
 {
+    if (dtype == ORC_F64)
+        return ((const double *)p)[i];
     if (dtype == ORC_F32)
         return (double)((const float *)p)[i];
     uint32_t bits = (uint32_t)((const uint16_t *)p)[i] << 16;
@@ -58,7 +68,7 @@ static double elem(const void *p, int dtype, int64_t i)
     return (double)f;
 }
 
-static size_t elem_size(int dtype) { return dtype == ORC_F32 ? 4u : 2u; }
+static size_t elem_size(int dtype) { return dtype == ORC_F64 ? 8u : (dtype == ORC_F32 ? 4u : 2u); }
 
 /* Pointer to element i of a typed buffer (used to address expert blocks). */
 static const void *elem_ptr(const void *p, int dtype, int64_t i)
@@ -254,12 +264,12 @@ static void swiglu_expert_acc(const double *xv, int64_t H, int64_t I,
  * ids/w are the routing of ALL tokens ([T][k]); tokens[] selects which rows to
  * evaluate; y is [n_tokens][H].
  */
-int orc_forward_tokens(const void *x, int dtype, int64_t H, int64_t E, int64_t k,
-                       int64_t I, int64_t n_micro,
-                       const void *const *w13, const void *const *w2,
-                       const void *sw13, const void *sw2, int64_t Is,
-                       const int32_t *ids, const double *w,
-                       const int64_t *tokens, int64_t n_tokens, double *y)
+int orc_forward_tokens_typed(const void *x, int dtype, int w_dtype, int s_dtype, int64_t H, int64_t E,
+                             int64_t k, int64_t I, int64_t n_micro,
+                             const void *const *w13, const void *const *w2,
+                             const void *sw13, const void *sw2, int64_t Is,
+                             const int32_t *ids, const double *w,
+                             const int64_t *tokens, int64_t n_tokens, double *y)
 {
     if (H <= 0 || E <= 0 || k <= 0 || I <= 0 || n_micro <= 0 || n_tokens < 0)
         return -1;
@@ -286,16 +296,28 @@ int orc_forward_tokens(const void *x, int dtype, int64_t H, int64_t E, int64_t k
             int64_t e = ids[t * k + j];
             for (int64_t m = 0; m < n_micro; ++m)
                 swiglu_expert_acc(xv, H, I,
-                                  elem_ptr(w13[m], dtype, e * 2 * I * H),
-                                  elem_ptr(w2[m], dtype, e * H * I),
-                                  dtype, w[t * k + j], acc, a);
+                                  elem_ptr(w13[m], w_dtype, e * 2 * I * H),
+                                  elem_ptr(w2[m], w_dtype, e * H * I),
+                                  w_dtype, w[t * k + j], acc, a);
         }
         if (sw13 && sw2 && Is > 0)
-            swiglu_expert_acc(xv, H, Is, sw13, sw2, dtype, 1.0, acc, a);
+            swiglu_expert_acc(xv, H, Is, sw13, sw2, s_dtype, 1.0, acc, a);
     }
     free(xbuf);
     free(abuf);
     return 0;
+}
+
+/* orc_forward_tokens_typed with the routed and shared weights in x's dtype. */
+int orc_forward_tokens(const void *x, int dtype, int64_t H, int64_t E, int64_t k,
+                       int64_t I, int64_t n_micro,
+                       const void *const *w13, const void *const *w2,
+                       const void *sw13, const void *sw2, int64_t Is,
+                       const int32_t *ids, const double *w,
+                       const int64_t *tokens, int64_t n_tokens, double *y)
+{
+    return orc_forward_tokens_typed(x, dtype, dtype, dtype, H, E, k, I, n_micro, w13, w2, sw13, sw2,
+                                    Is, ids, w, tokens, n_tokens, y);
 }
 
 /*
@@ -373,6 +395,140 @@ done:
     free(xbuf);
     free(abuf);
     return rc;
+}
+
+/*
+ * ---------------------------------------------------------------- MXFP8
+ * Value of an E4M3 code (OCP E4M3FN): sign, 4-bit exponent e (bias 7), 3-bit
+ * mantissa m; e == 0 is subnormal m * 2^-9; the code S.1111.111 is NaN (never
+ * produced by the quantiser below).
+ */
+static double e4m3_value(uint8_t c)
+{
+    int e = (c >> 3) & 0xF, m = c & 7;
+    double v = e == 0 ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, e - 7);
+    if (e == 15 && m == 7)
+        v = NAN;
+    return (c & 0x80) ? -v : v;
+}
+
+/*
+ * Magnitude code (0 .. 0x7E) of the E4M3 value nearest to u >= 0, ties to the
+ * even mantissa, saturating at 448: u is split into an exponent and a 3-bit
+ * mantissa (the subnormal range keeps the exponent of 2^-6) and the scaled
+ * mantissa is rounded half to even.
+ */
+static uint8_t e4m3_round_mag(double u)
+{
+    if (!(u < 448.0))
+        return 0x7E;
+    int e;
+    if (u < ldexp(1.0, -6)) {
+        e = -6;  /* subnormal: steps of 2^-9 */
+    } else {
+        int ex;
+        frexp(u, &ex);  /* u = f * 2^ex, f in [0.5, 1) */
+        e = ex - 1;
+    }
+    double scaled = ldexp(u, 3 - e);  /* u / 2^(e-3): the mantissa in units of 1/8 */
+    double q = nearbyint(scaled);     /* default rounding: to nearest, ties to even */
+    int64_t qi = (int64_t)q;
+    if (u < ldexp(1.0, -6))
+        return (uint8_t)qi;           /* 0..8; 8 is the normal 2^-6 (code 0x08) */
+    if (qi == 16) {                   /* mantissa overflowed: next binade */
+        qi = 8;
+        e += 1;
+    }
+    int code = ((e + 7) << 3) | (int)(qi - 8);
+    return code > 0x7E ? 0x7E : (uint8_t)code;
+}
+
+/*
+ * MXFP8 quantisation of w [groups][rows][cols] along cols, in blocks of 32
+ * (OCP Microscaling: shared exponent = floor(log2(max |v|)) - 8, 8 being the
+ * largest exponent of E4M3; codes = E4M3 of v / 2^shared, nearest, ties to
+ * even, saturating): codes [groups][rows][cols], scales [groups][cols/32][rows]
+ * as E8M0 codes S = shared + 127 (shared clamped to [-127, 127]; an all-zero
+ * block gets S = 127). The sign bit of a code is the sign bit of v.
+ */
+int orc_mx_quantize(const void *w, int dtype, int64_t groups, int64_t rows, int64_t cols,
+                    uint8_t *codes, uint8_t *scales)
+{
+    if (groups < 0 || rows < 0 || cols <= 0 || cols % 32 != 0)
+        return -1;
+    const int64_t nb = cols / 32;
+#pragma omp parallel for schedule(static)
+    for (int64_t gr = 0; gr < groups * rows; ++gr) {
+        const int64_t g = gr / rows, r = gr % rows;
+        for (int64_t b = 0; b < nb; ++b) {
+            const int64_t base = gr * cols + b * 32;
+            double amax = 0.0;
+            for (int i = 0; i < 32; ++i) {
+                double v = fabs(elem(w, dtype, base + i));
+                if (v > amax)
+                    amax = v;
+            }
+            int shared = 0;
+            if (amax > 0.0) {
+                int ex;
+                frexp(amax, &ex);
+                shared = (ex - 1) - 8;
+                if (shared < -127)
+                    shared = -127;
+                if (shared > 127)
+                    shared = 127;
+            }
+            scales[(g * nb + b) * rows + r] = (uint8_t)(shared + 127);
+            for (int i = 0; i < 32; ++i) {
+                double v = elem(w, dtype, base + i);
+                uint8_t mag = e4m3_round_mag(ldexp(fabs(v), -shared));
+                codes[base + i] = (uint8_t)(signbit(v) ? (0x80 | mag) : mag);
+            }
+        }
+    }
+    return 0;
+}
+
+/*
+ * IEEE binary16 rounding of v (nearest, ties to even; subnormals down to 2^-24;
+ * magnitudes from 65520 up round to infinity), returned as fp64.
+ */
+static double round_f16(double v)
+{
+    double a = fabs(v);
+    if (a == 0.0 || a != a)
+        return v;
+    int ex;
+    frexp(a, &ex);
+    int e = ex - 1;  /* a in [2^e, 2^(e+1)) */
+    if (e < -14)
+        e = -14;     /* subnormal range: fixed step 2^-24 */
+    double q = ldexp(nearbyint(ldexp(a, 10 - e)), e - 10);
+    if (q >= 65520.0 || q > 65504.0)
+        q = INFINITY;
+    return v < 0 ? -q : q;
+}
+
+/*
+ * The weights an MXFP8 layer computes with: f16 rounding of
+ * e4m3_value(code) * 2^(S - 127), for codes [groups][rows][cols] and scales
+ * [groups][cols/32][rows]; out [groups][rows][cols] fp64.
+ */
+int orc_mx_dequant(const uint8_t *codes, const uint8_t *scales, int64_t groups, int64_t rows,
+                   int64_t cols, double *out)
+{
+    if (groups < 0 || rows < 0 || cols <= 0 || cols % 32 != 0)
+        return -1;
+    const int64_t nb = cols / 32;
+#pragma omp parallel for schedule(static)
+    for (int64_t gr = 0; gr < groups * rows; ++gr) {
+        const int64_t g = gr / rows, r = gr % rows;
+        for (int64_t c = 0; c < cols; ++c) {
+            int S = scales[(g * nb + c / 32) * rows + r];
+            out[gr * cols + c] = round_f16(ldexp(e4m3_value(codes[gr * cols + c]), S - 127));
+        }
+    }
+    return 0;
 }
 
 /* Number of OpenMP threads the oracle uses (reported beside its timings). */

@@ -3,10 +3,12 @@
 TEST INFRASTRUCTURE. Only the tests, the smoke check and the benchmark's
 CPU-baseline leg load this module; the CUDA path never does.
 
-Arrays are numpy. Activations and weights are passed either as ``float32`` or
-as ``uint16`` bf16 bit patterns; the C side widens them exactly to fp64. Every
-function follows the steps of "HunyuanImage3 Hybrid Parallelism" section 6.1
-and the Ascend guide section 2.2, as documented in ``moe_oracle.c``.
+Arrays are numpy. Activations and weights are passed as ``float32``, as
+``uint16`` bf16 bit patterns or (weights) as ``float64``; the C side widens them
+exactly to fp64. Every function follows the steps of "HunyuanImage3 Hybrid
+Parallelism" section 6.1 and the Ascend guide section 2.2, as documented in
+``moe_oracle.c``; ``mx_quantize`` / ``mx_dequant`` define the block-scaled FP8
+(MXFP8) expert weights.
 """
 from __future__ import annotations
 
@@ -21,7 +23,7 @@ _SRC = os.path.join(_HERE, "moe_oracle.c")
 _SO = os.path.join(_HERE, "liboracle.so")
 _lib = None
 
-_F32, _BF16 = 0, 1
+_F32, _BF16, _F64 = 0, 1, 2
 _p = ctypes.c_void_p
 _i64 = ctypes.c_int64
 
@@ -45,12 +47,17 @@ def _bind(path: str):
     lib.orc_forward_tokens.argtypes = [
         _p, ctypes.c_int, _i64, _i64, _i64, _i64, _i64, _p, _p, _p, _p, _i64,
         _p, _p, _p, _i64, _p]
+    lib.orc_forward_tokens_typed.argtypes = [
+        _p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _i64, _i64, _i64, _i64, _i64, _p, _p, _p, _p,
+        _i64, _p, _p, _p, _i64, _p]
+    lib.orc_mx_quantize.argtypes = [_p, ctypes.c_int, _i64, _i64, _i64, _p, _p]
+    lib.orc_mx_dequant.argtypes = [_p, _p, _i64, _i64, _i64, _p]
     lib.orc_forward_permuted.argtypes = [
         _p, ctypes.c_int, _i64, _i64, _i64, _i64, _i64, _i64, _p, _p, _p, _p, _i64,
         _p, _p, _p, _p, _p]
     lib.orc_num_threads.argtypes = []
-    for fn in ("orc_logits", "orc_route", "orc_permute", "orc_forward_tokens",
-               "orc_forward_permuted", "orc_num_threads"):
+    for fn in ("orc_logits", "orc_route", "orc_permute", "orc_forward_tokens", "orc_forward_tokens_typed",
+               "orc_forward_permuted", "orc_num_threads", "orc_mx_quantize", "orc_mx_dequant"):
         getattr(lib, fn).restype = ctypes.c_int
     return lib
 
@@ -67,7 +74,9 @@ def _dtype_code(a: np.ndarray) -> int:
         return _F32
     if a.dtype == np.uint16:
         return _BF16
-    raise TypeError(f"oracle takes float32 or uint16 (bf16 bits), got {a.dtype}")
+    if a.dtype == np.float64:
+        return _F64
+    raise TypeError(f"oracle takes float32, uint16 (bf16 bits) or float64, got {a.dtype}")
 
 
 def _c(a: np.ndarray, dtype=None) -> np.ndarray:
@@ -136,11 +145,13 @@ def permute(ids: np.ndarray, num_experts: int, lib=None):
 
 
 def _weights(w13, w2, dt):
+    """Routed expert weights: x's dtype, or fp64 (e.g. dequantised MXFP8 weights)."""
     w13 = [_c(a) for a in w13]
     w2 = [_c(a) for a in w2]
+    wdt = _dtype_code(w13[0]) if w13 else dt
     for a in w13 + w2:
-        if _dtype_code(a) != dt:
-            raise TypeError("weights must share the activation dtype")
+        if _dtype_code(a) != wdt or wdt not in (dt, _F64):
+            raise TypeError("routed weights must all be in the activation dtype or all fp64")
     n_micro = len(w13)
     if len(w2) != n_micro or n_micro == 0:
         raise ValueError("w13 and w2 need one entry per micro-shard")
@@ -151,7 +162,7 @@ def _weights(w13, w2, dt):
             raise ValueError(f"bad expert shapes {a.shape} / {b.shape}")
     p13 = (ctypes.c_void_p * n_micro)(*[a.ctypes.data for a in w13])
     p2 = (ctypes.c_void_p * n_micro)(*[a.ctypes.data for a in w2])
-    return w13, w2, p13, p2, E, I, H, n_micro
+    return w13, w2, p13, p2, E, I, H, n_micro, wdt
 
 
 def _shared(sw13, sw2, H, dt):
@@ -174,7 +185,7 @@ def forward_tokens(x, ids, w, w13, w2, tokens=None, shared_w13=None, shared_w2=N
     x = _c(x)
     dt = _dtype_code(x)
     keep = _weights(w13, w2, dt)
-    _, _, p13, p2, E, I, H, n_micro = keep
+    _, _, p13, p2, E, I, H, n_micro, wdt = keep
     sw13, sw2, Is = _shared(shared_w13, shared_w2, H, dt)
     ids = _c(ids, np.int32)
     w = _c(w, np.float64)
@@ -183,8 +194,8 @@ def forward_tokens(x, ids, w, w13, w2, tokens=None, shared_w13=None, shared_w2=N
     if tok.size and (tok.min() < 0 or tok.max() >= T):
         raise IndexError("token index out of range")
     y = np.empty((tok.size, H), np.float64)
-    rc = (lib or _load()).orc_forward_tokens(
-        _ptr(x), dt, H, E, k, I, n_micro, p13, p2, _ptr(sw13), _ptr(sw2), Is,
+    rc = (lib or _load()).orc_forward_tokens_typed(
+        _ptr(x), dt, wdt, dt, H, E, k, I, n_micro, p13, p2, _ptr(sw13), _ptr(sw2), Is,
         _ptr(ids), _ptr(w), _ptr(tok), tok.size, _ptr(y))
     if rc:
         raise RuntimeError(f"orc_forward_tokens failed ({rc})")
@@ -197,7 +208,9 @@ def forward_permuted(x, w, offsets, perm, inv, w13, w2, shared_w13=None, shared_
     x = _c(x)
     dt = _dtype_code(x)
     keep = _weights(w13, w2, dt)
-    _, _, p13, p2, E, I, H, n_micro = keep
+    _, _, p13, p2, E, I, H, n_micro, wdt = keep
+    if wdt != dt:
+        raise TypeError("forward_permuted takes weights in the activation dtype")
     sw13, sw2, Is = _shared(shared_w13, shared_w2, H, dt)
     w = _c(w, np.float64)
     T, k = w.shape
@@ -224,3 +237,36 @@ def layer(x, wr, bias, w13, w2, k, shared_w13=None, shared_w2=None, tokens=None,
     counts, offsets, perm, inv = permute(ids, wr.shape[0], lib=lib)
     y = forward_tokens(x, ids, w, w13, w2, tokens, shared_w13, shared_w2, lib=lib)
     return dict(logits=lg, ids=ids, w=w, counts=counts, offsets=offsets, perm=perm, inv=inv, y=y)
+
+
+def mx_quantize(w: np.ndarray, lib=None):
+    """MXFP8 codes and scales of ``w`` ([G][R][C] or [R][C], float32 or bf16
+    bits), quantised along C in blocks of 32 (see ``orc_mx_quantize``).
+
+    Returns ``(codes uint8 [G][R][C], scales uint8 [G][C/32][R])`` (no G axis
+    for a 2-D input)."""
+    w = _c(w)
+    two_d = w.ndim == 2
+    w3 = w[None] if two_d else w
+    G, R, C = w3.shape
+    codes = np.empty((G, R, C), np.uint8)
+    scales = np.empty((G, C // 32, R), np.uint8)
+    rc = (lib or _load()).orc_mx_quantize(_ptr(w3), _dtype_code(w3), G, R, C, _ptr(codes), _ptr(scales))
+    if rc:
+        raise RuntimeError(f"orc_mx_quantize failed ({rc})")
+    return (codes[0], scales[0]) if two_d else (codes, scales)
+
+
+def mx_dequant(codes: np.ndarray, scales: np.ndarray, lib=None) -> np.ndarray:
+    """The fp64 weights an MXFP8 layer computes with (f16 of code * 2^(S-127))."""
+    two_d = codes.ndim == 2
+    c3 = _c(codes[None] if two_d else codes, np.uint8)
+    s3 = _c(scales[None] if two_d else scales, np.uint8)
+    G, R, C = c3.shape
+    if s3.shape != (G, C // 32, R):
+        raise ValueError(f"scales must be [G][C/32][R], got {s3.shape}")
+    out = np.empty((G, R, C), np.float64)
+    rc = (lib or _load()).orc_mx_dequant(_ptr(c3), _ptr(s3), G, R, C, _ptr(out))
+    if rc:
+        raise RuntimeError(f"orc_mx_dequant failed ({rc})")
+    return out[0] if two_d else out

@@ -279,4 +279,134 @@ def pin_bf16_widening(lib=None):
     assert np.array_equal(a["y"], b["y"])
 
 
+# ------------------------------------------------------------ MXFP8 weights
+# The block-scaled FP8 expert weights follow the OCP Microscaling (MX) MXFP8
+# format; the pins below hold the oracle's quantiser and dequantiser to torch's
+# float8_e4m3fn conversions and numpy's float16 rounding (library routines),
+# and to closed-form values of the shared-exponent rule.
+
+def _e4m3_torch_codes(v):
+    import torch
+    return torch.tensor(np.asarray(v, np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def _e4m3_torch_values():
+    import torch
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    return codes.view(torch.float8_e4m3fn).to(torch.float32).numpy().astype(np.float64)
+
+
+def _blocks_at_unit_scale(vals):
+    """Blocks of 32 whose first element (256) fixes the shared exponent at 0."""
+    vals = np.asarray(vals, np.float32)
+    n = -(-vals.size // 31)
+    w = np.zeros((n, 32), np.float32)
+    w[:, 0] = 256.0
+    w[:, 1:].flat[:vals.size] = vals
+    return w
+
+
+def pin_mx_e4m3_rounding_matches_torch(lib=None):
+    rng = np.random.default_rng(7)
+    rep = _e4m3_torch_values()[:127]                      # the non-negative finite values
+    mids = (rep[:-1] + rep[1:]) / 2                       # exact ties
+    vals = np.concatenate([rep, mids, rng.uniform(0, 448, 2000), rng.uniform(0, 2.0 ** -6, 500),
+                           np.array([448.0, 455.0, 463.9])]).astype(np.float32)
+    vals = np.concatenate([vals, -vals])
+    w = _blocks_at_unit_scale(vals)
+    codes, scales = oracle.mx_quantize(w, lib=lib)
+    assert (scales == 127).all(), "the leading 256 must fix the scale at 2^0"
+    got = codes[:, 1:].reshape(-1)[:vals.size]
+    assert np.array_equal(got, _e4m3_torch_codes(vals)), "E4M3 rounding differs from torch's"
+    sat = np.array([470.0, 500.0, 511.0, -480.0], np.float32)
+    c2, _ = oracle.mx_quantize(_blocks_at_unit_scale(sat), lib=lib)
+    assert list(c2[0, 1:5]) == [0x7E, 0x7E, 0x7E, 0xFE], "values above 448 must saturate"
+
+
+def pin_mx_e4m3_decode_matches_torch(lib=None):
+    codes = np.arange(256, dtype=np.uint8)
+    finite = codes[(codes & 0x7F) != 0x7F]
+    c = np.zeros((1, 1, 256), np.uint8)
+    c[0, 0, :finite.size] = finite
+    s = np.full((1, 8, 1), 127, np.uint8)
+    got = oracle.mx_dequant(c, s, lib=lib)[0, 0, :finite.size]
+    want = _e4m3_torch_values()[finite]
+    assert np.array_equal(got, want), "E4M3 decoding differs from torch's"
+
+
+def pin_mx_f16_rounding_matches_numpy(lib=None):
+    """Dequantised weights are the f16 (numpy float16: nearest-even, subnormals,
+    overflow to inf) of code * 2^(S-127), across scales that reach the f16
+    subnormal range, its ties and its overflow."""
+    sel = np.array([0x01, 0x03, 0x05, 0x08, 0x09, 0x0B, 0x33, 0x56, 0x7E, 0x81, 0xB3, 0xFE], np.uint8)
+    Ss = np.arange(96, 146)
+    c = np.zeros((1, 1, 32 * Ss.size), np.uint8)
+    s = np.zeros((1, Ss.size, 1), np.uint8)
+    for b, S in enumerate(Ss):
+        c[0, 0, 32 * b:32 * b + sel.size] = sel
+        s[0, b, 0] = S
+    got = oracle.mx_dequant(c, s, lib=lib)[0, 0]
+    val = _e4m3_torch_values()
+    for b, S in enumerate(Ss):
+        exact = val[sel] * 2.0 ** (int(S) - 127)
+        with np.errstate(over="ignore"):
+            want = exact.astype(np.float16).astype(np.float64)
+        g = got[32 * b:32 * b + sel.size]
+        assert np.array_equal(g, want), f"f16 rounding differs from numpy's at S={S}"
+
+
+def pin_mx_shared_exponent_rule(lib=None):
+    """Closed forms of the MX rule: shared = floor(log2 amax) - 8 (E4M3's largest
+    exponent), clamped to [-127, 127]; an all-zero block gets S = 127; scales are
+    laid out [G][C/32][R]."""
+    cases = [(1.0, 119), (0.75, 118), (448.0, 127), (511.0, 127), (512.0, 128), (2.0 ** -130, 0),
+             (3.0e38, 246)]
+    w = np.zeros((len(cases) + 1, 32), np.float32)
+    for i, (amax, _) in enumerate(cases):
+        w[i, 5] = -amax
+        w[i, 9] = amax / 4
+    codes, scales = oracle.mx_quantize(w, lib=lib)
+    for i, (amax, S) in enumerate(cases):
+        assert scales[0, i] == S, f"amax {amax}: S {scales[0, i]} != {S}"
+    assert scales[0, -1] == 127 and not codes[-1].any(), "an all-zero block: S = 127, codes 0"
+    # layout: a distinct amax at (g, r, block) must land in scales[g, block, r]
+    G, R, C = 2, 3, 96
+    w3 = np.full((G, R, C), 1.0, np.float32)
+    w3[1, 2, 64 + 7] = 8.0
+    _, s3 = oracle.mx_quantize(w3, lib=lib)
+    assert s3.shape == (G, C // 32, R)
+    assert s3[1, 2, 2] == 122 and (np.delete(s3.reshape(-1), (1 * 3 + 2) * 3 + 2) == 119).all()
+
+
+def pin_mx_roundtrip_error_bound(lib=None):
+    """|dequant(quant(w)) - w| is within half an E4M3 step of w (plus f16
+    rounding), except saturated elements, which become +-448 * 2^shared."""
+    rng = np.random.default_rng(3)
+    w = _f32(rng.normal(0, 0.02, (4, 64, 256))).astype(np.float32)
+    codes, scales = oracle.mx_quantize(w, lib=lib)
+    deq = oracle.mx_dequant(codes, scales, lib=lib)
+    shared = np.repeat(scales.astype(np.int64) - 127, 32, axis=1).transpose(0, 2, 1)  # [G][R][C]
+    unit = np.ldexp(1.0, shared)
+    u = np.abs(w.astype(np.float64)) / unit
+    sat = u >= 448.0
+    step = np.where(u < 2.0 ** -6, 2.0 ** -9, np.ldexp(1.0, np.floor(np.log2(np.maximum(u, 2.0 ** -6))).astype(int) - 3))
+    bound = (step / 2) * unit + np.abs(w) * 2.0 ** -11 + 2.0 ** -25
+    err = np.abs(deq - w.astype(np.float64))
+    assert (err[~sat] <= bound[~sat]).all(), "quantisation error beyond half a step"
+    assert np.array_equal(np.abs(deq[sat]), (448.0 * unit[sat]).astype(np.float16).astype(np.float64))
+
+
+def pin_forward_accepts_fp64_weights(lib=None):
+    """The fp64 weight path (used with dequantised weights) equals the fp32 path
+    on the same values."""
+    rng = np.random.default_rng(11)
+    x, wr, w13, w2, sw13, sw2 = _rand_layer(rng, 6, 64, 4, 2, 32, 2, Is=32)
+    lg = oracle.logits(x, wr, None, lib=lib)
+    ids, w = oracle.route(lg, 2, lib=lib)
+    y32 = oracle.forward_tokens(x, ids, w, w13, w2, None, sw13, sw2, lib=lib)
+    y64 = oracle.forward_tokens(x, ids, w, [a.astype(np.float64) for a in w13], [a.astype(np.float64) for a in w2],
+                                None, sw13, sw2, lib=lib)
+    assert np.array_equal(y32, y64)
+
+
 ALL_PINS = [v for k_, v in sorted(globals().items()) if k_.startswith("pin_")]

@@ -31,9 +31,15 @@ MUTANTS = [
     ("one_micro_only", "for (int64_t m = 0; m < n_micro; ++m)\n                swiglu_expert_acc(xv,",
      "for (int64_t m = 0; m < 1; ++m)\n                swiglu_expert_acc(xv,"),
     ("gather_wrong_token", "int64_t t = perm[i] / k;", "int64_t t = perm[i] % (k + 1);"),
-    ("shared_scaled", "swiglu_expert_acc(xv, H, Is, sw13, sw2, dtype, 1.0, acc, a);\n    }\n    free(xbuf);",
-     "swiglu_expert_acc(xv, H, Is, sw13, sw2, dtype, 0.5, acc, a);\n    }\n    free(xbuf);"),
+    ("shared_scaled", "swiglu_expert_acc(xv, H, Is, sw13, sw2, s_dtype, 1.0, acc, a);\n    }\n    free(xbuf);",
+     "swiglu_expert_acc(xv, H, Is, sw13, sw2, s_dtype, 0.5, acc, a);\n    }\n    free(xbuf);"),
     ("perm_holds_token", "perm[fill[ids[r]]++] = (int32_t)r;", "perm[fill[ids[r]]++] = (int32_t)(r / k);"),
+    ("mx_scale_from_ceil", "shared = (ex - 1) - 8;", "shared = ex - 8;"),
+    ("mx_ties_away_from_zero", "double q = nearbyint(scaled);", "double q = round(scaled);"),
+    ("mx_scale_layout_row_major", "scales[(g * nb + b) * rows + r] = (uint8_t)(shared + 127);",
+     "scales[(g * rows + r) * nb + b] = (uint8_t)(shared + 127);"),
+    ("f16_flush_subnormals", "    if (e < -14)\n        e = -14;", "    if (e < -14)\n        return 0.0;"),
+    ("fp64_weights_read_as_shared_dtype", "w_dtype, w[t * k + j], acc, a);", "dtype, w[t * k + j], acc, a);"),
 ]
 
 
