@@ -248,12 +248,13 @@ def config_of(wl):
                   f"{POOL} seeded batches"}
 
 
-def roofline_of(wl, prof, ids_pool, steps, peaks, sha):
+def roofline_of(wl, prof, ids_pool, steps, peaks, sha, mxfp8=False):
     """Roofline of the kernel with the largest share of the timed region."""
     dom, (ms, n) = max(prof.items(), key=lambda kv: kv[1][0])
     per_launch_s = ms / n / 1e3
     R = wl.T * wl.k
     esz = 4 if wl.dtype == "f32" else 2
+    wsz = (1 + 1 / 32) if mxfp8 else esz  # bytes per expert weight (MXFP8: code + a 32nd of a scale)
     # touched experts per step, averaged over the batches the timed steps used
     touched = statistics.mean(len(np.unique(ids_pool[i % len(ids_pool)])) for i in range(steps))
     I, H, M = wl.I, wl.H, wl.n_micro
@@ -261,7 +262,7 @@ def roofline_of(wl, prof, ids_pool, steps, peaks, sha):
     if wl.name == "decode":
         bound, unit, peak = "hbm", "GB/s", peaks["hbm"]
         algo = {
-            "gemm1_swiglu": (touched * 3 * I * H * esz * M + 3 * R * H * esz + 2 * R * M * I * esz + wl.T * H * esz)
+            "gemm1_swiglu": (touched * 3 * I * H * wsz * M + 3 * R * H * esz + 2 * R * M * I * esz + wl.T * H * esz)
             if fused
             else (touched * 2 * I * H * esz * M + R * H * esz + R * M * I * esz),
             "gemm2_down": touched * H * I * esz * M + R * M * I * esz + R * H * esz,
@@ -276,7 +277,7 @@ def roofline_of(wl, prof, ids_pool, steps, peaks, sha):
                 "shared_gemm1": 4 * wl.T * H * wl.shared_inter,
                 "shared_gemm2": 2 * wl.T * H * wl.shared_inter}.get(dom)
         achieved = algo / per_launch_s / 1e12 if algo else None
-    traffic = recorded_traffic(wl.name, dom, sha)
+    traffic = None if mxfp8 else recorded_traffic(wl.name, dom, sha)
     return {"kernel": dom + ("+gemm2_down+finalize (one launch)" if fused and dom == "gemm1_swiglu" else ""),
             "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
             "frac": (achieved / peak) if achieved else None, "traffic": traffic,
@@ -338,9 +339,16 @@ def run_ours(args, wl, world, rank, local):
         layer.set_shared_stream(True)
     y = torch.empty((wl.T, wl.H), dtype=wl.torch_dtype, device="cuda")
     args_w = (inp["router_w"], inp["router_bias"], inp["w13"], inp["w2"], inp["shared_w13"], inp["shared_w2"])
+    mx = args.weights == "mxfp8"
+    if mx:  # quantised once, outside every timed region (as weights are at load time)
+        args_w = (inp["router_w"], inp["router_bias"], [binding.quantize_mxfp8(t) for t in inp["w13"]],
+                  [binding.quantize_mxfp8(t) for t in inp["w2"]], inp["shared_w13"], inp["shared_w2"])
 
     def step(i):
-        layer.forward(pool[i % POOL], *args_w, out=y)
+        if mx:
+            layer.forward_mxfp8(pool[i % POOL], *args_w, out=y)
+        else:
+            layer.forward(pool[i % POOL], *args_w, out=y)
 
     ids_pool = [layer.route(x, inp["router_w"], inp["router_bias"])["ids"].cpu().numpy() for x in pool]
     stream = torch.cuda.current_stream()
@@ -381,19 +389,30 @@ def run_ours(args, wl, world, rank, local):
     layer.sync()
     shift = args.warmup % POOL
     ids_timed = ids_pool[shift:] + ids_pool[:shift]
-    roof = roofline_of(wl, prof, ids_timed, args.steps, peaks, src_sha())
+    roof = roofline_of(wl, prof, ids_timed, args.steps, peaks, src_sha(), mxfp8=mx)
 
     # end to end through the C ABI with host buffers (pinned), copies included
     host_pool = [x.cpu().pin_memory() for x in pool]
     y_host = torch.empty((wl.T, wl.H), dtype=wl.torch_dtype).pin_memory()
     e2e_steps = max(3, min(args.steps, 50))
+    x_dev = torch.empty_like(pool[0])
+
+    def e2e_step(i):
+        if mx:  # no host entry point for MXFP8: pinned copies around the device call
+            x_dev.copy_(host_pool[i % POOL], non_blocking=True)
+            layer.forward_mxfp8(x_dev, *args_w, out=y)
+            y_host.copy_(y, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+        else:
+            layer.forward_host(host_pool[i % POOL], *args_w, out_host=y_host)
+
     for i in range(2):
-        layer.forward_host(host_pool[i % POOL], *args_w, out_host=y_host)
+        e2e_step(i)
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for i in range(e2e_steps):
-        layer.forward_host(host_pool[i % POOL], *args_w, out_host=y_host)
+        e2e_step(i)
     _, e2e_value = job_throughput(world, wl.T, e2e_steps, (time.perf_counter() - t0) * 1e3)
     esz = 4 if wl.dtype == "f32" else 2
     e2e = {"value": e2e_value, "unit": "tokens/s",
@@ -418,8 +437,9 @@ def run_ours(args, wl, world, rank, local):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
-        "config": dict(config_of(wl), **({"shared_stream": True} if args.shared_stream else {})),
+        "vs_baseline": None, "dtype": "f16 (mxfp8 expert weights)" if mx else wl.dtype, "data": "synthetic",
+        "config": dict(config_of(wl), **({"shared_stream": True} if args.shared_stream else {}),
+                       **({"weights": "mxfp8 (E4M3 codes, E8M0 scale per 32 along K)"} if mx else {})),
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
         "kernels_ms_per_step": {k: v[0] / args.steps for k, v in prof.items()},
         "clocks": clk.summary(),
@@ -438,6 +458,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(W.WORKLOADS), default="decode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--weights", choices=["bf16", "mxfp8"], default="bf16",
+                    help="routed expert weights: the layer dtype, or MXFP8 (moe_forward_mxfp8, T <= 16)")
     ap.add_argument("--shared-stream", action="store_true",
                     help="run the shared expert's GEMMs on a second stream (moe_set_shared_stream)")
     ap.add_argument("--two-dispatch", action="store_true",

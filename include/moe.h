@@ -147,6 +147,46 @@ moe_status moe_forward_host(moe_handle *h, const void *x_host, const void *route
                             void *y_host, void *stream);
 
 /*
+ * Block-scaled FP8 expert weights (the pages list FP8 among the precision
+ * choices of the runtime: vflash architecture page, "Layered execution
+ * model"; they fix no format). The reading taken is the OCP Microscaling
+ * MXFP8 format: each expert weight is an FP8 E4M3 code (OCP E4M3FN, largest
+ * 448) with one E8M0 power-of-two scale per 32 consecutive elements along K;
+ * the layer computes with w = f16(code * 2^(S-127)) (nearest, ties to even).
+ * The routed experts' GEMMs then take f16 operands (the gathered token rows
+ * and h are rounded to f16; fp32 accumulation); the router, the shared expert
+ * (its weights stay bf16) and y keep the layer's bf16.
+ *
+ * Quantisation of bf16 weights w [groups][rows][cols] along cols (cols % 32
+ * == 0): codes [groups][rows][cols] uint8 and scales [groups][cols/32][rows]
+ * uint8. Per block: shared = floor(log2(max |v|)) - 8, clamped to
+ * [-127, 127] (0 for an all-zero block); code = E4M3 of v / 2^shared,
+ * nearest, ties to even, saturating at +-448; S = shared + 127. Device
+ * pointers; enqueued on `stream`; needs no handle. Returns MOE_ERR_INVALID_ARG
+ * for bad sizes or null pointers, MOE_ERR_CUDA on a launch failure.
+ * An expert's w13[m] [E][2I][H] is quantised with groups = E, rows = 2I,
+ * cols = H (scales [E][H/32][2I]); w2[m] [E][H][I] with rows = H, cols = I
+ * (scales [E][I/32][H]).
+ */
+moe_status moe_quantize_mxfp8(const void *w, int64_t groups, int32_t rows, int32_t cols,
+                              void *codes, void *scales, void *stream);
+
+/*
+ * moe_forward with MXFP8 routed-expert weights: w13_codes[m] / w13_scales[m]
+ * and w2_codes[m] / w2_scales[m] as produced by moe_quantize_mxfp8 (device
+ * pointers, 16-byte aligned). Supported for bf16 layers and batches of at
+ * most 16 tokens (the decode-sized calls whose time is the weight bytes);
+ * larger T returns MOE_ERR_UNSUPPORTED. Other arguments, ownership, the
+ * accumulate switch and errors as for moe_forward.
+ */
+moe_status moe_forward_mxfp8(moe_handle *h, const void *x, const void *router_w,
+                             const float *router_bias, const void *const *w13_codes,
+                             const void *const *w13_scales, const void *const *w2_codes,
+                             const void *const *w2_scales, int32_t n_micro, int32_t top_k,
+                             const void *shared_w13, const void *shared_w2, int32_t T,
+                             void *y, void *stream);
+
+/*
  * Output accumulation. With `on` non-zero, later moe_forward / moe_forward_host
  * calls on this handle add the layer's output into y (y += layer(x)): the
  * finalize reads y, adds it in fp32 and rounds once. It serves a residual add,

@@ -62,6 +62,8 @@ def load() -> ctypes.CDLL:
         "moe_route": (st, [p, p, p, p, i32, p, p, p, p, p, p]),
         "moe_forward": (st, [p, p, p, p, p, p, i32, i32, p, p, i32, p, p]),
         "moe_forward_host": (st, [p, p, p, p, p, p, i32, i32, p, p, i32, p, p]),
+        "moe_forward_mxfp8": (st, [p, p, p, p, p, p, p, p, i32, i32, p, p, i32, p, p]),
+        "moe_quantize_mxfp8": (st, [p, ctypes.c_int64, i32, i32, p, p, p]),
         "moe_sync": (st, [p]),
         "moe_last_error": (ctypes.c_char_p, [p]),
         "moe_status_string": (ctypes.c_char_p, [st]),
@@ -88,6 +90,23 @@ def _stream(device) -> int:
 
 def _ptr(t: torch.Tensor | None) -> int | None:
     return None if t is None else t.data_ptr()
+
+
+def quantize_mxfp8(w: torch.Tensor):
+    """``moe_quantize_mxfp8`` of a bf16 device tensor ``w`` [G, R, C] (or [R, C])
+    along C: returns ``(codes uint8 [G, R, C], scales uint8 [G, C/32, R])``."""
+    if w.dtype != torch.bfloat16 or not w.is_cuda or not w.is_contiguous() or w.dim() not in (2, 3):
+        raise ValueError("w must be a contiguous bf16 CUDA tensor of 2 or 3 dimensions")
+    w3 = w.unsqueeze(0) if w.dim() == 2 else w
+    G, R, C = w3.shape
+    if C % 32:
+        raise ValueError("the last dimension must be a multiple of 32")
+    codes = torch.empty((G, R, C), dtype=torch.uint8, device=w.device)
+    scales = torch.empty((G, C // 32, R), dtype=torch.uint8, device=w.device)
+    rc = load().moe_quantize_mxfp8(_ptr(w3), G, R, C, _ptr(codes), _ptr(scales), _stream(w.device))
+    if rc != 0:
+        raise MoEError(rc, "moe_quantize_mxfp8 failed")
+    return (codes[0], scales[0]) if w.dim() == 2 else (codes, scales)
 
 
 def selftest_wait_timeout(timeout_us: int = 1000) -> str:
@@ -223,6 +242,35 @@ class MoELayer:
         rc = self._lib.moe_forward_host(self._h, _ptr(x_host), _ptr(router_w), _ptr(router_bias), p13, p2,
                                         c.n_micro, c.top_k, _ptr(shared_w13), _ptr(shared_w2), T, _ptr(y),
                                         _stream(self.device))
+        self._check(rc)
+        return y
+
+    def forward_mxfp8(self, x, router_w, router_bias, w13_q, w2_q, shared_w13=None, shared_w2=None, out=None):
+        """``moe_forward_mxfp8``: routed experts in MXFP8 (``w13_q`` / ``w2_q``: per
+        micro, ``(codes, scales)`` pairs from ``quantize_mxfp8``); returns y [T, H]."""
+        c = self.cfg
+        T = x.shape[0]
+        self._tensor(x, "x", (T, c.hidden))
+        self._router(router_w, router_bias)
+        if len(w13_q) != c.n_micro or len(w2_q) != c.n_micro:
+            raise ValueError(f"expected {c.n_micro} micro-shards of w13 and w2")
+        E, H, I = c.num_experts, c.hidden, c.inter
+        for m in range(c.n_micro):
+            self._tensor(w13_q[m][0], f"w13 codes[{m}]", (E, 2 * I, H), torch.uint8)
+            self._tensor(w13_q[m][1], f"w13 scales[{m}]", (E, H // 32, 2 * I), torch.uint8)
+            self._tensor(w2_q[m][0], f"w2 codes[{m}]", (E, H, I), torch.uint8)
+            self._tensor(w2_q[m][1], f"w2 scales[{m}]", (E, I // 32, H), torch.uint8)
+        if c.shared_inter:
+            self._tensor(shared_w13, "shared_w13", (2 * c.shared_inter, H))
+            self._tensor(shared_w2, "shared_w2", (H, c.shared_inter))
+        arr = lambda ts: (ctypes.c_void_p * c.n_micro)(*[t.data_ptr() for t in ts])  # noqa: E731
+        y = torch.empty((T, H), dtype=self.dtype, device=self.device) if out is None else \
+            self._tensor(out, "out", (T, H))
+        rc = self._lib.moe_forward_mxfp8(self._h, _ptr(x), _ptr(router_w), _ptr(router_bias),
+                                         arr([q[0] for q in w13_q]), arr([q[1] for q in w13_q]),
+                                         arr([q[0] for q in w2_q]), arr([q[1] for q in w2_q]),
+                                         c.n_micro, c.top_k, _ptr(shared_w13), _ptr(shared_w2), T, _ptr(y),
+                                         _stream(self.device))
         self._check(rc)
         return y
 

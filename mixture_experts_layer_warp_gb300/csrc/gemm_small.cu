@@ -39,6 +39,7 @@
 // while the producer streams the current one, so neither global round trip
 // sits between two tiles of the weight stream. All waits are bounded.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "gemm_common.cuh"
 #include "kernels.h"
@@ -58,11 +59,28 @@ constexpr int kThreads = 256;
 constexpr int kGatherCtas = 128;               // kFused: CTAs that gather token rows
 constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kM, kTok);
 
+// MXFP8 expert weights (fused mode, moe_forward_mxfp8): each K-block's E4M3
+// codes (128 rows x 64 B) and E8M0 scales (2 per row) arrive through a deeper
+// ring beside the token rows, and four dequant warps (8..11) turn the codes
+// into f16 A tiles, code * 2^(S-127) rounded to f16, in one of kF8Dq 128B-
+// swizzled buffers; the routed GEMMs then run as f16 MMAs (the gathered token
+// rows and h are f16), with fp32 accumulators as before.
+constexpr int kF8Stages = 14;
+constexpr int kF8CodeBytes = kM * kTcBK;                          // 8 KB of codes
+constexpr int kF8SlotBytes = kF8CodeBytes + kM * (kTcBK / 32);    // + 256 B of scales
+constexpr int kF8Dq = 4;
+constexpr int kF8Threads = 384;
+constexpr int kF8SlotOff = kF8Stages * kBBytes;                   // after the token-row tiles
+constexpr int kF8DqOff = (kF8SlotOff + kF8Stages * kF8SlotBytes + 1023) / 1024 * 1024;
+constexpr int kF8CtlOff = kF8DqOff + kF8Dq * kABytes;
+constexpr uint32_t kIdescF16 = ptx::idesc_f16_f32(kM, kTok);
+constexpr int kMaxStages = kF8Stages > kStages ? kF8Stages : kStages;
+
 enum Mode { kSwiGLUOnly = 0, kDownOnly = 1, kFused = 2 };
 
 struct Ctl {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
+    uint64_t full[kMaxStages];
+    uint64_t empty[kMaxStages];
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t drain;
@@ -85,9 +103,14 @@ struct Ctl {
     uint64_t sq_empty;
     int sq_tile;
     int sq_rows;
+    // MXFP8: dequantised A tiles handed from the dequant warps to the MMA issuer
+    uint64_t dq_full[kF8Dq];
+    uint64_t dq_empty[kF8Dq];
 };
 
 constexpr int kSmemBytes = kStages * kStageBytes + (int)sizeof(Ctl) + 1024;
+constexpr int kF8SmemBytes = kF8CtlOff + (int)sizeof(Ctl) + 1024;
+static_assert(kF8SmemBytes <= 227 * 1024, "MXFP8 ring exceeds the shared memory of a CTA");
 
 struct SmallParams {
     TcGemmArgs g1;     // SwiGLU tiles (unused in kDownOnly)
@@ -107,8 +130,10 @@ struct SmallParams {
 struct SmallMaps {
     CUtensorMap x1;      // SwiGLU token rows [R][H], box {64, 16}
     CUtensorMap x2;      // down token rows (h) [R][M*I], box {64, 16}
-    CUtensorMap w1[kMaxMicro];  // w13[m] [E*2I][H], box {64, 64}
-    CUtensorMap w2[kMaxMicro];  // w2[m] [E*H][I], box {64, 128}
+    CUtensorMap w1[kMaxMicro];  // w13[m] [E*2I][H], box {64, 64} (MXFP8: uint8 codes)
+    CUtensorMap w2[kMaxMicro];  // w2[m] [E*H][I], box {64, 128} (MXFP8: uint8 codes)
+    CUtensorMap s1[kMaxMicro];  // MXFP8: w13[m] scales [E*H/32][2I] uint8, box {64, 2}
+    CUtensorMap s2[kMaxMicro];  // MXFP8: w2[m] scales [E*I/32][H] uint8, box {128, 2}
 };
 
 __device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
@@ -141,10 +166,23 @@ __device__ __forceinline__ int expert_of(const int* seg, int G, int pos) {
     return lo;
 }
 
+// Eight bf16 to eight f16 (nearest, ties to even).
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __half2 h = __floats2half2_rn(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+        w[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 // The gather xp[i] = x[perm[i] / k] (blog section 6.1: index_select once), as
 // the fused kernel's first phase, run by the four epilogue warps: CTA b <
 // kGatherCtas copies rows b, b + kGatherCtas, ... and counts each finished row
 // for its expert, so a SwiGLU tile only waits for the rows of its own expert.
+// With MXFP8 weights the rows are written as f16.
+template <bool F8>
 __device__ __forceinline__ void gather_rows(const Ctl& c, const SmallParams& p) {
     const int tid = threadIdx.x - 128;
     const int R = c.seg[p.g1.G];
@@ -162,7 +200,7 @@ __device__ __forceinline__ void gather_rows(const Ctl& c, const SmallParams& p) 
                 if (v0 + u * 128 < nvec) buf[u] = src[tok * nvec + v0 + u * 128];
 #pragma unroll
             for (int u = 0; u < kBatch; ++u)
-                if (v0 + u * 128 < nvec) dst[(int64_t)i * nvec + v0 + u * 128] = buf[u];
+                if (v0 + u * 128 < nvec) dst[(int64_t)i * nvec + v0 + u * 128] = F8 ? bf16x8_to_f16x8(buf[u]) : buf[u];
         }
         fence_proxy_async_global();  // the rows are read next by TMA (async proxy)
         epilogue_bar();
@@ -397,13 +435,52 @@ __device__ __forceinline__ int pop_scheduled(Ctl& c, uint32_t& phase, uint64_t l
     return t;
 }
 
-template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
+// Sixteen E4M3 codes (in K order) under the E8M0 scale S to sixteen f16: the
+// f16 rounding of code * 2^(S-127).
+// Fast form, for scales that are f16 numbers (2^-24 .. 2^15, dequant_in_f16
+// true): one f16 multiply per pair of exact operands, branch-free.
+__device__ __forceinline__ bool dequant_in_f16(int S) { return S >= 127 - 24 && S <= 127 + 15; }
+
+__device__ __forceinline__ void dequant16_f16(uint4 q, int S, uint32_t (&o)[8]) {
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    const int e = S - 127;
+    const unsigned short hb = e >= -14 ? (unsigned short)((e + 15) << 10) : (unsigned short)(1u << ((e + 24) & 15));
+    const __half2 sc = __halves2half2(__ushort_as_half(hb), __ushort_as_half(hb));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        uint32_t h = ptx::e4m3x2_to_f16x2((uint16_t)(w[i >> 1] >> (16 * (i & 1))));
+        const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&h), sc);
+        o[i] = *reinterpret_cast<const uint32_t*>(&r);
+    }
+}
+
+// Any scale: through fp32, where the product is exact, rounded once to f16.
+__device__ __forceinline__ void dequant16_f32(uint4 q, int S, uint32_t (&o)[8]) {
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    const int e = S - 127;
+    const float fs = e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(1u << (e + 149));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        uint32_t h = ptx::e4m3x2_to_f16x2((uint16_t)(w[i >> 1] >> (16 * (i & 1))));
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
+        const __half2 r = __floats2half2_rn(f.x * fs, f.y * fs);
+        o[i] = *reinterpret_cast<const uint32_t*>(&r);
+    }
+}
+
+template <int MODE, bool F8>
+__global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
     tc_small_kernel(const __grid_constant__ SmallMaps maps, const SmallParams p) {
+    static_assert(!F8 || MODE == kFused, "MXFP8 weights run in the fused mode only");
+    constexpr int kSt = F8 ? kF8Stages : kStages;
+    constexpr uint32_t kId = F8 ? kIdescF16 : kIdesc;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Ctl& c = *reinterpret_cast<Ctl*>(smem + kStages * kStageBytes);
+    Ctl& c = *reinterpret_cast<Ctl*>(smem + (F8 ? kF8CtlOff : kStages * kStageBytes));
+    // stage s: the A tile (bf16 weights, or MXFP8 codes + scales) and the token-row B tile
+    auto stage_a = [&](int st) { return smem + (F8 ? kF8SlotOff + st * kF8SlotBytes : st * kStageBytes); };
+    auto stage_b = [&](int st) { return smem + (F8 ? st * kBBytes : st * kStageBytes + kABytes); };
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const TcGemmArgs& a0 = MODE == kDownOnly ? p.g2 : p.g1;  // seg, tiles, G, err, limit
     // the next routing call's kernels may be placed as SMs free up; they wait
@@ -411,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (MODE == kFused) ptx::griddep_launch_dependents();
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kSt; ++s) {
             ptx::mbar_init(ptx::smem_u32(&c.full[s]), 1);
             ptx::mbar_init(ptx::smem_u32(&c.empty[s]), 1);
         }
@@ -419,10 +496,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(ptx::smem_u32(&c.tfull[b]), 1);
             ptx::mbar_init(ptx::smem_u32(&c.tempty[b]), 4);
         }
+        for (int b = 0; b < kF8Dq; ++b) {
+            ptx::mbar_init(ptx::smem_u32(&c.dq_full[b]), 4);  // the four dequant warps
+            ptx::mbar_init(ptx::smem_u32(&c.dq_empty[b]), 1);  // the MMA issuer's commit
+        }
         ptx::mbar_init(ptx::smem_u32(&c.drain), 1);
         for (int q = 0; q < 4; ++q) {
             ptx::mbar_init(ptx::smem_u32(&c.tq_full[q]), 1);
-            ptx::mbar_init(ptx::smem_u32(&c.tq_empty[q]), 5);  // MMA issuer + four epilogue warps
+            // MMA issuer + four epilogue warps (+ four dequant warps)
+            ptx::mbar_init(ptx::smem_u32(&c.tq_empty[q]), F8 ? 9 : 5);
         }
         ptx::mbar_init(ptx::smem_u32(&c.sq_full), 1);
         ptx::mbar_init(ptx::smem_u32(&c.sq_empty), 1);
@@ -431,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::fence_mbar_init();
     }
     if (MODE != kFused) {
-        for (int i = threadIdx.x; i <= a0.G; i += kThreads) {
+        for (int i = threadIdx.x; i <= a0.G; i += blockDim.x) {
             c.seg[i] = a0.seg[i];
             c.tiles[i] = a0.tiles[i];
         }
@@ -451,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // started early (programmatic dependent launch): nothing the router or
         // the shared expert's GEMMs write is read before this wait
         ptx::griddep_wait();
-        for (int i = threadIdx.x; i <= a0.G; i += kThreads) {
+        for (int i = threadIdx.x; i <= a0.G; i += blockDim.x) {
             c.seg[i] = a0.seg[i];
             c.tiles[i] = a0.tiles[i];
         }
@@ -467,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------ TMA producer
         const uint64_t wpol = ptx::policy_evict_first();  // each weight byte is read once per call
         int stage = 0;
-        uint32_t phase = 0, last_par[kStages];
+        uint32_t phase = 0, last_par[kSt];
         int issued = 0;
         bool ok = true;
         TileStream ts;
@@ -488,11 +570,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int* gcnt = (MODE == kFused && sw && p.gx != nullptr) ? p.done + 2 * p.g1.G + 1 + t.g : nullptr;
             bool rows_ready = gcnt == nullptr || rows_seen || ld_acquire(gcnt) >= t.row_end - t.row0;
             if (MODE == kFused) fence_proxy_async_global();  // the rows are read by TMA (async proxy)
-            int pend_stage[kStages], pend_kb[kStages], pending = 0;
+            int pend_stage[kSt], pend_kb[kSt], pending = 0;
             const int n_micro_k = sw ? 1 : g.n_micro;
             for (int mi = 0; ok && mi < n_micro_k; ++mi) {
                 const int m = sw ? t.m : mi;
                 const CUtensorMap* tw = sw ? &maps.w1[m] : &maps.w2[m];
+                const CUtensorMap* tsc = sw ? &maps.s1[m] : &maps.s2[m];  // MXFP8 scales
                 const CUtensorMap* tx = sw ? &maps.x1 : &maps.x2;
                 const int wrow = t.g * g.b_rows_per_group + t.nt * (sw ? 64 : kM);
                 for (int kb = 0; kb < g.k_blocks; ++kb) {
@@ -500,10 +583,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    const uint32_t sa = ptx::smem_u32(smem + stage * kStageBytes);
+                    const uint32_t sa = ptx::smem_u32(stage_a(stage));
                     const uint32_t fb = ptx::smem_u32(&c.full[stage]);
-                    ptx::mbar_arrive_expect_tx(fb, kStageBytes);
-                    if (sw) {
+                    ptx::mbar_arrive_expect_tx(fb, F8 ? kF8SlotBytes + kBBytes : kStageBytes);
+                    if (F8) {
+                        // codes: K-block kb of the tile's rows; scales: the two 32-blocks of kb
+                        const int srow = t.g * 2 * g.k_blocks + 2 * kb;
+                        if (sw) {
+                            ptx::tma_load_2d_hint(sa, tw, kb * kTcBK, wrow, fb, wpol);            // 64 gate rows
+                            ptx::tma_load_2d_hint(sa + kF8CodeBytes / 2, tw, kb * kTcBK, wrow + g.up_offset, fb,
+                                                  wpol);                                           // 64 up rows
+                            ptx::tma_load_2d(sa + kF8CodeBytes, tsc, t.nt * 64, srow, fb);
+                            ptx::tma_load_2d(sa + kF8CodeBytes + 128, tsc, g.up_offset + t.nt * 64, srow, fb);
+                        } else {
+                            ptx::tma_load_2d_hint(sa, tw, kb * kTcBK, wrow, fb, wpol);            // 128 rows
+                            ptx::tma_load_2d(sa + kF8CodeBytes, tsc, t.nt * kM, srow, fb);
+                        }
+                    } else if (sw) {
                         ptx::tma_load_2d_hint(sa, tw, kb * kTcBK, wrow, fb, wpol);            // 64 gate rows
                         ptx::tma_load_2d_hint(sa + kABytes / 2, tw, kb * kTcBK, wrow + g.up_offset, fb,
                                               wpol);                                           // 64 up rows
@@ -512,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const int kx = (sw ? 0 : m * g.a_micro_cols) + kb * kTcBK;
                     if (rows_ready) {
-                        ptx::tma_load_2d(sa + kABytes, tx, kx, t.row0, fb);                   // 16 token rows
+                        ptx::tma_load_2d(ptx::smem_u32(stage_b(stage)), tx, kx, t.row0, fb);  // 16 token rows
                     } else {
                         pend_stage[pending] = stage;
                         pend_kb[pending] = kx;
@@ -520,11 +616,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     last_par[stage] = phase;
                     ++issued;
-                    if (++stage == kStages) {
+                    if (++stage == kSt) {
                         stage = 0;
                         phase ^= 1u;
                     }
-                    if (!rows_ready && (pending == kStages || kb + 1 == g.k_blocks)) {
+                    if (!rows_ready && (pending == kSt || kb + 1 == g.k_blocks)) {
                         // every free stage holds weights: wait for the rows, then
                         // complete the pending stages with their token rows
                         const uint64_t t0 = ptx::globaltimer();
@@ -538,8 +634,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         fence_proxy_async_global();
                         for (int q = 0; q < pending; ++q) {  // completes the armed stages even on failure
-                            const uint32_t psa = ptx::smem_u32(smem + pend_stage[q] * kStageBytes);
-                            ptx::tma_load_2d(psa + kABytes, tx, pend_kb[q], t.row0,
+                            ptx::tma_load_2d(ptx::smem_u32(stage_b(pend_stage[q])), tx, pend_kb[q], t.row0,
                                              ptx::smem_u32(&c.full[pend_stage[q]]));
                         }
                         pending = 0;
@@ -557,7 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) {
             fail(c, a0.err);
-            const int n = issued < kStages ? issued : kStages;
+            const int n = issued < kSt ? issued : kSt;
             for (int s = 0; s < n; ++s) ptx::mbar_wait(ptx::smem_u32(&c.full[s]), last_par[s], a0.limit_ns, nullptr);
         }
     } else if (MODE == kFused && warp == 3 && lane == 0) {
@@ -565,8 +660,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         schedule_tiles(c, p, total);
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------ MMA issuer
-        int stage = 0;
-        uint32_t phase = 0;
+        int stage = 0, dq = 0;
+        uint32_t phase = 0, dq_phase = 0;
         bool ok = true;
         TileStream ts;
         ts.next_static = blockIdx.x;
@@ -588,22 +683,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int n_micro_k = sw ? 1 : g.n_micro;
             for (int mi = 0; ok && mi < n_micro_k; ++mi) {
                 for (int kb = 0; kb < g.k_blocks; ++kb) {
-                    if (!ptx::mbar_wait(ptx::smem_u32(&c.full[stage]), phase, g.limit_ns, &c.abort)) {
+                    if (!ptx::mbar_wait(ptx::smem_u32(&c.full[stage]), phase, g.limit_ns, &c.abort) ||
+                        (F8 && !ptx::mbar_wait(ptx::smem_u32(&c.dq_full[dq]), dq_phase, g.limit_ns, &c.abort))) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
-                    const uint32_t sa = ptx::smem_u32(smem + stage * kStageBytes);
-                    const uint64_t adesc = ptx::sw128_desc(sa), bdesc = ptx::sw128_desc(sa + kABytes);
+                    const uint32_t sa = F8 ? ptx::smem_u32(smem + kF8DqOff + dq * kABytes) : ptx::smem_u32(stage_a(stage));
+                    const uint64_t adesc = ptx::sw128_desc(sa), bdesc = ptx::sw128_desc(ptx::smem_u32(stage_b(stage)));
 #pragma unroll
                     for (int k = 0; k < kTcBK / 16; ++k) {
-                        ptx::mma_bf16(d, adesc + 2u * k, bdesc + 2u * k, kIdesc, accumulate);
+                        ptx::mma_bf16(d, adesc + 2u * k, bdesc + 2u * k, kId, accumulate);
                         accumulate = 1;
                     }
                     ptx::mma_commit(ptx::smem_u32(&c.empty[stage]));
-                    if (++stage == kStages) {
+                    if (++stage == kSt) {
                         stage = 0;
                         phase ^= 1u;
+                    }
+                    if (F8) {
+                        ptx::mma_commit(ptx::smem_u32(&c.dq_empty[dq]));
+                        if (++dq == kF8Dq) {
+                            dq = 0;
+                            dq_phase ^= 1u;
+                        }
                     }
                 }
             }
@@ -612,11 +715,92 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) fail(c, a0.err);
         ptx::mma_commit(ptx::smem_u32(&c.drain));
         ptx::mbar_wait(ptx::smem_u32(&c.drain), 0, a0.limit_ns, nullptr);
-    } else if (warp >= 4) {
+    } else if (F8 && warp >= 8) {
+        // ------------------------------------------------ MXFP8 dequant
+        // thread dt converts, per K-block, 16-code chunk dt % 4 of rows
+        // dt / 4 + 32 * pass into the swizzled f16 layout the MMA reads
+        const int dt = threadIdx.x - 256;
+        int stage = 0, dq = 0;
+        uint32_t phase = 0, dq_phase = 0;
+        bool ok = true;
+        TileStream ts;
+        ts.next_static = blockIdx.x;
+        for (;;) {
+            int tile = -1;
+            if (lane == 0) tile = consume_tile<MODE>(c, ts, total, a0.limit_ns);
+            tile = __shfl_sync(0xffffffffu, tile, 0);
+            if (tile < 0) break;
+            bool sw;
+            locate<MODE>(tile, c, p, sw);
+            const TcGemmArgs& g = sw ? p.g1 : p.g2;
+            const int nk = (sw ? 1 : g.n_micro) * g.k_blocks;
+            for (int i = 0; i < nk; ++i) {
+                bool got = ptx::mbar_wait(ptx::smem_u32(&c.full[stage]), phase, g.limit_ns, &c.abort) &&
+                           ptx::mbar_wait(ptx::smem_u32(&c.dq_empty[dq]), dq_phase ^ 1u, g.limit_ns, &c.abort);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+                const unsigned char* src = stage_a(stage);
+                unsigned char* dst = smem + kF8DqOff + dq * kABytes;
+                // all loads first (the stores below cannot move above them otherwise)
+                constexpr int kPasses = kM / 32;
+                const int ch = dt & 3;
+                uint4 codes[kPasses];
+                int scale[kPasses];
+#pragma unroll
+                for (int pass = 0; pass < kPasses; ++pass) {
+                    const int row = (dt >> 2) + 32 * pass;
+                    codes[pass] = *reinterpret_cast<const uint4*>(src + row * kTcBK + ch * 16);
+                    // scales: SwiGLU tiles [2][64] for the gate rows, then [2][64] for the up rows;
+                    // down tiles [2][128]
+                    scale[pass] = src[kF8CodeBytes + (sw ? (row >> 6) * 128 + (ch >> 1) * 64 + (row & 63)
+                                                          : (ch >> 1) * kM + row)];
+                }
+                // branch-free f16 form for every chunk; the rare chunks whose scale
+                // is not an f16 number are then redone through fp32
+                bool slow = false;
+#pragma unroll
+                for (int pass = 0; pass < kPasses; ++pass) {
+                    const int row = (dt >> 2) + 32 * pass;
+                    uint32_t o[8];
+                    dequant16_f16(codes[pass], scale[pass], o);
+                    slow |= !dequant_in_f16(scale[pass]);
+                    unsigned char* rp = dst + (row >> 3) * 1024 + (row & 7) * 128;
+                    *reinterpret_cast<uint4*>(rp + (((2 * ch) ^ (row & 7)) * 16)) = make_uint4(o[0], o[1], o[2], o[3]);
+                    *reinterpret_cast<uint4*>(rp + (((2 * ch + 1) ^ (row & 7)) * 16)) = make_uint4(o[4], o[5], o[6], o[7]);
+                }
+                if (slow) {
+                    for (int pass = 0; pass < kPasses; ++pass) {
+                        if (dequant_in_f16(scale[pass])) continue;
+                        const int row = (dt >> 2) + 32 * pass;
+                        uint32_t o[8];
+                        dequant16_f32(codes[pass], scale[pass], o);
+                        unsigned char* rp = dst + (row >> 3) * 1024 + (row & 7) * 128;
+                        *reinterpret_cast<uint4*>(rp + (((2 * ch) ^ (row & 7)) * 16)) = make_uint4(o[0], o[1], o[2], o[3]);
+                        *reinterpret_cast<uint4*>(rp + (((2 * ch + 1) ^ (row & 7)) * 16)) = make_uint4(o[4], o[5], o[6], o[7]);
+                    }
+                }
+                ptx::fence_proxy_async_smem();  // the tensor core reads these (async proxy)
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&c.dq_full[dq]));
+                if (++stage == kSt) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+                if (++dq == kF8Dq) {
+                    dq = 0;
+                    dq_phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+        }
+        if (!ok && lane == 0) fail(c, a0.err);
+    } else if (warp >= 4 && warp < 8) {
         // ------------------------------------------------ epilogue
         const int q = warp - 4;            // TMEM lanes 32q .. 32q+31 = weight rows
         const int r = q * 32 + lane;
-        if (MODE == kFused && p.gx != nullptr) gather_rows(c, p);
+        if (MODE == kFused && p.gx != nullptr) gather_rows<F8>(c, p);
         TileStream ts;
         ts.next_static = blockIdx.x;
         for (int local = 0;; ++local) {
@@ -660,7 +844,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int64_t col = (int64_t)t.m * g.out_micro_cols + t.nt * 64 + r;
                     for (int j = 0; j < cnt; ++j) {
                         const float h = silu(__uint_as_float(v[j])) * c.up[r][j];
-                        out[(int64_t)(t.row0 + j) * g.out_ld + col] = __float2bfloat16_rn(h);
+                        if (F8)  // the down tiles' B operand is f16 when the weights are MXFP8
+                            reinterpret_cast<__half*>(out)[(int64_t)(t.row0 + j) * g.out_ld + col] = __float2half_rn(h);
+                        else
+                            out[(int64_t)(t.row0 + j) * g.out_ld + col] = __float2bfloat16_rn(h);
                     }
                     if (MODE == kFused) fence_proxy_async_global();
                 }
@@ -694,13 +881,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int MODE>
+template <int MODE, bool F8 = false>
 cudaError_t launch_small(const SmallMaps& maps, const SmallParams& p, int max_tiles, int num_sms, cudaStream_t s) {
     if (max_tiles <= 0) return cudaSuccess;
+    constexpr int smem = F8 ? kF8SmemBytes : kSmemBytes;
+    constexpr int threads = F8 ? kF8Threads : kThreads;
     static bool configured = false;
     if (!configured) {
         cudaError_t e =
-            cudaFuncSetAttribute(tc_small_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+            cudaFuncSetAttribute(tc_small_kernel<MODE, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         configured = true;
     }
@@ -710,17 +899,17 @@ cudaError_t launch_small(const SmallMaps& maps, const SmallParams& p, int max_ti
         // kernel waits for its results (griddep_wait) after its own set-up
         cudaLaunchConfig_t cfg{};
         cfg.gridDim = dim3(grid);
-        cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = kSmemBytes;
+        cfg.blockDim = dim3(threads);
+        cfg.dynamicSmemBytes = smem;
         cfg.stream = s;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, tc_small_kernel<MODE>, maps, p);
+        return cudaLaunchKernelEx(&cfg, tc_small_kernel<MODE, F8>, maps, p);
     }
-    tc_small_kernel<MODE><<<grid, kThreads, kSmemBytes, s>>>(maps, p);
+    tc_small_kernel<MODE, F8><<<grid, threads, smem, s>>>(maps, p);
     return cudaGetLastError();
 }
 
@@ -741,7 +930,7 @@ void fill_maps(SmallMaps& m, const CUtensorMap& x, const CUtensorMap* w, int n_m
 
 cudaError_t launch_tc_small_swiglu(const TcGemmArgs& a, const CUtensorMap& tmX, const CUtensorMap* tmW,
                                    int num_sms, cudaStream_t s) {
-    SmallMaps maps;
+    SmallMaps maps{};
     fill_maps(maps, tmX, tmW, a.n_micro, true);
     fill_maps(maps, tmX, tmW, 1, false);  // unused slots
     SmallParams p{a, a, nullptr, FinalizeArgs{}, nullptr, nullptr, nullptr, 0, 0};
@@ -750,7 +939,7 @@ cudaError_t launch_tc_small_swiglu(const TcGemmArgs& a, const CUtensorMap& tmX, 
 
 cudaError_t launch_tc_small_down(const TcGemmArgs& a, const CUtensorMap& tmX, const CUtensorMap* tmW,
                                  int num_sms, cudaStream_t s) {
-    SmallMaps maps;
+    SmallMaps maps{};
     fill_maps(maps, tmX, tmW, a.n_micro, false);
     fill_maps(maps, tmX, tmW, 1, true);  // unused slots
     SmallParams p{a, a, nullptr, FinalizeArgs{}, nullptr, nullptr, nullptr, 0, 0};
@@ -761,11 +950,26 @@ cudaError_t launch_tc_small_fused(const TcGemmArgs& g1, const CUtensorMap& tmX1,
                                   const TcGemmArgs& g2, const CUtensorMap& tmX2, const CUtensorMap* tmW2,
                                   const FinalizeArgs& fin, const GatherArgs& gat, int* done, int num_sms,
                                   cudaStream_t s) {
-    SmallMaps maps;
+    SmallMaps maps{};
     fill_maps(maps, tmX1, tmW1, g1.n_micro, true);
     fill_maps(maps, tmX2, tmW2, g2.n_micro, false);
     SmallParams p{g1, g2, done, fin, gat.x, gat.xp, gat.perm, gat.k, (int)gat.row_bytes};
     return launch_small<kFused>(maps, p, g1.max_tiles + g2.max_tiles, num_sms, s);
+}
+
+cudaError_t launch_tc_small_fused_mxfp8(const TcGemmArgs& g1, const CUtensorMap& tmX1, const CUtensorMap* tmW1,
+                                        const CUtensorMap* tmS1, const TcGemmArgs& g2, const CUtensorMap& tmX2,
+                                        const CUtensorMap* tmW2, const CUtensorMap* tmS2, const FinalizeArgs& fin,
+                                        const GatherArgs& gat, int* done, int num_sms, cudaStream_t s) {
+    SmallMaps maps{};
+    fill_maps(maps, tmX1, tmW1, g1.n_micro, true);
+    fill_maps(maps, tmX2, tmW2, g2.n_micro, false);
+    for (int i = 0; i < kMaxMicro; ++i) {
+        maps.s1[i] = tmS1[i < g1.n_micro ? i : 0];
+        maps.s2[i] = tmS2[i < g2.n_micro ? i : 0];
+    }
+    SmallParams p{g1, g2, done, fin, gat.x, gat.xp, gat.perm, gat.k, (int)gat.row_bytes};
+    return launch_small<kFused, true>(maps, p, g1.max_tiles + g2.max_tiles, num_sms, s);
 }
 
 }  // namespace moe

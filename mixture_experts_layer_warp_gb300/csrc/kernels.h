@@ -168,6 +168,14 @@ cudaError_t launch_tc_small_down(const TcGemmArgs& a, const CUtensorMap& tmX, co
 // gathers xp from x (gat.x non-null). done[fused_counter_ints(E)] must be zero
 // at launch (the small-batch router zeroes it).
 inline int fused_counter_ints(int E) { return 3 * E + 2; }
+// The same with MXFP8 expert weights: tmW1[m] / tmW2[m] map the uint8 E4M3
+// codes (boxes {64, 64} / {64, 128}), tmS1[m] the w13 scales [E*H/32][2I]
+// (box {64, 2}), tmS2[m] the w2 scales [E*I/32][H] (box {128, 2}); gat.xp and
+// g1.out (h) hold f16.
+cudaError_t launch_tc_small_fused_mxfp8(const TcGemmArgs& g1, const CUtensorMap& tmX1, const CUtensorMap* tmW1,
+                                        const CUtensorMap* tmS1, const TcGemmArgs& g2, const CUtensorMap& tmX2,
+                                        const CUtensorMap* tmW2, const CUtensorMap* tmS2, const FinalizeArgs& fin,
+                                        const GatherArgs& gat, int* done, int num_sms, cudaStream_t s);
 cudaError_t launch_tc_small_fused(const TcGemmArgs& g1, const CUtensorMap& tmX1, const CUtensorMap* tmW1,
                                   const TcGemmArgs& g2, const CUtensorMap& tmX2, const CUtensorMap* tmW2,
                                   const FinalizeArgs& fin, const GatherArgs& gat, int* done, int num_sms,
@@ -242,6 +250,13 @@ cudaError_t enqueue_routing(const RoutingJob& j, cudaStream_t s, const LaunchHoo
 // 128-byte swizzle: the K-major operand layout of the tcgen05 kernels.
 bool encode_bf16_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
                     uint32_t box_rows);
+// Unswizzled uint8 map (MXFP8 codes and scales): box {box_inner bytes, box_rows}.
+bool encode_u8_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
+                  uint32_t box_inner, uint32_t box_rows);
+// MXFP8 quantisation (mxfp8.cu): w [groups][rows][cols] bf16 -> codes [groups][rows][cols],
+// scales [groups][cols/32][rows]; cols % 32 == 0.
+cudaError_t launch_mx_quantize(const void* w, int64_t groups, int rows, int cols, void* codes, void* scales,
+                               int num_sms, cudaStream_t s);
 
 // ------------------------------------------------------------ self-test
 cudaError_t launch_wait_selftest(int* err, uint64_t limit_ns, cudaStream_t s);

@@ -175,9 +175,16 @@ moe_status run_routing(moe_handle* h, const void* x, const void* router_w, const
     return MOE_OK;
 }
 
+// MXFP8 expert weights (moe_forward_mxfp8): per micro, the w13 / w2 arrays
+// passed to run_forward then hold E4M3 codes and these hold the E8M0 scales.
+struct MxScales {
+    const void* const* w13;  // [E][H/32][2I] per micro
+    const void* const* w2;   // [E][I/32][H] per micro
+};
+
 moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const float* bias,
                        const void* const* w13, const void* const* w2, const void* sw13, const void* sw2, int32_t T,
-                       void* y, cudaStream_t s) {
+                       void* y, cudaStream_t s, const MxScales* mx = nullptr) {
     const moe_config& c = h->cfg;
     const int H = c.hidden, E = c.num_experts, k = c.top_k, I = c.inter, M = c.n_micro, Is = c.shared_inter;
     const int64_t R = (int64_t)T * k;
@@ -226,7 +233,7 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
         const int active = (int)(R < E ? R : E);  // experts that can own routes
         if (!encode_bf16_2d(&tmX, h->xp, H, R, (uint64_t)H * 2, kSmallTokens))
             return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (xp)");
-        for (int m = 0; m < M; ++m)
+        for (int m = 0; m < M && mx == nullptr; ++m)
             if (!encode_bf16_2d(&tmW[m], w13[m], H, (uint64_t)E * 2 * I, (uint64_t)H * 2, 64))
                 return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (w13[%d])", m);
         TcGemmArgs g1{h->offsets, h->tiles_tc, E, M, H / kTcBK, I / 64, 2 * I, I, 0,
@@ -234,7 +241,7 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
         CUtensorMap tmX2, tmW2[kMaxMicro];
         if (!encode_bf16_2d(&tmX2, h->hbuf, (uint64_t)M * I, R, (uint64_t)M * I * 2, kSmallTokens))
             return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (h)");
-        for (int m = 0; m < M; ++m)
+        for (int m = 0; m < M && mx == nullptr; ++m)
             if (!encode_bf16_2d(&tmW2[m], w2[m], I, (uint64_t)E * H, (uint64_t)I * 2, 128))
                 return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (w2[%d])", m);
         TcGemmArgs g2{h->offsets, h->tiles_tc, E, M, I / kTcBK, H / 128, H, 0, I,
@@ -261,6 +268,23 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
         // gather, both GEMMs and the finalize in one launch (the
         // router zeroed h->done); the shared expert's GEMMs ran first
         FinalizeArgs fin{h->obuf, h->inv, h->topw, Is > 0 ? h->sbuf : nullptr, T, k, H, true, y, h->accumulate};
+        if (mx != nullptr) {
+            // MXFP8: the code and scale maps replace the bf16 weight maps
+            CUtensorMap c1[kMaxMicro], c2[kMaxMicro], s1[kMaxMicro], s2[kMaxMicro];
+            for (int m = 0; m < M; ++m)
+                if (!encode_u8_2d(&c1[m], w13[m], H, (uint64_t)E * 2 * I, (uint64_t)H, kTcBK, 64) ||
+                    !encode_u8_2d(&c2[m], w2[m], I, (uint64_t)E * H, (uint64_t)I, kTcBK, 128) ||
+                    !encode_u8_2d(&s1[m], mx->w13[m], 2 * (uint64_t)I, (uint64_t)E * (H / 32), 2 * (uint64_t)I, 64, 2) ||
+                    !encode_u8_2d(&s2[m], mx->w2[m], H, (uint64_t)E * (I / 32), (uint64_t)H, 128, 2))
+                    return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (MXFP8 weights, micro %d)", m);
+            if ((e = timed(h, kSlotGemm1, s, [&] {
+                     GatherArgs gat{x, h->perm, (int)R, k, (uint32_t)(H * 2), h->xp, h->err, h->limit_ns, h->num_sms};
+                     return launch_tc_small_fused_mxfp8(g1, tmX, c1, s1, g2, tmX2, c2, s2, fin, gat, h->done,
+                                                        h->num_sms, s);
+                 })) != cudaSuccess)
+                return cuda_err(h, e, "fused MXFP8 GEMM launch");
+            return MOE_OK;
+        }
         if ((e = timed(h, kSlotGemm1, s, [&] {
                  GatherArgs gat{x, h->perm, (int)R, k, (uint32_t)(H * 2), h->xp, h->err, h->limit_ns, h->num_sms};
                  return launch_tc_small_fused(g1, tmX, tmW, g2, tmX2, tmW2, fin, gat, h->done, h->num_sms, s);
@@ -528,6 +552,48 @@ moe_status moe_forward(moe_handle* h, const void* x, const void* router_w, const
     st = run_forward(h, x, router_w, router_bias, w13, w2, shared_w13, shared_w2, T, y, s);
     end_call(h);
     return st;
+}
+
+moe_status moe_forward_mxfp8(moe_handle* h, const void* x, const void* router_w, const float* router_bias,
+                             const void* const* w13_codes, const void* const* w13_scales,
+                             const void* const* w2_codes, const void* const* w2_scales, int32_t n_micro,
+                             int32_t top_k, const void* shared_w13, const void* shared_w2, int32_t T, void* y,
+                             void* stream) {
+    moe_status st = check_call(h, x, router_w, T);
+    if (st != MOE_OK) return st;
+    if (h->cfg.dtype != MOE_BF16)
+        return set_err(h, MOE_ERR_UNSUPPORTED, "MXFP8 expert weights need a bf16 layer");
+    if (T > kSmallTokens)
+        return set_err(h, MOE_ERR_UNSUPPORTED, "MXFP8 expert weights run batches of at most %d tokens", kSmallTokens);
+    if (T == 0) return MOE_OK;
+    st = check_weights(h, w13_codes, w2_codes, n_micro, top_k, shared_w13, shared_w2, y);
+    if (st != MOE_OK) return st;
+    if (w13_scales == nullptr || w2_scales == nullptr)
+        return set_err(h, MOE_ERR_INVALID_ARG, "w13 and w2 scale arrays must be non-null");
+    for (int m = 0; m < n_micro; ++m)
+        if (w13_scales[m] == nullptr || w2_scales[m] == nullptr || !aligned16(w13_scales[m]) ||
+            !aligned16(w2_scales[m]))
+            return set_err(h, MOE_ERR_INVALID_ARG, "micro %d scales null or not 16-byte aligned", m);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    h->last_stream = s;
+    const MxScales mx{w13_scales, w2_scales};
+    st = run_forward(h, x, router_w, router_bias, w13_codes, w2_codes, shared_w13, shared_w2, T, y, s, &mx);
+    end_call(h);
+    return st;
+}
+
+moe_status moe_quantize_mxfp8(const void* w, int64_t groups, int32_t rows, int32_t cols, void* codes,
+                              void* scales, void* stream) {
+    if (groups < 0 || rows < 0 || cols <= 0 || cols % 32 != 0) return MOE_ERR_INVALID_ARG;
+    if ((groups > 0 && rows > 0) && (w == nullptr || codes == nullptr || scales == nullptr)) return MOE_ERR_INVALID_ARG;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return launch_mx_quantize(w, groups, rows, cols, codes, scales, sms, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? MOE_OK
+               : MOE_ERR_CUDA;
 }
 
 moe_status moe_forward_host(moe_handle* h, const void* x_host, const void* router_w, const float* router_bias,

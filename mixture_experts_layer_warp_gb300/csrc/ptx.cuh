@@ -268,6 +268,18 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
 }
 
+// kind::f16 with f16 A and B (format code 0) and an fp32 accumulator.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+    return (1u << 4) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+}
+
+// Two FP8 E4M3 codes (the low byte is the first) to two f16, exactly.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+    return r;
+}
+
 // Shared-memory matrix descriptor of a K-major operand tile whose rows are
 // 128 bytes (64 bf16) and were written by TMA with 128-byte swizzling:
 // start address >> 4 in bits 0-13, leading byte offset (unused for this

@@ -1,0 +1,135 @@
+"""Block-scaled FP8 (MXFP8) expert weights on the GPU against the oracle.
+
+The quantiser must reproduce the oracle's codes and scales bit for bit (an
+integer decision taken on the same bf16 inputs); the layer run on MXFP8
+weights must match the oracle evaluated on the dequantised weights
+(f16(code * 2^(S-127)), fp64 arithmetic) within the bf16 layer tolerance.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import parity
+from mixture_experts_layer_warp_gb300 import binding
+from mixture_experts_layer_warp_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+TAU = 4e-6
+
+
+def _bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _special_weights(G=3, R=40, C=256, seed=5):
+    g = torch.Generator().manual_seed(seed)
+    w = torch.randn((G, R, C), generator=g) * 0.02
+    w[0, 0, :32] = 0.0                                   # an all-zero block
+    w[0, 1, :32] = -0.0
+    w[0, 2, :32] = 2.0 ** -130                           # bf16 subnormals
+    w[0, 3, :32] = torch.linspace(-1e30, 1e30, 32)       # huge values
+    w[0, 4, :32] = 256.0                                 # scale 2^0 ...
+    w[0, 4, 1:32] = torch.tensor([1.0625, 1.1875, 2.125, 3.25, -1.0625, 448.0, 460.0, 464.0, 470.0, 500.0,
+                                  2.0 ** -9, 3 * 2.0 ** -10, 2.0 ** -10, -(2.0 ** -10), 0.015625, 17.0,
+                                  18.0, 19.0, 200.0, 208.0, 216.0, -500.0, 0.0, -0.0, 1e-3, 5e-4, 7e-4,
+                                  300.0, 320.0, 352.0, 1.0])  # ... with ties and saturation
+    return w.to(torch.bfloat16)
+
+
+def test_quantizer_matches_the_oracle_bit_for_bit():
+    w = _special_weights()
+    codes, scales = binding.quantize_mxfp8(w.cuda())
+    torch.cuda.synchronize()
+    oc, os_ = oracle.mx_quantize(_bits(w))
+    assert np.array_equal(scales.cpu().numpy(), os_), "scales differ"
+    gc = codes.cpu().numpy()
+    bad = np.argwhere(gc != oc)
+    assert bad.size == 0, f"{len(bad)} codes differ, first at {bad[:3].tolist()}: {gc[tuple(bad[0])]} vs {oc[tuple(bad[0])]}"
+
+
+def _quantize_experts(dev):
+    w13 = [binding.quantize_mxfp8(t) for t in dev["w13"]]
+    w2 = [binding.quantize_mxfp8(t) for t in dev["w2"]]
+    return w13, w2
+
+
+def _dequant(q):
+    return [oracle.mx_dequant(c.cpu().numpy(), s.cpu().numpy()) for c, s in q]
+
+
+def _check(wl, inp, y, w13_q, w2_q, rows=None):
+    host = parity.to_host_numpy(inp)
+    orc = parity.oracle_routing(host, wl.k)
+    set_ok, _ = parity.decided(orc["lf"], orc["ids"], TAU)
+    T = host["x"].shape[0]
+    rows = np.arange(T) if rows is None else np.asarray(rows)
+    rows = rows[set_ok[rows]]
+    ref = oracle.forward_tokens(host["x"], orc["ids"], orc["w"], _dequant(w13_q), _dequant(w2_q), rows,
+                                host["shared_w13"], host["shared_w2"])
+    err = parity.y_error(y, ref, rows)
+    assert err <= parity.Y_TOL["bf16"], f"{wl.name}: rel err {err:.3e}"
+    return err
+
+
+SMALL = [
+    W.Workload("mx_two_micro", 8, 512, 16, 4, 256, 2),
+    W.Workload("mx_shared", 13, 512, 16, 4, 128, 1, shared_inter=256),
+    W.Workload("mx_one_token", 1, 256, 8, 2, 128, 1),
+    W.Workload("mx_e64_k8", 16, 1024, 64, 8, 256, 1),
+]
+
+
+@pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
+def test_mxfp8_layer_matches_the_oracle_on_dequantised_weights(wl):
+    inp = W.make_inputs(wl, seed=3)
+    dev = parity.to_device(inp)
+    w13_q, w2_q = _quantize_experts(dev)
+    layer = binding.MoELayer(wl.H, wl.E, wl.k, wl.I, wl.n_micro, max_tokens=wl.T, shared_inter=wl.shared_inter)
+    y = layer.forward_mxfp8(dev["x"], dev["router_w"], dev["router_bias"], w13_q, w2_q, dev["shared_w13"],
+                            dev["shared_w2"])
+    layer.sync()
+    y2 = layer.forward_mxfp8(dev["x"], dev["router_w"], dev["router_bias"], w13_q, w2_q, dev["shared_w13"],
+                             dev["shared_w2"])
+    layer.sync()
+    assert torch.equal(y, y2), "MXFP8 layer is not deterministic across calls"
+    layer.close()
+    _check(wl, inp, y, w13_q, w2_q)
+
+
+def test_mxfp8_decode_workload_matches_the_oracle():
+    wl = W.WORKLOADS["decode"]
+    inp = W.make_inputs(wl, seed=0, device="cuda")
+    w13_q, w2_q = _quantize_experts(inp)
+    layer = binding.MoELayer(wl.H, wl.E, wl.k, wl.I, wl.n_micro, max_tokens=wl.T)
+    y = layer.forward_mxfp8(inp["x"], inp["router_w"], inp["router_bias"], w13_q, w2_q)
+    layer.sync()
+    layer.close()
+    _check(wl, inp, y, w13_q, w2_q)
+
+
+def test_mxfp8_rejects_batches_above_sixteen_tokens():
+    wl = W.Workload("mx_17", 17, 256, 8, 2, 128, 1)
+    dev = parity.to_device(W.make_inputs(wl, seed=1))
+    w13_q, w2_q = _quantize_experts(dev)
+    layer = binding.MoELayer(wl.H, wl.E, wl.k, wl.I, 1, max_tokens=17)
+    with pytest.raises(binding.MoEError) as exc:
+        layer.forward_mxfp8(dev["x"], dev["router_w"], None, w13_q, w2_q)
+    assert exc.value.name == "MOE_ERR_UNSUPPORTED"
+    layer.close()
+
+
+def test_scales_outside_the_f16_range_take_the_exact_path():
+    """w2 scaled by 2^-14: its blocks get scales near 2^-26 (not f16 numbers),
+    so the dequantiser's fp32 form runs; y (made by w2) must still match."""
+    wl = W.Workload("mx_tiny_w2", 8, 512, 16, 4, 256, 1)
+    inp = W.make_inputs(wl, seed=4)
+    inp["w2"] = [(t.float() * 2.0 ** -14).to(torch.bfloat16) for t in inp["w2"]]
+    dev = parity.to_device(inp)
+    w13_q, w2_q = _quantize_experts(dev)
+    assert (w2_q[0][1] < 127 - 24).float().mean() > 0.5, "the test needs scales below 2^-24"
+    layer = binding.MoELayer(wl.H, wl.E, wl.k, wl.I, 1, max_tokens=wl.T)
+    y = layer.forward_mxfp8(dev["x"], dev["router_w"], None, w13_q, w2_q)
+    layer.sync()
+    layer.close()
+    _check(wl, inp, y, w13_q, w2_q)
