@@ -174,10 +174,11 @@ moe_status moe_quantize_mxfp8(const void *w, int64_t groups, int32_t rows, int32
 /*
  * moe_forward with MXFP8 routed-expert weights: w13_codes[m] / w13_scales[m]
  * and w2_codes[m] / w2_scales[m] as produced by moe_quantize_mxfp8 (device
- * pointers, 16-byte aligned). Supported for bf16 layers and batches of at
- * most 16 tokens (the decode-sized calls whose time is the weight bytes);
- * larger T returns MOE_ERR_UNSUPPORTED. Other arguments, ownership, the
- * accumulate switch and errors as for moe_forward.
+ * pointers, 16-byte aligned). Supported for bf16 layers (whose hidden and
+ * inter sizes, multiples of 256 and 128, fill its 128-deep K stages) and
+ * batches of at most 16 tokens (the decode-sized calls whose time is the
+ * weight bytes); larger T returns MOE_ERR_UNSUPPORTED. Other arguments,
+ * ownership, the accumulate switch and errors as for moe_forward.
  */
 moe_status moe_forward_mxfp8(moe_handle *h, const void *x, const void *router_w,
                              const float *router_bias, const void *const *w13_codes,

@@ -59,22 +59,35 @@ constexpr int kThreads = 256;
 constexpr int kGatherCtas = 128;               // kFused: CTAs that gather token rows
 constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kM, kTok);
 
-// MXFP8 expert weights (fused mode, moe_forward_mxfp8): each K-block's E4M3
-// codes (128 rows x 64 B) and E8M0 scales (2 per row) arrive through a deeper
-// ring beside the token rows, and four dequant warps (8..11) turn the codes
-// into f16 A tiles, code * 2^(S-127) rounded to f16, in one of kF8Dq 128B-
-// swizzled buffers; the routed GEMMs then run as f16 MMAs (the gathered token
-// rows and h are f16), with fp32 accumulators as before.
-constexpr int kF8Stages = 14;
-constexpr int kF8CodeBytes = kM * kTcBK;                          // 8 KB of codes
-constexpr int kF8SlotBytes = kF8CodeBytes + kM * (kTcBK / 32);    // + 256 B of scales
-constexpr int kF8Dq = 4;
-constexpr int kF8Threads = 384;
-constexpr int kF8SlotOff = kF8Stages * kBBytes;                   // after the token-row tiles
-constexpr int kF8DqOff = (kF8SlotOff + kF8Stages * kF8SlotBytes + 1023) / 1024 * 1024;
-constexpr int kF8CtlOff = kF8DqOff + kF8Dq * kABytes;
+// MXFP8 expert weights (fused mode, moe_forward_mxfp8): a stage covers 128 K
+// (twice the bf16 stage's K), so each weight row moves 128 contiguous bytes of
+// E4M3 codes per stage, as a bf16 row does (a 64-byte row per TMA box halves
+// the sustained stream rate); the codes arrive 128-byte swizzled with the four
+// E8M0 scales of each row and two token-row tiles. Eight dequant warps (8..15:
+// two per TMEM lane quadrant, taking alternate stages) turn each weight row's
+// 128 codes into f16, code * 2^(S-127) rounded to f16, in registers and store
+// them into one of kF8Dq A buffers in tensor memory; the MMA reads A from
+// tensor memory and the token rows (f16: the gathered rows and h) from shared
+// memory, into fp32 accumulators as before. No dequantised tile passes through
+// shared memory.
+constexpr int kF8Stages = 10;
+constexpr int kF8K = 2 * kTcBK;                      // 128 K per stage
+constexpr int kF8CodeBytes = kM * kF8K;              // 16 KB of codes
+constexpr int kF8ScaleBytes = kM * (kF8K / 32);      // 512 B of scales
+constexpr int kF8BBytes = 2 * kBBytes;               // two 64-K token-row tiles
+constexpr int kF8StageTx = kF8CodeBytes + kF8ScaleBytes + kF8BBytes;
+constexpr int kF8Dq = 4;                             // even: buffer parity = stage parity
+constexpr int kF8Threads = 512;                      // warps 8..15 dequantise
+constexpr int kF8CodeOff = kF8Stages * kF8BBytes;    // after the token-row tiles (1024-aligned)
+constexpr int kF8ScaleOff = kF8CodeOff + kF8Stages * kF8CodeBytes;
+constexpr int kF8CtlOff = kF8ScaleOff + kF8Stages * kF8ScaleBytes;
+constexpr int kF8TmemCols = 512;                     // accumulators at 0..31, A buffers from kF8ACol
+constexpr int kF8ACol = 64;                          // A buffer b: columns kF8ACol + 64 b .. + 63
 constexpr uint32_t kIdescF16 = ptx::idesc_f16_f32(kM, kTok);
 constexpr int kMaxStages = kF8Stages > kStages ? kF8Stages : kStages;
+static_assert(kF8ACol + kF8Dq * 64 <= kF8TmemCols, "A buffers exceed the TMEM allocation");
+static_assert(kF8Dq % 2 == 0, "each dequant warp set owns the buffers of its stage parity");
+static_assert(kF8CodeOff % 1024 == 0 && kF8CodeBytes % 1024 == 0, "128-byte swizzled tiles need 1024-byte alignment");
 
 enum Mode { kSwiGLUOnly = 0, kDownOnly = 1, kFused = 2 };
 
@@ -103,7 +116,8 @@ struct Ctl {
     uint64_t sq_empty;
     int sq_tile;
     int sq_rows;
-    // MXFP8: dequantised A tiles handed from the dequant warps to the MMA issuer
+    // MXFP8: dequantised A buffers (tensor memory) handed from the dequant warps
+    // to the MMA issuer
     uint64_t dq_full[kF8Dq];
     uint64_t dq_empty[kF8Dq];
 };
@@ -441,7 +455,7 @@ __device__ __forceinline__ int pop_scheduled(Ctl& c, uint32_t& phase, uint64_t l
 // true): one f16 multiply per pair of exact operands, branch-free.
 __device__ __forceinline__ bool dequant_in_f16(int S) { return S >= 127 - 24 && S <= 127 + 15; }
 
-__device__ __forceinline__ void dequant16_f16(uint4 q, int S, uint32_t (&o)[8]) {
+__device__ __forceinline__ void dequant16_f16(uint4 q, int S, uint32_t* o) {
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
     const int e = S - 127;
     const unsigned short hb = e >= -14 ? (unsigned short)((e + 15) << 10) : (unsigned short)(1u << ((e + 24) & 15));
@@ -455,7 +469,7 @@ __device__ __forceinline__ void dequant16_f16(uint4 q, int S, uint32_t (&o)[8]) 
 }
 
 // Any scale: through fp32, where the product is exact, rounded once to f16.
-__device__ __forceinline__ void dequant16_f32(uint4 q, int S, uint32_t (&o)[8]) {
+__device__ __forceinline__ void dequant16_f32(uint4 q, int S, uint32_t* o) {
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
     const int e = S - 127;
     const float fs = e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(1u << (e + 149));
@@ -478,9 +492,10 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Ctl& c = *reinterpret_cast<Ctl*>(smem + (F8 ? kF8CtlOff : kStages * kStageBytes));
-    // stage s: the A tile (bf16 weights, or MXFP8 codes + scales) and the token-row B tile
-    auto stage_a = [&](int st) { return smem + (F8 ? kF8SlotOff + st * kF8SlotBytes : st * kStageBytes); };
-    auto stage_b = [&](int st) { return smem + (F8 ? st * kBBytes : st * kStageBytes + kABytes); };
+    // stage s: the A tile (bf16 weights, or MXFP8 codes; their scales apart) and the token-row B tile
+    auto stage_a = [&](int st) { return smem + (F8 ? kF8CodeOff + st * kF8CodeBytes : st * kStageBytes); };
+    auto stage_s = [&](int st) { return smem + kF8ScaleOff + st * kF8ScaleBytes; };
+    auto stage_b = [&](int st) { return smem + (F8 ? st * kF8BBytes : st * kStageBytes + kABytes); };
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const TcGemmArgs& a0 = MODE == kDownOnly ? p.g2 : p.g1;  // seg, tiles, G, err, limit
     // the next routing call's kernels may be placed as SMs free up; they wait
@@ -497,14 +512,14 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
             ptx::mbar_init(ptx::smem_u32(&c.tempty[b]), 4);
         }
         for (int b = 0; b < kF8Dq; ++b) {
-            ptx::mbar_init(ptx::smem_u32(&c.dq_full[b]), 4);  // the four dequant warps
+            ptx::mbar_init(ptx::smem_u32(&c.dq_full[b]), 4);  // the four dequant warps of its parity
             ptx::mbar_init(ptx::smem_u32(&c.dq_empty[b]), 1);  // the MMA issuer's commit
         }
         ptx::mbar_init(ptx::smem_u32(&c.drain), 1);
         for (int q = 0; q < 4; ++q) {
             ptx::mbar_init(ptx::smem_u32(&c.tq_full[q]), 1);
-            // MMA issuer + four epilogue warps (+ four dequant warps)
-            ptx::mbar_init(ptx::smem_u32(&c.tq_empty[q]), F8 ? 9 : 5);
+            // MMA issuer + four epilogue warps (+ eight dequant warps)
+            ptx::mbar_init(ptx::smem_u32(&c.tq_empty[q]), F8 ? 13 : 5);
         }
         ptx::mbar_init(ptx::smem_u32(&c.sq_full), 1);
         ptx::mbar_init(ptx::smem_u32(&c.sq_empty), 1);
@@ -523,7 +538,7 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
         if (MODE != kSwiGLUOnly) ptx::prefetch_tmap(&maps.x2);
     }
     if (warp == 2) {
-        ptx::tmem_alloc(ptx::smem_u32(&c.tmem_base), kTmemCols);
+        ptx::tmem_alloc(ptx::smem_u32(&c.tmem_base), F8 ? kF8TmemCols : kTmemCols);
         ptx::tmem_relinquish();
     }
     ptx::tc_fence_before();
@@ -578,26 +593,35 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
                 const CUtensorMap* tsc = sw ? &maps.s1[m] : &maps.s2[m];  // MXFP8 scales
                 const CUtensorMap* tx = sw ? &maps.x1 : &maps.x2;
                 const int wrow = t.g * g.b_rows_per_group + t.nt * (sw ? 64 : kM);
-                for (int kb = 0; kb < g.k_blocks; ++kb) {
+                constexpr int kK = F8 ? kF8K : kTcBK;                      // K per stage
+                const int kbn = F8 ? g.k_blocks / 2 : g.k_blocks;         // stages per micro
+                // the token rows of a stage: one 64-K tile (two with MXFP8 weights)
+                auto load_rows = [&](int st, int kx, uint32_t bar) {
+                    const uint32_t sb = ptx::smem_u32(stage_b(st));
+                    ptx::tma_load_2d(sb, tx, kx, t.row0, bar);
+                    if (F8) ptx::tma_load_2d(sb + kBBytes, tx, kx + kTcBK, t.row0, bar);
+                };
+                for (int kb = 0; kb < kbn; ++kb) {
                     if (!ptx::mbar_wait(ptx::smem_u32(&c.empty[stage]), phase ^ 1u, g.limit_ns, &c.abort)) {
                         ok = false;
                         break;
                     }
                     const uint32_t sa = ptx::smem_u32(stage_a(stage));
                     const uint32_t fb = ptx::smem_u32(&c.full[stage]);
-                    ptx::mbar_arrive_expect_tx(fb, F8 ? kF8SlotBytes + kBBytes : kStageBytes);
+                    ptx::mbar_arrive_expect_tx(fb, F8 ? kF8StageTx : kStageBytes);
                     if (F8) {
-                        // codes: K-block kb of the tile's rows; scales: the two 32-blocks of kb
-                        const int srow = t.g * 2 * g.k_blocks + 2 * kb;
+                        // codes: 128 K of the tile's rows; scales: the four 32-blocks of those K
+                        const int srow = t.g * 2 * g.k_blocks + 4 * kb;
+                        const uint32_t ss = ptx::smem_u32(stage_s(stage));
                         if (sw) {
-                            ptx::tma_load_2d_hint(sa, tw, kb * kTcBK, wrow, fb, wpol);            // 64 gate rows
-                            ptx::tma_load_2d_hint(sa + kF8CodeBytes / 2, tw, kb * kTcBK, wrow + g.up_offset, fb,
+                            ptx::tma_load_2d_hint(sa, tw, kb * kK, wrow, fb, wpol);               // 64 gate rows
+                            ptx::tma_load_2d_hint(sa + kF8CodeBytes / 2, tw, kb * kK, wrow + g.up_offset, fb,
                                                   wpol);                                           // 64 up rows
-                            ptx::tma_load_2d(sa + kF8CodeBytes, tsc, t.nt * 64, srow, fb);
-                            ptx::tma_load_2d(sa + kF8CodeBytes + 128, tsc, g.up_offset + t.nt * 64, srow, fb);
+                            ptx::tma_load_2d(ss, tsc, t.nt * 64, srow, fb);
+                            ptx::tma_load_2d(ss + kF8ScaleBytes / 2, tsc, g.up_offset + t.nt * 64, srow, fb);
                         } else {
-                            ptx::tma_load_2d_hint(sa, tw, kb * kTcBK, wrow, fb, wpol);            // 128 rows
-                            ptx::tma_load_2d(sa + kF8CodeBytes, tsc, t.nt * kM, srow, fb);
+                            ptx::tma_load_2d_hint(sa, tw, kb * kK, wrow, fb, wpol);               // 128 rows
+                            ptx::tma_load_2d(ss, tsc, t.nt * kM, srow, fb);
                         }
                     } else if (sw) {
                         ptx::tma_load_2d_hint(sa, tw, kb * kTcBK, wrow, fb, wpol);            // 64 gate rows
@@ -606,9 +630,9 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
                     } else {
                         ptx::tma_load_2d_hint(sa, tw, kb * kTcBK, wrow, fb, wpol);            // 128 rows
                     }
-                    const int kx = (sw ? 0 : m * g.a_micro_cols) + kb * kTcBK;
+                    const int kx = (sw ? 0 : m * g.a_micro_cols) + kb * kK;
                     if (rows_ready) {
-                        ptx::tma_load_2d(ptx::smem_u32(stage_b(stage)), tx, kx, t.row0, fb);  // 16 token rows
+                        load_rows(stage, kx, fb);  // 16 token rows
                     } else {
                         pend_stage[pending] = stage;
                         pend_kb[pending] = kx;
@@ -620,7 +644,7 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
                         stage = 0;
                         phase ^= 1u;
                     }
-                    if (!rows_ready && (pending == kSt || kb + 1 == g.k_blocks)) {
+                    if (!rows_ready && (pending == kSt || kb + 1 == kbn)) {
                         // every free stage holds weights: wait for the rows, then
                         // complete the pending stages with their token rows
                         const uint64_t t0 = ptx::globaltimer();
@@ -633,10 +657,8 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
                             __nanosleep(32);
                         }
                         fence_proxy_async_global();
-                        for (int q = 0; q < pending; ++q) {  // completes the armed stages even on failure
-                            ptx::tma_load_2d(ptx::smem_u32(stage_b(pend_stage[q])), tx, pend_kb[q], t.row0,
-                                             ptx::smem_u32(&c.full[pend_stage[q]]));
-                        }
+                        for (int q = 0; q < pending; ++q)  // completes the armed stages even on failure
+                            load_rows(pend_stage[q], pend_kb[q], ptx::smem_u32(&c.full[pend_stage[q]]));
                         pending = 0;
                         rows_ready = true;
                         if (!ok) break;
@@ -681,20 +703,35 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
             const uint32_t d = tmem + (uint32_t)(acc * kTok);
             uint32_t accumulate = 0;
             const int n_micro_k = sw ? 1 : g.n_micro;
+            const int kbn = F8 ? g.k_blocks / 2 : g.k_blocks;  // stages per micro
             for (int mi = 0; ok && mi < n_micro_k; ++mi) {
-                for (int kb = 0; kb < g.k_blocks; ++kb) {
+                for (int kb = 0; kb < kbn; ++kb) {
                     if (!ptx::mbar_wait(ptx::smem_u32(&c.full[stage]), phase, g.limit_ns, &c.abort) ||
                         (F8 && !ptx::mbar_wait(ptx::smem_u32(&c.dq_full[dq]), dq_phase, g.limit_ns, &c.abort))) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
-                    const uint32_t sa = F8 ? ptx::smem_u32(smem + kF8DqOff + dq * kABytes) : ptx::smem_u32(stage_a(stage));
-                    const uint64_t adesc = ptx::sw128_desc(sa), bdesc = ptx::sw128_desc(ptx::smem_u32(stage_b(stage)));
+                    const uint64_t bdesc = ptx::sw128_desc(ptx::smem_u32(stage_b(stage)));
+                    if (F8) {
+                        // A buffer dq: 8 columns per 16 K; the second 64 K pair with the second token tile
+                        const uint32_t at = tmem + (uint32_t)(kF8ACol + dq * 64);
 #pragma unroll
-                    for (int k = 0; k < kTcBK / 16; ++k) {
-                        ptx::mma_bf16(d, adesc + 2u * k, bdesc + 2u * k, kId, accumulate);
-                        accumulate = 1;
+                        for (int h = 0; h < 2; ++h) {
+                            const uint64_t bd = ptx::sw128_desc(ptx::smem_u32(stage_b(stage)) + h * kBBytes);
+#pragma unroll
+                            for (int k = 0; k < kTcBK / 16; ++k) {
+                                ptx::mma_tmem_a(d, at + 32u * h + 8u * k, bd + 2u * k, kId, accumulate);
+                                accumulate = 1;
+                            }
+                        }
+                    } else {
+                        const uint64_t adesc = ptx::sw128_desc(ptx::smem_u32(stage_a(stage)));
+#pragma unroll
+                        for (int k = 0; k < kTcBK / 16; ++k) {
+                            ptx::mma_bf16(d, adesc + 2u * k, bdesc + 2u * k, kId, accumulate);
+                            accumulate = 1;
+                        }
                     }
                     ptx::mma_commit(ptx::smem_u32(&c.empty[stage]));
                     if (++stage == kSt) {
@@ -717,10 +754,14 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
         ptx::mbar_wait(ptx::smem_u32(&c.drain), 0, a0.limit_ns, nullptr);
     } else if (F8 && warp >= 8) {
         // ------------------------------------------------ MXFP8 dequant
-        // thread dt converts, per K-block, 16-code chunk dt % 4 of rows
-        // dt / 4 + 32 * pass into the swizzled f16 layout the MMA reads
-        const int dt = threadIdx.x - 256;
-        int stage = 0, dq = 0;
+        // warp 8 + 4 j + q owns TMEM lanes 32 q .. 32 q + 31 (weight rows, one
+        // per thread) of the stages of parity j: its thread reads the row's 128
+        // codes and 4 scales, converts them in registers and stores the 64 f16
+        // pairs into the row's lane of the A buffer
+        const int q = warp & 3, par = (warp - 8) >> 2;
+        const int r = q * 32 + lane;
+        const uint32_t a_lanes = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)kF8ACol;
+        int stage = 0, dq = 0, kseq = 0;
         uint32_t phase = 0, dq_phase = 0;
         bool ok = true;
         TileStream ts;
@@ -733,57 +774,52 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
             bool sw;
             locate<MODE>(tile, c, p, sw);
             const TcGemmArgs& g = sw ? p.g1 : p.g2;
-            const int nk = (sw ? 1 : g.n_micro) * g.k_blocks;
-            for (int i = 0; i < nk; ++i) {
-                bool got = ptx::mbar_wait(ptx::smem_u32(&c.full[stage]), phase, g.limit_ns, &c.abort) &&
-                           ptx::mbar_wait(ptx::smem_u32(&c.dq_empty[dq]), dq_phase ^ 1u, g.limit_ns, &c.abort);
-                if (!__all_sync(0xffffffffu, got)) {
-                    ok = false;
-                    break;
-                }
-                const unsigned char* src = stage_a(stage);
-                unsigned char* dst = smem + kF8DqOff + dq * kABytes;
-                // all loads first (the stores below cannot move above them otherwise)
-                constexpr int kPasses = kM / 32;
-                const int ch = dt & 3;
-                uint4 codes[kPasses];
-                int scale[kPasses];
-#pragma unroll
-                for (int pass = 0; pass < kPasses; ++pass) {
-                    const int row = (dt >> 2) + 32 * pass;
-                    codes[pass] = *reinterpret_cast<const uint4*>(src + row * kTcBK + ch * 16);
-                    // scales: SwiGLU tiles [2][64] for the gate rows, then [2][64] for the up rows;
-                    // down tiles [2][128]
-                    scale[pass] = src[kF8CodeBytes + (sw ? (row >> 6) * 128 + (ch >> 1) * 64 + (row & 63)
-                                                          : (ch >> 1) * kM + row)];
-                }
-                // branch-free f16 form for every chunk; the rare chunks whose scale
-                // is not an f16 number are then redone through fp32
-                bool slow = false;
-#pragma unroll
-                for (int pass = 0; pass < kPasses; ++pass) {
-                    const int row = (dt >> 2) + 32 * pass;
-                    uint32_t o[8];
-                    dequant16_f16(codes[pass], scale[pass], o);
-                    slow |= !dequant_in_f16(scale[pass]);
-                    unsigned char* rp = dst + (row >> 3) * 1024 + (row & 7) * 128;
-                    *reinterpret_cast<uint4*>(rp + (((2 * ch) ^ (row & 7)) * 16)) = make_uint4(o[0], o[1], o[2], o[3]);
-                    *reinterpret_cast<uint4*>(rp + (((2 * ch + 1) ^ (row & 7)) * 16)) = make_uint4(o[4], o[5], o[6], o[7]);
-                }
-                if (slow) {
-                    for (int pass = 0; pass < kPasses; ++pass) {
-                        if (dequant_in_f16(scale[pass])) continue;
-                        const int row = (dt >> 2) + 32 * pass;
-                        uint32_t o[8];
-                        dequant16_f32(codes[pass], scale[pass], o);
-                        unsigned char* rp = dst + (row >> 3) * 1024 + (row & 7) * 128;
-                        *reinterpret_cast<uint4*>(rp + (((2 * ch) ^ (row & 7)) * 16)) = make_uint4(o[0], o[1], o[2], o[3]);
-                        *reinterpret_cast<uint4*>(rp + (((2 * ch + 1) ^ (row & 7)) * 16)) = make_uint4(o[4], o[5], o[6], o[7]);
+            const int nk = (sw ? 1 : g.n_micro) * (g.k_blocks / 2);
+            for (int i = 0; i < nk; ++i, ++kseq) {
+                if ((kseq & 1) == par) {
+                    bool got = ptx::mbar_wait(ptx::smem_u32(&c.full[stage]), phase, g.limit_ns, &c.abort) &&
+                               ptx::mbar_wait(ptx::smem_u32(&c.dq_empty[dq]), dq_phase ^ 1u, g.limit_ns, &c.abort);
+                    if (!__all_sync(0xffffffffu, got)) {
+                        ok = false;
+                        break;
                     }
+                    ptx::tc_fence_after();
+                    // 16-byte chunk j of row r sits at chunk j ^ (r % 8) (128-byte swizzle)
+                    const unsigned char* row = stage_a(stage) + r * kF8K;
+                    uint4 cv[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) cv[j] = *reinterpret_cast<const uint4*>(row + ((j ^ (r & 7)) << 4));
+                    // scales: SwiGLU tiles [4][64] for the gate rows, then [4][64] for the up
+                    // rows; down tiles [4][128]
+                    const unsigned char* sp = stage_s(stage);
+                    const int so = sw ? (r >> 6) * (kF8ScaleBytes / 2) + (r & 63) : r;
+                    const int sstep = sw ? 64 : kM;
+                    int sc[4];
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) sc[b] = sp[so + b * sstep];
+                    bool slow = false;
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) slow |= !dequant_in_f16(sc[b]);
+                    // two halves of 64 K (32 columns each), so only one half's f16 pairs are live
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        uint32_t o[32];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) dequant16_f16(cv[4 * hf + j], sc[2 * hf + (j >> 1)], o + 8 * j);
+                        if (slow) {  // rare: scales that are not f16 numbers
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                if (!dequant_in_f16(sc[2 * hf + (j >> 1)]))
+                                    dequant16_f32(cv[4 * hf + j], sc[2 * hf + (j >> 1)], o + 8 * j);
+                        }
+                        __syncwarp();
+                        ptx::tmem_st32(a_lanes + (uint32_t)(dq * 64 + 32 * hf), o);
+                    }
+                    ptx::tmem_wait_st();
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&c.dq_full[dq]));
                 }
-                ptx::fence_proxy_async_smem();  // the tensor core reads these (async proxy)
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&c.dq_full[dq]));
                 if (++stage == kSt) {
                     stage = 0;
                     phase ^= 1u;
@@ -877,7 +913,7 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
     __syncthreads();
     if (warp == 2) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem, kTmemCols);
+        ptx::tmem_dealloc(tmem, F8 ? kF8TmemCols : kTmemCols);
     }
 }
 

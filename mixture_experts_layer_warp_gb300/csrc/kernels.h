@@ -250,9 +250,10 @@ cudaError_t enqueue_routing(const RoutingJob& j, cudaStream_t s, const LaunchHoo
 // 128-byte swizzle: the K-major operand layout of the tcgen05 kernels.
 bool encode_bf16_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
                     uint32_t box_rows);
-// Unswizzled uint8 map (MXFP8 codes and scales): box {box_inner bytes, box_rows}.
+// uint8 map (MXFP8 codes and scales): box {box_inner bytes, box_rows}, unswizzled
+// or with the 128-byte swizzle (16-byte chunk c of row r at chunk c ^ (r % 8)).
 bool encode_u8_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
-                  uint32_t box_inner, uint32_t box_rows);
+                  uint32_t box_inner, uint32_t box_rows, bool swizzle128);
 // MXFP8 quantisation (mxfp8.cu): w [groups][rows][cols] bf16 -> codes [groups][rows][cols],
 // scales [groups][cols/32][rows]; cols % 32 == 0.
 cudaError_t launch_mx_quantize(const void* w, int64_t groups, int rows, int cols, void* codes, void* scales,

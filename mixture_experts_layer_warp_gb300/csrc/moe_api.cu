@@ -272,10 +272,11 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
             // MXFP8: the code and scale maps replace the bf16 weight maps
             CUtensorMap c1[kMaxMicro], c2[kMaxMicro], s1[kMaxMicro], s2[kMaxMicro];
             for (int m = 0; m < M; ++m)
-                if (!encode_u8_2d(&c1[m], w13[m], H, (uint64_t)E * 2 * I, (uint64_t)H, kTcBK, 64) ||
-                    !encode_u8_2d(&c2[m], w2[m], I, (uint64_t)E * H, (uint64_t)I, kTcBK, 128) ||
-                    !encode_u8_2d(&s1[m], mx->w13[m], 2 * (uint64_t)I, (uint64_t)E * (H / 32), 2 * (uint64_t)I, 64, 2) ||
-                    !encode_u8_2d(&s2[m], mx->w2[m], H, (uint64_t)E * (I / 32), (uint64_t)H, 128, 2))
+                if (!encode_u8_2d(&c1[m], w13[m], H, (uint64_t)E * 2 * I, (uint64_t)H, 128, 64, true) ||
+                    !encode_u8_2d(&c2[m], w2[m], I, (uint64_t)E * H, (uint64_t)I, 128, 128, true) ||
+                    !encode_u8_2d(&s1[m], mx->w13[m], 2 * (uint64_t)I, (uint64_t)E * (H / 32), 2 * (uint64_t)I, 64, 4,
+                                  false) ||
+                    !encode_u8_2d(&s2[m], mx->w2[m], H, (uint64_t)E * (I / 32), (uint64_t)H, 128, 4, false))
                     return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (MXFP8 weights, micro %d)", m);
             if ((e = timed(h, kSlotGemm1, s, [&] {
                      GatherArgs gat{x, h->perm, (int)R, k, (uint32_t)(H * 2), h->xp, h->err, h->limit_ns, h->num_sms};

@@ -46,7 +46,7 @@ bool encode_bf16_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t r
 }
 
 bool encode_u8_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
-                  uint32_t box_inner, uint32_t box_rows) {
+                  uint32_t box_inner, uint32_t box_rows, bool swizzle128) {
     EncodeTiledFn enc = encode_fn();
     if (enc == nullptr) return false;
     cuuint64_t dims[2] = {inner, rows};
@@ -54,8 +54,8 @@ bool encode_u8_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t row
     cuuint32_t box[2] = {box_inner, box_rows};
     cuuint32_t estr[2] = {1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 cudaError_t enqueue_routing(const RoutingJob& j, cudaStream_t s, const LaunchHook* hook) {
