@@ -75,13 +75,12 @@ constexpr int kF8K = 2 * kTcBK;                      // 128 K per stage
 constexpr int kF8CodeBytes = kM * kF8K;              // 16 KB of codes
 constexpr int kF8ScaleBytes = kM * (kF8K / 32);      // 512 B of scales
 constexpr int kF8BBytes = 2 * kBBytes;               // two 64-K token-row tiles
-constexpr int kF8StageTx = kF8CodeBytes + kF8ScaleBytes + kF8BBytes;
 constexpr int kF8Dq = 4;                             // even: buffer parity = stage parity
 constexpr int kF8Threads = 512;                      // warps 8..15 dequantise
 constexpr int kF8CodeOff = kF8Stages * kF8BBytes;    // after the token-row tiles (1024-aligned)
 constexpr int kF8ScaleOff = kF8CodeOff + kF8Stages * kF8CodeBytes;
 constexpr int kF8CtlOff = kF8ScaleOff + kF8Stages * kF8ScaleBytes;
-constexpr int kF8TmemCols = 512;                     // accumulators at 0..31, A buffers from kF8ACol
+constexpr int kF8TmemCols = 512;                     // accumulators at 0..63, A buffers from kF8ACol
 constexpr int kF8ACol = 64;                          // A buffer b: columns kF8ACol + 64 b .. + 63
 constexpr uint32_t kIdescF16 = ptx::idesc_f16_f32(kM, kTok);
 constexpr int kMaxStages = kF8Stages > kStages ? kF8Stages : kStages;
@@ -97,6 +96,7 @@ struct Ctl {
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t drain;
+    uint64_t drain2;  // MXFP8: the second MMA issuer's
     uint32_t tmem_base;
     int abort;
     int seg[kMaxExperts + 1];
@@ -139,15 +139,24 @@ struct SmallParams {
     const int32_t* gperm;
     int gk;
     int grow_bytes;
+    // MXFP8: token rows per 64-K tile that the loads fill (8 when the batch has
+    // at most 8 tokens, as no expert then owns more routes; else 16). The MMA
+    // still reads 16 rows: rows past the loaded ones only feed output columns
+    // that the epilogue drops.
+    int brows;
 };
 
+// With MXFP8 weights every stage is three TMA instructions (the producer
+// thread's issue rate bounds the stream otherwise): the gate and up rows of a
+// SwiGLU stage come as one 3D box, so do their scales, and so do the two 64-K
+// token-row tiles.
 struct SmallMaps {
-    CUtensorMap x1;      // SwiGLU token rows [R][H], box {64, 16}
-    CUtensorMap x2;      // down token rows (h) [R][M*I], box {64, 16}
-    CUtensorMap w1[kMaxMicro];  // w13[m] [E*2I][H], box {64, 64} (MXFP8: uint8 codes)
-    CUtensorMap w2[kMaxMicro];  // w2[m] [E*H][I], box {64, 128} (MXFP8: uint8 codes)
-    CUtensorMap s1[kMaxMicro];  // MXFP8: w13[m] scales [E*H/32][2I] uint8, box {64, 2}
-    CUtensorMap s2[kMaxMicro];  // MXFP8: w2[m] scales [E*I/32][H] uint8, box {128, 2}
+    CUtensorMap x1;      // SwiGLU token rows [R][H], box {64, 16} (MXFP8: 3D {64, R, H/64}, box {64, 16, 2})
+    CUtensorMap x2;      // down token rows (h) [R][M*I], box {64, 16} (MXFP8: 3D as x1)
+    CUtensorMap w1[kMaxMicro];  // w13[m] [E*2I][H], box {64, 64} (MXFP8: uint8 codes, 3D {H, I, 2E}, box {128, 64, 2})
+    CUtensorMap w2[kMaxMicro];  // w2[m] [E*H][I], box {64, 128} (MXFP8: uint8 codes, box {128, 128})
+    CUtensorMap s1[kMaxMicro];  // MXFP8: w13[m] scales 3D {I, 2, E*H/32}, box {64, 2, 4}: [4][gate, up][64]
+    CUtensorMap s2[kMaxMicro];  // MXFP8: w2[m] scales [E*I/32][H] uint8, box {128, 4}: [4][128]
 };
 
 __device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
@@ -487,7 +496,6 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
     tc_small_kernel(const __grid_constant__ SmallMaps maps, const SmallParams p) {
     static_assert(!F8 || MODE == kFused, "MXFP8 weights run in the fused mode only");
     constexpr int kSt = F8 ? kF8Stages : kStages;
-    constexpr uint32_t kId = F8 ? kIdescF16 : kIdesc;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -508,7 +516,7 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
             ptx::mbar_init(ptx::smem_u32(&c.empty[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
-            ptx::mbar_init(ptx::smem_u32(&c.tfull[b]), 1);
+            ptx::mbar_init(ptx::smem_u32(&c.tfull[b]), F8 ? 2 : 1);  // the MMA issuer(s)' commits
             ptx::mbar_init(ptx::smem_u32(&c.tempty[b]), 4);
         }
         for (int b = 0; b < kF8Dq; ++b) {
@@ -516,10 +524,12 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
             ptx::mbar_init(ptx::smem_u32(&c.dq_empty[b]), 1);  // the MMA issuer's commit
         }
         ptx::mbar_init(ptx::smem_u32(&c.drain), 1);
+        ptx::mbar_init(ptx::smem_u32(&c.drain2), 1);
         for (int q = 0; q < 4; ++q) {
             ptx::mbar_init(ptx::smem_u32(&c.tq_full[q]), 1);
-            // MMA issuer + four epilogue warps (+ eight dequant warps)
-            ptx::mbar_init(ptx::smem_u32(&c.tq_empty[q]), F8 ? 13 : 5);
+            // MMA issuer + four epilogue warps (MXFP8: two MMA issuers, four epilogue
+            // and eight dequant warps)
+            ptx::mbar_init(ptx::smem_u32(&c.tq_empty[q]), F8 ? 14 : 5);
         }
         ptx::mbar_init(ptx::smem_u32(&c.sq_full), 1);
         ptx::mbar_init(ptx::smem_u32(&c.sq_empty), 1);
@@ -564,7 +574,7 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
         // ------------------------------------------------ TMA producer
         const uint64_t wpol = ptx::policy_evict_first();  // each weight byte is read once per call
         int stage = 0;
-        uint32_t phase = 0, last_par[kSt];
+        uint32_t phase = 0;
         int issued = 0;
         bool ok = true;
         TileStream ts;
@@ -598,8 +608,10 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
                 // the token rows of a stage: one 64-K tile (two with MXFP8 weights)
                 auto load_rows = [&](int st, int kx, uint32_t bar) {
                     const uint32_t sb = ptx::smem_u32(stage_b(st));
-                    ptx::tma_load_2d(sb, tx, kx, t.row0, bar);
-                    if (F8) ptx::tma_load_2d(sb + kBBytes, tx, kx + kTcBK, t.row0, bar);
+                    if (F8)
+                        ptx::tma_load_3d(sb, tx, 0, t.row0, kx / kTcBK, bar);  // both 64-K tiles (brows rows each)
+                    else
+                        ptx::tma_load_2d(sb, tx, kx, t.row0, bar);
                 };
                 for (int kb = 0; kb < kbn; ++kb) {
                     if (!ptx::mbar_wait(ptx::smem_u32(&c.empty[stage]), phase ^ 1u, g.limit_ns, &c.abort)) {
@@ -608,17 +620,15 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
                     }
                     const uint32_t sa = ptx::smem_u32(stage_a(stage));
                     const uint32_t fb = ptx::smem_u32(&c.full[stage]);
-                    ptx::mbar_arrive_expect_tx(fb, F8 ? kF8StageTx : kStageBytes);
+                    ptx::mbar_arrive_expect_tx(fb, F8 ? kF8CodeBytes + kF8ScaleBytes + p.brows * 256 : kStageBytes);
                     if (F8) {
                         // codes: 128 K of the tile's rows; scales: the four 32-blocks of those K
                         const int srow = t.g * 2 * g.k_blocks + 4 * kb;
                         const uint32_t ss = ptx::smem_u32(stage_s(stage));
                         if (sw) {
-                            ptx::tma_load_2d_hint(sa, tw, kb * kK, wrow, fb, wpol);               // 64 gate rows
-                            ptx::tma_load_2d_hint(sa + kF8CodeBytes / 2, tw, kb * kK, wrow + g.up_offset, fb,
-                                                  wpol);                                           // 64 up rows
-                            ptx::tma_load_2d(ss, tsc, t.nt * 64, srow, fb);
-                            ptx::tma_load_2d(ss + kF8ScaleBytes / 2, tsc, g.up_offset + t.nt * 64, srow, fb);
+                            // 64 gate rows, then the 64 matching up rows (half 2g + 1 of the map)
+                            ptx::tma_load_3d_hint(sa, tw, kb * kK, t.nt * 64, 2 * t.g, fb, wpol);
+                            ptx::tma_load_3d(ss, tsc, t.nt * 64, 0, srow, fb);
                         } else {
                             ptx::tma_load_2d_hint(sa, tw, kb * kK, wrow, fb, wpol);               // 128 rows
                             ptx::tma_load_2d(ss, tsc, t.nt * kM, srow, fb);
@@ -638,7 +648,6 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
                         pend_kb[pending] = kx;
                         ++pending;
                     }
-                    last_par[stage] = phase;
                     ++issued;
                     if (++stage == kSt) {
                         stage = 0;
@@ -675,15 +684,17 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
         if (!ok) {
             fail(c, a0.err);
             const int n = issued < kSt ? issued : kSt;
-            for (int s = 0; s < n; ++s) ptx::mbar_wait(ptx::smem_u32(&c.full[s]), last_par[s], a0.limit_ns, nullptr);
+            // slot s was last armed in this pass of the ring if s < stage, else in the previous one
+            for (int s = 0; s < n; ++s)
+                ptx::mbar_wait(ptx::smem_u32(&c.full[s]), s < stage ? phase : phase ^ 1u, a0.limit_ns, nullptr);
         }
     } else if (MODE == kFused && warp == 3 && lane == 0) {
         // ------------------------------------------------ scheduler
         schedule_tiles(c, p, total);
-    } else if (warp == 1 && lane == 0) {
+    } else if (!F8 && warp == 1 && lane == 0) {
         // ------------------------------------------------ MMA issuer
-        int stage = 0, dq = 0;
-        uint32_t phase = 0, dq_phase = 0;
+        int stage = 0;
+        uint32_t phase = 0;
         bool ok = true;
         TileStream ts;
         ts.next_static = blockIdx.x;
@@ -703,47 +714,24 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
             const uint32_t d = tmem + (uint32_t)(acc * kTok);
             uint32_t accumulate = 0;
             const int n_micro_k = sw ? 1 : g.n_micro;
-            const int kbn = F8 ? g.k_blocks / 2 : g.k_blocks;  // stages per micro
             for (int mi = 0; ok && mi < n_micro_k; ++mi) {
-                for (int kb = 0; kb < kbn; ++kb) {
-                    if (!ptx::mbar_wait(ptx::smem_u32(&c.full[stage]), phase, g.limit_ns, &c.abort) ||
-                        (F8 && !ptx::mbar_wait(ptx::smem_u32(&c.dq_full[dq]), dq_phase, g.limit_ns, &c.abort))) {
+                for (int kb = 0; kb < g.k_blocks; ++kb) {
+                    if (!ptx::mbar_wait(ptx::smem_u32(&c.full[stage]), phase, g.limit_ns, &c.abort)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
+                    const uint64_t adesc = ptx::sw128_desc(ptx::smem_u32(stage_a(stage)));
                     const uint64_t bdesc = ptx::sw128_desc(ptx::smem_u32(stage_b(stage)));
-                    if (F8) {
-                        // A buffer dq: 8 columns per 16 K; the second 64 K pair with the second token tile
-                        const uint32_t at = tmem + (uint32_t)(kF8ACol + dq * 64);
 #pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const uint64_t bd = ptx::sw128_desc(ptx::smem_u32(stage_b(stage)) + h * kBBytes);
-#pragma unroll
-                            for (int k = 0; k < kTcBK / 16; ++k) {
-                                ptx::mma_tmem_a(d, at + 32u * h + 8u * k, bd + 2u * k, kId, accumulate);
-                                accumulate = 1;
-                            }
-                        }
-                    } else {
-                        const uint64_t adesc = ptx::sw128_desc(ptx::smem_u32(stage_a(stage)));
-#pragma unroll
-                        for (int k = 0; k < kTcBK / 16; ++k) {
-                            ptx::mma_bf16(d, adesc + 2u * k, bdesc + 2u * k, kId, accumulate);
-                            accumulate = 1;
-                        }
+                    for (int k = 0; k < kTcBK / 16; ++k) {
+                        ptx::mma_bf16(d, adesc + 2u * k, bdesc + 2u * k, kIdesc, accumulate);
+                        accumulate = 1;
                     }
                     ptx::mma_commit(ptx::smem_u32(&c.empty[stage]));
                     if (++stage == kSt) {
                         stage = 0;
                         phase ^= 1u;
-                    }
-                    if (F8) {
-                        ptx::mma_commit(ptx::smem_u32(&c.dq_empty[dq]));
-                        if (++dq == kF8Dq) {
-                            dq = 0;
-                            dq_phase ^= 1u;
-                        }
                     }
                 }
             }
@@ -752,6 +740,76 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
         if (!ok) fail(c, a0.err);
         ptx::mma_commit(ptx::smem_u32(&c.drain));
         ptx::mbar_wait(ptx::smem_u32(&c.drain), 0, a0.limit_ns, nullptr);
+    } else if (F8 && (warp == 1 || warp == 2) && lane == 0) {
+        // ------------------------------------------------ MXFP8 MMA issuers
+        // Issuer j (warp 1 + j) takes the tile's stages of parity j into half j
+        // of its accumulator; the epilogue adds the halves (half 0 + half 1,
+        // the same order on every call). With N = 16 the stream rate is set by
+        // how fast one thread issues tcgen05 instructions (eight MMAs and two
+        // commits per stage), so two issuing threads raise it.
+        const int j = warp - 1;
+        int stage = 0, dq = 0;
+        uint32_t phase = 0, dq_phase = 0;
+        bool ok = true;
+        TileStream ts;
+        ts.next_static = blockIdx.x;
+        for (int local = 0; ok; ++local) {
+            const int tile = consume_tile<MODE>(c, ts, total, a0.limit_ns);
+            if (tile < 0) break;
+            bool sw;
+            locate<MODE>(tile, c, p, sw);
+            const TcGemmArgs& g = sw ? p.g1 : p.g2;
+            const int acc = local & 1;
+            const uint32_t acc_par = (uint32_t)(local >> 1) & 1u;
+            // the accumulator is free once the epilogue read the tile two back
+            // (waited for even without own stages: the commit to tfull below must
+            // land in this tile's phase)
+            if (!ptx::mbar_wait(ptx::smem_u32(&c.tempty[acc]), acc_par ^ 1u, g.limit_ns, &c.abort)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t d = tmem + (uint32_t)(acc * 2 * kTok + j * kTok);
+            uint32_t accumulate = 0;
+            const int nk = (sw ? 1 : g.n_micro) * (g.k_blocks / 2);
+            for (int i = 0; i < nk; ++i) {
+                if ((i & 1) == j) {
+                    if (!ptx::mbar_wait(ptx::smem_u32(&c.full[stage]), phase, g.limit_ns, &c.abort) ||
+                        !ptx::mbar_wait(ptx::smem_u32(&c.dq_full[dq]), dq_phase, g.limit_ns, &c.abort)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    // A buffer dq: 8 columns per 16 K; the second 64 K pair with the second token tile
+                    const uint32_t at = tmem + (uint32_t)(kF8ACol + dq * 64);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        // the second 64-K tile starts after the first one's brows rows
+                        const uint64_t bd = ptx::sw128_desc(ptx::smem_u32(stage_b(stage)) + h * p.brows * 128);
+#pragma unroll
+                        for (int k = 0; k < kTcBK / 16; ++k) {
+                            ptx::mma_tmem_a(d, at + 32u * h + 8u * k, bd + 2u * k, kIdescF16, accumulate);
+                            accumulate = 1;
+                        }
+                    }
+                    ptx::mma_commit(ptx::smem_u32(&c.empty[stage]));
+                    ptx::mma_commit(ptx::smem_u32(&c.dq_empty[dq]));
+                }
+                if (++stage == kSt) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+                if (++dq == kF8Dq) {
+                    dq = 0;
+                    dq_phase ^= 1u;
+                }
+            }
+            if (ok) ptx::mma_commit(ptx::smem_u32(&c.tfull[acc]));
+        }
+        if (!ok) fail(c, a0.err);
+        uint64_t* dr = j ? &c.drain2 : &c.drain;
+        ptx::mma_commit(ptx::smem_u32(dr));
+        ptx::mbar_wait(ptx::smem_u32(dr), 0, a0.limit_ns, nullptr);
     } else if (F8 && warp >= 8) {
         // ------------------------------------------------ MXFP8 dequant
         // warp 8 + 4 j + q owns TMEM lanes 32 q .. 32 q + 31 (weight rows, one
@@ -789,14 +847,11 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
                     uint4 cv[8];
 #pragma unroll
                     for (int j = 0; j < 8; ++j) cv[j] = *reinterpret_cast<const uint4*>(row + ((j ^ (r & 7)) << 4));
-                    // scales: SwiGLU tiles [4][64] for the gate rows, then [4][64] for the up
-                    // rows; down tiles [4][128]
+                    // scales [4][128 rows] (SwiGLU tiles: each block's 64 gate rows, then its 64 up rows)
                     const unsigned char* sp = stage_s(stage);
-                    const int so = sw ? (r >> 6) * (kF8ScaleBytes / 2) + (r & 63) : r;
-                    const int sstep = sw ? 64 : kM;
                     int sc[4];
 #pragma unroll
-                    for (int b = 0; b < 4; ++b) sc[b] = sp[so + b * sstep];
+                    for (int b = 0; b < 4; ++b) sc[b] = sp[b * kM + r];
                     bool slow = false;
 #pragma unroll
                     for (int b = 0; b < 4; ++b) slow |= !dequant_in_f16(sc[b]);
@@ -864,7 +919,18 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
             }
             ptx::tc_fence_after();
             uint32_t v[kTok];
-            ptx::tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kTok), v);
+            if (F8) {
+                // two halves (the tile's even and odd stages); a tile of one stage
+                // filled only half 0
+                uint32_t v2[2 * kTok];
+                ptx::tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * 2 * kTok), v2);
+                const bool both = (sw ? 1 : g.n_micro) * (g.k_blocks / 2) >= 2;
+#pragma unroll
+                for (int jj = 0; jj < kTok; ++jj)
+                    v[jj] = both ? __float_as_uint(__uint_as_float(v2[jj]) + __uint_as_float(v2[kTok + jj])) : v2[jj];
+            } else {
+                ptx::tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kTok), v);
+            }
             // the accumulator is in registers: hand it back to the MMA issuer
             ptx::tc_fence_before();
             __syncwarp();
@@ -912,6 +978,7 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
     ptx::tc_fence_before();
     __syncthreads();
     if (warp == 2) {
+        __syncwarp();  // lane 0 ran the second MMA issuer (MXFP8)
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, F8 ? kF8TmemCols : kTmemCols);
     }
@@ -996,7 +1063,8 @@ cudaError_t launch_tc_small_fused(const TcGemmArgs& g1, const CUtensorMap& tmX1,
 cudaError_t launch_tc_small_fused_mxfp8(const TcGemmArgs& g1, const CUtensorMap& tmX1, const CUtensorMap* tmW1,
                                         const CUtensorMap* tmS1, const TcGemmArgs& g2, const CUtensorMap& tmX2,
                                         const CUtensorMap* tmW2, const CUtensorMap* tmS2, const FinalizeArgs& fin,
-                                        const GatherArgs& gat, int* done, int num_sms, cudaStream_t s) {
+                                        const GatherArgs& gat, int brows, int* done, int num_sms,
+                                        cudaStream_t s) {
     SmallMaps maps{};
     fill_maps(maps, tmX1, tmW1, g1.n_micro, true);
     fill_maps(maps, tmX2, tmW2, g2.n_micro, false);
@@ -1004,7 +1072,7 @@ cudaError_t launch_tc_small_fused_mxfp8(const TcGemmArgs& g1, const CUtensorMap&
         maps.s1[i] = tmS1[i < g1.n_micro ? i : 0];
         maps.s2[i] = tmS2[i < g2.n_micro ? i : 0];
     }
-    SmallParams p{g1, g2, done, fin, gat.x, gat.xp, gat.perm, gat.k, (int)gat.row_bytes};
+    SmallParams p{g1, g2, done, fin, gat.x, gat.xp, gat.perm, gat.k, (int)gat.row_bytes, brows};
     return launch_small<kFused, true>(maps, p, g1.max_tiles + g2.max_tiles, num_sms, s);
 }
 

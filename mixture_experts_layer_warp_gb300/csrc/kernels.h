@@ -168,14 +168,17 @@ cudaError_t launch_tc_small_down(const TcGemmArgs& a, const CUtensorMap& tmX, co
 // gathers xp from x (gat.x non-null). done[fused_counter_ints(E)] must be zero
 // at launch (the small-batch router zeroes it).
 inline int fused_counter_ints(int E) { return 3 * E + 2; }
-// The same with MXFP8 expert weights: tmW1[m] / tmW2[m] map the uint8 E4M3
-// codes (boxes {64, 64} / {64, 128}), tmS1[m] the w13 scales [E*H/32][2I]
-// (box {64, 2}), tmS2[m] the w2 scales [E*I/32][H] (box {128, 2}); gat.xp and
-// g1.out (h) hold f16.
+// The same with MXFP8 expert weights: tmX1 / tmX2 map the f16 token rows as
+// 3D maps {64, rows, K/64} with box {64, brows, 2} (brows = 8 when the batch
+// has at most 8 tokens, else 16), tmW1[m] the w13 E4M3 codes as a 3D map
+// {H, I, 2E} with box {128, 64, 2} (gate rows, then the matching up rows),
+// tmW2[m] the w2 codes [E*H][I] (box {128, 128}), tmS1[m] the w13 scales as a
+// 3D map {I, 2, E*H/32} with box {64, 2, 4}, tmS2[m] the w2 scales
+// [E*I/32][H] (box {128, 4}); gat.xp and g1.out (h) hold f16.
 cudaError_t launch_tc_small_fused_mxfp8(const TcGemmArgs& g1, const CUtensorMap& tmX1, const CUtensorMap* tmW1,
                                         const CUtensorMap* tmS1, const TcGemmArgs& g2, const CUtensorMap& tmX2,
                                         const CUtensorMap* tmW2, const CUtensorMap* tmS2, const FinalizeArgs& fin,
-                                        const GatherArgs& gat, int* done, int num_sms, cudaStream_t s);
+                                        const GatherArgs& gat, int brows, int* done, int num_sms, cudaStream_t s);
 cudaError_t launch_tc_small_fused(const TcGemmArgs& g1, const CUtensorMap& tmX1, const CUtensorMap* tmW1,
                                   const TcGemmArgs& g2, const CUtensorMap& tmX2, const CUtensorMap* tmW2,
                                   const FinalizeArgs& fin, const GatherArgs& gat, int* done, int num_sms,
@@ -254,6 +257,10 @@ bool encode_bf16_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t r
 // or with the 128-byte swizzle (16-byte chunk c of row r at chunk c ^ (r % 8)).
 bool encode_u8_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
                   uint32_t box_inner, uint32_t box_rows, bool swizzle128);
+// 3D map (bf16 or uint8 elements): dims[0] innermost, strides in bytes of dims
+// 1 and 2, box in elements; unswizzled or with the 128-byte swizzle.
+bool encode_3d(CUtensorMap* m, bool bf16, const void* base, const uint64_t dims[3], const uint64_t strides[2],
+               const uint32_t box[3], bool swizzle128);
 // MXFP8 quantisation (mxfp8.cu): w [groups][rows][cols] bf16 -> codes [groups][rows][cols],
 // scales [groups][cols/32][rows]; cols % 32 == 0.
 cudaError_t launch_mx_quantize(const void* w, int64_t groups, int rows, int cols, void* codes, void* scales,

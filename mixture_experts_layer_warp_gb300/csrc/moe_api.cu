@@ -269,18 +269,29 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
         // router zeroed h->done); the shared expert's GEMMs ran first
         FinalizeArgs fin{h->obuf, h->inv, h->topw, Is > 0 ? h->sbuf : nullptr, T, k, H, true, y, h->accumulate};
         if (mx != nullptr) {
-            // MXFP8: the code and scale maps replace the bf16 weight maps
-            CUtensorMap c1[kMaxMicro], c2[kMaxMicro], s1[kMaxMicro], s2[kMaxMicro];
+            // MXFP8: the code and scale maps replace the bf16 weight maps; one
+            // box per stage and operand (3D maps: w13's gate and up rows, their
+            // scales, and the two 64-K chunks of 16 token rows)
+            CUtensorMap c1[kMaxMicro], c2[kMaxMicro], s1[kMaxMicro], s2[kMaxMicro], mX, mX2;
+            const uint64_t xd[3] = {64, (uint64_t)R, (uint64_t)H / 64}, xs[2] = {(uint64_t)H * 2, 128};
+            const uint64_t hd[3] = {64, (uint64_t)R, (uint64_t)M * I / 64}, hs[2] = {(uint64_t)M * I * 2, 128};
+            const int brows = T <= 8 ? 8 : kSmallTokens;  // no expert owns more routes than T
+            const uint32_t xb[3] = {64, (uint32_t)brows, 2};
+            if (!encode_3d(&mX, true, h->xp, xd, xs, xb, true) || !encode_3d(&mX2, true, h->hbuf, hd, hs, xb, true))
+                return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (MXFP8 token rows)");
+            const uint64_t cd[3] = {(uint64_t)H, (uint64_t)I, 2 * (uint64_t)E}, cs[2] = {(uint64_t)H, (uint64_t)I * H};
+            const uint32_t cb[3] = {128, 64, 2};
+            const uint64_t sd[3] = {(uint64_t)I, 2, (uint64_t)E * (H / 32)}, ss[2] = {(uint64_t)I, 2 * (uint64_t)I};
+            const uint32_t sb[3] = {64, 2, 4};
             for (int m = 0; m < M; ++m)
-                if (!encode_u8_2d(&c1[m], w13[m], H, (uint64_t)E * 2 * I, (uint64_t)H, 128, 64, true) ||
+                if (!encode_3d(&c1[m], false, w13[m], cd, cs, cb, true) ||
                     !encode_u8_2d(&c2[m], w2[m], I, (uint64_t)E * H, (uint64_t)I, 128, 128, true) ||
-                    !encode_u8_2d(&s1[m], mx->w13[m], 2 * (uint64_t)I, (uint64_t)E * (H / 32), 2 * (uint64_t)I, 64, 4,
-                                  false) ||
+                    !encode_3d(&s1[m], false, mx->w13[m], sd, ss, sb, false) ||
                     !encode_u8_2d(&s2[m], mx->w2[m], H, (uint64_t)E * (I / 32), (uint64_t)H, 128, 4, false))
                     return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (MXFP8 weights, micro %d)", m);
             if ((e = timed(h, kSlotGemm1, s, [&] {
                      GatherArgs gat{x, h->perm, (int)R, k, (uint32_t)(H * 2), h->xp, h->err, h->limit_ns, h->num_sms};
-                     return launch_tc_small_fused_mxfp8(g1, tmX, c1, s1, g2, tmX2, c2, s2, fin, gat, h->done,
+                     return launch_tc_small_fused_mxfp8(g1, mX, c1, s1, g2, mX2, c2, s2, fin, gat, brows, h->done,
                                                         h->num_sms, s);
                  })) != cudaSuccess)
                 return cuda_err(h, e, "fused MXFP8 GEMM launch");
