@@ -277,7 +277,7 @@ def roofline_of(wl, prof, ids_pool, steps, peaks, sha, mxfp8=False):
                 "shared_gemm1": 4 * wl.T * H * wl.shared_inter,
                 "shared_gemm2": 2 * wl.T * H * wl.shared_inter}.get(dom)
         achieved = algo / per_launch_s / 1e12 if algo else None
-    traffic = None if mxfp8 else recorded_traffic(wl.name, dom, sha)
+    traffic = recorded_traffic(wl.name + ("_mxfp8" if mxfp8 else ""), dom, sha)
     return {"kernel": dom + ("+gemm2_down+finalize (one launch)" if fused and dom == "gemm1_swiglu" else ""),
             "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
             "frac": (achieved / peak) if achieved else None, "traffic": traffic,
