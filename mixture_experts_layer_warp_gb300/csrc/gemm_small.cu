@@ -153,7 +153,7 @@ struct SmallParams {
 struct SmallMaps {
     CUtensorMap x1;      // SwiGLU token rows [R][H], box {64, 16} (MXFP8: 3D {64, R, H/64}, box {64, 16, 2})
     CUtensorMap x2;      // down token rows (h) [R][M*I], box {64, 16} (MXFP8: 3D as x1)
-    CUtensorMap w1[kMaxMicro];  // w13[m] [E*2I][H], box {64, 64} (MXFP8: uint8 codes, 3D {H, I, 2E}, box {128, 64, 2})
+    CUtensorMap w1[kMaxMicro];  // w13[m] 3D {H, I, 2E}, box {64, 64, 2} (MXFP8: uint8 codes, box {128, 64, 2})
     CUtensorMap w2[kMaxMicro];  // w2[m] [E*H][I], box {64, 128} (MXFP8: uint8 codes, box {128, 128})
     CUtensorMap s1[kMaxMicro];  // MXFP8: w13[m] scales 3D {I, 2, E*H/32}, box {64, 2, 4}: [4][gate, up][64]
     CUtensorMap s2[kMaxMicro];  // MXFP8: w2[m] scales [E*I/32][H] uint8, box {128, 4}: [4][128]
@@ -634,9 +634,8 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
                             ptx::tma_load_2d(ss, tsc, t.nt * kM, srow, fb);
                         }
                     } else if (sw) {
-                        ptx::tma_load_2d_hint(sa, tw, kb * kTcBK, wrow, fb, wpol);            // 64 gate rows
-                        ptx::tma_load_2d_hint(sa + kABytes / 2, tw, kb * kTcBK, wrow + g.up_offset, fb,
-                                              wpol);                                           // 64 up rows
+                        // 64 gate rows, then the 64 matching up rows (half 2g + 1 of the 3D map)
+                        ptx::tma_load_3d_hint(sa, tw, kb * kTcBK, t.nt * 64, 2 * t.g, fb, wpol);
                     } else {
                         ptx::tma_load_2d_hint(sa, tw, kb * kTcBK, wrow, fb, wpol);            // 128 rows
                     }

@@ -9,7 +9,8 @@
 // Two kernels from one template:
 //   SwiGLU (GEMM1): a tile is (micro m, expert e, 128 rows, 128 columns of h).
 //       Each K stage loads the gate rows [nt*128, +128) and the up rows
-//       [I + nt*128, +128) of w13[m][e] into one 256-row B tile, so a single
+//       [I + nt*128, +128) of w13[m][e] into one 256-row B tile (one box of a
+//       3D map {H, I, 2E}), so a single
 //       M=128 x N=256 MMA fills gate (TMEM columns 0-127) and up (128-255)
 //       side by side; the epilogue writes silu(gate) * up as bf16.
 //   down (GEMM2): a tile is (expert e, 128 rows, 256 output columns). The K
@@ -37,7 +38,6 @@ constexpr int kStages = 4;
 constexpr int kBN = 256;                           // MMA N
 constexpr int kABytes = kTcBM * kTcBK * 2;         // 16 KB
 constexpr int kBBytes = kBN * kTcBK * 2;           // 32 KB
-constexpr int kHalfB = 128 * kTcBK * 2;            // one 128-row box, 16 KB
 constexpr int kStageBytes = kABytes + kBBytes;     // 48 KB
 constexpr int kTmemCols = 2 * kBN;                 // two accumulators
 constexpr int kThreads = 256;
@@ -130,8 +130,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int mi = 0; ok && mi < n_micro_k; ++mi) {
                 const int m = SWIGLU ? t.m : mi;
                 const CUtensorMap* tb = pick_map(m, tmB0, tmB1, tmB2, tmB3);
-                const int brow = t.g * a.b_rows_per_group + t.nt * (SWIGLU ? 128 : kBN);
-                const int brow2 = brow + (SWIGLU ? a.up_offset : 128);
+                const int brow = t.g * a.b_rows_per_group + t.nt * kBN;  // down tiles
                 for (int kb = 0; kb < a.k_blocks; ++kb) {
                     if (!ptx::mbar_wait(ptx::smem_u32(&c.empty[stage]), phase ^ 1u, a.limit_ns, &c.abort)) {
                         ok = false;
@@ -143,8 +142,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::mbar_arrive_expect_tx(fb, kStageBytes);
                     const int ka = (SWIGLU ? 0 : m * a.a_micro_cols) + kb * kTcBK;
                     ptx::tma_load_2d(sa, &tmA, ka, t.row0, fb);
-                    ptx::tma_load_2d(sb, tb, kb * kTcBK, brow, fb);
-                    ptx::tma_load_2d(sb + kHalfB, tb, kb * kTcBK, brow2, fb);
+                    // one box per operand: the TMA instructions, not the bytes, set the
+                    // producer's pace (SwiGLU: 128 gate rows, then the matching up
+                    // rows, as half 2g + 1 of the 3D map; down: 256 rows)
+                    if (SWIGLU)
+                        ptx::tma_load_3d(sb, tb, kb * kTcBK, t.nt * 128, 2 * t.g, fb);
+                    else
+                        ptx::tma_load_2d(sb, tb, kb * kTcBK, brow, fb);
                     last_par[stage] = phase;
                     ++issued;
                     if (++stage == kStages) {

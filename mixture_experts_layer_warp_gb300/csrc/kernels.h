@@ -145,7 +145,9 @@ struct TcGemmArgs {
     uint64_t limit_ns;
     int dense_rows;           // rows of the dense segment when seg is null
 };
-// tmA: A [rows][K] bf16, box {64, 128}; tmB[m]: B_m [G*b_rows][K] bf16, box {64, 128}.
+// tmA: A [rows][K] bf16, box {64, 128}. tmB[m]: SwiGLU: w13_m [G][2I][K] bf16 as a
+// 3D map {K, I, 2G} with box {64, 128, 2} (128 gate rows and the matching up rows);
+// down: B_m [G*b_rows][K] bf16, box {64, 256}.
 cudaError_t launch_tc_gemm_swiglu(const TcGemmArgs& a, const CUtensorMap& tmA, const CUtensorMap* tmB,
                                   int num_sms, cudaStream_t s);
 cudaError_t launch_tc_gemm_down(const TcGemmArgs& a, const CUtensorMap& tmA, const CUtensorMap* tmB,
@@ -154,7 +156,8 @@ cudaError_t launch_tc_gemm_down(const TcGemmArgs& a, const CUtensorMap& tmA, con
 // Swapped-operand variants for batches of at most kSmallTokens tokens (every
 // expert then owns at most kSmallTokens routes): weights on the MMA M side,
 // tokens on N. tmX: activations [rows][K], box {64, 16}; tmW[m]: weights,
-// box {64, 64} (SwiGLU form: gate and up halves) or {64, 128} (down form).
+// a 3D map {K, I, 2G} with box {64, 64, 2} (SwiGLU form: 64 gate rows and the
+// matching up rows) or box {64, 128} (down form).
 // n_tiles counts 64 h-columns (SwiGLU) or 128 output columns (down).
 cudaError_t launch_tc_small_swiglu(const TcGemmArgs& a, const CUtensorMap& tmX, const CUtensorMap* tmW,
                                    int num_sms, cudaStream_t s);

@@ -120,6 +120,22 @@ bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, 
     return encode_bf16_2d(m, base, inner, rows, row_bytes, kTcBM);
 }
 
+// The GEMMs' weight operands, one box per K stage: w13 [G][2I][H] as a 3D map
+// {H, I, 2G} whose box {64, rows, 2} is `rows` gate rows and the matching up
+// rows (128 for the large GEMM, 64 for the small-batch one); w2 [rows][K] with
+// 256-row boxes for the large GEMM.
+bool encode_w13(CUtensorMap* m, const void* w13, uint64_t H, uint64_t I, uint64_t G, uint32_t rows) {
+    const uint64_t dims[3] = {H, I, 2 * G}, strides[2] = {H * 2, I * H * 2};
+    const uint32_t box[3] = {(uint32_t)kTcBK, rows, 2};
+    return encode_3d(m, true, w13, dims, strides, box, true);
+}
+bool encode_w13_tc(CUtensorMap* m, const void* w13, uint64_t H, uint64_t I, uint64_t G) {
+    return encode_w13(m, w13, H, I, G, 128);
+}
+bool encode_w2_tc(CUtensorMap* m, const void* w2, uint64_t K, uint64_t rows) {
+    return encode_bf16_2d(m, w2, K, rows, K * 2, 256);
+}
+
 void hook_before(void* ctx, int slot, cudaStream_t s) {
     moe_handle* h = static_cast<moe_handle*>(ctx);
     if (h->prof_on && h->prof_calls < h->prof_max)
@@ -203,14 +219,14 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
         const cudaStream_t ss = h->side;
         CUtensorMap sA, sB[kMaxMicro];
         const int stiles = (T + kTcBM - 1) / kTcBM;
-        if (!encode_2d(&sA, x, H, T, (uint64_t)H * 2) || !encode_2d(&sB[0], sw13, H, 2 * (uint64_t)Is, (uint64_t)H * 2))
+        if (!encode_2d(&sA, x, H, T, (uint64_t)H * 2) || !encode_w13_tc(&sB[0], sw13, H, Is, 1))
             return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (shared GEMM1)");
         TcGemmArgs s1{nullptr, nullptr, 1, 1, H / kTcBK, Is / 128, 2 * Is, Is, 0,
                       h->hs, (int64_t)Is, 0, stiles * (Is / 128), h->err, h->limit_ns, T};
         if ((e = timed(h, kSlotSharedGemm1, ss, [&] { return launch_tc_gemm_swiglu(s1, sA, sB, h->num_sms, ss); })) !=
             cudaSuccess)
             return cuda_err(h, e, "shared GEMM1 launch");
-        if (!encode_2d(&sA, h->hs, Is, T, (uint64_t)Is * 2) || !encode_2d(&sB[0], sw2, Is, H, (uint64_t)Is * 2))
+        if (!encode_2d(&sA, h->hs, Is, T, (uint64_t)Is * 2) || !encode_w2_tc(&sB[0], sw2, Is, H))
             return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (shared GEMM2)");
         TcGemmArgs s2{nullptr, nullptr, 1, 1, Is / kTcBK, H / 256, H, 0, Is,
                       h->sbuf, (int64_t)H, 0, stiles * (H / 256), h->err, h->limit_ns, T};
@@ -234,7 +250,7 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
         if (!encode_bf16_2d(&tmX, h->xp, H, R, (uint64_t)H * 2, kSmallTokens))
             return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (xp)");
         for (int m = 0; m < M && mx == nullptr; ++m)
-            if (!encode_bf16_2d(&tmW[m], w13[m], H, (uint64_t)E * 2 * I, (uint64_t)H * 2, 64))
+            if (!encode_w13(&tmW[m], w13[m], H, I, E, 64))
                 return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (w13[%d])", m);
         TcGemmArgs g1{h->offsets, h->tiles_tc, E, M, H / kTcBK, I / 64, 2 * I, I, 0,
                       h->hbuf, (int64_t)M * I, I, active * M * (I / 64), h->err, h->limit_ns};
@@ -249,7 +265,7 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
         if (Is > 0) {
             CUtensorMap sX, sW[1];
             if (!encode_bf16_2d(&sX, x, H, T, (uint64_t)H * 2, kSmallTokens) ||
-                !encode_bf16_2d(&sW[0], sw13, H, 2 * (uint64_t)Is, (uint64_t)H * 2, 64))
+                !encode_w13(&sW[0], sw13, H, Is, 1, 64))
                 return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (shared GEMM1)");
             TcGemmArgs s1{h->shared_meta, h->shared_meta + 2, 1, 1, H / kTcBK, Is / 64, 2 * Is, Is, 0,
                           h->hs, (int64_t)Is, 0, Is / 64, h->err, h->limit_ns};
@@ -308,7 +324,7 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
         if (!encode_2d(&tmA, h->xp, H, R, (uint64_t)H * 2))
             return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (xp)");
         for (int m = 0; m < M; ++m)
-            if (!encode_2d(&tmB[m], w13[m], H, (uint64_t)E * 2 * I, (uint64_t)H * 2))
+            if (!encode_w13_tc(&tmB[m], w13[m], H, I, E))
                 return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (w13[%d])", m);
         TcGemmArgs g1{h->offsets, h->tiles_tc, E, M, H / kTcBK, I / 128, 2 * I, I, 0,
                       h->hbuf, (int64_t)M * I, I, M * routed_tiles_tc * (I / 128), h->err, h->limit_ns};
@@ -318,7 +334,7 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
         if (!encode_2d(&tmA, h->hbuf, (uint64_t)M * I, R, (uint64_t)M * I * 2))
             return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (h)");
         for (int m = 0; m < M; ++m)
-            if (!encode_2d(&tmB[m], w2[m], I, (uint64_t)E * H, (uint64_t)I * 2))
+            if (!encode_w2_tc(&tmB[m], w2[m], I, (uint64_t)E * H))
                 return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (w2[%d])", m);
         TcGemmArgs g2{h->offsets, h->tiles_tc, E, M, I / kTcBK, H / 256, H, 0, I,
                       h->obuf, (int64_t)H, 0, routed_tiles_tc * (H / 256), h->err, h->limit_ns};
@@ -326,13 +342,13 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
             return cuda_err(h, e, "GEMM2 launch");
         if (Is > 0 && !fork) {
             const int stiles = (T + kTcBM - 1) / kTcBM;
-            if (!encode_2d(&tmA, x, H, T, (uint64_t)H * 2) || !encode_2d(&tmB[0], sw13, H, 2 * (uint64_t)Is, (uint64_t)H * 2))
+            if (!encode_2d(&tmA, x, H, T, (uint64_t)H * 2) || !encode_w13_tc(&tmB[0], sw13, H, Is, 1))
                 return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (shared GEMM1)");
             TcGemmArgs s1{h->shared_meta, h->shared_meta + 2, 1, 1, H / kTcBK, Is / 128, 2 * Is, Is, 0,
                           h->hs, (int64_t)Is, 0, stiles * (Is / 128), h->err, h->limit_ns};
             if ((e = timed(h, kSlotSharedGemm1, s, [&] { return launch_tc_gemm_swiglu(s1, tmA, tmB, h->num_sms, s); })) != cudaSuccess)
                 return cuda_err(h, e, "shared GEMM1 launch");
-            if (!encode_2d(&tmA, h->hs, Is, T, (uint64_t)Is * 2) || !encode_2d(&tmB[0], sw2, Is, H, (uint64_t)Is * 2))
+            if (!encode_2d(&tmA, h->hs, Is, T, (uint64_t)Is * 2) || !encode_w2_tc(&tmB[0], sw2, Is, H))
                 return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (shared GEMM2)");
             TcGemmArgs s2{h->shared_meta, h->shared_meta + 2, 1, 1, Is / kTcBK, H / 256, H, 0, Is,
                           h->sbuf, (int64_t)H, 0, stiles * (H / 256), h->err, h->limit_ns};
