@@ -104,7 +104,10 @@ struct GatherArgs {
     int* err;
     uint64_t limit_ns;
     int num_sms;
+    const int32_t* inv;       // [R] inverse of perm (launch_gather)
 };
+// xp[inv[t*k + j]] = x[t] for every token t and slot j: each row of x is read
+// once and written to its k routes' positions.
 cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s);
 
 // ------------------------------------------------------------ finalize

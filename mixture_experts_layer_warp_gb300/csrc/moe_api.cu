@@ -237,7 +237,7 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
     }
 
     if (!small_bf16) {  // small bf16 batches gather inside the fused GEMM launch
-        GatherArgs ga{x, h->perm, (int)R, k, (uint32_t)(H * h->esz), h->xp, h->err, h->limit_ns, h->num_sms};
+        GatherArgs ga{x, h->perm, (int)R, k, (uint32_t)(H * h->esz), h->xp, h->err, h->limit_ns, h->num_sms, h->inv};
         if ((e = timed(h, kSlotGather, s, [&] { return launch_gather(ga, s); })) != cudaSuccess)
             return cuda_err(h, e, "gather launch");
     }

@@ -95,47 +95,50 @@ __global__ void __launch_bounds__(kPlaceWarps * 32) place_kernel(PlaceArgs a) {
     place_chunk<kPlaceWarps>(sid, n, r0, a.E, R, [&](int e) { return base[e]; }, cnt, run, a.perm, a.inv, a.err);
 }
 
-// Gather xp[i] = x[perm[i] / k]: each single-warp block moves one row chunk
-// at a time global -> shared -> global with bulk (TMA engine) copies; many
-// blocks per SM keep enough bytes in flight to stream at HBM rate.
-constexpr uint32_t kGatherChunk = 16384;
+// The gather xp[i] = x[perm[i] / k], run as the equivalent scatter
+// xp[inv[t*k + j]] = x[t]: one warp per token reads its row once (16-byte
+// vector loads on the read-only path, four per lane in flight) and writes it
+// to its k routes' rows. Read in route order, every row of x would be fetched
+// k times, from DRAM once x outgrows L2.
+constexpr int kGatherThreads = 256;
+constexpr int kGatherUnroll = 4;
 
-__global__ void __launch_bounds__(32) gather_kernel(GatherArgs a) {
-    __shared__ __align__(128) unsigned char buf[kGatherChunk];
-    __shared__ __align__(8) uint64_t bar;
-    if (threadIdx.x != 0) return;
-    const uint32_t sbuf = ptx::smem_u32(buf), sbar = ptx::smem_u32(&bar);
-    ptx::mbar_init(sbar, 1);
-    ptx::fence_mbar_init();
-    const uint32_t chunks = (a.row_bytes + kGatherChunk - 1) / kGatherChunk;
-    const int64_t units = (int64_t)a.R * chunks;
-    const unsigned char* x = static_cast<const unsigned char*>(a.x);
-    unsigned char* xp = static_cast<unsigned char*>(a.xp);
-    uint32_t phase = 0;
-    for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
-        const int64_t i = u / chunks;
-        const uint32_t c = (uint32_t)(u - i * chunks);
-        const uint32_t bytes = min(kGatherChunk, a.row_bytes - c * kGatherChunk);
-        const int32_t r = a.perm[i];
-        if (r < 0 || r >= a.R) {
-            atomicOr(a.err, kErrCheck);
+__device__ __forceinline__ uint4 ld_nc_v4(const uint4* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int64_t T = a.R / a.k;
+    const int64_t nwarps = ((int64_t)gridDim.x * kGatherThreads) >> 5;
+    const int nvec = (int)(a.row_bytes / 16);
+    const uint4* __restrict__ x = static_cast<const uint4*>(a.x);
+    uint4* __restrict__ xp = static_cast<uint4*>(a.xp);
+    for (int64_t t = ((int64_t)blockIdx.x * kGatherThreads + threadIdx.x) >> 5; t < T; t += nwarps) {
+        // lane j < k holds the row of route t*k + j
+        const int dst = lane < a.k ? a.inv[t * a.k + lane] : 0;
+        if (__any_sync(0xffffffffu, dst < 0 || dst >= a.R)) {
+            if (lane == 0) atomicOr(a.err, kErrCheck);
             continue;
         }
-        const int64_t t = r / a.k;
-        ptx::bulk_wait_read_all();  // the previous store has finished reading buf
-        ptx::mbar_arrive_expect_tx(sbar, bytes);
-        ptx::bulk_g2s(sbuf, x + t * a.row_bytes + (int64_t)c * kGatherChunk, bytes, sbar);
-        if (!ptx::mbar_wait(sbar, phase, a.limit_ns, nullptr)) {
-            atomicOr(a.err, kErrTimeout);
-            ptx::mbar_wait(sbar, phase, a.limit_ns, nullptr);  // let the copy land before exit
-            break;
+        const uint4* src = x + t * nvec;
+        for (int v = lane; v < nvec; v += 32 * kGatherUnroll) {
+            uint4 buf[kGatherUnroll];
+#pragma unroll
+            for (int u = 0; u < kGatherUnroll; ++u)
+                if (v + 32 * u < nvec) buf[u] = ld_nc_v4(src + v + 32 * u);
+            for (int j = 0; j < a.k; ++j) {
+                uint4* out = xp + (int64_t)__shfl_sync(0xffffffffu, dst, j) * nvec;
+#pragma unroll
+                for (int u = 0; u < kGatherUnroll; ++u)
+                    if (v + 32 * u < nvec) out[v + 32 * u] = buf[u];
+            }
         }
-        phase ^= 1u;
-        ptx::fence_proxy_async_smem();
-        ptx::bulk_s2g(xp + i * a.row_bytes + (int64_t)c * kGatherChunk, sbuf, bytes);
-        ptx::bulk_commit();
     }
-    ptx::bulk_wait_all();
 }
 
 }  // namespace
@@ -153,10 +156,10 @@ cudaError_t launch_place(const PlaceArgs& a, cudaStream_t s) {
 
 cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s) {
     if (a.R == 0) return cudaSuccess;
-    const int64_t chunks = (a.row_bytes + kGatherChunk - 1) / kGatherChunk;
-    const int64_t units = (int64_t)a.R * chunks;
-    const int64_t grid = std::min<int64_t>(units, (int64_t)a.num_sms * 12);
-    gather_kernel<<<(unsigned)grid, 32, 0, s>>>(a);
+    constexpr int kWarps = kGatherThreads / 32;
+    const int64_t T = a.R / a.k;
+    const int64_t grid = std::min<int64_t>((T + kWarps - 1) / kWarps, (int64_t)a.num_sms * 8);
+    gather_kernel<<<(unsigned)grid, kGatherThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 
