@@ -68,8 +68,9 @@ constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kM, kTok);
 // 128 codes into f16, code * 2^(S-127) rounded to f16, in registers and store
 // them into one of kF8Dq A buffers in tensor memory; the MMA reads A from
 // tensor memory and the token rows (f16: the gathered rows and h) from shared
-// memory, into fp32 accumulators as before. No dequantised tile passes through
-// shared memory.
+// memory, into fp32 accumulators as before; two threads issue the MMAs (a
+// tile's even and odd stages, into two accumulator halves the epilogue adds).
+// No dequantised tile passes through shared memory.
 constexpr int kF8Stages = 10;
 constexpr int kF8K = 2 * kTcBK;                      // 128 K per stage
 constexpr int kF8CodeBytes = kM * kF8K;              // 16 KB of codes
