@@ -59,11 +59,14 @@ constexpr int kThreads = 256;
 constexpr int kGatherCtas = 128;               // kFused: CTAs that gather token rows
 constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kM, kTok);
 
-// MXFP8 expert weights (fused mode, moe_forward_mxfp8): a stage covers 128 K
-// (twice the bf16 stage's K), so each weight row moves 128 contiguous bytes of
-// E4M3 codes per stage, as a bf16 row does (a 64-byte row per TMA box halves
-// the sustained stream rate); the codes arrive 128-byte swizzled with the four
-// E8M0 scales of each row and two token-row tiles. Eight dequant warps (8..15:
+// MXFP8 expert weights (fused mode, moe_forward_mxfp8): a stage covers 256 K
+// as two 128-K code chunks, so each weight row moves 128 contiguous bytes of
+// E4M3 codes per TMA row (a 64-byte row halves the sustained stream rate) and
+// a stage is three TMA instructions for 32 KB of codes (the producer thread's
+// TMA issue, about as slow per instruction whatever the box, bounds the stream
+// otherwise); the codes arrive 128-byte swizzled with the eight E8M0 scales of
+// each row and four 64-K token-row tiles. A layer whose K is an odd multiple of
+// 128 ends with half a stage: the boxes past the weights read zero codes. Eight dequant warps (8..15:
 // two per TMEM lane quadrant, taking alternate stages) turn each weight row's
 // 128 codes into f16, code * 2^(S-127) rounded to f16, in registers and store
 // them into one of kF8Dq A buffers in tensor memory; the MMA reads A from
@@ -71,22 +74,26 @@ constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kM, kTok);
 // memory, into fp32 accumulators as before; two threads issue the MMAs (a
 // tile's even and odd stages, into two accumulator halves the epilogue adds).
 // No dequantised tile passes through shared memory.
-constexpr int kF8Stages = 10;
-constexpr int kF8K = 2 * kTcBK;                      // 128 K per stage
-constexpr int kF8CodeBytes = kM * kF8K;              // 16 KB of codes
-constexpr int kF8ScaleBytes = kM * (kF8K / 32);      // 512 B of scales
-constexpr int kF8BBytes = 2 * kBBytes;               // two 64-K token-row tiles
-constexpr int kF8Dq = 4;                             // even: buffer parity = stage parity
+constexpr int kF8Stages = 5;
+constexpr int kF8Chunks = 4;                         // 64-K MMA chunks per stage
+constexpr int kF8K = kF8Chunks * kTcBK;              // 256 K per stage
+constexpr int kF8CodeBytes = kM * kF8K;              // 32 KB of codes: two [128 rows][128 K] chunks
+constexpr int kF8ScaleBytes = kM * (kF8K / 32);      // 1 KB of scales
+constexpr int kF8BBytes = kF8Chunks * kBBytes;       // four 64-K token-row tiles
+constexpr int kF8Dq = 3;                             // TMEM A buffers
 constexpr int kF8Threads = 512;                      // warps 8..15 dequantise
 constexpr int kF8CodeOff = kF8Stages * kF8BBytes;    // after the token-row tiles (1024-aligned)
 constexpr int kF8ScaleOff = kF8CodeOff + kF8Stages * kF8CodeBytes;
 constexpr int kF8CtlOff = kF8ScaleOff + kF8Stages * kF8ScaleBytes;
 constexpr int kF8TmemCols = 512;                     // accumulators at 0..63, A buffers from kF8ACol
-constexpr int kF8ACol = 64;                          // A buffer b: columns kF8ACol + 64 b .. + 63
+constexpr int kF8ACol = 64;                          // A buffer b: columns kF8ACol + kF8ABuf b ..
+constexpr int kF8ABuf = kF8K / 2;                    // 128 columns: the stage's f16 pairs
 constexpr uint32_t kIdescF16 = ptx::idesc_f16_f32(kM, kTok);
 constexpr int kMaxStages = kF8Stages > kStages ? kF8Stages : kStages;
-static_assert(kF8ACol + kF8Dq * 64 <= kF8TmemCols, "A buffers exceed the TMEM allocation");
-static_assert(kF8Dq % 2 == 0, "each dequant warp set owns the buffers of its stage parity");
+static_assert(kF8ACol + kF8Dq * kF8ABuf <= kF8TmemCols, "A buffers exceed the TMEM allocation");
+
+// Stages of one micro's K (k_blocks 64-K blocks) with MXFP8 weights.
+__device__ __forceinline__ int f8_stages(int k_blocks) { return (k_blocks + kF8Chunks - 1) / kF8Chunks; }
 static_assert(kF8CodeOff % 1024 == 0 && kF8CodeBytes % 1024 == 0, "128-byte swizzled tiles need 1024-byte alignment");
 
 enum Mode { kSwiGLUOnly = 0, kDownOnly = 1, kFused = 2 };
@@ -117,10 +124,16 @@ struct Ctl {
     uint64_t sq_empty;
     int sq_tile;
     int sq_rows;
-    // MXFP8: dequantised A buffers (tensor memory) handed from the dequant warps
-    // to the MMA issuer
-    uint64_t dq_full[kF8Dq];
-    uint64_t dq_empty[kF8Dq];
+    // MXFP8. A stage is taken by dequant set p = (stage number) % 2 and MMA
+    // issuer j = (index in its tile) % 2, and uses code slot (stage number) %
+    // kF8Stages and A buffer (stage number) % kF8Dq. Every barrier below has
+    // one consumer, which waits all its completions in order (phase bits per
+    // slot), so no parity wait can run a phase ahead: a slot's next use for
+    // that consumer is armed only after the slot passed through it.
+    uint64_t fullD[2][kF8Stages];  // codes + scales landed, for dequant set p
+    uint64_t fullB[2][kF8Stages];  // token rows landed, for issuer j
+    uint64_t dq_full[2][kF8Dq];    // A buffer written, for issuer j (the four warps of a set)
+    uint64_t dq_empty[2][kF8Dq];   // A buffer read by the MMAs, for the set that writes it next
 };
 
 constexpr int kSmemBytes = kStages * kStageBytes + (int)sizeof(Ctl) + 1024;
@@ -520,9 +533,15 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
             ptx::mbar_init(ptx::smem_u32(&c.tfull[b]), F8 ? 2 : 1);  // the MMA issuer(s)' commits
             ptx::mbar_init(ptx::smem_u32(&c.tempty[b]), 4);
         }
-        for (int b = 0; b < kF8Dq; ++b) {
-            ptx::mbar_init(ptx::smem_u32(&c.dq_full[b]), 4);  // the four dequant warps of its parity
-            ptx::mbar_init(ptx::smem_u32(&c.dq_empty[b]), 1);  // the MMA issuer's commit
+        for (int q = 0; q < 2; ++q) {
+            for (int b = 0; b < kF8Dq; ++b) {
+                ptx::mbar_init(ptx::smem_u32(&c.dq_full[q][b]), 4);  // the four warps of a dequant set
+                ptx::mbar_init(ptx::smem_u32(&c.dq_empty[q][b]), 1);  // an MMA issuer's commit
+            }
+            for (int st = 0; st < kF8Stages; ++st) {
+                ptx::mbar_init(ptx::smem_u32(&c.fullD[q][st]), 1);  // the producer's expect_tx arrive
+                ptx::mbar_init(ptx::smem_u32(&c.fullB[q][st]), 1);
+            }
         }
         ptx::mbar_init(ptx::smem_u32(&c.drain), 1);
         ptx::mbar_init(ptx::smem_u32(&c.drain2), 1);
@@ -577,6 +596,10 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
         int stage = 0;
         uint32_t phase = 0;
         int issued = 0;
+        int gs = 0;  // stage number (MXFP8: picks the dequant set)
+        // MXFP8: per slot, the barriers it armed last and their phase parities
+        // (to wait out loads still in flight on failure); arm_* flip per arm
+        uint32_t last_d[kSt], last_b[kSt], last_dpar = 0, last_bpar = 0, arm_d[2] = {0, 0}, arm_b[2] = {0, 0};
         bool ok = true;
         TileStream ts;
         ts.next_static = blockIdx.x;
@@ -597,6 +620,7 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
             bool rows_ready = gcnt == nullptr || rows_seen || ld_acquire(gcnt) >= t.row_end - t.row0;
             if (MODE == kFused) fence_proxy_async_global();  // the rows are read by TMA (async proxy)
             int pend_stage[kSt], pend_kb[kSt], pending = 0;
+            uint32_t pend_bar[kSt];
             const int n_micro_k = sw ? 1 : g.n_micro;
             for (int mi = 0; ok && mi < n_micro_k; ++mi) {
                 const int m = sw ? t.m : mi;
@@ -605,12 +629,12 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
                 const CUtensorMap* tx = sw ? &maps.x1 : &maps.x2;
                 const int wrow = t.g * g.b_rows_per_group + t.nt * (sw ? 64 : kM);
                 constexpr int kK = F8 ? kF8K : kTcBK;                      // K per stage
-                const int kbn = F8 ? g.k_blocks / 2 : g.k_blocks;         // stages per micro
-                // the token rows of a stage: one 64-K tile (two with MXFP8 weights)
+                const int kbn = F8 ? f8_stages(g.k_blocks) : g.k_blocks;  // stages per micro
+                // the token rows of a stage: one 64-K tile (four with MXFP8 weights)
                 auto load_rows = [&](int st, int kx, uint32_t bar) {
                     const uint32_t sb = ptx::smem_u32(stage_b(st));
                     if (F8)
-                        ptx::tma_load_3d(sb, tx, 0, t.row0, kx / kTcBK, bar);  // both 64-K tiles (brows rows each)
+                        ptx::tma_load_3d(sb, tx, 0, t.row0, kx / kTcBK, bar);  // four 64-K tiles (brows rows each)
                     else
                         ptx::tma_load_2d(sb, tx, kx, t.row0, bar);
                 };
@@ -620,18 +644,35 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
                         break;
                     }
                     const uint32_t sa = ptx::smem_u32(stage_a(stage));
-                    const uint32_t fb = ptx::smem_u32(&c.full[stage]);
-                    ptx::mbar_arrive_expect_tx(fb, F8 ? kF8CodeBytes + kF8ScaleBytes + p.brows * 256 : kStageBytes);
+                    // MXFP8: codes and scales complete the barrier of the stage's dequant
+                    // set, the token rows that of its MMA issuer
+                    const int dset = gs & 1, iss = (mi * kbn + kb) & 1;
+                    const uint32_t fb = ptx::smem_u32(F8 ? &c.fullD[dset][stage] : &c.full[stage]);
+                    const uint32_t fbb = F8 ? ptx::smem_u32(&c.fullB[iss][stage]) : fb;
                     if (F8) {
-                        // codes: 128 K of the tile's rows; scales: the four 32-blocks of those K
-                        const int srow = t.g * 2 * g.k_blocks + 4 * kb;
+                        last_d[stage] = fb;
+                        last_b[stage] = fbb;
+                        last_dpar = (last_dpar & ~(1u << stage)) | (((arm_d[dset] >> stage) & 1u) << stage);
+                        last_bpar = (last_bpar & ~(1u << stage)) | (((arm_b[iss] >> stage) & 1u) << stage);
+                        arm_d[dset] ^= 1u << stage;
+                        arm_b[iss] ^= 1u << stage;
+                        ptx::mbar_arrive_expect_tx(fb, kF8CodeBytes + kF8ScaleBytes);
+                        ptx::mbar_arrive_expect_tx(fbb, p.brows * 512);
+                    } else {
+                        ptx::mbar_arrive_expect_tx(fb, kStageBytes);
+                    }
+                    ++gs;
+                    if (F8) {
+                        // codes: two 128-K chunks of the tile's rows; scales: the eight
+                        // 32-blocks of those K (rows of the scale maps)
+                        const int srow = t.g * 2 * g.k_blocks + 8 * kb;
                         const uint32_t ss = ptx::smem_u32(stage_s(stage));
                         if (sw) {
-                            // 64 gate rows, then the 64 matching up rows (half 2g + 1 of the map)
-                            ptx::tma_load_3d_hint(sa, tw, kb * kK, t.nt * 64, 2 * t.g, fb, wpol);
+                            // per chunk: 64 gate rows, then the 64 matching up rows (half 2g + 1)
+                            ptx::tma_load_4d_hint(sa, tw, 0, t.nt * 64, 2 * t.g, 2 * kb, fb, wpol);
                             ptx::tma_load_3d(ss, tsc, t.nt * 64, 0, srow, fb);
                         } else {
-                            ptx::tma_load_2d_hint(sa, tw, kb * kK, wrow, fb, wpol);               // 128 rows
+                            ptx::tma_load_3d_hint(sa, tw, 0, wrow, 2 * kb, fb, wpol);            // per chunk: 128 rows
                             ptx::tma_load_2d(ss, tsc, t.nt * kM, srow, fb);
                         }
                     } else if (sw) {
@@ -642,10 +683,11 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
                     }
                     const int kx = (sw ? 0 : m * g.a_micro_cols) + kb * kK;
                     if (rows_ready) {
-                        load_rows(stage, kx, fb);  // 16 token rows
+                        load_rows(stage, kx, fbb);  // 16 token rows
                     } else {
                         pend_stage[pending] = stage;
                         pend_kb[pending] = kx;
+                        pend_bar[pending] = fbb;
                         ++pending;
                     }
                     ++issued;
@@ -667,7 +709,7 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
                         }
                         fence_proxy_async_global();
                         for (int q = 0; q < pending; ++q)  // completes the armed stages even on failure
-                            load_rows(pend_stage[q], pend_kb[q], ptx::smem_u32(&c.full[pend_stage[q]]));
+                            load_rows(pend_stage[q], pend_kb[q], pend_bar[q]);
                         pending = 0;
                         rows_ready = true;
                         if (!ok) break;
@@ -685,8 +727,14 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
             fail(c, a0.err);
             const int n = issued < kSt ? issued : kSt;
             // slot s was last armed in this pass of the ring if s < stage, else in the previous one
-            for (int s = 0; s < n; ++s)
-                ptx::mbar_wait(ptx::smem_u32(&c.full[s]), s < stage ? phase : phase ^ 1u, a0.limit_ns, nullptr);
+            for (int s = 0; s < n; ++s) {
+                if (F8) {
+                    ptx::mbar_wait(last_d[s], (last_dpar >> s) & 1u, a0.limit_ns, nullptr);
+                    ptx::mbar_wait(last_b[s], (last_bpar >> s) & 1u, a0.limit_ns, nullptr);
+                } else {
+                    ptx::mbar_wait(ptx::smem_u32(&c.full[s]), s < stage ? phase : phase ^ 1u, a0.limit_ns, nullptr);
+                }
+            }
         }
     } else if (MODE == kFused && warp == 3 && lane == 0) {
         // ------------------------------------------------ scheduler
@@ -748,8 +796,8 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
         // how fast one thread issues tcgen05 instructions (eight MMAs and two
         // commits per stage), so two issuing threads raise it.
         const int j = warp - 1;
-        int stage = 0, dq = 0;
-        uint32_t phase = 0, dq_phase = 0;
+        int stage = 0, dq = 0, gs = 0;  // code slot, A buffer, stage number
+        uint32_t fb_bits = 0, dq_bits = 0;  // phase bits of this issuer's fullB / dq_full barriers
         bool ok = true;
         TileStream ts;
         ts.next_static = blockIdx.x;
@@ -771,19 +819,23 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
             ptx::tc_fence_after();
             const uint32_t d = tmem + (uint32_t)(acc * 2 * kTok + j * kTok);
             uint32_t accumulate = 0;
-            const int nk = (sw ? 1 : g.n_micro) * (g.k_blocks / 2);
+            const int nk = (sw ? 1 : g.n_micro) * f8_stages(g.k_blocks);
             for (int i = 0; i < nk; ++i) {
                 if ((i & 1) == j) {
-                    if (!ptx::mbar_wait(ptx::smem_u32(&c.full[stage]), phase, g.limit_ns, &c.abort) ||
-                        !ptx::mbar_wait(ptx::smem_u32(&c.dq_full[dq]), dq_phase, g.limit_ns, &c.abort)) {
+                    if (!ptx::mbar_wait(ptx::smem_u32(&c.fullB[j][stage]), (fb_bits >> stage) & 1u, g.limit_ns,
+                                        &c.abort) ||
+                        !ptx::mbar_wait(ptx::smem_u32(&c.dq_full[j][dq]), (dq_bits >> dq) & 1u, g.limit_ns,
+                                        &c.abort)) {
                         ok = false;
                         break;
                     }
+                    fb_bits ^= 1u << stage;
+                    dq_bits ^= 1u << dq;
                     ptx::tc_fence_after();
-                    // A buffer dq: 8 columns per 16 K; the second 64 K pair with the second token tile
-                    const uint32_t at = tmem + (uint32_t)(kF8ACol + dq * 64);
+                    // A buffer dq: 8 columns per 16 K; 64-K chunk h pairs with token tile h
+                    const uint32_t at = tmem + (uint32_t)(kF8ACol + dq * kF8ABuf);
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
+                    for (int h = 0; h < kF8Chunks; ++h) {
                         // the second 64-K tile starts after the first one's brows rows
                         const uint64_t bd = ptx::sw128_desc(ptx::smem_u32(stage_b(stage)) + h * p.brows * 128);
 #pragma unroll
@@ -792,17 +844,13 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
                             accumulate = 1;
                         }
                     }
-                    ptx::mma_commit(ptx::smem_u32(&c.empty[stage]));
-                    ptx::mma_commit(ptx::smem_u32(&c.dq_empty[dq]));
+                    ptx::mma_commit(ptx::smem_u32(&c.empty[stage]));  // the code slot (codes, scales, rows)
+                    // the A buffer, for the dequant set that writes it next
+                    ptx::mma_commit(ptx::smem_u32(&c.dq_empty[(gs + kF8Dq) & 1][dq]));
                 }
-                if (++stage == kSt) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-                if (++dq == kF8Dq) {
-                    dq = 0;
-                    dq_phase ^= 1u;
-                }
+                ++gs;
+                if (++stage == kSt) stage = 0;
+                if (++dq == kF8Dq) dq = 0;
             }
             if (ok) ptx::mma_commit(ptx::smem_u32(&c.tfull[acc]));
         }
@@ -819,8 +867,8 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
         const int q = warp & 3, par = (warp - 8) >> 2;
         const int r = q * 32 + lane;
         const uint32_t a_lanes = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)kF8ACol;
-        int stage = 0, dq = 0, kseq = 0;
-        uint32_t phase = 0, dq_phase = 0;
+        int stage = 0, dq = 0, kseq = 0;  // code slot, A buffer, stage number
+        uint32_t fd_bits = 0, de_bits = 0;  // phase bits of this set's fullD / dq_empty barriers
         bool ok = true;
         TileStream ts;
         ts.next_static = blockIdx.x;
@@ -832,57 +880,67 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
             bool sw;
             locate<MODE>(tile, c, p, sw);
             const TcGemmArgs& g = sw ? p.g1 : p.g2;
-            const int nk = (sw ? 1 : g.n_micro) * (g.k_blocks / 2);
+            const int nk = (sw ? 1 : g.n_micro) * f8_stages(g.k_blocks);
             for (int i = 0; i < nk; ++i, ++kseq) {
                 if ((kseq & 1) == par) {
-                    bool got = ptx::mbar_wait(ptx::smem_u32(&c.full[stage]), phase, g.limit_ns, &c.abort) &&
-                               ptx::mbar_wait(ptx::smem_u32(&c.dq_empty[dq]), dq_phase ^ 1u, g.limit_ns, &c.abort);
+                    // the buffer's first use needs no free signal; later ones wait for the
+                    // MMAs of its previous use, committed to this set
+                    const bool first_use = kseq < kF8Dq;
+                    bool got = ptx::mbar_wait(ptx::smem_u32(&c.fullD[par][stage]), (fd_bits >> stage) & 1u,
+                                              g.limit_ns, &c.abort) &&
+                               (first_use || ptx::mbar_wait(ptx::smem_u32(&c.dq_empty[par][dq]), (de_bits >> dq) & 1u,
+                                                            g.limit_ns, &c.abort));
+                    fd_bits ^= 1u << stage;
+                    if (!first_use) de_bits ^= 1u << dq;
                     if (!__all_sync(0xffffffffu, got)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
-                    // 16-byte chunk j of row r sits at chunk j ^ (r % 8) (128-byte swizzle)
-                    const unsigned char* row = stage_a(stage) + r * kF8K;
-                    uint4 cv[8];
+                    // the stage's two 128-K code chunks, one at a time (so only one
+                    // chunk's codes and one half's f16 pairs are live)
+#pragma unroll 1
+                    for (int kc = 0; kc < kF8K / 128; ++kc) {
+                        // 16-byte piece j of row r sits at piece j ^ (r % 8) (128-byte swizzle)
+                        const unsigned char* row = stage_a(stage) + kc * (kM * 128) + r * 128;
+                        uint4 cv[8];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) cv[j] = *reinterpret_cast<const uint4*>(row + ((j ^ (r & 7)) << 4));
-                    // scales [4][128 rows] (SwiGLU tiles: each block's 64 gate rows, then its 64 up rows)
-                    const unsigned char* sp = stage_s(stage);
-                    int sc[4];
+                        for (int j = 0; j < 8; ++j)
+                            cv[j] = *reinterpret_cast<const uint4*>(row + ((j ^ (r & 7)) << 4));
+                        // scales [8][128 rows] (SwiGLU tiles: each block's 64 gate rows, then its 64 up rows)
+                        const unsigned char* sp = stage_s(stage) + kc * 4 * kM;
+                        int sc[4];
 #pragma unroll
-                    for (int b = 0; b < 4; ++b) sc[b] = sp[b * kM + r];
-                    bool slow = false;
+                        for (int b = 0; b < 4; ++b) sc[b] = sp[b * kM + r];
+                        bool slow = false;
 #pragma unroll
-                    for (int b = 0; b < 4; ++b) slow |= !dequant_in_f16(sc[b]);
-                    // two halves of 64 K (32 columns each), so only one half's f16 pairs are live
+                        for (int b = 0; b < 4; ++b) slow |= !dequant_in_f16(sc[b]);
+                        // two halves of 64 K (32 columns each)
 #pragma unroll
-                    for (int hf = 0; hf < 2; ++hf) {
-                        uint32_t o[32];
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) dequant16_f16(cv[4 * hf + j], sc[2 * hf + (j >> 1)], o + 8 * j);
-                        if (slow) {  // rare: scales that are not f16 numbers
+                        for (int hf = 0; hf < 2; ++hf) {
+                            uint32_t o[32];
 #pragma unroll
                             for (int j = 0; j < 4; ++j)
-                                if (!dequant_in_f16(sc[2 * hf + (j >> 1)]))
-                                    dequant16_f32(cv[4 * hf + j], sc[2 * hf + (j >> 1)], o + 8 * j);
+                                dequant16_f16(cv[4 * hf + j], sc[2 * hf + (j >> 1)], o + 8 * j);
+                            if (slow) {  // rare: scales that are not f16 numbers
+#pragma unroll
+                                for (int j = 0; j < 4; ++j)
+                                    if (!dequant_in_f16(sc[2 * hf + (j >> 1)]))
+                                        dequant16_f32(cv[4 * hf + j], sc[2 * hf + (j >> 1)], o + 8 * j);
+                            }
+                            __syncwarp();
+                            ptx::tmem_st32(a_lanes + (uint32_t)(dq * kF8ABuf + 64 * kc + 32 * hf), o);
+                            ptx::tmem_wait_st();  // the registers of o are reused by the next half
                         }
-                        __syncwarp();
-                        ptx::tmem_st32(a_lanes + (uint32_t)(dq * 64 + 32 * hf), o);
                     }
                     ptx::tmem_wait_st();
                     ptx::tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&c.dq_full[dq]));
+                    // for the MMA issuer of the stage (its index in the tile picks it)
+                    if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&c.dq_full[i & 1][dq]));
                 }
-                if (++stage == kSt) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-                if (++dq == kF8Dq) {
-                    dq = 0;
-                    dq_phase ^= 1u;
-                }
+                if (++stage == kSt) stage = 0;
+                if (++dq == kF8Dq) dq = 0;
             }
             if (!ok) break;
         }
@@ -924,7 +982,7 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
                 // filled only half 0
                 uint32_t v2[2 * kTok];
                 ptx::tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * 2 * kTok), v2);
-                const bool both = (sw ? 1 : g.n_micro) * (g.k_blocks / 2) >= 2;
+                const bool both = (sw ? 1 : g.n_micro) * f8_stages(g.k_blocks) >= 2;
 #pragma unroll
                 for (int jj = 0; jj < kTok; ++jj)
                     v[jj] = both ? __float_as_uint(__uint_as_float(v2[jj]) + __uint_as_float(v2[kTok + jj])) : v2[jj];

@@ -267,6 +267,9 @@ bool encode_u8_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t row
 // 1 and 2, box in elements; unswizzled or with the 128-byte swizzle.
 bool encode_3d(CUtensorMap* m, bool bf16, const void* base, const uint64_t dims[3], const uint64_t strides[2],
                const uint32_t box[3], bool swizzle128);
+// The same for any rank 1..5 (strides of dims 1..rank-1).
+bool encode_nd(CUtensorMap* m, bool bf16, const void* base, int rank, const uint64_t* dims,
+               const uint64_t* strides, const uint32_t* box, bool swizzle128);
 // MXFP8 quantisation (mxfp8.cu): w [groups][rows][cols] bf16 -> codes [groups][rows][cols],
 // scales [groups][cols/32][rows]; cols % 32 == 0.
 cudaError_t launch_mx_quantize(const void* w, int64_t groups, int rows, int cols, void* codes, void* scales,

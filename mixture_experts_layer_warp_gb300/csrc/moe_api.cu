@@ -285,25 +285,30 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
         // router zeroed h->done); the shared expert's GEMMs ran first
         FinalizeArgs fin{h->obuf, h->inv, h->topw, Is > 0 ? h->sbuf : nullptr, T, k, H, true, y, h->accumulate};
         if (mx != nullptr) {
-            // MXFP8: the code and scale maps replace the bf16 weight maps; one
-            // box per stage and operand (3D maps: w13's gate and up rows, their
-            // scales, and the two 64-K chunks of 16 token rows)
+            // MXFP8: the code and scale maps replace the bf16 weight maps; a
+            // 256-K stage is one box per operand: w13 codes as a 4D map {128, I,
+            // 2E, H/128} (per 128-K chunk: 64 gate rows, then the matching up
+            // rows), w2 codes as a 3D map {128, E*H, I/128}, their scales (eight
+            // 32-blocks), and four 64-K chunks of the token rows
             CUtensorMap c1[kMaxMicro], c2[kMaxMicro], s1[kMaxMicro], s2[kMaxMicro], mX, mX2;
             const uint64_t xd[3] = {64, (uint64_t)R, (uint64_t)H / 64}, xs[2] = {(uint64_t)H * 2, 128};
             const uint64_t hd[3] = {64, (uint64_t)R, (uint64_t)M * I / 64}, hs[2] = {(uint64_t)M * I * 2, 128};
             const int brows = T <= 8 ? 8 : kSmallTokens;  // no expert owns more routes than T
-            const uint32_t xb[3] = {64, (uint32_t)brows, 2};
+            const uint32_t xb[3] = {64, (uint32_t)brows, 4};
             if (!encode_3d(&mX, true, h->xp, xd, xs, xb, true) || !encode_3d(&mX2, true, h->hbuf, hd, hs, xb, true))
                 return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (MXFP8 token rows)");
-            const uint64_t cd[3] = {(uint64_t)H, (uint64_t)I, 2 * (uint64_t)E}, cs[2] = {(uint64_t)H, (uint64_t)I * H};
-            const uint32_t cb[3] = {128, 64, 2};
+            const uint64_t cd[4] = {128, (uint64_t)I, 2 * (uint64_t)E, (uint64_t)H / 128};
+            const uint64_t cs[3] = {(uint64_t)H, (uint64_t)I * H, 128};
+            const uint32_t cb[4] = {128, 64, 2, 2};
+            const uint64_t dd[3] = {128, (uint64_t)E * H, (uint64_t)I / 128}, ds[2] = {(uint64_t)I, 128};
+            const uint32_t db[3] = {128, 128, 2};
             const uint64_t sd[3] = {(uint64_t)I, 2, (uint64_t)E * (H / 32)}, ss[2] = {(uint64_t)I, 2 * (uint64_t)I};
-            const uint32_t sb[3] = {64, 2, 4};
+            const uint32_t sb[3] = {64, 2, 8};
             for (int m = 0; m < M; ++m)
-                if (!encode_3d(&c1[m], false, w13[m], cd, cs, cb, true) ||
-                    !encode_u8_2d(&c2[m], w2[m], I, (uint64_t)E * H, (uint64_t)I, 128, 128, true) ||
+                if (!encode_nd(&c1[m], false, w13[m], 4, cd, cs, cb, true) ||
+                    !encode_nd(&c2[m], false, w2[m], 3, dd, ds, db, true) ||
                     !encode_3d(&s1[m], false, mx->w13[m], sd, ss, sb, false) ||
-                    !encode_u8_2d(&s2[m], mx->w2[m], H, (uint64_t)E * (I / 32), (uint64_t)H, 128, 4, false))
+                    !encode_u8_2d(&s2[m], mx->w2[m], H, (uint64_t)E * (I / 32), (uint64_t)H, 128, 8, false))
                     return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (MXFP8 weights, micro %d)", m);
             if ((e = timed(h, kSlotGemm1, s, [&] {
                      GatherArgs gat{x, h->perm, (int)R, k, (uint32_t)(H * 2), h->xp, h->err, h->limit_ns, h->num_sms};

@@ -157,6 +157,16 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void* tmap,
         : "memory");
 }
 
+// 4D tiled load with an L2 cache policy from policy_evict_*.
+__device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const void* tmap, int32_t c0, int32_t c1,
+                                                 int32_t c2, int32_t c3, uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar), "l"(policy)
+        : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
@@ -348,8 +358,10 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 }
 
 // Store 32 consecutive 32-bit columns of this warp's 32 TMEM lanes (one lane
-// per thread). The registers are read at issue; tmem_wait_st() waits until the
-// stores are done (before the columns are handed to the MMA).
+// per thread). The store completes asynchronously: the source registers must
+// keep their values until tmem_wait_st() (reusing them earlier corrupted the
+// stored columns now and then), which also orders the stores before the
+// columns are handed to the MMA.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "

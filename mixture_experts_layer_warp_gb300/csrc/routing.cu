@@ -58,18 +58,27 @@ bool encode_u8_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t row
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool encode_3d(CUtensorMap* m, bool bf16, const void* base, const uint64_t dims[3], const uint64_t strides[2],
-               const uint32_t box[3], bool swizzle128) {
+bool encode_nd(CUtensorMap* m, bool bf16, const void* base, int rank, const uint64_t* dims,
+               const uint64_t* strides, const uint32_t* box, bool swizzle128) {
     EncodeTiledFn enc = encode_fn();
-    if (enc == nullptr) return false;
-    cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
-    cuuint64_t st[2] = {strides[0], strides[1]};
-    cuuint32_t b[3] = {box[0], box[1], box[2]};
-    cuuint32_t estr[3] = {1, 1, 1};
-    return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base),
-               d, st, b, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    if (enc == nullptr || rank < 1 || rank > 5) return false;
+    cuuint64_t d[5], st[4];
+    cuuint32_t b[5], estr[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+        estr[i] = 1;
+        if (i + 1 < rank) st[i] = strides[i];
+    }
+    return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, (cuuint32_t)rank,
+               const_cast<void*>(base), d, st, b, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_3d(CUtensorMap* m, bool bf16, const void* base, const uint64_t dims[3], const uint64_t strides[2],
+               const uint32_t box[3], bool swizzle128) {
+    return encode_nd(m, bf16, base, 3, dims, strides, box, swizzle128);
 }
 
 cudaError_t enqueue_routing(const RoutingJob& j, cudaStream_t s, const LaunchHook* hook) {
