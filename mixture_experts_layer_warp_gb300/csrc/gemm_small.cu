@@ -930,7 +930,6 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
                             }
                             __syncwarp();
                             ptx::tmem_st32(a_lanes + (uint32_t)(dq * kF8ABuf + 64 * kc + 32 * hf), o);
-                            ptx::tmem_wait_st();  // the registers of o are reused by the next half
                         }
                     }
                     ptx::tmem_wait_st();

@@ -358,10 +358,8 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 }
 
 // Store 32 consecutive 32-bit columns of this warp's 32 TMEM lanes (one lane
-// per thread). The store completes asynchronously: the source registers must
-// keep their values until tmem_wait_st() (reusing them earlier corrupted the
-// stored columns now and then), which also orders the stores before the
-// columns are handed to the MMA.
+// per thread). tmem_wait_st() waits until the stores issued so far are done
+// (before the columns are handed to the MMA).
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
