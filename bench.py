@@ -147,16 +147,23 @@ def job_throughput(world: int, tokens_per_step: int, steps: int, ms_local: float
     return ms, world * tokens_per_step * steps / (ms / 1e3)
 
 
-def src_sha() -> str:
-    """Hash of every CUDA source of the library: recorded ncu counters are used
-    only while this matches the hash stored beside them."""
+# The sources each GEMM kernel is compiled from (its translation unit and the
+# headers it includes): the small-batch fused kernel, the large-batch tcgen05 GEMM.
+KERNEL_SOURCES = {
+    "small": ("gemm_small.cu", "gemm_common.cuh", "kernels.h", "ptx.cuh"),
+    "large": ("gemm_tc.cu", "gemm_common.cuh", "kernels.h", "ptx.cuh"),
+}
+
+
+def src_sha(kind: str) -> str:
+    """Hash of the CUDA sources of one GEMM kernel (KERNEL_SOURCES): recorded
+    ncu counters are used only while this matches the hash stored beside them."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "mixture_experts_layer_warp_gb300", "csrc")
-    for n in sorted(os.listdir(d)):
-        if n.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(d, n), "rb") as f:
-                h.update(n.encode())
-                h.update(f.read())
+    for n in KERNEL_SOURCES[kind]:
+        with open(os.path.join(d, n), "rb") as f:
+            h.update(n.encode())
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
@@ -248,7 +255,7 @@ def config_of(wl):
                   f"{POOL} seeded batches"}
 
 
-def roofline_of(wl, prof, ids_pool, steps, peaks, sha, mxfp8=False):
+def roofline_of(wl, prof, ids_pool, steps, peaks, mxfp8=False):
     """Roofline of the kernel with the largest share of the timed region."""
     dom, (ms, n) = max(prof.items(), key=lambda kv: kv[1][0])
     per_launch_s = ms / n / 1e3
@@ -277,6 +284,7 @@ def roofline_of(wl, prof, ids_pool, steps, peaks, sha, mxfp8=False):
                 "shared_gemm1": 4 * wl.T * H * wl.shared_inter,
                 "shared_gemm2": 2 * wl.T * H * wl.shared_inter}.get(dom)
         achieved = algo / per_launch_s / 1e12 if algo else None
+    sha = src_sha("small" if fused else "large")
     traffic = recorded_traffic(wl.name + ("_mxfp8" if mxfp8 else ""), dom, sha)
     return {"kernel": dom + ("+gemm2_down+finalize (one launch)" if fused and dom == "gemm1_swiglu" else ""),
             "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
@@ -389,7 +397,7 @@ def run_ours(args, wl, world, rank, local):
     layer.sync()
     shift = args.warmup % POOL
     ids_timed = ids_pool[shift:] + ids_pool[:shift]
-    roof = roofline_of(wl, prof, ids_timed, args.steps, peaks, src_sha(), mxfp8=mx)
+    roof = roofline_of(wl, prof, ids_timed, args.steps, peaks, mxfp8=mx)
 
     # end to end through the C ABI with host buffers (pinned), copies included
     host_pool = [x.cpu().pin_memory() for x in pool]
