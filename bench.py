@@ -196,6 +196,32 @@ def oracle_tokens_per_s(wl, host_pool, weights, budget_s: float, min_calls: int 
     return n_tok / dt, calls, dt, oracle.num_threads()
 
 
+# fp32 logit tolerance for calling a token's top-k decided: the spread of fp32
+# sums over H = 4096 products in different orders (the routing tests use it too)
+ROUTE_TAU = 4e-6
+
+
+def routing_check(layer, wl, x, inp, weights) -> dict:
+    """The routing contract on one timed batch: the oracle's fp64 logits,
+    rounded to fp32, against the CUDA routing of the same batch. A token is
+    undecided when its k-th and (k+1)-th logits (set) or two adjacent top-k
+    logits (order) lie within 2 * ROUTE_TAU, so either choice is correct;
+    every decided token must carry the oracle's ids in the oracle's order."""
+    import oracle
+    lg = oracle.logits(W.to_numpy(x), weights["router_w"], weights["router_bias"])
+    ids_o, _ = oracle.route(lg, wl.k)
+    ids_g = layer.route(x, inp["router_w"], inp["router_bias"])["ids"].cpu().numpy()
+    lf = lg.astype(np.float32).astype(np.float64)
+    srt = -np.sort(-lf, axis=1)
+    k, E = wl.k, wl.E
+    set_ok = (srt[:, k - 1] - srt[:, k]) > 2 * ROUTE_TAU if k < E else np.ones(len(lf), bool)
+    order_ok = set_ok & np.all((srt[:, :k - 1] - srt[:, 1:k]) > 2 * ROUTE_TAU, axis=1)
+    return {"tokens": int(len(lf)), "set_undecided": int((~set_ok).sum()),
+            "order_undecided": int((~order_ok).sum()),
+            "decided_mismatch": int((order_ok & np.any(ids_g != ids_o, axis=1)).sum()),
+            "tau": ROUTE_TAU}
+
+
 def host_weights(inp):
     out = {}
     for k in ("router_w", "shared_w13", "shared_w2"):
@@ -430,7 +456,7 @@ def run_ours(args, wl, world, rank, local):
     if args.two_dispatch and wl.n_micro > 1:
         two = time_two_dispatch(args, wl, inp, pool, ms / args.steps, world)
 
-    cpu = None
+    cpu = rcheck = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         weights = host_weights(inp)
         Ts = sample_tokens(wl)
@@ -438,6 +464,7 @@ def run_ours(args, wl, world, rank, local):
         v, calls, dt, cores = oracle_tokens_per_s(wl, hp, weights, budget_s=args.cpu_seconds)
         cpu = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                "sample": f"{calls} whole-layer oracle calls of {Ts} tokens ({dt:.1f} s)"}
+        rcheck = routing_check(layer, wl, pool[0], inp, weights)
 
     layer.close()
     if rank != 0:
@@ -452,6 +479,8 @@ def run_ours(args, wl, world, rank, local):
         "kernels_ms_per_step": {k: v[0] / args.steps for k, v in prof.items()},
         "clocks": clk.summary(),
     }
+    if rcheck is not None:
+        line["routing_check"] = rcheck
     if two is not None:
         line["two_dispatch"] = two
     print(json.dumps(line), flush=True)

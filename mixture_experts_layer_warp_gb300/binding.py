@@ -146,7 +146,7 @@ class MoELayer:
         self._lib = load()
         self._h = ctypes.c_void_p()
         self._wcache = None
-        self._valid = {}  # argument name -> (weak reference, data_ptr) of the tensor last validated there
+        self._valid = {}  # argument name -> {id(tensor): (weak reference, data_ptr)} of tensors validated there
         self._stream_id = None
         with torch.cuda.device(self.device):
             rc = self._lib.moe_create(ctypes.byref(self.cfg), ctypes.byref(self._h))
@@ -160,9 +160,11 @@ class MoELayer:
 
     def _tensor(self, t, name, shape, dtype=None, host=False):
         dtype = self.dtype if dtype is None else dtype
-        # the same tensor passed again in the same role (router matrix, output
-        # buffer) is not re-validated: a call's host time is part of its latency
-        memo = self._valid.get(name)
+        # a tensor passed again in the same role (router matrix, output buffer,
+        # a rotating set of input buffers) is not re-validated: a call's host
+        # time is part of its latency
+        seen = self._valid.get(name)
+        memo = seen.get(id(t)) if seen is not None else None
         if memo is not None and memo[0]() is t and memo[1] == t.data_ptr() and t.shape == shape \
                 and t.dtype == dtype:
             return t
@@ -178,7 +180,10 @@ class MoELayer:
             raise ValueError(f"{name} must be in host memory")
         if not host and t.device != self.device:
             raise ValueError(f"{name} must be on {self.device}")
-        self._valid[name] = (weakref.ref(t), t.data_ptr())
+        seen = self._valid.setdefault(name, {})
+        if len(seen) >= 16:
+            seen.clear()
+        seen[id(t)] = (weakref.ref(t), t.data_ptr())
         return t
 
     def _weights(self, w13, w2, shared_w13, shared_w2):
