@@ -464,6 +464,13 @@ def run_ours(args, wl, world, rank, local):
         v, calls, dt, cores = oracle_tokens_per_s(wl, hp, weights, budget_s=args.cpu_seconds)
         cpu = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                "sample": f"{calls} whole-layer oracle calls of {Ts} tokens ({dt:.1f} s)"}
+        if wl.T <= 64:  # the small configurations are also timed on one core
+            import oracle
+            oracle.set_threads(1)
+            v1, calls1, dt1, _ = oracle_tokens_per_s(wl, hp, weights, budget_s=args.cpu_seconds / 2)
+            oracle.set_threads(cores)
+            cpu["single_core"] = {"value": v1, "unit": "tokens/s", "cores": 1,
+                                  "sample": f"{calls1} whole-layer oracle calls of {Ts} tokens ({dt1:.1f} s)"}
         rcheck = routing_check(layer, wl, pool[0], inp, weights)
 
     layer.close()

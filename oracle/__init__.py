@@ -17,4 +17,5 @@ from .oracle import (  # noqa: F401
     num_threads,
     permute,
     route,
+    set_threads,
 )

@@ -533,3 +533,15 @@ int orc_mx_dequant(const uint8_t *codes, const uint8_t *scales, int64_t groups, 
 
 /* Number of OpenMP threads the oracle uses (reported beside its timings). */
 int orc_num_threads(void) { return max_threads(); }
+
+/* Sets the number of OpenMP threads of later calls from this thread (n >= 1;
+ * used to time the oracle on one core beside all cores); returns the number
+ * now in effect. */
+int orc_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n >= 1)
+        omp_set_num_threads(n);
+#endif
+    return max_threads();
+}

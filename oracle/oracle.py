@@ -56,8 +56,9 @@ def _bind(path: str):
         _p, ctypes.c_int, _i64, _i64, _i64, _i64, _i64, _i64, _p, _p, _p, _p, _i64,
         _p, _p, _p, _p, _p]
     lib.orc_num_threads.argtypes = []
+    lib.orc_set_threads.argtypes = [ctypes.c_int]
     for fn in ("orc_logits", "orc_route", "orc_permute", "orc_forward_tokens", "orc_forward_tokens_typed",
-               "orc_forward_permuted", "orc_num_threads", "orc_mx_quantize", "orc_mx_dequant"):
+               "orc_forward_permuted", "orc_num_threads", "orc_set_threads", "orc_mx_quantize", "orc_mx_dequant"):
         getattr(lib, fn).restype = ctypes.c_int
     return lib
 
@@ -95,6 +96,11 @@ def _ptr(a) -> int | None:
 
 def num_threads(lib=None) -> int:
     return int((lib or _load()).orc_num_threads())
+
+
+def set_threads(n: int, lib=None) -> int:
+    """OpenMP threads for later oracle calls from this thread; returns the number in effect."""
+    return int((lib or _load()).orc_set_threads(int(n)))
 
 
 def logits(x: np.ndarray, wr: np.ndarray, bias: np.ndarray | None = None, lib=None) -> np.ndarray:
