@@ -29,7 +29,7 @@ namespace {
 
 constexpr int kTok = kRouterTokensTc;   // 128 tokens per CTA = MMA M
 constexpr int kN = 64;                  // MMA N: experts, padded to 64
-constexpr int kStages = 6;
+constexpr int kStages = 6;  // even: a slot holds K-blocks of one parity (one MMA issuer)
 constexpr int kABytes = kTok * kTcBK * 2;   // 16 KB
 constexpr int kBBytes = kN * kTcBK * 2;     // 8 KB
 constexpr int kStageBytes = kABytes + kBBytes;
@@ -209,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(ptx::smem_u32(&c.full[s]), 1);
             ptx::mbar_init(ptx::smem_u32(&c.empty[s]), 1);
         }
-        ptx::mbar_init(ptx::smem_u32(&c.done), 1);
+        ptx::mbar_init(ptx::smem_u32(&c.done), 2);  // both MMA issuers' final commits
         c.abort = 0;
         ptx::fence_mbar_init();
     }
@@ -256,12 +256,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int n = issued < kStages ? issued : kStages;
             for (int s = 0; s < n; ++s) ptx::mbar_wait(ptx::smem_u32(&c.full[s]), last_par[s], a.limit_ns, nullptr);
         }
-    } else if (warp == 1 && lane == 0) {
-        // MMA issuer: K-block kb goes to partial accumulator kb % 8
-        int stage = 0;
+    } else if ((warp == 1 || warp == 3) && lane == 0) {
+        // MMA issuers: K-block kb goes to partial accumulator kb % 8, issued by
+        // warp 1 for even kb and warp 3 for odd kb (one thread issues an MMA
+        // about every 75 cycles; two halve the issue time). The partials and
+        // the K-blocks summed into each are those of a single issuer, so the
+        // logits are unchanged; with an even ring, slot s only ever holds
+        // K-blocks of one parity, so each slot's barriers have one consumer.
+        const int j = warp == 1 ? 0 : 1;
+        int stage = j;
         uint32_t phase = 0;
         bool ok = true;
-        for (int kb = 0; kb < kb_total; ++kb) {
+        for (int kb = j; kb < kb_total; kb += 2) {
             if (!ptx::mbar_wait(ptx::smem_u32(&c.full[stage]), phase, a.limit_ns, &c.abort)) {
                 ok = false;
                 break;
@@ -274,8 +280,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kk = 0; kk < kTcBK / 16; ++kk)
                 ptx::mma_bf16(d, adesc + 2u * kk, bdesc + 2u * kk, kIdesc, (kb >= kParts || kk > 0) ? 1u : 0u);
             ptx::mma_commit(ptx::smem_u32(&c.empty[stage]));
-            if (++stage == kStages) {
-                stage = 0;
+            stage += 2;
+            if (stage >= kStages) {
+                stage -= kStages;
                 phase ^= 1u;
             }
         }
