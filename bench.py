@@ -281,7 +281,14 @@ def config_of(wl):
                   f"{POOL} seeded batches"}
 
 
-def roofline_of(wl, prof, ids_pool, steps, peaks, mxfp8=False):
+# A step at least this long keeps the tensor cores busy for milliseconds at a
+# time, back to back: its GEMMs run under the board power limit, the condition
+# of the sustained bf16 peak (a seconds-long GEMM loop); shorter steps are
+# rated against the burst peak.
+LONG_STEP_MS = 2.0
+
+
+def roofline_of(wl, prof, ids_pool, steps, peaks, step_ms, mxfp8=False):
     """Roofline of the kernel with the largest share of the timed region."""
     dom, (ms, n) = max(prof.items(), key=lambda kv: kv[1][0])
     per_launch_s = ms / n / 1e3
@@ -305,19 +312,30 @@ def roofline_of(wl, prof, ids_pool, steps, peaks, mxfp8=False):
         }.get(dom)
         achieved = algo / per_launch_s / 1e9 if algo else None
     else:
-        bound, unit, peak = "tensor", "TFLOP/s", peaks["bf16"]
+        sustained = step_ms >= LONG_STEP_MS
+        bound, unit = "tensor", "TFLOP/s"
+        peak = peaks["bf16_sustained"] if sustained else peaks["bf16"]
         algo = {"gemm1_swiglu": 4 * R * H * I * M, "gemm2_down": 2 * R * H * I * M,
                 "shared_gemm1": 4 * wl.T * H * wl.shared_inter,
                 "shared_gemm2": 2 * wl.T * H * wl.shared_inter}.get(dom)
         achieved = algo / per_launch_s / 1e12 if algo else None
     sha = src_sha("small" if fused else "large")
     traffic = recorded_traffic(wl.name + ("_mxfp8" if mxfp8 else ""), dom, sha)
-    return {"kernel": dom + ("+gemm2_down+finalize (one launch)" if fused and dom == "gemm1_swiglu" else ""),
-            "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-            "frac": (achieved / peak) if achieved else None, "traffic": traffic,
+    out = {"kernel": dom + ("+gemm2_down+finalize (one launch)" if fused and dom == "gemm1_swiglu" else ""),
+           "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+           "frac": (achieved / peak) if achieved else None, "traffic": traffic,
             "algorithmic_per_launch": algo, "launch_ms": per_launch_s * 1e3,
-            "share": ms / sum(v[0] for v in prof.values()), "peak_source": peaks["source"],
-            "timing": "per-kernel CUDA events in a profiling pass of the same steps"}
+           "share": ms / sum(v[0] for v in prof.values()), "peak_source": peaks["source"],
+           "timing": "per-kernel CUDA events in a profiling pass of the same steps"}
+    if bound == "tensor":
+        out["peak_kind"] = ("sustained" if sustained else "burst") + \
+            f" (steps of {LONG_STEP_MS:g} ms or more are rated against the sustained peak)"
+        if achieved:
+            out["frac_burst"] = achieved / peaks["bf16"]
+            out["frac_sustained"] = achieved / peaks["bf16_sustained"]
+    else:
+        out["peak_kind"] = "measured copy bandwidth"
+    return out
 
 
 def time_two_dispatch(args, wl, inp, pool, multi_ms, world):
@@ -423,7 +441,7 @@ def run_ours(args, wl, world, rank, local):
     layer.sync()
     shift = args.warmup % POOL
     ids_timed = ids_pool[shift:] + ids_pool[:shift]
-    roof = roofline_of(wl, prof, ids_timed, args.steps, peaks, mxfp8=mx)
+    roof = roofline_of(wl, prof, ids_timed, args.steps, peaks, ms / args.steps, mxfp8=mx)
 
     # end to end through the C ABI with host buffers (pinned), copies included
     host_pool = [x.cpu().pin_memory() for x in pool]
