@@ -57,9 +57,29 @@ struct Ctl {
 
 constexpr int kSmemBytes = kStages * kStageBytes + (int)sizeof(Ctl) + 1024;
 
+// Row blocks of a (group, micro) with more than kRowChunk of them run in
+// chunks: every n-tile of chunk 0, then every n-tile of chunk 1, ... A
+// chunk's activation rows (16 MB at K = 4096) then stay in L2 while the
+// n-tiles sweep them; in the plain order a large group (the dense shared
+// expert: 256 row blocks, 268 MB of x) re-read all its rows from DRAM once per
+// n-tile. Smaller groups keep the plain order (n-tile, then row block).
+constexpr int kRowChunk = 16;
+
 template <bool SWIGLU>
 __device__ __forceinline__ Tile decode_tile(int tile, const Ctl& c, const TcGemmArgs& a) {
-    return decode_group_tile(tile, c.seg, c.tiles, a.G, a.n_tiles, a.n_micro, SWIGLU, kTcBM);
+    Tile t = decode_group_tile(tile, c.seg, c.tiles, a.G, a.n_tiles, a.n_micro, SWIGLU, kTcBM);
+    const int mtiles = c.tiles[t.g + 1] - c.tiles[t.g];
+    if (mtiles <= kRowChunk) return t;
+    // the tile's index within its (group, micro) in the plain order, mapped
+    // onto the chunked order (full chunks of kRowChunk row blocks, then the rest)
+    const int local = t.nt * mtiles + (t.row0 - c.seg[t.g]) / kTcBM;
+    const int span = kRowChunk * a.n_tiles, nfull = mtiles / kRowChunk;
+    const int chunk = min(local / span, nfull);
+    const int rows = chunk < nfull ? kRowChunk : mtiles - nfull * kRowChunk;
+    const int off = local - chunk * span;
+    t.nt = off / rows;
+    t.row0 = c.seg[t.g] + (chunk * kRowChunk + off % rows) * kTcBM;
+    return t;
 }
 
 __device__ __forceinline__ void fail(Ctl& c, int* err) {

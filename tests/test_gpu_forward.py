@@ -54,6 +54,9 @@ SMALL = [
     W.Workload("bf16_shared", 257, 256, 16, 4, 128, 2, shared_inter=256),
     W.Workload("bf16_four_micro", 70, 512, 8, 3, 128, 4),
     W.Workload("bf16_skew_bias", 600, 256, 64, 8, 128, 1, router_bias="log_zipf"),
+    # groups of more than 16 row blocks (about 3000 routes per expert; a 47-block
+    # dense shared segment): the large GEMM walks their row blocks in chunks
+    W.Workload("bf16_long_groups", 6000, 256, 4, 2, 128, 2, shared_inter=128),
     W.Workload("f32_tiny_multi_shared", 45, 128, 4, 2, 64, 2, shared_inter=64, dtype="f32"),
     W.WORKLOADS["tiny_fp32"],
 ]
