@@ -14,6 +14,7 @@
 #include <cuda_bf16.h>
 
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
@@ -55,6 +56,7 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads) finalize_kernel(FinalizeArgs a) {
     __shared__ int64_t rows[kMaxTopK];
     __shared__ float scale[kMaxTopK];
+    ptx::griddep_wait();  // launched early: the expert outputs are complete past here
     const int t = blockIdx.x;
     const int64_t R = (int64_t)a.T * a.k;
     if (threadIdx.x < a.k) {
@@ -92,6 +94,7 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(FinalizeArgs a) {
         }
         store8(y + (int64_t)t * a.H + v * 8, acc);
     }
+    ptx::griddep_launch_dependents();
 }
 
 }  // namespace
@@ -99,11 +102,8 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(FinalizeArgs a) {
 cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t s) {
     if (a.T == 0) return cudaSuccess;
     const dim3 grid(a.T, (a.H / 8 + kThreads - 1) / kThreads);
-    if (a.bf16)
-        finalize_kernel<__nv_bfloat16><<<grid, kThreads, 0, s>>>(a);
-    else
-        finalize_kernel<float><<<grid, kThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    return a.bf16 ? launch_kernel(finalize_kernel<__nv_bfloat16>, grid, dim3(kThreads), 0, s, a.early != 0, a)
+                  : launch_kernel(finalize_kernel<float>, grid, dim3(kThreads), 0, s, a.early != 0, a);
 }
 
 }  // namespace moe

@@ -484,10 +484,14 @@ __device__ __forceinline__ void dequant16_f16(uint4 q, int S, uint32_t* o) {
     const unsigned short hb = e >= -14 ? (unsigned short)((e + 15) << 10) : (unsigned short)(1u << ((e + 24) & 15));
     const __half2 sc = __halves2half2(__ushort_as_half(hb), __ushort_as_half(hb));
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        uint32_t h = ptx::e4m3x2_to_f16x2((uint16_t)(w[i >> 1] >> (16 * (i & 1))));
-        const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&h), sc);
-        o[i] = *reinterpret_cast<const uint32_t*>(&r);
+    for (int i = 0; i < 4; ++i) {
+        uint32_t h[2];
+        ptx::e4m3x4_to_f16x2x2(w[i], h[0], h[1]);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&h[j]), sc);
+            o[2 * i + j] = *reinterpret_cast<const uint32_t*>(&r);
+        }
     }
 }
 
@@ -497,11 +501,15 @@ __device__ __forceinline__ void dequant16_f32(uint4 q, int S, uint32_t* o) {
     const int e = S - 127;
     const float fs = e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(1u << (e + 149));
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        uint32_t h = ptx::e4m3x2_to_f16x2((uint16_t)(w[i >> 1] >> (16 * (i & 1))));
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
-        const __half2 r = __floats2half2_rn(f.x * fs, f.y * fs);
-        o[i] = *reinterpret_cast<const uint32_t*>(&r);
+    for (int i = 0; i < 4; ++i) {
+        uint32_t h[2];
+        ptx::e4m3x4_to_f16x2x2(w[i], h[0], h[1]);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[j]));
+            const __half2 r = __floats2half2_rn(f.x * fs, f.y * fs);
+            o[2 * i + j] = *reinterpret_cast<const uint32_t*>(&r);
+        }
     }
 }
 

@@ -111,6 +111,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         c.abort = 0;
         ptx::fence_mbar_init();
     }
+    // launched early (a.early): the segments and A rows are complete past here.
+    // No early trigger for the next kernel: it starts when this grid ends (a
+    // trigger at the last tile let the finalize's waiting blocks crowd the last
+    // tiles and measured slower on the long steps)
+    ptx::griddep_wait();
     if (a.seg != nullptr) {
         for (int i = threadIdx.x; i <= a.G; i += kThreads) {
             c.seg[i] = a.seg[i];
@@ -315,8 +320,8 @@ cudaError_t launch_tc(const TcGemmArgs& a, const CUtensorMap& tmA, const CUtenso
     const CUtensorMap& b1 = a.n_micro > 1 ? tmB[1] : tmB[0];
     const CUtensorMap& b2 = a.n_micro > 2 ? tmB[2] : tmB[0];
     const CUtensorMap& b3 = a.n_micro > 3 ? tmB[3] : tmB[0];
-    tc_gemm_kernel<SWIGLU><<<grid, kThreads, kSmemBytes, s>>>(tmA, tmB[0], b1, b2, b3, a);
-    return cudaGetLastError();
+    return launch_kernel(tc_gemm_kernel<SWIGLU>, dim3(grid), dim3(kThreads), kSmemBytes, s, a.early != 0, tmA,
+                         tmB[0], b1, b2, b3, a);
 }
 
 }  // namespace

@@ -6,8 +6,30 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 namespace moe {
+
+// Launches `kernel` on `s`. With `early` set, programmatic stream
+// serialization: its CTAs may be placed while the previous kernel in the
+// stream is still running, and the kernel executes griddepcontrol.wait (which
+// returns once that grid has completed and its writes are visible) before it
+// touches global memory. Without it, an ordinary launch.
+template <typename... P, typename... A>
+inline cudaError_t launch_kernel(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                 bool early, A&&... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = early ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<A>(args)...);
+}
 
 // Bits of the device error word.
 enum DeviceError : int {
@@ -105,6 +127,7 @@ struct GatherArgs {
     uint64_t limit_ns;
     int num_sms;
     const int32_t* inv;       // [R] inverse of perm (launch_gather)
+    int early;                // launch while the previous kernel in the stream finishes
 };
 // xp[inv[t*k + j]] = x[t] for every token t and slot j: each row of x is read
 // once and written to its k routes' positions.
@@ -120,6 +143,7 @@ struct FinalizeArgs {
     bool bf16;
     void* y;                  // [T][H]
     bool accumulate;          // y += result instead of y = result
+    int early;                // launch while the previous kernel in the stream finishes
 };
 cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t s);
 
@@ -147,6 +171,7 @@ struct TcGemmArgs {
     int* err;
     uint64_t limit_ns;
     int dense_rows;           // rows of the dense segment when seg is null
+    int early;                // launch while the previous kernel in the stream finishes
 };
 // tmA: A [rows][K] bf16, box {64, 128}. tmB[m]: SwiGLU: w13_m [G][2I][K] bf16 as a
 // 3D map {K, I, 2G} with box {64, 128, 2} (128 gate rows and the matching up rows);

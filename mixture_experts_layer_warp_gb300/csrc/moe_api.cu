@@ -237,7 +237,9 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
     }
 
     if (!small_bf16) {  // small bf16 batches gather inside the fused GEMM launch
-        GatherArgs ga{x, h->perm, (int)R, k, (uint32_t)(H * h->esz), h->xp, h->err, h->limit_ns, h->num_sms, h->inv};
+        // launched early behind the placement kernel (not behind the fork's event record)
+        GatherArgs ga{x,      h->perm,        (int)R, k, (uint32_t)(H * h->esz), h->xp, h->err, h->limit_ns,
+                      h->num_sms, h->inv, fork ? 0 : 1};
         if ((e = timed(h, kSlotGather, s, [&] { return launch_gather(ga, s); })) != cudaSuccess)
             return cuda_err(h, e, "gather launch");
     }
@@ -333,6 +335,7 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
                 return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (w13[%d])", m);
         TcGemmArgs g1{h->offsets, h->tiles_tc, E, M, H / kTcBK, I / 128, 2 * I, I, 0,
                       h->hbuf, (int64_t)M * I, I, M * routed_tiles_tc * (I / 128), h->err, h->limit_ns};
+        g1.early = 1;  // behind the gather
         if ((e = timed(h, kSlotGemm1, s, [&] { return launch_tc_gemm_swiglu(g1, tmA, tmB, h->num_sms, s); })) != cudaSuccess)
             return cuda_err(h, e, "GEMM1 launch");
         // GEMM2: h [R][M*I] x w2[m] [E*H][I], summed over m -> o [R][H]
@@ -343,6 +346,7 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
                 return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (w2[%d])", m);
         TcGemmArgs g2{h->offsets, h->tiles_tc, E, M, I / kTcBK, H / 256, H, 0, I,
                       h->obuf, (int64_t)H, 0, routed_tiles_tc * (H / 256), h->err, h->limit_ns};
+        g2.early = 1;  // behind GEMM1
         if ((e = timed(h, kSlotGemm2, s, [&] { return launch_tc_gemm_down(g2, tmA, tmB, h->num_sms, s); })) != cudaSuccess)
             return cuda_err(h, e, "GEMM2 launch");
         if (Is > 0 && !fork) {
@@ -351,12 +355,14 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
                 return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (shared GEMM1)");
             TcGemmArgs s1{h->shared_meta, h->shared_meta + 2, 1, 1, H / kTcBK, Is / 128, 2 * Is, Is, 0,
                           h->hs, (int64_t)Is, 0, stiles * (Is / 128), h->err, h->limit_ns};
+            s1.early = 1;  // behind the routed GEMM2
             if ((e = timed(h, kSlotSharedGemm1, s, [&] { return launch_tc_gemm_swiglu(s1, tmA, tmB, h->num_sms, s); })) != cudaSuccess)
                 return cuda_err(h, e, "shared GEMM1 launch");
             if (!encode_2d(&tmA, h->hs, Is, T, (uint64_t)Is * 2) || !encode_w2_tc(&tmB[0], sw2, Is, H))
                 return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (shared GEMM2)");
             TcGemmArgs s2{h->shared_meta, h->shared_meta + 2, 1, 1, Is / kTcBK, H / 256, H, 0, Is,
                           h->sbuf, (int64_t)H, 0, stiles * (H / 256), h->err, h->limit_ns};
+            s2.early = 1;  // behind the shared GEMM1
             if ((e = timed(h, kSlotSharedGemm2, s, [&] { return launch_tc_gemm_down(s2, tmA, tmB, h->num_sms, s); })) != cudaSuccess)
                 return cuda_err(h, e, "shared GEMM2 launch");
         }
@@ -422,8 +428,9 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
     }
     if (fork && (e = cudaStreamWaitEvent(s, h->ev_join, 0)) != cudaSuccess) return cuda_err(h, e, "shared-expert join");
     if (!small_bf16) {  // small bf16 batches finalize inside the fused GEMM launch
+        // launched early behind the last GEMM (not behind the join's event wait)
         FinalizeArgs fa{h->obuf, h->inv, h->topw, Is > 0 ? h->sbuf : nullptr, T, k, H, c.dtype == MOE_BF16, y,
-                        h->accumulate};
+                        h->accumulate, fork ? 0 : 1};
         if ((e = timed(h, kSlotFinalize, s, [&] { return launch_finalize(fa, s); })) != cudaSuccess)
             return cuda_err(h, e, "finalize launch");
     }

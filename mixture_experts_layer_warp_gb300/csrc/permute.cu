@@ -26,6 +26,7 @@ constexpr int kScanThreads = 1024;
 __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
     __shared__ int part[kScanThreads];   // [parts][E]
     __shared__ int off[kMaxExperts + 1];
+    ptx::griddep_wait();  // launched early: the router's histograms are complete past here
     const int E = a.E, NB = a.NB;
     const int parts = kScanThreads / E;
     const int tid = threadIdx.x;
@@ -77,6 +78,9 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
             run += a.blk_hist[(int64_t)b * E + e];
         }
     }
+    // the next kernel is placed once every CTA got here (a trigger at the start
+    // let the next kernels' waiting CTAs crowd this one and measured slower)
+    ptx::griddep_launch_dependents();
 }
 
 constexpr int kPlaceWarps = 8;
@@ -85,6 +89,7 @@ __global__ void __launch_bounds__(kPlaceWarps * 32) place_kernel(PlaceArgs a) {
     __shared__ int sid[kRouterTokensTc * kMaxTopK];
     __shared__ int cnt[kPlaceWarps][kMaxExperts];
     __shared__ int run[kPlaceWarps][kMaxExperts];
+    ptx::griddep_wait();  // launched early: the scan's bases are complete past here
     const int64_t R = (int64_t)a.T * a.k;
     const int64_t r0 = (int64_t)blockIdx.x * a.tok_per_blk * a.k;
     const int64_t left = R - r0;
@@ -93,6 +98,7 @@ __global__ void __launch_bounds__(kPlaceWarps * 32) place_kernel(PlaceArgs a) {
     __syncthreads();
     const int32_t* base = a.blk_base + (int64_t)blockIdx.x * a.E;
     place_chunk<kPlaceWarps>(sid, n, r0, a.E, R, [&](int e) { return base[e]; }, cnt, run, a.perm, a.inv, a.err);
+    ptx::griddep_launch_dependents();
 }
 
 // The gather xp[i] = x[perm[i] / k], run as the equivalent scatter
@@ -112,6 +118,7 @@ __device__ __forceinline__ uint4 ld_nc_v4(const uint4* p) {
 }
 
 __global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherArgs a) {
+    ptx::griddep_wait();  // launched early: the permutation is complete past here
     const int lane = threadIdx.x & 31;
     const int64_t T = a.R / a.k;
     const int64_t nwarps = ((int64_t)gridDim.x * kGatherThreads) >> 5;
@@ -139,19 +146,18 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherArgs a) {
             }
         }
     }
+    ptx::griddep_launch_dependents();
 }
 
 }  // namespace
 
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s) {
-    scan_kernel<<<1, kScanThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_kernel(scan_kernel, dim3(1), dim3(kScanThreads), 0, s, true, a);
 }
 
 cudaError_t launch_place(const PlaceArgs& a, cudaStream_t s) {
     if (a.NB == 0) return cudaSuccess;
-    place_kernel<<<a.NB, kPlaceWarps * 32, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_kernel(place_kernel, dim3(a.NB), dim3(kPlaceWarps * 32), 0, s, true, a);
 }
 
 cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s) {
@@ -159,8 +165,7 @@ cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s) {
     constexpr int kWarps = kGatherThreads / 32;
     const int64_t T = a.R / a.k;
     const int64_t grid = std::min<int64_t>((T + kWarps - 1) / kWarps, (int64_t)a.num_sms * 8);
-    gather_kernel<<<(unsigned)grid, kGatherThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_kernel(gather_kernel, dim3((unsigned)grid), dim3(kGatherThreads), 0, s, a.early != 0, a);
 }
 
 }  // namespace moe

@@ -315,11 +315,14 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
     return (1u << 4) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
 }
 
-// Two FP8 E4M3 codes (the low byte is the first) to two f16, exactly.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
-    uint32_t r;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
-    return r;
+// Four FP8 E4M3 codes (bytes 0..3 of w) to four f16, exactly: bytes 0-1 ->
+// lo, 2-3 -> hi (the lower byte in the lower half). The word is split into its
+// 16-bit halves in PTX, so no shift precedes the second conversion.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
 }
 
 // Shared-memory matrix descriptor of a K-major operand tile whose rows are
