@@ -194,6 +194,30 @@ def test_back_to_back_small_batches_reuse_the_workspace():
         assert torch.equal(ys[i], ref) and torch.equal(ys[i + 3], ref)
 
 
+def test_mixed_batch_sizes_back_to_back_match_isolated_calls():
+    """Calls of different sizes issued back to back on one stream, no sync in
+    between: each call's kernels may be placed while the previous kernel in the
+    stream still runs (programmatic dependent launch: the fused small-batch
+    kernel, the router, and the large-batch scan, placement, gather, GEMMs and
+    finalize), and small and large calls share the workspace. Every result must
+    equal the same call run on its own."""
+    base = W.Workload("mix", 300, 512, 16, 4, 128, 2, shared_inter=128)
+    wts = parity.to_device(W.make_inputs(base, seed=0))
+    args = (wts["router_w"], wts["router_bias"], wts["w13"], wts["w2"], wts["shared_w13"], wts["shared_w2"])
+    Ts = [300, 8, 257, 16, 1, 300, 13, 129, 8]
+    xs = [W.make_inputs(base, seed=40 + i, T=T, experts=False)["x"].cuda() for i, T in enumerate(Ts)]
+    layer = _layer(base)
+    outs = [torch.empty_like(x) for x in xs]
+    for x, y in zip(xs, outs):
+        layer.forward(x, *args, out=y)
+    layer.sync()
+    for T, x, y in zip(Ts, xs, outs):
+        ref = layer.forward(x, *args)
+        layer.sync()
+        assert torch.equal(y, ref), f"T={T}: back-to-back result differs from the isolated call"
+    layer.close()
+
+
 @pytest.mark.parametrize("wl", [W.Workload("side_17", 17, 512, 8, 2, 256, 2, shared_inter=128),
                                 W.Workload("side_257", 257, 256, 16, 4, 128, 2, shared_inter=256)],
                          ids=lambda w: w.name)

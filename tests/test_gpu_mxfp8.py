@@ -133,3 +133,29 @@ def test_scales_outside_the_f16_range_take_the_exact_path():
     layer.sync()
     layer.close()
     _check(wl, inp, y, w13_q, w2_q)
+
+
+def test_mxfp8_and_bf16_calls_back_to_back_match_isolated_calls():
+    """MXFP8 decode-sized calls interleaved with bf16 calls of both sizes on one
+    handle and stream, no sync in between, equal the same calls run alone."""
+    base = W.Workload("mx_mix", 200, 512, 16, 4, 256, 1)
+    wts = parity.to_device(W.make_inputs(base, seed=0))
+    w13_q, w2_q = _quantize_experts(wts)
+    layer = binding.MoELayer(base.H, base.E, base.k, base.I, 1, max_tokens=base.T)
+    plan = [("mx", 8), ("bf16", 200), ("mx", 16), ("bf16", 8), ("mx", 1), ("bf16", 200), ("mx", 8)]
+    xs = [W.make_inputs(base, seed=60 + i, T=T, experts=False)["x"].cuda() for i, (_, T) in enumerate(plan)]
+
+    def call(kind, x, out=None):
+        if kind == "mx":
+            return layer.forward_mxfp8(x, wts["router_w"], None, w13_q, w2_q, out=out)
+        return layer.forward(x, wts["router_w"], None, wts["w13"], wts["w2"], out=out)
+
+    outs = [torch.empty_like(x) for x in xs]
+    for (kind, _), x, y in zip(plan, xs, outs):
+        call(kind, x, y)
+    layer.sync()
+    for (kind, T), x, y in zip(plan, xs, outs):
+        ref = call(kind, x)
+        layer.sync()
+        assert torch.equal(y, ref), f"{kind} T={T}: back-to-back result differs from the isolated call"
+    layer.close()
