@@ -194,6 +194,32 @@ def test_back_to_back_small_batches_reuse_the_workspace():
         assert torch.equal(ys[i], ref) and torch.equal(ys[i + 3], ref)
 
 
+def test_empty_batches_return_empty_outputs_and_leave_the_handle_usable():
+    """T = 0 through the device and host entry points (and the MXFP8 one) is a
+    no-op that returns an empty y; the next call on the handle still matches
+    the oracle."""
+    wl = W.Workload("empty", 40, 512, 16, 4, 128, 2, shared_inter=128)
+    inp = W.make_inputs(wl, seed=9)
+    dev = parity.to_device(inp)
+    args = (dev["router_w"], dev["router_bias"], dev["w13"], dev["w2"], dev["shared_w13"], dev["shared_w2"])
+    layer = _layer(wl)
+    x0 = torch.empty((0, wl.H), dtype=torch.bfloat16, device="cuda")
+    assert layer.forward(x0, *args).shape == (0, wl.H)
+    assert layer.forward_host(torch.empty((0, wl.H), dtype=torch.bfloat16), *args).shape == (0, wl.H)
+    layer.sync()
+    y = _forward(layer, dev)
+    _check(wl, inp, y)
+    layer.close()
+    mx = W.Workload("empty_mx", 8, 512, 16, 4, 128, 1)
+    mdev = parity.to_device(W.make_inputs(mx, seed=9))
+    q13 = [binding.quantize_mxfp8(t) for t in mdev["w13"]]
+    q2 = [binding.quantize_mxfp8(t) for t in mdev["w2"]]
+    mlayer = binding.MoELayer(mx.H, mx.E, mx.k, mx.I, 1, max_tokens=mx.T)
+    assert mlayer.forward_mxfp8(x0, mdev["router_w"], None, q13, q2).shape == (0, mx.H)
+    mlayer.sync()
+    mlayer.close()
+
+
 def test_mixed_batch_sizes_back_to_back_match_isolated_calls():
     """Calls of different sizes issued back to back on one stream, no sync in
     between: each call's kernels may be placed while the previous kernel in the
