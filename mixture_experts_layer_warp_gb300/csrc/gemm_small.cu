@@ -1054,13 +1054,7 @@ cudaError_t launch_small(const SmallMaps& maps, const SmallParams& p, int max_ti
     if (max_tiles <= 0) return cudaSuccess;
     constexpr int smem = F8 ? kF8SmemBytes : kSmemBytes;
     constexpr int threads = F8 ? kF8Threads : kThreads;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e =
-            cudaFuncSetAttribute(tc_small_kernel<MODE, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    if (cudaError_t e = ensure_smem_limit<tc_small_kernel<MODE, F8>>(smem); e != cudaSuccess) return e;
     const int grid = max_tiles < num_sms ? max_tiles : num_sms;
     if (MODE == kFused) {
         // may start while the previous kernel in the stream still runs; the

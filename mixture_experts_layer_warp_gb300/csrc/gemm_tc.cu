@@ -309,13 +309,7 @@ template <bool SWIGLU>
 cudaError_t launch_tc(const TcGemmArgs& a, const CUtensorMap& tmA, const CUtensorMap* tmB, int num_sms,
                       cudaStream_t s) {
     if (a.max_tiles <= 0) return cudaSuccess;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kSmemBytes);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    if (cudaError_t e = ensure_smem_limit<tc_gemm_kernel<SWIGLU>>(kSmemBytes); e != cudaSuccess) return e;
     const int grid = a.max_tiles < num_sms ? a.max_tiles : num_sms;
     const CUtensorMap& b1 = a.n_micro > 1 ? tmB[1] : tmB[0];
     const CUtensorMap& b2 = a.n_micro > 2 ? tmB[2] : tmB[0];

@@ -4,11 +4,28 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <utility>
 
 namespace moe {
+
+// Raises the dynamic shared-memory limit of `Kernel` to `bytes` on the current
+// device, once per device (the attribute is per device; a process may drive
+// several GPUs). One instantiation, and so one record, per kernel.
+template <auto Kernel>
+inline cudaError_t ensure_smem_limit(int bytes) {
+    static std::atomic<uint64_t> done{0};  // bit d: set on device d
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev >= 0 && dev < 64 ? (uint64_t)1 << dev : 0;
+    if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+    e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_release);
+    return e;
+}
 
 // Launches `kernel` on `s`. With `early` set, programmatic stream
 // serialization: its CTAs may be placed while the previous kernel in the

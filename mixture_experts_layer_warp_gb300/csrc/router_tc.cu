@@ -665,13 +665,7 @@ cudaError_t launch_router_tc(const RouterTcArgs& a, const CUtensorMap& tmX, cons
                              cudaStream_t s) {
     const int nb = (a.T + kTok - 1) / kTok;
     if (nb == 0) return cudaSuccess;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e =
-            cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    if (cudaError_t e = ensure_smem_limit<router_tc_kernel>(kSmemBytes); e != cudaSuccess) return e;
     return launch_early(router_tc_kernel, dim3(nb), kSmemBytes, s, tmX, tmW, a);
 }
 
@@ -679,13 +673,7 @@ cudaError_t launch_router_tc_small(const RouterTcArgs& a, const CUtensorMap& tmX
                                    cudaStream_t s) {
     if (a.T <= 0) return cudaSuccess;
     if (a.T > kCTok) return cudaErrorInvalidValue;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(router_tc_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kCSmemBytes);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    if (cudaError_t e = ensure_smem_limit<router_tc_cluster_kernel>(kCSmemBytes); e != cudaSuccess) return e;
     return launch_early(router_tc_cluster_kernel, dim3(kCluster), kCSmemBytes, s, tmX, tmW, a);
 }
 
