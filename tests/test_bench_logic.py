@@ -1,0 +1,78 @@
+"""Host logic of the benchmark, without a GPU: the roofline's peak choice and
+algorithmic work, the traffic records' keying to the kernels' sources, and the
+whole-job throughput."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import bench
+from mixture_experts_layer_warp_gb300 import workloads as W
+
+PEAKS = dict(hbm=6783.1, bf16=1891.6, bf16_sustained=1690.3, source="measured")
+
+
+def _large_prof(gemm1_ms, n=10):
+    # total ms and launches per slot, as the profiling pass returns them
+    return {"router": (0.05 * n, n), "gemm1_swiglu": (gemm1_ms * n, n), "gemm2_down": (gemm1_ms * n / 2, n)}
+
+
+def test_large_gemm_is_rated_against_burst_unless_a_long_step_ran_power_capped():
+    wl = W.WORKLOADS["cfg_shared"]
+    ids = [np.zeros((wl.T, wl.k), np.int32)]
+    capped, free = {"reasons": ["sw_power_cap"]}, {"reasons": []}
+    flops = 4 * wl.T * wl.k * wl.H * wl.I * wl.n_micro
+    r = bench.roofline_of(wl, _large_prof(8.0), ids, 1, PEAKS, 15.0, capped)
+    assert r["bound"] == "tensor" and r["kernel"] == "gemm1_swiglu"
+    assert r["peak"] == PEAKS["bf16_sustained"] and r["peak_kind"].startswith("sustained")
+    assert r["achieved"] == pytest.approx(flops / 8.0e-3 / 1e12)
+    assert r["frac"] == pytest.approx(r["achieved"] / PEAKS["bf16_sustained"])
+    assert r["frac_burst"] == pytest.approx(r["achieved"] / PEAKS["bf16"])
+    for step_ms, clocks in [(15.0, free), (15.0, None), (1.5, capped)]:
+        other = bench.roofline_of(wl, _large_prof(8.0), ids, 1, PEAKS, step_ms, clocks)
+        assert other["peak"] == PEAKS["bf16"] and other["peak_kind"].startswith("burst")
+
+
+def test_decode_is_rated_against_hbm_over_the_touched_experts():
+    wl = W.WORKLOADS["decode"]
+    ids = [(np.arange(wl.T * wl.k, dtype=np.int32) % 40).reshape(wl.T, wl.k)]  # 40 experts touched
+    prof = {"router": (0.1, 10), "gemm1_swiglu": (1.3, 10)}  # the fused launch: no separate GEMM2
+    r = bench.roofline_of(wl, prof, ids, 1, PEAKS, 0.13, None)
+    assert r["bound"] == "hbm" and r["peak"] == PEAKS["hbm"]
+    assert r["kernel"].startswith("gemm1_swiglu+gemm2_down+finalize")
+    weights = 40 * 3 * wl.I * wl.H * 2
+    assert weights < r["algorithmic_per_launch"] < weights + 2e6  # plus token rows, h, o, y
+    assert r["achieved"] == pytest.approx(r["algorithmic_per_launch"] / 0.13e-3 / 1e9)
+    mx = bench.roofline_of(wl, prof, ids, 1, PEAKS, 0.09, None, mxfp8=True)
+    assert mx["algorithmic_per_launch"] < 0.6 * r["algorithmic_per_launch"]  # 1 + 1/32 bytes per weight
+
+
+def test_traffic_records_are_used_only_for_matching_sources(tmp_path, monkeypatch):
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "traffic.txt").write_text("# a comment line\ndecode gemm1_swiglu abc 123\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.recorded_traffic("decode", "gemm1_swiglu", "abc") == 123.0
+    assert bench.recorded_traffic("decode", "gemm1_swiglu", "abd") is None
+    assert bench.recorded_traffic("decode_mxfp8", "gemm1_swiglu", "abc") is None
+    assert bench.recorded_traffic("decode", "gemm2_down", "abc") is None
+
+
+def test_kernel_source_lists_cover_everything_their_kernels_include():
+    d = os.path.join(bench.ROOT, "mixture_experts_layer_warp_gb300", "csrc")
+    for kind, files in bench.KERNEL_SOURCES.items():
+        seen, todo = set(), [files[0]]
+        while todo:
+            f = todo.pop()
+            if f not in seen:
+                seen.add(f)
+                with open(os.path.join(d, f)) as src:
+                    todo += re.findall(r'#include "([^"]+)"', src.read())
+        assert seen <= set(files), (kind, sorted(seen - set(files)))
+        assert len(bench.src_sha(kind)) == 16
+    assert bench.src_sha("small") != bench.src_sha("large")
+
+
+def test_one_process_throughput_is_tokens_over_time():
+    ms, tps = bench.job_throughput(1, 8, 10, 1.5)
+    assert ms == 1.5 and tps == pytest.approx(8 * 10 / 1.5e-3)
