@@ -15,7 +15,13 @@
  *     must stay valid until the work enqueued on the stream has finished.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream). Calls enqueue asynchronously and never synchronise, except
- *     moe_sync and moe_forward_host as documented.
+ *     moe_sync and moe_forward_host as documented. Work is ordered exactly as
+ *     stream order: the library's kernels use programmatic dependent launch
+ *     (a kernel may be placed on SMs while the previous kernel in the stream
+ *     finishes), but each waits for that kernel to complete before it touches
+ *     global memory. A kernel launched after a call sees all its results; if
+ *     it uses programmatic dependent launch itself, it must wait likewise
+ *     (griddepcontrol.wait) before reading them.
  *   - After moe_create, no call allocates device memory: the handle owns a
  *     workspace sized for cfg.max_tokens.
  *   - Errors are returned, never raised or aborted. A kernel-side failure
