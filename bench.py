@@ -5,10 +5,16 @@
 
 A step is one call of the whole layer (router, scan, placement, gather,
 GEMM1+SwiGLU, GEMM2, shared expert if any, finalize) on one batch of seeded
-synthetic tokens whose inputs are already in HBM. The default workload is the
-AR-decode-shaped layer (8 tokens, H=4096, 64 experts, top-8, I=768). Between
-steps the token batch rotates through a pool, so each step routes to a
-different expert set; the expert weights (1.2 GB) are larger than L2.
+synthetic tokens whose inputs are already in HBM. The headline workload is the
+largest configuration that fits one GPU: the CFG-doubled denoise layer (32768
+tokens, H=4096, 64 experts, top-8, two micro-shards of I=1536, and a dense
+shared expert of 3072). Between steps the token batch rotates through a pool of
+seeded batches; the expert weights (4.9 GB) are far larger than L2.
+
+The same JSON line carries, under "workloads", one record per other
+configuration (AR decode, decode with MXFP8 expert weights, the two-micro
+denoise, the skewed large denoise, the tiny fp32 layer), each with its own
+timing, roofline, end-to-end figure and CPU-oracle baseline.
 
 Prints one JSON line on rank 0. ``--impl reference`` times the fp64 CPU oracle
 on the host cores instead (rank 0 only).
@@ -16,6 +22,7 @@ on the host cores instead (rank 0 only).
 from __future__ import annotations
 
 import argparse
+import gc
 import hashlib
 import math
 import json
@@ -25,6 +32,7 @@ import subprocess
 import sys
 import tempfile
 import time
+import traceback
 
 import numpy as np
 import torch
@@ -37,6 +45,11 @@ from mixture_experts_layer_warp_gb300 import workloads as W  # noqa: E402
 
 METRIC = "MoE-layer tokens/s on 1 GB300; % of binding roof (bf16 TC peak or HBM)"
 POOL = 8  # distinct token batches rotated through the timed steps
+HEADLINE = "cfg_shared"
+# the other configurations, measured in the same run ("decode_mxfp8": the
+# decode workload with MXFP8 expert weights)
+SUB_WORKLOADS = ("decode", "decode_mxfp8", "denoise_multi_micro", "skewed", "tiny_fp32")
+FP32_LANES_PER_SM = 128  # FP32 FMA units per SM (one FMA = 2 flop per clock)
 
 
 def load_peaks():
@@ -44,9 +57,16 @@ def load_peaks():
     if os.path.exists(path):
         with open(path) as f:
             p = json.load(f)
-        return dict(hbm=p["hbm_gbs"], bf16=p["bf16_tflops"], bf16_sustained=p["bf16_tflops_sustained"],
-                    source="measured")
-    return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+        out = dict(hbm=p["hbm_gbs"], bf16=p["bf16_tflops"], bf16_sustained=p["bf16_tflops_sustained"],
+                   sm_max_mhz=p.get("sm_max_mhz", 2070.0), source="measured")
+    else:
+        out = dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, sm_max_mhz=2070.0, source="fallback")
+    sms = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 152
+    # plain fp32 FMA arithmetic (the exact-fp32 GEMMs of fp32 layers): every
+    # FP32 lane of every SM retiring one FMA per clock at the maximum SM clock
+    out["fp32_alu"] = sms * FP32_LANES_PER_SM * 2 * out["sm_max_mhz"] * 1e6 / 1e12
+    out["sms"] = sms
+    return out
 
 
 # ---------------------------------------------------------------- clocks
@@ -102,8 +122,9 @@ class ClockSampler:
         sm = [float(r[1]) for r in rows]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        watts = [float(r[3]) for r in rows if r[3] not in ("", "[N/A]")]
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]), "reasons": reasons,
-                "samples": len(rows), "power_w_max": max(float(r[3]) for r in rows if r[3] not in ("", "[N/A]")),
+                "samples": len(rows), "power_w_max": max(watts) if watts else None,
                 "window": f"the timed steps plus {ROLL_S} s of the same steps run back to back before and "
                           f"after them (nvidia-smi samples every 200 ms)"}
 
@@ -205,21 +226,26 @@ def routing_check(layer, wl, x, inp, weights) -> dict:
     """The routing contract on one timed batch: the oracle's fp64 logits,
     rounded to fp32, against the CUDA routing of the same batch. A token is
     undecided when its k-th and (k+1)-th logits (set) or two adjacent top-k
-    logits (order) lie within 2 * ROUTE_TAU, so either choice is correct;
-    every decided token must carry the oracle's ids in the oracle's order."""
+    logits (order) lie within 2 * tau, so either choice is correct; every
+    decided token must carry the oracle's ids in the oracle's order. fp32
+    layers form their logits exactly enough that tau is 0 there."""
     import oracle
+    tau = ROUTE_TAU if wl.dtype == "bf16" else 0.0
     lg = oracle.logits(W.to_numpy(x), weights["router_w"], weights["router_bias"])
     ids_o, _ = oracle.route(lg, wl.k)
     ids_g = layer.route(x, inp["router_w"], inp["router_bias"])["ids"].cpu().numpy()
     lf = lg.astype(np.float32).astype(np.float64)
     srt = -np.sort(-lf, axis=1)
     k, E = wl.k, wl.E
-    set_ok = (srt[:, k - 1] - srt[:, k]) > 2 * ROUTE_TAU if k < E else np.ones(len(lf), bool)
-    order_ok = set_ok & np.all((srt[:, :k - 1] - srt[:, 1:k]) > 2 * ROUTE_TAU, axis=1)
+    set_ok = (srt[:, k - 1] - srt[:, k]) > 2 * tau if k < E else np.ones(len(lf), bool)
+    order_ok = set_ok & np.all((srt[:, :k - 1] - srt[:, 1:k]) > 2 * tau, axis=1)
+    if tau == 0:
+        set_ok[:] = True
+        order_ok[:] = True
     return {"tokens": int(len(lf)), "set_undecided": int((~set_ok).sum()),
             "order_undecided": int((~order_ok).sum()),
             "decided_mismatch": int((order_ok & np.any(ids_g != ids_o, axis=1)).sum()),
-            "tau": ROUTE_TAU}
+            "tau": tau}
 
 
 def host_weights(inp):
@@ -247,6 +273,7 @@ def run_reference(args, wl, world, rank):
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     inp = W.make_inputs(wl, seed=0, device=dev)
     weights = host_weights(inp)
+    del inp
     Ts = sample_tokens(wl)
     pool = [W.to_numpy(W.make_inputs(wl, seed=100 + i, device=dev, experts=False, T=Ts)["x"])
             for i in range(max(2, min(POOL, args.steps)))]
@@ -273,23 +300,34 @@ def run_reference(args, wl, world, rank):
     print(json.dumps(line), flush=True)
 
 
-def config_of(wl):
-    return {"workload": wl.name, "T": wl.T, "hidden": wl.H, "experts": wl.E, "top_k": wl.k, "inter": wl.I,
-            "n_micro": wl.n_micro, "shared_inter": wl.shared_inter,
-            "router": wl.router_init + ("+log_zipf_bias" if wl.router_bias else ""),
-            "l2": "inputs larger than L2: expert weights exceed the 129 MB L2; token batches rotate over "
-                  f"{POOL} seeded batches"}
+def config_of(wl, mx=False):
+    cfg = {"workload": wl.name, "T": wl.T, "hidden": wl.H, "experts": wl.E, "top_k": wl.k, "inter": wl.I,
+           "n_micro": wl.n_micro, "shared_inter": wl.shared_inter, "dtype": wl.dtype,
+           "router": wl.router_init + ("+log_zipf_bias" if wl.router_bias else ""),
+           "l2": "inputs larger than L2: expert weights exceed the 129 MB L2; token batches rotate over "
+                 f"{POOL} seeded batches"}
+    if wl.T * wl.E * wl.H < 2 ** 25:  # the tiny layer: weights fit in L2
+        cfg["l2"] = f"inputs smaller than L2 (a correctness-sized layer); token batches rotate over {POOL} " \
+                    "seeded batches"
+    if mx:
+        cfg["weights"] = "mxfp8 (E4M3 codes, E8M0 scale per 32 along K)"
+    return cfg
 
 
-# The sustained bf16 peak (a seconds-long GEMM loop) is the ceiling of GEMMs
-# that run for milliseconds at a time under the board power limit. A step at
-# least this long whose timed region the clock samples show power-capped is
-# rated against it; any other step against the burst peak.
-LONG_STEP_MS = 2.0
+def gemm_flops(wl) -> dict:
+    """Algorithmic flops per launch of each GEMM slot (padding never counts)."""
+    R = wl.T * wl.k
+    return {"gemm1_swiglu": 4 * R * wl.H * wl.I * wl.n_micro, "gemm2_down": 2 * R * wl.H * wl.I * wl.n_micro,
+            "shared_gemm1": 4 * wl.T * wl.H * wl.shared_inter, "shared_gemm2": 2 * wl.T * wl.H * wl.shared_inter}
 
 
 def roofline_of(wl, prof, ids_pool, steps, peaks, step_ms, clocks, mxfp8=False):
-    """Roofline of the kernel with the largest share of the timed region."""
+    """Roofline of the kernel with the largest share of the timed region.
+
+    Decode-sized bf16 layers are bound by HBM (the touched experts' weights),
+    the large bf16 layers by the tensor cores (rated against the burst bf16
+    peak; the fraction of the sustained peak is reported beside it), fp32
+    layers by plain FP32 FMA arithmetic."""
     dom, (ms, n) = max(prof.items(), key=lambda kv: kv[1][0])
     per_launch_s = ms / n / 1e3
     R = wl.T * wl.k
@@ -298,8 +336,16 @@ def roofline_of(wl, prof, ids_pool, steps, peaks, step_ms, clocks, mxfp8=False):
     # touched experts per step, averaged over the batches the timed steps used
     touched = statistics.mean(len(np.unique(ids_pool[i % len(ids_pool)])) for i in range(steps))
     I, H, M = wl.I, wl.H, wl.n_micro
-    fused = "gemm2_down" not in prof  # small batches run both GEMMs in one launch
-    if wl.name == "decode":
+    fused = "gemm2_down" not in prof and wl.dtype == "bf16"  # small batches run both GEMMs in one launch
+    flops = gemm_flops(wl)
+    extra = {}
+    if wl.dtype == "f32":
+        bound, unit, peak = "alu", "TFLOP/s", peaks["fp32_alu"]
+        algo = flops.get(dom)
+        achieved = algo / per_launch_s / 1e12 if algo else None
+        peak_kind = (f"fp32 FMA peak: {peaks['sms']} SMs x {FP32_LANES_PER_SM} lanes x 2 flop x "
+                     f"{peaks['sm_max_mhz']:g} MHz")
+    elif wl.T <= 16:
         bound, unit, peak = "hbm", "GB/s", peaks["hbm"]
         algo = {
             "gemm1_swiglu": (touched * 3 * I * H * wsz * M + 3 * R * H * esz + 2 * R * M * I * esz + wl.T * H * esz)
@@ -311,32 +357,33 @@ def roofline_of(wl, prof, ids_pool, steps, peaks, step_ms, clocks, mxfp8=False):
             "router": wl.T * H * esz + wl.E * H * esz,
         }.get(dom)
         achieved = algo / per_launch_s / 1e9 if algo else None
+        peak_kind = "measured copy bandwidth"
     else:
-        capped = clocks is not None and "sw_power_cap" in clocks["reasons"]
-        sustained = step_ms >= LONG_STEP_MS and capped
-        bound, unit = "tensor", "TFLOP/s"
-        peak = peaks["bf16_sustained"] if sustained else peaks["bf16"]
-        algo = {"gemm1_swiglu": 4 * R * H * I * M, "gemm2_down": 2 * R * H * I * M,
-                "shared_gemm1": 4 * wl.T * H * wl.shared_inter,
-                "shared_gemm2": 2 * wl.T * H * wl.shared_inter}.get(dom)
+        bound, unit, peak = "tensor", "TFLOP/s", peaks["bf16"]
+        algo = flops.get(dom)
         achieved = algo / per_launch_s / 1e12 if algo else None
+        peak_kind = "burst (measured cuBLAS bf16 GEMM)"
+        if achieved:
+            extra["frac_sustained"] = achieved / peaks["bf16_sustained"]
+        # every GEMM launch of the step together: their flops over their summed time
+        g_ms = sum(prof[s][0] for s in flops if s in prof)
+        g_fl = sum(flops[s] * prof[s][1] for s in flops if s in prof)
+        if g_ms > 0:
+            extra["gemms"] = {"achieved": g_fl / (g_ms / 1e3) / 1e12, "frac": g_fl / (g_ms / 1e3) / 1e12 / peak,
+                              "ms_per_step": g_ms / steps,
+                              "kernels": [s for s in flops if s in prof]}
+        capped = clocks is not None and "sw_power_cap" in clocks.get("reasons", [])
+        extra["power_capped"] = capped
     sha = src_sha("small" if fused else "large")
     traffic = recorded_traffic(wl.name + ("_mxfp8" if mxfp8 else ""), dom, sha)
     out = {"kernel": dom + ("+gemm2_down+finalize (one launch)" if fused and dom == "gemm1_swiglu" else ""),
            "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
            "frac": (achieved / peak) if achieved else None, "traffic": traffic,
-            "algorithmic_per_launch": algo, "launch_ms": per_launch_s * 1e3,
+           "algorithmic_per_launch": algo, "launch_ms": per_launch_s * 1e3,
            "share": ms / sum(v[0] for v in prof.values()), "peak_source": peaks["source"],
+           "peak_kind": peak_kind,
            "timing": "per-kernel CUDA events in a profiling pass of the same steps"}
-    if bound == "tensor":
-        out["peak_kind"] = ("sustained" if sustained else "burst") + \
-            f" (steps of {LONG_STEP_MS:g} ms or more that ran under the power cap are rated against the " \
-            "sustained peak)"
-        if achieved:
-            out["frac_burst"] = achieved / peaks["bf16"]
-            out["frac_sustained"] = achieved / peaks["bf16_sustained"]
-    else:
-        out["peak_kind"] = "measured copy bandwidth"
+    out.update(extra)
     return out
 
 
@@ -383,8 +430,10 @@ def roll_steps(step_ms: float) -> int:
     return int(min(20000, max(1, math.ceil(ROLL_S * 1e3 / max(step_ms, 1e-3)))))
 
 
-def run_ours(args, wl, world, rank, local):
-    peaks = load_peaks()
+def measure(args, wl, world, rank, local, peaks, mx=False, cpu_seconds=12.0, two_dispatch=False) -> dict:
+    """Times `args.steps` layer calls of workload `wl` (inputs resident in HBM),
+    then the per-kernel split, the end-to-end host-buffer path and the CPU
+    oracle; returns the record of the JSON line."""
     inp = W.make_inputs(wl, seed=0, device="cuda")
     pool = [W.make_inputs(wl, seed=100 + i, device="cuda", experts=False)["x"] for i in range(POOL)]
     layer = binding.MoELayer(wl.H, wl.E, wl.k, wl.I, wl.n_micro, max_tokens=wl.T,
@@ -393,7 +442,6 @@ def run_ours(args, wl, world, rank, local):
         layer.set_shared_stream(True)
     y = torch.empty((wl.T, wl.H), dtype=wl.torch_dtype, device="cuda")
     args_w = (inp["router_w"], inp["router_bias"], inp["w13"], inp["w2"], inp["shared_w13"], inp["shared_w2"])
-    mx = args.weights == "mxfp8"
     if mx:  # quantised once, outside every timed region (as weights are at load time)
         args_w = (inp["router_w"], inp["router_bias"], [binding.quantize_mxfp8(t) for t in inp["w13"]],
                   [binding.quantize_mxfp8(t) for t in inp["w2"]], inp["shared_w13"], inp["shared_w2"])
@@ -447,19 +495,21 @@ def run_ours(args, wl, world, rank, local):
     roof = roofline_of(wl, prof, ids_timed, args.steps, peaks, ms / args.steps, clocks, mxfp8=mx)
 
     # end to end through the C ABI with host buffers (pinned), copies included
-    host_pool = [x.cpu().pin_memory() for x in pool]
+    esz = 4 if wl.dtype == "f32" else 2
+    n_host = POOL if wl.T * wl.H * esz <= (64 << 20) else 2  # large batches: two pinned host batches
+    host_pool = [pool[i].cpu().pin_memory() for i in range(n_host)]
     y_host = torch.empty((wl.T, wl.H), dtype=wl.torch_dtype).pin_memory()
     e2e_steps = max(3, min(args.steps, 50))
     x_dev = torch.empty_like(pool[0])
 
     def e2e_step(i):
         if mx:  # no host entry point for MXFP8: pinned copies around the device call
-            x_dev.copy_(host_pool[i % POOL], non_blocking=True)
+            x_dev.copy_(host_pool[i % n_host], non_blocking=True)
             layer.forward_mxfp8(x_dev, *args_w, out=y)
             y_host.copy_(y, non_blocking=True)
             torch.cuda.current_stream().synchronize()
         else:
-            layer.forward_host(host_pool[i % POOL], *args_w, out_host=y_host)
+            layer.forward_host(host_pool[i % n_host], *args_w, out_host=y_host)
 
     for i in range(2):
         e2e_step(i)
@@ -469,12 +519,13 @@ def run_ours(args, wl, world, rank, local):
     for i in range(e2e_steps):
         e2e_step(i)
     _, e2e_value = job_throughput(world, wl.T, e2e_steps, (time.perf_counter() - t0) * 1e3)
-    esz = 4 if wl.dtype == "f32" else 2
     e2e = {"value": e2e_value, "unit": "tokens/s",
-           "h2d_bytes_per_step": wl.T * wl.H * esz, "d2h_bytes_per_step": wl.T * wl.H * esz}
+           "h2d_bytes_per_step": wl.T * wl.H * esz, "d2h_bytes_per_step": wl.T * wl.H * esz,
+           "entry_point": "moe_forward_host" if not mx else "pinned copies around moe_forward_mxfp8"}
+    del host_pool, y_host
 
     two = None
-    if args.two_dispatch and wl.n_micro > 1:
+    if two_dispatch and wl.n_micro > 1 and not mx:
         two = time_two_dispatch(args, wl, inp, pool, ms / args.steps, world)
 
     cpu = rcheck = None
@@ -482,53 +533,98 @@ def run_ours(args, wl, world, rank, local):
         weights = host_weights(inp)
         Ts = sample_tokens(wl)
         hp = [W.to_numpy(x[:Ts]) for x in pool]
-        v, calls, dt, cores = oracle_tokens_per_s(wl, hp, weights, budget_s=args.cpu_seconds)
+        v, calls, dt, cores = oracle_tokens_per_s(wl, hp, weights, budget_s=cpu_seconds)
         cpu = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-               "sample": f"{calls} whole-layer oracle calls of {Ts} tokens ({dt:.1f} s)"}
+               "sample": f"{calls} whole-layer oracle calls of {Ts} of the {wl.T} tokens ({dt:.1f} s)"}
         if wl.T <= 64:  # the small configurations are also timed on one core
             import oracle
             oracle.set_threads(1)
-            v1, calls1, dt1, _ = oracle_tokens_per_s(wl, hp, weights, budget_s=args.cpu_seconds / 2)
+            v1, calls1, dt1, _ = oracle_tokens_per_s(wl, hp, weights, budget_s=cpu_seconds / 2)
             oracle.set_threads(cores)
             cpu["single_core"] = {"value": v1, "unit": "tokens/s", "cores": 1,
                                   "sample": f"{calls1} whole-layer oracle calls of {Ts} tokens ({dt1:.1f} s)"}
         rcheck = routing_check(layer, wl, pool[0], inp, weights)
+        del weights
 
     layer.close()
+    rec = {"value": value, "unit": "tokens/s", "ms_per_step": ms / args.steps, "steps": args.steps,
+           "warmup": args.warmup,
+           "dtype": "f16 (mxfp8 expert weights)" if mx else wl.dtype,
+           "config": dict(config_of(wl, mx), **({"shared_stream": True} if args.shared_stream else {})),
+           "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+           "kernels_ms_per_step": {k: v[0] / args.steps for k, v in prof.items()},
+           "clocks": clocks}
+    if rcheck is not None:
+        rec["routing_check"] = rcheck
+    if two is not None:
+        rec["two_dispatch"] = two
+    del inp, pool, y, args_w, layer
+    gc.collect()
+    torch.cuda.empty_cache()
+    return rec
+
+
+def sub_workload(name):
+    """(Workload, mxfp8 weights?) of a name in SUB_WORKLOADS."""
+    if name.endswith("_mxfp8"):
+        return W.WORKLOADS[name[: -len("_mxfp8")]], True
+    return W.WORKLOADS[name], False
+
+
+def run_ours(args, wl, world, rank, local):
+    peaks = load_peaks()
+    mx = args.weights == "mxfp8"
+    head = measure(args, wl, world, rank, local, peaks, mx=mx, cpu_seconds=args.cpu_seconds,
+                   two_dispatch=args.two_dispatch)
+    subs = {}
+    if not args.no_sub:
+        for name in SUB_WORKLOADS:
+            swl, smx = sub_workload(name)
+            if swl.name == wl.name and smx == mx:
+                continue
+            try:
+                subs[name] = measure(args, swl, world, rank, local, peaks, mx=smx, cpu_seconds=args.sub_cpu_seconds,
+                                     two_dispatch=args.two_dispatch)
+            except Exception as exc:  # noqa: BLE001 - recorded in the line; the headline stands
+                subs[name] = {"error": f"{type(exc).__name__}: {exc}"}
+                traceback.print_exc()
     if rank != 0:
         return
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f16 (mxfp8 expert weights)" if mx else wl.dtype, "data": "synthetic",
-        "config": dict(config_of(wl), **({"shared_stream": True} if args.shared_stream else {}),
-                       **({"weights": "mxfp8 (E4M3 codes, E8M0 scale per 32 along K)"} if mx else {})),
-        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
-        "kernels_ms_per_step": {k: v[0] / args.steps for k, v in prof.items()},
-        "clocks": clocks,
+        "metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": head["dtype"], "data": "synthetic", "config": head["config"],
+        "roofline": head["roofline"], "cpu_baseline": head["cpu_baseline"], "e2e": head["e2e"],
+        "gpu_launches": head["gpu_launches"], "kernels_ms_per_step": head["kernels_ms_per_step"],
+        "clocks": head["clocks"],
     }
-    if rcheck is not None:
-        line["routing_check"] = rcheck
-    if two is not None:
-        line["two_dispatch"] = two
+    for k in ("routing_check", "two_dispatch"):
+        if k in head:
+            line[k] = head[k]
+    if subs:
+        line["workloads"] = subs
     print(json.dumps(line), flush=True)
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(W.WORKLOADS), default="decode")
+    ap.add_argument("--workload", choices=sorted(W.WORKLOADS), default=HEADLINE)
+    ap.add_argument("--no-sub", action="store_true",
+                    help="measure only --workload (no per-configuration records under 'workloads')")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--sub-cpu-seconds", type=float, default=4.0,
+                    help="CPU-oracle sample length of each record under 'workloads'")
     ap.add_argument("--weights", choices=["bf16", "mxfp8"], default="bf16",
                     help="routed expert weights: the layer dtype, or MXFP8 (moe_forward_mxfp8, T <= 16)")
     ap.add_argument("--shared-stream", action="store_true",
                     help="run the shared expert's GEMMs on a second stream (moe_set_shared_stream)")
-    ap.add_argument("--two-dispatch", action="store_true",
-                    help="also time the two-dispatch form of a multi-micro workload")
+    ap.add_argument("--no-two-dispatch", dest="two_dispatch", action="store_false",
+                    help="skip the two-dispatch comparison of the multi-micro workloads")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     wl = W.WORKLOADS[args.workload]

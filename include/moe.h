@@ -271,16 +271,31 @@ int64_t moe_launch_count(const moe_handle *h);
  *   or a null or misaligned pointer, returns MOE_ERR_INVALID_ARG.
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
- * capture. Every call shares the array and overwrites what the previous call
- * left there, so calls that overlap on the GPU race: order them (one stream).
- * Device-side check failures are recorded only in the array's error word and
- * are not reported by this entry point.
+ * capture. The cached address belongs to the device's primary context: a
+ * process that resets the device (cudaDeviceReset) must not call it again.
+ * Every call shares the array and overwrites what the previous call left
+ * there, so calls that overlap on the GPU race: order them (one stream).
+ * The call is asynchronous: a bounded device wait that ran out or a failed
+ * device-side check is recorded in the array's error word (cleared at the
+ * start of every call), which moe_route_noalloc_status reads back.
  */
 #define MOE_ROUTE_NOALLOC_MAX_TOKENS 16384
 moe_status moe_route_noalloc(const void *x, const void *router_w, const float *router_bias,
                              int32_t T, int32_t hidden, int32_t num_experts, int32_t top_k,
                              int32_t dtype, int32_t *topk_ids, float *topk_w, int32_t *perm,
                              int32_t *offsets, void *stream);
+
+/*
+ * Outcome of the last moe_route_noalloc call on the current device, for the
+ * same allocation-free callers (no counterpart on the pages either):
+ * synchronises `stream` (the stream that call used), copies the error word of
+ * the file-scope array to the host (no allocation) and returns MOE_OK,
+ * MOE_ERR_TIMEOUT (a bounded device wait ran out: the outputs are incomplete)
+ * or MOE_ERR_DEVICE_CHECK (a device-side consistency check failed: perm and
+ * offsets must not be used); MOE_ERR_CUDA if the stream or the copy failed.
+ * The word is not sticky: the next moe_route_noalloc call clears it.
+ */
+moe_status moe_route_noalloc_status(void *stream);
 
 /*
  * Self-test of the bounded device-side wait: launches one block whose thread

@@ -74,6 +74,7 @@ def load() -> ctypes.CDLL:
         "moe_profile_end": (st, [p, p, p]),
         "moe_launch_count": (ctypes.c_int64, [p]),
         "moe_route_noalloc": (st, [p, p, p, i32, i32, i32, i32, i32, p, p, p, p, p]),
+        "moe_route_noalloc_status": (st, [p]),
         "moe_set_accumulate": (st, [p, i32]),
         "moe_set_shared_stream": (st, [p, i32]),
     }

@@ -61,7 +61,10 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(FinalizeArgs a) {
     const int64_t R = (int64_t)a.T * a.k;
     if (threadIdx.x < a.k) {
         int64_t r = a.inv[(int64_t)t * a.k + threadIdx.x];
-        if (r < 0 || r >= R) r = 0;  // unreachable for a valid permutation
+        if (r < 0 || r >= R) {  // unreachable for a valid permutation: reported, never dereferenced
+            if (a.err != nullptr) atomicOr(a.err, kErrCheck);
+            r = 0;
+        }
         rows[threadIdx.x] = r;
         scale[threadIdx.x] = a.w[(int64_t)t * a.k + threadIdx.x];
     }

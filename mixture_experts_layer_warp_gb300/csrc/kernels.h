@@ -161,6 +161,7 @@ struct FinalizeArgs {
     void* y;                  // [T][H]
     bool accumulate;          // y += result instead of y = result
     int early;                // launch while the previous kernel in the stream finishes
+    int* err;                 // device error word: kErrCheck for an inverse entry outside [0, R), or null
 };
 cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t s);
 

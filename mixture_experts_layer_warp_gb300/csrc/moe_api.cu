@@ -430,7 +430,7 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
     if (!small_bf16) {  // small bf16 batches finalize inside the fused GEMM launch
         // launched early behind the last GEMM (not behind the join's event wait)
         FinalizeArgs fa{h->obuf, h->inv, h->topw, Is > 0 ? h->sbuf : nullptr, T, k, H, c.dtype == MOE_BF16, y,
-                        h->accumulate, fork ? 0 : 1};
+                        h->accumulate, fork ? 0 : 1, h->err};
         if ((e = timed(h, kSlotFinalize, s, [&] { return launch_finalize(fa, s); })) != cudaSuccess)
             return cuda_err(h, e, "finalize launch");
     }

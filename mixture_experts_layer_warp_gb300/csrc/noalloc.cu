@@ -41,6 +41,8 @@ constexpr size_t kScratchBytes = kSharedOff + 256;
 __device__ __align__(256) unsigned char g_route_scratch[kScratchBytes];
 
 // Device address of g_route_scratch per device, looked up once per device.
+// The address belongs to the device's primary context; the cache assumes that
+// context lives as long as the process (no cudaDeviceReset in between).
 std::mutex g_mu;
 constexpr int kMaxDevices = 64;
 void* g_addr[kMaxDevices] = {};
@@ -97,5 +99,17 @@ extern "C" moe_status moe_route_noalloc(const void* x, const void* router_w, con
                  nullptr, perm, inv, offsets, tiles_tc, tiles_simt, shared, hist, blk_base, err,
                  2000000000ull, nullptr, 0};
     if (enqueue_routing(j, s, nullptr) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+extern "C" moe_status moe_route_noalloc_status(void* stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int word = 0;
+    if (cudaMemcpyFromSymbolAsync(&word, g_route_scratch, sizeof word, kErrOff, cudaMemcpyDeviceToHost, s) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (word & kErrTimeout) return MOE_ERR_TIMEOUT;
+    if (word & kErrCheck) return MOE_ERR_DEVICE_CHECK;
     return MOE_OK;
 }

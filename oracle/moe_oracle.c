@@ -40,8 +40,8 @@
  * pages name no format, the reading taken is the OCP Microscaling (MX) MXFP8
  * format): codes are FP8 E4M3 (OCP E4M3FN: 4 exponent bits, bias 7, 3 mantissa
  * bits, no infinities, largest 448), one shared power-of-two scale (E8M0 code
- * S, value 2^(S-127)) per block of 32 consecutive elements along K; the
- * weights the layer computes with are the f16 roundings of code * scale.
+ * S, value 2^(S-127)) per block of 32 consecutive elements along K; the value
+ * of a weight is exactly code * scale (the MX definition), formed in fp64.
  */
 #include <math.h>
 #include <stdint.h>
@@ -490,29 +490,10 @@ int orc_mx_quantize(const void *w, int dtype, int64_t groups, int64_t rows, int6
 }
 
 /*
- * IEEE binary16 rounding of v (nearest, ties to even; subnormals down to 2^-24;
- * magnitudes from 65520 up round to infinity), returned as fp64.
- */
-static double round_f16(double v)
-{
-    double a = fabs(v);
-    if (a == 0.0 || a != a)
-        return v;
-    int ex;
-    frexp(a, &ex);
-    int e = ex - 1;  /* a in [2^e, 2^(e+1)) */
-    if (e < -14)
-        e = -14;     /* subnormal range: fixed step 2^-24 */
-    double q = ldexp(nearbyint(ldexp(a, 10 - e)), e - 10);
-    if (q >= 65520.0 || q > 65504.0)
-        q = INFINITY;
-    return v < 0 ? -q : q;
-}
-
-/*
- * The weights an MXFP8 layer computes with: f16 rounding of
- * e4m3_value(code) * 2^(S - 127), for codes [groups][rows][cols] and scales
- * [groups][cols/32][rows]; out [groups][rows][cols] fp64.
+ * The value of MXFP8 weights (OCP Microscaling: element value = the E4M3
+ * code's value times the block's E8M0 scale 2^(S - 127), exact in fp64 for
+ * every code and every finite scale), for codes [groups][rows][cols] and
+ * scales [groups][cols/32][rows]; out [groups][rows][cols] fp64.
  */
 int orc_mx_dequant(const uint8_t *codes, const uint8_t *scales, int64_t groups, int64_t rows,
                    int64_t cols, double *out)
@@ -525,7 +506,7 @@ int orc_mx_dequant(const uint8_t *codes, const uint8_t *scales, int64_t groups, 
         const int64_t g = gr / rows, r = gr % rows;
         for (int64_t c = 0; c < cols; ++c) {
             int S = scales[(g * nb + c / 32) * rows + r];
-            out[gr * cols + c] = round_f16(ldexp(e4m3_value(codes[gr * cols + c]), S - 127));
+            out[gr * cols + c] = ldexp(e4m3_value(codes[gr * cols + c]), S - 127);
         }
     }
     return 0;

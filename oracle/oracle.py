@@ -264,7 +264,7 @@ def mx_quantize(w: np.ndarray, lib=None):
 
 
 def mx_dequant(codes: np.ndarray, scales: np.ndarray, lib=None) -> np.ndarray:
-    """The fp64 weights an MXFP8 layer computes with (f16 of code * 2^(S-127))."""
+    """The fp64 value of MXFP8 weights: E4M3 code value times 2^(S-127), exactly."""
     two_d = codes.ndim == 2
     c3 = _c(codes[None] if two_d else codes, np.uint8)
     s3 = _c(scales[None] if two_d else scales, np.uint8)

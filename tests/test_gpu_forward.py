@@ -1,7 +1,8 @@
 """The whole layer (moe_forward) against the fp64 oracle.
 
 Small shapes are compared on every token; the five workloads at full size on a
-sample of tokens (the oracle evaluates the per-token definition for those).
+sample of tokens that puts a checked row into every 128-row block of every
+expert segment (the oracle evaluates the per-token definition for those).
 """
 import ctypes
 
@@ -30,12 +31,27 @@ def _forward(layer, dev):
     return y
 
 
-def _check(wl, inp, y, rows=None):
+def covering_tokens(orc: dict, T: int, k: int, stride: int = 128) -> np.ndarray:
+    """Tokens such that every `stride`-row block of every expert segment of the
+    sorted routes (and of the dense segment [0, T) of a shared expert) holds at
+    least one of their routes, plus each segment's last row: every tile of the
+    grouped GEMMs, whatever their row blocking at that granularity, then has a
+    row the oracle checks."""
+    off, perm = orc["offsets"], orc["perm"]
+    rows = [np.arange(off[e], off[e + 1], stride) for e in range(len(off) - 1)]
+    rows += [np.array([off[e + 1] - 1]) for e in range(len(off) - 1) if off[e + 1] > off[e]]
+    routed = perm[np.concatenate(rows)] // k
+    return np.unique(np.concatenate([routed, np.arange(0, T, stride), [T - 1]]))
+
+
+def _check(wl, inp, y, rows=None, cover: bool = False):
     host = parity.to_host_numpy(inp)
     orc = parity.oracle_routing(host, wl.k)
     set_ok, _ = parity.decided(orc["lf"], orc["ids"], TAU if wl.dtype == "bf16" else 0.0)
     T = host["x"].shape[0]
     rows = np.arange(T) if rows is None else np.asarray(rows)
+    if cover:
+        rows = np.union1d(rows, covering_tokens(orc, T, wl.k))
     rows = rows[set_ok[rows]]
     ref = oracle.forward_tokens(host["x"], orc["ids"], orc["w"], host["w13"], host["w2"], rows,
                                 host["shared_w13"], host["shared_w2"])
@@ -80,9 +96,10 @@ def test_workload_matches_oracle_on_sampled_tokens(name):
     y = _forward(layer, inp)
     rng = np.random.default_rng(0)
     rows = np.unique(np.concatenate([[0, wl.T - 1], rng.integers(0, wl.T, 30)]))
-    err = _check(wl, inp, y, rows)
-    print(f"{name}: rel err {err:.3e} on {rows.size} tokens")
     layer.close()
+    del layer
+    err = _check(wl, inp, y, rows, cover=True)
+    print(f"{name}: rel err {err:.3e}")
 
 
 def test_bitwise_deterministic_across_calls():
@@ -111,6 +128,27 @@ def test_two_dispatches_sum_to_the_multi_micro_call(T):
     l1.sync()
     err = (y.float() - both).abs().max().item() / both.abs().max().item()
     assert err < 1e-2
+    # and the two-dispatch output against the oracle's multi-micro layer
+    _check(wl, W.make_inputs(wl, seed=3), y)
+
+
+def test_two_dispatches_at_denoise_size_match_the_oracle():
+    """The pages' two-dispatch form ("HunyuanImage3 Hybrid Parallelism",
+    section 10.3) of the two-micro denoise workload at full size: one
+    single-micro layer call per micro-shard, the second accumulating into the
+    first's y, against the oracle's multi-micro layer on covering tokens."""
+    wl = W.WORKLOADS["denoise_multi_micro"]
+    inp = W.make_inputs(wl, seed=0, device="cuda")
+    one = W.Workload("m1", wl.T, wl.H, wl.E, wl.k, wl.I, 1, router_init=wl.router_init)
+    l0, l1 = _layer(one), _layer(one)
+    l1.set_accumulate(True)
+    y = l0.forward(inp["x"], inp["router_w"], None, inp["w13"][:1], inp["w2"][:1])
+    l1.forward(inp["x"], inp["router_w"], None, inp["w13"][1:], inp["w2"][1:], out=y)
+    l1.sync()
+    l0.close()
+    l1.close()
+    err = _check(wl, inp, y, [0], cover=True)
+    print(f"two dispatches, denoise: rel err {err:.3e}")
 
 
 @pytest.mark.parametrize("wl", [W.Workload("acc_small", 12, 512, 16, 4, 128, 2, shared_inter=128),

@@ -2,8 +2,11 @@
 
 The quantiser must reproduce the oracle's codes and scales bit for bit (an
 integer decision taken on the same bf16 inputs); the layer run on MXFP8
-weights must match the oracle evaluated on the dequantised weights
-(f16(code * 2^(S-127)), fp64 arithmetic) within the bf16 layer tolerance.
+weights must match the oracle evaluated on the exact value of those weights
+(code * 2^(S-127), the MX definition, in fp64) within the bf16 layer
+tolerance. The kernel converts codes to f16 (exact for scales in f16's range,
+an fp32 form outside it) and rounds the token rows and h to f16; that rounding
+is an implementation detail the tolerance covers.
 """
 import numpy as np
 import pytest
@@ -121,7 +124,8 @@ def test_mxfp8_rejects_batches_above_sixteen_tokens():
 
 def test_scales_outside_the_f16_range_take_the_exact_path():
     """w2 scaled by 2^-14: its blocks get scales near 2^-26 (not f16 numbers),
-    so the dequantiser's fp32 form runs; y (made by w2) must still match."""
+    so the dequantiser's fp32 form runs; y (made by w2) must still match the
+    exact MX weight values."""
     wl = W.Workload("mx_tiny_w2", 8, 512, 16, 4, 256, 1)
     inp = W.make_inputs(wl, seed=4)
     inp["w2"] = [(t.float() * 2.0 ** -14).to(torch.bfloat16) for t in inp["w2"]]

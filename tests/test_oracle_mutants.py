@@ -38,7 +38,10 @@ MUTANTS = [
     ("mx_ties_away_from_zero", "double q = nearbyint(scaled);", "double q = round(scaled);"),
     ("mx_scale_layout_row_major", "scales[(g * nb + b) * rows + r] = (uint8_t)(shared + 127);",
      "scales[(g * rows + r) * nb + b] = (uint8_t)(shared + 127);"),
-    ("f16_flush_subnormals", "    if (e < -14)\n        e = -14;", "    if (e < -14)\n        return 0.0;"),
+    ("mx_scale_bias_off_by_one", "ldexp(e4m3_value(codes[gr * cols + c]), S - 127);",
+     "ldexp(e4m3_value(codes[gr * cols + c]), S - 126);"),
+    ("mx_dequant_scale_of_wrong_block", "int S = scales[(g * nb + c / 32) * rows + r];",
+     "int S = scales[(g * nb + c / 64) * rows + r];"),
     ("fp64_weights_read_as_shared_dtype", "w_dtype, w[t * k + j], acc, a);", "dtype, w[t * k + j], acc, a);"),
 ]
 

@@ -4,8 +4,9 @@ take cudaMalloc's implicit synchronisation). It keeps its intermediate data in
 a file-scope device array of the library instead of a handle's workspace.
 
 Checked through the C ABI against moe_route on two calls in a row with
-different inputs (the shared array keeps the first call's contents when the
-second one starts), and against its size limit. This file is collected last.
+different inputs and routing paths (the shared array keeps the first call's
+contents when the second one starts), through its status query, and against its
+size limit. This file is collected last.
 """
 import ctypes
 
@@ -31,22 +32,40 @@ def _noalloc(lib, x, wr, bias, k, dtype_code):
     return rc, out
 
 
-def test_noalloc_routing_matches_moe_route_on_two_calls_in_a_row():
+# every routing path the entry point can take: the multi-CTA tensor-core router
+# with scan and placement (T > 128), the single-CTA router with fused scan and
+# placement (16 < T <= 128), the 8-CTA cluster router (T <= 16), and the fp32
+# SIMT router whose histogram uses every row of the array (T at the limit)
+CASES = [
+    (W.Workload("a", 3000, 4096, 64, 8, 768, 1, router_bias="log_zipf"), torch.bfloat16, 1),
+    (W.Workload("b", 777, 512, 16, 4, 128, 1), torch.bfloat16, 1),
+    (W.Workload("c", 8, 4096, 64, 8, 768, 1), torch.bfloat16, 1),
+    (W.Workload("d", 100, 512, 64, 8, 128, 1), torch.bfloat16, 1),
+    (W.Workload("e", 16384, 256, 8, 2, 64, 1, dtype="f32"), torch.float32, 0),
+]
+
+
+@pytest.mark.parametrize("first,second", [(0, 1), (2, 3), (4, 2), (3, 4)])
+def test_noalloc_routing_matches_moe_route_on_two_calls_in_a_row(first, second):
+    """Two different calls back to back (the second starts with the first one's
+    data left in the shared array), each equal to moe_route bit for bit, and
+    the status query reports a clean run after each."""
     lib = binding.load()
-    cases = [(W.Workload("a", 3000, 4096, 64, 8, 768, 1, router_bias="log_zipf"), torch.bfloat16, 1),
-             (W.Workload("b", 777, 512, 16, 4, 128, 1), torch.bfloat16, 1)]
-    for call, (wl, dt, code) in enumerate(cases):
-        inp = W.make_inputs(wl, seed=10 + call, device="cuda", experts=False)
-        layer = binding.MoELayer(wl.H, wl.E, wl.k, 128, 1, max_tokens=wl.T, dtype=dt)
+    stream = torch.cuda.current_stream().cuda_stream
+    for call, idx in enumerate((first, second)):
+        wl, dt, code = CASES[idx]
+        inp = W.make_inputs(wl, seed=10 + 7 * idx + call, device="cuda", experts=False)
+        layer = binding.MoELayer(wl.H, wl.E, wl.k, 128 if dt == torch.bfloat16 else 64, 1, max_tokens=wl.T,
+                                 dtype=dt)
         ref = layer.route(inp["x"], inp["router_w"], inp["router_bias"])
         layer.sync()
         rc, got = _noalloc(lib, inp["x"], inp["router_w"], inp["router_bias"], wl.k, code)
         assert binding.STATUS[rc] == "MOE_OK"
-        torch.cuda.synchronize()
-        assert torch.equal(got["ids"], ref["ids"]), call
-        assert torch.equal(got["perm"], ref["perm"]), call
-        assert torch.equal(got["offsets"], ref["offsets"]), call
-        assert (got["w"] - ref["w"]).abs().max().item() <= 1e-5, call
+        assert binding.STATUS[lib.moe_route_noalloc_status(stream)] == "MOE_OK"
+        assert torch.equal(got["ids"], ref["ids"]), (wl.name, call)
+        assert torch.equal(got["perm"], ref["perm"]), (wl.name, call)
+        assert torch.equal(got["offsets"], ref["offsets"]), (wl.name, call)
+        assert (got["w"] - ref["w"]).abs().max().item() <= 1e-5, (wl.name, call)
         layer.close()
 
 
@@ -57,6 +76,9 @@ def test_noalloc_rejects_sizes_beyond_its_limit():
     wr = torch.zeros((8, 256), dtype=torch.bfloat16, device="cuda")
     rc, _ = _noalloc(lib, x, wr, None, 2, 1)
     assert binding.STATUS[rc] == "MOE_ERR_INVALID_ARG"
-    rc, _ = _noalloc(lib, x[:limit], wr, None, 2, 1)
+    rc, got = _noalloc(lib, x[:limit], wr, None, 2, 1)
     assert binding.STATUS[rc] == "MOE_OK"
-    torch.cuda.synchronize()
+    assert binding.STATUS[lib.moe_route_noalloc_status(torch.cuda.current_stream().cuda_stream)] == "MOE_OK"
+    # all logits tie (zero inputs): every token takes experts 0 and 1, in order
+    assert got["offsets"].tolist() == [0, limit, 2 * limit] + [2 * limit] * 6
+    assert torch.equal(got["ids"].cpu(), torch.tensor([[0, 1]], dtype=torch.int32).expand(limit, 2))
