@@ -172,7 +172,7 @@ def job_throughput(world: int, tokens_per_step: int, steps: int, ms_local: float
 # headers it includes): the small-batch fused kernel, the large-batch tcgen05 GEMM.
 KERNEL_SOURCES = {
     "small": ("gemm_small.cu", "gemm_common.cuh", "kernels.h", "ptx.cuh"),
-    "large": ("gemm_tc.cu", "gemm_common.cuh", "kernels.h", "ptx.cuh"),
+    "large": ("gemm_pair.cu", "gemm_common.cuh", "kernels.h", "ptx.cuh"),
 }
 
 

@@ -1,0 +1,448 @@
+// gemm_pair.cu - grouped GEMMs of the routed experts on CTA pairs (sm_103a).
+//
+// "HunyuanImage3 Hybrid Parallelism", section 6.1/6.2: every micro-shard runs
+// grouped GEMM1 -> split gate/up -> SwiGLU -> grouped GEMM2 over the
+// expert-sorted routes; the micro partials are added in fp32 and the finalize
+// runs once. Ascend Hunyuan Image 3.0 guide, section 2.2: the expert is
+// down(SiLU(gate(x)) * up(x)) with w13 = [gate; up].
+//
+// Operand roles. The two CTAs of a cluster issue one tcgen05.mma.cta_group::2
+// of M = 256 weight rows (128 held by each CTA) by N tokens (N/2 token rows
+// held by each CTA), so each CTA stages 16 KB of weights and at most 16 KB of
+// token rows per 64-deep K stage: half the operand bytes per SM of a one-SM
+// 128 x 256 tile for the same tensor-core work. Tokens on N let a group's
+// rows be cut into chunks of at most 256 padded to a multiple of 32 (a group
+// of c routes costs ceil(c / 32) * 32 columns, not ceil(c / 128) * 128 rows).
+//
+//   SwiGLU (GEMM1): a tile is (micro m, expert e, 128 features f*128.., one
+//       chunk of e's routes). CTA r holds features f*128 + r*64 + [0, 64) as
+//       four groups of 16 gate rows followed by the 16 matching up rows (one
+//       box of a 5D map over w13), so TMEM lanes 32j..32j+15 of each CTA hold
+//       gate and lanes 32j+16..32j+31 the up values of the same 16 features:
+//       an epilogue warp pairs them with one shuffle per two tokens and writes
+//       silu(gate) * up as bf16 into h[route][m*I + feature].
+//   down (GEMM2): a tile is (expert e, 256 output columns f*256.., one chunk).
+//       CTA r holds w2 rows f*256 + r*128 + [0, 128). The K loop runs over
+//       micro 0's I columns of h against w2[0][e], then micro 1's against
+//       w2[1][e], ... into ONE fp32 TMEM accumulator: the per-micro partial
+//       outputs of the pages never exist.
+//
+// Structure: persistent pairs, static round-robin over tiles in the order
+// expert -> micro -> feature tile -> chunk, so the pairs working at the same
+// time share one expert's token rows and weight tiles through L2. 8 warps per
+// CTA: warp 0 issues TMA loads into a 6-stage ring (both CTAs; completion
+// counted on the leader's barrier), warp 1 of the leader issues the MMAs into
+// one of two TMEM accumulators (2 x 256 fp32 columns), warp 2 owns the TMEM
+// allocation, warps 4-7 drain an accumulator (one TMEM lane quarter each)
+// while the next tile accumulates into the other. All waits are bounded.
+#include <cuda_bf16.h>
+
+#include "gemm_common.cuh"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kStages = 6;
+constexpr int kChunk = 256;                          // tokens per tile at most (MMA N)
+constexpr int kWRows = 128;                          // weight rows per CTA (MMA M = 256 per pair)
+constexpr int kABytes = kWRows * kTcBK * 2;          // 16 KB
+constexpr int kBBytes = (kChunk / 2) * kTcBK * 2;    // 16 KB: up to 128 token rows per CTA
+constexpr int kStageBytes = kABytes + kBBytes;       // 32 KB
+constexpr int kTmemCols = 2 * kChunk;                // two accumulators
+constexpr int kThreads = 256;
+constexpr int kEpiArrivals = 8;                      // 4 epilogue warps in each CTA of the pair
+
+struct Ctl {
+    uint64_t full[kStages];   // leader: both CTAs' loads of a stage have landed
+    uint64_t empty[kStages];  // both CTAs: the MMAs reading a stage are done
+    uint64_t tfull[2];        // both CTAs: an accumulator is complete
+    uint64_t tempty[2];       // leader: both CTAs' epilogues drained an accumulator
+    uint64_t drain;           // leader: every MMA issued has completed
+    uint32_t tmem_base;
+    int abort;
+    int seg[kMaxExperts + 1];
+    int chunks[kMaxExperts + 1];  // prefix over groups of ceil(rows / kChunk)
+};
+
+constexpr int kSmemBytes = kStages * kStageBytes + (int)sizeof(Ctl) + 1024;
+
+struct PairTile {
+    int m, g, f;
+    int start;  // first route row of the chunk
+    int len;    // routes in the chunk (<= kChunk)
+    int n;      // MMA N: len rounded up to a multiple of 32
+};
+
+// Chunks of one group: ceil(rows / kChunk) of near-equal length, so no chunk
+// is a nearly empty remainder (the weight bytes of a tile do not shrink with N).
+template <bool SWIGLU>
+__device__ __forceinline__ PairTile decode_pair_tile(int tile, const Ctl& c, const PairGemmArgs& a) {
+    PairTile t;
+    const int per = (SWIGLU ? a.n_micro : 1) * a.n_ftiles;  // tiles per chunk
+    int lo = 0, hi = a.G - 1;  // largest g with chunks[g] * per <= tile
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (c.chunks[mid] * per <= tile)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    t.g = lo;
+    const int C = c.chunks[lo + 1] - c.chunks[lo];
+    int local = tile - c.chunks[lo] * per;
+    t.m = 0;
+    if (SWIGLU) {
+        t.m = local / (a.n_ftiles * C);
+        local -= t.m * a.n_ftiles * C;
+    }
+    t.f = local / C;
+    const int ch = local - t.f * C;
+    const int rows = c.seg[lo + 1] - c.seg[lo];
+    const int base = rows / C, rem = rows % C;
+    t.start = c.seg[lo] + ch * base + min(ch, rem);
+    t.len = base + (ch < rem ? 1 : 0);
+    t.n = (t.len + 31) & ~31;
+    return t;
+}
+
+__device__ __forceinline__ void fail(Ctl& c, int* err) {
+    c.abort = 1;
+    atomicOr(err, kErrTimeout);
+}
+
+// Failure path of a CTA whose loads complete on the other CTA's barrier: it
+// cannot wait for them itself, so it gives any copy still in flight 1 ms to
+// land before the CTA can leave (copies take microseconds).
+__device__ __forceinline__ void settle_inflight_copies() {
+    const uint64_t t0 = ptx::globaltimer();
+    while (ptx::globaltimer() - t0 < 1000000ull) {
+    }
+}
+
+template <bool SWIGLU>
+__global__ void __launch_bounds__(kThreads, 1)
+    pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant__ CUtensorMap tmW1,
+                     const __grid_constant__ CUtensorMap tmW2, const __grid_constant__ CUtensorMap tmW3,
+                     const __grid_constant__ CUtensorMap tmX0, const __grid_constant__ CUtensorMap tmX1,
+                     const __grid_constant__ CUtensorMap tmX2, const __grid_constant__ CUtensorMap tmX3,
+                     const PairGemmArgs a) {
+    extern __shared__ unsigned char smem_raw[];
+    // the same offset in both CTAs: the leader's MMA addresses the peer's
+    // operands through its own shared-memory descriptors
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Ctl& c = *reinterpret_cast<Ctl*>(smem + kStages * kStageBytes);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t rank = ptx::cluster_ctarank();
+    const bool leader = rank == 0;
+    const int pair = blockIdx.x / 2, npairs = gridDim.x / 2;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            ptx::mbar_init(ptx::smem_u32(&c.full[s]), 1);
+            ptx::mbar_init(ptx::smem_u32(&c.empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(ptx::smem_u32(&c.tfull[b]), 1);
+            ptx::mbar_init(ptx::smem_u32(&c.tempty[b]), kEpiArrivals);
+        }
+        ptx::mbar_init(ptx::smem_u32(&c.drain), 1);
+        c.abort = 0;
+        ptx::fence_mbar_init();
+    }
+    // launched early (a.early): the segments and token rows are complete past here
+    ptx::griddep_wait();
+    if (a.seg != nullptr) {
+        for (int i = threadIdx.x; i <= a.G; i += kThreads) c.seg[i] = a.seg[i];
+    } else if (threadIdx.x == 0) {  // one dense segment (the shared expert over all T rows)
+        c.seg[0] = 0;
+        c.seg[1] = a.dense_rows;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        c.chunks[0] = 0;
+        for (int g = 0; g < a.G; ++g) c.chunks[g + 1] = c.chunks[g] + (c.seg[g + 1] - c.seg[g] + kChunk - 1) / kChunk;
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tmap(&tmW0);
+        ptx::prefetch_tmap(&tmX0);
+    }
+    if (warp == 2) {
+        ptx::tmem_alloc_pair(ptx::smem_u32(&c.tmem_base), kTmemCols);
+        ptx::tmem_relinquish_pair();
+    }
+    // the barriers of both CTAs are initialised and the TMEM columns allocated
+    // before either CTA signals the other
+    __syncwarp();
+    ptx::tc_fence_before();
+    ptx::cluster_sync();
+    ptx::tc_fence_after();
+
+    const uint32_t tmem = c.tmem_base;
+    const int total = (SWIGLU ? a.n_micro : 1) * c.chunks[a.G] * a.n_ftiles;
+    const int n_micro_k = SWIGLU ? 1 : a.n_micro;
+
+    // The producer and MMA roles run as whole warps: every lane takes part in
+    // the waits and the bookkeeping (so the descriptors and coordinates are
+    // warp-uniform values), and one elected lane issues the TMA and tcgen05
+    // instructions. A single-lane loop issued each tcgen05.mma about 85 cycles
+    // apart, close to the 128 tensor-core cycles of one M256 x N256 x K16 MMA.
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer (both CTAs)
+        const bool issuer = ptx::elect_one();
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t last_par[kStages];
+        int issued = 0;
+        bool ok = true;
+        for (int tile = pair; ok && tile < total; tile += npairs) {
+            const PairTile t = decode_pair_tile<SWIGLU>(tile, c, a);
+            const int half = t.n / 2;               // token rows held by each CTA
+            const int box = (half + 31) / 32 - 1;   // token-row box of 32, 64, 96 or 128 rows
+            const CUtensorMap* tx = box == 0 ? &tmX0 : box == 1 ? &tmX1 : box == 2 ? &tmX2 : &tmX3;
+            const uint32_t bytes = 2u * (uint32_t)(kABytes + (box + 1) * 32 * kTcBK * 2);
+            const int xrow = t.start + (int)rank * half;
+            for (int mi = 0; ok && mi < n_micro_k; ++mi) {
+                const int m = SWIGLU ? t.m : mi;
+                const CUtensorMap* tw = pick_map(m, tmW0, tmW1, tmW2, tmW3);
+                for (int kb = 0; kb < a.k_blocks; ++kb) {
+                    const bool got = ptx::mbar_wait(ptx::smem_u32(&c.empty[stage]), phase ^ 1u, a.limit_ns, &c.abort);
+                    if (!__all_sync(0xffffffffu, got)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = ptx::smem_u32(smem + stage * kStageBytes);
+                    const uint32_t sb = sa + kABytes;
+                    const uint32_t fb = ptx::smem_u32(&c.full[stage]);
+                    const uint32_t fb_leader = ptx::map_to_rank(fb, 0);
+                    if (issuer) {
+                        if (leader) ptx::mbar_arrive_expect_tx(fb, bytes);
+                        if (SWIGLU) {
+                            // 4 groups of (16 gate rows, 16 up rows) of features f*128 + r*64 ..
+                            ptx::tma_load_5d_pair(sa, tw, kb * kTcBK, 0, 0, (t.f * 128 + (int)rank * 64) / 16, t.g,
+                                                  fb_leader);
+                            ptx::tma_load_2d_pair(sb, tx, kb * kTcBK, xrow, fb_leader);
+                        } else {
+                            ptx::tma_load_2d_pair(sa, tw, kb * kTcBK,
+                                                  t.g * a.w_rows_per_group + t.f * 256 + (int)rank * 128, fb_leader);
+                            ptx::tma_load_2d_pair(sb, tx, m * a.x_micro_cols + kb * kTcBK, xrow, fb_leader);
+                        }
+                    }
+                    __syncwarp();
+                    last_par[stage] = phase;
+                    ++issued;
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+        if (!ok && issuer) {
+            fail(c, a.err);
+            if (leader) {
+                // let every load still in flight (either CTA's) land before the pair can exit
+                const int n = issued < kStages ? issued : kStages;
+                for (int s = 0; s < n; ++s)
+                    ptx::mbar_wait(ptx::smem_u32(&c.full[s]), last_par[s], a.limit_ns, nullptr);
+            } else {
+                settle_inflight_copies();
+            }
+        }
+    } else if (warp == 1 && leader) {
+        // ------------------------------------------------ MMA issuer (leader)
+        const bool issuer = ptx::elect_one();
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        int local = 0;
+        for (int tile = pair; ok && tile < total; tile += npairs, ++local) {
+            const PairTile t = decode_pair_tile<SWIGLU>(tile, c, a);
+            const uint32_t idesc = ptx::idesc_bf16_f32(2 * kWRows, t.n);
+            const int acc = local & 1;
+            const uint32_t acc_par = (uint32_t)(local >> 1) & 1u;
+            const bool drained = ptx::mbar_wait(ptx::smem_u32(&c.tempty[acc]), acc_par ^ 1u, a.limit_ns, &c.abort);
+            if (!__all_sync(0xffffffffu, drained)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t d = tmem + (uint32_t)(acc * kChunk);
+            uint32_t accumulate = 0;
+            for (int mi = 0; ok && mi < n_micro_k; ++mi) {
+                for (int kb = 0; kb < a.k_blocks; ++kb) {
+                    const bool got = ptx::mbar_wait(ptx::smem_u32(&c.full[stage]), phase, a.limit_ns, &c.abort);
+                    if (!__all_sync(0xffffffffu, got)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t sa = ptx::smem_u32(smem + stage * kStageBytes);
+                    const uint64_t adesc = ptx::sw128_desc(sa);
+                    const uint64_t bdesc = ptx::sw128_desc(sa + kABytes);
+                    if (issuer) {
+#pragma unroll
+                        for (int k = 0; k < kTcBK / 16; ++k)
+                            ptx::mma_bf16_pair(d, adesc + 2u * k, bdesc + 2u * k, idesc, accumulate | (uint32_t)k);
+                        ptx::mma_commit_pair_both(ptx::smem_u32(&c.empty[stage]));
+                    }
+                    __syncwarp();
+                    accumulate = 1;
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (ok && issuer) ptx::mma_commit_pair_both(ptx::smem_u32(&c.tfull[acc]));
+            __syncwarp();
+        }
+        if (issuer) {
+            if (!ok) fail(c, a.err);
+            // every MMA issued so far completes before either CTA's TMEM is released
+            ptx::mma_commit_pair_local(ptx::smem_u32(&c.drain));
+            ptx::mbar_wait(ptx::smem_u32(&c.drain), 0, a.limit_ns, nullptr);
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ------------------------------------------------ epilogue (both CTAs)
+        const int q = warp - 4;  // TMEM lanes 32q .. 32q+31
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+        const uint32_t tempty_leader0 = ptx::map_to_rank(ptx::smem_u32(&c.tempty[0]), 0);
+        int local = 0;
+        for (int tile = pair; tile < total; tile += npairs, ++local) {
+            const int acc = local & 1;
+            const uint32_t acc_par = (uint32_t)(local >> 1) & 1u;
+            const PairTile t = decode_pair_tile<SWIGLU>(tile, c, a);
+            bool ready = false;
+            if (lane == 0)
+                ready = ptx::mbar_wait(ptx::smem_u32(&c.tfull[acc]), acc_par, a.limit_ns, &c.abort);
+            ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
+            if (!ready) {
+                if (lane == 0) fail(c, a.err);
+                break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kChunk);
+            if (SWIGLU) {
+                // lanes 0-15: gate of features feat0 + lane; lanes 16-31: up of the same
+                const int feat = t.m * a.out_micro_cols + t.f * 128 + (int)rank * 64 + q * 16 + (lane & 15);
+                const bool is_gate = lane < 16;
+                __nv_bfloat16* dst = out + (int64_t)t.start * a.out_ld + feat;
+#pragma unroll 1
+                for (int c0 = 0; c0 < t.n; c0 += 32) {
+                    uint32_t v[32];
+                    ptx::tmem_ld32(tbase + c0, v);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        // token c0+2i goes to the gate lane, c0+2i+1 to the up lane
+                        const float v0 = __uint_as_float(v[2 * i]), v1 = __uint_as_float(v[2 * i + 1]);
+                        const float other = __shfl_xor_sync(0xffffffffu, is_gate ? v1 : v0, 16);
+                        const float h = is_gate ? silu(v0) * other : silu(other) * v1;
+                        const int tok = c0 + 2 * i + (is_gate ? 0 : 1);
+                        if (tok < t.len) dst[(int64_t)tok * a.out_ld] = __float2bfloat16_rn(h);
+                    }
+                }
+            } else {
+                const int feat = t.f * 256 + (int)rank * 128 + q * 32 + lane;
+                __nv_bfloat16* dst = out + (int64_t)t.start * a.out_ld + feat;
+#pragma unroll 1
+                for (int c0 = 0; c0 < t.n; c0 += 32) {
+                    uint32_t v[32];
+                    ptx::tmem_ld32(tbase + c0, v);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (c0 + i < t.len) dst[(int64_t)(c0 + i) * a.out_ld] = __float2bfloat16_rn(__uint_as_float(v[i]));
+                }
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (leader)
+                    ptx::mbar_arrive(ptx::smem_u32(&c.tempty[acc]));
+                else
+                    ptx::mbar_arrive_cluster(tempty_leader0 + (uint32_t)(acc * sizeof(uint64_t)));
+            }
+        }
+    }
+
+    // neither CTA leaves (or frees TMEM) while the other may still signal it
+    __syncwarp();
+    ptx::tc_fence_before();
+    ptx::cluster_sync();
+    if (warp == 2) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc_pair(tmem, kTmemCols);
+    }
+}
+
+// Pairs resident at once (one per TPC at most), looked up once per device.
+template <bool SWIGLU>
+int max_pairs() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cached[dev] > 0) return cached[dev];
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, pair_gemm_kernel<SWIGLU>, &cfg) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        return 0;
+    }
+    cached[dev] = n;
+    return n;
+}
+
+template <bool SWIGLU>
+cudaError_t launch_pair(const PairGemmArgs& a, const CUtensorMap* tmW, const CUtensorMap* tmX, cudaStream_t s) {
+    if (a.max_tiles <= 0) return cudaSuccess;
+    if (cudaError_t e = ensure_smem_limit<pair_gemm_kernel<SWIGLU>>(kSmemBytes); e != cudaSuccess) return e;
+    const int pairs_max = max_pairs<SWIGLU>();
+    if (pairs_max <= 0) return cudaErrorLaunchOutOfResources;
+    const int pairs = a.max_tiles < pairs_max ? a.max_tiles : pairs_max;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(2 * pairs);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = a.early ? 2 : 1;
+    const CUtensorMap& w1 = a.n_micro > 1 ? tmW[1] : tmW[0];
+    const CUtensorMap& w2 = a.n_micro > 2 ? tmW[2] : tmW[0];
+    const CUtensorMap& w3 = a.n_micro > 3 ? tmW[3] : tmW[0];
+    return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<SWIGLU>, tmW[0], w1, w2, w3, tmX[0], tmX[1], tmX[2], tmX[3],
+                              a);
+}
+
+}  // namespace
+
+cudaError_t launch_pair_gemm_swiglu(const PairGemmArgs& a, const CUtensorMap* tmW, const CUtensorMap* tmX,
+                                    cudaStream_t s) {
+    return launch_pair<true>(a, tmW, tmX, s);
+}
+
+cudaError_t launch_pair_gemm_down(const PairGemmArgs& a, const CUtensorMap* tmW, const CUtensorMap* tmX,
+                                  cudaStream_t s) {
+    return launch_pair<false>(a, tmW, tmX, s);
+}
+
+}  // namespace moe

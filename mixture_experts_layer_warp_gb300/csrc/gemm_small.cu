@@ -1,7 +1,7 @@
 // gemm_small.cu - the grouped GEMMs for batches of at most 16 tokens
 // (AR-decode-sized calls), with the operands swapped.
 //
-// Same computation as gemm_tc.cu ("HunyuanImage3 Hybrid Parallelism",
+// Same computation as gemm_pair.cu ("HunyuanImage3 Hybrid Parallelism",
 // section 6.1: per micro grouped GEMM1 -> SwiGLU -> grouped GEMM2, micros
 // summed in fp32), but with T <= 16 every expert owns at most 16 routes, so
 // the expert WEIGHTS take the MMA's M side (128 rows) and the expert's token

@@ -191,13 +191,36 @@ struct TcGemmArgs {
     int dense_rows;           // rows of the dense segment when seg is null
     int early;                // launch while the previous kernel in the stream finishes
 };
-// tmA: A [rows][K] bf16, box {64, 128}. tmB[m]: SwiGLU: w13_m [G][2I][K] bf16 as a
-// 3D map {K, I, 2G} with box {64, 128, 2} (128 gate rows and the matching up rows);
-// down: B_m [G*b_rows][K] bf16, box {64, 256}.
-cudaError_t launch_tc_gemm_swiglu(const TcGemmArgs& a, const CUtensorMap& tmA, const CUtensorMap* tmB,
-                                  int num_sms, cudaStream_t s);
-cudaError_t launch_tc_gemm_down(const TcGemmArgs& a, const CUtensorMap& tmA, const CUtensorMap* tmB,
-                                int num_sms, cudaStream_t s);
+// Grouped GEMMs on CTA pairs (gemm_pair.cu): weights on the MMA's M side (256
+// rows over the pair), the routes of a group on N in chunks of at most 256,
+// padded to a multiple of 32.
+//   SwiGLU form (GEMM1): out[r][m*I + n] = silu(x_r . W_m[g][n]) * (x_r . W_m[g][I + n])
+//   Plain form (GEMM2):  out[r][n] = sum_m x_r[m*I:(m+1)*I] . W_m[g][n]
+struct PairGemmArgs {
+    const int32_t* seg;       // [G+1] route-row offsets of the groups, or null: one dense segment [0, dense_rows)
+    int G;
+    int n_micro;
+    int k_blocks;             // kTcBK-blocks of K per micro
+    int n_ftiles;             // feature tiles per (group, micro): I/128 (SwiGLU) or H/256 (plain)
+    int w_rows_per_group;     // plain form: rows of W per group (H)
+    int x_micro_cols;         // plain form: columns of the token rows per micro (I)
+    void* out;                // bf16
+    int64_t out_ld;           // elements per output row
+    int out_micro_cols;       // SwiGLU form: I (column offset of micro m in out)
+    int max_tiles;            // upper bound on the tiles (sizes the grid)
+    int* err;
+    uint64_t limit_ns;
+    int dense_rows;           // rows of the dense segment when seg is null
+    int early;                // launch while the previous kernel in the stream finishes
+};
+// tmW[m]: SwiGLU form: w13_m [G][2I][K] as a 5D map {K, 16, 2, I/16, G} (strides
+// of a row, of the up half, of 16 rows, of a group) with box {64, 16, 2, 4, 1};
+// plain form: W_m [G*H][I] with box {64, 128}. tmX[0..3]: the token rows
+// [rows][K] with boxes {64, 32}, {64, 64}, {64, 96}, {64, 128}. All 128B-swizzled.
+cudaError_t launch_pair_gemm_swiglu(const PairGemmArgs& a, const CUtensorMap* tmW, const CUtensorMap* tmX,
+                                    cudaStream_t s);
+cudaError_t launch_pair_gemm_down(const PairGemmArgs& a, const CUtensorMap* tmW, const CUtensorMap* tmX,
+                                  cudaStream_t s);
 
 // Swapped-operand variants for batches of at most kSmallTokens tokens (every
 // expert then owns at most kSmallTokens routes): weights on the MMA M side,

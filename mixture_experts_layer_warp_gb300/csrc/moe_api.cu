@@ -116,25 +116,39 @@ moe_status check_cfg(const moe_config* c, char* msg, size_t n) {
     return MOE_OK;
 }
 
-bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t row_bytes) {
-    return encode_bf16_2d(m, base, inner, rows, row_bytes, kTcBM);
-}
-
-// The GEMMs' weight operands, one box per K stage: w13 [G][2I][H] as a 3D map
-// {H, I, 2G} whose box {64, rows, 2} is `rows` gate rows and the matching up
-// rows (128 for the large GEMM, 64 for the small-batch one); w2 [rows][K] with
-// 256-row boxes for the large GEMM.
+// The small-batch GEMMs' w13 operand, one box per K stage: w13 [G][2I][H] as a
+// 3D map {H, I, 2G} whose box {64, rows, 2} is `rows` gate rows and the
+// matching up rows.
 bool encode_w13(CUtensorMap* m, const void* w13, uint64_t H, uint64_t I, uint64_t G, uint32_t rows) {
     const uint64_t dims[3] = {H, I, 2 * G}, strides[2] = {H * 2, I * H * 2};
     const uint32_t box[3] = {(uint32_t)kTcBK, rows, 2};
     return encode_3d(m, true, w13, dims, strides, box, true);
 }
-bool encode_w13_tc(CUtensorMap* m, const void* w13, uint64_t H, uint64_t I, uint64_t G) {
-    return encode_w13(m, w13, H, I, G, 128);
+
+// Operands of the pair GEMMs (gemm_pair.cu). Token rows [rows][K]: four maps
+// with boxes of 32, 64, 96 and 128 rows (a CTA loads the smallest one that
+// covers its half of a chunk). w13 [G][2I][H] as a 5D map {H, 16, 2, I/16, G}
+// whose box {64, 16, 2, 4, 1} is four groups of 16 gate rows followed by the
+// matching 16 up rows; w2 [G*H][I] with 128-row boxes.
+bool encode_rows_pair(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows) {
+    for (uint32_t b = 0; b < 4; ++b)
+        if (!encode_bf16_2d(&m[b], base, K, rows, K * 2, 32 * (b + 1))) return false;
+    return true;
 }
-bool encode_w2_tc(CUtensorMap* m, const void* w2, uint64_t K, uint64_t rows) {
-    return encode_bf16_2d(m, w2, K, rows, K * 2, 256);
+bool encode_w13_pair(CUtensorMap* m, const void* w13, uint64_t H, uint64_t I, uint64_t G) {
+    const uint64_t dims[5] = {H, 16, 2, I / 16, G};
+    const uint64_t strides[4] = {H * 2, I * H * 2, 16 * H * 2, 2 * I * H * 2};
+    const uint32_t box[5] = {(uint32_t)kTcBK, 16, 2, 4, 1};
+    return encode_nd(m, true, w13, 5, dims, strides, box, true);
 }
+bool encode_w2_pair(CUtensorMap* m, const void* w2, uint64_t K, uint64_t rows) {
+    return encode_bf16_2d(m, w2, K, rows, K * 2, 128);
+}
+
+// The shared expert's two GEMMs over the dense segment [0, T) on stream `ss`
+// (`early`: launched behind the preceding kernel in that stream).
+moe_status run_shared_pair(moe_handle* h, const void* x, const void* sw13, const void* sw2, int32_t T,
+                           cudaStream_t ss, int early);
 
 void hook_before(void* ctx, int slot, cudaStream_t s) {
     moe_handle* h = static_cast<moe_handle*>(ctx);
@@ -217,22 +231,7 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
         return cuda_err(h, e, "shared-expert fork");
     if (fork) {
         const cudaStream_t ss = h->side;
-        CUtensorMap sA, sB[kMaxMicro];
-        const int stiles = (T + kTcBM - 1) / kTcBM;
-        if (!encode_2d(&sA, x, H, T, (uint64_t)H * 2) || !encode_w13_tc(&sB[0], sw13, H, Is, 1))
-            return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (shared GEMM1)");
-        TcGemmArgs s1{nullptr, nullptr, 1, 1, H / kTcBK, Is / 128, 2 * Is, Is, 0,
-                      h->hs, (int64_t)Is, 0, stiles * (Is / 128), h->err, h->limit_ns, T};
-        if ((e = timed(h, kSlotSharedGemm1, ss, [&] { return launch_tc_gemm_swiglu(s1, sA, sB, h->num_sms, ss); })) !=
-            cudaSuccess)
-            return cuda_err(h, e, "shared GEMM1 launch");
-        if (!encode_2d(&sA, h->hs, Is, T, (uint64_t)Is * 2) || !encode_w2_tc(&sB[0], sw2, Is, H))
-            return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (shared GEMM2)");
-        TcGemmArgs s2{nullptr, nullptr, 1, 1, Is / kTcBK, H / 256, H, 0, Is,
-                      h->sbuf, (int64_t)H, 0, stiles * (H / 256), h->err, h->limit_ns, T};
-        if ((e = timed(h, kSlotSharedGemm2, ss, [&] { return launch_tc_gemm_down(s2, sA, sB, h->num_sms, ss); })) !=
-            cudaSuccess)
-            return cuda_err(h, e, "shared GEMM2 launch");
+        if ((st = run_shared_pair(h, x, sw13, sw2, T, ss, 0)) != MOE_OK) return st;
         if ((e = cudaEventRecord(h->ev_join, ss)) != cudaSuccess) return cuda_err(h, e, "shared-expert join");
     }
 
@@ -244,7 +243,6 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
             return cuda_err(h, e, "gather launch");
     }
 
-    const int routed_tiles_tc = (int)(R / kTcBM) + E;  // bound on sum of ceil(count/128)
     if (c.dtype == MOE_BF16 && T <= kSmallTokens) {
         // swapped operands: weights on the MMA M side, the <= 16 tokens on N
         CUtensorMap tmX, tmW[kMaxMicro];
@@ -326,46 +324,28 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
              })) != cudaSuccess)
             return cuda_err(h, e, "fused GEMM launch");
     } else if (c.dtype == MOE_BF16) {
-        CUtensorMap tmA, tmB[kMaxMicro];
-        // GEMM1 + SwiGLU: xp [R][H] x w13[m] [E*2I][H] -> h [R][M*I]
-        if (!encode_2d(&tmA, h->xp, H, R, (uint64_t)H * 2))
-            return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (xp)");
+        CUtensorMap tmW[kMaxMicro], tmX[4];
+        const int chunk_bound = (int)(R / 256) + E;  // bound on sum over experts of ceil(count/256)
+        // GEMM1 + SwiGLU: xp [R][H] x w13[m] [E][2I][H] -> h [R][M*I]
+        if (!encode_rows_pair(tmX, h->xp, H, R)) return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (xp)");
         for (int m = 0; m < M; ++m)
-            if (!encode_w13_tc(&tmB[m], w13[m], H, I, E))
+            if (!encode_w13_pair(&tmW[m], w13[m], H, I, E))
                 return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (w13[%d])", m);
-        TcGemmArgs g1{h->offsets, h->tiles_tc, E, M, H / kTcBK, I / 128, 2 * I, I, 0,
-                      h->hbuf, (int64_t)M * I, I, M * routed_tiles_tc * (I / 128), h->err, h->limit_ns};
-        g1.early = 1;  // behind the gather
-        if ((e = timed(h, kSlotGemm1, s, [&] { return launch_tc_gemm_swiglu(g1, tmA, tmB, h->num_sms, s); })) != cudaSuccess)
+        PairGemmArgs g1{h->offsets, E, M, H / kTcBK, I / 128, 0, 0, h->hbuf, (int64_t)M * I, I,
+                        M * chunk_bound * (I / 128), h->err, h->limit_ns, 0, 1};  // early: behind the gather
+        if ((e = timed(h, kSlotGemm1, s, [&] { return launch_pair_gemm_swiglu(g1, tmW, tmX, s); })) != cudaSuccess)
             return cuda_err(h, e, "GEMM1 launch");
         // GEMM2: h [R][M*I] x w2[m] [E*H][I], summed over m -> o [R][H]
-        if (!encode_2d(&tmA, h->hbuf, (uint64_t)M * I, R, (uint64_t)M * I * 2))
+        if (!encode_rows_pair(tmX, h->hbuf, (uint64_t)M * I, R))
             return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (h)");
         for (int m = 0; m < M; ++m)
-            if (!encode_w2_tc(&tmB[m], w2[m], I, (uint64_t)E * H))
+            if (!encode_w2_pair(&tmW[m], w2[m], I, (uint64_t)E * H))
                 return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (w2[%d])", m);
-        TcGemmArgs g2{h->offsets, h->tiles_tc, E, M, I / kTcBK, H / 256, H, 0, I,
-                      h->obuf, (int64_t)H, 0, routed_tiles_tc * (H / 256), h->err, h->limit_ns};
-        g2.early = 1;  // behind GEMM1
-        if ((e = timed(h, kSlotGemm2, s, [&] { return launch_tc_gemm_down(g2, tmA, tmB, h->num_sms, s); })) != cudaSuccess)
+        PairGemmArgs g2{h->offsets, E, M, I / kTcBK, H / 256, H, I, h->obuf, (int64_t)H, 0,
+                        chunk_bound * (H / 256), h->err, h->limit_ns, 0, 1};  // early: behind GEMM1
+        if ((e = timed(h, kSlotGemm2, s, [&] { return launch_pair_gemm_down(g2, tmW, tmX, s); })) != cudaSuccess)
             return cuda_err(h, e, "GEMM2 launch");
-        if (Is > 0 && !fork) {
-            const int stiles = (T + kTcBM - 1) / kTcBM;
-            if (!encode_2d(&tmA, x, H, T, (uint64_t)H * 2) || !encode_w13_tc(&tmB[0], sw13, H, Is, 1))
-                return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (shared GEMM1)");
-            TcGemmArgs s1{h->shared_meta, h->shared_meta + 2, 1, 1, H / kTcBK, Is / 128, 2 * Is, Is, 0,
-                          h->hs, (int64_t)Is, 0, stiles * (Is / 128), h->err, h->limit_ns};
-            s1.early = 1;  // behind the routed GEMM2
-            if ((e = timed(h, kSlotSharedGemm1, s, [&] { return launch_tc_gemm_swiglu(s1, tmA, tmB, h->num_sms, s); })) != cudaSuccess)
-                return cuda_err(h, e, "shared GEMM1 launch");
-            if (!encode_2d(&tmA, h->hs, Is, T, (uint64_t)Is * 2) || !encode_w2_tc(&tmB[0], sw2, Is, H))
-                return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (shared GEMM2)");
-            TcGemmArgs s2{h->shared_meta, h->shared_meta + 2, 1, 1, Is / kTcBK, H / 256, H, 0, Is,
-                          h->sbuf, (int64_t)H, 0, stiles * (H / 256), h->err, h->limit_ns};
-            s2.early = 1;  // behind the shared GEMM1
-            if ((e = timed(h, kSlotSharedGemm2, s, [&] { return launch_tc_gemm_down(s2, tmA, tmB, h->num_sms, s); })) != cudaSuccess)
-                return cuda_err(h, e, "shared GEMM2 launch");
-        }
+        if (Is > 0 && !fork && (st = run_shared_pair(h, x, sw13, sw2, T, s, 1)) != MOE_OK) return st;
     } else {
         const int routed_tiles = (int)(R / kSimtBM) + E;
         SimtGemmArgs g1{};
@@ -434,6 +414,27 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
         if ((e = timed(h, kSlotFinalize, s, [&] { return launch_finalize(fa, s); })) != cudaSuccess)
             return cuda_err(h, e, "finalize launch");
     }
+    return MOE_OK;
+}
+
+moe_status run_shared_pair(moe_handle* h, const void* x, const void* sw13, const void* sw2, int32_t T,
+                           cudaStream_t ss, int early) {
+    const int H = h->cfg.hidden, Is = h->cfg.shared_inter;
+    const int chunks = (T + 255) / 256;
+    CUtensorMap tmW[1], tmX[4];
+    cudaError_t e;
+    if (!encode_rows_pair(tmX, x, H, T) || !encode_w13_pair(&tmW[0], sw13, H, Is, 1))
+        return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (shared GEMM1)");
+    PairGemmArgs s1{nullptr, 1, 1, H / kTcBK, Is / 128, 0, 0, h->hs, (int64_t)Is, 0, chunks * (Is / 128), h->err,
+                    h->limit_ns, T, early};
+    if ((e = timed(h, kSlotSharedGemm1, ss, [&] { return launch_pair_gemm_swiglu(s1, tmW, tmX, ss); })) != cudaSuccess)
+        return cuda_err(h, e, "shared GEMM1 launch");
+    if (!encode_rows_pair(tmX, h->hs, Is, T) || !encode_w2_pair(&tmW[0], sw2, Is, H))
+        return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (shared GEMM2)");
+    PairGemmArgs s2{nullptr, 1, 1, Is / kTcBK, H / 256, H, Is, h->sbuf, (int64_t)H, 0, chunks * (H / 256), h->err,
+                    h->limit_ns, T, early};
+    if ((e = timed(h, kSlotSharedGemm2, ss, [&] { return launch_pair_gemm_down(s2, tmW, tmX, ss); })) != cudaSuccess)
+        return cuda_err(h, e, "shared GEMM2 launch");
     return MOE_OK;
 }
 
