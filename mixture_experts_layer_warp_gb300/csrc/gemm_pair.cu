@@ -33,8 +33,9 @@
 // CTA: warp 0 issues TMA loads into a 6-stage ring (both CTAs; completion
 // counted on the leader's barrier), warp 1 of the leader issues the MMAs into
 // one of two TMEM accumulators (2 x 256 fp32 columns), warp 2 owns the TMEM
-// allocation, warps 4-7 drain an accumulator (one TMEM lane quarter each)
-// while the next tile accumulates into the other. All waits are bounded.
+// allocation, warps 4-7 drain an accumulator (one TMEM lane quarter each,
+// transposed through shared memory into 16-byte stores of token rows) while
+// the next tile accumulates into the other. All waits are bounded.
 #include <cuda_bf16.h>
 
 #include "gemm_common.cuh"
@@ -66,7 +67,14 @@ struct Ctl {
     int chunks[kMaxExperts + 1];  // prefix over groups of ceil(rows / kChunk)
 };
 
-constexpr int kSmemBytes = kStages * kStageBytes + (int)sizeof(Ctl) + 1024;
+// Epilogue staging, per epilogue warp: one 32-token block of its accumulator
+// lanes, transposed through shared memory so that each thread stores 16-byte
+// pieces of token rows (GEMM2: 32 x 33 fp32 with a pad column against bank
+// conflicts; GEMM1: 32 tokens x 16 features of bf16).
+constexpr int kEpiFloats = 32 * 33;
+constexpr int kEpiBytes = 4 * kEpiFloats * 4;
+
+constexpr int kSmemBytes = kStages * kStageBytes + kEpiBytes + (int)sizeof(Ctl) + 1024;
 
 struct PairTile {
     int m, g, f;
@@ -133,7 +141,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // operands through its own shared-memory descriptors
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Ctl& c = *reinterpret_cast<Ctl*>(smem + kStages * kStageBytes);
+    float* epi_buf = reinterpret_cast<float*>(smem + kStages * kStageBytes);
+    Ctl& c = *reinterpret_cast<Ctl*>(smem + kStages * kStageBytes + kEpiBytes);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t rank = ptx::cluster_ctarank();
     const bool leader = rank == 0;
@@ -326,35 +335,57 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ptx::tc_fence_after();
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kChunk);
+            float* buf = epi_buf + q * kEpiFloats;
             if (SWIGLU) {
                 // lanes 0-15: gate of features feat0 + lane; lanes 16-31: up of the same
-                const int feat = t.m * a.out_micro_cols + t.f * 128 + (int)rank * 64 + q * 16 + (lane & 15);
+                const int feat0 = t.m * a.out_micro_cols + t.f * 128 + (int)rank * 64 + q * 16;
                 const bool is_gate = lane < 16;
-                __nv_bfloat16* dst = out + (int64_t)t.start * a.out_ld + feat;
+                __nv_bfloat16* hb = reinterpret_cast<__nv_bfloat16*>(buf);  // [32 tokens][16 features]
 #pragma unroll 1
                 for (int c0 = 0; c0 < t.n; c0 += 32) {
                     uint32_t v[32];
                     ptx::tmem_ld32(tbase + c0, v);
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        // token c0+2i goes to the gate lane, c0+2i+1 to the up lane
+                        // token 2i goes to the gate lane, 2i+1 to the up lane; either way
+                        // element (token, feature) lands at hb[32 i + lane]
                         const float v0 = __uint_as_float(v[2 * i]), v1 = __uint_as_float(v[2 * i + 1]);
                         const float other = __shfl_xor_sync(0xffffffffu, is_gate ? v1 : v0, 16);
                         const float h = is_gate ? silu(v0) * other : silu(other) * v1;
-                        const int tok = c0 + 2 * i + (is_gate ? 0 : 1);
-                        if (tok < t.len) dst[(int64_t)tok * a.out_ld] = __float2bfloat16_rn(h);
+                        hb[32 * i + lane] = __float2bfloat16_rn(h);
                     }
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const int piece = lane + 32 * j, tok = piece >> 1, half = piece & 1;
+                        const uint4 u = *reinterpret_cast<const uint4*>(hb + tok * 16 + half * 8);
+                        if (c0 + tok < t.len)
+                            *reinterpret_cast<uint4*>(out + (int64_t)(t.start + c0 + tok) * a.out_ld + feat0 + half * 8) = u;
+                    }
+                    __syncwarp();
                 }
             } else {
-                const int feat = t.f * 256 + (int)rank * 128 + q * 32 + lane;
-                __nv_bfloat16* dst = out + (int64_t)t.start * a.out_ld + feat;
+                // lane = output feature feat0 + lane; each thread then stores 8
+                // features of 4 tokens
+                const int feat0 = t.f * 256 + (int)rank * 128 + q * 32;
+                const int sub = lane & 3;
 #pragma unroll 1
                 for (int c0 = 0; c0 < t.n; c0 += 32) {
                     uint32_t v[32];
                     ptx::tmem_ld32(tbase + c0, v);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (c0 + i < t.len) dst[(int64_t)(c0 + i) * a.out_ld] = __float2bfloat16_rn(__uint_as_float(v[i]));
+                    for (int i = 0; i < 32; ++i) buf[i * 33 + lane] = __uint_as_float(v[i]);
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int tok = j * 8 + (lane >> 2);
+                        const float* r = buf + tok * 33 + sub * 8;
+                        const uint4 u = make_uint4(pack_bf16x2(r[0], r[1]), pack_bf16x2(r[2], r[3]),
+                                                   pack_bf16x2(r[4], r[5]), pack_bf16x2(r[6], r[7]));
+                        if (c0 + tok < t.len)
+                            *reinterpret_cast<uint4*>(out + (int64_t)(t.start + c0 + tok) * a.out_ld + feat0 + sub * 8) = u;
+                    }
+                    __syncwarp();
                 }
             }
             ptx::tc_fence_before();
