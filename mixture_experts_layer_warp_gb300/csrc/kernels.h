@@ -105,6 +105,10 @@ struct RouterTcArgs {
 // tmX: x [T][H] bf16, box {64, 128}; tmW: Wr [E][H] bf16, box {64, 64}.
 cudaError_t launch_router_tc(const RouterTcArgs& a, const CUtensorMap& tmX, const CUtensorMap& tmW,
                              cudaStream_t s);
+// Mid-size batches: 4-CTA clusters per 128 tokens splitting K (tmX box {64, 128});
+// same logits and the same 128-token block histograms as launch_router_tc.
+cudaError_t launch_router_tc_split(const RouterTcArgs& a, const CUtensorMap& tmX, const CUtensorMap& tmW,
+                                   cudaStream_t s);
 // T <= kSmallTokens: one 8-CTA cluster; tmX box {64, 16}. Same logits bit for bit.
 cudaError_t launch_router_tc_small(const RouterTcArgs& a, const CUtensorMap& tmX, const CUtensorMap& tmW,
                                    cudaStream_t s);
@@ -133,6 +137,10 @@ struct PlaceArgs {
     int* err;
 };
 cudaError_t launch_place(const PlaceArgs& a, cudaStream_t s);
+// Both in one launch when NB * E <= kScanPlaceMaxInts (each block reads every
+// histogram row to find its own bases).
+constexpr int kScanPlaceMaxInts = 16384;
+cudaError_t launch_scan_place(const ScanArgs& sa, const PlaceArgs& a, cudaStream_t s);
 
 struct GatherArgs {
     const void* x;            // [T][row_bytes]

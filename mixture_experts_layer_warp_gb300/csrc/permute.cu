@@ -101,6 +101,112 @@ __global__ void __launch_bounds__(kPlaceWarps * 32) place_kernel(PlaceArgs a) {
     ptx::griddep_launch_dependents();
 }
 
+// Scan and placement in one launch, for batches whose block histograms are
+// small enough for every block to read them all (NB * E <= kScanPlaceMaxInts):
+// block b sums every histogram row itself, which gives offsets[e] (all routes
+// of experts < e) and its own base[b][e] = offsets[e] + (routes of expert e in
+// blocks < b) without a separate pass; block 0 also writes the offsets, the
+// tile prefixes and the shared expert's segment. The placement is the same
+// stable warp-round placement as place_kernel.
+constexpr int kSumParts = kPlaceWarps * 32 / kMaxExperts;  // 4 threads per expert sum the rows
+
+__global__ void __launch_bounds__(kPlaceWarps * 32) scan_place_kernel(ScanArgs sa, PlaceArgs a) {
+    __shared__ int sid[kRouterTokensTc * kMaxTopK];
+    __shared__ int cnt[kPlaceWarps][kMaxExperts];
+    __shared__ int run[kPlaceWarps][kMaxExperts];
+    __shared__ int tot_part[kSumParts][kMaxExperts];
+    __shared__ int bef_part[kSumParts][kMaxExperts];
+    __shared__ int off[kMaxExperts + 1];
+    __shared__ int base[kMaxExperts];
+    ptx::griddep_wait();  // launched early: the router's ids and histograms are complete past here
+    const int E = a.E, NB = a.NB, b = blockIdx.x, tid = threadIdx.x;
+    const int64_t R = (int64_t)a.T * a.k;
+    const int64_t r0 = (int64_t)b * a.tok_per_blk * a.k;
+    const int64_t left = R - r0;
+    const int n = (int)(left < (int64_t)a.tok_per_blk * a.k ? left : (int64_t)a.tok_per_blk * a.k);
+    for (int i = tid; i < n; i += blockDim.x) sid[i] = a.ids[r0 + i];
+    {
+        const int e = tid % kMaxExperts, q = tid / kMaxExperts;
+        int tot = 0, bef = 0;
+        if (e < E) {
+#pragma unroll 16
+            for (int row = q; row < NB; row += kSumParts) {
+                const int v = sa.blk_hist[(int64_t)row * E + e];
+                tot += v;
+                bef += row < b ? v : 0;
+            }
+        }
+        tot_part[q][e] = tot;
+        bef_part[q][e] = bef;
+    }
+    __syncthreads();
+    if (tid < 32) {
+        // warp-wide exclusive scan of the expert totals (two experts per lane)
+        const int lane = tid, e0 = 2 * lane, e1 = 2 * lane + 1;
+        int c0 = 0, c1 = 0;
+#pragma unroll
+        for (int q = 0; q < kSumParts; ++q) {
+            c0 += tot_part[q][e0];
+            c1 += tot_part[q][e1];
+        }
+        int s_cnt = c0 + c1;
+        int s_tc = (c0 + kTcBM - 1) / kTcBM + (c1 + kTcBM - 1) / kTcBM;
+        int s_si = (c0 + kSimtBM - 1) / kSimtBM + (c1 + kSimtBM - 1) / kSimtBM;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int a0 = __shfl_up_sync(0xffffffffu, s_cnt, d);
+            const int a1 = __shfl_up_sync(0xffffffffu, s_tc, d);
+            const int a2 = __shfl_up_sync(0xffffffffu, s_si, d);
+            if (lane >= d) {
+                s_cnt += a0;
+                s_tc += a1;
+                s_si += a2;
+            }
+        }
+        const int x_cnt = s_cnt - c0 - c1;
+        const int x_tc = s_tc - (c0 + kTcBM - 1) / kTcBM - (c1 + kTcBM - 1) / kTcBM;
+        const int x_si = s_si - (c0 + kSimtBM - 1) / kSimtBM - (c1 + kSimtBM - 1) / kSimtBM;
+        if (e0 <= E) off[e0] = x_cnt;
+        if (e1 <= E) off[e1] = x_cnt + c0;
+        if (E == kMaxExperts && lane == 31) off[kMaxExperts] = s_cnt;
+        if (b == 0) {
+            if (e0 <= E) {
+                sa.offsets[e0] = x_cnt;
+                sa.tiles_tc[e0] = x_tc;
+                sa.tiles_simt[e0] = x_si;
+            }
+            if (e1 <= E) {
+                sa.offsets[e1] = x_cnt + c0;
+                sa.tiles_tc[e1] = x_tc + (c0 + kTcBM - 1) / kTcBM;
+                sa.tiles_simt[e1] = x_si + (c0 + kSimtBM - 1) / kSimtBM;
+            }
+            if (E == kMaxExperts && lane == 31) {
+                sa.offsets[kMaxExperts] = s_cnt;
+                sa.tiles_tc[kMaxExperts] = s_tc;
+                sa.tiles_simt[kMaxExperts] = s_si;
+            }
+            if (lane == 0) {
+                sa.shared_seg[0] = 0;
+                sa.shared_seg[1] = sa.T;
+                sa.shared_tiles_tc[0] = 0;
+                sa.shared_tiles_tc[1] = (sa.T + kTcBM - 1) / kTcBM;
+                sa.shared_tiles_simt[0] = 0;
+                sa.shared_tiles_simt[1] = (sa.T + kSimtBM - 1) / kSimtBM;
+            }
+        }
+    }
+    __syncthreads();
+    if (tid < E) {
+        int bef = off[tid];
+#pragma unroll
+        for (int q = 0; q < kSumParts; ++q) bef += bef_part[q][tid];
+        base[tid] = bef;
+    }
+    __syncthreads();
+    place_chunk<kPlaceWarps>(sid, n, r0, E, R, [&](int e) { return base[e]; }, cnt, run, a.perm, a.inv, a.err);
+    ptx::griddep_launch_dependents();
+}
+
 // The gather xp[i] = x[perm[i] / k], run as the equivalent scatter
 // xp[inv[t*k + j]] = x[t]: one warp per token reads its row once (16-byte
 // vector loads on the read-only path, four per lane in flight) and writes it
@@ -158,6 +264,12 @@ cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s) {
 cudaError_t launch_place(const PlaceArgs& a, cudaStream_t s) {
     if (a.NB == 0) return cudaSuccess;
     return launch_kernel(place_kernel, dim3(a.NB), dim3(kPlaceWarps * 32), 0, s, true, a);
+}
+
+cudaError_t launch_scan_place(const ScanArgs& sa, const PlaceArgs& a, cudaStream_t s) {
+    if (a.NB == 0) return cudaSuccess;
+    if ((int64_t)a.NB * a.E > kScanPlaceMaxInts) return cudaErrorInvalidValue;
+    return launch_kernel(scan_place_kernel, dim3(a.NB), dim3(kPlaceWarps * 32), 0, s, true, sa, a);
 }
 
 cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s) {

@@ -479,6 +479,11 @@ __device__ __forceinline__ void tma_load_5d_pair(uint32_t dst, const void* tmap,
         : "memory");
 }
 
+// Atomic add to a 32-bit word in another CTA's shared memory (shared::cluster address).
+__device__ __forceinline__ void red_add_cluster(uint32_t caddr, uint32_t v) {
+    asm volatile("red.relaxed.cluster.shared::cluster.add.u32 [%0], %1;" ::"r"(caddr), "r"(v) : "memory");
+}
+
 // Arrive on a barrier of another CTA of the cluster (shared::cluster address),
 // releasing this thread's prior writes at cluster scope.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cbar) {

@@ -640,6 +640,316 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     ptx::cluster_wait();   // no CTA leaves before CTA 0 holds every partial
 }
 
+// ------------------------------------------------------------------------
+// Mid-size batches (a few thousand tokens): a cluster of kSplit = 4 CTAs per
+// 128-token block splits K, so the batch fills the GPU instead of one SM per
+// 128 tokens. CTA r accumulates exactly the K-blocks of partials 2r and 2r+1 of
+// router_tc_kernel (kb = 8i + 2r and 8i + 2r + 1), in the same order, into two
+// TMEM accumulators. Then every CTA sends each 32-token slice of its two
+// partials to the CTA that owns the slice (st.async completing bytes on the
+// owner's exchange barrier), and CTA r combines the eight partials of tokens
+// 32r .. 32r+31 in the same compensated order as router_tc_kernel: the logits
+// are bit-identical to the other kernels'. Four threads per token select the
+// top-k. The four CTAs add their expert counts into CTA 0 (shared-memory
+// reductions across the cluster), which writes the 128-token block's histogram
+// row, as router_tc_kernel does.
+constexpr int kSplit = 4;
+constexpr int kSplitTok = kTok / kSplit;              // 32 tokens combined per CTA
+constexpr int kSPartsPer = kParts / kSplit;           // 2 partials accumulated per CTA
+constexpr int kSStages = 6;
+constexpr int kSRecvBytes = kParts * kSplitTok * kN * 4;   // [partial][token][expert] fp32: 64 KB
+constexpr int kSSendBytes = kSPartsPer * kSplitTok * kN * 4;  // one CTA's contribution to a slice: 16 KB
+constexpr int kSGroup = kThreads / kSplitTok;         // 4 threads per token in the top-k
+constexpr int kSPer = kN / kSGroup;                   // 16 experts per thread
+static_assert(kSplitTok == 32 && kSGroup == 4, "one TMEM lane quarter per destination CTA");
+
+struct SCtl {
+    uint64_t full[kSStages];
+    uint64_t empty[kSStages];
+    uint64_t done;
+    uint64_t xfer;  // completes when the other CTAs' slices of this CTA's tokens have arrived
+    uint32_t tmem;
+    int abort;
+    int hist[kMaxExperts];
+    int hist_all[kMaxExperts];  // CTA 0: the four CTAs' counts
+};
+constexpr int kSSmemBytes = kSStages * kStageBytes + kSRecvBytes + (int)sizeof(SCtl) + 1024;
+
+__global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kThreads, 1)
+    router_tc_split_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                           const RouterTcArgs a) {
+    ptx::griddep_launch_dependents();
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float* recv = reinterpret_cast<float*>(smem + kSStages * kStageBytes);
+    SCtl& c = *reinterpret_cast<SCtl*>(smem + kSStages * kStageBytes + kSRecvBytes);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int rank = (int)ptx::cluster_ctarank();
+    const int blk = blockIdx.x / kSplit;
+    const int t0 = blk * kTok;
+    const int E = a.E, k = a.k;
+    const int kb_total = a.H / kTcBK;
+    const int nparts = kb_total < kParts ? kb_total : kParts;
+    // this CTA's K-blocks, in increasing kb: q -> 8 (q / 2) + 2 rank + q % 2
+    int my_blocks = 0;
+    for (int kb0 = 2 * rank; kb0 < kb_total; kb0 += kParts) my_blocks += (kb0 + 1 < kb_total) ? 2 : 1;
+    const uint32_t xfer = ptx::smem_u32(&c.xfer);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kSStages; ++s) {
+            ptx::mbar_init(ptx::smem_u32(&c.full[s]), 1);
+            ptx::mbar_init(ptx::smem_u32(&c.empty[s]), 1);
+        }
+        ptx::mbar_init(ptx::smem_u32(&c.done), 1);
+        ptx::mbar_init(xfer, 1);
+        // the bytes the other three CTAs will send, announced before any can
+        // start (they first pass the cluster barrier that follows the init)
+        ptx::mbar_arrive_expect_tx(xfer, (uint32_t)((kSplit - 1) * kSSendBytes));
+        c.abort = 0;
+        ptx::fence_mbar_init();
+    }
+    if (threadIdx.x < kMaxExperts) c.hist[threadIdx.x] = c.hist_all[threadIdx.x] = 0;
+    if (warp == 2) {
+        ptx::tmem_alloc(ptx::smem_u32(&c.tmem), kSPartsPer * kN);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    ptx::cluster_arrive();   // first phase: barrier inits visible cluster-wide
+    // launched early (programmatic dependent launch): no global memory is
+    // touched before the previous kernel in the stream has completed
+    ptx::griddep_wait();
+    const uint32_t tmem = c.tmem;
+
+    if (warp == 0) {
+        // TMA producer (whole warp; one elected lane issues)
+        const bool issuer = ptx::elect_one();
+        const uint64_t wpol = ptx::policy_evict_last();  // the router matrix is read on every call
+        int stage = 0;
+        uint32_t phase = 0, last_par[kSStages];
+        int issued = 0;
+        bool ok = true;
+        for (int q = 0; q < my_blocks; ++q) {
+            const int kb = kParts * (q / 2) + 2 * rank + (q & 1);
+            const bool got = ptx::mbar_wait(ptx::smem_u32(&c.empty[stage]), phase ^ 1u, a.limit_ns, &c.abort);
+            if (!__all_sync(0xffffffffu, got)) {
+                ok = false;
+                break;
+            }
+            const uint32_t sa = ptx::smem_u32(smem + stage * kStageBytes);
+            const uint32_t fb = ptx::smem_u32(&c.full[stage]);
+            if (issuer) {
+                ptx::mbar_arrive_expect_tx(fb, kStageBytes);
+                ptx::tma_load_2d(sa, &tmX, kb * kTcBK, t0, fb);
+                ptx::tma_load_2d_hint(sa + kABytes, &tmW, kb * kTcBK, 0, fb, wpol);
+            }
+            __syncwarp();
+            last_par[stage] = phase;
+            ++issued;
+            if (++stage == kSStages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        if (!ok && issuer) {
+            c.abort = 1;
+            atomicOr(a.err, kErrTimeout);
+            const int n = issued < kSStages ? issued : kSStages;
+            for (int s = 0; s < n; ++s) ptx::mbar_wait(ptx::smem_u32(&c.full[s]), last_par[s], a.limit_ns, nullptr);
+        }
+    } else if (warp == 1) {
+        // MMA issuer (whole warp; one elected lane issues): K-block q goes to
+        // accumulator q % 2 (partial 2 rank + q % 2)
+        const bool issuer = ptx::elect_one();
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int q = 0; q < my_blocks; ++q) {
+            const bool got = ptx::mbar_wait(ptx::smem_u32(&c.full[stage]), phase, a.limit_ns, &c.abort);
+            if (!__all_sync(0xffffffffu, got)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t sa = ptx::smem_u32(smem + stage * kStageBytes);
+            const uint64_t adesc = ptx::sw128_desc(sa), bdesc = ptx::sw128_desc(sa + kABytes);
+            const uint32_t d = tmem + (uint32_t)((q & 1) * kN);
+            if (issuer) {
+#pragma unroll
+                for (int kk = 0; kk < kTcBK / 16; ++kk)
+                    ptx::mma_bf16(d, adesc + 2u * kk, bdesc + 2u * kk, kIdesc, (q >= 2 || kk > 0) ? 1u : 0u);
+                ptx::mma_commit(ptx::smem_u32(&c.empty[stage]));
+            }
+            __syncwarp();
+            if (++stage == kSStages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        if (issuer) {
+            if (!ok) {
+                c.abort = 1;
+                atomicOr(a.err, kErrTimeout);
+            }
+            ptx::mma_commit(ptx::smem_u32(&c.done));
+        }
+        __syncwarp();
+    }
+
+    bool ready = false;
+    if (lane == 0)
+        ready = ptx::mbar_wait(ptx::smem_u32(&c.done), 0, a.limit_ns, nullptr) &&
+                *static_cast<volatile int*>(&c.abort) == 0;
+    ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
+    ptx::tc_fence_after();
+    ptx::cluster_wait();   // every CTA's exchange barrier is armed before anyone sends
+
+    // warp w holds TMEM lanes 32w.. = the tokens CTA w combines: send both
+    // partials of each of them there (partial slot 2 rank + j of its buffer).
+    // Every CTA sends, also one without K-blocks (H < 512): the owner expects
+    // the bytes and skips the partials that do not exist.
+    if (ready) {
+        const int dst_cta = warp;
+        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+#pragma unroll
+        for (int j = 0; j < kSPartsPer; ++j) {
+            uint32_t v[kN];
+            const uint32_t b = lane_base + (uint32_t)(j * kN);
+            ptx::tmem_ld16x4(b, b + 16u, b + 32u, b + 48u, v);
+            float* mine = recv + ((size_t)(kSPartsPer * rank + j) * kSplitTok + lane) * kN;
+            if (dst_cta == rank) {
+#pragma unroll
+                for (int q = 0; q < kN / 4; ++q)
+                    reinterpret_cast<float4*>(mine)[q] = make_float4(
+                        __uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]), __uint_as_float(v[4 * q + 2]),
+                        __uint_as_float(v[4 * q + 3]));
+            } else {
+                const uint32_t dst = ptx::map_to_rank(ptx::smem_u32(mine), (uint32_t)dst_cta);
+                const uint32_t bar = ptx::map_to_rank(xfer, (uint32_t)dst_cta);
+#pragma unroll
+                for (int q = 0; q < kN / 4; ++q)
+                    ptx::st_async_v4(dst + 16u * q, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3], bar);
+            }
+        }
+    } else if (lane == 0) {
+        atomicOr(a.err, kErrTimeout);
+    }
+    __syncthreads();  // this CTA's own slice is in shared memory
+
+    // the other CTAs' slices: bounded wait on the exchange barrier (also when
+    // this CTA failed, so that no write lands after it has exited)
+    bool got = true;
+    if (threadIdx.x == 0) {
+        got = ptx::mbar_wait_cluster(xfer, 0, a.limit_ns);
+        if (!got) atomicOr(a.err, kErrTimeout);
+    }
+    const bool go = __syncthreads_and(got && ready) != 0;
+
+    const int r = threadIdx.x / kSGroup, g = threadIdx.x % kSGroup;
+    const int64_t t = (int64_t)t0 + kSplitTok * rank + r;
+    if (go && t < a.T) {
+        // thread (token r, group position g) owns experts 16g .. 16g+15
+        const unsigned gmask = 0xfu << (lane & ~(kSGroup - 1));
+        float l[kSPer];
+        {
+            float sum[kSPer], comp[kSPer];
+#pragma unroll
+            for (int i = 0; i < kSPer; ++i) sum[i] = comp[i] = 0.f;
+            for (int p = 0; p < nparts; ++p) {  // partials in order 0..7, as router_tc_kernel
+                const float4* src = reinterpret_cast<const float4*>(recv + ((size_t)p * kSplitTok + r) * kN + g * kSPer);
+#pragma unroll
+                for (int q = 0; q < kSPer / 4; ++q) {
+                    const float4 v = src[q];
+                    kahan_add(sum[4 * q], comp[4 * q], v.x);
+                    kahan_add(sum[4 * q + 1], comp[4 * q + 1], v.y);
+                    kahan_add(sum[4 * q + 2], comp[4 * q + 2], v.z);
+                    kahan_add(sum[4 * q + 3], comp[4 * q + 3], v.w);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < kSPer; ++i) {
+                const int e = g * kSPer + i;
+                l[i] = sum[i];
+                if (e < E) {
+                    if (a.bias != nullptr) l[i] += a.bias[e];
+                    if (a.logits != nullptr) a.logits[t * E + e] = l[i];
+                } else {
+                    l[i] = -INFINITY;
+                }
+            }
+        }
+        // k rounds: the group's maximum logit, lower expert index on equal
+        // logits (the rule of select_topk), then masked out; weights summed in
+        // round order as select_topk does. Thread g keeps slots g, g+4, g+8, g+12.
+        float v0 = 0.f, den = 0.f, wk[kMaxTopK / kSGroup];
+        int idk[kMaxTopK / kSGroup];
+#pragma unroll
+        for (int u = 0; u < kMaxTopK / kSGroup; ++u) {
+            wk[u] = 0.f;
+            idk[u] = 0;
+        }
+#pragma unroll 1
+        for (int j = 0; j < k; ++j) {
+            float bv = l[0];
+            int bi = 0;
+#pragma unroll
+            for (int i = 1; i < kSPer; ++i)
+                if (l[i] > bv) {
+                    bv = l[i];
+                    bi = i;
+                }
+            bi += g * kSPer;
+#pragma unroll
+            for (int d = 1; d < kSGroup; d <<= 1) {
+                const float ov = __shfl_xor_sync(gmask, bv, d);
+                const int oi = __shfl_xor_sync(gmask, bi, d);
+                if (ov > bv || (ov == bv && oi < bi)) {
+                    bv = ov;
+                    bi = oi;
+                }
+            }
+            if (g == 0 && (bv != bv || bi >= E)) atomicOr(a.err, kErrCheck);  // NaN logits only
+#pragma unroll
+            for (int i = 0; i < kSPer; ++i)
+                if (g * kSPer + i == bi) l[i] = -INFINITY;
+            if (j == 0) v0 = bv;
+            const float ej = expf(bv - v0);
+            den += ej;
+#pragma unroll
+            for (int u = 0; u < kMaxTopK / kSGroup; ++u)
+                if (j == g + kSGroup * u) {
+                    wk[u] = ej;
+                    idk[u] = bi;
+                }
+        }
+#pragma unroll
+        for (int u = 0; u < kMaxTopK / kSGroup; ++u) {
+            const int slot = g + kSGroup * u;
+            if (slot < k) {
+                a.ids[t * k + slot] = idk[u];
+                a.w[t * k + slot] = wk[u] / den;
+                atomicAdd(&c.hist[idk[u]], 1);
+            }
+        }
+    }
+    __syncthreads();
+    // this CTA's counts into CTA 0's; the second cluster phase orders them
+    // before CTA 0 reads the sum (and keeps every CTA alive until all hold their slices)
+    if ((int)threadIdx.x < E && c.hist[threadIdx.x] != 0)
+        ptx::red_add_cluster(ptx::map_to_rank(ptx::smem_u32(&c.hist_all[threadIdx.x]), 0),
+                             (uint32_t)c.hist[threadIdx.x]);
+    ptx::tc_fence_before();
+    ptx::cluster_arrive();
+    ptx::cluster_wait();
+    if (rank == 0 && (int)threadIdx.x < E) a.blk_hist[(int64_t)blk * E + threadIdx.x] = c.hist_all[threadIdx.x];
+    if (warp == 2) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, kSPartsPer * kN);
+    }
+}
+
 // Launch with programmatic stream serialization: the CTAs may be placed while
 // the previous kernel in the stream finishes (its CTAs free SMs); each kernel
 // here waits for it (griddep_wait) after its shared-memory and TMEM set-up.
@@ -667,6 +977,14 @@ cudaError_t launch_router_tc(const RouterTcArgs& a, const CUtensorMap& tmX, cons
     if (nb == 0) return cudaSuccess;
     if (cudaError_t e = ensure_smem_limit<router_tc_kernel>(kSmemBytes); e != cudaSuccess) return e;
     return launch_early(router_tc_kernel, dim3(nb), kSmemBytes, s, tmX, tmW, a);
+}
+
+cudaError_t launch_router_tc_split(const RouterTcArgs& a, const CUtensorMap& tmX, const CUtensorMap& tmW,
+                                   cudaStream_t s) {
+    const int nb = (a.T + kTok - 1) / kTok;
+    if (nb == 0) return cudaSuccess;
+    if (cudaError_t e = ensure_smem_limit<router_tc_split_kernel>(kSSmemBytes); e != cudaSuccess) return e;
+    return launch_early(router_tc_split_kernel, dim3(nb * kSplit), kSSmemBytes, s, tmX, tmW, a);
 }
 
 cudaError_t launch_router_tc_small(const RouterTcArgs& a, const CUtensorMap& tmX, const CUtensorMap& tmW,

@@ -22,6 +22,15 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
+// SMs of the current device, looked up once per device.
+int num_sms() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cached[dev] == 0) cudaDeviceGetAttribute(&cached[dev], cudaDevAttrMultiProcessorCount, dev);
+    return cached[dev];
+}
+
 template <typename F>
 cudaError_t hooked(const LaunchHook* hook, int slot, cudaStream_t s, F&& launch) {
     if (hook && hook->before) hook->before(hook->ctx, slot, s);
@@ -93,13 +102,19 @@ cudaError_t enqueue_routing(const RoutingJob& j, cudaStream_t s, const LaunchHoo
         RouterTcArgs ra{j.bias, j.T, j.H, j.E, j.k, j.ids, j.w, j.logits, j.blk_hist, j.offsets, j.tiles_tc,
                         j.tiles_simt, j.shared_meta, j.shared_meta + 2, j.shared_meta + 4, j.perm, j.inv,
                         j.zero_counters, j.zero_count, j.err, j.limit_ns};
+        // one CTA (T <= 128) also scans and places; batches whose 4-CTA
+        // clusters fit the GPU at once split K; larger ones keep one CTA per
+        // 128 tokens, several waves of which already fill the GPU
+        const bool single = j.T <= kRouterTokensTc;
+        const bool split = !single && (int64_t)(j.T + kRouterTokensTc - 1) / kRouterTokensTc * 4 <= num_sms();
         e = hooked(hook, kSlotRouter, s, [&] {
-            return small ? launch_router_tc_small(ra, tmX, tmW, s) : launch_router_tc(ra, tmX, tmW, s);
+            return small ? launch_router_tc_small(ra, tmX, tmW, s)
+                   : split ? launch_router_tc_split(ra, tmX, tmW, s) : launch_router_tc(ra, tmX, tmW, s);
         });
         if (e != cudaSuccess) return e;
+        if (single) return cudaSuccess;
         tpb = kRouterTokensTc;
         NB = (j.T + tpb - 1) / tpb;
-        if (NB <= 1) return cudaSuccess;  // the single CTA also scanned and placed
     } else {
         tpb = kRouterTokens;
         NB = (j.T + tpb - 1) / tpb;
@@ -108,8 +123,10 @@ cudaError_t enqueue_routing(const RoutingJob& j, cudaStream_t s, const LaunchHoo
     }
     ScanArgs sa{j.blk_hist, NB, j.E, j.T, j.k, j.blk_base, j.offsets, j.tiles_tc, j.tiles_simt, j.shared_meta,
                 j.shared_meta + 2, j.shared_meta + 4};
-    if ((e = hooked(hook, kSlotScan, s, [&] { return launch_scan(sa, s); })) != cudaSuccess) return e;
     PlaceArgs pa{j.ids, j.blk_base, j.T, j.k, j.E, NB, tpb, j.perm, j.inv, j.err};
+    if ((int64_t)NB * j.E <= kScanPlaceMaxInts)
+        return hooked(hook, kSlotPlace, s, [&] { return launch_scan_place(sa, pa, s); });
+    if ((e = hooked(hook, kSlotScan, s, [&] { return launch_scan(sa, s); })) != cudaSuccess) return e;
     return hooked(hook, kSlotPlace, s, [&] { return launch_place(pa, s); });
 }
 
