@@ -747,22 +747,29 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
     } else if (MODE == kFused && warp == 3 && lane == 0) {
         // ------------------------------------------------ scheduler
         schedule_tiles(c, p, total);
-    } else if (!F8 && warp == 1 && lane == 0) {
+    } else if (!F8 && warp == 1) {
         // ------------------------------------------------ MMA issuer
+        // The whole warp runs the loop (waits and bookkeeping, so descriptors are
+        // warp-uniform values) and one elected lane issues the tcgen05
+        // instructions; lane 0 takes the tiles and broadcasts them.
+        const bool issuer = ptx::elect_one();
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
         TileStream ts;
         ts.next_static = blockIdx.x;
         for (int local = 0; ok; ++local) {
-            const int tile = consume_tile<MODE>(c, ts, total, a0.limit_ns);
+            int tile = -1;
+            if (lane == 0) tile = consume_tile<MODE>(c, ts, total, a0.limit_ns);
+            tile = __shfl_sync(0xffffffffu, tile, 0);
             if (tile < 0) break;
             bool sw;
             locate<MODE>(tile, c, p, sw);
             const TcGemmArgs& g = sw ? p.g1 : p.g2;
             const int acc = local & 1;
             const uint32_t acc_par = (uint32_t)(local >> 1) & 1u;
-            if (!ptx::mbar_wait(ptx::smem_u32(&c.tempty[acc]), acc_par ^ 1u, g.limit_ns, &c.abort)) {
+            const bool drained = ptx::mbar_wait(ptx::smem_u32(&c.tempty[acc]), acc_par ^ 1u, g.limit_ns, &c.abort);
+            if (!__all_sync(0xffffffffu, drained)) {
                 ok = false;
                 break;
             }
@@ -772,37 +779,46 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
             const int n_micro_k = sw ? 1 : g.n_micro;
             for (int mi = 0; ok && mi < n_micro_k; ++mi) {
                 for (int kb = 0; kb < g.k_blocks; ++kb) {
-                    if (!ptx::mbar_wait(ptx::smem_u32(&c.full[stage]), phase, g.limit_ns, &c.abort)) {
+                    const bool got = ptx::mbar_wait(ptx::smem_u32(&c.full[stage]), phase, g.limit_ns, &c.abort);
+                    if (!__all_sync(0xffffffffu, got)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
                     const uint64_t adesc = ptx::sw128_desc(ptx::smem_u32(stage_a(stage)));
                     const uint64_t bdesc = ptx::sw128_desc(ptx::smem_u32(stage_b(stage)));
+                    if (issuer) {
 #pragma unroll
-                    for (int k = 0; k < kTcBK / 16; ++k) {
-                        ptx::mma_bf16(d, adesc + 2u * k, bdesc + 2u * k, kIdesc, accumulate);
-                        accumulate = 1;
+                        for (int k = 0; k < kTcBK / 16; ++k)
+                            ptx::mma_bf16(d, adesc + 2u * k, bdesc + 2u * k, kIdesc, accumulate | (uint32_t)k);
+                        ptx::mma_commit(ptx::smem_u32(&c.empty[stage]));
                     }
-                    ptx::mma_commit(ptx::smem_u32(&c.empty[stage]));
+                    __syncwarp();
+                    accumulate = 1;
                     if (++stage == kSt) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
             }
-            if (ok) ptx::mma_commit(ptx::smem_u32(&c.tfull[acc]));
+            if (ok && issuer) ptx::mma_commit(ptx::smem_u32(&c.tfull[acc]));
+            __syncwarp();
         }
-        if (!ok) fail(c, a0.err);
-        ptx::mma_commit(ptx::smem_u32(&c.drain));
-        ptx::mbar_wait(ptx::smem_u32(&c.drain), 0, a0.limit_ns, nullptr);
-    } else if (F8 && (warp == 1 || warp == 2) && lane == 0) {
+        if (issuer) {
+            if (!ok) fail(c, a0.err);
+            ptx::mma_commit(ptx::smem_u32(&c.drain));
+            ptx::mbar_wait(ptx::smem_u32(&c.drain), 0, a0.limit_ns, nullptr);
+        }
+        __syncwarp();
+    } else if (F8 && (warp == 1 || warp == 2)) {
         // ------------------------------------------------ MXFP8 MMA issuers
         // Issuer j (warp 1 + j) takes the tile's stages of parity j into half j
         // of its accumulator; the epilogue adds the halves (half 0 + half 1,
         // the same order on every call). With N = 16 the stream rate is set by
-        // how fast one thread issues tcgen05 instructions (eight MMAs and two
-        // commits per stage), so two issuing threads raise it.
+        // how fast tcgen05 instructions are issued (eight MMAs and two commits
+        // per stage), so two issuing warps raise it. Each runs as a whole warp
+        // with one elected lane issuing, as the bf16 issuer above.
+        const bool issuer = ptx::elect_one();
         const int j = warp - 1;
         int stage = 0, dq = 0, gs = 0;  // code slot, A buffer, stage number
         uint32_t fb_bits = 0, dq_bits = 0;  // phase bits of this issuer's fullB / dq_full barriers
@@ -810,7 +826,9 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
         TileStream ts;
         ts.next_static = blockIdx.x;
         for (int local = 0; ok; ++local) {
-            const int tile = consume_tile<MODE>(c, ts, total, a0.limit_ns);
+            int tile = -1;
+            if (lane == 0) tile = consume_tile<MODE>(c, ts, total, a0.limit_ns);
+            tile = __shfl_sync(0xffffffffu, tile, 0);
             if (tile < 0) break;
             bool sw;
             locate<MODE>(tile, c, p, sw);
@@ -820,7 +838,8 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
             // the accumulator is free once the epilogue read the tile two back
             // (waited for even without own stages: the commit to tfull below must
             // land in this tile's phase)
-            if (!ptx::mbar_wait(ptx::smem_u32(&c.tempty[acc]), acc_par ^ 1u, g.limit_ns, &c.abort)) {
+            const bool drained = ptx::mbar_wait(ptx::smem_u32(&c.tempty[acc]), acc_par ^ 1u, g.limit_ns, &c.abort);
+            if (!__all_sync(0xffffffffu, drained)) {
                 ok = false;
                 break;
             }
@@ -830,10 +849,11 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
             const int nk = (sw ? 1 : g.n_micro) * f8_stages(g.k_blocks);
             for (int i = 0; i < nk; ++i) {
                 if ((i & 1) == j) {
-                    if (!ptx::mbar_wait(ptx::smem_u32(&c.fullB[j][stage]), (fb_bits >> stage) & 1u, g.limit_ns,
-                                        &c.abort) ||
-                        !ptx::mbar_wait(ptx::smem_u32(&c.dq_full[j][dq]), (dq_bits >> dq) & 1u, g.limit_ns,
-                                        &c.abort)) {
+                    const bool got = ptx::mbar_wait(ptx::smem_u32(&c.fullB[j][stage]), (fb_bits >> stage) & 1u,
+                                                    g.limit_ns, &c.abort) &&
+                                     ptx::mbar_wait(ptx::smem_u32(&c.dq_full[j][dq]), (dq_bits >> dq) & 1u,
+                                                    g.limit_ns, &c.abort);
+                    if (!__all_sync(0xffffffffu, got)) {
                         ok = false;
                         break;
                     }
@@ -842,30 +862,40 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
                     ptx::tc_fence_after();
                     // A buffer dq: 8 columns per 16 K; 64-K chunk h pairs with token tile h
                     const uint32_t at = tmem + (uint32_t)(kF8ACol + dq * kF8ABuf);
+                    const uint32_t sb0 = ptx::smem_u32(stage_b(stage));
+                    if (issuer) {
+                        uint32_t acc_flag = accumulate;
 #pragma unroll
-                    for (int h = 0; h < kF8Chunks; ++h) {
-                        // the second 64-K tile starts after the first one's brows rows
-                        const uint64_t bd = ptx::sw128_desc(ptx::smem_u32(stage_b(stage)) + h * p.brows * 128);
+                        for (int h = 0; h < kF8Chunks; ++h) {
+                            // the second 64-K tile starts after the first one's brows rows
+                            const uint64_t bd = ptx::sw128_desc(sb0 + h * p.brows * 128);
 #pragma unroll
-                        for (int k = 0; k < kTcBK / 16; ++k) {
-                            ptx::mma_tmem_a(d, at + 32u * h + 8u * k, bd + 2u * k, kIdescF16, accumulate);
-                            accumulate = 1;
+                            for (int k = 0; k < kTcBK / 16; ++k) {
+                                ptx::mma_tmem_a(d, at + 32u * h + 8u * k, bd + 2u * k, kIdescF16, acc_flag);
+                                acc_flag = 1;
+                            }
                         }
+                        ptx::mma_commit(ptx::smem_u32(&c.empty[stage]));  // the code slot (codes, scales, rows)
+                        // the A buffer, for the dequant set that writes it next
+                        ptx::mma_commit(ptx::smem_u32(&c.dq_empty[(gs + kF8Dq) & 1][dq]));
                     }
-                    ptx::mma_commit(ptx::smem_u32(&c.empty[stage]));  // the code slot (codes, scales, rows)
-                    // the A buffer, for the dequant set that writes it next
-                    ptx::mma_commit(ptx::smem_u32(&c.dq_empty[(gs + kF8Dq) & 1][dq]));
+                    __syncwarp();
+                    accumulate = 1;
                 }
                 ++gs;
                 if (++stage == kSt) stage = 0;
                 if (++dq == kF8Dq) dq = 0;
             }
-            if (ok) ptx::mma_commit(ptx::smem_u32(&c.tfull[acc]));
+            if (ok && issuer) ptx::mma_commit(ptx::smem_u32(&c.tfull[acc]));
+            __syncwarp();
         }
-        if (!ok) fail(c, a0.err);
-        uint64_t* dr = j ? &c.drain2 : &c.drain;
-        ptx::mma_commit(ptx::smem_u32(dr));
-        ptx::mbar_wait(ptx::smem_u32(dr), 0, a0.limit_ns, nullptr);
+        if (issuer) {
+            if (!ok) fail(c, a0.err);
+            uint64_t* dr = j ? &c.drain2 : &c.drain;
+            ptx::mma_commit(ptx::smem_u32(dr));
+            ptx::mbar_wait(ptx::smem_u32(dr), 0, a0.limit_ns, nullptr);
+        }
+        __syncwarp();
     } else if (F8 && warp >= 8) {
         // ------------------------------------------------ MXFP8 dequant
         // warp 8 + 4 j + q owns TMEM lanes 32 q .. 32 q + 31 (weight rows, one
