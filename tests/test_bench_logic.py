@@ -113,3 +113,11 @@ def test_kernel_source_lists_cover_everything_their_kernels_include():
 def test_one_process_throughput_is_tokens_over_time():
     ms, tps = bench.job_throughput(1, 8, 10, 1.5)
     assert ms == 1.5 and tps == pytest.approx(8 * 10 / 1.5e-3)
+
+
+def test_run_layer_cli_parses_without_a_gpu():
+    import subprocess
+    import sys
+    out = subprocess.run([sys.executable, "-m", "mixture_experts_layer_warp_gb300.run_layer", "--help"],
+                         capture_output=True, text=True, cwd=bench.ROOT, timeout=120)
+    assert out.returncode == 0 and "--tokens" in out.stdout and "mxfp8" in out.stdout
