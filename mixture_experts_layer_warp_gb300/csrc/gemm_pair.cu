@@ -11,8 +11,9 @@
 // held by each CTA), so each CTA stages 16 KB of weights and at most 16 KB of
 // token rows per 64-deep K stage: half the operand bytes per SM of a one-SM
 // 128 x 256 tile for the same tensor-core work. Tokens on N let a group's
-// rows be cut into chunks of at most 256 padded to a multiple of 32 (a group
-// of c routes costs ceil(c / 32) * 32 columns, not ceil(c / 128) * 128 rows).
+// rows be cut into chunks of at most 256 padded to a multiple of 16 (a group
+// of c routes costs about c columns, not ceil(c / 128) * 128 rows; M = 256
+// pair MMAs take any N that is a multiple of 16 up to 256).
 //
 //   SwiGLU (GEMM1): a tile is (micro m, expert e, 128 features f*128.., one
 //       chunk of e's routes). CTA r holds features f*128 + r*64 + [0, 64) as
@@ -80,7 +81,7 @@ struct PairTile {
     int m, g, f;
     int start;  // first route row of the chunk
     int len;    // routes in the chunk (<= kChunk)
-    int n;      // MMA N: len rounded up to a multiple of 32
+    int n;      // MMA N: len rounded up to a multiple of 16 (each CTA holds n/2 rows, whole 8-row atoms)
 };
 
 // Chunks of one group: ceil(rows / kChunk) of near-equal length, so no chunk
@@ -111,7 +112,7 @@ __device__ __forceinline__ PairTile decode_pair_tile(int tile, const Ctl& c, con
     const int base = rows / C, rem = rows % C;
     t.start = c.seg[lo] + ch * base + min(ch, rem);
     t.len = base + (ch < rem ? 1 : 0);
-    t.n = (t.len + 31) & ~31;
+    t.n = (t.len + 15) & ~15;
     return t;
 }
 

@@ -201,7 +201,7 @@ struct TcGemmArgs {
 };
 // Grouped GEMMs on CTA pairs (gemm_pair.cu): weights on the MMA's M side (256
 // rows over the pair), the routes of a group on N in chunks of at most 256,
-// padded to a multiple of 32.
+// padded to a multiple of 16.
 //   SwiGLU form (GEMM1): out[r][m*I + n] = silu(x_r . W_m[g][n]) * (x_r . W_m[g][I + n])
 //   Plain form (GEMM2):  out[r][n] = sum_m x_r[m*I:(m+1)*I] . W_m[g][n]
 struct PairGemmArgs {
