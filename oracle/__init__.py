@@ -10,6 +10,7 @@ from .oracle import (  # noqa: F401
     load_variant,
     forward_permuted,
     forward_tokens,
+    forward_tokens_mx,
     layer,
     logits,
     mx_dequant,

@@ -78,6 +78,8 @@ static const void *elem_ptr(const void *p, int dtype, int64_t i)
 
 static double silu(double z) { return z / (1.0 + exp(-z)); }
 
+static void mx_round_vec(double *v, int64_t n);
+
 static int max_threads(void)
 {
 #ifdef _OPENMP
@@ -232,11 +234,13 @@ int orc_permute(const int32_t *ids, int64_t T, int64_t k, int64_t E,
  *     u_i = sum_h w13[I+i][h] * x[h]
  *     a_i = silu(g_i) * u_i,   silu(z) = z / (1 + exp(-z))
  *     acc[h] += scale * sum_i w2[h][i] * a_i
- * w13 is [2I][H], w2 is [H][I]; a is caller scratch of length I.
+ * w13 is [2I][H], w2 is [H][I]; a is caller scratch of length I. With mx_act
+ * set, a is replaced by its MXFP8 value (blocks of 32 along I) before the
+ * down projection: the activation input of a block-scaled FP8 GEMM2.
  */
 static void swiglu_expert_acc(const double *xv, int64_t H, int64_t I,
                               const void *w13, const void *w2, int dtype,
-                              double scale, double *acc, double *a)
+                              double scale, double *acc, double *a, int mx_act)
 {
     for (int64_t i = 0; i < I; ++i) {
         double g = 0.0, u = 0.0;
@@ -246,6 +250,8 @@ static void swiglu_expert_acc(const double *xv, int64_t H, int64_t I,
         }
         a[i] = silu(g) * u;
     }
+    if (mx_act)
+        mx_round_vec(a, I);
     for (int64_t h = 0; h < H; ++h) {
         double s = 0.0;
         for (int64_t i = 0; i < I; ++i)
@@ -269,13 +275,15 @@ int orc_forward_tokens_typed(const void *x, int dtype, int w_dtype, int s_dtype,
                              const void *const *w13, const void *const *w2,
                              const void *sw13, const void *sw2, int64_t Is,
                              const int32_t *ids, const double *w,
-                             const int64_t *tokens, int64_t n_tokens, double *y)
+                             const int64_t *tokens, int64_t n_tokens, double *y, int mx_act)
 {
     if (H <= 0 || E <= 0 || k <= 0 || I <= 0 || n_micro <= 0 || n_tokens < 0)
         return -1;
+    if (mx_act && (H % 32 != 0 || I % 32 != 0))
+        return -1;
     int nt = max_threads();
     int64_t scratch = I > Is ? I : Is;
-    double *xbuf = (double *)malloc(sizeof(double) * (size_t)(H * nt));
+    double *xbuf = (double *)malloc(sizeof(double) * (size_t)(2 * H * nt));
     double *abuf = (double *)malloc(sizeof(double) * (size_t)(scratch * nt));
     if (!xbuf || !abuf) {
         free(xbuf);
@@ -284,24 +292,28 @@ int orc_forward_tokens_typed(const void *x, int dtype, int w_dtype, int s_dtype,
     }
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t n = 0; n < n_tokens; ++n) {
-        double *xv = xbuf + (int64_t)thread_id() * H;
+        double *xv = xbuf + (int64_t)thread_id() * 2 * H;
+        double *xq = xv + H;  /* the routed experts' input: x, or its MXFP8 value */
         double *a = abuf + (int64_t)thread_id() * scratch;
         int64_t t = tokens[n];
         double *acc = y + n * H;
         for (int64_t h = 0; h < H; ++h) {
             xv[h] = elem(x, dtype, t * H + h);
+            xq[h] = xv[h];
             acc[h] = 0.0;
         }
+        if (mx_act)
+            mx_round_vec(xq, H);
         for (int64_t j = 0; j < k; ++j) {
             int64_t e = ids[t * k + j];
             for (int64_t m = 0; m < n_micro; ++m)
-                swiglu_expert_acc(xv, H, I,
+                swiglu_expert_acc(xq, H, I,
                                   elem_ptr(w13[m], w_dtype, e * 2 * I * H),
                                   elem_ptr(w2[m], w_dtype, e * H * I),
-                                  w_dtype, w[t * k + j], acc, a);
+                                  w_dtype, w[t * k + j], acc, a, mx_act);
         }
         if (sw13 && sw2 && Is > 0)
-            swiglu_expert_acc(xv, H, Is, sw13, sw2, s_dtype, 1.0, acc, a);
+            swiglu_expert_acc(xv, H, Is, sw13, sw2, s_dtype, 1.0, acc, a, 0);
     }
     free(xbuf);
     free(abuf);
@@ -317,7 +329,7 @@ int orc_forward_tokens(const void *x, int dtype, int64_t H, int64_t E, int64_t k
                        const int64_t *tokens, int64_t n_tokens, double *y)
 {
     return orc_forward_tokens_typed(x, dtype, dtype, dtype, H, E, k, I, n_micro, w13, w2, sw13, sw2,
-                                    Is, ids, w, tokens, n_tokens, y);
+                                    Is, ids, w, tokens, n_tokens, y, 0);
 }
 
 /*
@@ -367,7 +379,7 @@ int orc_forward_permuted(const void *x, int dtype, int64_t T, int64_t H, int64_t
                 swiglu_expert_acc(xp + i * H, H, I,
                                   elem_ptr(w13[m], dtype, e * 2 * I * H),
                                   elem_ptr(w2[m], dtype, e * H * I),
-                                  dtype, 1.0, o + i * H, a);
+                                  dtype, 1.0, o + i * H, a, 0);
         }
     }
     /* finalize: routing scale applied once, top-k reduced once */
@@ -386,7 +398,7 @@ int orc_forward_permuted(const void *x, int dtype, int64_t T, int64_t H, int64_t
         if (sw13 && sw2 && Is > 0) {
             for (int64_t h = 0; h < H; ++h)
                 xv[h] = elem(x, dtype, t * H + h);
-            swiglu_expert_acc(xv, H, Is, sw13, sw2, dtype, 1.0, acc, a);
+            swiglu_expert_acc(xv, H, Is, sw13, sw2, dtype, 1.0, acc, a, 0);
         }
     }
 done:
@@ -441,6 +453,37 @@ static uint8_t e4m3_round_mag(double u)
     }
     int code = ((e + 7) << 3) | (int)(qi - 8);
     return code > 0x7E ? 0x7E : (uint8_t)code;
+}
+
+/*
+ * The MXFP8 value of a vector v[0..n) (n % 32 == 0), in place: each block of
+ * 32 consecutive elements takes the shared exponent floor(log2(max |v|)) - 8
+ * (clamped to [-127, 127]; 0 for an all-zero block) and every element becomes
+ * its E4M3 code (nearest, ties to even, saturating at 448) times 2^shared --
+ * the same rule as orc_mx_quantize, applied to activations.
+ */
+static void mx_round_vec(double *v, int64_t n)
+{
+    for (int64_t b = 0; b < n; b += 32) {
+        double amax = 0.0;
+        for (int i = 0; i < 32; ++i)
+            if (fabs(v[b + i]) > amax)
+                amax = fabs(v[b + i]);
+        int shared = 0;
+        if (amax > 0.0) {
+            int ex;
+            frexp(amax, &ex);
+            shared = (ex - 1) - 8;
+            if (shared < -127)
+                shared = -127;
+            if (shared > 127)
+                shared = 127;
+        }
+        for (int i = 0; i < 32; ++i) {
+            double q = ldexp(e4m3_value(e4m3_round_mag(ldexp(fabs(v[b + i]), -shared))), shared);
+            v[b + i] = signbit(v[b + i]) ? -q : q;
+        }
+    }
 }
 
 /*

@@ -49,7 +49,7 @@ def _bind(path: str):
         _p, _p, _p, _i64, _p]
     lib.orc_forward_tokens_typed.argtypes = [
         _p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _i64, _i64, _i64, _i64, _i64, _p, _p, _p, _p,
-        _i64, _p, _p, _p, _i64, _p]
+        _i64, _p, _p, _p, _i64, _p, ctypes.c_int]
     lib.orc_mx_quantize.argtypes = [_p, ctypes.c_int, _i64, _i64, _i64, _p, _p]
     lib.orc_mx_dequant.argtypes = [_p, _p, _i64, _i64, _i64, _p]
     lib.orc_forward_permuted.argtypes = [
@@ -183,7 +183,7 @@ def _shared(sw13, sw2, H, dt):
     return sw13, sw2, Is
 
 
-def forward_tokens(x, ids, w, w13, w2, tokens=None, shared_w13=None, shared_w2=None, lib=None):
+def forward_tokens(x, ids, w, w13, w2, tokens=None, shared_w13=None, shared_w2=None, lib=None, mx_act=False):
     """Per-token definition ``y[t] = sum_j w_tj sum_m FFN_{m,e_j}(x_t) (+ shared)``.
 
     ``tokens`` selects rows to evaluate (default: all). Returns fp64 [n, H].
@@ -202,10 +202,20 @@ def forward_tokens(x, ids, w, w13, w2, tokens=None, shared_w13=None, shared_w2=N
     y = np.empty((tok.size, H), np.float64)
     rc = (lib or _load()).orc_forward_tokens_typed(
         _ptr(x), dt, wdt, dt, H, E, k, I, n_micro, p13, p2, _ptr(sw13), _ptr(sw2), Is,
-        _ptr(ids), _ptr(w), _ptr(tok), tok.size, _ptr(y))
+        _ptr(ids), _ptr(w), _ptr(tok), tok.size, _ptr(y), 1 if mx_act else 0)
     if rc:
         raise RuntimeError(f"orc_forward_tokens failed ({rc})")
     return y
+
+
+def forward_tokens_mx(x, ids, w, w13, w2, tokens=None, shared_w13=None, shared_w2=None, lib=None):
+    """The layer with block-scaled FP8 arithmetic in the routed experts: as
+    ``forward_tokens`` (``w13``/``w2`` typically the exact values of MXFP8
+    weights, fp64), with each token's input to the routed experts replaced by
+    its MXFP8 value (blocks of 32 along H) and each expert's SwiGLU output by
+    its MXFP8 value (blocks of 32 along I) before the down projection. The
+    shared expert takes the unquantised input."""
+    return forward_tokens(x, ids, w, w13, w2, tokens, shared_w13, shared_w2, lib=lib, mx_act=True)
 
 
 def forward_permuted(x, w, offsets, perm, inv, w13, w2, shared_w13=None, shared_w2=None,

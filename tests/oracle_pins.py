@@ -401,6 +401,59 @@ def pin_mx_roundtrip_error_bound(lib=None):
     assert np.array_equal(np.abs(deq[sat]), 448.0 * unit[sat])
 
 
+def _mx_value_torch(v):
+    """MXFP8 value of v along its last axis (blocks of 32) from library
+    routines: numpy frexp for the shared exponent, torch's float8_e4m3fn cast
+    (nearest, ties to even) for the code, saturated at 448."""
+    import torch
+    v = np.asarray(v, np.float64)
+    b = v.reshape(-1, 32)
+    amax = np.abs(b).max(axis=1)
+    _, ex = np.frexp(np.where(amax > 0, amax, 1.0))
+    shared = np.clip(np.where(amax > 0, ex - 1 - 8, 0), -127, 127)[:, None]
+    u = np.minimum(np.abs(b) * np.ldexp(1.0, -shared), 448.0)
+    q = torch.tensor(u).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    return (np.sign(b) * q * np.ldexp(1.0, shared)).reshape(v.shape)
+
+
+def pin_mx_activation_forward_matches_library_rounding(lib=None):
+    """forward_tokens_mx: each token's routed input replaced by its MXFP8 value
+    along H, each expert's SwiGLU output by its MXFP8 value along I (per micro),
+    the shared expert on the unrounded input; checked against the same layer
+    built from library routines (torch's E4M3 cast for every rounding)."""
+    rng = np.random.default_rng(21)
+    T, H, E, k, I, M, Is = 5, 64, 3, 2, 64, 2, 32
+    x = _f32(rng.normal(0, 1.0, (T, H))).astype(np.float32)
+    w13 = [rng.normal(0, 0.2, (E, 2 * I, H)) for _ in range(M)]
+    w2 = [rng.normal(0, 0.2, (E, H, I)) for _ in range(M)]
+    sw13 = _f32(rng.normal(0, 0.2, (2 * Is, H))).astype(np.float32)
+    sw2 = _f32(rng.normal(0, 0.2, (H, Is))).astype(np.float32)
+    ids = np.array([[0, 2], [1, 0], [2, 1], [0, 1], [2, 0]], np.int32)
+    w = rng.uniform(0.2, 0.8, (T, k))
+    got = oracle.forward_tokens_mx(x, ids, w, w13, w2, None, sw13, sw2, lib=lib)
+    silu = lambda z: z / (1.0 + np.exp(-z))  # noqa: E731
+    xs = x.astype(np.float64)
+    want = np.zeros((T, H))
+    for t in range(T):
+        xq = _mx_value_torch(xs[t])
+        for j in range(k):
+            e = ids[t, j]
+            for m in range(M):
+                g = w13[m][e, :I] @ xq
+                u = w13[m][e, I:] @ xq
+                want[t] += w[t, j] * (w2[m][e] @ _mx_value_torch(silu(g) * u))
+        gs = sw13[:Is].astype(np.float64) @ xs[t]
+        us = sw13[Is:].astype(np.float64) @ xs[t]
+        want[t] += sw2.astype(np.float64) @ (silu(gs) * us)
+    assert np.allclose(got, want, rtol=1e-12, atol=1e-12 * np.abs(want).max()), "MX activation forward differs"
+    # rounding to MX values is idempotent: inputs already on the grid are unchanged
+    xg = _mx_value_torch(xs).astype(np.float32)
+    assert np.array_equal(_mx_value_torch(xg.astype(np.float64)), xg.astype(np.float64))
+    plain = oracle.forward_tokens(xg, ids, w, w13, w2, None, None, None, lib=lib)
+    mxv = oracle.forward_tokens_mx(xg, ids, w, w13, w2, None, None, None, lib=lib)
+    assert not np.allclose(plain, mxv, rtol=1e-6), "the SwiGLU outputs must be rounded too"
+
+
 def pin_forward_accepts_fp64_weights(lib=None):
     """The fp64 weight path (used with dequantised weights) equals the fp32 path
     on the same values."""

@@ -28,13 +28,15 @@ MUTANTS = [
     ("unstable_route_sort", "for (int64_t r = 0; r < R; ++r)\n        perm[fill[ids[r]]++] = (int32_t)r;",
      "for (int64_t r = R - 1; r >= 0; --r)\n        perm[fill[ids[r]]++] = (int32_t)r;"),
     ("inverse_not_inverted", "inv[perm[i]] = (int32_t)i;", "inv[i] = perm[i];"),
-    ("one_micro_only", "for (int64_t m = 0; m < n_micro; ++m)\n                swiglu_expert_acc(xv,",
-     "for (int64_t m = 0; m < 1; ++m)\n                swiglu_expert_acc(xv,"),
+    ("one_micro_only", "for (int64_t m = 0; m < n_micro; ++m)\n                swiglu_expert_acc(xq,",
+     "for (int64_t m = 0; m < 1; ++m)\n                swiglu_expert_acc(xq,"),
     ("gather_wrong_token", "int64_t t = perm[i] / k;", "int64_t t = perm[i] % (k + 1);"),
-    ("shared_scaled", "swiglu_expert_acc(xv, H, Is, sw13, sw2, s_dtype, 1.0, acc, a);\n    }\n    free(xbuf);",
-     "swiglu_expert_acc(xv, H, Is, sw13, sw2, s_dtype, 0.5, acc, a);\n    }\n    free(xbuf);"),
+    ("shared_scaled", "swiglu_expert_acc(xv, H, Is, sw13, sw2, s_dtype, 1.0, acc, a, 0);",
+     "swiglu_expert_acc(xv, H, Is, sw13, sw2, s_dtype, 0.5, acc, a, 0);"),
     ("perm_holds_token", "perm[fill[ids[r]]++] = (int32_t)r;", "perm[fill[ids[r]]++] = (int32_t)(r / k);"),
-    ("mx_scale_from_ceil", "shared = (ex - 1) - 8;", "shared = ex - 8;"),
+    ("mx_scale_from_ceil", "                shared = (ex - 1) - 8;", "                shared = ex - 8;"),
+    ("mx_act_scale_from_ceil", "            shared = (ex - 1) - 8;\n            if (shared < -127)\n                shared = -127;\n            if (shared > 127)\n                shared = 127;\n        }\n        for (int i = 0; i < 32; ++i) {",
+     "            shared = ex - 8;\n            if (shared < -127)\n                shared = -127;\n            if (shared > 127)\n                shared = 127;\n        }\n        for (int i = 0; i < 32; ++i) {"),
     ("mx_ties_away_from_zero", "double q = nearbyint(scaled);", "double q = round(scaled);"),
     ("mx_scale_layout_row_major", "scales[(g * nb + b) * rows + r] = (uint8_t)(shared + 127);",
      "scales[(g * rows + r) * nb + b] = (uint8_t)(shared + 127);"),
@@ -42,7 +44,13 @@ MUTANTS = [
      "ldexp(e4m3_value(codes[gr * cols + c]), S - 126);"),
     ("mx_dequant_scale_of_wrong_block", "int S = scales[(g * nb + c / 32) * rows + r];",
      "int S = scales[(g * nb + c / 64) * rows + r];"),
-    ("fp64_weights_read_as_shared_dtype", "w_dtype, w[t * k + j], acc, a);", "dtype, w[t * k + j], acc, a);"),
+    ("fp64_weights_read_as_shared_dtype", "w_dtype, w[t * k + j], acc, a, mx_act);",
+     "dtype, w[t * k + j], acc, a, mx_act);"),
+    ("mx_act_h_not_rounded", "    if (mx_act)\n        mx_round_vec(a, I);", "    if (0)\n        mx_round_vec(a, I);"),
+    ("mx_act_x_not_rounded", "        if (mx_act)\n            mx_round_vec(xq, H);",
+     "        if (0)\n            mx_round_vec(xq, H);"),
+    ("mx_act_block_of_16", "    for (int64_t b = 0; b < n; b += 32) {\n        double amax = 0.0;\n        for (int i = 0; i < 32; ++i)",
+     "    for (int64_t b = 0; b < n; b += 16) {\n        double amax = 0.0;\n        for (int i = 0; i < 16; ++i)"),
 ]
 
 
