@@ -6,6 +6,7 @@ benchmark's CPU-baseline leg (``bench.py`` ``cpu_baseline`` and
 and shares no code with it.
 """
 from .oracle import (  # noqa: F401
+    bf16_round,
     build,
     load_variant,
     forward_permuted,

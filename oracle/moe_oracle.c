@@ -79,6 +79,7 @@ static const void *elem_ptr(const void *p, int dtype, int64_t i)
 static double silu(double z) { return z / (1.0 + exp(-z)); }
 
 static void mx_round_vec(double *v, int64_t n);
+static double bf16_round(double v);
 
 static int max_threads(void)
 {
@@ -235,8 +236,10 @@ int orc_permute(const int32_t *ids, int64_t T, int64_t k, int64_t E,
  *     a_i = silu(g_i) * u_i,   silu(z) = z / (1 + exp(-z))
  *     acc[h] += scale * sum_i w2[h][i] * a_i
  * w13 is [2I][H], w2 is [H][I]; a is caller scratch of length I. With mx_act
- * set, a is replaced by its MXFP8 value (blocks of 32 along I) before the
- * down projection: the activation input of a block-scaled FP8 GEMM2.
+ * set, a is the layer's bf16 activation (each a_i rounded to bf16, nearest,
+ * ties to even: the precision h is stored in between the GEMMs) and is
+ * replaced by its MXFP8 value (blocks of 32 along I) before the down
+ * projection: the activation input of a block-scaled FP8 GEMM2.
  */
 static void swiglu_expert_acc(const double *xv, int64_t H, int64_t I,
                               const void *w13, const void *w2, int dtype,
@@ -250,8 +253,11 @@ static void swiglu_expert_acc(const double *xv, int64_t H, int64_t I,
         }
         a[i] = silu(g) * u;
     }
-    if (mx_act)
+    if (mx_act) {
+        for (int64_t i = 0; i < I; ++i)
+            a[i] = bf16_round(a[i]);
         mx_round_vec(a, I);
+    }
     for (int64_t h = 0; h < H; ++h) {
         double s = 0.0;
         for (int64_t i = 0; i < I; ++i)
@@ -453,6 +459,41 @@ static uint8_t e4m3_round_mag(double u)
     }
     int code = ((e + 7) << 3) | (int)(qi - 8);
     return code > 0x7E ? 0x7E : (uint8_t)code;
+}
+
+/*
+ * v rounded to bfloat16 (1 sign, 8 exponent and 7 fraction bits: 8 significant
+ * bits, smallest normal 2^-126, subnormal steps of 2^-133, largest finite
+ * (2 - 2^-7) * 2^127), nearest with ties to even; beyond the largest finite
+ * value after rounding: infinity. Exact in fp64: scaling by powers of two.
+ */
+static double bf16_round(double v)
+{
+    double u = fabs(v);
+    if (u == 0.0 || isnan(u) || isinf(u))
+        return v;
+    int e;
+    if (u < ldexp(1.0, -126)) {
+        e = -126;  /* subnormal: the step of the smallest normal binade */
+    } else {
+        int ex;
+        frexp(u, &ex);  /* u = f * 2^ex, f in [0.5, 1) */
+        e = ex - 1;
+    }
+    double q = ldexp(nearbyint(ldexp(u, 7 - e)), e - 7);  /* 128 steps per binade; 256 carries into the next */
+    if (q > ldexp(255.0, 120))  /* (2 - 2^-7) * 2^127 */
+        q = INFINITY;
+    return signbit(v) ? -q : q;
+}
+
+/* bf16_round of n values (for tests of the rounding rule). */
+int orc_bf16_round(const double *v, int64_t n, double *out)
+{
+    if (n < 0)
+        return -1;
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = bf16_round(v[i]);
+    return 0;
 }
 
 /*

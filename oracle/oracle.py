@@ -52,13 +52,15 @@ def _bind(path: str):
         _i64, _p, _p, _p, _i64, _p, ctypes.c_int]
     lib.orc_mx_quantize.argtypes = [_p, ctypes.c_int, _i64, _i64, _i64, _p, _p]
     lib.orc_mx_dequant.argtypes = [_p, _p, _i64, _i64, _i64, _p]
+    lib.orc_bf16_round.argtypes = [_p, _i64, _p]
     lib.orc_forward_permuted.argtypes = [
         _p, ctypes.c_int, _i64, _i64, _i64, _i64, _i64, _i64, _p, _p, _p, _p, _i64,
         _p, _p, _p, _p, _p]
     lib.orc_num_threads.argtypes = []
     lib.orc_set_threads.argtypes = [ctypes.c_int]
     for fn in ("orc_logits", "orc_route", "orc_permute", "orc_forward_tokens", "orc_forward_tokens_typed",
-               "orc_forward_permuted", "orc_num_threads", "orc_set_threads", "orc_mx_quantize", "orc_mx_dequant"):
+               "orc_forward_permuted", "orc_num_threads", "orc_set_threads", "orc_mx_quantize", "orc_mx_dequant",
+               "orc_bf16_round"):
         getattr(lib, fn).restype = ctypes.c_int
     return lib
 
@@ -212,9 +214,10 @@ def forward_tokens_mx(x, ids, w, w13, w2, tokens=None, shared_w13=None, shared_w
     """The layer with block-scaled FP8 arithmetic in the routed experts: as
     ``forward_tokens`` (``w13``/``w2`` typically the exact values of MXFP8
     weights, fp64), with each token's input to the routed experts replaced by
-    its MXFP8 value (blocks of 32 along H) and each expert's SwiGLU output by
-    its MXFP8 value (blocks of 32 along I) before the down projection. The
-    shared expert takes the unquantised input."""
+    its MXFP8 value (blocks of 32 along H) and each expert's SwiGLU output,
+    rounded to bf16 (the layer's activation dtype), by its MXFP8 value (blocks
+    of 32 along I) before the down projection. The shared expert takes the
+    unquantised input."""
     return forward_tokens(x, ids, w, w13, w2, tokens, shared_w13, shared_w2, lib=lib, mx_act=True)
 
 
@@ -286,3 +289,13 @@ def mx_dequant(codes: np.ndarray, scales: np.ndarray, lib=None) -> np.ndarray:
     if rc:
         raise RuntimeError(f"orc_mx_dequant failed ({rc})")
     return out[0] if two_d else out
+
+
+def bf16_round(v, lib=None) -> np.ndarray:
+    """fp64 values rounded to bfloat16 (nearest, ties to even), as fp64."""
+    v = _c(np.asarray(v, np.float64).ravel(), np.float64)
+    out = np.empty_like(v)
+    rc = (lib or _load()).orc_bf16_round(_ptr(v), v.size, _ptr(out))
+    if rc:
+        raise RuntimeError(f"orc_bf16_round failed ({rc})")
+    return out

@@ -416,11 +416,51 @@ def _mx_value_torch(v):
     return (np.sign(b) * q * np.ldexp(1.0, shared)).reshape(v.shape)
 
 
+def _bf16_value_torch(v):
+    """bf16 value of fp64 v from torch's cast. torch converts fp64 through fp32,
+    which equals the direct rounding unless the fp32 value is itself a bf16
+    tie (low 16 bits 0x8000); the caller's values are checked to hold none."""
+    import torch
+    v = np.asarray(v, np.float64)
+    bits = v.astype(np.float32).view(np.uint32)
+    assert not ((bits & 0xFFFF) == 0x8000).any(), "an fp32 tie: torch's cast would round twice"
+    return torch.tensor(v).to(torch.bfloat16).to(torch.float64).numpy()
+
+
+def pin_bf16_rounding(lib=None):
+    """bf16_round against the format's closed forms (8 significant bits,
+    ties to even, subnormal step 2^-133, overflow past (2 - 2^-7) 2^127) and
+    torch's cast on random values of every magnitude."""
+    t = 2.0 ** -8
+    cases = {
+        1.0 + t: 1.0,                      # a tie: to the even neighbour 1
+        1.0 + 3 * t: 1.0 + 4 * t,          # a tie: to the even neighbour 1 + 2^-6
+        1.0 + t + 2.0 ** -30: 1.0 + 2 * t,  # just past the tie (lost in fp32)
+        -(1.0 + t + 2.0 ** -30): -(1.0 + 2 * t),
+        255.5: 256.0,                      # 8 significant bits: 255.5 is a tie, 256 even
+        254.5: 254.0,
+        2.0 ** -133 * 0.5: 0.0,            # half the smallest subnormal: tie to 0
+        2.0 ** -133 * 0.75: 2.0 ** -133,
+        2.0 ** -133 * 3.5: 2.0 ** -131,     # 3.5 steps: tie to 4
+        (2.0 - 2.0 ** -7) * 2.0 ** 127: (2.0 - 2.0 ** -7) * 2.0 ** 127,
+        (2.0 - 2.0 ** -9) * 2.0 ** 127: np.inf,  # rounds up past the largest finite value
+        0.0: 0.0,
+    }
+    got = oracle.bf16_round(np.array(list(cases)), lib=lib)
+    assert np.array_equal(got, np.array(list(cases.values()))), f"bf16 closed forms: {got}"
+    rng = np.random.default_rng(5)
+    v = rng.normal(0, 1, 4000) * np.ldexp(1.0, rng.integers(-140, 120, 4000))
+    v = v[np.abs(v) >= 2.0 ** -126]
+    v = v[(v.astype(np.float32).view(np.uint32) & 0xFFFF) != 0x8000]  # where torch's cast rounds once
+    assert np.array_equal(oracle.bf16_round(v, lib=lib), _bf16_value_torch(v)), "bf16 rounding differs from torch"
+
+
 def pin_mx_activation_forward_matches_library_rounding(lib=None):
     """forward_tokens_mx: each token's routed input replaced by its MXFP8 value
-    along H, each expert's SwiGLU output by its MXFP8 value along I (per micro),
-    the shared expert on the unrounded input; checked against the same layer
-    built from library routines (torch's E4M3 cast for every rounding)."""
+    along H, each expert's SwiGLU output rounded to bf16 and then replaced by
+    its MXFP8 value along I (per micro), the shared expert on the unrounded
+    input; checked against the same layer built from library routines
+    (torch's bf16 and E4M3 casts for every rounding)."""
     rng = np.random.default_rng(21)
     T, H, E, k, I, M, Is = 5, 64, 3, 2, 64, 2, 32
     x = _f32(rng.normal(0, 1.0, (T, H))).astype(np.float32)
@@ -441,7 +481,7 @@ def pin_mx_activation_forward_matches_library_rounding(lib=None):
             for m in range(M):
                 g = w13[m][e, :I] @ xq
                 u = w13[m][e, I:] @ xq
-                want[t] += w[t, j] * (w2[m][e] @ _mx_value_torch(silu(g) * u))
+                want[t] += w[t, j] * (w2[m][e] @ _mx_value_torch(_bf16_value_torch(silu(g) * u)))
         gs = sw13[:Is].astype(np.float64) @ xs[t]
         us = sw13[Is:].astype(np.float64) @ xs[t]
         want[t] += sw2.astype(np.float64) @ (silu(gs) * us)

@@ -46,7 +46,12 @@ MUTANTS = [
      "int S = scales[(g * nb + c / 64) * rows + r];"),
     ("fp64_weights_read_as_shared_dtype", "w_dtype, w[t * k + j], acc, a, mx_act);",
      "dtype, w[t * k + j], acc, a, mx_act);"),
-    ("mx_act_h_not_rounded", "    if (mx_act)\n        mx_round_vec(a, I);", "    if (0)\n        mx_round_vec(a, I);"),
+    ("mx_act_h_not_rounded", "            a[i] = bf16_round(a[i]);\n        mx_round_vec(a, I);",
+     "            a[i] = bf16_round(a[i]);\n        (void)0;"),
+    ("mx_act_h_not_bf16", "            a[i] = bf16_round(a[i]);", "            a[i] = a[i];"),
+    ("bf16_ties_away", "double q = ldexp(nearbyint(ldexp(u, 7 - e)), e - 7);",
+     "double q = ldexp(round(ldexp(u, 7 - e)), e - 7);"),
+    ("bf16_six_fraction_bits", "ldexp(nearbyint(ldexp(u, 7 - e)), e - 7)", "ldexp(nearbyint(ldexp(u, 6 - e)), e - 6)"),
     ("mx_act_x_not_rounded", "        if (mx_act)\n            mx_round_vec(xq, H);",
      "        if (0)\n            mx_round_vec(xq, H);"),
     ("mx_act_block_of_16", "    for (int64_t b = 0; b < n; b += 32) {\n        double amax = 0.0;\n        for (int i = 0; i < 32; ++i)",
