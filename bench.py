@@ -48,8 +48,10 @@ POOL = 8  # distinct token batches rotated through the timed steps
 HEADLINE = "cfg_shared"
 # the other configurations, measured in the same run ("decode_mxfp8": the
 # decode workload with MXFP8 expert weights)
-SUB_WORKLOADS = ("decode", "decode_mxfp8", "denoise_multi_micro", "skewed", "tiny_fp32")
+SUB_WORKLOADS = ("decode", "decode_mxfp8", "denoise_multi_micro", "denoise_multi_micro_mxfp8", "skewed",
+                 "tiny_fp32")
 FP32_LANES_PER_SM = 128  # FP32 FMA units per SM (one FMA = 2 flop per clock)
+FP8_PER_BF16 = 2.0  # nominal dense tensor-core rate of fp8 over bf16 (4.5 / 2.25 PFLOP/s)
 
 
 def load_peaks():
@@ -311,6 +313,8 @@ def config_of(wl, mx=False):
                     "seeded batches"
     if mx:
         cfg["weights"] = "mxfp8 (E4M3 codes, E8M0 scale per 32 along K)"
+        if wl.T > 16:
+            cfg["activations"] = "mxfp8 token rows and h (block-scaled FP8 MMA, fp32 accumulate)"
     return cfg
 
 
@@ -359,12 +363,16 @@ def roofline_of(wl, prof, ids_pool, steps, peaks, step_ms, clocks, mxfp8=False):
         achieved = algo / per_launch_s / 1e9 if algo else None
         peak_kind = "measured copy bandwidth"
     else:
-        bound, unit, peak = "tensor", "TFLOP/s", peaks["bf16"]
+        # block-scaled FP8 GEMMs: the bf16 peaks times the nominal fp8 : bf16
+        # dense tensor ratio (4.5 : 2.25 PFLOP/s)
+        ratio = FP8_PER_BF16 if mxfp8 else 1.0
+        bound, unit, peak = "tensor", "TFLOP/s", peaks["bf16"] * ratio
         algo = flops.get(dom)
         achieved = algo / per_launch_s / 1e12 if algo else None
-        peak_kind = "burst (measured cuBLAS bf16 GEMM)"
+        peak_kind = ("fp8: measured cuBLAS bf16 burst x 2 (nominal fp8:bf16 dense ratio)" if mxfp8
+                     else "burst (measured cuBLAS bf16 GEMM)")
         if achieved:
-            extra["frac_sustained"] = achieved / peaks["bf16_sustained"]
+            extra["frac_sustained"] = achieved / (peaks["bf16_sustained"] * ratio)
         # every GEMM launch of the step together: their flops over their summed time
         g_ms = sum(prof[s][0] for s in flops if s in prof)
         g_fl = sum(flops[s] * prof[s][1] for s in flops if s in prof)
@@ -549,7 +557,8 @@ def measure(args, wl, world, rank, local, peaks, mx=False, cpu_seconds=12.0, two
     layer.close()
     rec = {"value": value, "unit": "tokens/s", "ms_per_step": ms / args.steps, "steps": args.steps,
            "warmup": args.warmup,
-           "dtype": "f16 (mxfp8 expert weights)" if mx else wl.dtype,
+           "dtype": ("e4m3 (mxfp8 weights and activations)" if wl.T > 16 else "f16 (mxfp8 expert weights)")
+           if mx else wl.dtype,
            "config": dict(config_of(wl, mx), **({"shared_stream": True} if args.shared_stream else {})),
            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
            "kernels_ms_per_step": {k: v[0] / args.steps for k, v in prof.items()},
@@ -620,7 +629,7 @@ def main():
     ap.add_argument("--sub-cpu-seconds", type=float, default=4.0,
                     help="CPU-oracle sample length of each record under 'workloads'")
     ap.add_argument("--weights", choices=["bf16", "mxfp8"], default="bf16",
-                    help="routed expert weights: the layer dtype, or MXFP8 (moe_forward_mxfp8, T <= 16)")
+                    help="routed expert weights: the layer dtype, or MXFP8 (moe_forward_mxfp8)")
     ap.add_argument("--shared-stream", action="store_true",
                     help="run the shared expert's GEMMs on a second stream (moe_set_shared_stream)")
     ap.add_argument("--no-two-dispatch", dest="two_dispatch", action="store_false",

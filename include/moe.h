@@ -158,10 +158,15 @@ moe_status moe_forward_host(moe_handle *h, const void *x_host, const void *route
  * model"; they fix no format). The reading taken is the OCP Microscaling
  * MXFP8 format: each expert weight is an FP8 E4M3 code (OCP E4M3FN, largest
  * 448) with one E8M0 power-of-two scale per 32 consecutive elements along K;
- * the layer computes with w = f16(code * 2^(S-127)) (nearest, ties to even).
- * The routed experts' GEMMs then take f16 operands (the gathered token rows
- * and h are rounded to f16; fp32 accumulation); the router, the shared expert
- * (its weights stay bf16) and y keep the layer's bf16.
+ * the layer computes with w = code * 2^(S-127). Batches of at most 16 tokens
+ * (whose time is the weight bytes) take f16 operands: w rounded to f16
+ * (nearest, ties to even), the gathered token rows and h rounded to f16.
+ * Larger batches (whose time is the tensor-core work) run the block-scaled
+ * FP8 MMA: the gathered token rows and h are quantised to MXFP8 by the same
+ * rule as the weights (along H and along each micro's I), and each GEMM
+ * multiplies the codes with their scales exactly. Both accumulate in fp32;
+ * the router, the shared expert (its weights stay bf16) and y keep the
+ * layer's bf16.
  *
  * Quantisation of bf16 weights w [groups][rows][cols] along cols (cols % 32
  * == 0): codes [groups][rows][cols] uint8 and scales [groups][cols/32][rows]
@@ -181,10 +186,11 @@ moe_status moe_quantize_mxfp8(const void *w, int64_t groups, int32_t rows, int32
  * moe_forward with MXFP8 routed-expert weights: w13_codes[m] / w13_scales[m]
  * and w2_codes[m] / w2_scales[m] as produced by moe_quantize_mxfp8 (device
  * pointers, 16-byte aligned). Supported for bf16 layers (whose hidden and
- * inter sizes, multiples of 256 and 128, fill its 128-deep K stages) and
- * batches of at most 16 tokens (the decode-sized calls whose time is the
- * weight bytes); larger T returns MOE_ERR_UNSUPPORTED. Other arguments,
- * ownership, the accumulate switch and errors as for moe_forward.
+ * inter sizes, multiples of 256 and 128, fill its 128-deep K stages); for
+ * T > 16 the MXFP8 copy of h must fit the workspace of the gathered token
+ * rows, n_micro * inter * 33/32 <= 2 * hidden (about), else the call returns
+ * MOE_ERR_UNSUPPORTED. Other arguments, ownership, the accumulate switch and
+ * errors as for moe_forward.
  */
 moe_status moe_forward_mxfp8(moe_handle *h, const void *x, const void *router_w,
                              const float *router_bias, const void *const *w13_codes,
@@ -233,7 +239,9 @@ const char *moe_status_string(moe_status s);
  * Diagnostics for tests: device address of a workspace buffer of the last
  * call. which: 0 = gathered input xp [T*k][H], 1 = SwiGLU output h [T*k][n_micro*I],
  * 2 = expert outputs o [T*k][H], 3 = inverse permutation [T*k] int32,
- * 4 = device error word (int32). Returns NULL for an unknown `which`.
+ * 4 = device error word (int32). Returns NULL for an unknown `which`. After a
+ * moe_forward_mxfp8 call with T > 16, region 0 holds the MXFP8 codes of h
+ * [T*k][n_micro*I] (uint8) instead of xp.
  */
 void *moe_workspace_ptr(const moe_handle *h, int32_t which);
 
@@ -243,10 +251,12 @@ void *moe_workspace_ptr(const moe_handle *h, int32_t which);
  * moe_forward_host / moe_route record an event pair around every kernel they
  * launch, on the call's stream. moe_profile_end synchronises those events and
  * writes, per kernel slot, the summed duration in milliseconds and the number
- * of launches. Slots: 0 router, 1 scan, 2 place, 3 gather, 4 GEMM1 (+SwiGLU),
- * 5 GEMM2, 6 shared-expert GEMM1, 7 shared-expert GEMM2, 8 finalize.
+ * of launches. Slots: 0 router, 1 scan, 2 place, 3 gather (with MXFP8 expert
+ * weights and T > 16: gather and MXFP8 quantisation of the token rows),
+ * 4 GEMM1 (+SwiGLU), 5 GEMM2, 6 shared-expert GEMM1, 7 shared-expert GEMM2,
+ * 8 finalize, 9 MXFP8 quantisation of h (MXFP8 expert weights, T > 16).
  */
-#define MOE_PROFILE_SLOTS 9
+#define MOE_PROFILE_SLOTS 10
 moe_status moe_profile_begin(moe_handle *h, int32_t max_calls);
 moe_status moe_profile_end(moe_handle *h, float *ms /* [MOE_PROFILE_SLOTS] */,
                            int32_t *launches /* [MOE_PROFILE_SLOTS] */);

@@ -36,7 +36,10 @@
 // one of two TMEM accumulators (2 x 256 fp32 columns), warp 2 owns the TMEM
 // allocation, warps 4-7 drain an accumulator (one TMEM lane quarter each,
 // transposed through shared memory into 16-byte stores of token rows) while
-// the next tile accumulates into the other. All waits are bounded.
+// the next tile accumulates into the other. With block-scaled FP8 operands
+// warp 3 loads the scales into a ring of their own and warps 8-11 copy them
+// into TMEM (see Cfg). All waits are bounded, and every load a CTA issues has
+// landed before it exits.
 #include <cuda_bf16.h>
 
 #include "gemm_common.cuh"
@@ -47,14 +50,43 @@ namespace moe {
 namespace {
 
 constexpr int kStages = 6;
-constexpr int kChunk = 256;                          // tokens per tile at most (MMA N)
 constexpr int kWRows = 128;                          // weight rows per CTA (MMA M = 256 per pair)
-constexpr int kABytes = kWRows * kTcBK * 2;          // 16 KB
-constexpr int kBBytes = (kChunk / 2) * kTcBK * 2;    // 16 KB: up to 128 token rows per CTA
-constexpr int kStageBytes = kABytes + kBBytes;       // 32 KB
-constexpr int kTmemCols = 2 * kChunk;                // two accumulators
-constexpr int kThreads = 256;
+constexpr int kABytes = 16384;                       // weight rows of a stage: 128 rows x 128 bytes
+constexpr int kBBytes = 16384;                       // up to 128 token rows x 128 bytes per CTA
+constexpr int kTmemCols = 512;                       // all of TMEM
 constexpr int kEpiArrivals = 8;                      // 4 epilogue warps in each CTA of the pair
+
+// bf16 operands (MX = false): 64 K per stage, chunks of up to 256 routes, two
+// 256-column accumulators. MXFP8 operands (MX = true, block-scaled FP8 MMA):
+// 128 K per stage (E4M3 codes, one byte each), chunks of up to 208 routes so
+// that two accumulators (416 columns) and six scale-factor buffers (16 columns
+// each: the weights' words at +0, the routes' at +8) fit the 512 TMEM columns;
+// 12 warps. Each stage's scales (the weights' 128 rows x 4 blocks, 512 bytes;
+// the token rows' stage-major scale words, 65 x 16 bytes from the chunk's
+// first route rounded down to 4) come through a ring of their own, loaded by
+// warp 3, so that they run ahead of the operand stages; warps 8-11 copy them
+// into a TMEM buffer as soon as the MMAs that read that buffer six stages
+// earlier have completed. (Scales that shared the operand slots could only
+// load once a slot freed, and the MMAs then waited out the load latency plus
+// the copy into TMEM on every stage.)
+template <bool MX>
+struct Cfg {
+    static constexpr int kSfBufs = 6;                 // scale-factor buffers in TMEM (MX)
+    static constexpr int kChunk = MX ? 208 : 256;     // routes per tile at most (MMA N)
+    static constexpr int kK = MX ? 128 : 64;          // K elements per stage
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kSfStages = MX ? 8 : 0;      // scale ring slots
+    static constexpr int kSfaOff = 0;                 // within a scale slot
+    static constexpr int kSfaBytes = 512;
+    static constexpr int kSfbOff = kSfaOff + kSfaBytes;
+    static constexpr int kSfbRows = 65;               // 16-byte rows: 4 routes' scale words each
+    static constexpr int kSfbBytes = kSfbRows * 16;
+    static constexpr int kSfSlotBytes = 1664;         // 128-byte multiple
+    static constexpr int kThreads = MX ? 384 : 256;
+    static constexpr int kSfCol = 2 * kChunk;         // scale-factor buffers of 16 columns: SFA at +0, SFB at +8
+};
+static_assert(Cfg<true>::kSfbOff + Cfg<true>::kSfbBytes <= Cfg<true>::kSfSlotBytes, "scale slot layout");
+static_assert(Cfg<true>::kSfCol + Cfg<true>::kSfBufs * 16 <= kTmemCols, "TMEM layout");
 
 struct Ctl {
     uint64_t full[kStages];   // leader: both CTAs' loads of a stage have landed
@@ -62,10 +94,14 @@ struct Ctl {
     uint64_t tfull[2];        // both CTAs: an accumulator is complete
     uint64_t tempty[2];       // leader: both CTAs' epilogues drained an accumulator
     uint64_t drain;           // leader: every MMA issued has completed
+    uint64_t sfs_full[8];     // MX, each CTA: this CTA's scales of a stage have landed in a ring slot
+    uint64_t sfs_empty[8];    // MX, each CTA: its 4 scale warps have read a ring slot
+    uint64_t sf_full[6];      // MX, leader: both CTAs wrote a scale-factor buffer
+    uint64_t sf_empty[6];     // MX, both CTAs: the MMAs reading a scale-factor buffer are done
     uint32_t tmem_base;
     int abort;
     int seg[kMaxExperts + 1];
-    int chunks[kMaxExperts + 1];  // prefix over groups of ceil(rows / kChunk)
+    int chunks[kMaxExperts + 1];  // prefix over groups of ceil(rows / chunk)
 };
 
 // Epilogue staging, per epilogue warp: one 32-token block of its accumulator
@@ -75,16 +111,25 @@ struct Ctl {
 constexpr int kEpiFloats = 32 * 33;
 constexpr int kEpiBytes = 4 * kEpiFloats * 4;
 
-constexpr int kSmemBytes = kStages * kStageBytes + kEpiBytes + (int)sizeof(Ctl) + 1024;
+template <bool MX>
+constexpr int smem_bytes() {
+    return kStages * Cfg<MX>::kStageBytes + Cfg<MX>::kSfStages * Cfg<MX>::kSfSlotBytes + kEpiBytes + (int)sizeof(Ctl) +
+           1024;
+}
+static_assert(smem_bytes<true>() <= 232448 && smem_bytes<false>() <= 232448, "shared memory per CTA");
 
 struct PairTile {
     int m, g, f;
     int start;  // first route row of the chunk
-    int len;    // routes in the chunk (<= kChunk)
+    int len;    // routes in the chunk (<= the chunk size)
     int n;      // MMA N: len rounded up to a multiple of 16 (each CTA holds n/2 rows, whole 8-row atoms)
 };
 
-// Chunks of one group: ceil(rows / kChunk) of near-equal length, so no chunk
+// Token-row map of a chunk: the smallest box (32, 64, 96 or 128 rows) that
+// covers the n/2 rows each CTA holds.
+__device__ __forceinline__ int token_box(const PairTile& t) { return (t.n / 2 + 31) / 32 - 1; }
+
+// Chunks of one group: ceil(rows / chunk) of near-equal length, so no chunk
 // is a nearly empty remainder (the weight bytes of a tile do not shrink with N).
 template <bool SWIGLU>
 __device__ __forceinline__ PairTile decode_pair_tile(int tile, const Ctl& c, const PairGemmArgs& a) {
@@ -130,20 +175,27 @@ __device__ __forceinline__ void settle_inflight_copies() {
     }
 }
 
-template <bool SWIGLU>
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool SWIGLU, bool MX>
+__global__ void __launch_bounds__(Cfg<MX>::kThreads, 1)
     pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant__ CUtensorMap tmW1,
                      const __grid_constant__ CUtensorMap tmW2, const __grid_constant__ CUtensorMap tmW3,
                      const __grid_constant__ CUtensorMap tmX0, const __grid_constant__ CUtensorMap tmX1,
                      const __grid_constant__ CUtensorMap tmX2, const __grid_constant__ CUtensorMap tmX3,
-                     const PairGemmArgs a) {
+                     const __grid_constant__ CUtensorMap tmSA0, const __grid_constant__ CUtensorMap tmSA1,
+                     const __grid_constant__ CUtensorMap tmSA2, const __grid_constant__ CUtensorMap tmSA3,
+                     const __grid_constant__ CUtensorMap tmSB, const PairGemmArgs a) {
+    using C = Cfg<MX>;
+    constexpr int kChunk = C::kChunk;
+    constexpr int kStageBytes = C::kStageBytes;
+    constexpr int kThreads = C::kThreads;
     extern __shared__ unsigned char smem_raw[];
     // the same offset in both CTAs: the leader's MMA addresses the peer's
     // operands through its own shared-memory descriptors
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    float* epi_buf = reinterpret_cast<float*>(smem + kStages * kStageBytes);
-    Ctl& c = *reinterpret_cast<Ctl*>(smem + kStages * kStageBytes + kEpiBytes);
+    unsigned char* sf_ring = smem + kStages * kStageBytes;  // MX: C::kSfStages scale slots
+    float* epi_buf = reinterpret_cast<float*>(sf_ring + C::kSfStages * C::kSfSlotBytes);
+    Ctl& c = *reinterpret_cast<Ctl*>(sf_ring + C::kSfStages * C::kSfSlotBytes + kEpiBytes);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t rank = ptx::cluster_ctarank();
     const bool leader = rank == 0;
@@ -159,6 +211,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(ptx::smem_u32(&c.tempty[b]), kEpiArrivals);
         }
         ptx::mbar_init(ptx::smem_u32(&c.drain), 1);
+        if (MX) {
+            for (int s = 0; s < C::kSfStages; ++s) {
+                ptx::mbar_init(ptx::smem_u32(&c.sfs_full[s]), 1);
+                ptx::mbar_init(ptx::smem_u32(&c.sfs_empty[s]), 4);  // the 4 scale warps of this CTA
+            }
+            for (int b = 0; b < C::kSfBufs; ++b) {
+                ptx::mbar_init(ptx::smem_u32(&c.sf_full[b]), 8);  // 4 scale-factor warps in each CTA
+                ptx::mbar_init(ptx::smem_u32(&c.sf_empty[b]), 1);
+            }
+        }
         c.abort = 0;
         ptx::fence_mbar_init();
     }
@@ -210,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int tile = pair; ok && tile < total; tile += npairs) {
             const PairTile t = decode_pair_tile<SWIGLU>(tile, c, a);
             const int half = t.n / 2;               // token rows held by each CTA
-            const int box = (half + 31) / 32 - 1;   // token-row box of 32, 64, 96 or 128 rows
+            const int box = token_box(t);
             const CUtensorMap* tx = box == 0 ? &tmX0 : box == 1 ? &tmX1 : box == 2 ? &tmX2 : &tmX3;
             const uint32_t bytes = 2u * (uint32_t)(kABytes + (box + 1) * 32 * kTcBK * 2);
             const int xrow = t.start + (int)rank * half;
@@ -231,13 +293,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (leader) ptx::mbar_arrive_expect_tx(fb, bytes);
                         if (SWIGLU) {
                             // 4 groups of (16 gate rows, 16 up rows) of features f*128 + r*64 ..
-                            ptx::tma_load_5d_pair(sa, tw, kb * kTcBK, 0, 0, (t.f * 128 + (int)rank * 64) / 16, t.g,
+                            ptx::tma_load_5d_pair(sa, tw, kb * C::kK, 0, 0, (t.f * 128 + (int)rank * 64) / 16, t.g,
                                                   fb_leader);
-                            ptx::tma_load_2d_pair(sb, tx, kb * kTcBK, xrow, fb_leader);
+                            ptx::tma_load_2d_pair(sb, tx, kb * C::kK, xrow, fb_leader);
                         } else {
-                            ptx::tma_load_2d_pair(sa, tw, kb * kTcBK,
+                            ptx::tma_load_2d_pair(sa, tw, kb * C::kK,
                                                   t.g * a.w_rows_per_group + t.f * 256 + (int)rank * 128, fb_leader);
-                            ptx::tma_load_2d_pair(sb, tx, m * a.x_micro_cols + kb * kTcBK, xrow, fb_leader);
+                            ptx::tma_load_2d_pair(sb, tx, m * a.x_micro_cols + kb * C::kK, xrow, fb_leader);
                         }
                     }
                     __syncwarp();
@@ -250,14 +312,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-        if (!ok && issuer) {
-            fail(c, a.err);
+        if (!ok && issuer) fail(c, a.err);
+        if (issuer) {
             if (leader) {
-                // let every load still in flight (either CTA's) land before the pair can exit
+                // every load issued (either CTA's) lands before the pair can exit, also
+                // when another role gave up on it: the last phase of each slot completes
                 const int n = issued < kStages ? issued : kStages;
                 for (int s = 0; s < n; ++s)
                     ptx::mbar_wait(ptx::smem_u32(&c.full[s]), last_par[s], a.limit_ns, nullptr);
-            } else {
+            } else if (!ok) {
                 settle_inflight_copies();
             }
         }
@@ -268,6 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t phase = 0;
         bool ok = true;
         int local = 0;
+        int sfi = 0;  // MX: stages consumed, which picks the scale-factor buffer and its phase
         for (int tile = pair; ok && tile < total; tile += npairs, ++local) {
             const PairTile t = decode_pair_tile<SWIGLU>(tile, c, a);
             const uint32_t idesc = ptx::idesc_bf16_f32(2 * kWRows, t.n);
@@ -283,7 +347,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t accumulate = 0;
             for (int mi = 0; ok && mi < n_micro_k; ++mi) {
                 for (int kb = 0; kb < a.k_blocks; ++kb) {
-                    const bool got = ptx::mbar_wait(ptx::smem_u32(&c.full[stage]), phase, a.limit_ns, &c.abort);
+                    const int sfb = sfi % C::kSfBufs;  // MX: scale-factor buffer of this stage
+                    bool got = ptx::mbar_wait(ptx::smem_u32(&c.full[stage]), phase, a.limit_ns, &c.abort);
+                    if (MX)  // both CTAs' scale words are in tensor memory
+                        got = got && ptx::mbar_wait(ptx::smem_u32(&c.sf_full[sfb]), (uint32_t)(sfi / C::kSfBufs) & 1u,
+                                                    a.limit_ns, &c.abort);
                     if (!__all_sync(0xffffffffu, got)) {
                         ok = false;
                         break;
@@ -293,13 +361,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t adesc = ptx::sw128_desc(sa);
                     const uint64_t bdesc = ptx::sw128_desc(sa + kABytes);
                     if (issuer) {
+                        if (MX) {
+                            // 4 MMAs of 32 codes; byte k of every scale word belongs to the k-th
+                            const uint32_t sfa_t = tmem + (uint32_t)(C::kSfCol + sfb * 16);
 #pragma unroll
-                        for (int k = 0; k < kTcBK / 16; ++k)
-                            ptx::mma_bf16_pair(d, adesc + 2u * k, bdesc + 2u * k, idesc, accumulate | (uint32_t)k);
-                        ptx::mma_commit_pair_both(ptx::smem_u32(&c.empty[stage]));
+                            for (int k = 0; k < 4; ++k)
+                                ptx::mma_mx_pair(d, adesc + 2u * k, bdesc + 2u * k, ptx::idesc_mx(2 * kWRows, t.n, k, k),
+                                                 sfa_t, sfa_t + 8u, accumulate | (uint32_t)k);
+                            ptx::mma_commit_pair_both(ptx::smem_u32(&c.empty[stage]));
+                            ptx::mma_commit_pair_both(ptx::smem_u32(&c.sf_empty[sfb]));
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < kTcBK / 16; ++k)
+                                ptx::mma_bf16_pair(d, adesc + 2u * k, bdesc + 2u * k, idesc, accumulate | (uint32_t)k);
+                            ptx::mma_commit_pair_both(ptx::smem_u32(&c.empty[stage]));
+                        }
                     }
                     __syncwarp();
                     accumulate = 1;
+                    ++sfi;
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
@@ -316,7 +396,124 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_wait(ptx::smem_u32(&c.drain), 0, a.limit_ns, nullptr);
         }
         __syncwarp();
-    } else if (warp >= 4) {
+    } else if (MX && warp == 3) {
+        // ------------------------------------------------ scale producer (both CTAs)
+        // This CTA's scales of every stage into the scale ring, on its own
+        // barriers: the weight rows' 4 blocks (the row order of the weight
+        // tile) and every route's scale word of the chunk (both CTAs' halves).
+        const bool issuer = ptx::elect_one();
+        int slot = 0, issued = 0;
+        uint32_t phase = 0;
+        uint32_t last_par[C::kSfStages > 0 ? C::kSfStages : 1];
+        bool ok = true;
+        for (int tile = pair; ok && tile < total; tile += npairs) {
+            const PairTile t = decode_pair_tile<SWIGLU>(tile, c, a);
+            for (int mi = 0; ok && mi < n_micro_k; ++mi) {
+                const int m = SWIGLU ? t.m : mi;
+                const CUtensorMap* tsa = pick_map(m, tmSA0, tmSA1, tmSA2, tmSA3);
+                for (int kb = 0; kb < a.k_blocks; ++kb) {
+                    const bool got =
+                        ptx::mbar_wait(ptx::smem_u32(&c.sfs_empty[slot]), phase ^ 1u, a.limit_ns, &c.abort);
+                    if (!__all_sync(0xffffffffu, got)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t dst = ptx::smem_u32(sf_ring + slot * C::kSfSlotBytes);
+                    const uint32_t bar = ptx::smem_u32(&c.sfs_full[slot]);
+                    if (issuer) {
+                        ptx::mbar_arrive_expect_tx(bar, (uint32_t)(C::kSfaBytes + C::kSfbBytes));
+                        if (SWIGLU)
+                            ptx::tma_load_5d(dst + C::kSfaOff, tsa, 0, 0, (t.f * 128 + (int)rank * 64) / 16, kb * 4, t.g,
+                                             bar);
+                        else
+                            ptx::tma_load_3d(dst + C::kSfaOff, tsa, t.f * 256 + (int)rank * 128, kb * 4, t.g, bar);
+                        ptx::tma_load_3d(dst + C::kSfbOff, &tmSB, 0, t.start >> 2, (SWIGLU ? 0 : m) * a.k_blocks + kb,
+                                         bar);
+                    }
+                    __syncwarp();
+                    last_par[slot] = phase;
+                    ++issued;
+                    if (++slot == C::kSfStages) {
+                        slot = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+        if (!ok && issuer) fail(c, a.err);
+        if (issuer) {
+            // every scale load issued lands before the CTA can exit, also when the
+            // scale warps gave up on it: the last phase of each slot completes
+            const int n = issued < C::kSfStages ? issued : C::kSfStages;
+            for (int s2 = 0; s2 < n; ++s2)
+                ptx::mbar_wait(ptx::smem_u32(&c.sfs_full[s2]), last_par[s2], a.limit_ns, nullptr);
+        }
+        __syncwarp();
+    } else if (MX && warp >= 8) {
+        // ------------------------------------------------ scale factors into TMEM (both CTAs)
+        // Warp 8 + q writes lane quarter q of a scale-factor buffer (the MMA
+        // reads every quarter): column j, lane L holds the four block scales of
+        // weight row L + 32 j (columns +0..3) and the scale word of route L + 32 j
+        // of the chunk (columns +8..15); byte i of a word is K block i of the stage.
+        const int q = warp - 8;
+        const uint32_t sf_full0 = ptx::map_to_rank(ptx::smem_u32(&c.sf_full[0]), 0);
+        int slot = 0, sfi = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int tile = pair; ok && tile < total; tile += npairs) {
+            const PairTile t = decode_pair_tile<SWIGLU>(tile, c, a);
+            const int off = t.start & 3;  // the chunk's first scale word in the loaded 16-byte rows
+            for (int mi = 0; ok && mi < n_micro_k; ++mi) {
+                for (int kb = 0; kb < a.k_blocks; ++kb) {
+                    const int sfb = sfi % C::kSfBufs;
+                    // the stage's scales into registers (the ring slot is then free),
+                    // then wait for the TMEM buffer
+                    bool got = ptx::mbar_wait(ptx::smem_u32(&c.sfs_full[slot]), phase, a.limit_ns, &c.abort);
+                    uint32_t wa[4], wb[8];
+                    if (got) {
+                        const unsigned char* sfa = sf_ring + slot * C::kSfSlotBytes + C::kSfaOff;  // [4 blocks][128 rows]
+                        const uint32_t* sfw =
+                            reinterpret_cast<const uint32_t*>(sf_ring + slot * C::kSfSlotBytes + C::kSfbOff);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int r = lane + 32 * j;
+                            wa[j] = (uint32_t)sfa[r] | ((uint32_t)sfa[128 + r] << 8) | ((uint32_t)sfa[256 + r] << 16) |
+                                    ((uint32_t)sfa[384 + r] << 24);
+                        }
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) wb[j] = sfw[off + lane + 32 * j];  // routes past the chunk: unused
+                        __syncwarp();
+                        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&c.sfs_empty[slot]));
+                        got = ptx::mbar_wait(ptx::smem_u32(&c.sf_empty[sfb]),
+                                             ((uint32_t)(sfi / C::kSfBufs) & 1u) ^ 1u, a.limit_ns, &c.abort);
+                    }
+                    if (!__all_sync(0xffffffffu, got)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t col = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(C::kSfCol + sfb * 16);
+                    ptx::tmem_st4(col, wa[0], wa[1], wa[2], wa[3]);
+                    ptx::tmem_st8(col + 8u, wb);
+                    ptx::tmem_wait_st();
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (leader)
+                            ptx::mbar_arrive(ptx::smem_u32(&c.sf_full[sfb]));
+                        else
+                            ptx::mbar_arrive_remote(sf_full0 + (uint32_t)(sfb * sizeof(uint64_t)));
+                    }
+                    ++sfi;
+                    if (++slot == C::kSfStages) {
+                        slot = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+        if (!ok && lane == 0) fail(c, a.err);
+    } else if (warp >= 4 && warp < 8) {
         // ------------------------------------------------ epilogue (both CTAs)
         const int q = warp - 4;  // TMEM lanes 32q .. 32q+31
         __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
@@ -395,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (leader)
                     ptx::mbar_arrive(ptx::smem_u32(&c.tempty[acc]));
                 else
-                    ptx::mbar_arrive_cluster(tempty_leader0 + (uint32_t)(acc * sizeof(uint64_t)));
+                    ptx::mbar_arrive_remote(tempty_leader0 + (uint32_t)(acc * sizeof(uint64_t)));
             }
         }
     }
@@ -411,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Pairs resident at once (one per TPC at most), looked up once per device.
-template <bool SWIGLU>
+template <bool SWIGLU, bool MX>
 int max_pairs() {
     static int cached[64] = {0};
     int dev = 0;
@@ -419,8 +616,8 @@ int max_pairs() {
     if (cached[dev] > 0) return cached[dev];
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(2);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.blockDim = dim3(Cfg<MX>::kThreads);
+    cfg.dynamicSmemBytes = smem_bytes<MX>();
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
@@ -429,7 +626,7 @@ int max_pairs() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, pair_gemm_kernel<SWIGLU>, &cfg) != cudaSuccess || n <= 0) {
+    if (cudaOccupancyMaxActiveClusters(&n, pair_gemm_kernel<SWIGLU, MX>, &cfg) != cudaSuccess || n <= 0) {
         cudaGetLastError();
         return 0;
     }
@@ -437,17 +634,19 @@ int max_pairs() {
     return n;
 }
 
-template <bool SWIGLU>
-cudaError_t launch_pair(const PairGemmArgs& a, const CUtensorMap* tmW, const CUtensorMap* tmX, cudaStream_t s) {
+template <bool SWIGLU, bool MX>
+cudaError_t launch_pair(const PairGemmArgs& a, const CUtensorMap* tmW, const CUtensorMap* tmX,
+                        const CUtensorMap* tmSA, const CUtensorMap& tmSB, cudaStream_t s) {
     if (a.max_tiles <= 0) return cudaSuccess;
-    if (cudaError_t e = ensure_smem_limit<pair_gemm_kernel<SWIGLU>>(kSmemBytes); e != cudaSuccess) return e;
-    const int pairs_max = max_pairs<SWIGLU>();
+    constexpr int smem = smem_bytes<MX>();
+    if (cudaError_t e = ensure_smem_limit<pair_gemm_kernel<SWIGLU, MX>>(smem); e != cudaSuccess) return e;
+    const int pairs_max = max_pairs<SWIGLU, MX>();
     if (pairs_max <= 0) return cudaErrorLaunchOutOfResources;
     const int pairs = a.max_tiles < pairs_max ? a.max_tiles : pairs_max;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(2 * pairs);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.blockDim = dim3(Cfg<MX>::kThreads);
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -458,23 +657,33 @@ cudaError_t launch_pair(const PairGemmArgs& a, const CUtensorMap* tmW, const CUt
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = a.early ? 2 : 1;
-    const CUtensorMap& w1 = a.n_micro > 1 ? tmW[1] : tmW[0];
-    const CUtensorMap& w2 = a.n_micro > 2 ? tmW[2] : tmW[0];
-    const CUtensorMap& w3 = a.n_micro > 3 ? tmW[3] : tmW[0];
-    return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<SWIGLU>, tmW[0], w1, w2, w3, tmX[0], tmX[1], tmX[2], tmX[3],
-                              a);
+    const int nm = a.n_micro;
+    return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<SWIGLU, MX>, tmW[0], tmW[nm > 1 ? 1 : 0], tmW[nm > 2 ? 2 : 0],
+                              tmW[nm > 3 ? 3 : 0], tmX[0], tmX[1], tmX[2], tmX[3], tmSA[0], tmSA[nm > 1 ? 1 : 0],
+                              tmSA[nm > 2 ? 2 : 0], tmSA[nm > 3 ? 3 : 0], tmSB, a);
 }
 
 }  // namespace
 
+// bf16 operands: the scale-map parameters are unused (any valid map).
 cudaError_t launch_pair_gemm_swiglu(const PairGemmArgs& a, const CUtensorMap* tmW, const CUtensorMap* tmX,
                                     cudaStream_t s) {
-    return launch_pair<true>(a, tmW, tmX, s);
+    return launch_pair<true, false>(a, tmW, tmX, tmW, tmX[0], s);
 }
 
 cudaError_t launch_pair_gemm_down(const PairGemmArgs& a, const CUtensorMap* tmW, const CUtensorMap* tmX,
                                   cudaStream_t s) {
-    return launch_pair<false>(a, tmW, tmX, s);
+    return launch_pair<false, false>(a, tmW, tmX, tmW, tmX[0], s);
+}
+
+cudaError_t launch_pair_gemm_swiglu_mx(const PairGemmArgs& a, const CUtensorMap* tmW, const CUtensorMap* tmX,
+                                       const CUtensorMap* tmSA, const CUtensorMap& tmSB, cudaStream_t s) {
+    return launch_pair<true, true>(a, tmW, tmX, tmSA, tmSB, s);
+}
+
+cudaError_t launch_pair_gemm_down_mx(const PairGemmArgs& a, const CUtensorMap* tmW, const CUtensorMap* tmX,
+                                     const CUtensorMap* tmSA, const CUtensorMap& tmSB, cudaStream_t s) {
+    return launch_pair<false, true>(a, tmW, tmX, tmSA, tmSB, s);
 }
 
 }  // namespace moe

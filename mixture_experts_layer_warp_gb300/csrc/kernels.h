@@ -208,7 +208,7 @@ struct PairGemmArgs {
     const int32_t* seg;       // [G+1] route-row offsets of the groups, or null: one dense segment [0, dense_rows)
     int G;
     int n_micro;
-    int k_blocks;             // kTcBK-blocks of K per micro
+    int k_blocks;             // K stages per micro: 64 K (bf16 operands) or 128 K (MXFP8 codes)
     int n_ftiles;             // feature tiles per (group, micro): I/128 (SwiGLU) or H/256 (plain)
     int w_rows_per_group;     // plain form: rows of W per group (H)
     int x_micro_cols;         // plain form: columns of the token rows per micro (I)
@@ -229,6 +229,19 @@ cudaError_t launch_pair_gemm_swiglu(const PairGemmArgs& a, const CUtensorMap* tm
                                     cudaStream_t s);
 cudaError_t launch_pair_gemm_down(const PairGemmArgs& a, const CUtensorMap* tmW, const CUtensorMap* tmX,
                                   cudaStream_t s);
+// The same GEMMs on block-scaled FP8 operands (tcgen05 kind::mxf8f6f4,
+// E4M3 codes with one UE8M0 scale per 32 K of every weight row and token row;
+// 128 K per stage, chunks of at most 208 routes). tmW / tmX as above over the
+// uint8 codes with 128-byte boxes ({128, ...}). tmSA[m]: the weights' scales
+// [G][K/32][rows] (rows innermost): SwiGLU form a 5D map {16, 2, I/16, K/32, G}
+// with box {16, 2, 4, 4, 1} (the row order of the w13 box), plain form a 3D
+// map {H, I/32, G} with box {128, 4, 1}. tmSB: the token rows' scale words,
+// stage-major [n_micro * K/128][rows_pad][4] (launch_gather_mx layout) as a 3D
+// map {16, rows_pad/4, n_micro * K/128} with box {16, 65, 1}, no swizzle.
+cudaError_t launch_pair_gemm_swiglu_mx(const PairGemmArgs& a, const CUtensorMap* tmW, const CUtensorMap* tmX,
+                                       const CUtensorMap* tmSA, const CUtensorMap& tmSB, cudaStream_t s);
+cudaError_t launch_pair_gemm_down_mx(const PairGemmArgs& a, const CUtensorMap* tmW, const CUtensorMap* tmX,
+                                     const CUtensorMap* tmSA, const CUtensorMap& tmSB, cudaStream_t s);
 
 // Swapped-operand variants for batches of at most kSmallTokens tokens (every
 // expert then owns at most kSmallTokens routes): weights on the MMA M side,
@@ -324,7 +337,7 @@ struct LaunchHook {
 };
 
 enum KernelSlot { kSlotRouter = 0, kSlotScan, kSlotPlace, kSlotGather, kSlotGemm1, kSlotGemm2, kSlotSharedGemm1,
-                  kSlotSharedGemm2, kSlotFinalize, kNumSlots };
+                  kSlotSharedGemm2, kSlotFinalize, kSlotQuantH, kNumSlots };
 
 // Returns cudaErrorInvalidValue if a tensor map cannot be encoded.
 cudaError_t enqueue_routing(const RoutingJob& j, cudaStream_t s, const LaunchHook* hook);
@@ -344,6 +357,26 @@ bool encode_3d(CUtensorMap* m, bool bf16, const void* base, const uint64_t dims[
 // The same for any rank 1..5 (strides of dims 1..rank-1).
 bool encode_nd(CUtensorMap* m, bool bf16, const void* base, int rank, const uint64_t* dims,
                const uint64_t* strides, const uint32_t* box, bool swizzle128);
+// MXFP8 activations for the block-scaled FP8 GEMMs (mx_act.cu): codes [rows][K]
+// uint8, scales stage-major [K/128][rows_pad][4] (the four 32-block scales of a
+// 128-element stage of a row in one 32-bit word).
+struct MxActArgs {
+    const void* src;          // bf16: x [T][K] (gather) or the rows [rows][K]
+    const int32_t* inv;       // gather: [rows] inverse permutation (route t*k+j -> its row)
+    int64_t rows;             // gather: R = T*k routes; else the rows of src
+    int k;                    // gather: top_k
+    int K;                    // elements per row, a multiple of 128
+    int64_t rows_pad;         // rows of the scale array (>= rows)
+    void* codes;
+    void* scales;
+    int* err;
+    int num_sms;
+    int early;                // launch while the previous kernel in the stream finishes
+};
+// codes[inv[t*k + j]] = MXFP8 of x[t] for every token t and slot j (x read once)
+cudaError_t launch_gather_mx(const MxActArgs& a, cudaStream_t s);
+// codes[r] = MXFP8 of src[r] for every row r
+cudaError_t launch_quantize_rows_mx(const MxActArgs& a, cudaStream_t s);
 // MXFP8 quantisation (mxfp8.cu): w [groups][rows][cols] bf16 -> codes [groups][rows][cols],
 // scales [groups][cols/32][rows]; cols % 32 == 0.
 cudaError_t launch_mx_quantize(const void* w, int64_t groups, int rows, int cols, void* codes, void* scales,

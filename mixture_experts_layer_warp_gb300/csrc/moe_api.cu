@@ -15,6 +15,8 @@
 
 using namespace moe;
 
+static_assert(kNumSlots == MOE_PROFILE_SLOTS, "profile slots of the C ABI");
+
 namespace {
 
 constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s per bounded wait
@@ -212,6 +214,77 @@ struct MxScales {
     const void* const* w2;   // [E][I/32][H] per micro
 };
 
+// Bytes of the MXFP8 form of R rows of K elements in the xp region: the codes
+// [R][K], then (256-aligned) the stage-major scale words [K/128][rows_pad][4].
+int64_t mx_rows_pad(int64_t R) { return (R + 3) / 4 * 4; }
+size_t mx_scales_off(int64_t R, int64_t K) { return round_up((size_t)(R * K), 256); }
+size_t mx_act_bytes(int64_t R, int64_t K) { return mx_scales_off(R, K) + (size_t)(K / 128) * mx_rows_pad(R) * 4; }
+
+// The routed experts of a batch of more than kSmallTokens tokens with MXFP8
+// expert weights: gather and quantise the token rows to MXFP8 (one pass over
+// x), block-scaled FP8 GEMM1 + SwiGLU into bf16 h, MXFP8 of h, block-scaled
+// FP8 GEMM2 into o. The MXFP8 token rows live in the xp region, later replaced
+// by those of h (GEMM1 has completed when the quantisation of h starts).
+moe_status run_routed_mx(moe_handle* h, const void* x, const void* const* w13, const void* const* w2,
+                         const MxScales& mx, int32_t T, cudaStream_t s, int early_gather) {
+    const moe_config& c = h->cfg;
+    const int H = c.hidden, E = c.num_experts, k = c.top_k, I = c.inter, M = c.n_micro;
+    const int64_t R = (int64_t)T * k, rows_pad = mx_rows_pad(R), MI = (int64_t)M * I;
+    const int chunk_bound = (int)(R / 208) + E;  // bound on sum over experts of ceil(count/208)
+    char* q = static_cast<char*>(h->xp);
+    cudaError_t e;
+    CUtensorMap tmW[kMaxMicro], tmS[kMaxMicro], tmX[4], tmSB;
+    auto encode_rows = [&](int64_t K) {
+        for (uint32_t b = 0; b < 4; ++b)
+            if (!encode_u8_2d(&tmX[b], q, K, R, K, 128, 32 * (b + 1), true)) return false;
+        const uint64_t d[3] = {16, (uint64_t)rows_pad / 4, (uint64_t)K / 128}, st[2] = {16, (uint64_t)rows_pad * 4};
+        const uint32_t box[3] = {16, 65, 1};
+        return encode_3d(&tmSB, false, q + mx_scales_off(R, K), d, st, box, false);
+    };
+
+    MxActArgs gx{x, h->inv, R, k, H, rows_pad, q, q + mx_scales_off(R, H), h->err, h->num_sms, early_gather};
+    if ((e = timed(h, kSlotGather, s, [&] { return launch_gather_mx(gx, s); })) != cudaSuccess)
+        return cuda_err(h, e, "MXFP8 gather launch");
+    // GEMM1 + SwiGLU: codes of w13[m] [E][2I][H] as a 5D map {H, 16, 2, I/16, E}
+    // (box: 4 groups of 16 gate rows and the matching up rows, 128 K), their
+    // scales [E][H/32][2I] in the same row order
+    if (!encode_rows(H)) return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (MXFP8 token rows)");
+    for (int m = 0; m < M; ++m) {
+        const uint64_t cd[5] = {(uint64_t)H, 16, 2, (uint64_t)I / 16, (uint64_t)E};
+        const uint64_t cs[4] = {(uint64_t)H, (uint64_t)I * H, 16 * (uint64_t)H, 2 * (uint64_t)I * H};
+        const uint32_t cb[5] = {128, 16, 2, 4, 1};
+        const uint64_t sd[5] = {16, 2, (uint64_t)I / 16, (uint64_t)H / 32, (uint64_t)E};
+        const uint64_t ss[4] = {(uint64_t)I, 16, 2 * (uint64_t)I, (uint64_t)H / 32 * 2 * I};
+        const uint32_t sb[5] = {16, 2, 4, 4, 1};
+        if (!encode_nd(&tmW[m], false, w13[m], 5, cd, cs, cb, true) ||
+            !encode_nd(&tmS[m], false, mx.w13[m], 5, sd, ss, sb, false))
+            return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (MXFP8 w13[%d])", m);
+    }
+    PairGemmArgs g1{h->offsets, E, M, H / 128, I / 128, 0, 0, h->hbuf, MI, I,
+                    M * chunk_bound * (I / 128), h->err, h->limit_ns, 0, 1};  // early: behind the gather
+    if ((e = timed(h, kSlotGemm1, s, [&] { return launch_pair_gemm_swiglu_mx(g1, tmW, tmX, tmS, tmSB, s); })) !=
+        cudaSuccess)
+        return cuda_err(h, e, "MXFP8 GEMM1 launch");
+    MxActArgs gh{h->hbuf, nullptr, R, 1, (int)MI, rows_pad, q, q + mx_scales_off(R, MI), h->err, h->num_sms, 1};
+    if ((e = timed(h, kSlotQuantH, s, [&] { return launch_quantize_rows_mx(gh, s); })) != cudaSuccess)
+        return cuda_err(h, e, "MXFP8 quantisation of h launch");
+    // GEMM2: codes of w2[m] [E*H][I] (128-row boxes), scales [E][I/32][H]
+    if (!encode_rows(MI)) return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (MXFP8 h)");
+    for (int m = 0; m < M; ++m) {
+        const uint64_t sd[3] = {(uint64_t)H, (uint64_t)I / 32, (uint64_t)E}, ss[2] = {(uint64_t)H, (uint64_t)I / 32 * H};
+        const uint32_t sb[3] = {128, 4, 1};
+        if (!encode_u8_2d(&tmW[m], w2[m], I, (uint64_t)E * H, I, 128, 128, true) ||
+            !encode_3d(&tmS[m], false, mx.w2[m], sd, ss, sb, false))
+            return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (MXFP8 w2[%d])", m);
+    }
+    PairGemmArgs g2{h->offsets, E, M, I / 128, H / 256, H, I, h->obuf, (int64_t)H, 0,
+                    chunk_bound * (H / 256), h->err, h->limit_ns, 0, 1};  // early: behind the quantisation
+    if ((e = timed(h, kSlotGemm2, s, [&] { return launch_pair_gemm_down_mx(g2, tmW, tmX, tmS, tmSB, s); })) !=
+        cudaSuccess)
+        return cuda_err(h, e, "MXFP8 GEMM2 launch");
+    return MOE_OK;
+}
+
 moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const float* bias,
                        const void* const* w13, const void* const* w2, const void* sw13, const void* sw2, int32_t T,
                        void* y, cudaStream_t s, const MxScales* mx = nullptr) {
@@ -235,7 +308,7 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
         if ((e = cudaEventRecord(h->ev_join, ss)) != cudaSuccess) return cuda_err(h, e, "shared-expert join");
     }
 
-    if (!small_bf16) {  // small bf16 batches gather inside the fused GEMM launch
+    if (!small_bf16 && mx == nullptr) {  // small bf16 batches gather inside the fused GEMM launch
         // launched early behind the placement kernel (not behind the fork's event record)
         GatherArgs ga{x,      h->perm,        (int)R, k, (uint32_t)(H * h->esz), h->xp, h->err, h->limit_ns,
                       h->num_sms, h->inv, fork ? 0 : 1};
@@ -323,6 +396,9 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
                  return launch_tc_small_fused(g1, tmX, tmW, g2, tmX2, tmW2, fin, gat, h->done, h->num_sms, s);
              })) != cudaSuccess)
             return cuda_err(h, e, "fused GEMM launch");
+    } else if (mx != nullptr) {
+        if ((st = run_routed_mx(h, x, w13, w2, *mx, T, s, fork ? 0 : 1)) != MOE_OK) return st;
+        if (Is > 0 && !fork && (st = run_shared_pair(h, x, sw13, sw2, T, s, 1)) != MOE_OK) return st;
     } else if (c.dtype == MOE_BF16) {
         CUtensorMap tmW[kMaxMicro], tmX[4];
         const int chunk_bound = (int)(R / 256) + E;  // bound on sum over experts of ceil(count/256)
@@ -604,9 +680,16 @@ moe_status moe_forward_mxfp8(moe_handle* h, const void* x, const void* router_w,
     if (st != MOE_OK) return st;
     if (h->cfg.dtype != MOE_BF16)
         return set_err(h, MOE_ERR_UNSUPPORTED, "MXFP8 expert weights need a bf16 layer");
-    if (T > kSmallTokens)
-        return set_err(h, MOE_ERR_UNSUPPORTED, "MXFP8 expert weights run batches of at most %d tokens", kSmallTokens);
     if (T == 0) return MOE_OK;
+    if (T > kSmallTokens) {
+        // the MXFP8 rows of h replace those of the token rows in the xp region
+        const moe_config& c = h->cfg;
+        const int64_t R = (int64_t)T * c.top_k;
+        const size_t cap = (size_t)c.max_tokens * c.top_k * c.hidden * h->esz;
+        if (mx_act_bytes(R, (int64_t)c.n_micro * c.inter) > cap)
+            return set_err(h, MOE_ERR_UNSUPPORTED,
+                           "MXFP8 expert weights with T > %d need n_micro * inter * 33/32 <= 2 * hidden", kSmallTokens);
+    }
     st = check_weights(h, w13_codes, w2_codes, n_micro, top_k, shared_w13, shared_w2, y);
     if (st != MOE_OK) return st;
     if (w13_scales == nullptr || w2_scales == nullptr)

@@ -101,6 +101,21 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
     }
 }
 
+// mbar_wait_cluster that also gives up once *abort becomes non-zero: for
+// phases completed by arrivals that other CTAs released at cluster scope.
+__device__ __forceinline__ bool mbar_wait_acq_cluster(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                                      volatile int* abort) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((it & 31u) == 0u) {
+            if (abort != nullptr && *abort) return false;
+            if (globaltimer() - t0 > limit_ns) return false;
+        }
+    }
+}
+
 // ---------------------------------------------------------------------- TMA
 // L2 eviction-priority policies for cache-hinted loads: data streamed once
 // (expert weights) goes first, small data reused on every call (the router
@@ -482,6 +497,64 @@ __device__ __forceinline__ void tma_load_5d_pair(uint32_t dst, const void* tmap,
 // Atomic add to a 32-bit word in another CTA's shared memory (shared::cluster address).
 __device__ __forceinline__ void red_add_cluster(uint32_t caddr, uint32_t v) {
     asm volatile("red.relaxed.cluster.shared::cluster.add.u32 [%0], %1;" ::"r"(caddr), "r"(v) : "memory");
+}
+
+// Block-scaled FP8 MMA over the pair (leader only): D (+)= (A * 2^SFA) x
+// (B * 2^SFB)^T, A and B E4M3 codes (K-major, 32 codes per MMA), one UE8M0
+// scale per 32 K of every row of A and of B in tensor memory: the scale word of
+// A row m lies in lane m % 32 of every lane quarter, column sfa + m / 32 (each
+// CTA holds its own 128 rows); that of B row n in lane n % 32, column sfb + n /
+// 32, every CTA holding all N rows; byte i of a word is picked by the
+// descriptor's scale ids (idesc_mx).
+__device__ __forceinline__ void mma_mx_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Instruction descriptor of the block-scaled MMA: E4M3 A and B, both K-major,
+// UE8M0 scales; byte sfa_id / sfb_id of the scale words; shape M x N.
+//   bits 4-5 B scale id, 7-9 A format (0 = E4M3), 10-12 B format, 15/16 A/B
+//   major (0 = K), 17-22 N >> 3, 23 scale type (1 = UE8M0), 24-28 M >> 4,
+//   29-30 A scale id.
+__host__ __device__ constexpr uint32_t idesc_mx(int M, int N, int sfa_id, int sfb_id) {
+    return (uint32_t(sfb_id) << 4) | (uint32_t(N >> 3) << 17) | (1u << 23) | (uint32_t(M >> 4) << 24) |
+           (uint32_t(sfa_id) << 29);
+}
+
+// 5D tiled load completing on this CTA's own barrier.
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const void* tmap, int32_t c0, int32_t c1, int32_t c2,
+                                            int32_t c3, int32_t c4, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar)
+        : "memory");
+}
+
+// Store 4 / 8 consecutive 32-bit columns of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a), "r"(b),
+                 "r"(c), "r"(d)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+
+// Arrive on a barrier of another CTA of the cluster (shared::cluster address)
+// with the default semantics (release at CTA scope): for signals whose data
+// lies in tensor memory, ordered by tcgen05 waits and fences rather than by
+// the arrival. A cluster-scope release makes the arrival wait for the SM's
+// outstanding memory traffic: over a thousand cycles under TMA load streams.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cbar) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cbar) : "memory");
 }
 
 // Arrive on a barrier of another CTA of the cluster (shared::cluster address),

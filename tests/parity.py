@@ -134,3 +134,16 @@ def y_error(y_gpu: torch.Tensor, y_ref: np.ndarray, rows=None) -> float:
         g = g[rows]
     den = np.abs(y_ref).max()
     return float(np.abs(g - y_ref).max() / den) if den > 0 else float(np.abs(g - y_ref).max())
+
+
+def covering_tokens(orc: dict, T: int, k: int, stride: int = 128) -> np.ndarray:
+    """Tokens such that every `stride`-row block of every expert segment of the
+    sorted routes (and of the dense segment [0, T) of a shared expert) holds at
+    least one of their routes, plus each segment's last row: every tile of the
+    grouped GEMMs, whatever their row blocking at that granularity, then has a
+    row the oracle checks."""
+    off, perm = orc["offsets"], orc["perm"]
+    rows = [np.arange(off[e], off[e + 1], stride) for e in range(len(off) - 1)]
+    rows += [np.array([off[e + 1] - 1]) for e in range(len(off) - 1) if off[e + 1] > off[e]]
+    routed = perm[np.concatenate(rows)] // k
+    return np.unique(np.concatenate([routed, np.arange(0, T, stride), [T - 1]]))

@@ -31,19 +31,6 @@ def _forward(layer, dev):
     return y
 
 
-def covering_tokens(orc: dict, T: int, k: int, stride: int = 128) -> np.ndarray:
-    """Tokens such that every `stride`-row block of every expert segment of the
-    sorted routes (and of the dense segment [0, T) of a shared expert) holds at
-    least one of their routes, plus each segment's last row: every tile of the
-    grouped GEMMs, whatever their row blocking at that granularity, then has a
-    row the oracle checks."""
-    off, perm = orc["offsets"], orc["perm"]
-    rows = [np.arange(off[e], off[e + 1], stride) for e in range(len(off) - 1)]
-    rows += [np.array([off[e + 1] - 1]) for e in range(len(off) - 1) if off[e + 1] > off[e]]
-    routed = perm[np.concatenate(rows)] // k
-    return np.unique(np.concatenate([routed, np.arange(0, T, stride), [T - 1]]))
-
-
 def _check(wl, inp, y, rows=None, cover: bool = False):
     host = parity.to_host_numpy(inp)
     orc = parity.oracle_routing(host, wl.k)
@@ -51,7 +38,7 @@ def _check(wl, inp, y, rows=None, cover: bool = False):
     T = host["x"].shape[0]
     rows = np.arange(T) if rows is None else np.asarray(rows)
     if cover:
-        rows = np.union1d(rows, covering_tokens(orc, T, wl.k))
+        rows = np.union1d(rows, parity.covering_tokens(orc, T, wl.k))
     rows = rows[set_ok[rows]]
     ref = oracle.forward_tokens(host["x"], orc["ids"], orc["w"], host["w13"], host["w2"], rows,
                                 host["shared_w13"], host["shared_w2"])

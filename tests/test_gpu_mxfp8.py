@@ -4,9 +4,17 @@ The quantiser must reproduce the oracle's codes and scales bit for bit (an
 integer decision taken on the same bf16 inputs); the layer run on MXFP8
 weights must match the oracle evaluated on the exact value of those weights
 (code * 2^(S-127), the MX definition, in fp64) within the bf16 layer
-tolerance. The kernel converts codes to f16 (exact for scales in f16's range,
-an fp32 form outside it) and rounds the token rows and h to f16; that rounding
-is an implementation detail the tolerance covers.
+tolerance.
+
+Batches of at most 16 tokens: the kernel converts codes to f16 (exact for
+scales in f16's range, an fp32 form outside it) and rounds the token rows and
+h to f16; that rounding is an implementation detail the tolerance covers, and
+the oracle is the plain layer on the exact weights. Larger batches run the
+block-scaled FP8 MMA on MXFP8 token rows and h: the oracle then takes the
+MXFP8 values of each token's input and of each SwiGLU output too
+(``forward_tokens_mx``), both taking h's codes on its bf16 value (the kernel
+rounds its fp32 accumulator, the oracle the fp64 h: they differ where the two
+roundings do, which the tolerance covers).
 """
 import numpy as np
 import pytest
@@ -61,15 +69,18 @@ def _dequant(q):
     return [oracle.mx_dequant(c.cpu().numpy(), s.cpu().numpy()) for c, s in q]
 
 
-def _check(wl, inp, y, w13_q, w2_q, rows=None):
+def _check(wl, inp, y, w13_q, w2_q, rows=None, cover=False):
     host = parity.to_host_numpy(inp)
     orc = parity.oracle_routing(host, wl.k)
     set_ok, _ = parity.decided(orc["lf"], orc["ids"], TAU)
     T = host["x"].shape[0]
     rows = np.arange(T) if rows is None else np.asarray(rows)
+    if cover:
+        rows = np.union1d(rows, parity.covering_tokens(orc, T, wl.k))
     rows = rows[set_ok[rows]]
-    ref = oracle.forward_tokens(host["x"], orc["ids"], orc["w"], _dequant(w13_q), _dequant(w2_q), rows,
-                                host["shared_w13"], host["shared_w2"])
+    fwd = oracle.forward_tokens_mx if T > 16 else oracle.forward_tokens
+    ref = fwd(host["x"], orc["ids"], orc["w"], _dequant(w13_q), _dequant(w2_q), rows,
+              host["shared_w13"], host["shared_w2"])
     err = parity.y_error(y, ref, rows)
     assert err <= parity.Y_TOL["bf16"], f"{wl.name}: rel err {err:.3e}"
     return err
@@ -111,15 +122,86 @@ def test_mxfp8_decode_workload_matches_the_oracle():
     _check(wl, inp, y, w13_q, w2_q)
 
 
-def test_mxfp8_rejects_batches_above_sixteen_tokens():
-    wl = W.Workload("mx_17", 17, 256, 8, 2, 128, 1)
+# Batches above 16 tokens: block-scaled FP8 MMA on MXFP8 token rows and h.
+# Ragged expert segments, chunks split at 240 routes (an expert with ~300
+# routes), every micro count, a shared expert, E = 64 with k = 8.
+LARGE = [
+    W.Workload("mx_large_17", 17, 256, 8, 2, 128, 1),
+    W.Workload("mx_large_two_micro", 200, 512, 16, 4, 256, 2),
+    W.Workload("mx_large_shared", 37, 256, 8, 2, 128, 1, shared_inter=256),
+    W.Workload("mx_large_long_chunks", 600, 256, 4, 2, 128, 1),
+    W.Workload("mx_large_four_micro", 64, 512, 16, 4, 128, 4),
+    W.Workload("mx_large_e64_k8", 300, 1024, 64, 8, 256, 1),
+]
+
+
+@pytest.mark.parametrize("wl", LARGE, ids=lambda w: w.name)
+def test_mxfp8_large_batch_matches_the_oracle_with_mxfp8_activations(wl):
+    inp = W.make_inputs(wl, seed=7)
+    dev = parity.to_device(inp)
+    w13_q, w2_q = _quantize_experts(dev)
+    layer = binding.MoELayer(wl.H, wl.E, wl.k, wl.I, wl.n_micro, max_tokens=wl.T, shared_inter=wl.shared_inter)
+    y = layer.forward_mxfp8(dev["x"], dev["router_w"], dev["router_bias"], w13_q, w2_q, dev["shared_w13"],
+                            dev["shared_w2"])
+    layer.sync()
+    y2 = layer.forward_mxfp8(dev["x"], dev["router_w"], dev["router_bias"], w13_q, w2_q, dev["shared_w13"],
+                             dev["shared_w2"])
+    layer.sync()
+    assert torch.equal(y, y2), "MXFP8 layer is not deterministic across calls"
+    layer.close()
+    _check(wl, inp, y, w13_q, w2_q)
+
+
+def test_mxfp8_large_batch_differs_from_the_f16_reading():
+    """The large-batch oracle is not the small-batch one: on the same inputs
+    the MXFP8 activations move y by far more than the kernel's error against
+    forward_tokens_mx, so the parity test above tells the two readings apart."""
+    wl = LARGE[1]
+    inp = W.make_inputs(wl, seed=7)
+    dev = parity.to_device(inp)
+    w13_q, w2_q = _quantize_experts(dev)
+    layer = binding.MoELayer(wl.H, wl.E, wl.k, wl.I, wl.n_micro, max_tokens=wl.T)
+    y = layer.forward_mxfp8(dev["x"], dev["router_w"], dev["router_bias"], w13_q, w2_q)
+    layer.sync()
+    layer.close()
+    host = parity.to_host_numpy(inp)
+    orc = parity.oracle_routing(host, wl.k)
+    set_ok, _ = parity.decided(orc["lf"], orc["ids"], TAU)
+    rows = np.arange(wl.T)[set_ok]
+    args = (host["x"], orc["ids"], orc["w"], _dequant(w13_q), _dequant(w2_q), rows)
+    e_mx = parity.y_error(y, oracle.forward_tokens_mx(*args), rows)
+    e_plain = parity.y_error(y, oracle.forward_tokens(*args), rows)
+    assert e_mx < e_plain / 3, f"kernel vs MX oracle {e_mx:.3e}, vs plain oracle {e_plain:.3e}"
+
+
+def test_mxfp8_denoise_workload_matches_the_oracle():
+    """The two-micro denoise layer (T=4096, H=4096, E=64, k=8, I=768) at full
+    size, in the launch configuration the benchmark times, on the tokens that
+    cover every chunk of every expert segment."""
+    wl = W.WORKLOADS["denoise_multi_micro"]
+    inp = W.make_inputs(wl, seed=0, device="cuda")
+    w13_q, w2_q = _quantize_experts(inp)
+    layer = binding.MoELayer(wl.H, wl.E, wl.k, wl.I, wl.n_micro, max_tokens=wl.T)
+    y = layer.forward_mxfp8(inp["x"], inp["router_w"], inp["router_bias"], w13_q, w2_q)
+    layer.sync()
+    layer.close()
+    _check(wl, inp, y, w13_q, w2_q, rows=np.arange(0, wl.T, 512), cover=True)
+
+
+def test_mxfp8_rejects_h_larger_than_the_token_row_workspace():
+    """n_micro * I * 33/32 > 2H: the MXFP8 copy of h does not fit where the
+    token rows were, so batches above 16 tokens are refused; 16 tokens run."""
+    wl = W.Workload("mx_wide_h", 40, 256, 8, 2, 512, 1)
     dev = parity.to_device(W.make_inputs(wl, seed=1))
     w13_q, w2_q = _quantize_experts(dev)
-    layer = binding.MoELayer(wl.H, wl.E, wl.k, wl.I, 1, max_tokens=17)
+    layer = binding.MoELayer(wl.H, wl.E, wl.k, wl.I, 1, max_tokens=wl.T)
     with pytest.raises(binding.MoEError) as exc:
         layer.forward_mxfp8(dev["x"], dev["router_w"], None, w13_q, w2_q)
     assert exc.value.name == "MOE_ERR_UNSUPPORTED"
+    y = layer.forward_mxfp8(dev["x"][:16].contiguous(), dev["router_w"], None, w13_q, w2_q)
+    layer.sync()
     layer.close()
+    assert torch.isfinite(y.float()).all()
 
 
 def test_scales_outside_the_f16_range_take_the_exact_path():
@@ -140,13 +222,14 @@ def test_scales_outside_the_f16_range_take_the_exact_path():
 
 
 def test_mxfp8_and_bf16_calls_back_to_back_match_isolated_calls():
-    """MXFP8 decode-sized calls interleaved with bf16 calls of both sizes on one
-    handle and stream, no sync in between, equal the same calls run alone."""
+    """MXFP8 calls of both sizes interleaved with bf16 calls of both sizes on
+    one handle and stream, no sync in between, equal the same calls run alone."""
     base = W.Workload("mx_mix", 200, 512, 16, 4, 256, 1)
     wts = parity.to_device(W.make_inputs(base, seed=0))
     w13_q, w2_q = _quantize_experts(wts)
     layer = binding.MoELayer(base.H, base.E, base.k, base.I, 1, max_tokens=base.T)
-    plan = [("mx", 8), ("bf16", 200), ("mx", 16), ("bf16", 8), ("mx", 1), ("bf16", 200), ("mx", 8)]
+    plan = [("mx", 8), ("bf16", 200), ("mx", 16), ("mx", 200), ("bf16", 8), ("mx", 1), ("bf16", 200), ("mx", 150),
+            ("mx", 8)]
     xs = [W.make_inputs(base, seed=60 + i, T=T, experts=False)["x"].cuda() for i, (_, T) in enumerate(plan)]
 
     def call(kind, x, out=None):
