@@ -506,31 +506,32 @@ def measure(args, wl, world, rank, local, peaks, mx=False, cpu_seconds=12.0, two
     esz = 4 if wl.dtype == "f32" else 2
     n_host = POOL if wl.T * wl.H * esz <= (64 << 20) else 2  # large batches: two pinned host batches
     host_pool = [pool[i].cpu().pin_memory() for i in range(n_host)]
-    y_host = torch.empty((wl.T, wl.H), dtype=wl.torch_dtype).pin_memory()
+    y_hosts = [torch.empty((wl.T, wl.H), dtype=wl.torch_dtype).pin_memory() for _ in range(2)]
     e2e_steps = max(3, min(args.steps, 50))
-    x_dev = torch.empty_like(pool[0])
 
     def e2e_step(i):
-        if mx:  # no host entry point for MXFP8: pinned copies around the device call
-            x_dev.copy_(host_pool[i % n_host], non_blocking=True)
-            layer.forward_mxfp8(x_dev, *args_w, out=y)
-            y_host.copy_(y, non_blocking=True)
-            torch.cuda.current_stream().synchronize()
+        # the serving loop's form: each call enqueues its own copies and returns;
+        # call i+1's copy of x and call i-1's copy of y overlap call i
+        if mx:
+            layer.forward_mxfp8(host_pool[i % n_host], *args_w, out=y_hosts[i % 2], host_async=True)
         else:
-            layer.forward_host(host_pool[i % n_host], *args_w, out_host=y_host)
+            layer.forward_host(host_pool[i % n_host], *args_w, out_host=y_hosts[i % 2], wait=False)
 
     for i in range(2):
         e2e_step(i)
+    layer.sync()
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for i in range(e2e_steps):
         e2e_step(i)
+    layer.sync()  # every step's y is in host memory
     _, e2e_value = job_throughput(world, wl.T, e2e_steps, (time.perf_counter() - t0) * 1e3)
     e2e = {"value": e2e_value, "unit": "tokens/s",
            "h2d_bytes_per_step": wl.T * wl.H * esz, "d2h_bytes_per_step": wl.T * wl.H * esz,
-           "entry_point": "moe_forward_host" if not mx else "pinned copies around moe_forward_mxfp8"}
-    del host_pool, y_host
+           "entry_point": ("moe_forward_mxfp8_host_async" if mx else "moe_forward_host_async") +
+           " from pinned buffers, calls back to back, one moe_sync after the last"}
+    del host_pool, y_hosts
 
     two = None
     if two_dispatch and wl.n_micro > 1 and not mx:

@@ -142,15 +142,33 @@ moe_status moe_forward(moe_handle *h, const void *x, const void *router_w,
 
 /*
  * moe_forward with x and y in HOST memory (pinned memory gives the fastest
- * copies): copies x to the handle's device staging buffer, runs the layer and
- * copies y back, all on `stream`, then synchronises the stream. Weights and
- * the router are device pointers as in moe_forward.
+ * copies, and only pinned memory lets the copies overlap the layer): copies x
+ * to one of the handle's two device staging buffers, runs the layer on
+ * `stream` and copies y back, then waits until y is in y_host. Weights and the
+ * router are device pointers as in moe_forward. The copies run on two streams
+ * the handle creates on its first host-buffer call (MOE_ERR_CUDA if it cannot),
+ * ordered against the layer by events.
  */
 moe_status moe_forward_host(moe_handle *h, const void *x_host, const void *router_w,
                             const float *router_bias, const void *const *w13,
                             const void *const *w2, int32_t n_micro, int32_t top_k,
                             const void *shared_w13, const void *shared_w2, int32_t T,
                             void *y_host, void *stream);
+
+/*
+ * moe_forward_host without the wait: enqueues the copy of x, the layer and the
+ * copy of y, and returns. Consecutive calls alternate between the two staging
+ * buffers, so the copy of x of call n+1 and the copy of y of call n-1 overlap
+ * the layer of call n (the serving loop's host I/O hides behind the GPU work).
+ * x_host must stay unchanged, and y_host unread, until moe_sync returns (which
+ * waits for every copy); with accumulation on (moe_set_accumulate), y_host is
+ * also read, so calls in flight together need distinct y_host buffers.
+ */
+moe_status moe_forward_host_async(moe_handle *h, const void *x_host, const void *router_w,
+                                  const float *router_bias, const void *const *w13,
+                                  const void *const *w2, int32_t n_micro, int32_t top_k,
+                                  const void *shared_w13, const void *shared_w2, int32_t T,
+                                  void *y_host, void *stream);
 
 /*
  * Block-scaled FP8 expert weights (the pages list FP8 among the precision
@@ -199,6 +217,14 @@ moe_status moe_forward_mxfp8(moe_handle *h, const void *x, const void *router_w,
                              const void *shared_w13, const void *shared_w2, int32_t T,
                              void *y, void *stream);
 
+/* moe_forward_mxfp8 with x and y in host memory, as moe_forward_host_async. */
+moe_status moe_forward_mxfp8_host_async(moe_handle *h, const void *x_host, const void *router_w,
+                                        const float *router_bias, const void *const *w13_codes,
+                                        const void *const *w13_scales, const void *const *w2_codes,
+                                        const void *const *w2_scales, int32_t n_micro, int32_t top_k,
+                                        const void *shared_w13, const void *shared_w2, int32_t T,
+                                        void *y_host, void *stream);
+
 /*
  * Output accumulation. With `on` non-zero, later moe_forward / moe_forward_host
  * calls on this handle add the layer's output into y (y += layer(x)): the
@@ -223,9 +249,10 @@ moe_status moe_set_accumulate(moe_handle *h, int32_t on);
 moe_status moe_set_shared_stream(moe_handle *h, int32_t on);
 
 /*
- * Synchronise the stream of the handle's last call and read its device error
- * word. Returns MOE_OK, or MOE_ERR_TIMEOUT / MOE_ERR_DEVICE_CHECK (and makes
- * the handle sticky), or MOE_ERR_CUDA.
+ * Synchronise the stream of the handle's last call (and the host-copy streams
+ * of the host-buffer calls) and read its device error word. Returns MOE_OK, or
+ * MOE_ERR_TIMEOUT / MOE_ERR_DEVICE_CHECK (and makes the handle sticky), or
+ * MOE_ERR_CUDA.
  */
 moe_status moe_sync(moe_handle *h);
 

@@ -63,7 +63,9 @@ def load() -> ctypes.CDLL:
         "moe_route": (st, [p, p, p, p, i32, p, p, p, p, p, p]),
         "moe_forward": (st, [p, p, p, p, p, p, i32, i32, p, p, i32, p, p]),
         "moe_forward_host": (st, [p, p, p, p, p, p, i32, i32, p, p, i32, p, p]),
+        "moe_forward_host_async": (st, [p, p, p, p, p, p, i32, i32, p, p, i32, p, p]),
         "moe_forward_mxfp8": (st, [p, p, p, p, p, p, p, p, i32, i32, p, p, i32, p, p]),
+        "moe_forward_mxfp8_host_async": (st, [p, p, p, p, p, p, p, p, i32, i32, p, p, i32, p, p]),
         "moe_quantize_mxfp8": (st, [p, ctypes.c_int64, i32, i32, p, p, p]),
         "moe_sync": (st, [p]),
         "moe_last_error": (ctypes.c_char_p, [p]),
@@ -255,8 +257,9 @@ class MoELayer:
         return y
 
     def forward_host(self, x_host, router_w, router_bias, w13, w2, shared_w13=None, shared_w2=None,
-                     out_host=None):
-        """``moe_forward_host``: x and y in (preferably pinned) host memory."""
+                     out_host=None, wait=True):
+        """``moe_forward_host`` (``wait=False``: ``moe_forward_host_async``, y valid
+        after ``sync()``): x and y in (preferably pinned) host memory."""
         c = self.cfg
         T = x_host.shape[0]
         self._tensor(x_host, "x_host", (T, c.hidden), host=True)
@@ -264,18 +267,21 @@ class MoELayer:
         p13, p2 = self._weights(w13, w2, shared_w13, shared_w2)
         y = torch.empty((T, c.hidden), dtype=self.dtype, pin_memory=True) if out_host is None else \
             self._tensor(out_host, "out_host", (T, c.hidden), host=True)
-        rc = self._lib.moe_forward_host(self._h, _ptr(x_host), _ptr(router_w), _ptr(router_bias), p13, p2,
-                                        c.n_micro, c.top_k, _ptr(shared_w13), _ptr(shared_w2), T, _ptr(y),
-                                        _stream(self.device))
+        fn = self._lib.moe_forward_host if wait else self._lib.moe_forward_host_async
+        rc = fn(self._h, _ptr(x_host), _ptr(router_w), _ptr(router_bias), p13, p2, c.n_micro, c.top_k,
+                _ptr(shared_w13), _ptr(shared_w2), T, _ptr(y), _stream(self.device))
         self._check(rc)
         return y
 
-    def forward_mxfp8(self, x, router_w, router_bias, w13_q, w2_q, shared_w13=None, shared_w2=None, out=None):
+    def forward_mxfp8(self, x, router_w, router_bias, w13_q, w2_q, shared_w13=None, shared_w2=None, out=None,
+                      host_async=False):
         """``moe_forward_mxfp8``: routed experts in MXFP8 (``w13_q`` / ``w2_q``: per
-        micro, ``(codes, scales)`` pairs from ``quantize_mxfp8``); returns y [T, H]."""
+        micro, ``(codes, scales)`` pairs from ``quantize_mxfp8``); returns y [T, H].
+        ``host_async``: x and ``out`` in host memory through
+        ``moe_forward_mxfp8_host_async`` (y valid after ``sync()``)."""
         c = self.cfg
         T = x.shape[0]
-        self._tensor(x, "x", (T, c.hidden))
+        self._tensor(x, "x_host" if host_async else "x", (T, c.hidden), host=host_async)
         self._router(router_w, router_bias)
         if len(w13_q) != c.n_micro or len(w2_q) != c.n_micro:
             raise ValueError(f"expected {c.n_micro} micro-shards of w13 and w2")
@@ -289,13 +295,17 @@ class MoELayer:
             self._tensor(shared_w13, "shared_w13", (2 * c.shared_inter, H))
             self._tensor(shared_w2, "shared_w2", (H, c.shared_inter))
         arr = lambda ts: (ctypes.c_void_p * c.n_micro)(*[t.data_ptr() for t in ts])  # noqa: E731
-        y = torch.empty((T, H), dtype=self.dtype, device=self.device) if out is None else \
-            self._tensor(out, "out", (T, H))
-        rc = self._lib.moe_forward_mxfp8(self._h, _ptr(x), _ptr(router_w), _ptr(router_bias),
-                                         arr([q[0] for q in w13_q]), arr([q[1] for q in w13_q]),
-                                         arr([q[0] for q in w2_q]), arr([q[1] for q in w2_q]),
-                                         c.n_micro, c.top_k, _ptr(shared_w13), _ptr(shared_w2), T, _ptr(y),
-                                         _stream(self.device))
+        if host_async:
+            y = torch.empty((T, H), dtype=self.dtype, pin_memory=True) if out is None else \
+                self._tensor(out, "out_host", (T, H), host=True)
+        else:
+            y = torch.empty((T, H), dtype=self.dtype, device=self.device) if out is None else \
+                self._tensor(out, "out", (T, H))
+        fn = self._lib.moe_forward_mxfp8_host_async if host_async else self._lib.moe_forward_mxfp8
+        rc = fn(self._h, _ptr(x), _ptr(router_w), _ptr(router_bias),
+                arr([q[0] for q in w13_q]), arr([q[1] for q in w13_q]),
+                arr([q[0] for q in w2_q]), arr([q[1] for q in w2_q]),
+                c.n_micro, c.top_k, _ptr(shared_w13), _ptr(shared_w2), T, _ptr(y), _stream(self.device))
         self._check(rc)
         return y
 

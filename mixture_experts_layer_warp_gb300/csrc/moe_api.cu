@@ -52,8 +52,13 @@ struct moe_handle {
     void* obuf = nullptr;
     void* hs = nullptr;
     void* sbuf = nullptr;
-    void* x_stage = nullptr;
-    void* y_stage = nullptr;
+    void* x_stage[2] = {nullptr, nullptr};  // host-buffer calls: device staging, used alternately
+    void* y_stage[2] = {nullptr, nullptr};
+    // host-buffer calls: x is copied in on `in`, y out on `out` (both created on
+    // the first such call); events order the reuse of each staging slot
+    cudaStream_t pipe_in = nullptr, pipe_out = nullptr;
+    cudaEvent_t ev_h2d[2] = {nullptr, nullptr}, ev_comp[2] = {nullptr, nullptr}, ev_d2h[2] = {nullptr, nullptr};
+    int pipe_slot = 0;
     // moe_set_shared_stream: bf16 layers with a shared expert and more than
     // kSmallTokens tokens run the shared expert's GEMMs on this stream
     bool shared_stream = false;
@@ -531,6 +536,80 @@ moe_status check_weights(moe_handle* h, const void* const* w13, const void* cons
     return MOE_OK;
 }
 
+// Host-buffer calls (moe_forward_host and the _async entry points). Call n
+// uses staging slot n % 2: x is copied in on pipe_in once the compute of call
+// n-2 has read the slot (and, when y is accumulated, its copy-out of y is
+// done); the layer runs on the caller's stream once the copy-in is done (and
+// the slot's y was copied out); y is copied out on pipe_out once the compute is
+// done. So call n+1's copy-in and call n-1's copy-out overlap call n.
+moe_status ensure_pipe(moe_handle* h) {
+    if (h->pipe_out != nullptr) return MOE_OK;
+    bool ok = cudaStreamCreateWithFlags(&h->pipe_in, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&h->pipe_out, cudaStreamNonBlocking) == cudaSuccess;
+    for (int i = 0; ok && i < 2; ++i)
+        ok = cudaEventCreateWithFlags(&h->ev_h2d[i], cudaEventDisableTiming) == cudaSuccess &&
+             cudaEventCreateWithFlags(&h->ev_comp[i], cudaEventDisableTiming) == cudaSuccess &&
+             cudaEventCreateWithFlags(&h->ev_d2h[i], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) {
+        cudaGetLastError();
+        return set_err(h, MOE_ERR_CUDA, "could not create the host-copy streams");
+    }
+    return MOE_OK;
+}
+
+template <typename Run>
+moe_status host_call(moe_handle* h, const void* x_host, int32_t T, void* y_host, cudaStream_t s, Run&& run) {
+    moe_status st = ensure_pipe(h);
+    if (st != MOE_OK) return st;
+    const int b = h->pipe_slot;
+    h->pipe_slot ^= 1;
+    const size_t bytes = (size_t)T * h->cfg.hidden * h->esz;
+    cudaError_t e;
+    if ((e = cudaStreamWaitEvent(h->pipe_in, h->ev_comp[b], 0)) != cudaSuccess ||
+        (h->accumulate && (e = cudaStreamWaitEvent(h->pipe_in, h->ev_d2h[b], 0)) != cudaSuccess) ||
+        (e = cudaMemcpyAsync(h->x_stage[b], x_host, bytes, cudaMemcpyHostToDevice, h->pipe_in)) != cudaSuccess ||
+        (h->accumulate &&
+         (e = cudaMemcpyAsync(h->y_stage[b], y_host, bytes, cudaMemcpyHostToDevice, h->pipe_in)) != cudaSuccess) ||
+        (e = cudaEventRecord(h->ev_h2d[b], h->pipe_in)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(s, h->ev_h2d[b], 0)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(s, h->ev_d2h[b], 0)) != cudaSuccess)
+        return cuda_err(h, e, "copy x to device");
+    st = run(h->x_stage[b], h->y_stage[b]);
+    end_call(h);
+    // recorded whatever run enqueued, so that the slot's next use waits for it
+    if ((e = cudaEventRecord(h->ev_comp[b], s)) != cudaSuccess) return cuda_err(h, e, "record compute event");
+    if (st != MOE_OK) return st;
+    if ((e = cudaStreamWaitEvent(h->pipe_out, h->ev_comp[b], 0)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(y_host, h->y_stage[b], bytes, cudaMemcpyDeviceToHost, h->pipe_out)) != cudaSuccess ||
+        (e = cudaEventRecord(h->ev_d2h[b], h->pipe_out)) != cudaSuccess)
+        return cuda_err(h, e, "copy y to host");
+    return MOE_OK;
+}
+
+moe_status check_mxfp8(moe_handle* h, const void* const* w13_codes, const void* const* w13_scales,
+                       const void* const* w2_codes, const void* const* w2_scales, int32_t n_micro, int32_t top_k,
+                       const void* shared_w13, const void* shared_w2, int32_t T, const void* y) {
+    if (h->cfg.dtype != MOE_BF16) return set_err(h, MOE_ERR_UNSUPPORTED, "MXFP8 expert weights need a bf16 layer");
+    if (T > kSmallTokens) {
+        // the MXFP8 rows of h replace those of the token rows in the xp region
+        const moe_config& c = h->cfg;
+        const int64_t R = (int64_t)T * c.top_k;
+        const size_t cap = (size_t)c.max_tokens * c.top_k * c.hidden * h->esz;
+        if (mx_act_bytes(R, (int64_t)c.n_micro * c.inter) > cap)
+            return set_err(h, MOE_ERR_UNSUPPORTED,
+                           "MXFP8 expert weights with T > %d need n_micro * inter * 33/32 <= 2 * hidden", kSmallTokens);
+    }
+    moe_status st = check_weights(h, w13_codes, w2_codes, n_micro, top_k, shared_w13, shared_w2, y);
+    if (st != MOE_OK) return st;
+    if (w13_scales == nullptr || w2_scales == nullptr)
+        return set_err(h, MOE_ERR_INVALID_ARG, "w13 and w2 scale arrays must be non-null");
+    for (int m = 0; m < n_micro; ++m)
+        if (w13_scales[m] == nullptr || w2_scales[m] == nullptr || !aligned16(w13_scales[m]) ||
+            !aligned16(w2_scales[m]))
+            return set_err(h, MOE_ERR_INVALID_ARG, "micro %d scales null or not 16-byte aligned", m);
+    return MOE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -582,7 +661,8 @@ moe_status moe_create(const moe_config* cfg, moe_handle** out) {
     const size_t o_hist = take(NB * E * 4), o_base = take(NB * E * 4), o_done = take(fused_counter_ints((int)E) * 4);
     const size_t o_xp = take(R * H * esz), o_h = take(R * M * I * esz), o_o = take(R * H * esz);
     const size_t o_hs = take(T * Is * esz), o_s = take(Is ? T * H * esz : 0);
-    const size_t o_xst = take(T * H * esz), o_yst = take(T * H * esz);
+    const size_t o_xst0 = take(T * H * esz), o_xst1 = take(T * H * esz);
+    const size_t o_yst0 = take(T * H * esz), o_yst1 = take(T * H * esz);
     h->ws_bytes = off;
     if (cudaMalloc(&h->ws, h->ws_bytes) != cudaSuccess) {
         cudaGetLastError();
@@ -607,8 +687,10 @@ moe_status moe_create(const moe_config* cfg, moe_handle** out) {
     h->obuf = b + o_o;
     h->hs = b + o_hs;
     h->sbuf = b + o_s;
-    h->x_stage = b + o_xst;
-    h->y_stage = b + o_yst;
+    h->x_stage[0] = b + o_xst0;
+    h->x_stage[1] = b + o_xst1;
+    h->y_stage[0] = b + o_yst0;
+    h->y_stage[1] = b + o_yst1;
     if (cudaMemset(h->err, 0, sizeof(int)) != cudaSuccess) {
         cudaFree(h->ws);
         delete h;
@@ -622,6 +704,13 @@ void moe_destroy(moe_handle* h) {
     if (h == nullptr) return;
     cudaDeviceSynchronize();
     for (cudaEvent_t ev : h->prof_ev) cudaEventDestroy(ev);
+    for (int i = 0; i < 2; ++i) {
+        if (h->ev_h2d[i] != nullptr) cudaEventDestroy(h->ev_h2d[i]);
+        if (h->ev_comp[i] != nullptr) cudaEventDestroy(h->ev_comp[i]);
+        if (h->ev_d2h[i] != nullptr) cudaEventDestroy(h->ev_d2h[i]);
+    }
+    if (h->pipe_in != nullptr) cudaStreamDestroy(h->pipe_in);
+    if (h->pipe_out != nullptr) cudaStreamDestroy(h->pipe_out);
     if (h->ev_fork != nullptr) cudaEventDestroy(h->ev_fork);
     if (h->ev_join != nullptr) cudaEventDestroy(h->ev_join);
     if (h->side != nullptr) cudaStreamDestroy(h->side);
@@ -678,32 +767,38 @@ moe_status moe_forward_mxfp8(moe_handle* h, const void* x, const void* router_w,
                              void* stream) {
     moe_status st = check_call(h, x, router_w, T);
     if (st != MOE_OK) return st;
-    if (h->cfg.dtype != MOE_BF16)
-        return set_err(h, MOE_ERR_UNSUPPORTED, "MXFP8 expert weights need a bf16 layer");
+    if (h->cfg.dtype != MOE_BF16) return set_err(h, MOE_ERR_UNSUPPORTED, "MXFP8 expert weights need a bf16 layer");
     if (T == 0) return MOE_OK;
-    if (T > kSmallTokens) {
-        // the MXFP8 rows of h replace those of the token rows in the xp region
-        const moe_config& c = h->cfg;
-        const int64_t R = (int64_t)T * c.top_k;
-        const size_t cap = (size_t)c.max_tokens * c.top_k * c.hidden * h->esz;
-        if (mx_act_bytes(R, (int64_t)c.n_micro * c.inter) > cap)
-            return set_err(h, MOE_ERR_UNSUPPORTED,
-                           "MXFP8 expert weights with T > %d need n_micro * inter * 33/32 <= 2 * hidden", kSmallTokens);
-    }
-    st = check_weights(h, w13_codes, w2_codes, n_micro, top_k, shared_w13, shared_w2, y);
+    st = check_mxfp8(h, w13_codes, w13_scales, w2_codes, w2_scales, n_micro, top_k, shared_w13, shared_w2, T, y);
     if (st != MOE_OK) return st;
-    if (w13_scales == nullptr || w2_scales == nullptr)
-        return set_err(h, MOE_ERR_INVALID_ARG, "w13 and w2 scale arrays must be non-null");
-    for (int m = 0; m < n_micro; ++m)
-        if (w13_scales[m] == nullptr || w2_scales[m] == nullptr || !aligned16(w13_scales[m]) ||
-            !aligned16(w2_scales[m]))
-            return set_err(h, MOE_ERR_INVALID_ARG, "micro %d scales null or not 16-byte aligned", m);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     h->last_stream = s;
     const MxScales mx{w13_scales, w2_scales};
     st = run_forward(h, x, router_w, router_bias, w13_codes, w2_codes, shared_w13, shared_w2, T, y, s, &mx);
     end_call(h);
     return st;
+}
+
+moe_status moe_forward_mxfp8_host_async(moe_handle* h, const void* x_host, const void* router_w,
+                                        const float* router_bias, const void* const* w13_codes,
+                                        const void* const* w13_scales, const void* const* w2_codes,
+                                        const void* const* w2_scales, int32_t n_micro, int32_t top_k,
+                                        const void* shared_w13, const void* shared_w2, int32_t T, void* y_host,
+                                        void* stream) {
+    moe_status st = check_call(h, h ? h->x_stage[0] : nullptr, router_w, T);
+    if (st != MOE_OK) return st;
+    if (h->cfg.dtype != MOE_BF16) return set_err(h, MOE_ERR_UNSUPPORTED, "MXFP8 expert weights need a bf16 layer");
+    if (T == 0) return MOE_OK;
+    if (x_host == nullptr || y_host == nullptr) return set_err(h, MOE_ERR_INVALID_ARG, "host x and y must be non-null");
+    st = check_mxfp8(h, w13_codes, w13_scales, w2_codes, w2_scales, n_micro, top_k, shared_w13, shared_w2, T,
+                     h->y_stage[0]);
+    if (st != MOE_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    h->last_stream = s;
+    const MxScales mx{w13_scales, w2_scales};
+    return host_call(h, x_host, T, y_host, s, [&](const void* xd, void* yd) {
+        return run_forward(h, xd, router_w, router_bias, w13_codes, w2_codes, shared_w13, shared_w2, T, yd, s, &mx);
+    });
 }
 
 moe_status moe_quantize_mxfp8(const void* w, int64_t groups, int32_t rows, int32_t cols, void* codes,
@@ -720,29 +815,32 @@ moe_status moe_quantize_mxfp8(const void* w, int64_t groups, int32_t rows, int32
                : MOE_ERR_CUDA;
 }
 
+moe_status moe_forward_host_async(moe_handle* h, const void* x_host, const void* router_w,
+                                  const float* router_bias, const void* const* w13, const void* const* w2,
+                                  int32_t n_micro, int32_t top_k, const void* shared_w13, const void* shared_w2,
+                                  int32_t T, void* y_host, void* stream) {
+    moe_status st = check_call(h, h ? h->x_stage[0] : nullptr, router_w, T);
+    if (st != MOE_OK) return st;
+    if (T == 0) return MOE_OK;
+    if (x_host == nullptr || y_host == nullptr) return set_err(h, MOE_ERR_INVALID_ARG, "host x and y must be non-null");
+    st = check_weights(h, w13, w2, n_micro, top_k, shared_w13, shared_w2, h->y_stage[0]);
+    if (st != MOE_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    h->last_stream = s;
+    return host_call(h, x_host, T, y_host, s, [&](const void* xd, void* yd) {
+        return run_forward(h, xd, router_w, router_bias, w13, w2, shared_w13, shared_w2, T, yd, s);
+    });
+}
+
 moe_status moe_forward_host(moe_handle* h, const void* x_host, const void* router_w, const float* router_bias,
                             const void* const* w13, const void* const* w2, int32_t n_micro, int32_t top_k,
                             const void* shared_w13, const void* shared_w2, int32_t T, void* y_host,
                             void* stream) {
-    moe_status st = check_call(h, h ? h->x_stage : nullptr, router_w, T);
-    if (st != MOE_OK) return st;
-    if (T == 0) return MOE_OK;
-    if (x_host == nullptr || y_host == nullptr) return set_err(h, MOE_ERR_INVALID_ARG, "host x and y must be non-null");
-    st = check_weights(h, w13, w2, n_micro, top_k, shared_w13, shared_w2, h->y_stage);
-    if (st != MOE_OK) return st;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    h->last_stream = s;
-    const size_t bytes = (size_t)T * h->cfg.hidden * h->esz;
-    cudaError_t e = cudaMemcpyAsync(h->x_stage, x_host, bytes, cudaMemcpyHostToDevice, s);
-    if (e != cudaSuccess) return cuda_err(h, e, "copy x to device");
-    if (h->accumulate && (e = cudaMemcpyAsync(h->y_stage, y_host, bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess)
-        return cuda_err(h, e, "copy y to device");
-    st = run_forward(h, h->x_stage, router_w, router_bias, w13, w2, shared_w13, shared_w2, T, h->y_stage, s);
-    end_call(h);
-    if (st != MOE_OK) return st;
-    if ((e = cudaMemcpyAsync(y_host, h->y_stage, bytes, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
-        return cuda_err(h, e, "copy y to host");
-    if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_err(h, e, "stream synchronize");
+    moe_status st = moe_forward_host_async(h, x_host, router_w, router_bias, w13, w2, n_micro, top_k, shared_w13,
+                                           shared_w2, T, y_host, stream);
+    if (st != MOE_OK || T == 0) return st;
+    cudaError_t e = cudaStreamSynchronize(h->pipe_out);
+    if (e != cudaSuccess) return cuda_err(h, e, "stream synchronize");
     return MOE_OK;
 }
 
@@ -750,6 +848,8 @@ moe_status moe_sync(moe_handle* h) {
     if (h == nullptr) return MOE_ERR_INVALID_ARG;
     if (h->sticky) return set_err(h, MOE_ERR_STICKY, "handle is sticky after an earlier device error");
     cudaError_t e = cudaStreamSynchronize(h->last_stream);
+    if (e == cudaSuccess && h->pipe_out != nullptr) e = cudaStreamSynchronize(h->pipe_out);
+    if (e == cudaSuccess && h->pipe_in != nullptr) e = cudaStreamSynchronize(h->pipe_in);
     if (e != cudaSuccess) return cuda_err(h, e, "stream synchronize");
     int word = 0;
     if ((e = cudaMemcpy(&word, h->err, sizeof word, cudaMemcpyDeviceToHost)) != cudaSuccess)

@@ -7,8 +7,8 @@ from mixture_experts_layer_warp_gb300 import binding
 
 def test_header_declares_the_layer_entry_points():
     names = binding.declared_functions()
-    for n in ("moe_create", "moe_destroy", "moe_route", "moe_forward", "moe_forward_host", "moe_sync",
-              "moe_last_error"):
+    for n in ("moe_create", "moe_destroy", "moe_route", "moe_forward", "moe_forward_host", "moe_forward_host_async",
+              "moe_forward_mxfp8", "moe_forward_mxfp8_host_async", "moe_sync", "moe_last_error"):
         assert n in names
 
 

@@ -175,6 +175,50 @@ def test_host_entry_point_matches_device_entry_point():
     layer.close()
 
 
+def test_async_host_calls_overlap_and_match_device_calls():
+    """moe_forward_host_async: a run of calls of mixed sizes (decode-sized and
+    large, so both launch sequences), each on its own pinned buffers, issued
+    back to back and read after one moe_sync, equals the same calls through
+    moe_forward; a blocking host call in the middle of the run keeps the order."""
+    wl = W.Workload("host_async", 300, 256, 8, 2, 128, 2, shared_inter=128)
+    wts = parity.to_device(W.make_inputs(wl, seed=6))
+    layer = _layer(wl)
+    sizes = [8, 300, 16, 1, 200, 300, 5, 64]
+    xs = [W.make_inputs(wl, seed=80 + i, T=T, experts=False)["x"].pin_memory() for i, T in enumerate(sizes)]
+    ys = [torch.empty_like(x).pin_memory() for x in xs]
+    args = (wts["router_w"], wts["router_bias"], wts["w13"], wts["w2"], wts["shared_w13"], wts["shared_w2"])
+    for i, (x, y) in enumerate(zip(xs, ys)):
+        layer.forward_host(x, *args, out_host=y, wait=(i == 4))
+    layer.sync()
+    for T, x, y in zip(sizes, xs, ys):
+        ref = layer.forward(x.cuda(), *args)
+        layer.sync()
+        assert torch.equal(y, ref.cpu()), f"T={T}: async host result differs from the device call"
+    layer.close()
+
+
+def test_async_host_calls_accumulate_into_their_own_buffers():
+    wl = W.Workload("host_async_acc", 40, 256, 8, 2, 128, 1)
+    wts = parity.to_device(W.make_inputs(wl, seed=7))
+    layer = _layer(wl)
+    args = (wts["router_w"], None, wts["w13"], wts["w2"])
+    xs = [W.make_inputs(wl, seed=90 + i, experts=False)["x"].pin_memory() for i in range(3)]
+    plain = [layer.forward(x.cuda(), *args).float().cpu() for x in xs]
+    layer.sync()
+    g = torch.Generator().manual_seed(3)
+    y0 = [torch.randn((wl.T, wl.H), generator=g).to(torch.bfloat16) for _ in xs]
+    ys = [y.clone().pin_memory() for y in y0]
+    layer.set_accumulate(True)
+    for x, y in zip(xs, ys):
+        layer.forward_host(x, *args, out_host=y, wait=False)
+    layer.sync()
+    for y, a, p_ in zip(ys, y0, plain):
+        want = a.float() + p_
+        err = (y.float() - want).abs().max().item() / want.abs().max().item()
+        assert err <= 1e-2
+    layer.close()
+
+
 def test_invalid_arguments_are_rejected_without_poisoning_the_handle():
     wl = W.Workload("args", 16, 256, 8, 2, 128, 2)
     dev = parity.to_device(W.make_inputs(wl, seed=5))

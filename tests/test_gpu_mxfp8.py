@@ -188,6 +188,26 @@ def test_mxfp8_denoise_workload_matches_the_oracle():
     _check(wl, inp, y, w13_q, w2_q, rows=np.arange(0, wl.T, 512), cover=True)
 
 
+def test_mxfp8_async_host_calls_match_device_calls():
+    """moe_forward_mxfp8_host_async on both batch sizes, back to back on pinned
+    buffers, equals moe_forward_mxfp8 on the same inputs."""
+    wl = W.Workload("mx_host_async", 120, 512, 16, 4, 256, 1)
+    wts = parity.to_device(W.make_inputs(wl, seed=2))
+    w13_q, w2_q = _quantize_experts(wts)
+    layer = binding.MoELayer(wl.H, wl.E, wl.k, wl.I, 1, max_tokens=wl.T)
+    sizes = [8, 120, 16, 70]
+    xs = [W.make_inputs(wl, seed=40 + i, T=T, experts=False)["x"].pin_memory() for i, T in enumerate(sizes)]
+    ys = [torch.empty_like(x).pin_memory() for x in xs]
+    for x, y in zip(xs, ys):
+        layer.forward_mxfp8(x, wts["router_w"], None, w13_q, w2_q, out=y, host_async=True)
+    layer.sync()
+    for T, x, y in zip(sizes, xs, ys):
+        ref = layer.forward_mxfp8(x.cuda(), wts["router_w"], None, w13_q, w2_q)
+        layer.sync()
+        assert torch.equal(y, ref.cpu()), f"T={T}: async host result differs from the device call"
+    layer.close()
+
+
 def test_mxfp8_rejects_h_larger_than_the_token_row_workspace():
     """n_micro * I * 33/32 > 2H: the MXFP8 copy of h does not fit where the
     token rows were, so batches above 16 tokens are refused; 16 tokens run."""
