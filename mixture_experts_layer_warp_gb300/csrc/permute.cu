@@ -108,12 +108,16 @@ __global__ void __launch_bounds__(kPlaceWarps * 32) place_kernel(PlaceArgs a) {
 // blocks < b) without a separate pass; block 0 also writes the offsets, the
 // tile prefixes and the shared expert's segment. The placement is the same
 // stable warp-round placement as place_kernel.
-constexpr int kSumParts = kPlaceWarps * 32 / kMaxExperts;  // 4 threads per expert sum the rows
+// 8 warps (32 measured slower: the per-expert scans and sums then take longer
+// than the rounds they save).
+constexpr int kSPWarps = 8;
+constexpr int kSumParts = kSPWarps * 32 / kMaxExperts;  // 4 threads per expert sum the rows
+constexpr int kSPIds = kRouterTokensTc * kMaxTopK / (kSPWarps * 32);  // ids per thread
 
-__global__ void __launch_bounds__(kPlaceWarps * 32) scan_place_kernel(ScanArgs sa, PlaceArgs a) {
+__global__ void __launch_bounds__(kSPWarps * 32) scan_place_kernel(ScanArgs sa, PlaceArgs a) {
     __shared__ int sid[kRouterTokensTc * kMaxTopK];
-    __shared__ int cnt[kPlaceWarps][kMaxExperts];
-    __shared__ int run[kPlaceWarps][kMaxExperts];
+    __shared__ int cnt[kSPWarps][kMaxExperts];
+    __shared__ int run[kSPWarps][kMaxExperts];
     __shared__ int tot_part[kSumParts][kMaxExperts];
     __shared__ int bef_part[kSumParts][kMaxExperts];
     __shared__ int off[kMaxExperts + 1];
@@ -124,12 +128,18 @@ __global__ void __launch_bounds__(kPlaceWarps * 32) scan_place_kernel(ScanArgs s
     const int64_t r0 = (int64_t)b * a.tok_per_blk * a.k;
     const int64_t left = R - r0;
     const int n = (int)(left < (int64_t)a.tok_per_blk * a.k ? left : (int64_t)a.tok_per_blk * a.k);
-    for (int i = tid; i < n; i += blockDim.x) sid[i] = a.ids[r0 + i];
     {
+        // the block's ids and the histogram rows, all loads in flight together
+        int ids[kSPIds];
+#pragma unroll
+        for (int u = 0; u < kSPIds; ++u) {
+            const int i = tid + u * kSPWarps * 32;
+            ids[u] = i < n ? a.ids[r0 + i] : 0;
+        }
         const int e = tid % kMaxExperts, q = tid / kMaxExperts;
         int tot = 0, bef = 0;
         if (e < E) {
-#pragma unroll 16
+#pragma unroll 4
             for (int row = q; row < NB; row += kSumParts) {
                 const int v = sa.blk_hist[(int64_t)row * E + e];
                 tot += v;
@@ -138,6 +148,11 @@ __global__ void __launch_bounds__(kPlaceWarps * 32) scan_place_kernel(ScanArgs s
         }
         tot_part[q][e] = tot;
         bef_part[q][e] = bef;
+#pragma unroll
+        for (int u = 0; u < kSPIds; ++u) {
+            const int i = tid + u * kSPWarps * 32;
+            if (i < n) sid[i] = ids[u];
+        }
     }
     __syncthreads();
     if (tid < 32) {
@@ -203,7 +218,7 @@ __global__ void __launch_bounds__(kPlaceWarps * 32) scan_place_kernel(ScanArgs s
         base[tid] = bef;
     }
     __syncthreads();
-    place_chunk<kPlaceWarps>(sid, n, r0, E, R, [&](int e) { return base[e]; }, cnt, run, a.perm, a.inv, a.err);
+    place_chunk<kSPWarps>(sid, n, r0, E, R, [&](int e) { return base[e]; }, cnt, run, a.perm, a.inv, a.err);
     ptx::griddep_launch_dependents();
 }
 
@@ -269,7 +284,7 @@ cudaError_t launch_place(const PlaceArgs& a, cudaStream_t s) {
 cudaError_t launch_scan_place(const ScanArgs& sa, const PlaceArgs& a, cudaStream_t s) {
     if (a.NB == 0) return cudaSuccess;
     if ((int64_t)a.NB * a.E > kScanPlaceMaxInts) return cudaErrorInvalidValue;
-    return launch_kernel(scan_place_kernel, dim3(a.NB), dim3(kPlaceWarps * 32), 0, s, true, sa, a);
+    return launch_kernel(scan_place_kernel, dim3(a.NB), dim3(kSPWarps * 32), 0, s, true, sa, a);
 }
 
 cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s) {

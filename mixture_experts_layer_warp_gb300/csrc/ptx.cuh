@@ -526,6 +526,18 @@ __host__ __device__ constexpr uint32_t idesc_mx(int M, int N, int sfa_id, int sf
            (uint32_t(sfa_id) << 29);
 }
 
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// from this CTA's shared memory to another CTA's (a shared::cluster address),
+// completing on that CTA's barrier (a shared::cluster address). The source
+// must be written and fenced (fence_proxy_async_smem) before the copy.
+__device__ __forceinline__ void bulk_copy_s2c(uint32_t dst_cluster, uint32_t src, uint32_t bytes,
+                                              uint32_t bar_cluster) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst_cluster),
+                 "r"(src), "r"(bytes), "r"(bar_cluster)
+                 : "memory");
+}
+
 // 5D tiled load completing on this CTA's own barrier.
 __device__ __forceinline__ void tma_load_5d(uint32_t dst, const void* tmap, int32_t c0, int32_t c1, int32_t c2,
                                             int32_t c3, int32_t c4, uint32_t bar) {

@@ -649,8 +649,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
 // partials to the CTA that owns the slice (st.async completing bytes on the
 // owner's exchange barrier), and CTA r combines the eight partials of tokens
 // 32r .. 32r+31 in the same compensated order as router_tc_kernel: the logits
-// are bit-identical to the other kernels'. Four threads per token select the
-// top-k. The four CTAs add their expert counts into CTA 0 (shared-memory
+// are bit-identical to the other kernels'. Eight threads per token (256 per
+// CTA; warps 4-7 wait out the loads) select the top-k. The four CTAs add their expert counts into CTA 0 (shared-memory
 // reductions across the cluster), which writes the 128-token block's histogram
 // row, as router_tc_kernel does.
 constexpr int kSplit = 4;
@@ -659,9 +659,16 @@ constexpr int kSPartsPer = kParts / kSplit;           // 2 partials accumulated 
 constexpr int kSStages = 6;
 constexpr int kSRecvBytes = kParts * kSplitTok * kN * 4;   // [partial][token][expert] fp32: 64 KB
 constexpr int kSSendBytes = kSPartsPer * kSplitTok * kN * 4;  // one CTA's contribution to a slice: 16 KB
-constexpr int kSGroup = kThreads / kSplitTok;         // 4 threads per token in the top-k
-constexpr int kSPer = kN / kSGroup;                   // 16 experts per thread
-static_assert(kSplitTok == 32 && kSGroup == 4, "one TMEM lane quarter per destination CTA");
+constexpr int kSThreads = 256;                        // warps 4-7 join for the combine and the top-k
+constexpr int kSGroup = kSThreads / kSplitTok;        // 8 threads per token in the top-k
+constexpr int kSPer = kN / kSGroup;                   // 8 experts per thread
+static_assert(kSplitTok == 32 && kSGroup == 8, "32 tokens combined per CTA, 8 threads each");
+static_assert(kSplit * kSSendBytes <= kSStages * kStageBytes, "send slices staged in the load ring");
+
+// The float4 slot of logits 4q .. 4q+3 within row `row` of a received slice:
+// XOR-swizzled by the row, so that the 32 rows written one per lane and the
+// 8 float4 of a token read by its 8 threads fall in distinct banks.
+__device__ __forceinline__ int recv_q(int q, int row) { return q ^ (row & 15); }
 
 struct SCtl {
     uint64_t full[kSStages];
@@ -675,7 +682,7 @@ struct SCtl {
 };
 constexpr int kSSmemBytes = kSStages * kStageBytes + kSRecvBytes + (int)sizeof(SCtl) + 1024;
 
-__global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kSThreads, 1)
     router_tc_split_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                            const RouterTcArgs a) {
     ptx::griddep_launch_dependents();
@@ -806,32 +813,37 @@ __global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     ptx::cluster_wait();   // every CTA's exchange barrier is armed before anyone sends
 
-    // warp w holds TMEM lanes 32w.. = the tokens CTA w combines: send both
+    // warp w < 4 holds TMEM lanes 32w.. = the tokens CTA w combines: send both
     // partials of each of them there (partial slot 2 rank + j of its buffer).
     // Every CTA sends, also one without K-blocks (H < 512): the owner expects
-    // the bytes and skips the partials that do not exist.
-    if (ready) {
+    // the bytes and skips the partials that do not exist. A slice for another
+    // CTA is written in the owner's layout into the (now idle) load ring and
+    // goes over in one bulk copy.
+    if (warp >= 4) {
+    } else if (ready) {
         const int dst_cta = warp;
         const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        float* slice = dst_cta == rank ? recv + (size_t)kSPartsPer * rank * kSplitTok * kN
+                                       : reinterpret_cast<float*>(smem) + (size_t)warp * (kSSendBytes / 4);
 #pragma unroll
         for (int j = 0; j < kSPartsPer; ++j) {
             uint32_t v[kN];
             const uint32_t b = lane_base + (uint32_t)(j * kN);
             ptx::tmem_ld16x4(b, b + 16u, b + 32u, b + 48u, v);
-            float* mine = recv + ((size_t)(kSPartsPer * rank + j) * kSplitTok + lane) * kN;
-            if (dst_cta == rank) {
+            float4* row = reinterpret_cast<float4*>(slice + ((size_t)j * kSplitTok + lane) * kN);
 #pragma unroll
-                for (int q = 0; q < kN / 4; ++q)
-                    reinterpret_cast<float4*>(mine)[q] = make_float4(
-                        __uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]), __uint_as_float(v[4 * q + 2]),
-                        __uint_as_float(v[4 * q + 3]));
-            } else {
-                const uint32_t dst = ptx::map_to_rank(ptx::smem_u32(mine), (uint32_t)dst_cta);
-                const uint32_t bar = ptx::map_to_rank(xfer, (uint32_t)dst_cta);
-#pragma unroll
-                for (int q = 0; q < kN / 4; ++q)
-                    ptx::st_async_v4(dst + 16u * q, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3], bar);
-            }
+            for (int q = 0; q < kN / 4; ++q)
+                row[recv_q(q, lane)] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                                   __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+        }
+        if (dst_cta != rank) {
+            ptx::fence_proxy_async_smem();  // the slice, visible to the bulk copy
+            __syncwarp();
+            if (lane == 0)
+                ptx::bulk_copy_s2c(ptx::map_to_rank(ptx::smem_u32(recv + (size_t)kSPartsPer * rank * kSplitTok * kN),
+                                                    (uint32_t)dst_cta),
+                                   ptx::smem_u32(slice), (uint32_t)kSSendBytes,
+                                   ptx::map_to_rank(xfer, (uint32_t)dst_cta));
         }
     } else if (lane == 0) {
         atomicOr(a.err, kErrTimeout);
@@ -851,17 +863,19 @@ __global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kThreads, 1)
     const int64_t t = (int64_t)t0 + kSplitTok * rank + r;
     if (go && t < a.T) {
         // thread (token r, group position g) owns experts 16g .. 16g+15
-        const unsigned gmask = 0xfu << (lane & ~(kSGroup - 1));
+        const unsigned gmask = ((1u << kSGroup) - 1u) << (lane & ~(kSGroup - 1));
         float l[kSPer];
         {
             float sum[kSPer], comp[kSPer];
 #pragma unroll
             for (int i = 0; i < kSPer; ++i) sum[i] = comp[i] = 0.f;
-            for (int p = 0; p < nparts; ++p) {  // partials in order 0..7, as router_tc_kernel
-                const float4* src = reinterpret_cast<const float4*>(recv + ((size_t)p * kSplitTok + r) * kN + g * kSPer);
+#pragma unroll
+            for (int p = 0; p < kParts; ++p) {  // partials in order 0..7, as router_tc_kernel
+                if (p >= nparts) break;
+                const float4* src = reinterpret_cast<const float4*>(recv + ((size_t)p * kSplitTok + r) * kN);
 #pragma unroll
                 for (int q = 0; q < kSPer / 4; ++q) {
-                    const float4 v = src[q];
+                    const float4 v = src[recv_q(g * (kSPer / 4) + q, r)];
                     kahan_add(sum[4 * q], comp[4 * q], v.x);
                     kahan_add(sum[4 * q + 1], comp[4 * q + 1], v.y);
                     kahan_add(sum[4 * q + 2], comp[4 * q + 2], v.z);
@@ -955,10 +969,10 @@ __global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kThreads, 1)
 // here waits for it (griddep_wait) after its shared-memory and TMEM set-up.
 template <typename K>
 cudaError_t launch_early(K kernel, dim3 grid, int smem, cudaStream_t s, const CUtensorMap& tmX,
-                         const CUtensorMap& tmW, const RouterTcArgs& a) {
+                         const CUtensorMap& tmW, const RouterTcArgs& a, int threads = kThreads) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = (size_t)smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -984,7 +998,7 @@ cudaError_t launch_router_tc_split(const RouterTcArgs& a, const CUtensorMap& tmX
     const int nb = (a.T + kTok - 1) / kTok;
     if (nb == 0) return cudaSuccess;
     if (cudaError_t e = ensure_smem_limit<router_tc_split_kernel>(kSSmemBytes); e != cudaSuccess) return e;
-    return launch_early(router_tc_split_kernel, dim3(nb * kSplit), kSSmemBytes, s, tmX, tmW, a);
+    return launch_early(router_tc_split_kernel, dim3(nb * kSplit), kSSmemBytes, s, tmX, tmW, a, kSThreads);
 }
 
 cudaError_t launch_router_tc_small(const RouterTcArgs& a, const CUtensorMap& tmX, const CUtensorMap& tmW,
