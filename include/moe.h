@@ -204,11 +204,8 @@ moe_status moe_quantize_mxfp8(const void *w, int64_t groups, int32_t rows, int32
  * moe_forward with MXFP8 routed-expert weights: w13_codes[m] / w13_scales[m]
  * and w2_codes[m] / w2_scales[m] as produced by moe_quantize_mxfp8 (device
  * pointers, 16-byte aligned). Supported for bf16 layers (whose hidden and
- * inter sizes, multiples of 256 and 128, fill its 128-deep K stages); for
- * T > 16 the MXFP8 copy of h must fit the workspace of the gathered token
- * rows, n_micro * inter * 33/32 <= 2 * hidden (about), else the call returns
- * MOE_ERR_UNSUPPORTED. Other arguments, ownership, the accumulate switch and
- * errors as for moe_forward.
+ * inter sizes, multiples of 256 and 128, fill its 128-deep K stages). Other
+ * arguments, ownership, the accumulate switch and errors as for moe_forward.
  */
 moe_status moe_forward_mxfp8(moe_handle *h, const void *x, const void *router_w,
                              const float *router_bias, const void *const *w13_codes,
@@ -267,8 +264,8 @@ const char *moe_status_string(moe_status s);
  * call. which: 0 = gathered input xp [T*k][H], 1 = SwiGLU output h [T*k][n_micro*I],
  * 2 = expert outputs o [T*k][H], 3 = inverse permutation [T*k] int32,
  * 4 = device error word (int32). Returns NULL for an unknown `which`. After a
- * moe_forward_mxfp8 call with T > 16, region 0 holds the MXFP8 codes of h
- * [T*k][n_micro*I] (uint8) instead of xp.
+ * moe_forward_mxfp8 call with T > 16, regions 0 and 1 hold the MXFP8 codes
+ * (uint8) of xp [T*k][H] and of h [T*k][n_micro*I].
  */
 void *moe_workspace_ptr(const moe_handle *h, int32_t which);
 
@@ -280,10 +277,11 @@ void *moe_workspace_ptr(const moe_handle *h, int32_t which);
  * writes, per kernel slot, the summed duration in milliseconds and the number
  * of launches. Slots: 0 router, 1 scan, 2 place, 3 gather (with MXFP8 expert
  * weights and T > 16: gather and MXFP8 quantisation of the token rows),
- * 4 GEMM1 (+SwiGLU), 5 GEMM2, 6 shared-expert GEMM1, 7 shared-expert GEMM2,
- * 8 finalize, 9 MXFP8 quantisation of h (MXFP8 expert weights, T > 16).
+ * 4 GEMM1 (+SwiGLU; with MXFP8 expert weights and T > 16 also the MXFP8
+ * quantisation of h), 5 GEMM2, 6 shared-expert GEMM1, 7 shared-expert GEMM2,
+ * 8 finalize.
  */
-#define MOE_PROFILE_SLOTS 10
+#define MOE_PROFILE_SLOTS 9
 moe_status moe_profile_begin(moe_handle *h, int32_t max_calls);
 moe_status moe_profile_end(moe_handle *h, float *ms /* [MOE_PROFILE_SLOTS] */,
                            int32_t *launches /* [MOE_PROFILE_SLOTS] */);

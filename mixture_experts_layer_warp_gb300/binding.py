@@ -322,7 +322,7 @@ class MoELayer:
         self._check(self._lib.moe_sync(self._h))
 
     PROFILE_SLOTS = ("router", "scan", "place", "gather", "gemm1_swiglu", "gemm2_down", "shared_gemm1",
-                     "shared_gemm2", "finalize", "quantize_h")
+                     "shared_gemm2", "finalize")
 
     def profile_begin(self, max_calls: int):
         """Start per-kernel event timing for the next ``max_calls`` calls."""

@@ -55,4 +55,30 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 __device__ __forceinline__ float silu(float z) { return z / (1.f + __expf(-z)); }
 
+// MXFP8 of activations (OCP Microscaling, the rule of the weights' quantiser):
+// per 32-element block, shared exponent floor(log2(max |v|)) - 8 clamped to
+// [-127, 127] (0 for an all-zero block), codes E4M3 of v / 2^shared (nearest,
+// ties to even, saturating at +-448), scale byte shared + 127.
+
+// 2^k as an fp32 for k in [-127, 127] (2^-127 is subnormal).
+__device__ __forceinline__ float pow2f(int k) {
+    return k >= -126 ? __uint_as_float((uint32_t)(k + 127) << 23) : __uint_as_float(1u << (k + 149));
+}
+
+// The block's shared exponent from its largest magnitude.
+__device__ __forceinline__ int mx_shared_exp(float amax) {
+    if (!(amax > 0.f)) return 0;
+    int ex;
+    frexpf(amax, &ex);  // amax = f * 2^ex, f in [0.5, 1): floor(log2 amax) = ex - 1
+    return min(max(ex - 1 - 8, -127), 127);
+}
+
+// E4M3 codes of (lo, hi) in bytes 0 and 1 (the instruction converts its
+// first source into the upper byte).
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+    uint16_t pair;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(hi), "f"(lo));
+    return pair;
+}
+
 }  // namespace moe

@@ -110,6 +110,10 @@ struct Ctl {
 // conflicts; GEMM1: 32 tokens x 16 features of bf16).
 constexpr int kEpiFloats = 32 * 33;
 constexpr int kEpiBytes = 4 * kEpiFloats * 4;
+// MXFP8 SwiGLU epilogue: past the warp's 32 x 16 bf16 of h, two slots of 32
+// per-token |max| read by the partner warp
+constexpr int kEpiAmaxOff = 32 * 16 / 2;
+static_assert(kEpiAmaxOff + 64 <= kEpiFloats, "epilogue staging");
 
 template <bool MX>
 constexpr int smem_bytes() {
@@ -527,6 +531,9 @@ __global__ void __launch_bounds__(Cfg<MX>::kThreads, 1)
             if (lane == 0)
                 ready = ptx::mbar_wait(ptx::smem_u32(&c.tfull[acc]), acc_par, a.limit_ns, &c.abort);
             ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
+            // the MXFP8 SwiGLU epilogue pairs warps q and q^1 at a named barrier
+            // per 32 tokens: they take the tile, or leave, together
+            if (MX && SWIGLU) ready = ptx::named_barrier_and(1 + (q >> 1), 64, ready);
             if (!ready) {
                 if (lane == 0) fail(c, a.err);
                 break;
@@ -540,7 +547,7 @@ __global__ void __launch_bounds__(Cfg<MX>::kThreads, 1)
                 const bool is_gate = lane < 16;
                 __nv_bfloat16* hb = reinterpret_cast<__nv_bfloat16*>(buf);  // [32 tokens][16 features]
 #pragma unroll 1
-                for (int c0 = 0; c0 < t.n; c0 += 32) {
+                for (int c0 = 0, it = 0; c0 < t.n; c0 += 32, ++it) {
                     uint32_t v[32];
                     ptx::tmem_ld32(tbase + c0, v);
 #pragma unroll
@@ -553,12 +560,53 @@ __global__ void __launch_bounds__(Cfg<MX>::kThreads, 1)
                         hb[32 * i + lane] = __float2bfloat16_rn(h);
                     }
                     __syncwarp();
+                    if (MX) {
+                        // MXFP8 of h: lane = token; this warp holds features 16 (q%2) .. +16
+                        // of block q/2 of the CTA's 64, the partner warp q^1 the other 16:
+                        // each posts its per-token |max| (two slots by chunk parity) and
+                        // the pair meets at a named barrier
+                        const uint4* hr = reinterpret_cast<const uint4*>(hb + lane * 16);
+                        const uint4 p0 = hr[0], p1 = hr[1];
+                        const __nv_bfloat162* hv0 = reinterpret_cast<const __nv_bfloat162*>(&p0);
+                        const __nv_bfloat162* hv1 = reinterpret_cast<const __nv_bfloat162*>(&p1);
+                        float2 f[8];
+                        float am = 0.f;
 #pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        const int piece = lane + 32 * j, tok = piece >> 1, half = piece & 1;
-                        const uint4 u = *reinterpret_cast<const uint4*>(hb + tok * 16 + half * 8);
-                        if (c0 + tok < t.len)
-                            *reinterpret_cast<uint4*>(out + (int64_t)(t.start + c0 + tok) * a.out_ld + feat0 + half * 8) = u;
+                        for (int i = 0; i < 4; ++i) {
+                            f[i] = __bfloat1622float2(hv0[i]);
+                            f[4 + i] = __bfloat1622float2(hv1[i]);
+                        }
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) am = fmaxf(am, fmaxf(fabsf(f[i].x), fabsf(f[i].y)));
+                        float* amx = buf + kEpiAmaxOff;
+                        amx[(it & 1) * 32 + lane] = am;
+                        ptx::named_barrier_sync(1 + (q >> 1), 64);
+                        am = fmaxf(am, epi_buf[(q ^ 1) * kEpiFloats + kEpiAmaxOff + (it & 1) * 32 + lane]);
+                        const int shared = mx_shared_exp(am);
+                        const float sc = pow2f(-shared);  // exact: a power-of-two scaling
+                        uint32_t w[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            w[i] = e4m3x2(f[2 * i].x * sc, f[2 * i].y * sc) |
+                                   (e4m3x2(f[2 * i + 1].x * sc, f[2 * i + 1].y * sc) << 16);
+                        if (c0 + lane < t.len) {
+                            const int64_t row = t.start + c0 + lane;
+                            unsigned char* codes = static_cast<unsigned char*>(a.out);
+                            *reinterpret_cast<uint4*>(codes + row * a.out_ld + feat0) = make_uint4(w[0], w[1], w[2], w[3]);
+                            if ((q & 1) == 0) {  // one scale byte per block: K block feat0/32 of the row
+                                const int kblk = feat0 / 32;
+                                static_cast<unsigned char*>(a.out_scales)[((int64_t)(kblk / 4) * a.out_rows_pad + row) * 4 +
+                                                                         (kblk & 3)] = (unsigned char)(shared + 127);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) {
+                            const int piece = lane + 32 * j, tok = piece >> 1, half = piece & 1;
+                            const uint4 u = *reinterpret_cast<const uint4*>(hb + tok * 16 + half * 8);
+                            if (c0 + tok < t.len)
+                                *reinterpret_cast<uint4*>(out + (int64_t)(t.start + c0 + tok) * a.out_ld + feat0 + half * 8) = u;
+                        }
                     }
                     __syncwarp();
                 }

@@ -212,7 +212,7 @@ struct PairGemmArgs {
     int n_ftiles;             // feature tiles per (group, micro): I/128 (SwiGLU) or H/256 (plain)
     int w_rows_per_group;     // plain form: rows of W per group (H)
     int x_micro_cols;         // plain form: columns of the token rows per micro (I)
-    void* out;                // bf16
+    void* out;                // bf16 (MXFP8 SwiGLU form: the E4M3 codes of h, one byte each)
     int64_t out_ld;           // elements per output row
     int out_micro_cols;       // SwiGLU form: I (column offset of micro m in out)
     int max_tiles;            // upper bound on the tiles (sizes the grid)
@@ -220,6 +220,12 @@ struct PairGemmArgs {
     uint64_t limit_ns;
     int dense_rows;           // rows of the dense segment when seg is null
     int early;                // launch while the previous kernel in the stream finishes
+    // MXFP8 SwiGLU form: h leaves the epilogue as MXFP8 (each 32 features of a
+    // row one block, from the bf16-rounded values): codes in `out`, scale
+    // bytes stage-major [out_ld/128][out_rows_pad][4] here (launch_gather_mx
+    // layout), ready for the block-scaled down GEMM.
+    void* out_scales;
+    int64_t out_rows_pad;
 };
 // tmW[m]: SwiGLU form: w13_m [G][2I][K] as a 5D map {K, 16, 2, I/16, G} (strides
 // of a row, of the up half, of 16 rows, of a group) with box {64, 16, 2, 4, 1};
@@ -337,7 +343,7 @@ struct LaunchHook {
 };
 
 enum KernelSlot { kSlotRouter = 0, kSlotScan, kSlotPlace, kSlotGather, kSlotGemm1, kSlotGemm2, kSlotSharedGemm1,
-                  kSlotSharedGemm2, kSlotFinalize, kSlotQuantH, kNumSlots };
+                  kSlotSharedGemm2, kSlotFinalize, kNumSlots };
 
 // Returns cudaErrorInvalidValue if a tensor map cannot be encoded.
 cudaError_t enqueue_routing(const RoutingJob& j, cudaStream_t s, const LaunchHook* hook);
@@ -375,8 +381,6 @@ struct MxActArgs {
 };
 // codes[inv[t*k + j]] = MXFP8 of x[t] for every token t and slot j (x read once)
 cudaError_t launch_gather_mx(const MxActArgs& a, cudaStream_t s);
-// codes[r] = MXFP8 of src[r] for every row r
-cudaError_t launch_quantize_rows_mx(const MxActArgs& a, cudaStream_t s);
 // MXFP8 quantisation (mxfp8.cu): w [groups][rows][cols] bf16 -> codes [groups][rows][cols],
 // scales [groups][cols/32][rows]; cols % 32 == 0.
 cudaError_t launch_mx_quantize(const void* w, int64_t groups, int rows, int cols, void* codes, void* scales,

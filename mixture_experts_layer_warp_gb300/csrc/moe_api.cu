@@ -219,17 +219,16 @@ struct MxScales {
     const void* const* w2;   // [E][I/32][H] per micro
 };
 
-// Bytes of the MXFP8 form of R rows of K elements in the xp region: the codes
-// [R][K], then (256-aligned) the stage-major scale words [K/128][rows_pad][4].
+// The MXFP8 form of R rows of K elements in a workspace region: the codes
+// [R][K], then (256-aligned) the stage-major scale words [K/128][rows_pad][4]
+// (at most half the bytes of the region's bf16 rows).
 int64_t mx_rows_pad(int64_t R) { return (R + 3) / 4 * 4; }
 size_t mx_scales_off(int64_t R, int64_t K) { return round_up((size_t)(R * K), 256); }
-size_t mx_act_bytes(int64_t R, int64_t K) { return mx_scales_off(R, K) + (size_t)(K / 128) * mx_rows_pad(R) * 4; }
 
 // The routed experts of a batch of more than kSmallTokens tokens with MXFP8
 // expert weights: gather and quantise the token rows to MXFP8 (one pass over
-// x), block-scaled FP8 GEMM1 + SwiGLU into bf16 h, MXFP8 of h, block-scaled
-// FP8 GEMM2 into o. The MXFP8 token rows live in the xp region, later replaced
-// by those of h (GEMM1 has completed when the quantisation of h starts).
+// x) into the xp region, block-scaled FP8 GEMM1 + SwiGLU whose epilogue writes
+// h as MXFP8 into the h region, block-scaled FP8 GEMM2 into o.
 moe_status run_routed_mx(moe_handle* h, const void* x, const void* const* w13, const void* const* w2,
                          const MxScales& mx, int32_t T, cudaStream_t s, int early_gather) {
     const moe_config& c = h->cfg;
@@ -237,14 +236,15 @@ moe_status run_routed_mx(moe_handle* h, const void* x, const void* const* w13, c
     const int64_t R = (int64_t)T * k, rows_pad = mx_rows_pad(R), MI = (int64_t)M * I;
     const int chunk_bound = (int)(R / 208) + E;  // bound on sum over experts of ceil(count/208)
     char* q = static_cast<char*>(h->xp);
+    char* hq = static_cast<char*>(h->hbuf);
     cudaError_t e;
     CUtensorMap tmW[kMaxMicro], tmS[kMaxMicro], tmX[4], tmSB;
-    auto encode_rows = [&](int64_t K) {
+    auto encode_rows = [&](const char* base, int64_t K) {  // MXFP8 rows at base: codes, then scale words
         for (uint32_t b = 0; b < 4; ++b)
-            if (!encode_u8_2d(&tmX[b], q, K, R, K, 128, 32 * (b + 1), true)) return false;
+            if (!encode_u8_2d(&tmX[b], base, K, R, K, 128, 32 * (b + 1), true)) return false;
         const uint64_t d[3] = {16, (uint64_t)rows_pad / 4, (uint64_t)K / 128}, st[2] = {16, (uint64_t)rows_pad * 4};
         const uint32_t box[3] = {16, 65, 1};
-        return encode_3d(&tmSB, false, q + mx_scales_off(R, K), d, st, box, false);
+        return encode_3d(&tmSB, false, base + mx_scales_off(R, K), d, st, box, false);
     };
 
     MxActArgs gx{x, h->inv, R, k, H, rows_pad, q, q + mx_scales_off(R, H), h->err, h->num_sms, early_gather};
@@ -253,7 +253,7 @@ moe_status run_routed_mx(moe_handle* h, const void* x, const void* const* w13, c
     // GEMM1 + SwiGLU: codes of w13[m] [E][2I][H] as a 5D map {H, 16, 2, I/16, E}
     // (box: 4 groups of 16 gate rows and the matching up rows, 128 K), their
     // scales [E][H/32][2I] in the same row order
-    if (!encode_rows(H)) return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (MXFP8 token rows)");
+    if (!encode_rows(q, H)) return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (MXFP8 token rows)");
     for (int m = 0; m < M; ++m) {
         const uint64_t cd[5] = {(uint64_t)H, 16, 2, (uint64_t)I / 16, (uint64_t)E};
         const uint64_t cs[4] = {(uint64_t)H, (uint64_t)I * H, 16 * (uint64_t)H, 2 * (uint64_t)I * H};
@@ -265,16 +265,14 @@ moe_status run_routed_mx(moe_handle* h, const void* x, const void* const* w13, c
             !encode_nd(&tmS[m], false, mx.w13[m], 5, sd, ss, sb, false))
             return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (MXFP8 w13[%d])", m);
     }
-    PairGemmArgs g1{h->offsets, E, M, H / 128, I / 128, 0, 0, h->hbuf, MI, I,
-                    M * chunk_bound * (I / 128), h->err, h->limit_ns, 0, 1};  // early: behind the gather
+    PairGemmArgs g1{h->offsets, E, M, H / 128, I / 128, 0, 0, hq, MI, I,
+                    M * chunk_bound * (I / 128), h->err, h->limit_ns, 0, 1,  // early: behind the gather
+                    hq + mx_scales_off(R, MI), rows_pad};
     if ((e = timed(h, kSlotGemm1, s, [&] { return launch_pair_gemm_swiglu_mx(g1, tmW, tmX, tmS, tmSB, s); })) !=
         cudaSuccess)
         return cuda_err(h, e, "MXFP8 GEMM1 launch");
-    MxActArgs gh{h->hbuf, nullptr, R, 1, (int)MI, rows_pad, q, q + mx_scales_off(R, MI), h->err, h->num_sms, 1};
-    if ((e = timed(h, kSlotQuantH, s, [&] { return launch_quantize_rows_mx(gh, s); })) != cudaSuccess)
-        return cuda_err(h, e, "MXFP8 quantisation of h launch");
     // GEMM2: codes of w2[m] [E*H][I] (128-row boxes), scales [E][I/32][H]
-    if (!encode_rows(MI)) return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (MXFP8 h)");
+    if (!encode_rows(hq, MI)) return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (MXFP8 h)");
     for (int m = 0; m < M; ++m) {
         const uint64_t sd[3] = {(uint64_t)H, (uint64_t)I / 32, (uint64_t)E}, ss[2] = {(uint64_t)H, (uint64_t)I / 32 * H};
         const uint32_t sb[3] = {128, 4, 1};
@@ -283,7 +281,7 @@ moe_status run_routed_mx(moe_handle* h, const void* x, const void* const* w13, c
             return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (MXFP8 w2[%d])", m);
     }
     PairGemmArgs g2{h->offsets, E, M, I / 128, H / 256, H, I, h->obuf, (int64_t)H, 0,
-                    chunk_bound * (H / 256), h->err, h->limit_ns, 0, 1};  // early: behind the quantisation
+                    chunk_bound * (H / 256), h->err, h->limit_ns, 0, 1};  // early: behind GEMM1
     if ((e = timed(h, kSlotGemm2, s, [&] { return launch_pair_gemm_down_mx(g2, tmW, tmX, tmS, tmSB, s); })) !=
         cudaSuccess)
         return cuda_err(h, e, "MXFP8 GEMM2 launch");
@@ -588,17 +586,8 @@ moe_status host_call(moe_handle* h, const void* x_host, int32_t T, void* y_host,
 
 moe_status check_mxfp8(moe_handle* h, const void* const* w13_codes, const void* const* w13_scales,
                        const void* const* w2_codes, const void* const* w2_scales, int32_t n_micro, int32_t top_k,
-                       const void* shared_w13, const void* shared_w2, int32_t T, const void* y) {
+                       const void* shared_w13, const void* shared_w2, const void* y) {
     if (h->cfg.dtype != MOE_BF16) return set_err(h, MOE_ERR_UNSUPPORTED, "MXFP8 expert weights need a bf16 layer");
-    if (T > kSmallTokens) {
-        // the MXFP8 rows of h replace those of the token rows in the xp region
-        const moe_config& c = h->cfg;
-        const int64_t R = (int64_t)T * c.top_k;
-        const size_t cap = (size_t)c.max_tokens * c.top_k * c.hidden * h->esz;
-        if (mx_act_bytes(R, (int64_t)c.n_micro * c.inter) > cap)
-            return set_err(h, MOE_ERR_UNSUPPORTED,
-                           "MXFP8 expert weights with T > %d need n_micro * inter * 33/32 <= 2 * hidden", kSmallTokens);
-    }
     moe_status st = check_weights(h, w13_codes, w2_codes, n_micro, top_k, shared_w13, shared_w2, y);
     if (st != MOE_OK) return st;
     if (w13_scales == nullptr || w2_scales == nullptr)
@@ -769,7 +758,7 @@ moe_status moe_forward_mxfp8(moe_handle* h, const void* x, const void* router_w,
     if (st != MOE_OK) return st;
     if (h->cfg.dtype != MOE_BF16) return set_err(h, MOE_ERR_UNSUPPORTED, "MXFP8 expert weights need a bf16 layer");
     if (T == 0) return MOE_OK;
-    st = check_mxfp8(h, w13_codes, w13_scales, w2_codes, w2_scales, n_micro, top_k, shared_w13, shared_w2, T, y);
+    st = check_mxfp8(h, w13_codes, w13_scales, w2_codes, w2_scales, n_micro, top_k, shared_w13, shared_w2, y);
     if (st != MOE_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     h->last_stream = s;
@@ -790,7 +779,7 @@ moe_status moe_forward_mxfp8_host_async(moe_handle* h, const void* x_host, const
     if (h->cfg.dtype != MOE_BF16) return set_err(h, MOE_ERR_UNSUPPORTED, "MXFP8 expert weights need a bf16 layer");
     if (T == 0) return MOE_OK;
     if (x_host == nullptr || y_host == nullptr) return set_err(h, MOE_ERR_INVALID_ARG, "host x and y must be non-null");
-    st = check_mxfp8(h, w13_codes, w13_scales, w2_codes, w2_scales, n_micro, top_k, shared_w13, shared_w2, T,
+    st = check_mxfp8(h, w13_codes, w13_scales, w2_codes, w2_scales, n_micro, top_k, shared_w13, shared_w2,
                      h->y_stage[0]);
     if (st != MOE_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

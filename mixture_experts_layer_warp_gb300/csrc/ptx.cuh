@@ -259,6 +259,24 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 // memory operations are visible.
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Named barrier `id` (1..15; 0 is __syncthreads) over `count` threads (a
+// multiple of 32, whole warps). Every participating warp must reach it: use
+// it only where all of them run the same iterations, after agreeing with
+// named_barrier_and on whether to run them.
+__device__ __forceinline__ void named_barrier_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+// The same barrier returning the AND of `pred` over the participating threads.
+__device__ __forceinline__ bool named_barrier_and(int id, int count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.and.pred p, %2, %3, q;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
 // Whole-cluster barrier with release/acquire semantics on shared::cluster data.
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
