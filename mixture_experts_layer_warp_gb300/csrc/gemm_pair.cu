@@ -135,34 +135,72 @@ __device__ __forceinline__ int token_box(const PairTile& t) { return (t.n / 2 + 
 
 // Chunks of one group: ceil(rows / chunk) of near-equal length, so no chunk
 // is a nearly empty remainder (the weight bytes of a tile do not shrink with N).
-template <bool SWIGLU>
-__device__ __forceinline__ PairTile decode_pair_tile(int tile, const Ctl& c, const PairGemmArgs& a) {
+__device__ __forceinline__ PairTile make_tile(int g, int m, int f, int ch, int C, const Ctl& c) {
     PairTile t;
-    const int per = (SWIGLU ? a.n_micro : 1) * a.n_ftiles;  // tiles per chunk
+    t.g = g;
+    t.m = m;
+    t.f = f;
+    const int rows = c.seg[g + 1] - c.seg[g];
+    const int base = rows / C, rem = rows % C;
+    t.start = c.seg[g] + ch * base + min(ch, rem);
+    t.len = base + (ch < rem ? 1 : 0);
+    t.n = (t.len + 15) & ~15;
+    return t;
+}
+
+// A pair's walk over its tiles: tiles pair, pair + npairs, ... of the global
+// order group -> block of a.chunk_block chunks -> micro -> feature tile ->
+// chunk within the block. The pairs running at once take consecutive tiles,
+// which share a weight tile and (within a block) token rows through L2; every
+// pair gets the same number of tiles within one. A block's token rows stay in
+// L2 while every weight tile of the group passes over them, where a group of
+// many chunks (the shared expert's dense segment) would otherwise stream all
+// its rows once per feature tile. (Handing each pair whole units of one weight
+// tile over consecutive chunks instead tripled the DRAM traffic of the CFG
+// GEMMs: the pairs then stream several experts' rows at once.)
+struct Walk {
+    int tile;
+    PairTile t;
+};
+
+template <bool SWIGLU>
+__device__ __forceinline__ bool walk_load(Walk& w, const Ctl& c, const PairGemmArgs& a) {
+    const int per = (SWIGLU ? a.n_micro : 1) * a.n_ftiles;  // tiles of a chunk (micros x feature tiles)
+    if (w.tile >= per * c.chunks[a.G]) return false;
     int lo = 0, hi = a.G - 1;  // largest g with chunks[g] * per <= tile
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (c.chunks[mid] * per <= tile)
+        if (c.chunks[mid] * per <= w.tile)
             lo = mid;
         else
             hi = mid - 1;
     }
-    t.g = lo;
     const int C = c.chunks[lo + 1] - c.chunks[lo];
-    int local = tile - c.chunks[lo] * per;
-    t.m = 0;
+    int local = w.tile - c.chunks[lo] * per;
+    const int Bc = a.chunk_block > 0 && a.chunk_block < C ? a.chunk_block : C;
+    const int b = local / (Bc * per) < (C - 1) / Bc ? local / (Bc * per) : (C - 1) / Bc;
+    local -= b * Bc * per;
+    const int cb = C - b * Bc < Bc ? C - b * Bc : Bc;  // chunks in this block
+    int m = 0;
     if (SWIGLU) {
-        t.m = local / (a.n_ftiles * C);
-        local -= t.m * a.n_ftiles * C;
+        m = local / (a.n_ftiles * cb);
+        local -= m * a.n_ftiles * cb;
     }
-    t.f = local / C;
-    const int ch = local - t.f * C;
-    const int rows = c.seg[lo + 1] - c.seg[lo];
-    const int base = rows / C, rem = rows % C;
-    t.start = c.seg[lo] + ch * base + min(ch, rem);
-    t.len = base + (ch < rem ? 1 : 0);
-    t.n = (t.len + 15) & ~15;
-    return t;
+    const int f = local / cb;
+    w.t = make_tile(lo, m, f, b * Bc + local - f * cb, C, c);
+    return true;
+}
+
+template <bool SWIGLU>
+__device__ __forceinline__ bool walk_first(Walk& w, int pair, const Ctl& c, const PairGemmArgs& a) {
+    w.tile = pair;
+    return walk_load<SWIGLU>(w, c, a);
+}
+
+template <bool SWIGLU>
+__device__ __forceinline__ bool walk_next(Walk& w, int npairs, const Ctl& c, const PairGemmArgs& a) {
+    w.tile += npairs;
+    return walk_load<SWIGLU>(w, c, a);
 }
 
 __device__ __forceinline__ void fail(Ctl& c, int* err) {
@@ -257,7 +295,6 @@ __global__ void __launch_bounds__(Cfg<MX>::kThreads, 1)
     ptx::tc_fence_after();
 
     const uint32_t tmem = c.tmem_base;
-    const int total = (SWIGLU ? a.n_micro : 1) * c.chunks[a.G] * a.n_ftiles;
     const int n_micro_k = SWIGLU ? 1 : a.n_micro;
 
     // The producer and MMA roles run as whole warps: every lane takes part in
@@ -273,8 +310,9 @@ __global__ void __launch_bounds__(Cfg<MX>::kThreads, 1)
         uint32_t last_par[kStages];
         int issued = 0;
         bool ok = true;
-        for (int tile = pair; ok && tile < total; tile += npairs) {
-            const PairTile t = decode_pair_tile<SWIGLU>(tile, c, a);
+        Walk w;
+        for (bool more = walk_first<SWIGLU>(w, pair, c, a); ok && more; more = walk_next<SWIGLU>(w, npairs, c, a)) {
+            const PairTile t = w.t;
             const int half = t.n / 2;               // token rows held by each CTA
             const int box = token_box(t);
             const CUtensorMap* tx = box == 0 ? &tmX0 : box == 1 ? &tmX1 : box == 2 ? &tmX2 : &tmX3;
@@ -336,8 +374,10 @@ __global__ void __launch_bounds__(Cfg<MX>::kThreads, 1)
         bool ok = true;
         int local = 0;
         int sfi = 0;  // MX: stages consumed, which picks the scale-factor buffer and its phase
-        for (int tile = pair; ok && tile < total; tile += npairs, ++local) {
-            const PairTile t = decode_pair_tile<SWIGLU>(tile, c, a);
+        Walk w;
+        for (bool more = walk_first<SWIGLU>(w, pair, c, a); ok && more;
+             more = walk_next<SWIGLU>(w, npairs, c, a), ++local) {
+            const PairTile t = w.t;
             const uint32_t idesc = ptx::idesc_bf16_f32(2 * kWRows, t.n);
             const int acc = local & 1;
             const uint32_t acc_par = (uint32_t)(local >> 1) & 1u;
@@ -410,8 +450,9 @@ __global__ void __launch_bounds__(Cfg<MX>::kThreads, 1)
         uint32_t phase = 0;
         uint32_t last_par[C::kSfStages > 0 ? C::kSfStages : 1];
         bool ok = true;
-        for (int tile = pair; ok && tile < total; tile += npairs) {
-            const PairTile t = decode_pair_tile<SWIGLU>(tile, c, a);
+        Walk w;
+        for (bool more = walk_first<SWIGLU>(w, pair, c, a); ok && more; more = walk_next<SWIGLU>(w, npairs, c, a)) {
+            const PairTile t = w.t;
             for (int mi = 0; ok && mi < n_micro_k; ++mi) {
                 const int m = SWIGLU ? t.m : mi;
                 const CUtensorMap* tsa = pick_map(m, tmSA0, tmSA1, tmSA2, tmSA3);
@@ -464,8 +505,9 @@ __global__ void __launch_bounds__(Cfg<MX>::kThreads, 1)
         int slot = 0, sfi = 0;
         uint32_t phase = 0;
         bool ok = true;
-        for (int tile = pair; ok && tile < total; tile += npairs) {
-            const PairTile t = decode_pair_tile<SWIGLU>(tile, c, a);
+        Walk w;
+        for (bool more = walk_first<SWIGLU>(w, pair, c, a); ok && more; more = walk_next<SWIGLU>(w, npairs, c, a)) {
+            const PairTile t = w.t;
             const int off = t.start & 3;  // the chunk's first scale word in the loaded 16-byte rows
             for (int mi = 0; ok && mi < n_micro_k; ++mi) {
                 for (int kb = 0; kb < a.k_blocks; ++kb) {
@@ -523,10 +565,11 @@ __global__ void __launch_bounds__(Cfg<MX>::kThreads, 1)
         __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
         const uint32_t tempty_leader0 = ptx::map_to_rank(ptx::smem_u32(&c.tempty[0]), 0);
         int local = 0;
-        for (int tile = pair; tile < total; tile += npairs, ++local) {
+        Walk w;
+        for (bool more = walk_first<SWIGLU>(w, pair, c, a); more; more = walk_next<SWIGLU>(w, npairs, c, a), ++local) {
             const int acc = local & 1;
             const uint32_t acc_par = (uint32_t)(local >> 1) & 1u;
-            const PairTile t = decode_pair_tile<SWIGLU>(tile, c, a);
+            const PairTile t = w.t;
             bool ready = false;
             if (lane == 0)
                 ready = ptx::mbar_wait(ptx::smem_u32(&c.tfull[acc]), acc_par, a.limit_ns, &c.abort);

@@ -226,6 +226,7 @@ struct PairGemmArgs {
     // layout), ready for the block-scaled down GEMM.
     void* out_scales;
     int64_t out_rows_pad;
+    int chunk_block;          // chunks of a group taken together past every weight tile (0: all)
 };
 // tmW[m]: SwiGLU form: w13_m [G][2I][K] as a 5D map {K, 16, 2, I/16, G} (strides
 // of a row, of the up half, of 16 rows, of a group) with box {64, 16, 2, 4, 1};
