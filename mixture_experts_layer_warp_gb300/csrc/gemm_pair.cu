@@ -98,11 +98,16 @@ struct Ctl {
     uint64_t sfs_empty[8];    // MX, each CTA: its 4 scale warps have read a ring slot
     uint64_t sf_full[6];      // MX, leader: both CTAs wrote a scale-factor buffer
     uint64_t sf_empty[6];     // MX, both CTAs: the MMAs reading a scale-factor buffer are done
+    uint64_t rfull[8];        // both CTAs: a tile index is in the hand-out ring slot
+    uint64_t rempty[8];       // leader: every consuming warp of both CTAs has taken it
+    int tring[8];             // the hand-out ring: tile indices, -1 = no more tiles
     uint32_t tmem_base;
     int abort;
     int seg[kMaxExperts + 1];
     int chunks[kMaxExperts + 1];  // prefix over groups of ceil(rows / chunk)
 };
+constexpr int kDynamicTilesPerPair = 64;  // tiles per pair (bound) from which the hand-out is dynamic
+constexpr int kFeed = 4;  // hand-out ring slots: the scheduler runs at most ~2 tiles ahead of the producer
 
 // Epilogue staging, per epilogue warp: one 32-token block of its accumulator
 // lanes, transposed through shared memory so that each thread stores 16-byte
@@ -191,21 +196,69 @@ __device__ __forceinline__ bool walk_load(Walk& w, const Ctl& c, const PairGemmA
     return true;
 }
 
-template <bool SWIGLU>
-__device__ __forceinline__ bool walk_first(Walk& w, int pair, const Ctl& c, const PairGemmArgs& a) {
-    w.tile = pair;
-    return walk_load<SWIGLU>(w, c, a);
-}
-
-template <bool SWIGLU>
-__device__ __forceinline__ bool walk_next(Walk& w, int npairs, const Ctl& c, const PairGemmArgs& a) {
-    w.tile += npairs;
-    return walk_load<SWIGLU>(w, c, a);
-}
-
 __device__ __forceinline__ void fail(Ctl& c, int* err) {
     c.abort = 1;
     atomicOr(err, kErrTimeout);
+}
+
+// Tile hand-out. The pairs take tiles of the order above from a global counter
+// (a.sched[0]) as they become free, so the pairs running at once stay on
+// consecutive tiles for the whole launch (statically assigned, every pair's
+// share was the same but the pairs drifted apart over the ~320 rounds of a
+// large launch, and a weight tile shared by neighbouring pairs was fetched
+// from HBM again: 13-20 GB of DRAM traffic for the CFG GEMM1's 7 GB). The
+// leader's warp 2 (otherwise idle between the TMEM allocation and release)
+// takes tiles ahead of use and publishes each index to every warp of the
+// pair that walks the tiles: into this CTA's ring slot, and into the peer's
+// slot by st.async completing on the peer's barrier; -1 ends the walk. A
+// slot is reused once every consuming warp of both CTAs has taken it.
+// With few tiles per pair (a.dynamic == 0) the scheduler hands out the static
+// sequence pair, pair + npairs, ... instead: pairs that reserve a tile or two
+// ahead would leave the last tiles of a short launch unevenly spread (denoise
+// GEMMs, ~30-40 tiles per pair: 0.51 -> 0.57 ms), where drift never builds up.
+//   take: the next index for a consuming warp (-2: a wait ran out).
+//   hand_out: the scheduler warp's loop.
+__device__ __forceinline__ int feed_take(Ctl& c, int& n, bool leader, uint32_t rempty0, const PairGemmArgs& a) {
+    const int slot = n % kFeed;
+    const bool got = ptx::mbar_wait(ptx::smem_u32(&c.rfull[slot]), (uint32_t)(n / kFeed) & 1u, a.limit_ns, &c.abort);
+    if (!__all_sync(0xffffffffu, got)) return -2;
+    // the shuffle needs the loaded value, so the read is complete before the
+    // arrival below lets the scheduler write the slot again
+    const int tile = __shfl_sync(0xffffffffu, *static_cast<volatile int*>(&c.tring[slot]), 0);
+    if ((threadIdx.x & 31) == 0) {
+        if (leader)
+            ptx::mbar_arrive(ptx::smem_u32(&c.rempty[slot]));
+        else
+            ptx::mbar_arrive_remote(rempty0 + (uint32_t)(slot * sizeof(uint64_t)));
+    }
+    ++n;
+    return tile;
+}
+
+__device__ __forceinline__ void hand_out(Ctl& c, int total, const PairGemmArgs& a, int pair, int npairs) {
+    const uint32_t peer_tring = ptx::map_to_rank(ptx::smem_u32(&c.tring[0]), 1);
+    const uint32_t peer_rfull = ptx::map_to_rank(ptx::smem_u32(&c.rfull[0]), 1);
+    for (int n = 0;; ++n) {
+        const int slot = n % kFeed;
+        const bool got = ptx::mbar_wait(ptx::smem_u32(&c.rempty[slot]), ((uint32_t)(n / kFeed) & 1u) ^ 1u, a.limit_ns,
+                                        &c.abort);
+        if (!__all_sync(0xffffffffu, got)) {
+            if ((threadIdx.x & 31) == 0) fail(c, a.err);
+            return;
+        }
+        int tile = 0;
+        if ((threadIdx.x & 31) == 0) {
+            tile = a.dynamic ? atomicAdd(a.sched, 1) : pair + n * npairs;
+            if (tile >= total) tile = -1;
+            c.tring[slot] = tile;
+            ptx::mbar_arrive(ptx::smem_u32(&c.rfull[slot]));
+            ptx::mbar_arrive_expect_tx_remote(peer_rfull + (uint32_t)(slot * sizeof(uint64_t)), 4);
+            ptx::st_async_u32(peer_tring + (uint32_t)(slot * 4), (uint32_t)tile,
+                              peer_rfull + (uint32_t)(slot * sizeof(uint64_t)));
+        }
+        tile = __shfl_sync(0xffffffffu, tile, 0);
+        if (tile < 0) return;
+    }
 }
 
 // Failure path of a CTA whose loads complete on the other CTA's barrier: it
@@ -253,6 +306,13 @@ __global__ void __launch_bounds__(Cfg<MX>::kThreads, 1)
             ptx::mbar_init(ptx::smem_u32(&c.tempty[b]), kEpiArrivals);
         }
         ptx::mbar_init(ptx::smem_u32(&c.drain), 1);
+        // the warps that take every tile index: producer + MMA + 4 epilogue
+        // warps (leader), producer + 4 epilogue warps (peer), and with MXFP8
+        // operands the scale producer and the 4 scale warps of each CTA
+        for (int r = 0; r < kFeed; ++r) {
+            ptx::mbar_init(ptx::smem_u32(&c.rfull[r]), 1);
+            ptx::mbar_init(ptx::smem_u32(&c.rempty[r]), MX ? 21 : 11);
+        }
         if (MX) {
             for (int s = 0; s < C::kSfStages; ++s) {
                 ptx::mbar_init(ptx::smem_u32(&c.sfs_full[s]), 1);
@@ -296,6 +356,8 @@ __global__ void __launch_bounds__(Cfg<MX>::kThreads, 1)
 
     const uint32_t tmem = c.tmem_base;
     const int n_micro_k = SWIGLU ? 1 : a.n_micro;
+    const int total = (SWIGLU ? a.n_micro : 1) * a.n_ftiles * c.chunks[a.G];
+    const uint32_t rempty0 = ptx::map_to_rank(ptx::smem_u32(&c.rempty[0]), 0);  // the leader's
 
     // The producer and MMA roles run as whole warps: every lane takes part in
     // the waits and the bookkeeping (so the descriptors and coordinates are
@@ -310,8 +372,13 @@ __global__ void __launch_bounds__(Cfg<MX>::kThreads, 1)
         uint32_t last_par[kStages];
         int issued = 0;
         bool ok = true;
-        Walk w;
-        for (bool more = walk_first<SWIGLU>(w, pair, c, a); ok && more; more = walk_next<SWIGLU>(w, npairs, c, a)) {
+        int fn = 0;
+        while (ok) {
+            const int tile = feed_take(c, fn, leader, rempty0, a);
+            if (tile == -2) ok = false;
+            if (tile < 0) break;
+            Walk w{tile, {}};
+            walk_load<SWIGLU>(w, c, a);
             const PairTile t = w.t;
             const int half = t.n / 2;               // token rows held by each CTA
             const int box = token_box(t);
@@ -366,6 +433,9 @@ __global__ void __launch_bounds__(Cfg<MX>::kThreads, 1)
                 settle_inflight_copies();
             }
         }
+    } else if (warp == 2 && leader) {
+        // ------------------------------------------------ tile scheduler (leader)
+        hand_out(c, total, a, pair, npairs);
     } else if (warp == 1 && leader) {
         // ------------------------------------------------ MMA issuer (leader)
         const bool issuer = ptx::elect_one();
@@ -374,9 +444,13 @@ __global__ void __launch_bounds__(Cfg<MX>::kThreads, 1)
         bool ok = true;
         int local = 0;
         int sfi = 0;  // MX: stages consumed, which picks the scale-factor buffer and its phase
-        Walk w;
-        for (bool more = walk_first<SWIGLU>(w, pair, c, a); ok && more;
-             more = walk_next<SWIGLU>(w, npairs, c, a), ++local) {
+        int fn = 0;
+        for (; ok; ++local) {
+            const int tile = feed_take(c, fn, true, rempty0, a);
+            if (tile == -2) ok = false;
+            if (tile < 0) break;
+            Walk w{tile, {}};
+            walk_load<SWIGLU>(w, c, a);
             const PairTile t = w.t;
             const uint32_t idesc = ptx::idesc_bf16_f32(2 * kWRows, t.n);
             const int acc = local & 1;
@@ -450,8 +524,13 @@ __global__ void __launch_bounds__(Cfg<MX>::kThreads, 1)
         uint32_t phase = 0;
         uint32_t last_par[C::kSfStages > 0 ? C::kSfStages : 1];
         bool ok = true;
-        Walk w;
-        for (bool more = walk_first<SWIGLU>(w, pair, c, a); ok && more; more = walk_next<SWIGLU>(w, npairs, c, a)) {
+        int fn = 0;
+        while (ok) {
+            const int tile = feed_take(c, fn, leader, rempty0, a);
+            if (tile == -2) ok = false;
+            if (tile < 0) break;
+            Walk w{tile, {}};
+            walk_load<SWIGLU>(w, c, a);
             const PairTile t = w.t;
             for (int mi = 0; ok && mi < n_micro_k; ++mi) {
                 const int m = SWIGLU ? t.m : mi;
@@ -505,8 +584,13 @@ __global__ void __launch_bounds__(Cfg<MX>::kThreads, 1)
         int slot = 0, sfi = 0;
         uint32_t phase = 0;
         bool ok = true;
-        Walk w;
-        for (bool more = walk_first<SWIGLU>(w, pair, c, a); ok && more; more = walk_next<SWIGLU>(w, npairs, c, a)) {
+        int fn = 0;
+        while (ok) {
+            const int tile = feed_take(c, fn, leader, rempty0, a);
+            if (tile == -2) ok = false;
+            if (tile < 0) break;
+            Walk w{tile, {}};
+            walk_load<SWIGLU>(w, c, a);
             const PairTile t = w.t;
             const int off = t.start & 3;  // the chunk's first scale word in the loaded 16-byte rows
             for (int mi = 0; ok && mi < n_micro_k; ++mi) {
@@ -564,11 +648,20 @@ __global__ void __launch_bounds__(Cfg<MX>::kThreads, 1)
         const int q = warp - 4;  // TMEM lanes 32q .. 32q+31
         __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
         const uint32_t tempty_leader0 = ptx::map_to_rank(ptx::smem_u32(&c.tempty[0]), 0);
-        int local = 0;
-        Walk w;
-        for (bool more = walk_first<SWIGLU>(w, pair, c, a); more; more = walk_next<SWIGLU>(w, npairs, c, a), ++local) {
+        int local = 0, fn = 0;
+        for (;; ++local) {
+            const int tile = feed_take(c, fn, leader, rempty0, a);
+            // the MXFP8 SwiGLU epilogue's warp pairs agree first (see below)
+            bool live = tile >= 0;
+            if (MX && SWIGLU) live = ptx::named_barrier_and(1 + (q >> 1), 64, live);
+            if (!live) {
+                if (tile == -2 && lane == 0) fail(c, a.err);
+                break;
+            }
             const int acc = local & 1;
             const uint32_t acc_par = (uint32_t)(local >> 1) & 1u;
+            Walk w{tile, {}};
+            walk_load<SWIGLU>(w, c, a);
             const PairTile t = w.t;
             bool ready = false;
             if (lane == 0)
@@ -692,6 +785,16 @@ __global__ void __launch_bounds__(Cfg<MX>::kThreads, 1)
     __syncwarp();
     ptx::tc_fence_before();
     ptx::cluster_sync();
+    if (leader && threadIdx.x == 0) {
+        // the last pair to finish (every pair has stopped taking tiles) resets
+        // the hand-out counter for the next launch in the stream
+        __threadfence();
+        if (atomicAdd(a.sched + 1, 1) == npairs - 1) {
+            a.sched[0] = 0;
+            a.sched[1] = 0;
+            __threadfence();
+        }
+    }
     if (warp == 2) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc_pair(tmem, kTmemCols);
@@ -734,6 +837,8 @@ cudaError_t launch_pair(const PairGemmArgs& a, const CUtensorMap* tmW, const CUt
     const int pairs_max = max_pairs<SWIGLU, MX>();
     if (pairs_max <= 0) return cudaErrorLaunchOutOfResources;
     const int pairs = a.max_tiles < pairs_max ? a.max_tiles : pairs_max;
+    PairGemmArgs ad = a;
+    ad.dynamic = a.max_tiles >= kDynamicTilesPerPair * pairs ? 1 : 0;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(2 * pairs);
     cfg.blockDim = dim3(Cfg<MX>::kThreads);
@@ -751,7 +856,7 @@ cudaError_t launch_pair(const PairGemmArgs& a, const CUtensorMap* tmW, const CUt
     const int nm = a.n_micro;
     return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<SWIGLU, MX>, tmW[0], tmW[nm > 1 ? 1 : 0], tmW[nm > 2 ? 2 : 0],
                               tmW[nm > 3 ? 3 : 0], tmX[0], tmX[1], tmX[2], tmX[3], tmSA[0], tmSA[nm > 1 ? 1 : 0],
-                              tmSA[nm > 2 ? 2 : 0], tmSA[nm > 3 ? 3 : 0], tmSB, a);
+                              tmSA[nm > 2 ? 2 : 0], tmSA[nm > 3 ? 3 : 0], tmSB, ad);
 }
 
 }  // namespace

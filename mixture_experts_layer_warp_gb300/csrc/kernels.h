@@ -227,6 +227,9 @@ struct PairGemmArgs {
     void* out_scales;
     int64_t out_rows_pad;
     int chunk_block;          // chunks of a group taken together past every weight tile (0: all)
+    int* sched;               // 2 ints, zero at launch (and left zero): the tile hand-out counter and
+                              // the count of pairs done; one pair per stream at a time
+    int dynamic;              // set by the launcher: tiles from the counter (else a static sequence)
 };
 // tmW[m]: SwiGLU form: w13_m [G][2I][K] as a 5D map {K, 16, 2, I/16, G} (strides
 // of a row, of the up half, of 16 rows, of a group) with box {64, 16, 2, 4, 1};

@@ -47,6 +47,7 @@ struct moe_handle {
     int32_t* blk_hist = nullptr;
     int32_t* blk_base = nullptr;
     int* done = nullptr;  // counters of the fused small-batch kernel (fused_counter_ints of them)
+    int* sched = nullptr;  // tile hand-out counters of the pair GEMMs: [0..1] the call's stream, [2..3] the side stream
     void* xp = nullptr;
     void* hbuf = nullptr;
     void* obuf = nullptr;
@@ -279,7 +280,7 @@ moe_status run_routed_mx(moe_handle* h, const void* x, const void* const* w13, c
     }
     PairGemmArgs g1{h->offsets, E, M, H / 128, I / 128, 0, 0, hq, MI, I,
                     M * chunk_bound * (I / 128), h->err, h->limit_ns, 0, 1,  // early: behind the gather
-                    hq + mx_scales_off(R, MI), rows_pad, chunk_block(208, H)};
+                    hq + mx_scales_off(R, MI), rows_pad, chunk_block(208, H), h->sched};
     if ((e = timed(h, kSlotGemm1, s, [&] { return launch_pair_gemm_swiglu_mx(g1, tmW, tmX, tmS, tmSB, s); })) !=
         cudaSuccess)
         return cuda_err(h, e, "MXFP8 GEMM1 launch");
@@ -294,7 +295,7 @@ moe_status run_routed_mx(moe_handle* h, const void* x, const void* const* w13, c
     }
     PairGemmArgs g2{h->offsets, E, M, I / 128, H / 256, H, I, h->obuf, (int64_t)H, 0,
                     chunk_bound * (H / 256), h->err, h->limit_ns, 0, 1,  // early: behind GEMM1
-                    nullptr, 0, chunk_block(208, MI)};
+                    nullptr, 0, chunk_block(208, MI), h->sched};
     if ((e = timed(h, kSlotGemm2, s, [&] { return launch_pair_gemm_down_mx(g2, tmW, tmX, tmS, tmSB, s); })) !=
         cudaSuccess)
         return cuda_err(h, e, "MXFP8 GEMM2 launch");
@@ -425,7 +426,7 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
                 return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (w13[%d])", m);
         PairGemmArgs g1{h->offsets, E, M, H / kTcBK, I / 128, 0, 0, h->hbuf, (int64_t)M * I, I,
                         M * chunk_bound * (I / 128), h->err, h->limit_ns, 0, 1,  // early: behind the gather
-                        nullptr, 0, chunk_block(256, (int64_t)H * 2)};
+                        nullptr, 0, chunk_block(256, (int64_t)H * 2), h->sched};
         if ((e = timed(h, kSlotGemm1, s, [&] { return launch_pair_gemm_swiglu(g1, tmW, tmX, s); })) != cudaSuccess)
             return cuda_err(h, e, "GEMM1 launch");
         // GEMM2: h [R][M*I] x w2[m] [E*H][I], summed over m -> o [R][H]
@@ -436,7 +437,7 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
                 return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (w2[%d])", m);
         PairGemmArgs g2{h->offsets, E, M, I / kTcBK, H / 256, H, I, h->obuf, (int64_t)H, 0,
                         chunk_bound * (H / 256), h->err, h->limit_ns, 0, 1,  // early: behind GEMM1
-                        nullptr, 0, chunk_block(256, (int64_t)M * I * 2)};
+                        nullptr, 0, chunk_block(256, (int64_t)M * I * 2), h->sched};
         if ((e = timed(h, kSlotGemm2, s, [&] { return launch_pair_gemm_down(g2, tmW, tmX, s); })) != cudaSuccess)
             return cuda_err(h, e, "GEMM2 launch");
         if (Is > 0 && !fork && (st = run_shared_pair(h, x, sw13, sw2, T, s, 1)) != MOE_OK) return st;
@@ -515,18 +516,19 @@ moe_status run_shared_pair(moe_handle* h, const void* x, const void* sw13, const
                            cudaStream_t ss, int early) {
     const int H = h->cfg.hidden, Is = h->cfg.shared_inter;
     const int chunks = (T + 255) / 256;
+    int* sched = ss == h->side && ss != nullptr ? h->sched + 2 : h->sched;  // the side stream's own counters
     CUtensorMap tmW[1], tmX[4];
     cudaError_t e;
     if (!encode_rows_pair(tmX, x, H, T) || !encode_w13_pair(&tmW[0], sw13, H, Is, 1))
         return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (shared GEMM1)");
     PairGemmArgs s1{nullptr, 1, 1, H / kTcBK, Is / 128, 0, 0, h->hs, (int64_t)Is, 0, chunks * (Is / 128), h->err,
-                    h->limit_ns, T, early, nullptr, 0, chunk_block(256, (int64_t)H * 2)};
+                    h->limit_ns, T, early, nullptr, 0, chunk_block(256, (int64_t)H * 2), sched};
     if ((e = timed(h, kSlotSharedGemm1, ss, [&] { return launch_pair_gemm_swiglu(s1, tmW, tmX, ss); })) != cudaSuccess)
         return cuda_err(h, e, "shared GEMM1 launch");
     if (!encode_rows_pair(tmX, h->hs, Is, T) || !encode_w2_pair(&tmW[0], sw2, Is, H))
         return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (shared GEMM2)");
     PairGemmArgs s2{nullptr, 1, 1, Is / kTcBK, H / 256, H, Is, h->sbuf, (int64_t)H, 0, chunks * (H / 256), h->err,
-                    h->limit_ns, T, early, nullptr, 0, chunk_block(256, (int64_t)Is * 2)};
+                    h->limit_ns, T, early, nullptr, 0, chunk_block(256, (int64_t)Is * 2), sched};
     if ((e = timed(h, kSlotSharedGemm2, ss, [&] { return launch_pair_gemm_down(s2, tmW, tmX, ss); })) != cudaSuccess)
         return cuda_err(h, e, "shared GEMM2 launch");
     return MOE_OK;
@@ -663,6 +665,7 @@ moe_status moe_create(const moe_config* cfg, moe_handle** out) {
     const size_t o_off = take((E + 1) * 4), o_ttc = take((E + 1) * 4), o_tsi = take((E + 1) * 4);
     const size_t o_smeta = take(6 * 4);
     const size_t o_hist = take(NB * E * 4), o_base = take(NB * E * 4), o_done = take(fused_counter_ints((int)E) * 4);
+    const size_t o_sched = take(4 * 4);
     const size_t o_xp = take(R * H * esz), o_h = take(R * M * I * esz), o_o = take(R * H * esz);
     const size_t o_hs = take(T * Is * esz), o_s = take(Is ? T * H * esz : 0);
     const size_t o_xst0 = take(T * H * esz), o_xst1 = take(T * H * esz);
@@ -686,6 +689,7 @@ moe_status moe_create(const moe_config* cfg, moe_handle** out) {
     h->blk_hist = reinterpret_cast<int32_t*>(b + o_hist);
     h->blk_base = reinterpret_cast<int32_t*>(b + o_base);
     h->done = reinterpret_cast<int*>(b + o_done);
+    h->sched = reinterpret_cast<int*>(b + o_sched);
     h->xp = b + o_xp;
     h->hbuf = b + o_h;
     h->obuf = b + o_o;
@@ -695,7 +699,7 @@ moe_status moe_create(const moe_config* cfg, moe_handle** out) {
     h->x_stage[1] = b + o_xst1;
     h->y_stage[0] = b + o_yst0;
     h->y_stage[1] = b + o_yst1;
-    if (cudaMemset(h->err, 0, sizeof(int)) != cudaSuccess) {
+    if (cudaMemset(h->err, 0, sizeof(int)) != cudaSuccess || cudaMemset(h->sched, 0, 4 * sizeof(int)) != cudaSuccess) {
         cudaFree(h->ws);
         delete h;
         return MOE_ERR_CUDA;

@@ -230,6 +230,20 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t caddr, float v) {
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(caddr), "f"(v) : "memory");
 }
 
+// A 32-bit word into another CTA's shared memory (shared::cluster address
+// `caddr`), completing 4 bytes of transaction count on that CTA's mbarrier
+// `cbar`; the receiver's wait on `cbar` then sees the word.
+__device__ __forceinline__ void st_async_u32(uint32_t caddr, uint32_t v, uint32_t cbar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(caddr), "r"(v),
+                 "r"(cbar)
+                 : "memory");
+}
+// Arrive on another CTA's barrier (shared::cluster address) announcing `bytes`
+// of transaction count that writes into its memory will complete.
+__device__ __forceinline__ void mbar_arrive_expect_tx_remote(uint32_t cbar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cluster.b64 _, [%0], %1;" ::"r"(cbar), "r"(bytes) : "memory");
+}
+
 // 16 bytes into another CTA's shared memory (shared::cluster address `caddr`);
 // the write completes 16 bytes of transaction count on that CTA's mbarrier
 // `cbar` (also a shared::cluster address), so the receiver waits on its own
