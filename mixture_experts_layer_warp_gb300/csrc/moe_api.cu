@@ -156,9 +156,10 @@ bool encode_w2_pair(CUtensorMap* m, const void* w2, uint64_t K, uint64_t rows) {
 // Chunks of a group taken together past all its weight tiles (the pair GEMMs'
 // tile order): as many as keep the block's token rows within kL2RowBytes, so
 // they stay in L2 while the group's weight tiles stream past them. Measured on
-// the CFG workload (full size, DRAM bytes per launch): the shared expert's
-// GEMM1 6.4 GB without blocks, 1.1 GB with 32 MB blocks; the routed GEMM1 (32 MB
-// of rows per expert) 17.8 vs 16.1 GB; 4-16 MB blocks gave 20.5-22 GB there.
+// the CFG workload (full size, DRAM bytes per launch, tiles assigned
+// statically): the shared expert's GEMM1 6.4 GB without blocks, 1.1 GB with
+// 32 MB blocks; the routed GEMM1 (32 MB of rows per expert) 17.8 vs 16.1 GB;
+// 4-16 MB blocks gave 20.5-22 GB there.
 constexpr int64_t kL2RowBytes = 32ll << 20;
 int chunk_block(int chunk_rows, int64_t row_bytes) {
     const int64_t b = kL2RowBytes / ((int64_t)chunk_rows * row_bytes);
@@ -521,14 +522,18 @@ moe_status run_shared_pair(moe_handle* h, const void* x, const void* sw13, const
     cudaError_t e;
     if (!encode_rows_pair(tmX, x, H, T) || !encode_w13_pair(&tmW[0], sw13, H, Is, 1))
         return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (shared GEMM1)");
+    // one dense segment of many chunks: chunk by chunk past every weight tile
+    // (chunk blocks of 1), so the shared weights (50 MB at Is = 3072) stay in
+    // L2 while x streams once (CFG, DRAM bytes per launch: GEMM1 1.00 -> 0.83 GB,
+    // GEMM2 0.66 -> 0.47 GB against 32 MB blocks of rows)
     PairGemmArgs s1{nullptr, 1, 1, H / kTcBK, Is / 128, 0, 0, h->hs, (int64_t)Is, 0, chunks * (Is / 128), h->err,
-                    h->limit_ns, T, early, nullptr, 0, chunk_block(256, (int64_t)H * 2), sched};
+                    h->limit_ns, T, early, nullptr, 0, 1, sched};
     if ((e = timed(h, kSlotSharedGemm1, ss, [&] { return launch_pair_gemm_swiglu(s1, tmW, tmX, ss); })) != cudaSuccess)
         return cuda_err(h, e, "shared GEMM1 launch");
     if (!encode_rows_pair(tmX, h->hs, Is, T) || !encode_w2_pair(&tmW[0], sw2, Is, H))
         return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (shared GEMM2)");
     PairGemmArgs s2{nullptr, 1, 1, Is / kTcBK, H / 256, H, Is, h->sbuf, (int64_t)H, 0, chunks * (H / 256), h->err,
-                    h->limit_ns, T, early, nullptr, 0, chunk_block(256, (int64_t)Is * 2), sched};
+                    h->limit_ns, T, early, nullptr, 0, 1, sched};
     if ((e = timed(h, kSlotSharedGemm2, ss, [&] { return launch_pair_gemm_down(s2, tmW, tmX, ss); })) != cudaSuccess)
         return cuda_err(h, e, "shared GEMM2 launch");
     return MOE_OK;
