@@ -313,8 +313,7 @@ def config_of(wl, mx=False):
                     "seeded batches"
     if mx:
         cfg["weights"] = "mxfp8 (E4M3 codes, E8M0 scale per 32 along K)"
-        if wl.T > 16:
-            cfg["activations"] = "mxfp8 token rows and h (block-scaled FP8 MMA, fp32 accumulate)"
+        cfg["activations"] = "mxfp8 token rows and h (block-scaled FP8 MMA, fp32 accumulate)"
     return cfg
 
 
@@ -337,6 +336,7 @@ def roofline_of(wl, prof, ids_pool, steps, peaks, step_ms, clocks, mxfp8=False):
     R = wl.T * wl.k
     esz = 4 if wl.dtype == "f32" else 2
     wsz = (1 + 1 / 32) if mxfp8 else esz  # bytes per expert weight (MXFP8: code + a 32nd of a scale)
+    asz = wsz  # bytes per element of the gathered rows and h (MXFP8 with MXFP8 weights)
     # touched experts per step, averaged over the batches the timed steps used
     touched = statistics.mean(len(np.unique(ids_pool[i % len(ids_pool)])) for i in range(steps))
     I, H, M = wl.I, wl.H, wl.n_micro
@@ -352,7 +352,8 @@ def roofline_of(wl, prof, ids_pool, steps, peaks, step_ms, clocks, mxfp8=False):
     elif wl.T <= 16:
         bound, unit, peak = "hbm", "GB/s", peaks["hbm"]
         algo = {
-            "gemm1_swiglu": (touched * 3 * I * H * wsz * M + 3 * R * H * esz + 2 * R * M * I * esz + wl.T * H * esz)
+            "gemm1_swiglu": (touched * 3 * I * H * wsz * M + R * H * esz + 2 * R * H * asz + 2 * R * M * I * asz
+                             + wl.T * H * esz)
             if fused
             else (touched * 2 * I * H * esz * M + R * H * esz + R * M * I * esz),
             "gemm2_down": touched * H * I * esz * M + R * M * I * esz + R * H * esz,
@@ -558,7 +559,7 @@ def measure(args, wl, world, rank, local, peaks, mx=False, cpu_seconds=12.0, two
     layer.close()
     rec = {"value": value, "unit": "tokens/s", "ms_per_step": ms / args.steps, "steps": args.steps,
            "warmup": args.warmup,
-           "dtype": ("e4m3 (mxfp8 weights and activations)" if wl.T > 16 else "f16 (mxfp8 expert weights)")
+           "dtype": "e4m3 (mxfp8 weights and activations)"
            if mx else wl.dtype,
            "config": dict(config_of(wl, mx), **({"shared_stream": True} if args.shared_stream else {})),
            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,

@@ -176,15 +176,12 @@ moe_status moe_forward_host_async(moe_handle *h, const void *x_host, const void 
  * model"; they fix no format). The reading taken is the OCP Microscaling
  * MXFP8 format: each expert weight is an FP8 E4M3 code (OCP E4M3FN, largest
  * 448) with one E8M0 power-of-two scale per 32 consecutive elements along K;
- * the layer computes with w = code * 2^(S-127). Batches of at most 16 tokens
- * (whose time is the weight bytes) take f16 operands: w rounded to f16
- * (nearest, ties to even), the gathered token rows and h rounded to f16.
- * Larger batches (whose time is the tensor-core work) run the block-scaled
- * FP8 MMA: the gathered token rows and h are quantised to MXFP8 by the same
- * rule as the weights (along H and along each micro's I), and each GEMM
- * multiplies the codes with their scales exactly. Both accumulate in fp32;
- * the router, the shared expert (its weights stay bf16) and y keep the
- * layer's bf16.
+ * the layer computes with w = code * 2^(S-127). Every batch size runs the
+ * tensor cores' block-scaled FP8 MMA: the gathered token rows and h (taken at
+ * its bf16 value) are quantised to MXFP8 by the same rule as the weights
+ * (along H and along each micro's I), and each GEMM multiplies the codes with
+ * their scales exactly, accumulating in fp32; the router, the shared expert
+ * (its weights stay bf16) and y keep the layer's bf16.
  *
  * Quantisation of bf16 weights w [groups][rows][cols] along cols (cols % 32
  * == 0): codes [groups][rows][cols] uint8 and scales [groups][cols/32][rows]

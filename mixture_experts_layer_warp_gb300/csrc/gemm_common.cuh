@@ -81,4 +81,23 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
     return pair;
 }
 
+// MXFP8 form of 128 consecutive bf16 values, four per lane (lane l holds
+// elements 4l .. 4l+3): the E4M3 codes of this lane's four (returned, element
+// order in the bytes) and, in every lane, the scale word of the four 32-blocks
+// (byte b: block b), by the MX rule (shared exponent floor(log2 amax) - 8,
+// codes nearest-even, saturating).
+__device__ __forceinline__ uint32_t mx_quantize128(uint2 raw, int lane, uint32_t& word) {
+    const __nv_bfloat162* v = reinterpret_cast<const __nv_bfloat162*>(&raw);
+    const float2 f0 = __bfloat1622float2(v[0]), f1 = __bfloat1622float2(v[1]);
+    float a = fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)), fmaxf(fabsf(f1.x), fabsf(f1.y)));
+#pragma unroll
+    for (int d = 1; d < 8; d <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, d));  // the block's 8 lanes
+    const int shared = mx_shared_exp(a);
+    const float sc = pow2f(-shared);  // exact: a power of two
+    const uint32_t codes = e4m3x2(f0.x * sc, f0.y * sc) | (e4m3x2(f1.x * sc, f1.y * sc) << 16);
+    const uint32_t b = (lane & 7) == 0 ? (uint32_t)(shared + 127) << (8 * (lane >> 3)) : 0u;
+    word = __reduce_or_sync(0xffffffffu, b);
+    return codes;
+}
+
 }  // namespace moe

@@ -59,42 +59,43 @@ constexpr int kThreads = 256;
 constexpr int kGatherCtas = 128;               // kFused: CTAs that gather token rows
 constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kM, kTok);
 
-// MXFP8 expert weights (fused mode, moe_forward_mxfp8): a stage covers 256 K
-// as two 128-K code chunks, so each weight row moves 128 contiguous bytes of
-// E4M3 codes per TMA row (a 64-byte row halves the sustained stream rate) and
-// a stage is three TMA instructions for 32 KB of codes (the producer thread's
-// TMA issue, about as slow per instruction whatever the box, bounds the stream
-// otherwise); the codes arrive 128-byte swizzled with the eight E8M0 scales of
-// each row and four 64-K token-row tiles. A layer whose K is an odd multiple of
-// 128 ends with half a stage: the boxes past the weights read zero codes. Eight dequant warps (8..15:
-// two per TMEM lane quadrant, taking alternate stages) turn each weight row's
-// 128 codes into f16, code * 2^(S-127) rounded to f16, in registers and store
-// them into one of kF8Dq A buffers in tensor memory; the MMA reads A from
-// tensor memory and the token rows (f16: the gathered rows and h) from shared
-// memory, into fp32 accumulators as before; two threads issue the MMAs (a
-// tile's even and odd stages, into two accumulator halves the epilogue adds).
-// No dequantised tile passes through shared memory.
-constexpr int kF8Stages = 5;
-constexpr int kF8Chunks = 4;                         // 64-K MMA chunks per stage
-constexpr int kF8K = kF8Chunks * kTcBK;              // 256 K per stage
+// MXFP8 expert weights (fused mode, moe_forward_mxfp8): the block-scaled FP8
+// MMA (kind::mxf8f6f4, E4M3 x E4M3, one UE8M0 scale per 32 K on each side,
+// exact products, fp32 accumulation) on the weights' codes and the MXFP8 token
+// rows and h. A stage covers 256 K. Ring A holds only weight bytes: the codes
+// as two 128-K chunks (128 rows of 128 contiguous bytes each, 128-byte
+// swizzled; a 64-byte row halves the sustained stream rate) and their eight
+// scales per row, two TMA instructions per stage from the producer thread.
+// Ring B holds the 16 token rows' codes (two [16][128] chunks) and scale bytes
+// of the same 256 K, loaded from L2 by a second producer thread, so the
+// weight stream keeps kF8StagesA x 33 KB in flight. Four scale warps copy each
+// stage's scales into tensor memory in the layout the MMA reads (per 128-K
+// chunk one word per row: the A row m in lane m % 32 of every lane quarter,
+// column m / 32; the B row n in lane n, column 8), and one thread issues the
+// stage's eight MMAs. The gather phase writes the token rows in MXFP8 and the
+// SwiGLU epilogue writes h in MXFP8 (scales [R][pitch] for the token rows,
+// [micro][R][pitch] for h, pitch a multiple of 16 bytes).
+constexpr int kF8StagesA = 6;
+constexpr int kF8StagesB = 4;
+constexpr int kF8K = 256;                            // K per stage
 constexpr int kF8CodeBytes = kM * kF8K;              // 32 KB of codes: two [128 rows][128 K] chunks
-constexpr int kF8ScaleBytes = kM * (kF8K / 32);      // 1 KB of scales
-constexpr int kF8BBytes = kF8Chunks * kBBytes;       // four 64-K token-row tiles
-constexpr int kF8Dq = 3;                             // TMEM A buffers
-constexpr int kF8Threads = 512;                      // warps 8..15 dequantise
-constexpr int kF8CodeOff = kF8Stages * kF8BBytes;    // after the token-row tiles (1024-aligned)
-constexpr int kF8ScaleOff = kF8CodeOff + kF8Stages * kF8CodeBytes;
-constexpr int kF8CtlOff = kF8ScaleOff + kF8Stages * kF8ScaleBytes;
-constexpr int kF8TmemCols = 512;                     // accumulators at 0..63, A buffers from kF8ACol
-constexpr int kF8ACol = 64;                          // A buffer b: columns kF8ACol + kF8ABuf b ..
-constexpr int kF8ABuf = kF8K / 2;                    // 128 columns: the stage's f16 pairs
-constexpr uint32_t kIdescF16 = ptx::idesc_f16_f32(kM, kTok);
-constexpr int kMaxStages = kF8Stages > kStages ? kF8Stages : kStages;
-static_assert(kF8ACol + kF8Dq * kF8ABuf <= kF8TmemCols, "A buffers exceed the TMEM allocation");
+constexpr int kF8ScaleBytes = kM * (kF8K / 32);      // 1 KB of scales: [8 blocks][128 rows]
+constexpr int kF8SlotA = kF8CodeBytes + kF8ScaleBytes;
+constexpr int kF8BCodeBytes = kTok * kF8K;           // 4 KB: two [16 rows][128 K] chunks
+constexpr int kF8BScaleBytes = kTok * 16;            // [16 rows][16 scale bytes] (512 K; the stage uses 8)
+constexpr int kF8SlotB = 5 * 1024;
+constexpr int kF8BOff = kF8StagesA * kF8SlotA;       // ring B after ring A
+constexpr int kF8CtlOff = kF8BOff + kF8StagesB * kF8SlotB;
+constexpr int kF8Threads = 384;                      // warps 8..11 copy scales into tensor memory
+constexpr int kF8TmemCols = 256;                     // accumulators at 0..31, scale buffers from kF8SfCol
+constexpr int kF8SfCol = 32;                         // ring A slot s: 32 columns, chunk c at +16 c (SFA +0, SFB +8)
+constexpr int kMaxStages = kF8StagesA > kStages ? kF8StagesA : kStages;
+static_assert(kF8SlotA % 1024 == 0 && kF8SlotB % 1024 == 0 && kF8BCodeBytes + kF8BScaleBytes <= kF8SlotB,
+              "128-byte swizzled tiles need 1024-byte alignment");
+static_assert(kF8SfCol + kF8StagesA * 32 <= kF8TmemCols, "scale buffers exceed the TMEM allocation");
 
 // Stages of one micro's K (k_blocks 64-K blocks) with MXFP8 weights.
-__device__ __forceinline__ int f8_stages(int k_blocks) { return (k_blocks + kF8Chunks - 1) / kF8Chunks; }
-static_assert(kF8CodeOff % 1024 == 0 && kF8CodeBytes % 1024 == 0, "128-byte swizzled tiles need 1024-byte alignment");
+__device__ __forceinline__ int f8_stages(int k_blocks) { return (k_blocks + 3) / 4; }
 
 enum Mode { kSwiGLUOnly = 0, kDownOnly = 1, kFused = 2 };
 
@@ -104,7 +105,6 @@ struct Ctl {
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t drain;
-    uint64_t drain2;  // MXFP8: the second MMA issuer's
     uint32_t tmem_base;
     int abort;
     int seg[kMaxExperts + 1];
@@ -124,16 +124,10 @@ struct Ctl {
     uint64_t sq_empty;
     int sq_tile;
     int sq_rows;
-    // MXFP8. A stage is taken by dequant set p = (stage number) % 2 and MMA
-    // issuer j = (index in its tile) % 2, and uses code slot (stage number) %
-    // kF8Stages and A buffer (stage number) % kF8Dq. Every barrier below has
-    // one consumer, which waits all its completions in order (phase bits per
-    // slot), so no parity wait can run a phase ahead: a slot's next use for
-    // that consumer is armed only after the slot passed through it.
-    uint64_t fullD[2][kF8Stages];  // codes + scales landed, for dequant set p
-    uint64_t fullB[2][kF8Stages];  // token rows landed, for issuer j
-    uint64_t dq_full[2][kF8Dq];    // A buffer written, for issuer j (the four warps of a set)
-    uint64_t dq_empty[2][kF8Dq];   // A buffer read by the MMAs, for the set that writes it next
+    // MXFP8: ring B (token rows) and the scale warps' signal per ring A slot
+    uint64_t fullB[kF8StagesB];
+    uint64_t emptyB[kF8StagesB];
+    uint64_t sf_full[kF8StagesA];
 };
 
 constexpr int kSmemBytes = kStages * kStageBytes + (int)sizeof(Ctl) + 1024;
@@ -153,24 +147,23 @@ struct SmallParams {
     const int32_t* gperm;
     int gk;
     int grow_bytes;
-    // MXFP8: token rows per 64-K tile that the loads fill (8 when the batch has
-    // at most 8 tokens, as no expert then owns more routes; else 16). The MMA
-    // still reads 16 rows: rows past the loaded ones only feed output columns
-    // that the epilogue drops.
-    int brows;
+    // MXFP8: the gathered rows' scale bytes [R][xs_pitch] (their codes at gxp,
+    // [R][H]), and h's [n_micro][R][hs_pitch] (its codes at g1.out, [R][n_micro*I])
+    unsigned char* xs;
+    int xs_pitch;
+    unsigned char* hs;
+    int hs_pitch;
 };
 
-// With MXFP8 weights every stage is three TMA instructions (the producer
-// thread's issue rate bounds the stream otherwise): the gate and up rows of a
-// SwiGLU stage come as one 3D box, so do their scales, and so do the two 64-K
-// token-row tiles.
 struct SmallMaps {
-    CUtensorMap x1;      // SwiGLU token rows [R][H], box {64, 16} (MXFP8: 3D {64, R, H/64}, box {64, 16, 2})
-    CUtensorMap x2;      // down token rows (h) [R][M*I], box {64, 16} (MXFP8: 3D as x1)
-    CUtensorMap w1[kMaxMicro];  // w13[m] 3D {H, I, 2E}, box {64, 64, 2} (MXFP8: uint8 codes, box {128, 64, 2})
-    CUtensorMap w2[kMaxMicro];  // w2[m] [E*H][I], box {64, 128} (MXFP8: uint8 codes, box {128, 128})
-    CUtensorMap s1[kMaxMicro];  // MXFP8: w13[m] scales 3D {I, 2, E*H/32}, box {64, 2, 4}: [4][gate, up][64]
-    CUtensorMap s2[kMaxMicro];  // MXFP8: w2[m] scales [E*I/32][H] uint8, box {128, 4}: [4][128]
+    CUtensorMap x1;      // SwiGLU token rows [R][H], box {64, 16} (MXFP8: codes as 3D {128, R, H/128}, box {128, 16, 2})
+    CUtensorMap x2;      // down token rows (h) [R][M*I], box {64, 16} (MXFP8: codes, 3D as x1)
+    CUtensorMap w1[kMaxMicro];  // w13[m] 3D {H, I, 2E}, box {64, 64, 2} (MXFP8: codes 4D {128, I, 2E, H/128}, box {128, 64, 2, 2})
+    CUtensorMap w2[kMaxMicro];  // w2[m] [E*H][I], box {64, 128} (MXFP8: codes 3D {128, E*H, I/128}, box {128, 128, 2})
+    CUtensorMap s1[kMaxMicro];  // MXFP8: w13[m] scales 3D {I, 2, E*H/32}, box {64, 2, 8}: [8][gate, up][64]
+    CUtensorMap s2[kMaxMicro];  // MXFP8: w2[m] scales [E*I/32][H] uint8, box {128, 8}: [8][128]
+    CUtensorMap xs1;     // MXFP8: token rows' scales 3D {xs_pitch, R, 1}, box {16, 16, 1}
+    CUtensorMap xs2;     // MXFP8: h's scales 3D {hs_pitch, R, n_micro}, box {16, 16, 1}
 };
 
 __device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
@@ -203,41 +196,57 @@ __device__ __forceinline__ int expert_of(const int* seg, int G, int pos) {
     return lo;
 }
 
-// Eight bf16 to eight f16 (nearest, ties to even).
-__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
-    uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const __half2 h = __floats2half2_rn(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
-        w[i] = *reinterpret_cast<const uint32_t*>(&h);
-    }
-    return make_uint4(w[0], w[1], w[2], w[3]);
-}
-
 // The gather xp[i] = x[perm[i] / k] (blog section 6.1: index_select once), as
 // the fused kernel's first phase, run by the four epilogue warps: CTA b <
 // kGatherCtas copies rows b, b + kGatherCtas, ... and counts each finished row
 // for its expert, so a SwiGLU tile only waits for the rows of its own expert.
-// With MXFP8 weights the rows are written as f16.
+// With MXFP8 weights each row is written in MXFP8: its codes (one byte per
+// element) and its scale bytes (per 32-block; the row's pitch past H/32 zero),
+// warp q taking the 128-element stages q, q + 4, ...
 template <bool F8>
 __device__ __forceinline__ void gather_rows(const Ctl& c, const SmallParams& p) {
     const int tid = threadIdx.x - 128;
     const int R = c.seg[p.g1.G];
     const int nvec = p.grow_bytes / 16;
-    const uint4* __restrict__ src = static_cast<const uint4*>(p.gx);
-    uint4* __restrict__ dst = static_cast<uint4*>(p.gxp);
     const int gctas = (int)gridDim.x < kGatherCtas ? (int)gridDim.x : kGatherCtas;
     for (int i = blockIdx.x; i < R; i += gctas) {
         const int64_t tok = p.gperm[i] / p.gk;
-        constexpr int kBatch = 8;
-        for (int v0 = tid; v0 < nvec; v0 += 128 * kBatch) {
-            uint4 buf[kBatch];
+        if (F8) {
+            const int lane = tid & 31, q = tid >> 5;
+            const int H = p.grow_bytes / 2, stages = H / 128;
+            const uint2* __restrict__ src = static_cast<const uint2*>(p.gx) + tok * (H / 4);
+            uint32_t* __restrict__ codes = static_cast<uint32_t*>(p.gxp) + (int64_t)i * (H / 4);
+            uint32_t* __restrict__ words = reinterpret_cast<uint32_t*>(p.xs + (int64_t)i * p.xs_pitch);
+            constexpr int kBatch = 8;
+            for (int s0 = q; s0 < stages; s0 += 4 * kBatch) {
+                uint2 raw[kBatch];
 #pragma unroll
-            for (int u = 0; u < kBatch; ++u)
-                if (v0 + u * 128 < nvec) buf[u] = src[tok * nvec + v0 + u * 128];
+                for (int u = 0; u < kBatch; ++u)
+                    if (s0 + 4 * u < stages) raw[u] = src[(s0 + 4 * u) * 32 + lane];
 #pragma unroll
-            for (int u = 0; u < kBatch; ++u)
-                if (v0 + u * 128 < nvec) dst[(int64_t)i * nvec + v0 + u * 128] = F8 ? bf16x8_to_f16x8(buf[u]) : buf[u];
+                for (int u = 0; u < kBatch; ++u) {
+                    const int st = s0 + 4 * u;
+                    if (st < stages) {  // warp-uniform
+                        uint32_t word;
+                        codes[st * 32 + lane] = mx_quantize128(raw[u], lane, word);
+                        if (lane == 0) words[st] = word;
+                    }
+                }
+            }
+            for (int w = stages + tid; w < p.xs_pitch / 4; w += 128) words[w] = 0u;
+        } else {
+            const uint4* __restrict__ src = static_cast<const uint4*>(p.gx);
+            uint4* __restrict__ dst = static_cast<uint4*>(p.gxp);
+            constexpr int kBatch = 8;
+            for (int v0 = tid; v0 < nvec; v0 += 128 * kBatch) {
+                uint4 buf[kBatch];
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u)
+                    if (v0 + u * 128 < nvec) buf[u] = src[tok * nvec + v0 + u * 128];
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u)
+                    if (v0 + u * 128 < nvec) dst[(int64_t)i * nvec + v0 + u * 128] = buf[u];
+            }
         }
         fence_proxy_async_global();  // the rows are read next by TMA (async proxy)
         epilogue_bar();
@@ -472,60 +481,19 @@ __device__ __forceinline__ int pop_scheduled(Ctl& c, uint32_t& phase, uint64_t l
     return t;
 }
 
-// Sixteen E4M3 codes (in K order) under the E8M0 scale S to sixteen f16: the
-// f16 rounding of code * 2^(S-127).
-// Fast form, for scales that are f16 numbers (2^-24 .. 2^15, dequant_in_f16
-// true): one f16 multiply per pair of exact operands, branch-free.
-__device__ __forceinline__ bool dequant_in_f16(int S) { return S >= 127 - 24 && S <= 127 + 15; }
-
-__device__ __forceinline__ void dequant16_f16(uint4 q, int S, uint32_t* o) {
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-    const int e = S - 127;
-    const unsigned short hb = e >= -14 ? (unsigned short)((e + 15) << 10) : (unsigned short)(1u << ((e + 24) & 15));
-    const __half2 sc = __halves2half2(__ushort_as_half(hb), __ushort_as_half(hb));
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        uint32_t h[2];
-        ptx::e4m3x4_to_f16x2x2(w[i], h[0], h[1]);
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&h[j]), sc);
-            o[2 * i + j] = *reinterpret_cast<const uint32_t*>(&r);
-        }
-    }
-}
-
-// Any scale: through fp32, where the product is exact, rounded once to f16.
-__device__ __forceinline__ void dequant16_f32(uint4 q, int S, uint32_t* o) {
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-    const int e = S - 127;
-    const float fs = e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(1u << (e + 149));
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        uint32_t h[2];
-        ptx::e4m3x4_to_f16x2x2(w[i], h[0], h[1]);
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[j]));
-            const __half2 r = __floats2half2_rn(f.x * fs, f.y * fs);
-            o[2 * i + j] = *reinterpret_cast<const uint32_t*>(&r);
-        }
-    }
-}
-
 template <int MODE, bool F8>
 __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
     tc_small_kernel(const __grid_constant__ SmallMaps maps, const SmallParams p) {
     static_assert(!F8 || MODE == kFused, "MXFP8 weights run in the fused mode only");
-    constexpr int kSt = F8 ? kF8Stages : kStages;
+    constexpr int kSt = F8 ? kF8StagesA : kStages;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Ctl& c = *reinterpret_cast<Ctl*>(smem + (F8 ? kF8CtlOff : kStages * kStageBytes));
-    // stage s: the A tile (bf16 weights, or MXFP8 codes; their scales apart) and the token-row B tile
-    auto stage_a = [&](int st) { return smem + (F8 ? kF8CodeOff + st * kF8CodeBytes : st * kStageBytes); };
-    auto stage_s = [&](int st) { return smem + kF8ScaleOff + st * kF8ScaleBytes; };
-    auto stage_b = [&](int st) { return smem + (F8 ? st * kF8BBytes : st * kStageBytes + kABytes); };
+    // stage s: the A tile (bf16 weights; MXFP8: codes, then their scales) and
+    // the token-row B tile (MXFP8: slot s of ring B, codes then scale bytes)
+    auto stage_a = [&](int st) { return smem + (F8 ? st * kF8SlotA : st * kStageBytes); };
+    auto stage_b = [&](int st) { return smem + (F8 ? kF8BOff + st * kF8SlotB : st * kStageBytes + kABytes); };
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const TcGemmArgs& a0 = MODE == kDownOnly ? p.g2 : p.g1;  // seg, tiles, G, err, limit
     // the next routing call's kernels may be placed as SMs free up; they wait
@@ -538,26 +506,22 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
             ptx::mbar_init(ptx::smem_u32(&c.empty[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
-            ptx::mbar_init(ptx::smem_u32(&c.tfull[b]), F8 ? 2 : 1);  // the MMA issuer(s)' commits
+            ptx::mbar_init(ptx::smem_u32(&c.tfull[b]), 1);  // the MMA issuer's commit
             ptx::mbar_init(ptx::smem_u32(&c.tempty[b]), 4);
         }
-        for (int q = 0; q < 2; ++q) {
-            for (int b = 0; b < kF8Dq; ++b) {
-                ptx::mbar_init(ptx::smem_u32(&c.dq_full[q][b]), 4);  // the four warps of a dequant set
-                ptx::mbar_init(ptx::smem_u32(&c.dq_empty[q][b]), 1);  // an MMA issuer's commit
+        if (F8) {
+            for (int st = 0; st < kF8StagesB; ++st) {
+                ptx::mbar_init(ptx::smem_u32(&c.fullB[st]), 1);   // the row producer's expect_tx arrive
+                ptx::mbar_init(ptx::smem_u32(&c.emptyB[st]), 1);  // the MMA issuer's commit
             }
-            for (int st = 0; st < kF8Stages; ++st) {
-                ptx::mbar_init(ptx::smem_u32(&c.fullD[q][st]), 1);  // the producer's expect_tx arrive
-                ptx::mbar_init(ptx::smem_u32(&c.fullB[q][st]), 1);
-            }
+            for (int st = 0; st < kF8StagesA; ++st) ptx::mbar_init(ptx::smem_u32(&c.sf_full[st]), 4);  // scale warps
         }
         ptx::mbar_init(ptx::smem_u32(&c.drain), 1);
-        ptx::mbar_init(ptx::smem_u32(&c.drain2), 1);
         for (int q = 0; q < 4; ++q) {
             ptx::mbar_init(ptx::smem_u32(&c.tq_full[q]), 1);
-            // MMA issuer + four epilogue warps (MXFP8: two MMA issuers, four epilogue
-            // and eight dequant warps)
-            ptx::mbar_init(ptx::smem_u32(&c.tq_empty[q]), F8 ? 14 : 5);
+            // MMA issuer + four epilogue warps (MXFP8: also the row producer and
+            // the four scale warps)
+            ptx::mbar_init(ptx::smem_u32(&c.tq_empty[q]), F8 ? 10 : 5);
         }
         ptx::mbar_init(ptx::smem_u32(&c.sq_full), 1);
         ptx::mbar_init(ptx::smem_u32(&c.sq_empty), 1);
@@ -598,16 +562,12 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
     const int n2 = MODE == kSwiGLUOnly ? 0 : c.tiles[p.g2.G] * p.g2.n_tiles;
     const int total = n1 + n2;
 
-    if (warp == 0 && lane == 0) {
+    if (!F8 && warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer
         const uint64_t wpol = ptx::policy_evict_first();  // each weight byte is read once per call
         int stage = 0;
         uint32_t phase = 0;
         int issued = 0;
-        int gs = 0;  // stage number (MXFP8: picks the dequant set)
-        // MXFP8: per slot, the barriers it armed last and their phase parities
-        // (to wait out loads still in flight on failure); arm_* flip per arm
-        uint32_t last_d[kSt], last_b[kSt], last_dpar = 0, last_bpar = 0, arm_d[2] = {0, 0}, arm_b[2] = {0, 0};
         bool ok = true;
         TileStream ts;
         ts.next_static = blockIdx.x;
@@ -628,74 +588,30 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
             bool rows_ready = gcnt == nullptr || rows_seen || ld_acquire(gcnt) >= t.row_end - t.row0;
             if (MODE == kFused) fence_proxy_async_global();  // the rows are read by TMA (async proxy)
             int pend_stage[kSt], pend_kb[kSt], pending = 0;
-            uint32_t pend_bar[kSt];
             const int n_micro_k = sw ? 1 : g.n_micro;
             for (int mi = 0; ok && mi < n_micro_k; ++mi) {
                 const int m = sw ? t.m : mi;
                 const CUtensorMap* tw = sw ? &maps.w1[m] : &maps.w2[m];
-                const CUtensorMap* tsc = sw ? &maps.s1[m] : &maps.s2[m];  // MXFP8 scales
                 const CUtensorMap* tx = sw ? &maps.x1 : &maps.x2;
-                const int wrow = t.g * g.b_rows_per_group + t.nt * (sw ? 64 : kM);
-                constexpr int kK = F8 ? kF8K : kTcBK;                      // K per stage
-                const int kbn = F8 ? f8_stages(g.k_blocks) : g.k_blocks;  // stages per micro
-                // the token rows of a stage: one 64-K tile (four with MXFP8 weights)
-                auto load_rows = [&](int st, int kx, uint32_t bar) {
-                    const uint32_t sb = ptx::smem_u32(stage_b(st));
-                    if (F8)
-                        ptx::tma_load_3d(sb, tx, 0, t.row0, kx / kTcBK, bar);  // four 64-K tiles (brows rows each)
-                    else
-                        ptx::tma_load_2d(sb, tx, kx, t.row0, bar);
-                };
-                for (int kb = 0; kb < kbn; ++kb) {
+                const int wrow = t.g * g.b_rows_per_group + t.nt * kM;
+                for (int kb = 0; kb < g.k_blocks; ++kb) {
                     if (!ptx::mbar_wait(ptx::smem_u32(&c.empty[stage]), phase ^ 1u, g.limit_ns, &c.abort)) {
                         ok = false;
                         break;
                     }
                     const uint32_t sa = ptx::smem_u32(stage_a(stage));
-                    // MXFP8: codes and scales complete the barrier of the stage's dequant
-                    // set, the token rows that of its MMA issuer
-                    const int dset = gs & 1, iss = (mi * kbn + kb) & 1;
-                    const uint32_t fb = ptx::smem_u32(F8 ? &c.fullD[dset][stage] : &c.full[stage]);
-                    const uint32_t fbb = F8 ? ptx::smem_u32(&c.fullB[iss][stage]) : fb;
-                    if (F8) {
-                        last_d[stage] = fb;
-                        last_b[stage] = fbb;
-                        last_dpar = (last_dpar & ~(1u << stage)) | (((arm_d[dset] >> stage) & 1u) << stage);
-                        last_bpar = (last_bpar & ~(1u << stage)) | (((arm_b[iss] >> stage) & 1u) << stage);
-                        arm_d[dset] ^= 1u << stage;
-                        arm_b[iss] ^= 1u << stage;
-                        ptx::mbar_arrive_expect_tx(fb, kF8CodeBytes + kF8ScaleBytes);
-                        ptx::mbar_arrive_expect_tx(fbb, p.brows * 512);
-                    } else {
-                        ptx::mbar_arrive_expect_tx(fb, kStageBytes);
-                    }
-                    ++gs;
-                    if (F8) {
-                        // codes: two 128-K chunks of the tile's rows; scales: the eight
-                        // 32-blocks of those K (rows of the scale maps)
-                        const int srow = t.g * 2 * g.k_blocks + 8 * kb;
-                        const uint32_t ss = ptx::smem_u32(stage_s(stage));
-                        if (sw) {
-                            // per chunk: 64 gate rows, then the 64 matching up rows (half 2g + 1)
-                            ptx::tma_load_4d_hint(sa, tw, 0, t.nt * 64, 2 * t.g, 2 * kb, fb, wpol);
-                            ptx::tma_load_3d(ss, tsc, t.nt * 64, 0, srow, fb);
-                        } else {
-                            ptx::tma_load_3d_hint(sa, tw, 0, wrow, 2 * kb, fb, wpol);            // per chunk: 128 rows
-                            ptx::tma_load_2d(ss, tsc, t.nt * kM, srow, fb);
-                        }
-                    } else if (sw) {
-                        // 64 gate rows, then the 64 matching up rows (half 2g + 1 of the 3D map)
+                    const uint32_t fb = ptx::smem_u32(&c.full[stage]);
+                    ptx::mbar_arrive_expect_tx(fb, kStageBytes);
+                    if (sw)  // 64 gate rows, then the 64 matching up rows (half 2g + 1 of the 3D map)
                         ptx::tma_load_3d_hint(sa, tw, kb * kTcBK, t.nt * 64, 2 * t.g, fb, wpol);
-                    } else {
-                        ptx::tma_load_2d_hint(sa, tw, kb * kTcBK, wrow, fb, wpol);            // 128 rows
-                    }
-                    const int kx = (sw ? 0 : m * g.a_micro_cols) + kb * kK;
+                    else
+                        ptx::tma_load_2d_hint(sa, tw, kb * kTcBK, wrow, fb, wpol);  // 128 rows
+                    const int kx = (sw ? 0 : m * g.a_micro_cols) + kb * kTcBK;
                     if (rows_ready) {
-                        load_rows(stage, kx, fbb);  // 16 token rows
+                        ptx::tma_load_2d(ptx::smem_u32(stage_b(stage)), tx, kx, t.row0, fb);  // 16 token rows
                     } else {
                         pend_stage[pending] = stage;
                         pend_kb[pending] = kx;
-                        pend_bar[pending] = fbb;
                         ++pending;
                     }
                     ++issued;
@@ -703,21 +619,14 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
                         stage = 0;
                         phase ^= 1u;
                     }
-                    if (!rows_ready && (pending == kSt || kb + 1 == kbn)) {
+                    if (!rows_ready && (pending == kSt || kb + 1 == g.k_blocks)) {
                         // every free stage holds weights: wait for the rows, then
                         // complete the pending stages with their token rows
-                        const uint64_t t0 = ptx::globaltimer();
-                        uint32_t it = 0;
-                        while (ld_acquire(gcnt) < t.row_end - t.row0) {
-                            if ((++it & 15u) == 0u && (c.abort || ptx::globaltimer() - t0 > g.limit_ns)) {
-                                ok = false;
-                                break;
-                            }
-                            __nanosleep(32);
-                        }
+                        if (!wait_count(gcnt, t.row_end - t.row0, c, g.limit_ns)) ok = false;
                         fence_proxy_async_global();
                         for (int q = 0; q < pending; ++q)  // completes the armed stages even on failure
-                            load_rows(pend_stage[q], pend_kb[q], pend_bar[q]);
+                            ptx::tma_load_2d(ptx::smem_u32(stage_b(pend_stage[q])), tx, pend_kb[q], t.row0,
+                                             ptx::smem_u32(&c.full[pend_stage[q]]));
                         pending = 0;
                         rows_ready = true;
                         if (!ok) break;
@@ -731,19 +640,125 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
                 break;
             }
         }
-        if (!ok) {
-            fail(c, a0.err);
-            const int n = issued < kSt ? issued : kSt;
-            // slot s was last armed in this pass of the ring if s < stage, else in the previous one
-            for (int s = 0; s < n; ++s) {
-                if (F8) {
-                    ptx::mbar_wait(last_d[s], (last_dpar >> s) & 1u, a0.limit_ns, nullptr);
-                    ptx::mbar_wait(last_b[s], (last_bpar >> s) & 1u, a0.limit_ns, nullptr);
-                } else {
-                    ptx::mbar_wait(ptx::smem_u32(&c.full[s]), s < stage ? phase : phase ^ 1u, a0.limit_ns, nullptr);
+        if (!ok) fail(c, a0.err);
+        // no load outlives the kernel, even one that an aborted MMA never took:
+        // slot s was last armed in this pass of the ring if s < stage, else in
+        // the previous one (a wait on a completed phase returns at once)
+        const int n = issued < kSt ? issued : kSt;
+        for (int s = 0; s < n; ++s)
+            ptx::mbar_wait(ptx::smem_u32(&c.full[s]), s < stage ? phase : phase ^ 1u, a0.limit_ns, nullptr);
+    } else if (F8 && warp == 0 && lane == 0) {
+        // ------------------------------------------------ MXFP8 weight producer (ring A)
+        const uint64_t wpol = ptx::policy_evict_first();  // each weight byte is read once per call
+        int stage = 0;
+        uint32_t phase = 0;
+        int issued = 0;
+        bool ok = true;
+        TileStream ts;
+        uint32_t sq_phase = 0;
+        for (;;) {
+            bool rows_seen = false;
+            const int next = pop_scheduled(c, sq_phase, a0.limit_ns, rows_seen, ok);
+            const int tile = produce_tile<MODE>(c, ts, total, next, a0.limit_ns, ok);
+            if (tile < 0) break;
+            bool sw;
+            const Tile t = locate<MODE>(tile, c, p, sw);
+            const TcGemmArgs& g = sw ? p.g1 : p.g2;
+            const int n_micro_k = sw ? 1 : g.n_micro;
+            for (int mi = 0; ok && mi < n_micro_k; ++mi) {
+                const int m = sw ? t.m : mi;
+                for (int kb = 0; kb < f8_stages(g.k_blocks); ++kb) {
+                    if (!ptx::mbar_wait(ptx::smem_u32(&c.empty[stage]), phase ^ 1u, g.limit_ns, &c.abort)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = ptx::smem_u32(stage_a(stage)), ss = sa + kF8CodeBytes;
+                    const uint32_t fb = ptx::smem_u32(&c.full[stage]);
+                    ptx::mbar_arrive_expect_tx(fb, kF8SlotA);
+                    // codes: two 128-K chunks of the tile's rows; scales: the eight
+                    // 32-blocks of those K (rows of the scale maps). A half stage
+                    // (K an odd multiple of 128) reads zeros or the next block's
+                    // codes past the weights, which no MMA consumes.
+                    const int srow = t.g * 2 * g.k_blocks + 8 * kb;
+                    if (sw) {
+                        // per chunk: 64 gate rows, then the 64 matching up rows (half 2g + 1)
+                        ptx::tma_load_4d_hint(sa, &maps.w1[m], 0, t.nt * 64, 2 * t.g, 2 * kb, fb, wpol);
+                        ptx::tma_load_3d(ss, &maps.s1[m], t.nt * 64, 0, srow, fb);
+                    } else {
+                        const int wrow = t.g * g.b_rows_per_group + t.nt * kM;
+                        ptx::tma_load_3d_hint(sa, &maps.w2[m], 0, wrow, 2 * kb, fb, wpol);  // per chunk: 128 rows
+                        ptx::tma_load_2d(ss, &maps.s2[m], t.nt * kM, srow, fb);
+                    }
+                    ++issued;
+                    if (++stage == kSt) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
                 }
             }
+            if (!ok) {
+                c.abort = 1;
+                produce_tile<MODE>(c, ts, total, -1, a0.limit_ns, ok);
+                break;
+            }
         }
+        if (!ok) fail(c, a0.err);
+        const int n = issued < kSt ? issued : kSt;  // as the bf16 producer
+        for (int s = 0; s < n; ++s)
+            ptx::mbar_wait(ptx::smem_u32(&c.full[s]), s < stage ? phase : phase ^ 1u, a0.limit_ns, nullptr);
+    } else if (F8 && warp == 2 && lane == 0) {
+        // ------------------------------------------------ MXFP8 token-row producer (ring B)
+        // Per stage the 16 rows' codes of the stage's 256 K (3D box: two 128-K
+        // chunks) and their scale bytes (16 per row: the 512 K around the
+        // stage, of which it uses half). A SwiGLU tile's rows are loaded once
+        // the gather phase counted all rows of its expert; a down tile's h rows
+        // were complete when the scheduler handed the tile out.
+        int stage = 0;
+        uint32_t phase = 0;
+        int issued = 0;
+        bool ok = true;
+        TileStream ts;
+        for (;;) {
+            const int tile = consume_tile<MODE>(c, ts, total, a0.limit_ns);
+            if (tile < 0) break;
+            bool sw;
+            const Tile t = locate<MODE>(tile, c, p, sw);
+            const TcGemmArgs& g = sw ? p.g1 : p.g2;
+            if (sw && p.gx != nullptr &&
+                !wait_count(p.done + 2 * p.g1.G + 1 + t.g, t.row_end - t.row0, c, g.limit_ns)) {
+                ok = false;
+                break;
+            }
+            fence_proxy_async_global();  // the rows are read by TMA (async proxy)
+            const CUtensorMap* tx = sw ? &maps.x1 : &maps.x2;
+            const CUtensorMap* tsx = sw ? &maps.xs1 : &maps.xs2;
+            const int n_micro_k = sw ? 1 : g.n_micro;
+            for (int mi = 0; ok && mi < n_micro_k; ++mi) {
+                const int m = sw ? 0 : mi;
+                for (int kb = 0; kb < f8_stages(g.k_blocks); ++kb) {
+                    if (!ptx::mbar_wait(ptx::smem_u32(&c.emptyB[stage]), phase ^ 1u, g.limit_ns, &c.abort)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sb = ptx::smem_u32(stage_b(stage));
+                    const uint32_t fb = ptx::smem_u32(&c.fullB[stage]);
+                    ptx::mbar_arrive_expect_tx(fb, kF8BCodeBytes + kF8BScaleBytes);
+                    const int kx = (sw ? 0 : m * g.a_micro_cols) + kb * kF8K;
+                    ptx::tma_load_3d(sb, tx, 0, t.row0, kx / 128, fb);
+                    ptx::tma_load_3d(sb + kF8BCodeBytes, tsx, (8 * kb) & ~15, t.row0, m, fb);
+                    ++issued;
+                    if (++stage == kF8StagesB) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) break;
+        }
+        if (!ok) fail(c, a0.err);
+        const int n = issued < kF8StagesB ? issued : kF8StagesB;  // as the bf16 producer
+        for (int s = 0; s < n; ++s)
+            ptx::mbar_wait(ptx::smem_u32(&c.fullB[s]), s < stage ? phase : phase ^ 1u, a0.limit_ns, nullptr);
     } else if (MODE == kFused && warp == 3 && lane == 0) {
         // ------------------------------------------------ scheduler
         schedule_tiles(c, p, total);
@@ -810,21 +825,18 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
             ptx::mbar_wait(ptx::smem_u32(&c.drain), 0, a0.limit_ns, nullptr);
         }
         __syncwarp();
-    } else if (F8 && (warp == 1 || warp == 2)) {
-        // ------------------------------------------------ MXFP8 MMA issuers
-        // Issuer j (warp 1 + j) takes the tile's stages of parity j into half j
-        // of its accumulator; the epilogue adds the halves (half 0 + half 1,
-        // the same order on every call). With N = 16 the stream rate is set by
-        // how fast tcgen05 instructions are issued (eight MMAs and two commits
-        // per stage), so two issuing warps raise it. Each runs as a whole warp
-        // with one elected lane issuing, as the bf16 issuer above.
+    } else if (F8 && warp == 1) {
+        // ------------------------------------------------ MXFP8 MMA issuer
+        // Per stage: the codes and weight scales (ring A), the token rows (ring
+        // B) and the stage's scales in tensor memory (the scale warps, one
+        // buffer per ring A slot); per 128-K chunk four MMAs of K = 32, the
+        // scale byte picked by the instruction descriptor. Whole warp in the
+        // loop, one elected lane issuing, as the bf16 issuer.
         const bool issuer = ptx::elect_one();
-        const int j = warp - 1;
-        int stage = 0, dq = 0, gs = 0;  // code slot, A buffer, stage number
-        uint32_t fb_bits = 0, dq_bits = 0;  // phase bits of this issuer's fullB / dq_full barriers
+        int sa = 0, sb = 0;
+        uint32_t pa = 0, pb = 0;
         bool ok = true;
         TileStream ts;
-        ts.next_static = blockIdx.x;
         for (int local = 0; ok; ++local) {
             int tile = -1;
             if (lane == 0) tile = consume_tile<MODE>(c, ts, total, a0.limit_ns);
@@ -835,81 +847,74 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
             const TcGemmArgs& g = sw ? p.g1 : p.g2;
             const int acc = local & 1;
             const uint32_t acc_par = (uint32_t)(local >> 1) & 1u;
-            // the accumulator is free once the epilogue read the tile two back
-            // (waited for even without own stages: the commit to tfull below must
-            // land in this tile's phase)
             const bool drained = ptx::mbar_wait(ptx::smem_u32(&c.tempty[acc]), acc_par ^ 1u, g.limit_ns, &c.abort);
             if (!__all_sync(0xffffffffu, drained)) {
                 ok = false;
                 break;
             }
             ptx::tc_fence_after();
-            const uint32_t d = tmem + (uint32_t)(acc * 2 * kTok + j * kTok);
+            const uint32_t d = tmem + (uint32_t)(acc * kTok);
             uint32_t accumulate = 0;
-            const int nk = (sw ? 1 : g.n_micro) * f8_stages(g.k_blocks);
-            for (int i = 0; i < nk; ++i) {
-                if ((i & 1) == j) {
-                    const bool got = ptx::mbar_wait(ptx::smem_u32(&c.fullB[j][stage]), (fb_bits >> stage) & 1u,
-                                                    g.limit_ns, &c.abort) &&
-                                     ptx::mbar_wait(ptx::smem_u32(&c.dq_full[j][dq]), (dq_bits >> dq) & 1u,
-                                                    g.limit_ns, &c.abort);
+            const int n_micro_k = sw ? 1 : g.n_micro;
+            for (int mi = 0; ok && mi < n_micro_k; ++mi) {
+                const int chunks = g.k_blocks / 2;  // 128-K chunks of a micro's K
+                for (int kb = 0; kb < f8_stages(g.k_blocks); ++kb) {
+                    const bool got = ptx::mbar_wait(ptx::smem_u32(&c.full[sa]), pa, g.limit_ns, &c.abort) &&
+                                     ptx::mbar_wait(ptx::smem_u32(&c.fullB[sb]), pb, g.limit_ns, &c.abort) &&
+                                     ptx::mbar_wait(ptx::smem_u32(&c.sf_full[sa]), pa, g.limit_ns, &c.abort);
                     if (!__all_sync(0xffffffffu, got)) {
                         ok = false;
                         break;
                     }
-                    fb_bits ^= 1u << stage;
-                    dq_bits ^= 1u << dq;
                     ptx::tc_fence_after();
-                    // A buffer dq: 8 columns per 16 K; 64-K chunk h pairs with token tile h
-                    const uint32_t at = tmem + (uint32_t)(kF8ACol + dq * kF8ABuf);
-                    const uint32_t sb0 = ptx::smem_u32(stage_b(stage));
+                    const int nch = chunks - 2 * kb < 2 ? chunks - 2 * kb : 2;
                     if (issuer) {
-                        uint32_t acc_flag = accumulate;
+                        for (int ch = 0; ch < nch; ++ch) {
+                            const uint64_t ad = ptx::sw128_desc(ptx::smem_u32(stage_a(sa)) + ch * (kM * 128));
+                            const uint64_t bd = ptx::sw128_desc(ptx::smem_u32(stage_b(sb)) + ch * (kTok * 128));
+                            const uint32_t sf = tmem + (uint32_t)(kF8SfCol + 32 * sa + 16 * ch);
 #pragma unroll
-                        for (int h = 0; h < kF8Chunks; ++h) {
-                            // the second 64-K tile starts after the first one's brows rows
-                            const uint64_t bd = ptx::sw128_desc(sb0 + h * p.brows * 128);
-#pragma unroll
-                            for (int k = 0; k < kTcBK / 16; ++k) {
-                                ptx::mma_tmem_a(d, at + 32u * h + 8u * k, bd + 2u * k, kIdescF16, acc_flag);
-                                acc_flag = 1;
+                            for (int k = 0; k < 4; ++k) {
+                                ptx::mma_mx(d, ad + 2u * k, bd + 2u * k, ptx::idesc_mx(kM, kTok, k, k), sf, sf + 8u,
+                                            accumulate);
+                                accumulate = 1;
                             }
                         }
-                        ptx::mma_commit(ptx::smem_u32(&c.empty[stage]));  // the code slot (codes, scales, rows)
-                        // the A buffer, for the dequant set that writes it next
-                        ptx::mma_commit(ptx::smem_u32(&c.dq_empty[(gs + kF8Dq) & 1][dq]));
+                        ptx::mma_commit(ptx::smem_u32(&c.empty[sa]));   // codes and weight scales
+                        ptx::mma_commit(ptx::smem_u32(&c.emptyB[sb]));  // token rows
                     }
                     __syncwarp();
                     accumulate = 1;
+                    if (++sa == kSt) {
+                        sa = 0;
+                        pa ^= 1u;
+                    }
+                    if (++sb == kF8StagesB) {
+                        sb = 0;
+                        pb ^= 1u;
+                    }
                 }
-                ++gs;
-                if (++stage == kSt) stage = 0;
-                if (++dq == kF8Dq) dq = 0;
             }
             if (ok && issuer) ptx::mma_commit(ptx::smem_u32(&c.tfull[acc]));
             __syncwarp();
         }
         if (issuer) {
             if (!ok) fail(c, a0.err);
-            uint64_t* dr = j ? &c.drain2 : &c.drain;
-            ptx::mma_commit(ptx::smem_u32(dr));
-            ptx::mbar_wait(ptx::smem_u32(dr), 0, a0.limit_ns, nullptr);
+            ptx::mma_commit(ptx::smem_u32(&c.drain));
+            ptx::mbar_wait(ptx::smem_u32(&c.drain), 0, a0.limit_ns, nullptr);
         }
         __syncwarp();
     } else if (F8 && warp >= 8) {
-        // ------------------------------------------------ MXFP8 dequant
-        // warp 8 + 4 j + q owns TMEM lanes 32 q .. 32 q + 31 (weight rows, one
-        // per thread) of the stages of parity j: its thread reads the row's 128
-        // codes and 4 scales, converts them in registers and stores the 64 f16
-        // pairs into the row's lane of the A buffer
-        const int q = warp & 3, par = (warp - 8) >> 2;
-        const int r = q * 32 + lane;
-        const uint32_t a_lanes = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)kF8ACol;
-        int stage = 0, dq = 0, kseq = 0;  // code slot, A buffer, stage number
-        uint32_t fd_bits = 0, de_bits = 0;  // phase bits of this set's fullD / dq_empty barriers
+        // ------------------------------------------------ MXFP8 scale warps
+        // Warp 8 + q writes lane quarter q of the stage's scale buffer (every
+        // quarter holds the same words): per 128-K chunk, the weight rows'
+        // words (row lane + 32 j in column j; byte i: 32-block i of the chunk)
+        // and the token rows' word (row lane in column 8; lanes past 16 zero).
+        const int q = warp & 3;
+        int sa = 0, sb = 0;
+        uint32_t pa = 0, pb = 0;
         bool ok = true;
         TileStream ts;
-        ts.next_static = blockIdx.x;
         for (;;) {
             int tile = -1;
             if (lane == 0) tile = consume_tile<MODE>(c, ts, total, a0.limit_ns);
@@ -918,66 +923,50 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
             bool sw;
             locate<MODE>(tile, c, p, sw);
             const TcGemmArgs& g = sw ? p.g1 : p.g2;
-            const int nk = (sw ? 1 : g.n_micro) * f8_stages(g.k_blocks);
-            for (int i = 0; i < nk; ++i, ++kseq) {
-                if ((kseq & 1) == par) {
-                    // the buffer's first use needs no free signal; later ones wait for the
-                    // MMAs of its previous use, committed to this set
-                    const bool first_use = kseq < kF8Dq;
-                    bool got = ptx::mbar_wait(ptx::smem_u32(&c.fullD[par][stage]), (fd_bits >> stage) & 1u,
-                                              g.limit_ns, &c.abort) &&
-                               (first_use || ptx::mbar_wait(ptx::smem_u32(&c.dq_empty[par][dq]), (de_bits >> dq) & 1u,
-                                                            g.limit_ns, &c.abort));
-                    fd_bits ^= 1u << stage;
-                    if (!first_use) de_bits ^= 1u << dq;
+            const int n_micro_k = sw ? 1 : g.n_micro;
+            for (int mi = 0; ok && mi < n_micro_k; ++mi) {
+                for (int kb = 0; kb < f8_stages(g.k_blocks); ++kb) {
+                    const bool got = ptx::mbar_wait(ptx::smem_u32(&c.full[sa]), pa, g.limit_ns, &c.abort) &&
+                                     ptx::mbar_wait(ptx::smem_u32(&c.fullB[sb]), pb, g.limit_ns, &c.abort);
                     if (!__all_sync(0xffffffffu, got)) {
                         ok = false;
                         break;
                     }
+                    // weight scales [8 blocks][128 rows]; token-row scale bytes
+                    // [16 rows][16], this stage's eight at 8 * (kb & 1)
+                    const unsigned char* sp = stage_a(sa) + kF8CodeBytes;
+                    const unsigned char* bp = stage_b(sb) + kF8BCodeBytes + 8 * (kb & 1);
                     ptx::tc_fence_after();
-                    // the stage's two 128-K code chunks, one at a time (so only one
-                    // chunk's codes and one half's f16 pairs are live)
-#pragma unroll 1
-                    for (int kc = 0; kc < kF8K / 128; ++kc) {
-                        // 16-byte piece j of row r sits at piece j ^ (r % 8) (128-byte swizzle)
-                        const unsigned char* row = stage_a(stage) + kc * (kM * 128) + r * 128;
-                        uint4 cv[8];
 #pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            cv[j] = *reinterpret_cast<const uint4*>(row + ((j ^ (r & 7)) << 4));
-                        // scales [8][128 rows] (SwiGLU tiles: each block's 64 gate rows, then its 64 up rows)
-                        const unsigned char* sp = stage_s(stage) + kc * 4 * kM;
-                        int sc[4];
+                    for (int ch = 0; ch < 2; ++ch) {
+                        uint32_t wa[4];
 #pragma unroll
-                        for (int b = 0; b < 4; ++b) sc[b] = sp[b * kM + r];
-                        bool slow = false;
-#pragma unroll
-                        for (int b = 0; b < 4; ++b) slow |= !dequant_in_f16(sc[b]);
-                        // two halves of 64 K (32 columns each)
-#pragma unroll
-                        for (int hf = 0; hf < 2; ++hf) {
-                            uint32_t o[32];
-#pragma unroll
-                            for (int j = 0; j < 4; ++j)
-                                dequant16_f16(cv[4 * hf + j], sc[2 * hf + (j >> 1)], o + 8 * j);
-                            if (slow) {  // rare: scales that are not f16 numbers
-#pragma unroll
-                                for (int j = 0; j < 4; ++j)
-                                    if (!dequant_in_f16(sc[2 * hf + (j >> 1)]))
-                                        dequant16_f32(cv[4 * hf + j], sc[2 * hf + (j >> 1)], o + 8 * j);
-                            }
-                            __syncwarp();
-                            ptx::tmem_st32(a_lanes + (uint32_t)(dq * kF8ABuf + 64 * kc + 32 * hf), o);
+                        for (int j = 0; j < 4; ++j) {
+                            const int r = lane + 32 * j;
+                            wa[j] = (uint32_t)sp[(4 * ch) * kM + r] | ((uint32_t)sp[(4 * ch + 1) * kM + r] << 8) |
+                                    ((uint32_t)sp[(4 * ch + 2) * kM + r] << 16) |
+                                    ((uint32_t)sp[(4 * ch + 3) * kM + r] << 24);
                         }
+                        const uint32_t wb =
+                            lane < kTok ? *reinterpret_cast<const uint32_t*>(bp + 16 * lane + 4 * ch) : 0u;
+                        const uint32_t col =
+                            tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(kF8SfCol + 32 * sa + 16 * ch);
+                        ptx::tmem_st4(col, wa[0], wa[1], wa[2], wa[3]);
+                        ptx::tmem_st1(col + 8u, wb);
                     }
                     ptx::tmem_wait_st();
                     ptx::tc_fence_before();
                     __syncwarp();
-                    // for the MMA issuer of the stage (its index in the tile picks it)
-                    if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&c.dq_full[i & 1][dq]));
+                    if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&c.sf_full[sa]));
+                    if (++sa == kSt) {
+                        sa = 0;
+                        pa ^= 1u;
+                    }
+                    if (++sb == kF8StagesB) {
+                        sb = 0;
+                        pb ^= 1u;
+                    }
                 }
-                if (++stage == kSt) stage = 0;
-                if (++dq == kF8Dq) dq = 0;
             }
             if (!ok) break;
         }
@@ -1014,18 +1003,7 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
             }
             ptx::tc_fence_after();
             uint32_t v[kTok];
-            if (F8) {
-                // two halves (the tile's even and odd stages); a tile of one stage
-                // filled only half 0
-                uint32_t v2[2 * kTok];
-                ptx::tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * 2 * kTok), v2);
-                const bool both = (sw ? 1 : g.n_micro) * f8_stages(g.k_blocks) >= 2;
-#pragma unroll
-                for (int jj = 0; jj < kTok; ++jj)
-                    v[jj] = both ? __float_as_uint(__uint_as_float(v2[jj]) + __uint_as_float(v2[kTok + jj])) : v2[jj];
-            } else {
-                ptx::tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kTok), v);
-            }
+            ptx::tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kTok), v);
             // the accumulator is in registers: hand it back to the MMA issuer
             ptx::tc_fence_before();
             __syncwarp();
@@ -1041,10 +1019,22 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
                     const int64_t col = (int64_t)t.m * g.out_micro_cols + t.nt * 64 + r;
                     for (int j = 0; j < cnt; ++j) {
                         const float h = silu(__uint_as_float(v[j])) * c.up[r][j];
-                        if (F8)  // the down tiles' B operand is f16 when the weights are MXFP8
-                            reinterpret_cast<__half*>(out)[(int64_t)(t.row0 + j) * g.out_ld + col] = __float2half_rn(h);
-                        else
+                        if (F8) {
+                            // h in MXFP8 for the down tiles: warp q holds the 32-block
+                            // 2 nt + q of micro m's features; the block's scale from
+                            // the largest |h| taken at h's bf16 value
+                            const float hb = __bfloat162float(__float2bfloat16_rn(h));
+                            const uint32_t amax = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hb)));
+                            const int shared = mx_shared_exp(__uint_as_float(amax));
+                            const int64_t row = t.row0 + j;
+                            reinterpret_cast<unsigned char*>(out)[row * g.out_ld + col] =
+                                (unsigned char)e4m3x2(hb * pow2f(-shared), 0.f);
+                            if (lane == 0)
+                                p.hs[((int64_t)t.m * c.seg[g.G] + row) * p.hs_pitch + 2 * t.nt + q] =
+                                    (unsigned char)(shared + 127);
+                        } else {
                             out[(int64_t)(t.row0 + j) * g.out_ld + col] = __float2bfloat16_rn(h);
+                        }
                     }
                     if (MODE == kFused) fence_proxy_async_global();
                 }
@@ -1073,7 +1063,7 @@ __global__ void __launch_bounds__(F8 ? kF8Threads : kThreads, 1)
     ptx::tc_fence_before();
     __syncthreads();
     if (warp == 2) {
-        __syncwarp();  // lane 0 ran the second MMA issuer (MXFP8)
+        __syncwarp();  // lane 0 ran the token-row producer (MXFP8)
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, F8 ? kF8TmemCols : kTmemCols);
     }
@@ -1125,7 +1115,7 @@ cudaError_t launch_tc_small_swiglu(const TcGemmArgs& a, const CUtensorMap& tmX, 
     SmallMaps maps{};
     fill_maps(maps, tmX, tmW, a.n_micro, true);
     fill_maps(maps, tmX, tmW, 1, false);  // unused slots
-    SmallParams p{a, a, nullptr, FinalizeArgs{}, nullptr, nullptr, nullptr, 0, 0};
+    SmallParams p{a, a, nullptr, FinalizeArgs{}, nullptr, nullptr, nullptr, 0, 0, nullptr, 0, nullptr, 0};
     return launch_small<kSwiGLUOnly>(maps, p, a.max_tiles, num_sms, s);
 }
 
@@ -1134,7 +1124,7 @@ cudaError_t launch_tc_small_down(const TcGemmArgs& a, const CUtensorMap& tmX, co
     SmallMaps maps{};
     fill_maps(maps, tmX, tmW, a.n_micro, false);
     fill_maps(maps, tmX, tmW, 1, true);  // unused slots
-    SmallParams p{a, a, nullptr, FinalizeArgs{}, nullptr, nullptr, nullptr, 0, 0};
+    SmallParams p{a, a, nullptr, FinalizeArgs{}, nullptr, nullptr, nullptr, 0, 0, nullptr, 0, nullptr, 0};
     return launch_small<kDownOnly>(maps, p, a.max_tiles, num_sms, s);
 }
 
@@ -1145,15 +1135,15 @@ cudaError_t launch_tc_small_fused(const TcGemmArgs& g1, const CUtensorMap& tmX1,
     SmallMaps maps{};
     fill_maps(maps, tmX1, tmW1, g1.n_micro, true);
     fill_maps(maps, tmX2, tmW2, g2.n_micro, false);
-    SmallParams p{g1, g2, done, fin, gat.x, gat.xp, gat.perm, gat.k, (int)gat.row_bytes};
+    SmallParams p{g1, g2, done, fin, gat.x, gat.xp, gat.perm, gat.k, (int)gat.row_bytes, nullptr, 0, nullptr, 0};
     return launch_small<kFused>(maps, p, g1.max_tiles + g2.max_tiles, num_sms, s);
 }
 
-cudaError_t launch_tc_small_fused_mxfp8(const TcGemmArgs& g1, const CUtensorMap& tmX1, const CUtensorMap* tmW1,
-                                        const CUtensorMap* tmS1, const TcGemmArgs& g2, const CUtensorMap& tmX2,
-                                        const CUtensorMap* tmW2, const CUtensorMap* tmS2, const FinalizeArgs& fin,
-                                        const GatherArgs& gat, int brows, int* done, int num_sms,
-                                        cudaStream_t s) {
+cudaError_t launch_tc_small_fused_mxfp8(const TcGemmArgs& g1, const CUtensorMap& tmX1, const CUtensorMap& tmXS1,
+                                        const CUtensorMap* tmW1, const CUtensorMap* tmS1, const TcGemmArgs& g2,
+                                        const CUtensorMap& tmX2, const CUtensorMap& tmXS2, const CUtensorMap* tmW2,
+                                        const CUtensorMap* tmS2, const FinalizeArgs& fin, const GatherArgs& gat,
+                                        const MxSmallActs& act, int* done, int num_sms, cudaStream_t s) {
     SmallMaps maps{};
     fill_maps(maps, tmX1, tmW1, g1.n_micro, true);
     fill_maps(maps, tmX2, tmW2, g2.n_micro, false);
@@ -1161,7 +1151,10 @@ cudaError_t launch_tc_small_fused_mxfp8(const TcGemmArgs& g1, const CUtensorMap&
         maps.s1[i] = tmS1[i < g1.n_micro ? i : 0];
         maps.s2[i] = tmS2[i < g2.n_micro ? i : 0];
     }
-    SmallParams p{g1, g2, done, fin, gat.x, gat.xp, gat.perm, gat.k, (int)gat.row_bytes, brows};
+    maps.xs1 = tmXS1;
+    maps.xs2 = tmXS2;
+    SmallParams p{g1,  g2,         done,   fin,         gat.x, gat.xp, gat.perm, gat.k, (int)gat.row_bytes,
+                  act.xs, act.xs_pitch, act.hs, act.hs_pitch};
     return launch_small<kFused, true>(maps, p, g1.max_tiles + g2.max_tiles, num_sms, s);
 }
 

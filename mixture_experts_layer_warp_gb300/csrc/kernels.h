@@ -271,17 +271,27 @@ cudaError_t launch_tc_small_down(const TcGemmArgs& a, const CUtensorMap& tmX, co
 // gathers xp from x (gat.x non-null). done[fused_counter_ints(E)] must be zero
 // at launch (the small-batch router zeroes it).
 inline int fused_counter_ints(int E) { return 3 * E + 2; }
-// The same with MXFP8 expert weights: tmX1 / tmX2 map the f16 token rows as
-// 3D maps {64, rows, K/64} with box {64, brows, 2} (brows = 8 when the batch
-// has at most 8 tokens, else 16), tmW1[m] the w13 E4M3 codes as a 3D map
-// {H, I, 2E} with box {128, 64, 2} (gate rows, then the matching up rows),
-// tmW2[m] the w2 codes [E*H][I] (box {128, 128}), tmS1[m] the w13 scales as a
-// 3D map {I, 2, E*H/32} with box {64, 2, 4}, tmS2[m] the w2 scales
-// [E*I/32][H] (box {128, 4}); gat.xp and g1.out (h) hold f16.
-cudaError_t launch_tc_small_fused_mxfp8(const TcGemmArgs& g1, const CUtensorMap& tmX1, const CUtensorMap* tmW1,
-                                        const CUtensorMap* tmS1, const TcGemmArgs& g2, const CUtensorMap& tmX2,
-                                        const CUtensorMap* tmW2, const CUtensorMap* tmS2, const FinalizeArgs& fin,
-                                        const GatherArgs& gat, int brows, int* done, int num_sms, cudaStream_t s);
+// The same with MXFP8 expert weights, on the block-scaled FP8 MMA: the token
+// rows and h in MXFP8 too. tmX1 / tmX2 map the codes of the gathered rows
+// (gat.xp, [R][H]) and of h (g1.out, [R][M*I]) as 3D maps {128, R, K/128}
+// with box {128, 16, 2}; tmXS1 / tmXS2 their scale bytes act.xs [R][xs_pitch]
+// and act.hs [M][R][hs_pitch] (pitches multiples of 16) as 3D maps {pitch, R,
+// 1 or M} with box {16, 16, 1}; tmW1[m] the w13 codes as a 4D map {128, I, 2E,
+// H/128} with box {128, 64, 2, 2} (per 128-K chunk: gate rows, then the
+// matching up rows), tmW2[m] the w2 codes as a 3D map {128, E*H, I/128} with
+// box {128, 128, 2}, tmS1[m] the w13 scales as a 3D map {I, 2, E*H/32} with box
+// {64, 2, 8}, tmS2[m] the w2 scales [E*I/32][H] (box {128, 8}).
+struct MxSmallActs {
+    unsigned char* xs;
+    int xs_pitch;
+    unsigned char* hs;
+    int hs_pitch;
+};
+cudaError_t launch_tc_small_fused_mxfp8(const TcGemmArgs& g1, const CUtensorMap& tmX1, const CUtensorMap& tmXS1,
+                                        const CUtensorMap* tmW1, const CUtensorMap* tmS1, const TcGemmArgs& g2,
+                                        const CUtensorMap& tmX2, const CUtensorMap& tmXS2, const CUtensorMap* tmW2,
+                                        const CUtensorMap* tmS2, const FinalizeArgs& fin, const GatherArgs& gat,
+                                        const MxSmallActs& act, int* done, int num_sms, cudaStream_t s);
 cudaError_t launch_tc_small_fused(const TcGemmArgs& g1, const CUtensorMap& tmX1, const CUtensorMap* tmW1,
                                   const TcGemmArgs& g2, const CUtensorMap& tmX2, const CUtensorMap* tmW2,
                                   const FinalizeArgs& fin, const GatherArgs& gat, int* done, int num_sms,

@@ -376,17 +376,30 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
         // router zeroed h->done); the shared expert's GEMMs ran first
         FinalizeArgs fin{h->obuf, h->inv, h->topw, Is > 0 ? h->sbuf : nullptr, T, k, H, true, y, h->accumulate};
         if (mx != nullptr) {
-            // MXFP8: the code and scale maps replace the bf16 weight maps; a
-            // 256-K stage is one box per operand: w13 codes as a 4D map {128, I,
-            // 2E, H/128} (per 128-K chunk: 64 gate rows, then the matching up
-            // rows), w2 codes as a 3D map {128, E*H, I/128}, their scales (eight
-            // 32-blocks), and four 64-K chunks of the token rows
-            CUtensorMap c1[kMaxMicro], c2[kMaxMicro], s1[kMaxMicro], s2[kMaxMicro], mX, mX2;
-            const uint64_t xd[3] = {64, (uint64_t)R, (uint64_t)H / 64}, xs[2] = {(uint64_t)H * 2, 128};
-            const uint64_t hd[3] = {64, (uint64_t)R, (uint64_t)M * I / 64}, hs[2] = {(uint64_t)M * I * 2, 128};
-            const int brows = T <= 8 ? 8 : kSmallTokens;  // no expert owns more routes than T
-            const uint32_t xb[3] = {64, (uint32_t)brows, 4};
-            if (!encode_3d(&mX, true, h->xp, xd, xs, xb, true) || !encode_3d(&mX2, true, h->hbuf, hd, hs, xb, true))
+            // MXFP8: the block-scaled FP8 MMA on MXFP8 token rows and h. The
+            // gather phase writes the rows' codes [R][H] at xp and their scale
+            // bytes [R][xs_pitch] after them; the SwiGLU epilogue writes h's
+            // codes [R][M*I] at hbuf and its scale bytes [M][R][hs_pitch] after
+            // them. A 256-K stage is one box per operand: w13 codes as a 4D map
+            // {128, I, 2E, H/128} (per 128-K chunk: 64 gate rows, then the
+            // matching up rows), w2 codes as a 3D map {128, E*H, I/128}, their
+            // scales (eight 32-blocks), the 16 token rows' codes (two 128-K
+            // chunks) and their scale bytes (16 per row).
+            CUtensorMap c1[kMaxMicro], c2[kMaxMicro], s1[kMaxMicro], s2[kMaxMicro], mX, mX2, mXS, mHS;
+            const int xs_pitch = (int)round_up((size_t)H / 32, 16), hs_pitch = (int)round_up((size_t)I / 32, 16);
+            unsigned char* xq = static_cast<unsigned char*>(h->xp);
+            unsigned char* hq = static_cast<unsigned char*>(h->hbuf);
+            unsigned char* xs = xq + mx_scales_off(R, H);
+            unsigned char* hsc = hq + mx_scales_off(R, (int64_t)M * I);
+            const uint64_t xd[3] = {128, (uint64_t)R, (uint64_t)H / 128}, xst[2] = {(uint64_t)H, 128};
+            const uint64_t hd[3] = {128, (uint64_t)R, (uint64_t)M * I / 128}, hst[2] = {(uint64_t)M * I, 128};
+            const uint32_t xb[3] = {128, (uint32_t)kSmallTokens, 2};
+            const uint64_t xsd[3] = {(uint64_t)xs_pitch, (uint64_t)R, 1}, xss[2] = {(uint64_t)xs_pitch, (uint64_t)R * xs_pitch};
+            const uint64_t hsd[3] = {(uint64_t)hs_pitch, (uint64_t)R, (uint64_t)M},
+                           hss[2] = {(uint64_t)hs_pitch, (uint64_t)R * hs_pitch};
+            const uint32_t sbx[3] = {16, (uint32_t)kSmallTokens, 1};
+            if (!encode_3d(&mX, false, xq, xd, xst, xb, true) || !encode_3d(&mX2, false, hq, hd, hst, xb, true) ||
+                !encode_3d(&mXS, false, xs, xsd, xss, sbx, false) || !encode_3d(&mHS, false, hsc, hsd, hss, sbx, false))
                 return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (MXFP8 token rows)");
             const uint64_t cd[4] = {128, (uint64_t)I, 2 * (uint64_t)E, (uint64_t)H / 128};
             const uint64_t cs[3] = {(uint64_t)H, (uint64_t)I * H, 128};
@@ -402,9 +415,10 @@ moe_status run_forward(moe_handle* h, const void* x, const void* router_w, const
                     !encode_u8_2d(&s2[m], mx->w2[m], H, (uint64_t)E * (I / 32), (uint64_t)H, 128, 8, false))
                     return set_err(h, MOE_ERR_CUDA, "tensor map encode failed (MXFP8 weights, micro %d)", m);
             if ((e = timed(h, kSlotGemm1, s, [&] {
-                     GatherArgs gat{x, h->perm, (int)R, k, (uint32_t)(H * 2), h->xp, h->err, h->limit_ns, h->num_sms};
-                     return launch_tc_small_fused_mxfp8(g1, mX, c1, s1, g2, mX2, c2, s2, fin, gat, brows, h->done,
-                                                        h->num_sms, s);
+                     GatherArgs gat{x, h->perm, (int)R, k, (uint32_t)(H * 2), xq, h->err, h->limit_ns, h->num_sms};
+                     const MxSmallActs act{xs, xs_pitch, hsc, hs_pitch};
+                     return launch_tc_small_fused_mxfp8(g1, mX, mXS, c1, s1, g2, mX2, mHS, c2, s2, fin, gat, act,
+                                                        h->done, h->num_sms, s);
                  })) != cudaSuccess)
                 return cuda_err(h, e, "fused MXFP8 GEMM launch");
             return MOE_OK;
@@ -671,7 +685,14 @@ moe_status moe_create(const moe_config* cfg, moe_handle** out) {
     const size_t o_smeta = take(6 * 4);
     const size_t o_hist = take(NB * E * 4), o_base = take(NB * E * 4), o_done = take(fused_counter_ints((int)E) * 4);
     const size_t o_sched = take(4 * 4);
-    const size_t o_xp = take(R * H * esz), o_h = take(R * M * I * esz), o_o = take(R * H * esz);
+    // the xp and h regions also hold the MXFP8 rows of a call with MXFP8
+    // weights: codes, then (256-aligned) scale bytes of at most K/32 + 16 per
+    // row and micro; the end grows with the call's R, so R's bound suffices
+    auto rows_region = [&](size_t K, size_t micros) {
+        const size_t mx = mx_scales_off(R, (int64_t)K) + R * micros * round_up(K / micros / 32, 16);
+        return R * K * esz > mx ? R * K * esz : mx;
+    };
+    const size_t o_xp = take(rows_region(H, 1)), o_h = take(rows_region(M * I, M)), o_o = take(R * H * esz);
     const size_t o_hs = take(T * Is * esz), o_s = take(Is ? T * H * esz : 0);
     const size_t o_xst0 = take(T * H * esz), o_xst1 = take(T * H * esz);
     const size_t o_yst0 = take(T * H * esz), o_yst1 = take(T * H * esz);

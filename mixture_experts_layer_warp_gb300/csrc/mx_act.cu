@@ -30,25 +30,6 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kBatch = 4;  // stages loaded ahead per warp
 
-
-// MXFP8 of this lane's four elements of one 128-element stage: returns the
-// four codes (byte i = element 4l + i) and, in `word`, the stage's scale word
-// (identical in every lane).
-__device__ __forceinline__ uint32_t quantize_stage(uint2 raw, int lane, uint32_t& word) {
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
-    const float2 f0 = __bfloat1622float2(h[0]), f1 = __bfloat1622float2(h[1]);
-    float a = fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)), fmaxf(fabsf(f1.x), fabsf(f1.y)));
-#pragma unroll
-    for (int d = 1; d < 8; d <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, d));  // the 8 lanes of a block
-    const int shared = mx_shared_exp(a);
-    const float s = pow2f(-shared);  // exact: a power-of-two scaling
-    const uint32_t codes = e4m3x2(f0.x * s, f0.y * s) | (e4m3x2(f1.x * s, f1.y * s) << 16);
-    // byte b of the word: the scale of block b, from the first lane of its 8
-    const uint32_t sc = (lane & 7) == 0 ? (uint32_t)(shared + 127) << (8 * (lane >> 3)) : 0u;
-    word = __reduce_or_sync(0xffffffffu, sc);
-    return codes;
-}
-
 // The gather splits a token's stages into parts of kPartStages, one warp per
 // (token, part): one warp per token (4096 at the denoise size) left too few
 // warps in flight to cover the latency of the quantisation's dependent
@@ -90,7 +71,7 @@ __global__ void __launch_bounds__(kThreads) gather_mx_kernel(MxActArgs a) {
                 const int s = s0 + u;
                 if (s >= s_hi) break;
                 uint32_t word;
-                const uint32_t c = quantize_stage(raw[u], lane, word);
+                const uint32_t c = mx_quantize128(raw[u], lane, word);
 #pragma unroll
                 for (int j = 0; j < kMaxTopK; ++j) {
                     if (j >= a.k) break;

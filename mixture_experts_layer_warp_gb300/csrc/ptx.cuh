@@ -331,18 +331,6 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
         : "memory");
 }
 
-// The same MMA with the A operand in tensor memory at a_tmem: 128 rows (row i
-// in lane i) x 16 K values, two 16-bit values per 32-bit column (the lower K
-// index in the low half), so one MMA reads 8 columns.
-__device__ __forceinline__ void mma_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                           uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
 // Arrive once on `bar` when every tcgen05 op issued so far by this thread is done.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -355,21 +343,6 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
 //   (1 = bf16), 15/16 A/B major (0 = K), 17-22 N >> 3, 24-28 M >> 4.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
-}
-
-// kind::f16 with f16 A and B (format code 0) and an fp32 accumulator.
-__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
-    return (1u << 4) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
-}
-
-// Four FP8 E4M3 codes (bytes 0..3 of w) to four f16, exactly: bytes 0-1 ->
-// lo, 2-3 -> hi (the lower byte in the lower half). The word is split into its
-// 16-bit halves in PTX, so no shift precedes the second conversion.
-__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
-    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.rn.f16x2.e4m3x2 %0, l;\n\t"
-        "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
-        : "=r"(lo), "=r"(hi)
-        : "r"(w));
 }
 
 // Shared-memory matrix descriptor of a K-major operand tile whose rows are
@@ -407,21 +380,8 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         : "memory");
 }
 
-// Store 32 consecutive 32-bit columns of this warp's 32 TMEM lanes (one lane
-// per thread). tmem_wait_st() waits until the stores issued so far are done
-// (before the columns are handed to the MMA).
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
-        "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
-        "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-        : "memory");
-}
-
+// Waits until this thread's TMEM stores issued so far are done (before the
+// columns are handed to the MMA).
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Four 16-column loads (columns c0, c1, c2, c3) with a single wait.
@@ -531,6 +491,21 @@ __device__ __forceinline__ void red_add_cluster(uint32_t caddr, uint32_t v) {
     asm volatile("red.relaxed.cluster.shared::cluster.add.u32 [%0], %1;" ::"r"(caddr), "r"(v) : "memory");
 }
 
+// Block-scaled FP8 MMA on one CTA: D (+)= (A * 2^SFA) x (B * 2^SFB)^T, A and B
+// E4M3 codes (K-major, 32 codes per MMA), the scale words in tensor memory in
+// the layout of mma_mx_pair (A row m: lane m % 32 of every lane quarter,
+// column sfa + m / 32; B row n: lane n % 32, column sfb + n / 32; byte picked
+// by the descriptor's scale ids).
+__device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
 // Block-scaled FP8 MMA over the pair (leader only): D (+)= (A * 2^SFA) x
 // (B * 2^SFB)^T, A and B E4M3 codes (K-major, 32 codes per MMA), one UE8M0
 // scale per 32 K of every row of A and of B in tensor memory: the scale word of
@@ -580,7 +555,10 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const void* tmap, int3
         : "memory");
 }
 
-// Store 4 / 8 consecutive 32-bit columns of this warp's 32 TMEM lanes.
+// Store 1 / 4 / 8 consecutive 32-bit columns of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t a) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(a) : "memory");
+}
 __device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a), "r"(b),
                  "r"(c), "r"(d)

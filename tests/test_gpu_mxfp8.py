@@ -6,15 +6,11 @@ weights must match the oracle evaluated on the exact value of those weights
 (code * 2^(S-127), the MX definition, in fp64) within the bf16 layer
 tolerance.
 
-Batches of at most 16 tokens: the kernel converts codes to f16 (exact for
-scales in f16's range, an fp32 form outside it) and rounds the token rows and
-h to f16; that rounding is an implementation detail the tolerance covers, and
-the oracle is the plain layer on the exact weights. Larger batches run the
-block-scaled FP8 MMA on MXFP8 token rows and h: the oracle then takes the
-MXFP8 values of each token's input and of each SwiGLU output too
-(``forward_tokens_mx``), both taking h's codes on its bf16 value (the kernel
-rounds its fp32 accumulator, the oracle the fp64 h: they differ where the two
-roundings do, which the tolerance covers).
+Every batch size runs the tensor cores' block-scaled FP8 MMA on MXFP8 token
+rows and h, so the oracle takes the MXFP8 values of each token's input and of
+each SwiGLU output too (``forward_tokens_mx``), both taking h's codes on its
+bf16 value (the kernel rounds its fp32 accumulator, the oracle the fp64 h:
+they differ where the two roundings do, which the tolerance covers).
 """
 import numpy as np
 import pytest
@@ -78,8 +74,7 @@ def _check(wl, inp, y, w13_q, w2_q, rows=None, cover=False):
     if cover:
         rows = np.union1d(rows, parity.covering_tokens(orc, T, wl.k))
     rows = rows[set_ok[rows]]
-    fwd = oracle.forward_tokens_mx if T > 16 else oracle.forward_tokens
-    ref = fwd(host["x"], orc["ids"], orc["w"], _dequant(w13_q), _dequant(w2_q), rows,
+    ref = oracle.forward_tokens_mx(host["x"], orc["ids"], orc["w"], _dequant(w13_q), _dequant(w2_q), rows,
               host["shared_w13"], host["shared_w2"])
     err = parity.y_error(y, ref, rows)
     assert err <= parity.Y_TOL["bf16"], f"{wl.name}: rel err {err:.3e}"
@@ -153,11 +148,13 @@ def test_mxfp8_large_batch_matches_the_oracle_with_mxfp8_activations(wl):
     _check(wl, inp, y, w13_q, w2_q)
 
 
-def test_mxfp8_large_batch_differs_from_the_f16_reading():
-    """The large-batch oracle is not the small-batch one: on the same inputs
-    the MXFP8 activations move y by far more than the kernel's error against
-    forward_tokens_mx, so the parity test above tells the two readings apart."""
-    wl = LARGE[1]
+@pytest.mark.parametrize("which", ["small", "large"])
+def test_mxfp8_activations_are_distinguishable_from_the_plain_layer(which):
+    """The MXFP8 oracle is not the plain layer on the MX weights: on the same
+    inputs the MXFP8 activations move y by far more than the kernel's error
+    against forward_tokens_mx, so the parity tests tell the two readings
+    apart, for the small-batch kernel and the large-batch one."""
+    wl = SMALL[0] if which == "small" else LARGE[1]
     inp = W.make_inputs(wl, seed=7)
     dev = parity.to_device(inp)
     w13_q, w2_q = _quantize_experts(dev)
@@ -209,10 +206,10 @@ def test_mxfp8_async_host_calls_match_device_calls():
     layer.close()
 
 
-def test_scales_outside_the_f16_range_take_the_exact_path():
-    """w2 scaled by 2^-14: its blocks get scales near 2^-26 (not f16 numbers),
-    so the dequantiser's fp32 form runs; y (made by w2) must still match the
-    exact MX weight values."""
+def test_weight_scales_below_the_f16_range_are_exact():
+    """w2 scaled by 2^-14: its blocks get scales near 2^-26 (below f16's
+    range); the block-scaled MMA applies them exactly, so y (made by w2) must
+    still match the exact MX weight values."""
     wl = W.Workload("mx_tiny_w2", 8, 512, 16, 4, 256, 1)
     inp = W.make_inputs(wl, seed=4)
     inp["w2"] = [(t.float() * 2.0 ** -14).to(torch.bfloat16) for t in inp["w2"]]
