@@ -98,9 +98,9 @@ struct Ctl {
     uint64_t sfs_empty[8];    // MX, each CTA: its 4 scale warps have read a ring slot
     uint64_t sf_full[6];      // MX, leader: both CTAs wrote a scale-factor buffer
     uint64_t sf_empty[6];     // MX, both CTAs: the MMAs reading a scale-factor buffer are done
-    uint64_t rfull[8];        // both CTAs: a tile index is in the hand-out ring slot
+    uint64_t rfull[8];        // both CTAs: a tile is in the hand-out ring slot
     uint64_t rempty[8];       // leader: every consuming warp of both CTAs has taken it
-    int tring[8];             // the hand-out ring: tile indices, -1 = no more tiles
+    uint2 tring[8];           // the hand-out ring: decoded tiles (pack_tile), x = -1: no more tiles
     uint32_t tmem_base;
     int abort;
     int seg[kMaxExperts + 1];
@@ -201,6 +201,23 @@ __device__ __forceinline__ void fail(Ctl& c, int* err) {
     atomicOr(err, kErrTimeout);
 }
 
+// A decoded tile in two words: the chunk's first route row, then len (9 bits,
+// <= 256), group (7 bits), micro (3 bits) and feature tile (13 bits).
+__device__ __forceinline__ uint2 pack_tile(const PairTile& t) {
+    return make_uint2((uint32_t)t.start,
+                      (uint32_t)t.len | ((uint32_t)t.g << 9) | ((uint32_t)t.m << 16) | ((uint32_t)t.f << 19));
+}
+__device__ __forceinline__ PairTile unpack_tile(uint2 w) {
+    PairTile t;
+    t.start = (int)w.x;
+    t.len = (int)(w.y & 511u);
+    t.g = (int)((w.y >> 9) & 127u);
+    t.m = (int)((w.y >> 16) & 7u);
+    t.f = (int)(w.y >> 19);
+    t.n = (t.len + 15) & ~15;
+    return t;
+}
+
 // Tile hand-out. The pairs take tiles of the order above from a global counter
 // (a.sched[0]) as they become free, so the pairs running at once stay on
 // consecutive tiles for the whole launch (statically assigned, every pair's
@@ -216,15 +233,23 @@ __device__ __forceinline__ void fail(Ctl& c, int* err) {
 // sequence pair, pair + npairs, ... instead: pairs that reserve a tile or two
 // ahead would leave the last tiles of a short launch unevenly spread (denoise
 // GEMMs, ~30-40 tiles per pair: 0.51 -> 0.57 ms), where drift never builds up.
-//   take: the next index for a consuming warp (-2: a wait ran out).
+// The scheduler also decodes each tile (walk_load) before it publishes it, so
+// no consuming warp spends the binary search and divisions between two tiles:
+// in the MMA warp they left the tensor pipe idle ~900 cycles per tile (7% of
+// the denoise GEMM2, whose tiles are short).
+//   take: the next tile for a consuming warp (0; -1: no more; -2: a wait ran out).
 //   hand_out: the scheduler warp's loop.
-__device__ __forceinline__ int feed_take(Ctl& c, int& n, bool leader, uint32_t rempty0, const PairGemmArgs& a) {
+__device__ __forceinline__ int feed_take(Ctl& c, int& n, bool leader, uint32_t rempty0, const PairGemmArgs& a,
+                                         PairTile& t) {
     const int slot = n % kFeed;
     const bool got = ptx::mbar_wait(ptx::smem_u32(&c.rfull[slot]), (uint32_t)(n / kFeed) & 1u, a.limit_ns, &c.abort);
     if (!__all_sync(0xffffffffu, got)) return -2;
-    // the shuffle needs the loaded value, so the read is complete before the
+    // the shuffles need the loaded values, so the reads are complete before the
     // arrival below lets the scheduler write the slot again
-    const int tile = __shfl_sync(0xffffffffu, *static_cast<volatile int*>(&c.tring[slot]), 0);
+    const volatile uint2* src = &c.tring[slot];
+    uint2 w;
+    w.x = __shfl_sync(0xffffffffu, src->x, 0);
+    w.y = __shfl_sync(0xffffffffu, src->y, 0);
     if ((threadIdx.x & 31) == 0) {
         if (leader)
             ptx::mbar_arrive(ptx::smem_u32(&c.rempty[slot]));
@@ -232,9 +257,12 @@ __device__ __forceinline__ int feed_take(Ctl& c, int& n, bool leader, uint32_t r
             ptx::mbar_arrive_remote(rempty0 + (uint32_t)(slot * sizeof(uint64_t)));
     }
     ++n;
-    return tile;
+    if ((int)w.x < 0) return -1;
+    t = unpack_tile(w);
+    return 0;
 }
 
+template <bool SWIGLU>
 __device__ __forceinline__ void hand_out(Ctl& c, int total, const PairGemmArgs& a, int pair, int npairs) {
     const uint32_t peer_tring = ptx::map_to_rank(ptx::smem_u32(&c.tring[0]), 1);
     const uint32_t peer_rfull = ptx::map_to_rank(ptx::smem_u32(&c.rfull[0]), 1);
@@ -246,18 +274,21 @@ __device__ __forceinline__ void hand_out(Ctl& c, int total, const PairGemmArgs& 
             if ((threadIdx.x & 31) == 0) fail(c, a.err);
             return;
         }
-        int tile = 0;
+        int end = 0;
         if ((threadIdx.x & 31) == 0) {
-            tile = a.dynamic ? atomicAdd(a.sched, 1) : pair + n * npairs;
-            if (tile >= total) tile = -1;
-            c.tring[slot] = tile;
+            const int tile = a.dynamic ? atomicAdd(a.sched, 1) : pair + n * npairs;
+            Walk w{tile, {}};
+            const bool live = tile < total && walk_load<SWIGLU>(w, c, a);
+            const uint2 word = live ? pack_tile(w.t) : make_uint2(0xffffffffu, 0u);
+            end = live ? 0 : 1;
+            c.tring[slot] = word;
             ptx::mbar_arrive(ptx::smem_u32(&c.rfull[slot]));
-            ptx::mbar_arrive_expect_tx_remote(peer_rfull + (uint32_t)(slot * sizeof(uint64_t)), 4);
-            ptx::st_async_u32(peer_tring + (uint32_t)(slot * 4), (uint32_t)tile,
-                              peer_rfull + (uint32_t)(slot * sizeof(uint64_t)));
+            const uint32_t rf = peer_rfull + (uint32_t)(slot * sizeof(uint64_t));
+            ptx::mbar_arrive_expect_tx_remote(rf, 8);
+            ptx::st_async_u32(peer_tring + (uint32_t)(slot * 8), word.x, rf);
+            ptx::st_async_u32(peer_tring + (uint32_t)(slot * 8 + 4), word.y, rf);
         }
-        tile = __shfl_sync(0xffffffffu, tile, 0);
-        if (tile < 0) return;
+        if (__shfl_sync(0xffffffffu, end, 0)) return;
     }
 }
 
@@ -374,12 +405,10 @@ __global__ void __launch_bounds__(Cfg<MX>::kThreads, 1)
         bool ok = true;
         int fn = 0;
         while (ok) {
-            const int tile = feed_take(c, fn, leader, rempty0, a);
-            if (tile == -2) ok = false;
-            if (tile < 0) break;
-            Walk w{tile, {}};
-            walk_load<SWIGLU>(w, c, a);
-            const PairTile t = w.t;
+            PairTile t;
+            const int got = feed_take(c, fn, leader, rempty0, a, t);
+            if (got == -2) ok = false;
+            if (got < 0) break;
             const int half = t.n / 2;               // token rows held by each CTA
             const int box = token_box(t);
             const CUtensorMap* tx = box == 0 ? &tmX0 : box == 1 ? &tmX1 : box == 2 ? &tmX2 : &tmX3;
@@ -435,7 +464,7 @@ __global__ void __launch_bounds__(Cfg<MX>::kThreads, 1)
         }
     } else if (warp == 2 && leader) {
         // ------------------------------------------------ tile scheduler (leader)
-        hand_out(c, total, a, pair, npairs);
+        hand_out<SWIGLU>(c, total, a, pair, npairs);
     } else if (warp == 1 && leader) {
         // ------------------------------------------------ MMA issuer (leader)
         const bool issuer = ptx::elect_one();
@@ -446,12 +475,10 @@ __global__ void __launch_bounds__(Cfg<MX>::kThreads, 1)
         int sfi = 0;  // MX: stages consumed, which picks the scale-factor buffer and its phase
         int fn = 0;
         for (; ok; ++local) {
-            const int tile = feed_take(c, fn, true, rempty0, a);
-            if (tile == -2) ok = false;
-            if (tile < 0) break;
-            Walk w{tile, {}};
-            walk_load<SWIGLU>(w, c, a);
-            const PairTile t = w.t;
+            PairTile t;
+            const int got = feed_take(c, fn, true, rempty0, a, t);
+            if (got == -2) ok = false;
+            if (got < 0) break;
             const uint32_t idesc = ptx::idesc_bf16_f32(2 * kWRows, t.n);
             const int acc = local & 1;
             const uint32_t acc_par = (uint32_t)(local >> 1) & 1u;
@@ -526,12 +553,10 @@ __global__ void __launch_bounds__(Cfg<MX>::kThreads, 1)
         bool ok = true;
         int fn = 0;
         while (ok) {
-            const int tile = feed_take(c, fn, leader, rempty0, a);
-            if (tile == -2) ok = false;
-            if (tile < 0) break;
-            Walk w{tile, {}};
-            walk_load<SWIGLU>(w, c, a);
-            const PairTile t = w.t;
+            PairTile t;
+            const int got = feed_take(c, fn, leader, rempty0, a, t);
+            if (got == -2) ok = false;
+            if (got < 0) break;
             for (int mi = 0; ok && mi < n_micro_k; ++mi) {
                 const int m = SWIGLU ? t.m : mi;
                 const CUtensorMap* tsa = pick_map(m, tmSA0, tmSA1, tmSA2, tmSA3);
@@ -586,12 +611,10 @@ __global__ void __launch_bounds__(Cfg<MX>::kThreads, 1)
         bool ok = true;
         int fn = 0;
         while (ok) {
-            const int tile = feed_take(c, fn, leader, rempty0, a);
-            if (tile == -2) ok = false;
-            if (tile < 0) break;
-            Walk w{tile, {}};
-            walk_load<SWIGLU>(w, c, a);
-            const PairTile t = w.t;
+            PairTile t;
+            const int got = feed_take(c, fn, leader, rempty0, a, t);
+            if (got == -2) ok = false;
+            if (got < 0) break;
             const int off = t.start & 3;  // the chunk's first scale word in the loaded 16-byte rows
             for (int mi = 0; ok && mi < n_micro_k; ++mi) {
                 for (int kb = 0; kb < a.k_blocks; ++kb) {
@@ -650,19 +673,17 @@ __global__ void __launch_bounds__(Cfg<MX>::kThreads, 1)
         const uint32_t tempty_leader0 = ptx::map_to_rank(ptx::smem_u32(&c.tempty[0]), 0);
         int local = 0, fn = 0;
         for (;; ++local) {
-            const int tile = feed_take(c, fn, leader, rempty0, a);
+            PairTile t;
+            const int got = feed_take(c, fn, leader, rempty0, a, t);
             // the MXFP8 SwiGLU epilogue's warp pairs agree first (see below)
-            bool live = tile >= 0;
+            bool live = got >= 0;
             if (MX && SWIGLU) live = ptx::named_barrier_and(1 + (q >> 1), 64, live);
             if (!live) {
-                if (tile == -2 && lane == 0) fail(c, a.err);
+                if (got == -2 && lane == 0) fail(c, a.err);
                 break;
             }
             const int acc = local & 1;
             const uint32_t acc_par = (uint32_t)(local >> 1) & 1u;
-            Walk w{tile, {}};
-            walk_load<SWIGLU>(w, c, a);
-            const PairTile t = w.t;
             bool ready = false;
             if (lane == 0)
                 ready = ptx::mbar_wait(ptx::smem_u32(&c.tfull[acc]), acc_par, a.limit_ns, &c.abort);
