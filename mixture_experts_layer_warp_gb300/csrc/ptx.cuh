@@ -101,21 +101,6 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
     }
 }
 
-// mbar_wait_cluster that also gives up once *abort becomes non-zero: for
-// phases completed by arrivals that other CTAs released at cluster scope.
-__device__ __forceinline__ bool mbar_wait_acq_cluster(uint32_t bar, uint32_t parity, uint64_t limit_ns,
-                                                      volatile int* abort) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    const uint64_t t0 = globaltimer();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait_cluster(bar, parity)) return true;
-        if ((it & 31u) == 0u) {
-            if (abort != nullptr && *abort) return false;
-            if (globaltimer() - t0 > limit_ns) return false;
-        }
-    }
-}
-
 // ---------------------------------------------------------------------- TMA
 // L2 eviction-priority policies for cache-hinted loads: data streamed once
 // (expert weights) goes first, small data reused on every call (the router
@@ -186,32 +171,6 @@ __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
-// Non-tensor bulk copy global -> shared (size and both addresses 16-byte multiples).
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-        : "memory");
-}
-
-// Non-tensor bulk copy shared -> global, tracked by the bulk async-group.
-__device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
-                     reinterpret_cast<uint64_t>(dst)),
-                 "r"(src), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-
-// Wait until every committed bulk group has finished READING shared memory.
-__device__ __forceinline__ void bulk_wait_read_all() {
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-
-// Wait until every committed bulk group has fully completed (writes visible).
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
 // ------------------------------------------------------------------ cluster
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
@@ -224,10 +183,6 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
     uint32_t out;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(saddr), "r"(rank));
     return out;
-}
-
-__device__ __forceinline__ void st_cluster_f32(uint32_t caddr, float v) {
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(caddr), "f"(v) : "memory");
 }
 
 // A 32-bit word into another CTA's shared memory (shared::cluster address
@@ -577,12 +532,6 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
 // outstanding memory traffic: over a thousand cycles under TMA load streams.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cbar) {
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cbar) : "memory");
-}
-
-// Arrive on a barrier of another CTA of the cluster (shared::cluster address),
-// releasing this thread's prior writes at cluster scope.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cbar) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cbar) : "memory");
 }
 
 }  // namespace ptx

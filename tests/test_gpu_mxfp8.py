@@ -86,6 +86,9 @@ SMALL = [
     W.Workload("mx_shared", 13, 512, 16, 4, 128, 1, shared_inter=256),
     W.Workload("mx_one_token", 1, 256, 8, 2, 128, 1),
     W.Workload("mx_e64_k8", 16, 1024, 64, 8, 256, 1),
+    # H/32 = 24 scale bytes per row (a 32-byte pitch), I = 384: the down
+    # projection's last 256-K stage is half a stage, in each of two micros
+    W.Workload("mx_h768_i384", 12, 768, 16, 4, 384, 2),
 ]
 
 
