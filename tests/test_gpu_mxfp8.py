@@ -89,6 +89,8 @@ SMALL = [
     # H/32 = 24 scale bytes per row (a 32-byte pitch), I = 384: the down
     # projection's last 256-K stage is half a stage, in each of two micros
     W.Workload("mx_h768_i384", 12, 768, 16, 4, 384, 2),
+    # four micros of I = 128: h's scale map four deep, a half stage per micro
+    W.Workload("mx_four_micro_small", 5, 256, 8, 2, 128, 4),
 ]
 
 
