@@ -14,10 +14,8 @@
 // file quantises the gathered token rows; h is quantised in the epilogue of
 // the SwiGLU GEMM (gemm_pair.cu) into the same layout.
 //
-// One warp per row part: lane l holds elements 4l .. 4l+3 of each
-// 128-element stage (one 8-byte load), 8 lanes per 32-block. A warp loads
-// kBatch stages before it quantises them, so that several loads per lane are
-// in flight.
+// One warp per token row (below): sixteen 16-byte loads per lane in flight,
+// four lanes per 32-block.
 #include <cuda_bf16.h>
 
 #include "gemm_common.cuh"
@@ -28,15 +26,46 @@ namespace moe {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kBatch = 4;  // stages loaded ahead per warp
 
-// The gather splits a token's stages into parts of kPartStages, one warp per
-// (token, part): one warp per token (4096 at the denoise size) left too few
-// warps in flight to cover the latency of the quantisation's dependent
-// shuffles and conversions (78 -> 61 us).
-constexpr int kPartStages = 8;
+// One warp per token: lane l loads elements 8l .. 8l+7 of each 256-element
+// unit (one 16-byte load; a 32-block spans four lanes), sixteen units in
+// flight (a whole 8 KB row of a 4096-wide layer), quantises them and writes
+// the codes to the token's k route rows (8 bytes per lane and route) and each
+// stage's scale word (lanes 0-15 hold the unit's first stage, 16-31 its
+// second). The earlier form (a warp per 8 stages of a token, 8-byte loads
+// four stages ahead) ran at 0.42 of the HBM bandwidth, bound by the latency of
+// its loads and of the quantisation's dependent shuffles.
+constexpr int kUnits = 16;  // 256-element units in flight per warp
 
-__device__ __forceinline__ int parts_of(int stages) { return (stages + kPartStages - 1) / kPartStages; }
+// MXFP8 of this lane's eight elements of a 256-element unit: the eight codes
+// (element order in the bytes) and, in every lane of the half-warp, the scale
+// word of the half-warp's stage (byte b: 32-block b of the stage).
+__device__ __forceinline__ uint2 quantize_unit(uint4 raw, int lane, uint32_t& word) {
+    const __nv_bfloat162* v = reinterpret_cast<const __nv_bfloat162*>(&raw);
+    float f[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 p = __bfloat1622float2(v[i]);
+        f[2 * i] = p.x;
+        f[2 * i + 1] = p.y;
+    }
+    float a = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(f[i]));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));  // the block's four lanes
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+    const int shared = mx_shared_exp(a);
+    const float sc = pow2f(-shared);  // exact: a power of two
+    const uint2 codes = make_uint2(e4m3x2(f[0] * sc, f[1] * sc) | (e4m3x2(f[2] * sc, f[3] * sc) << 16),
+                                   e4m3x2(f[4] * sc, f[5] * sc) | (e4m3x2(f[6] * sc, f[7] * sc) << 16));
+    // every lane of a block holds its exponent: byte (lane / 4) % 4, then the
+    // stage's four blocks (16 lanes) combined in every lane
+    uint32_t w = (uint32_t)(shared + 127) << (8 * ((lane >> 2) & 3));
+    w |= __shfl_xor_sync(0xffffffffu, w, 4);
+    w |= __shfl_xor_sync(0xffffffffu, w, 8);
+    word = w;
+    return codes;
+}
 
 // Token t's row of x, quantised once, written to its k routes' rows
 // inv[t*k + j] (the gather of the routes and the quantisation in one pass).
@@ -45,39 +74,34 @@ __global__ void __launch_bounds__(kThreads) gather_mx_kernel(MxActArgs a) {
     const int lane = threadIdx.x & 31;
     const int64_t T = a.rows / a.k;
     const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
-    const int stages = a.K / 128, P = parts_of(stages);
-    const uint2* __restrict__ src = static_cast<const uint2*>(a.src);
-    uint32_t* __restrict__ codes = static_cast<uint32_t*>(a.codes);
+    const int units = a.K / 256;
+    const uint4* __restrict__ src = static_cast<const uint4*>(a.src);
+    unsigned char* __restrict__ codes = static_cast<unsigned char*>(a.codes);
     uint32_t* __restrict__ scales = static_cast<uint32_t*>(a.scales);
-    for (int64_t item = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5; item < T * P; item += nwarps) {
-        const int64_t t = item / P;
-        const int s_lo = (int)(item % P) * kPartStages;
-        const int s_hi = s_lo + kPartStages < stages ? s_lo + kPartStages : stages;
-        const int dst = lane < a.k ? a.inv[t * a.k + lane] : 0;
-        if (__any_sync(0xffffffffu, dst < 0 || dst >= a.rows)) {
+    const int half = lane >> 4, l16 = lane & 15;
+    for (int64_t t = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5; t < T; t += nwarps) {
+        // lane j < k holds the row of route t*k + j; lanes 16 + j the same
+        const int mine = l16 < a.k ? a.inv[t * a.k + l16] : 0;
+        if (__any_sync(0xffffffffu, mine < 0 || mine >= a.rows)) {
             if (lane == 0) atomicOr(a.err, kErrCheck);
             continue;
         }
-        int64_t rows[kMaxTopK];  // the token's route rows, in every lane
+        for (int u0 = 0; u0 < units; u0 += kUnits) {
+            uint4 raw[kUnits];
 #pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j) rows[j] = __shfl_sync(0xffffffffu, dst, j);
-        for (int s0 = s_lo; s0 < s_hi; s0 += kBatch) {
-            uint2 raw[kBatch];
+            for (int u = 0; u < kUnits; ++u)
+                if (u0 + u < units) raw[u] = __ldg(src + (t * a.K + (int64_t)(u0 + u) * 256) / 8 + lane);
 #pragma unroll
-            for (int u = 0; u < kBatch; ++u)
-                if (s0 + u < s_hi) raw[u] = __ldg(src + (t * a.K + (s0 + u) * 128) / 4 + lane);
-#pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
-                const int s = s0 + u;
-                if (s >= s_hi) break;
+            for (int u = 0; u < kUnits; ++u) {
+                if (u0 + u >= units) break;
                 uint32_t word;
-                const uint32_t c = mx_quantize128(raw[u], lane, word);
-#pragma unroll
-                for (int j = 0; j < kMaxTopK; ++j) {
-                    if (j >= a.k) break;
-                    codes[(rows[j] * a.K + s * 128) / 4 + lane] = c;
-                    if (lane == j) scales[(int64_t)s * a.rows_pad + rows[j]] = word;
+                const uint2 c = quantize_unit(raw[u], lane, word);
+                const int s = 2 * (u0 + u) + half;  // this half-warp's stage
+                for (int j = 0; j < a.k; ++j) {
+                    const int64_t row = __shfl_sync(0xffffffffu, mine, j);
+                    *reinterpret_cast<uint2*>(codes + row * a.K + (int64_t)s * 128 + 8 * l16) = c;
                 }
+                if (l16 < a.k) scales[(int64_t)s * a.rows_pad + mine] = word;
             }
         }
     }
@@ -94,9 +118,8 @@ int grid_for(int64_t warps_needed, int num_sms) {
 
 cudaError_t launch_gather_mx(const MxActArgs& a, cudaStream_t s) {
     if (a.rows == 0) return cudaSuccess;
-    if (a.K % 128 != 0) return cudaErrorInvalidValue;
-    const int64_t parts = (a.K / 128 + kPartStages - 1) / kPartStages;
-    return launch_kernel(gather_mx_kernel, dim3(grid_for(a.rows / a.k * parts, a.num_sms)), dim3(kThreads), 0, s,
+    if (a.K % 256 != 0) return cudaErrorInvalidValue;  // whole 256-element units (bf16 layers: H % 256 == 0)
+    return launch_kernel(gather_mx_kernel, dim3(grid_for(a.rows / a.k, a.num_sms)), dim3(kThreads), 0, s,
                          a.early != 0, a);
 }
 
