@@ -71,7 +71,7 @@ constexpr int kEpiArrivals = 8;                      // 4 epilogue warps in each
 // the copy into TMEM on every stage.)
 template <bool MX>
 struct Cfg {
-    static constexpr int kSfBufs = 6;                 // scale-factor buffers in TMEM (MX)
+    static constexpr int kSfBufs = kStages;           // scale-factor buffers in TMEM (MX): one per ring slot
     static constexpr int kChunk = MX ? 208 : 256;     // routes per tile at most (MMA N)
     static constexpr int kK = MX ? 128 : 64;          // K elements per stage
     static constexpr int kStageBytes = kABytes + kBBytes;
@@ -97,7 +97,6 @@ struct Ctl {
     uint64_t sfs_full[8];     // MX, each CTA: this CTA's scales of a stage have landed in a ring slot
     uint64_t sfs_empty[8];    // MX, each CTA: its 4 scale warps have read a ring slot
     uint64_t sf_full[6];      // MX, leader: both CTAs wrote a scale-factor buffer
-    uint64_t sf_empty[6];     // MX, both CTAs: the MMAs reading a scale-factor buffer are done
     uint64_t rfull[8];        // both CTAs: a tile is in the hand-out ring slot
     uint64_t rempty[8];       // leader: every consuming warp of both CTAs has taken it
     uint2 tring[8];           // the hand-out ring: decoded tiles (pack_tile), x = -1: no more tiles
@@ -351,7 +350,6 @@ __global__ void __launch_bounds__(Cfg<MX>::kThreads, 1)
             }
             for (int b = 0; b < C::kSfBufs; ++b) {
                 ptx::mbar_init(ptx::smem_u32(&c.sf_full[b]), 8);  // 4 scale-factor warps in each CTA
-                ptx::mbar_init(ptx::smem_u32(&c.sf_empty[b]), 1);
             }
         }
         c.abort = 0;
@@ -513,8 +511,8 @@ __global__ void __launch_bounds__(Cfg<MX>::kThreads, 1)
                             for (int k = 0; k < 4; ++k)
                                 ptx::mma_mx_pair(d, adesc + 2u * k, bdesc + 2u * k, ptx::idesc_mx(2 * kWRows, t.n, k, k),
                                                  sfa_t, sfa_t + 8u, accumulate | (uint32_t)k);
+                            // frees the ring slot and its scale buffer (buffer sfb = slot stage)
                             ptx::mma_commit_pair_both(ptx::smem_u32(&c.empty[stage]));
-                            ptx::mma_commit_pair_both(ptx::smem_u32(&c.sf_empty[sfb]));
                         } else {
 #pragma unroll
                             for (int k = 0; k < kTcBK / 16; ++k)
@@ -637,7 +635,10 @@ __global__ void __launch_bounds__(Cfg<MX>::kThreads, 1)
                         for (int j = 0; j < 8; ++j) wb[j] = sfw[off + lane + 32 * j];  // routes past the chunk: unused
                         __syncwarp();
                         if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&c.sfs_empty[slot]));
-                        got = ptx::mbar_wait(ptx::smem_u32(&c.sf_empty[sfb]),
+                        // the buffer is free once the MMAs of its previous use are done:
+                        // buffer sfb goes with ring slot sfb, whose empty barrier the MMA
+                        // commit completes (one commit per stage frees both)
+                        got = ptx::mbar_wait(ptx::smem_u32(&c.empty[sfb]),
                                              ((uint32_t)(sfi / C::kSfBufs) & 1u) ^ 1u, a.limit_ns, &c.abort);
                     }
                     if (!__all_sync(0xffffffffu, got)) {
