@@ -37,8 +37,8 @@
 // allocation, warps 4-7 drain an accumulator (one TMEM lane quarter each,
 // transposed through shared memory into 16-byte stores of token rows) while
 // the next tile accumulates into the other. With block-scaled FP8 operands
-// warp 3 loads the scales into a ring of their own and warps 8-11 copy them
-// into TMEM (see Cfg). All waits are bounded, and every load a CTA issues has
+// warp 3 loads the scales into a ring of their own and warps 8-15 (two sets
+// taking alternate stages) copy them into TMEM (see Cfg). All waits are bounded, and every load a CTA issues has
 // landed before it exits.
 #include <cuda_bf16.h>
 
@@ -61,12 +61,12 @@ constexpr int kEpiArrivals = 8;                      // 4 epilogue warps in each
 // 128 K per stage (E4M3 codes, one byte each), chunks of up to 208 routes so
 // that two accumulators (416 columns) and six scale-factor buffers (16 columns
 // each: the weights' words at +0, the routes' at +8) fit the 512 TMEM columns;
-// 12 warps. Each stage's scales (the weights' 128 rows x 4 blocks, 512 bytes;
+// 16 warps. Each stage's scales (the weights' 128 rows x 4 blocks, 512 bytes;
 // the token rows' stage-major scale words, 65 x 16 bytes from the chunk's
 // first route rounded down to 4) come through a ring of their own, loaded by
-// warp 3, so that they run ahead of the operand stages; warps 8-11 copy them
-// into a TMEM buffer as soon as the MMAs that read that buffer six stages
-// earlier have completed. (Scales that shared the operand slots could only
+// warp 3, so that they run ahead of the operand stages; warps 8-15 (two sets
+// of four, alternate stages) copy them into a TMEM buffer as soon as the MMAs
+// that read that buffer six stages earlier have completed. (Scales that shared the operand slots could only
 // load once a slot freed, and the MMAs then waited out the load latency plus
 // the copy into TMEM on every stage.)
 template <bool MX>
@@ -118,6 +118,16 @@ constexpr int kEpiBytes = 4 * kEpiFloats * 4;
 // per-token |max| read by the partner warp
 constexpr int kEpiAmaxOff = 32 * 16 / 2;
 static_assert(kEpiAmaxOff + 64 <= kEpiFloats, "epilogue staging");
+
+// Scale-warp sets and threads of a kernel: the MXFP8 down GEMM runs two sets
+// of four scale warps on alternate stages (one set took ~700 cycles per stage
+// against ~350-420 of MMA work; -8% cycles), the MXFP8 SwiGLU GEMM one (its
+// h-quantising epilogue keeps the SM sub-partitions busy enough that four more
+// warps slowed it, +7% cycles).
+template <bool SWIGLU, bool MX>
+constexpr int kSfSets = MX && !SWIGLU ? 2 : 1;
+template <bool SWIGLU, bool MX>
+constexpr int kPairThreads = Cfg<MX>::kThreads + (kSfSets<SWIGLU, MX> - 1) * 128;
 
 template <bool MX>
 constexpr int smem_bytes() {
@@ -301,7 +311,7 @@ __device__ __forceinline__ void settle_inflight_copies() {
 }
 
 template <bool SWIGLU, bool MX>
-__global__ void __launch_bounds__(Cfg<MX>::kThreads, 1)
+__global__ void __launch_bounds__(kPairThreads<SWIGLU, MX>, 1)
     pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant__ CUtensorMap tmW1,
                      const __grid_constant__ CUtensorMap tmW2, const __grid_constant__ CUtensorMap tmW3,
                      const __grid_constant__ CUtensorMap tmX0, const __grid_constant__ CUtensorMap tmX1,
@@ -312,7 +322,7 @@ __global__ void __launch_bounds__(Cfg<MX>::kThreads, 1)
     using C = Cfg<MX>;
     constexpr int kChunk = C::kChunk;
     constexpr int kStageBytes = C::kStageBytes;
-    constexpr int kThreads = C::kThreads;
+    constexpr int kThreads = kPairThreads<SWIGLU, MX>;
     extern __shared__ unsigned char smem_raw[];
     // the same offset in both CTAs: the leader's MMA addresses the peer's
     // operands through its own shared-memory descriptors
@@ -338,10 +348,10 @@ __global__ void __launch_bounds__(Cfg<MX>::kThreads, 1)
         ptx::mbar_init(ptx::smem_u32(&c.drain), 1);
         // the warps that take every tile index: producer + MMA + 4 epilogue
         // warps (leader), producer + 4 epilogue warps (peer), and with MXFP8
-        // operands the scale producer and the 4 scale warps of each CTA
+        // operands the scale producer and the 4 or 8 scale warps of each CTA
         for (int r = 0; r < kFeed; ++r) {
             ptx::mbar_init(ptx::smem_u32(&c.rfull[r]), 1);
-            ptx::mbar_init(ptx::smem_u32(&c.rempty[r]), MX ? 21 : 11);
+            ptx::mbar_init(ptx::smem_u32(&c.rempty[r]), MX ? 21 + 8 * (kSfSets<SWIGLU, MX> - 1) : 11);
         }
         if (MX) {
             for (int s = 0; s < C::kSfStages; ++s) {
@@ -598,11 +608,16 @@ __global__ void __launch_bounds__(Cfg<MX>::kThreads, 1)
         __syncwarp();
     } else if (MX && warp >= 8) {
         // ------------------------------------------------ scale factors into TMEM (both CTAs)
-        // Warp 8 + q writes lane quarter q of a scale-factor buffer (the MMA
-        // reads every quarter): column j, lane L holds the four block scales of
-        // weight row L + 32 j (columns +0..3) and the scale word of route L + 32 j
-        // of the chunk (columns +8..15); byte i of a word is K block i of the stage.
-        const int q = warp - 8;
+        // With two sets of four warps (the down GEMM) they take alternate stages
+        // (set p the stages of parity p, so also the ring slots and buffers of
+        // parity p). Warp 8 + 4p + q writes lane quarter q of a scale-factor
+        // buffer (the MMA reads every quarter):
+        // column j, lane L holds the four block scales of weight row L + 32 j
+        // (columns +0..3) and the scale word of route L + 32 j of the chunk
+        // (columns +8..15); byte i of a word is K block i of the stage.
+        constexpr int kSets = kSfSets<SWIGLU, MX>;
+        const int q = warp & 3, set = (warp - 8) >> 2;
+        static_assert(C::kSfStages % 2 == 0 && C::kSfBufs % 2 == 0, "a set keeps to slots of its parity");
         const uint32_t sf_full0 = ptx::map_to_rank(ptx::smem_u32(&c.sf_full[0]), 0);
         int slot = 0, sfi = 0;
         uint32_t phase = 0;
@@ -617,6 +632,14 @@ __global__ void __launch_bounds__(Cfg<MX>::kThreads, 1)
             for (int mi = 0; ok && mi < n_micro_k; ++mi) {
                 for (int kb = 0; kb < a.k_blocks; ++kb) {
                     const int sfb = sfi % C::kSfBufs;
+                    if (kSets == 2 && (sfi & 1) != set) {  // the other set's stage
+                        ++sfi;
+                        if (++slot == C::kSfStages) {
+                            slot = 0;
+                            phase ^= 1u;
+                        }
+                        continue;
+                    }
                     // the stage's scales into registers (the ring slot is then free),
                     // then wait for the TMEM buffer
                     bool got = ptx::mbar_wait(ptx::smem_u32(&c.sfs_full[slot]), phase, a.limit_ns, &c.abort);
@@ -832,7 +855,7 @@ int max_pairs() {
     if (cached[dev] > 0) return cached[dev];
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(2);
-    cfg.blockDim = dim3(Cfg<MX>::kThreads);
+    cfg.blockDim = dim3(kPairThreads<SWIGLU, MX>);
     cfg.dynamicSmemBytes = smem_bytes<MX>();
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -863,7 +886,7 @@ cudaError_t launch_pair(const PairGemmArgs& a, const CUtensorMap* tmW, const CUt
     ad.dynamic = a.max_tiles >= kDynamicTilesPerPair * pairs ? 1 : 0;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(2 * pairs);
-    cfg.blockDim = dim3(Cfg<MX>::kThreads);
+    cfg.blockDim = dim3(kPairThreads<SWIGLU, MX>);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
