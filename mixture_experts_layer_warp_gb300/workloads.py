@@ -29,6 +29,10 @@ import torch
 # seed 0 (checked by a CPU test on the oracle's routing).
 LOG_ZIPF_S = 1.1
 LOG_ZIPF_ALPHA = 0.365
+# "hot" router bias: +HOT_BIAS on a seeded set of k experts, far above the
+# spread of the logits x.Wr (about N(0, 1)), so every token routes to those k
+# and every other expert's segment is empty (the most skewed load top-k allows)
+HOT_BIAS = 16.0
 
 
 @dataclass(frozen=True)
@@ -43,7 +47,7 @@ class Workload:
     shared_inter: int = 0          # Is of the dense shared expert (0 = none)
     dtype: str = "bf16"            # "bf16" or "f32"
     router_init: str = "normal"    # "normal" N(0,1/H) or "uniform" U(+-1/sqrt(H))
-    router_bias: str | None = None  # None or "log_zipf"
+    router_bias: str | None = None  # None, "log_zipf" or "hot"
     x_parts: int = 1               # x drawn as this many independent halves (CFG)
     note: str = field(default="", compare=False)
 
@@ -120,6 +124,11 @@ def make_inputs(wl: Workload, seed: int = 0, device="cpu", T: int | None = None,
         rank = torch.randperm(E, generator=_gen(base + 11, "cpu")).to(torch.float64) + 1.0
         bias = -LOG_ZIPF_ALPHA * LOG_ZIPF_S * torch.log(rank)
         out["router_bias"] = bias.to(torch.float32).to(device)
+    elif wl.router_bias == "hot":
+        hot = torch.randperm(E, generator=_gen(base + 12, "cpu"))[: wl.k]
+        bias = torch.zeros(E, dtype=torch.float32)
+        bias[hot] = HOT_BIAS
+        out["router_bias"] = bias.to(device)
     else:
         out["router_bias"] = None
 

@@ -57,6 +57,10 @@ SMALL = [
     W.Workload("bf16_shared", 257, 256, 16, 4, 128, 2, shared_inter=256),
     W.Workload("bf16_four_micro", 70, 512, 8, 3, 128, 4),
     W.Workload("bf16_skew_bias", 600, 256, 64, 8, 128, 1, router_bias="log_zipf"),
+    # every token to the same 4 of 16 experts: 12 empty segments, 4 of 700
+    # routes (three chunks each); and the same at a decode-sized batch
+    W.Workload("bf16_hot_experts", 700, 256, 16, 4, 128, 2, shared_inter=128, router_bias="hot"),
+    W.Workload("bf16_hot_experts_small", 12, 512, 16, 4, 128, 2, router_bias="hot"),
     # groups of more than 16 row blocks (about 3000 routes per expert; a 47-block
     # dense shared segment): the large GEMM walks their row blocks in chunks
     W.Workload("bf16_long_groups", 6000, 256, 4, 2, 128, 2, shared_inter=128),

@@ -91,6 +91,8 @@ SMALL = [
     W.Workload("mx_h768_i384", 12, 768, 16, 4, 384, 2),
     # four micros of I = 128: h's scale map four deep, a half stage per micro
     W.Workload("mx_four_micro_small", 5, 256, 8, 2, 128, 4),
+    # every token to the same 4 of 16 experts (12 experts untouched)
+    W.Workload("mx_hot_experts_small", 12, 512, 16, 4, 128, 2, router_bias="hot"),
 ]
 
 
@@ -133,6 +135,9 @@ LARGE = [
     W.Workload("mx_large_four_micro", 64, 512, 16, 4, 128, 4),
     W.Workload("mx_large_e64_k8", 300, 1024, 64, 8, 256, 1),
     W.Workload("mx_large_wide_h", 40, 256, 8, 2, 512, 2),  # n_micro * I = 4 H
+    # every token to the same 4 of 16 experts: 12 empty segments, 4 of 500
+    # routes (three chunks each)
+    W.Workload("mx_large_hot_experts", 500, 256, 16, 4, 128, 2, router_bias="hot"),
 ]
 
 

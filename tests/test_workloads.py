@@ -58,3 +58,18 @@ def test_skewed_load_is_about_ten_to_one():
     ids, _ = oracle.route(lg, wl.k)
     c = np.bincount(ids.ravel(), minlength=wl.E)
     assert 8.0 <= c.max() / c.min() <= 12.0, (c.max(), c.min())
+
+
+def test_hot_bias_routes_every_token_to_the_same_k_experts():
+    """The "hot" bias: every token's top-k is the seeded set of k experts, in
+    some order, and the other experts receive no route (oracle routing)."""
+    wl = W.Workload("hot", 300, 256, 16, 4, 128, 1, router_bias="hot")
+    inp = W.make_inputs(wl, seed=1, experts=False)
+    bias = inp["router_bias"].numpy()
+    hot = np.flatnonzero(bias)
+    assert len(hot) == wl.k and np.all(bias[hot] == W.HOT_BIAS)
+    lg = oracle.logits(W.to_numpy(inp["x"]), W.to_numpy(inp["router_w"]), bias)
+    ids, w = oracle.route(lg, wl.k)
+    assert np.all(np.sort(ids, axis=1) == hot[None, :])
+    assert np.allclose(w.sum(axis=1), 1.0)
+    assert w.min() > 0.0
