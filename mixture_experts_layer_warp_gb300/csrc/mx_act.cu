@@ -30,9 +30,9 @@ constexpr int kThreads = 256;
 // One warp per token: lane l loads elements 8l .. 8l+7 of each 256-element
 // unit (one 16-byte load; a 32-block spans four lanes), sixteen units in
 // flight (a whole 8 KB row of a 4096-wide layer), quantises them and writes
-// the codes to the token's k route rows (8 bytes per lane and route) and each
-// stage's scale word (lanes 0-15 hold the unit's first stage, 16-31 its
-// second). The earlier form (a warp per 8 stages of a token, 8-byte loads
+// the codes to the token's k route rows (8 bytes per lane and route; the rows
+// are taken from the route lanes once per token) and each stage's scale word
+// (lanes 0-15 hold the unit's first stage, 16-31 its second). The earlier form (a warp per 8 stages of a token, 8-byte loads
 // four stages ahead) ran at 0.42 of the HBM bandwidth, bound by the latency of
 // its loads and of the quantisation's dependent shuffles.
 constexpr int kUnits = 16;  // 256-element units in flight per warp
@@ -86,6 +86,9 @@ __global__ void __launch_bounds__(kThreads) gather_mx_kernel(MxActArgs a) {
             if (lane == 0) atomicOr(a.err, kErrCheck);
             continue;
         }
+        int rows[kMaxTopK];  // the token's route rows, in every lane (j >= k: unused)
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j) rows[j] = __shfl_sync(0xffffffffu, mine, j);
         for (int u0 = 0; u0 < units; u0 += kUnits) {
             uint4 raw[kUnits];
 #pragma unroll
@@ -97,10 +100,10 @@ __global__ void __launch_bounds__(kThreads) gather_mx_kernel(MxActArgs a) {
                 uint32_t word;
                 const uint2 c = quantize_unit(raw[u], lane, word);
                 const int s = 2 * (u0 + u) + half;  // this half-warp's stage
-                for (int j = 0; j < a.k; ++j) {
-                    const int64_t row = __shfl_sync(0xffffffffu, mine, j);
-                    *reinterpret_cast<uint2*>(codes + row * a.K + (int64_t)s * 128 + 8 * l16) = c;
-                }
+                const int col = s * 128 + 8 * l16;
+#pragma unroll
+                for (int j = 0; j < kMaxTopK; ++j)
+                    if (j < a.k) *reinterpret_cast<uint2*>(codes + (int64_t)rows[j] * a.K + col) = c;
                 if (l16 < a.k) scales[(int64_t)s * a.rows_pad + mine] = word;
             }
         }
